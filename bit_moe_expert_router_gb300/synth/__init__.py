@@ -1,0 +1,211 @@
+"""Seeded synthetic inputs for the routed-expert W4A8 MoE layer.
+
+The shapes and value distributions are those of the five workloads the layer
+is built and measured on (a tiny parity case, two decode batches, a prefill
+chunk and a larger expert bank).  The expert bank is quantised to signed
+int4 per (row, K-group), packed two codes per byte with the low nibble
+first; activations are bf16-rounded N(0,1) values with a per-token
+symmetric int8 code.  This module holds none of the layer's arithmetic; the
+CPU oracle and the CUDA path both consume its arrays.
+
+The numeric work runs in ``libsynth.so`` (a counter-based SplitMix64 stream
+per tensor, Box-Muller normals), built from ``synth.c`` beside this file.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libsynth.so")
+_lib = None
+
+# Stream numbers of the counter-based generator, one per tensor.
+STREAM_X, STREAM_LOGITS, STREAM_BIAS, STREAM_TWOBIT, STREAM_W13, STREAM_W2 = 1, 2, 3, 4, 5, 6
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: run __graft_entry__.build() first")
+    lib = ctypes.CDLL(_LIB_PATH)
+    u64, i64, p = ctypes.c_uint64, ctypes.c_int64, ctypes.c_void_p
+    lib.synth_normal_f32.argtypes = [u64, u64, u64, i64, ctypes.c_double, p]
+    lib.synth_uniform_f64.argtypes = [u64, u64, i64, p]
+    lib.synth_activations.argtypes = [u64, i64, i64, p, p, p]
+    lib.synth_weight_matrix.argtypes = [u64, u64, i64, i64, i64, i64, ctypes.c_double,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p, p]
+    lib.synth_u64.argtypes = [u64, u64]
+    lib.synth_u64.restype = u64
+    lib.synth_stream_base.argtypes = [u64, u64]
+    lib.synth_stream_base.restype = u64
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One layer shape plus the recipe of its synthetic inputs."""
+    name: str
+    T: int            # tokens in the batch
+    H: int            # hidden size
+    I: int            # expert intermediate size
+    E: int            # routed experts
+    S: int            # always-on shared experts (bank slots E .. E+S-1)
+    top_k: int
+    group: int        # int4 quantisation group along K
+    logit_sigma: float = 1.0
+    bias: str = "none"          # "none" | "zipf" | "request"
+    zipf_s: float = 0.0
+    requests: int = 0           # for bias == "request": tokens are request-major
+    positions: int = 0
+    beta: float = 0.0           # per-request bias strength
+    twobit_frac: float = 0.0    # share of routed experts with 2-bit codes
+    seed: int = 0
+
+    @property
+    def slots(self) -> int:
+        return self.E + self.S
+
+    @property
+    def pairs(self) -> int:
+        return self.T * self.top_k + self.T * self.S
+
+    def with_tokens(self, T: int) -> "Workload":
+        """Same layer and recipe with another batch size (for ragged/edge cases)."""
+        if self.bias == "request":
+            return dataclasses.replace(self, T=T, requests=max(1, -(-T // max(1, self.positions))))
+        return dataclasses.replace(self, T=T)
+
+
+# The per-request bias strength of the draft-verification batch: set by
+# bisection so that the three positions of one request share 60% of their
+# top-10 experts on average (mean pairwise overlap over 4 requests x 3 pairs,
+# averaged over calibration seeds 1..59; seed 0 itself gives 0.65).  The
+# tests check the generator against that target.
+VERIFY_BETA = 3.32
+
+WORKLOADS = {
+    "tiny": Workload("tiny", T=16, H=256, I=128, E=8, S=0, top_k=2, group=64),
+    "decode_t4": Workload("decode_t4", T=4, H=2048, I=512, E=512, S=1, top_k=10, group=128),
+    "decode_verify_t12": Workload("decode_verify_t12", T=12, H=2048, I=512, E=512, S=1, top_k=10, group=128,
+                                  bias="request", requests=4, positions=3, beta=VERIFY_BETA),
+    "prefill_t8192": Workload("prefill_t8192", T=8192, H=2048, I=512, E=512, S=1, top_k=10, group=128,
+                              bias="zipf", zipf_s=1.1),
+    "large_bank_t2048": Workload("large_bank_t2048", T=2048, H=4096, I=1536, E=288, S=1, top_k=8, group=128,
+                                 logit_sigma=1.5, bias="zipf", zipf_s=1.0, twobit_frac=0.25),
+}
+
+
+@dataclasses.dataclass
+class Bank:
+    """Packed int4 expert bank: slots 0..E-1 routed, E..E+S-1 shared."""
+    w13: np.ndarray   # uint8 [slots, 2I, H/2]; rows [0, I) gate, [I, 2I) up
+    s13: np.ndarray   # float32 [slots, 2I, H/g]
+    w2: np.ndarray    # uint8 [slots, H, I/2]
+    s2: np.ndarray    # float32 [slots, H, I/g]
+    twobit: np.ndarray  # bool [slots]: expert quantised to the 2-bit code range
+
+
+@dataclasses.dataclass
+class Tokens:
+    x_q: np.ndarray      # int8 [T, H]
+    x_scale: np.ndarray  # float32 [T]
+    logits: np.ndarray   # float32 [T, E]
+
+
+def normal_f32(seed: int, stream: int, n: int, sigma: float = 1.0, first: int = 0) -> np.ndarray:
+    out = np.empty(n, dtype=np.float32)
+    if n:
+        _load().synth_normal_f32(seed, stream, first, n, sigma, _ptr(out))
+    return out
+
+
+def uniform_f64(seed: int, stream: int, n: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.float64)
+    if n:
+        _load().synth_uniform_f64(seed, stream, n, _ptr(out))
+    return out
+
+
+def twobit_experts(w: Workload) -> np.ndarray:
+    """The seeded choice of routed experts that carry 2-bit codes."""
+    flags = np.zeros(w.slots, dtype=bool)
+    n = int(round(w.twobit_frac * w.E))
+    if n:
+        order = np.argsort(uniform_f64(w.seed, STREAM_TWOBIT, w.E), kind="stable")
+        flags[order[:n]] = True
+    return flags
+
+
+def make_bank(w: Workload, with_codes: bool = False):
+    """The packed bank; with_codes also returns the int8 codes (w13 [slots,2I,H], w2 [slots,H,I])."""
+    lib = _load()
+    H, I, g, slots = w.H, w.I, w.group, w.slots
+    w13 = np.empty((slots, 2 * I, H // 2), dtype=np.uint8)
+    s13 = np.empty((slots, 2 * I, H // g), dtype=np.float32)
+    w2 = np.empty((slots, H, I // 2), dtype=np.uint8)
+    s2 = np.empty((slots, H, I // g), dtype=np.float32)
+    c13 = np.empty((slots, 2 * I, H), dtype=np.int8) if with_codes else None
+    c2 = np.empty((slots, H, I), dtype=np.int8) if with_codes else None
+    twobit = twobit_experts(w)
+    for e in range(slots):
+        qmax, qlo, qhi = (2, -2, 1) if twobit[e] else (7, -8, 7)
+        lib.synth_weight_matrix(w.seed, STREAM_W13, e, 2 * I, H, g, 0.02, qmax, qlo, qhi,
+                                _ptr(w13[e]), _ptr(s13[e]), _ptr(c13[e]) if with_codes else None)
+        lib.synth_weight_matrix(w.seed, STREAM_W2, e, H, I, g, 0.02, qmax, qlo, qhi,
+                                _ptr(w2[e]), _ptr(s2[e]), _ptr(c2[e]) if with_codes else None)
+    bank = Bank(w13, s13, w2, s2, twobit)
+    return (bank, c13, c2) if with_codes else bank
+
+
+def logit_bias(w: Workload) -> np.ndarray:
+    """fp64 [T, E] bias added to the N(0, sigma) router logits."""
+    T, E = w.T, w.E
+    if w.bias == "none":
+        return np.zeros((T, E))
+    if w.bias == "zipf":
+        # Expert popularity ranks r_e = 1..E from a seeded permutation; bias -s * ln(r_e).
+        order = np.argsort(uniform_f64(w.seed, STREAM_BIAS, E), kind="stable")
+        rank = np.empty(E, dtype=np.float64)
+        rank[order] = np.arange(1, E + 1, dtype=np.float64)
+        return np.broadcast_to(-w.zipf_s * np.log(rank), (T, E)).copy()
+    if w.bias == "request":
+        # Tokens are request-major (t = r * positions + p); one N(0,1) vector per request.
+        z = normal_f32(w.seed, STREAM_BIAS, w.requests * E).astype(np.float64).reshape(w.requests, E)
+        req = np.minimum(np.arange(T) // w.positions, w.requests - 1)
+        return w.beta * z[req]
+    raise ValueError(w.bias)
+
+
+def make_tokens(w: Workload, batch: int = 0) -> Tokens:
+    """Activations and router logits of batch `batch` (batch 0 is the workload's own seed)."""
+    lib = _load()
+    seed = w.seed + batch
+    x_q = np.empty((w.T, w.H), dtype=np.int8)
+    x_scale = np.empty(w.T, dtype=np.float32)
+    if w.T:
+        lib.synth_activations(seed, w.T, w.H, _ptr(x_q), _ptr(x_scale), None)
+    noise = normal_f32(seed, STREAM_LOGITS, w.T * w.E, w.logit_sigma).astype(np.float64).reshape(w.T, w.E)
+    logits = (noise + logit_bias(w)).astype(np.float32)
+    return Tokens(x_q, x_scale, logits)
+
+
+def bf16_activations(w: Workload, batch: int = 0) -> np.ndarray:
+    """The bf16-rounded activations (as fp32) that make_tokens quantised."""
+    x_q = np.empty((w.T, w.H), dtype=np.int8)
+    x_scale = np.empty(w.T, dtype=np.float32)
+    xb = np.empty((w.T, w.H), dtype=np.float32)
+    if w.T:
+        _load().synth_activations(w.seed + batch, w.T, w.H, _ptr(x_q), _ptr(x_scale), _ptr(xb))
+    return xb
