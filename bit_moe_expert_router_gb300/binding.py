@@ -1,0 +1,231 @@
+"""ctypes binding of ``libmoe_w4a8.so`` (C ABI in ``include/moe_w4a8.h``).
+
+Argument marshalling only: torch tensors are checked for dtype, shape,
+contiguity and device, and their ``data_ptr()`` is passed with the current
+CUDA stream.  Every step of the layer runs in the library's CUDA kernels;
+there is no CPU fallback -- if the library is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_w4a8.so")
+ABI_VERSION = 1
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed with status {status}: {_load().moe_w4a8_status_string(status).decode()}")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("T", "H", "I", "E", "n_shared", "top_k", "group")]
+
+    def __repr__(self):
+        return "Dims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    p, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    dp = ctypes.POINTER(Dims)
+    lib.moe_w4a8_version.restype = ctypes.c_int
+    lib.moe_w4a8_status_string.argtypes = [ctypes.c_int]
+    lib.moe_w4a8_status_string.restype = ctypes.c_char_p
+    lib.moe_w4a8_workspace_size.argtypes = [dp]
+    lib.moe_w4a8_workspace_size.restype = sz
+    lib.moe_w4a8_forward.argtypes = [p, p, p, p, p, p, p, dp, p, p, sz, p]
+    lib.moe_w4a8_forward_debug.argtypes = [p, p, p, p, p, p, p, dp, p, p, p, p, p, sz, p]
+    lib.moe_w4a8_route.argtypes = [p, dp, p, p, p, p, p, p, p, sz, p]
+    lib.moe_w4a8_gemm1_partials.argtypes = [p, p, dp, p, p, i64, p, p, sz, p]
+    lib.moe_w4a8_gemm2_partials.argtypes = [p, p, dp, p, i64, p, p, sz, p]
+    for name in ("moe_w4a8_forward", "moe_w4a8_forward_debug", "moe_w4a8_route", "moe_w4a8_gemm1_partials",
+                 "moe_w4a8_gemm2_partials"):
+        getattr(lib, name).restype = ctypes.c_int
+    if lib.moe_w4a8_version() != ABI_VERSION:
+        raise RuntimeError(f"{LIB_PATH}: ABI version {lib.moe_w4a8_version()} != {ABI_VERSION}")
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise MoeError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name, dtype, shape=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def dims_of(T, H, I, E, n_shared, top_k, group) -> Dims:
+    return Dims(T, H, I, E, n_shared, top_k, group)
+
+
+def moe_w4a8_version() -> int:
+    return _load().moe_w4a8_version()
+
+
+def moe_w4a8_status_string(status: int) -> str:
+    return _load().moe_w4a8_status_string(status).decode()
+
+
+def moe_w4a8_workspace_size(d: Dims) -> int:
+    n = _load().moe_w4a8_workspace_size(ctypes.byref(d))
+    if n == 0:
+        raise MoeError("moe_w4a8_workspace_size", 1)
+    return n
+
+
+def partials_workspace_size(d: Dims, n_pairs: int) -> int:
+    """Workspace of moe_w4a8_gemm{1,2}_partials for n_pairs pairs."""
+    return moe_w4a8_workspace_size(Dims(max(n_pairs, 1), d.H, d.I, d.E + d.n_shared, 0, 1, d.group))
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+
+
+def _ws_view(ws: torch.Tensor):
+    """(pointer, bytes) of the 256-byte aligned part of a uint8 workspace tensor."""
+    base = ws.data_ptr()
+    aligned = (base + 255) & ~255
+    return ctypes.c_void_p(aligned), ws.numel() - (aligned - base)
+
+
+def _bank_shapes(d: Dims):
+    slots = d.E + d.n_shared
+    return ((slots, 2 * d.I, d.H // 2), (slots, 2 * d.I, d.H // d.group), (slots, d.H, d.I // 2),
+            (slots, d.H, d.I // d.group))
+
+
+def _check_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out):
+    s13, s13s, s2, s2s = _bank_shapes(d)
+    _need(x_q, "x_q", torch.int8, (d.T, d.H))
+    _need(x_scale, "x_scale", torch.float32, (d.T,))
+    _need(router_logits, "router_logits", torch.float32, (d.T, d.E))
+    _need(w13_packed, "w13_packed", torch.uint8, s13)
+    _need(w13_scale, "w13_scale", torch.float32, s13s)
+    _need(w2_packed, "w2_packed", torch.uint8, s2)
+    _need(w2_scale, "w2_scale", torch.float32, s2s)
+    _need(out, "out", torch.float32, (d.T, d.H))
+
+
+def moe_w4a8_forward(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d: Dims, out,
+                     workspace: torch.Tensor):
+    _check_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out)
+    wp, wb = _ws_view(workspace)
+    _check("moe_w4a8_forward", _load().moe_w4a8_forward(
+        _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
+        _ptr(w2_scale), ctypes.byref(d), _ptr(out), wp, wb, _stream(out.device)))
+    return out
+
+
+def moe_w4a8_forward_debug(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d: Dims, out,
+                           workspace, h_q=None, s_h=None, y=None):
+    _check_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out)
+    P = d.T * (d.top_k + d.n_shared)
+    if h_q is not None:
+        _need(h_q, "h_q", torch.int8, (P, d.I))
+    if s_h is not None:
+        _need(s_h, "s_h", torch.float32, (P,))
+    if y is not None:
+        _need(y, "y", torch.float32, (P, d.H))
+    wp, wb = _ws_view(workspace)
+    _check("moe_w4a8_forward_debug", _load().moe_w4a8_forward_debug(
+        _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
+        _ptr(w2_scale), ctypes.byref(d), _ptr(out), _ptr(h_q), _ptr(s_h), _ptr(y), wp, wb, _stream(out.device)))
+    return out
+
+
+def moe_w4a8_route(router_logits, d: Dims, topk_ids, topk_w, counts, offsets, perm, inv, workspace):
+    _need(router_logits, "router_logits", torch.float32, (d.T, d.E))
+    _need(topk_ids, "topk_ids", torch.int32, (d.T, d.top_k))
+    _need(topk_w, "topk_w", torch.float32, (d.T, d.top_k))
+    _need(counts, "counts", torch.int32, (d.E,))
+    _need(offsets, "offsets", torch.int32, (d.E + 1,))
+    _need(perm, "perm", torch.int32, (d.T * d.top_k,))
+    _need(inv, "inv", torch.int32, (d.T * d.top_k,))
+    wp, wb = _ws_view(workspace)
+    _check("moe_w4a8_route", _load().moe_w4a8_route(
+        _ptr(router_logits), ctypes.byref(d), _ptr(topk_ids), _ptr(topk_w), _ptr(counts), _ptr(offsets),
+        _ptr(perm), _ptr(inv), wp, wb, _stream(router_logits.device)))
+
+
+def moe_w4a8_gemm1_partials(x_q, w13_packed, d: Dims, pair_token, pair_slot, p1, workspace):
+    n = pair_slot.shape[0]
+    _need(x_q, "x_q", torch.int8, (d.T, d.H))
+    _need(w13_packed, "w13_packed", torch.uint8, _bank_shapes(d)[0])
+    _need(pair_token, "pair_token", torch.int32, (n,))
+    _need(pair_slot, "pair_slot", torch.int32, (n,))
+    _need(p1, "p1", torch.int32, (n, 2 * d.I, d.H // d.group))
+    wp, wb = _ws_view(workspace)
+    _check("moe_w4a8_gemm1_partials", _load().moe_w4a8_gemm1_partials(
+        _ptr(x_q), _ptr(w13_packed), ctypes.byref(d), _ptr(pair_token), _ptr(pair_slot), n, _ptr(p1), wp, wb,
+        _stream(p1.device)))
+
+
+def moe_w4a8_gemm2_partials(h_q, w2_packed, d: Dims, pair_slot, p2, workspace):
+    n = pair_slot.shape[0]
+    _need(h_q, "h_q", torch.int8, (n, d.I))
+    _need(w2_packed, "w2_packed", torch.uint8, _bank_shapes(d)[2])
+    _need(pair_slot, "pair_slot", torch.int32, (n,))
+    _need(p2, "p2", torch.int32, (n, d.H, d.I // d.group))
+    wp, wb = _ws_view(workspace)
+    _check("moe_w4a8_gemm2_partials", _load().moe_w4a8_gemm2_partials(
+        _ptr(h_q), _ptr(w2_packed), ctypes.byref(d), _ptr(pair_slot), n, _ptr(p2), wp, wb, _stream(p2.device)))
+
+
+class Layer:
+    """A device-resident expert bank with its dims and a workspace; forward() runs the layer."""
+
+    def __init__(self, d: Dims, w13, s13, w2, s2, device):
+        self.d, self.device = d, torch.device(device)
+        self.w13, self.s13, self.w2, self.s2 = w13, s13, w2, s2
+        self.workspace = alloc_workspace(moe_w4a8_workspace_size(d), self.device)
+
+    @classmethod
+    def from_numpy(cls, w, bank, device, T=None):
+        d = Dims(w.T if T is None else T, w.H, w.I, w.E, w.S, w.top_k, w.group)
+        dev = torch.device(device)
+        t = lambda a: torch.from_numpy(a).to(dev)  # noqa: E731
+        return cls(d, t(bank.w13), t(bank.s13), t(bank.w2), t(bank.s2), dev)
+
+    def forward(self, x_q, x_scale, router_logits, out=None):
+        if out is None:
+            out = torch.empty((self.d.T, self.d.H), dtype=torch.float32, device=self.device)
+        return moe_w4a8_forward(x_q, x_scale, router_logits, self.w13, self.s13, self.w2, self.s2, self.d, out,
+                                self.workspace)
+
+    def forward_numpy(self, tokens):
+        t = lambda a: torch.from_numpy(a).to(self.device)  # noqa: E731
+        out = self.forward(t(tokens.x_q), t(tokens.x_scale), t(tokens.logits))
+        torch.cuda.synchronize(self.device)
+        return out

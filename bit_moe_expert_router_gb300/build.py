@@ -80,7 +80,7 @@ def build_cuda(force: bool = False, verbose_ptxas: bool = False) -> str:
         results = list(ex.map(compile_one, srcs))
     objs = [o for o, _ in results]
     if force or not _newer(LIB, objs):
-        _run([nvcc, *ARCH, "-shared", "-o", LIB, *objs, "-lcuda"])
+        _run([nvcc, *ARCH, "-shared", "-o", LIB, *objs])
     if verbose_ptxas:
         return "\n".join(log for _, log in results)
     return LIB

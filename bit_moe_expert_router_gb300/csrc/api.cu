@@ -1,0 +1,308 @@
+// C ABI of the routed-expert W4A8 MoE layer: argument checks, workspace
+// carving and the launch sequence.  Host code only; every step of the layer
+// runs in the kernels of route.cu and gemm_mma.cu.
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "moe_w4a8.h"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using moe::WsLayout;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(const moe_dims_t* d) {
+    if (!d) return MOE_ERR_INVALID_ARG;
+    if (d->T < 0 || d->H < 1 || d->I < 1 || d->E < 1 || d->n_shared < 0 || d->top_k < 1 || d->top_k > d->E ||
+        d->group < 32 || d->group % 32 != 0 || d->H % d->group != 0 || d->I % d->group != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (d->E > moe::kMaxExperts || d->n_shared > moe::kMaxShared || d->top_k > moe::kMaxTopK ||
+        d->group > moe::kMaxGroup || d->I % 64 != 0 || d->H % 128 != 0)
+        return MOE_ERR_UNSUPPORTED;
+    const int64_t P = d->T * (d->top_k + d->n_shared);
+    if (d->T > (int64_t(1) << 24) || P >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> ptrs) {
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+WsLayout layout_of(const moe_dims_t* d) { return moe::ws_layout(d->T, d->H, d->I, d->E, d->n_shared, d->top_k); }
+
+int check_ws(const WsLayout& L, const void* ws, size_t bytes) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    if (bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                          \
+    do {                                       \
+        int _rc = (expr);                      \
+        if (_rc != MOE_OK) return _rc;         \
+    } while (0)
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+struct Views {
+    moe::Header* hdr;
+    int32_t *ids, *seg_cnt, *seg_off, *perm, *inv, *row_token, *chunk_counts, *tile_slot, *tile_row0;
+    float *wts, *h, *y;
+    uint32_t* amax;
+};
+
+Views views(void* ws, const WsLayout& L) {
+    Views v;
+    v.hdr = moe::ws_at<moe::Header>(ws, L.hdr);
+    v.ids = moe::ws_at<int32_t>(ws, L.ids);
+    v.wts = moe::ws_at<float>(ws, L.wts);
+    v.seg_cnt = moe::ws_at<int32_t>(ws, L.seg_cnt);
+    v.seg_off = moe::ws_at<int32_t>(ws, L.seg_off);
+    v.perm = moe::ws_at<int32_t>(ws, L.perm);
+    v.inv = moe::ws_at<int32_t>(ws, L.inv);
+    v.row_token = moe::ws_at<int32_t>(ws, L.row_token);
+    v.chunk_counts = moe::ws_at<int32_t>(ws, L.chunk_counts);
+    v.tile_slot = moe::ws_at<int32_t>(ws, L.tile_slot);
+    v.tile_row0 = moe::ws_at<int32_t>(ws, L.tile_row0);
+    v.amax = moe::ws_at<uint32_t>(ws, L.amax);
+    v.h = moe::ws_at<float>(ws, L.h);
+    v.y = moe::ws_at<float>(ws, L.y);
+    return v;
+}
+
+moe::SortArgs sort_args(const Views& v, const int32_t* ids, int64_t T, int64_t k, int64_t E, int64_t S, int64_t P) {
+    moe::SortArgs a{};
+    a.ids = ids;
+    a.T = T;
+    a.k = k;
+    a.E = E;
+    a.S = S;
+    a.tok_map = nullptr;
+    a.chunk_counts = v.chunk_counts;
+    a.seg_cnt = v.seg_cnt;
+    a.seg_off = v.seg_off;
+    a.perm = v.perm;
+    a.inv = v.inv;
+    a.row_token = v.row_token;
+    a.tile_slot = v.tile_slot;
+    a.tile_row0 = v.tile_row0;
+    a.hdr = v.hdr;
+    a.amax = v.amax;
+    a.P = P;
+    a.counts_out = nullptr;
+    a.offsets_out = nullptr;
+    return a;
+}
+
+// route + permute + gemm1 + gemm2 + combine on the workspace views.
+int run_layer(const int8_t* x_q, const float* x_scale, const float* logits, const uint8_t* w13, const float* s13,
+              const uint8_t* w2, const float* s2, const moe_dims_t* d, float* out, const WsLayout& L, const Views& v,
+              cudaStream_t st) {
+    MOE_CUDA(moe::launch_route_topk(logits, d->T, d->E, d->top_k, v.ids, v.wts, st));
+    MOE_CUDA(moe::launch_sort(sort_args(v, v.ids, d->T, d->top_k, d->E, d->n_shared, L.P), st));
+
+    moe::Gemm1Args g1{};
+    g1.x_q = x_q;
+    g1.x_scale = x_scale;
+    g1.w13 = w13;
+    g1.s13 = s13;
+    g1.T = d->T;
+    g1.H = d->H;
+    g1.I = d->I;
+    g1.g = d->group;
+    g1.seg_off = v.seg_off;
+    g1.seg_cnt = v.seg_cnt;
+    g1.row_token = v.row_token;
+    g1.tile_slot = v.tile_slot;
+    g1.tile_row0 = v.tile_row0;
+    g1.hdr = v.hdr;
+    g1.h = v.h;
+    g1.amax = v.amax;
+    MOE_CUDA(moe::launch_gemm1(moe::Gemm1Mode::kHidden, g1, static_cast<int>(L.max_tiles), st));
+
+    moe::Gemm2Args g2{};
+    g2.h = v.h;
+    g2.amax = v.amax;
+    g2.w2 = w2;
+    g2.s2 = s2;
+    g2.H = d->H;
+    g2.I = d->I;
+    g2.g = d->group;
+    g2.seg_off = v.seg_off;
+    g2.seg_cnt = v.seg_cnt;
+    g2.tile_slot = v.tile_slot;
+    g2.tile_row0 = v.tile_row0;
+    g2.hdr = v.hdr;
+    g2.y = v.y;
+    MOE_CUDA(moe::launch_gemm2(moe::Gemm2Mode::kOutput, g2, static_cast<int>(L.max_tiles), st));
+
+    moe::CombineArgs c{};
+    c.y = v.y;
+    c.wts = v.wts;
+    c.inv = v.inv;
+    c.T = d->T;
+    c.H = d->H;
+    c.k = d->top_k;
+    c.S = d->n_shared;
+    c.out = out;
+    MOE_CUDA(moe::launch_combine(c, st));
+    return MOE_OK;
+}
+
+}  // namespace
+
+MOE_API int moe_w4a8_version(void) { return MOE_W4A8_ABI_VERSION; }
+
+MOE_API const char* moe_w4a8_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, or inconsistent sizes)";
+        case MOE_ERR_UNSUPPORTED: return "sizes beyond the kernels' limits";
+        case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA launch error";
+        case MOE_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+        default: return "unknown status";
+    }
+}
+
+MOE_API size_t moe_w4a8_workspace_size(const moe_dims_t* d) {
+    if (check_dims(d) != MOE_OK) return 0;
+    return layout_of(d).total;
+}
+
+MOE_API int moe_w4a8_forward(const int8_t* x_q, const float* x_scale, const float* router_logits,
+                             const uint8_t* w13_packed, const float* w13_scale, const uint8_t* w2_packed,
+                             const float* w2_scale, const moe_dims_t* d, float* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    MOE_TRY(check_dims(d));
+    MOE_TRY(check_ptrs({w13_packed, w13_scale, w2_packed, w2_scale}));
+    if (d->T == 0) return MOE_OK;
+    MOE_TRY(check_ptrs({x_q, x_scale, router_logits, out}));
+    const WsLayout L = layout_of(d);
+    MOE_TRY(check_ws(L, workspace, workspace_bytes));
+    return run_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out, L,
+                     views(workspace, L), static_cast<cudaStream_t>(stream));
+}
+
+MOE_API int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, const float* router_logits,
+                                   const uint8_t* w13_packed, const float* w13_scale, const uint8_t* w2_packed,
+                                   const float* w2_scale, const moe_dims_t* d, float* out, int8_t* h_q, float* s_h,
+                                   float* y, void* workspace, size_t workspace_bytes, void* stream) {
+    MOE_TRY(check_dims(d));
+    MOE_TRY(check_ptrs({w13_packed, w13_scale, w2_packed, w2_scale}));
+    if (d->T == 0) return MOE_OK;
+    MOE_TRY(check_ptrs({x_q, x_scale, router_logits, out}));
+    for (const void* p : {static_cast<const void*>(h_q), static_cast<const void*>(s_h), static_cast<const void*>(y)})
+        if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = layout_of(d);
+    MOE_TRY(check_ws(L, workspace, workspace_bytes));
+    const Views v = views(workspace, L);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    MOE_TRY(run_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out, L, v, st));
+    if (h_q || s_h) MOE_CUDA(moe::launch_requant_copy(v.h, v.amax, L.P, d->I, h_q, s_h, st));
+    if (y) MOE_CUDA(cudaMemcpyAsync(y, v.y, sizeof(float) * L.P * d->H, cudaMemcpyDeviceToDevice, st));
+    return MOE_OK;
+}
+
+MOE_API int moe_w4a8_route(const float* router_logits, const moe_dims_t* d, int32_t* topk_ids, float* topk_w,
+                           int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    MOE_TRY(check_dims(d));
+    if (d->T == 0) return MOE_OK;
+    MOE_TRY(check_ptrs({router_logits, topk_ids, topk_w, counts, offsets, perm, inv}));
+    const WsLayout L = layout_of(d);
+    MOE_TRY(check_ws(L, workspace, workspace_bytes));
+    Views v = views(workspace, L);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    MOE_CUDA(moe::launch_route_topk(router_logits, d->T, d->E, d->top_k, topk_ids, topk_w, st));
+    moe::SortArgs a = sort_args(v, topk_ids, d->T, d->top_k, d->E, d->n_shared, L.P);
+    a.perm = perm;
+    a.inv = inv;
+    a.counts_out = counts;
+    a.offsets_out = offsets;
+    MOE_CUDA(moe::launch_sort(a, st));
+    return MOE_OK;
+}
+
+namespace {
+// Grouping of an explicit pair list by bank slot (sorted ascending): the
+// counting sort over E + S slots with one "expert" per pair.
+int group_pairs(const moe_dims_t* d, const int32_t* pair_token, const int32_t* pair_slot, int64_t n_pairs,
+                void* workspace, size_t workspace_bytes, cudaStream_t st, WsLayout* L_out, Views* v_out) {
+    const int64_t slots = d->E + d->n_shared;
+    const WsLayout L = moe::ws_layout(n_pairs, d->H, d->I, slots, 0, 1);
+    MOE_TRY(check_ws(L, workspace, workspace_bytes));
+    Views v = views(workspace, L);
+    moe::SortArgs a = sort_args(v, pair_slot, n_pairs, 1, slots, 0, L.P);
+    a.tok_map = pair_token;
+    a.amax = nullptr;
+    MOE_CUDA(moe::launch_sort(a, st));
+    *L_out = L;
+    *v_out = v;
+    return MOE_OK;
+}
+}  // namespace
+
+MOE_API int moe_w4a8_gemm1_partials(const int8_t* x_q, const uint8_t* w13_packed, const moe_dims_t* d,
+                                    const int32_t* pair_token, const int32_t* pair_slot, int64_t n_pairs, int32_t* p1,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+    MOE_TRY(check_dims(d));
+    if (n_pairs < 0 || n_pairs >= (int64_t(1) << 24)) return MOE_ERR_INVALID_ARG;
+    if (n_pairs == 0) return MOE_OK;
+    if (d->E + d->n_shared > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED;
+    MOE_TRY(check_ptrs({x_q, w13_packed, pair_token, pair_slot, p1}));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    WsLayout L;
+    Views v;
+    MOE_TRY(group_pairs(d, pair_token, pair_slot, n_pairs, workspace, workspace_bytes, st, &L, &v));
+    moe::Gemm1Args g1{};
+    g1.x_q = x_q;
+    g1.w13 = w13_packed;
+    g1.T = d->T;
+    g1.H = d->H;
+    g1.I = d->I;
+    g1.g = d->group;
+    g1.seg_off = v.seg_off;
+    g1.seg_cnt = v.seg_cnt;
+    g1.row_token = v.row_token;
+    g1.tile_slot = v.tile_slot;
+    g1.tile_row0 = v.tile_row0;
+    g1.hdr = v.hdr;
+    g1.p1 = p1;
+    MOE_CUDA(moe::launch_gemm1(moe::Gemm1Mode::kPartials, g1, static_cast<int>(L.max_tiles), st));
+    return MOE_OK;
+}
+
+MOE_API int moe_w4a8_gemm2_partials(const int8_t* h_q, const uint8_t* w2_packed, const moe_dims_t* d,
+                                    const int32_t* pair_slot, int64_t n_pairs, int32_t* p2, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    MOE_TRY(check_dims(d));
+    if (n_pairs < 0 || n_pairs >= (int64_t(1) << 24)) return MOE_ERR_INVALID_ARG;
+    if (n_pairs == 0) return MOE_OK;
+    if (d->E + d->n_shared > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED;
+    MOE_TRY(check_ptrs({h_q, w2_packed, pair_slot, p2}));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    WsLayout L;
+    Views v;
+    MOE_TRY(group_pairs(d, pair_slot, pair_slot, n_pairs, workspace, workspace_bytes, st, &L, &v));
+    moe::Gemm2Args g2{};
+    g2.h_q = h_q;
+    g2.w2 = w2_packed;
+    g2.H = d->H;
+    g2.I = d->I;
+    g2.g = d->group;
+    g2.seg_off = v.seg_off;
+    g2.seg_cnt = v.seg_cnt;
+    g2.tile_slot = v.tile_slot;
+    g2.tile_row0 = v.tile_row0;
+    g2.hdr = v.hdr;
+    g2.p2 = p2;
+    MOE_CUDA(moe::launch_gemm2(moe::Gemm2Mode::kPartials, g2, static_cast<int>(L.max_tiles), st));
+    return MOE_OK;
+}

@@ -1,0 +1,249 @@
+// Routing and grouping of the W4A8 MoE layer.
+//
+// Tokens are routed to experts on the device, and the (token, expert) pairs
+// are grouped per expert so the projections can run as grouped GEMMs
+// ("Two 96 GB Ascend cards run Qwen3.8 Flash-Next", section 3: route tokens
+// to experts on the device; routing and tile reuse).
+//
+//   route_topk_kernel  one warp per token: the k largest logits (ties to
+//                      the lower index), softmax over the selected k.
+//   count_kernel       per-chunk expert histogram (chunks of kChunk pairs).
+//   scan_kernel        one block: expert offsets, per-chunk bases, segment
+//                      table of all E + S bank slots and the m-tile schedule.
+//   scatter_kernel     one warp per chunk: stable placement of each pair at
+//                      base + its rank among equal ids (warp match + popc).
+#include <float.h>
+#include <math.h>
+
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+// (v, e) beats (bv, be): larger value, or equal value and lower index.
+__device__ __forceinline__ bool beats(float v, int e, float bv, int be) {
+    return v > bv || (v == bv && e < be);
+}
+
+template <int MAXJ>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                         int32_t* __restrict__ ids, float* __restrict__ wts) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const float* l = logits + static_cast<int64_t>(t) * E;
+    float v[MAXJ];
+#pragma unroll
+    for (int j = 0; j < MAXJ; ++j) {
+        int e = lane + 32 * j;
+        v[j] = e < E ? __ldg(l + e) : -FLT_MAX;
+    }
+    uint32_t taken = 0;  // bit j: element lane + 32 j already selected (or absent)
+#pragma unroll
+    for (int j = 0; j < MAXJ; ++j)
+        if (lane + 32 * j >= E) taken |= 1u << j;
+    float my_v = 0.0f;
+    int my_e = 0;
+    for (int s = 0; s < k; ++s) {
+        float bv = -INFINITY;
+        int be = INT32_MAX;
+#pragma unroll
+        for (int j = 0; j < MAXJ; ++j) {
+            int e = lane + 32 * j;
+            if (!(taken >> j & 1u) && beats(v[j], e, bv, be)) {
+                bv = v[j];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            if (beats(ov, oe, bv, be)) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == s) {
+            my_v = bv;
+            my_e = be;
+        }
+    }
+    // softmax over the selected logits, relative to the largest (selected first)
+    const float m = __shfl_sync(0xffffffffu, my_v, 0);
+    float ex = lane < k ? expf(my_v - m) : 0.0f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane < k) {
+        ids[static_cast<int64_t>(t) * k + lane] = my_e;
+        wts[static_cast<int64_t>(t) * k + lane] = ex / sum;
+    }
+}
+
+__global__ void __launch_bounds__(256) count_kernel(SortArgs a, int64_t n) {
+    extern __shared__ int hist[];
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int64_t c = blockIdx.x;
+    const int64_t i_end = min(n, (c + 1) * kChunk);
+    for (int64_t i = c * kChunk + threadIdx.x; i < i_end; i += blockDim.x) {
+        const int e = a.ids[i];
+        if (static_cast<unsigned>(e) < static_cast<unsigned>(a.E)) atomicAdd(&hist[e], 1);  // out-of-range ids are dropped
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) a.chunk_counts[c * a.E + e] = hist[e];
+    // side jobs spread over the grid: clear the row maxima, name the shared rows' tokens
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (a.amax)
+        for (int64_t r = gid; r < a.P; r += stride) a.amax[r] = 0u;
+    for (int64_t r = gid; r < a.T * a.S; r += stride) a.row_token[n + r] = static_cast<int32_t>(r % a.T);
+}
+
+// In-place exclusive scan of data[0..n) (n <= 4 * blockDim.x); returns the total.
+__device__ int block_exclusive_scan(int* data, int n, int* warp_sums) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+    int loc[4];
+    int s = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        int idx = tid * 4 + j;
+        loc[j] = idx < n ? data[idx] : 0;
+        s += loc[j];
+    }
+    int incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int ws = lane < nw ? warp_sums[lane] : 0;
+        int wi = ws;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int o = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off) wi += o;
+        }
+        if (lane < nw) warp_sums[lane] = wi - ws;  // exclusive
+        if (lane == 31) warp_sums[32] = wi;        // total
+    }
+    __syncthreads();
+    int run = warp_sums[wid] + incl - s;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        int idx = tid * 4 + j;
+        if (idx < n) data[idx] = run;
+        run += loc[j];
+    }
+    int total = warp_sums[32];
+    __syncthreads();
+    return total;
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(SortArgs a, int64_t n_chunks) {
+    __shared__ int tot[kMaxExperts + kMaxShared + 1];
+    __shared__ int tiles[kMaxExperts + kMaxShared + 1];
+    __shared__ int warp_sums[33];
+    const int E = static_cast<int>(a.E), slots = static_cast<int>(a.E + a.S);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int64_t c = 0; c < n_chunks; ++c) {
+            int v = a.chunk_counts[c * E + e];
+            a.chunk_counts[c * E + e] = run;
+            run += v;
+        }
+        tot[e] = run;
+    }
+    for (int s = threadIdx.x; s < a.S; s += blockDim.x) tot[E + s] = static_cast<int>(a.T);
+    __syncthreads();
+    for (int s = threadIdx.x; s < slots; s += blockDim.x) {
+        a.seg_cnt[s] = tot[s];
+        if (a.counts_out && s < E) a.counts_out[s] = tot[s];
+        tiles[s] = (tot[s] + kTileM - 1) / kTileM;
+    }
+    __syncthreads();
+    int total_rows = block_exclusive_scan(tot, slots, warp_sums);  // tot -> segment offsets
+    int n_tiles = block_exclusive_scan(tiles, slots, warp_sums);   // tiles -> tile offsets
+    for (int s = threadIdx.x; s <= slots; s += blockDim.x) {
+        int off = s < slots ? tot[s] : total_rows;
+        a.seg_off[s] = off;
+        if (a.offsets_out && s <= E) a.offsets_out[s] = off;
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        for (int64_t c = 0; c < n_chunks; ++c) a.chunk_counts[c * E + e] += tot[e];
+    for (int s = threadIdx.x; s < slots; s += blockDim.x) {
+        int cnt = a.seg_cnt[s];
+        int nt = (cnt + kTileM - 1) / kTileM;
+        for (int j = 0; j < nt; ++j) {
+            a.tile_slot[tiles[s] + j] = s;
+            a.tile_row0[tiles[s] + j] = tot[s] + j * kTileM;
+        }
+    }
+    if (threadIdx.x == 0) {
+        a.hdr->n_tiles = static_cast<uint32_t>(n_tiles);
+        a.hdr->status = kDevOk;
+    }
+}
+
+__global__ void __launch_bounds__(32) scatter_kernel(SortArgs a, int64_t n) {
+    extern __shared__ int cursor[];
+    const int lane = threadIdx.x;
+    const int64_t c = blockIdx.x;
+    for (int e = lane; e < a.E; e += 32) cursor[e] = a.chunk_counts[c * a.E + e];
+    __syncwarp();
+    const int64_t i0 = c * kChunk, i_end = min(n, i0 + kChunk);
+    for (int64_t base = i0; base < i_end; base += 32) {
+        const int64_t i = base + lane;
+        const int id = i < i_end ? a.ids[i] : -1;
+        const bool valid = static_cast<unsigned>(id) < static_cast<unsigned>(a.E);
+        const int e = valid ? id : -1 - lane;  // absent or out-of-range lanes match nobody
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(same & ((1u << lane) - 1u));
+        if (valid) {
+            const int pos = cursor[e] + rank;
+            a.perm[pos] = static_cast<int32_t>(i);
+            a.inv[i] = pos;
+            a.row_token[pos] = a.tok_map ? a.tok_map[i] : static_cast<int32_t>(i / a.k);
+        }
+        __syncwarp();
+        if (valid && rank == 0) cursor[e] += __popc(same);
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_route_topk(const float* logits, int64_t T, int64_t E, int64_t k, int32_t* ids, float* wts,
+                              cudaStream_t st) {
+    const int warps = 8;
+    dim3 grid(static_cast<unsigned>((T + warps - 1) / warps)), block(32 * warps);
+    const int Ti = static_cast<int>(T), Ei = static_cast<int>(E), ki = static_cast<int>(k);
+    if (E <= 32) route_topk_kernel<1><<<grid, block, 0, st>>>(logits, Ti, Ei, ki, ids, wts);
+    else if (E <= 64) route_topk_kernel<2><<<grid, block, 0, st>>>(logits, Ti, Ei, ki, ids, wts);
+    else if (E <= 128) route_topk_kernel<4><<<grid, block, 0, st>>>(logits, Ti, Ei, ki, ids, wts);
+    else if (E <= 256) route_topk_kernel<8><<<grid, block, 0, st>>>(logits, Ti, Ei, ki, ids, wts);
+    else if (E <= 512) route_topk_kernel<16><<<grid, block, 0, st>>>(logits, Ti, Ei, ki, ids, wts);
+    else route_topk_kernel<32><<<grid, block, 0, st>>>(logits, Ti, Ei, ki, ids, wts);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sort(const SortArgs& a, cudaStream_t st) {
+    const int64_t n = a.T * a.k;
+    const int64_t n_chunks = (n + kChunk - 1) / kChunk;
+    const size_t hist_bytes = sizeof(int) * a.E;
+    if (n_chunks > 0) {
+        count_kernel<<<static_cast<unsigned>(n_chunks), 256, hist_bytes, st>>>(a, n);
+    } else if (a.amax) {
+        cudaMemsetAsync(a.amax, 0, sizeof(uint32_t) * a.P, st);
+    }
+    scan_kernel<<<1, 1024, 0, st>>>(a, n_chunks);
+    if (n_chunks > 0) scatter_kernel<<<static_cast<unsigned>(n_chunks), 32, hist_bytes, st>>>(a, n);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,165 @@
+/*
+ * moe_w4a8.h -- C ABI of the routed-expert W4A8 MoE layer (CUDA, sm_103a).
+ *
+ * What it computes.  Source: "Two 96 GB Ascend cards run Qwen3.8 Flash-Next:
+ * hardware notes, vLLM work, benchmarks and next steps" (ai-pulse-lab.com,
+ * 2026-10-03), section 3, "Keep low-bit weights packed and do the work on
+ * the NPU": tokens are routed to experts on the device and the grouped
+ * expert projections run directly on the packed W4 bank -- fused gate/up,
+ * blocked (per-group) reduction, W4A8 execution -- instead of expanding the
+ * bank into a larger temporary; the same section's eager reference
+ * dequantises the packed weights and calls a plain matmul (same result,
+ * slower, far more memory).  The page prints no formulas; the numeric
+ * recipe below is the layer's stated W4A8 format.
+ *
+ * Notation: T tokens, H hidden, I expert intermediate, E routed experts,
+ * S shared experts, k = top_k, g = int4 quantisation group along K.
+ *
+ *   route    per token: the k largest logits (descending; equal logits go
+ *            to the lower expert index), weights w[t][j] = softmax over the
+ *            selected k logits (= softmax, top-k, renormalise).
+ *   permute  stable counting sort of the flattened pairs i = t*k + j by
+ *            expert: counts[E], offsets[E+1] (exclusive), perm[pos] = i,
+ *            inv[i] = pos.
+ *   gemm1    per pair p = (t, e), row n < 2I, group q:
+ *            P1[p][n][q] = sum_{kk in q} x_q[t][kk] * W13[e][n][kk]  (int32)
+ *            G[p][n] = x_scale[t] * sum_q s13[e][n][q] * P1[p][n][q]
+ *   act      h[p][i] = SiLU(G[p][i]) * G[p][I + i],  SiLU(z) = z/(1+e^-z)
+ *   requant  s_h[p] = max_i |h[p][i]| / 127 (fp32),
+ *            h_q[p][i] = clamp(RNE(h[p][i] / s_h[p]), -127, 127); s_h = 0
+ *            gives h_q = 0
+ *   gemm2    P2[p][n][q] = sum_{kk in q} h_q[p][kk] * W2[e][n][kk]  (int32)
+ *            Y[p][n] = s_h[p] * sum_q s2[e][n][q] * P2[p][n][q]
+ *   combine  out[t][n] = sum_j w[t][j] * Y[(t, ids[t][j])][n]
+ *                        + sum_s Y[(t, E + s)][n]   (fixed order; overwrite)
+ *
+ * Data layout (all row-major, contiguous, no padding):
+ *   x_q      int8    [T][H]        per-token symmetric int8 activations
+ *   x_scale  float   [T]           their scales
+ *   logits   float   [T][E]        router logits
+ *   w13      uint8   [E+S][2I][H/2] packed int4: element 2j in the low
+ *                                   nibble of byte j, 2j+1 in the high
+ *                                   nibble, two's complement; rows [0, I)
+ *                                   are the gate projection, [I, 2I) up
+ *   s13      float   [E+S][2I][H/g]
+ *   w2       uint8   [E+S][H][I/2] same packing
+ *   s2       float   [E+S][H][I/g]
+ *   out      float   [T][H]        fully overwritten
+ * Bank slots E .. E+S-1 are the always-on shared experts (weight 1).
+ * "Pair rows" are ordered by sorted position: routed pair i sits at row
+ * inv[i] (0 .. T*k-1), the shared pair (t, E+s) at row T*k + s*T + t.
+ *
+ * Ownership and streams.  Every pointer is a device pointer owned by the
+ * caller, except where an argument says host.  The library allocates
+ * nothing, keeps no state between calls and never synchronises: each call
+ * only enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).  The workspace carries all intermediates; calls that may run at
+ * the same time need distinct workspaces.
+ *
+ * Errors.  Host-detected errors are returned before anything is enqueued:
+ * MOE_ERR_INVALID_ARG for a null or misaligned pointer (16-byte alignment
+ * is required for every array), non-positive sizes, top_k outside [1, E],
+ * g not a multiple of 32, or H or I not a multiple of g;
+ * MOE_ERR_UNSUPPORTED for sizes beyond the kernels' limits (E + S > 4096,
+ * top_k > 32, g > 256); MOE_ERR_WORKSPACE_TOO_SMALL; MOE_ERR_CUDA if a
+ * launch is rejected.  Errors that occur while the kernels run surface at
+ * the caller's next synchronisation, as for any CUDA work.  T = 0 is valid
+ * and enqueues nothing.
+ */
+#ifndef MOE_W4A8_H
+#define MOE_W4A8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_W4A8_ABI_VERSION 1
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,
+    MOE_ERR_UNSUPPORTED = 2,
+    MOE_ERR_WORKSPACE_TOO_SMALL = 3,
+    MOE_ERR_CUDA = 4,
+    MOE_ERR_DEVICE_TIMEOUT = 5
+} moe_status_t;
+
+/* Layer sizes.  n_shared = S; group = g. */
+typedef struct {
+    int64_t T, H, I, E, n_shared, top_k, group;
+} moe_dims_t;
+
+/* ABI version of the loaded library (MOE_W4A8_ABI_VERSION of its build).
+ * The Python binding refuses a library whose version differs. */
+int moe_w4a8_version(void);
+
+/* Static text for a status code (never NULL). */
+const char* moe_w4a8_status_string(int status);
+
+/* Bytes of workspace moe_w4a8_forward and moe_w4a8_route need for `d`
+ * (0 if `d` is invalid).  Host call, no device work. */
+size_t moe_w4a8_workspace_size(const moe_dims_t* d);
+
+/*
+ * The whole layer: route, permute, gemm1 + act + requant, gemm2, combine.
+ * out [T][H] is overwritten.  workspace: device memory of at least
+ * moe_w4a8_workspace_size(d) bytes, 256-byte aligned, contents arbitrary
+ * on entry (the call initialises what it uses).
+ */
+int moe_w4a8_forward(const int8_t* x_q, const float* x_scale, const float* router_logits,
+                     const uint8_t* w13_packed, const float* w13_scale,
+                     const uint8_t* w2_packed, const float* w2_scale,
+                     const moe_dims_t* d, float* out,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Routing and grouping alone (the first two steps of moe_w4a8_forward, same
+ * kernels): topk_ids int32 [T][k], topk_w float [T][k], counts int32 [E],
+ * offsets int32 [E+1], perm int32 [T*k], inv int32 [T*k].
+ */
+int moe_w4a8_route(const float* router_logits, const moe_dims_t* d,
+                   int32_t* topk_ids, float* topk_w, int32_t* counts, int32_t* offsets,
+                   int32_t* perm, int32_t* inv,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The layer with its intermediates exposed, for checking: runs exactly the
+ * kernels of moe_w4a8_forward and additionally copies out h_q int8
+ * [P][I] and s_h float [P] (P = T*k + T*S pair rows, in pair-row order), and
+ * Y float [P][H] (the per-pair down-projection outputs).  Any of the three
+ * may be NULL.
+ */
+int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, const float* router_logits,
+                           const uint8_t* w13_packed, const float* w13_scale,
+                           const uint8_t* w2_packed, const float* w2_scale,
+                           const moe_dims_t* d, float* out, int8_t* h_q, float* s_h, float* y,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Int32 partial sums of the gate/up projection for an explicit list of
+ * pairs, through the same grouped-GEMM main loop as moe_w4a8_forward:
+ * for pair r (token pair_token[r], bank slot pair_slot[r], both int32
+ * device arrays of n_pairs entries), p1[r][n][q] = P1 for n < 2I, q < H/g.
+ * The pairs are grouped by slot internally; pair_slot must be sorted
+ * ascending.  workspace as for moe_w4a8_forward.
+ */
+int moe_w4a8_gemm1_partials(const int8_t* x_q, const uint8_t* w13_packed, const moe_dims_t* d,
+                            const int32_t* pair_token, const int32_t* pair_slot, int64_t n_pairs,
+                            int32_t* p1, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Int32 partial sums of the down projection for given int8 rows: for pair
+ * r with activation row h_q[r][:] (int8 [n_pairs][I]) and bank slot
+ * pair_slot[r] (sorted ascending), p2[r][n][q] = P2 for n < H, q < I/g.
+ */
+int moe_w4a8_gemm2_partials(const int8_t* h_q, const uint8_t* w2_packed, const moe_dims_t* d,
+                            const int32_t* pair_slot, int64_t n_pairs,
+                            int32_t* p2, void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_W4A8_H */

@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI: the library loads, exports what the header
+declares, and rejects bad arguments before touching the device (no GPU
+needed: every call here returns before any CUDA work)."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+REPO = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(REPO, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"\b(moe_w4a8_\w+)\s*\(", src))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib(cuda_lib):
+    from bit_moe_expert_router_gb300 import binding
+    return binding._load()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_symbols()
+    assert {"moe_w4a8_forward", "moe_w4a8_route", "moe_w4a8_workspace_size", "moe_w4a8_version",
+            "moe_w4a8_status_string", "moe_w4a8_gemm1_partials", "moe_w4a8_gemm2_partials",
+            "moe_w4a8_forward_debug"} <= names
+
+
+def test_library_exports_every_declared_symbol(cuda_lib, lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", cuda_lib], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (moe_w4a8_\w+)", out))
+    missing = _declared_symbols() - exported
+    assert not missing, missing
+    for name in _declared_symbols():
+        assert getattr(lib, name) is not None
+    # nothing but the C ABI is exported
+    assert all(s.startswith("moe_w4a8_") for s in re.findall(r"\bT (\w+)", out))
+
+
+def test_version_and_status_strings(lib):
+    from bit_moe_expert_router_gb300 import binding
+    assert lib.moe_w4a8_version() == binding.ABI_VERSION == 1
+    for s in range(6):
+        assert binding.moe_w4a8_status_string(s)
+    assert binding.moe_w4a8_status_string(99) == "unknown status"
+
+
+def test_workspace_size_grows_with_tokens(lib):
+    from bit_moe_expert_router_gb300 import binding
+    from bit_moe_expert_router_gb300.synth import WORKLOADS
+    w = WORKLOADS["decode_t4"]
+    sizes = [binding.moe_w4a8_workspace_size(binding.dims_of(T, w.H, w.I, w.E, w.S, w.top_k, w.group))
+             for T in (1, 4, 64, 8192)]
+    assert all(s % 256 == 0 for s in sizes)
+    assert sizes == sorted(sizes) and sizes[0] < sizes[-1]
+    # the per-pair intermediates dominate: h (I floats) and Y (H floats) per pair row
+    P = 8192 * (w.top_k + w.S)
+    assert sizes[-1] >= P * (w.I + w.H) * 4
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("E", 0, 1), ("top_k", 0, 1), ("top_k", 9, 1), ("group", 48, 1), ("group", 0, 1), ("H", 200, 1),
+    ("I", 96, 1), ("T", -1, 1), ("n_shared", -1, 1),
+    ("E", 2048, 2), ("group", 512, 1), ("n_shared", 9, 2), ("H", 320, 2),
+])
+def test_bad_dims_are_rejected(lib, field, value, status):
+    from bit_moe_expert_router_gb300 import binding
+    d = binding.dims_of(16, 256, 128, 8, 0, 2, 64)
+    setattr(d, field, value)
+    assert lib.moe_w4a8_workspace_size(ctypes.byref(d)) == 0
+    rc = lib.moe_w4a8_forward(None, None, None, None, None, None, None, ctypes.byref(d), None, None, 0, None)
+    assert rc == status
+
+
+def test_group_beyond_limit_is_unsupported(lib):
+    from bit_moe_expert_router_gb300 import binding
+    d = binding.dims_of(16, 1024, 512, 8, 0, 2, 512)
+    assert lib.moe_w4a8_forward(None, None, None, None, None, None, None, ctypes.byref(d), None, None, 0, None) == 2
+
+
+def test_null_and_misaligned_pointers_are_rejected(lib):
+    from bit_moe_expert_router_gb300 import binding
+    d = binding.dims_of(16, 256, 128, 8, 0, 2, 64)
+    fake = ctypes.c_void_p(0x100000)       # never dereferenced: the checks fail first
+    odd = ctypes.c_void_p(0x100008)
+    args = [fake] * 7
+    assert lib.moe_w4a8_forward(*args[:3], None, *args[4:7], ctypes.byref(d), fake, fake, 1 << 30, None) == 1
+    assert lib.moe_w4a8_forward(*args[:3], odd, *args[4:7], ctypes.byref(d), fake, fake, 1 << 30, None) == 1
+    # workspace: misaligned, then too small
+    ws_unaligned = ctypes.c_void_p(0x100010)
+    assert lib.moe_w4a8_forward(*args, ctypes.byref(d), fake, ws_unaligned, 1 << 30, None) == 1
+    need = lib.moe_w4a8_workspace_size(ctypes.byref(d))
+    assert lib.moe_w4a8_forward(*args, ctypes.byref(d), fake, fake, need - 256, None) == 3
+    assert lib.moe_w4a8_route(fake, ctypes.byref(d), fake, fake, fake, fake, fake, None, fake, need, None) == 1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    from bit_moe_expert_router_gb300 import binding
+    d = binding.dims_of(0, 256, 128, 8, 0, 2, 64)
+    fake = ctypes.c_void_p(0x100000)
+    # T = 0: valid, nothing enqueued, activations may be null
+    assert lib.moe_w4a8_forward(None, None, None, fake, fake, fake, fake, ctypes.byref(d), None, None, 0, None) == 0
+    assert lib.moe_w4a8_route(None, ctypes.byref(d), None, None, None, None, None, None, None, 0, None) == 0

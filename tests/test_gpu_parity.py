@@ -1,0 +1,261 @@
+"""Parity of the CUDA path with the CPU oracle, through the C ABI.
+
+Bit-exact: top-k ids, the permutation (counts, offsets, perm, inv) and the
+int32 per-group partial sums of both projections.  Floating point: the
+routing weights (fp32 vs fp64) and the layer output within the stated
+tolerance (max |err| <= 2e-2 rms, 99.9% within 1e-2 rms).  The requantised
+intermediate is compared code by code; a code may differ by one only where
+the oracle's value sits within rounding distance of a half-step boundary
+(the two sides' fp32 h differ in the last bits, the decision is the same
+fp32 RNE on both).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_moe_expert_router_gb300 import binding, synth
+
+import _gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+ALL = list(synth.WORKLOADS)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_lib):
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    binding._load()
+
+
+def _route_gpu(w, logits):
+    d = gh.dims(w)
+    T, k, E = w.T, w.top_k, w.E
+    dev = "cuda:0"
+    out = dict(ids=torch.empty((T, k), dtype=torch.int32, device=dev),
+               w=torch.empty((T, k), dtype=torch.float32, device=dev),
+               counts=torch.empty(E, dtype=torch.int32, device=dev),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+               perm=torch.empty(T * k, dtype=torch.int32, device=dev),
+               inv=torch.empty(T * k, dtype=torch.int32, device=dev))
+    ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), dev)
+    binding.moe_w4a8_route(gh.to_dev(logits), d, out["ids"], out["w"], out["counts"], out["offsets"], out["perm"],
+                           out["inv"], ws)
+    torch.cuda.synchronize()
+    return {k_: v.cpu().numpy() for k_, v in out.items()}
+
+
+def _check_route(w, logits):
+    got = _route_gpu(w, logits)
+    ids, wt = oracle.route(logits, w.top_k)
+    counts, offsets, perm, inv = oracle.permute(ids, w.E)
+    assert np.array_equal(got["ids"], ids)
+    assert np.array_equal(got["counts"], counts)
+    assert np.array_equal(got["offsets"], offsets)
+    assert np.array_equal(got["perm"], perm)
+    assert np.array_equal(got["inv"], inv)
+    assert np.max(np.abs(got["w"] - wt)) < 2e-6
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_route_bit_exact(name):
+    w = synth.WORKLOADS[name]
+    _check_route(w, synth.make_tokens(w).logits)
+
+
+def test_route_planted_ties():
+    rng = np.random.default_rng(5)
+    w = synth.Workload("ties", T=300, H=256, I=128, E=64, S=0, top_k=6, group=64)
+    logits = rng.integers(-2, 3, size=(w.T, w.E)).astype(np.float32)  # massive ties
+    logits[rng.random(logits.shape) < 0.2] = -0.0
+    logits[0, :] = 0.0
+    logits[1, :] = -0.0
+    _check_route(w, logits)
+    w1 = synth.Workload("ties_k1", T=300, H=256, I=128, E=64, S=0, top_k=1, group=64)
+    _check_route(w1, logits)
+    wE = synth.Workload("ties_kE", T=50, H=256, I=128, E=32, S=0, top_k=32, group=64)
+    _check_route(wE, logits[:50, :32].copy())
+
+
+def test_route_all_tokens_to_one_expert():
+    w = synth.WORKLOADS["prefill_t8192"].with_tokens(3000)
+    logits = synth.make_tokens(w).logits
+    logits[:, 77] = 1e4
+    _check_route(w, logits)
+
+
+def _sample_pairs(w, tok, n, seed=0):
+    """Sorted (slot, token) pairs: routed pairs of sampled tokens plus the shared slots."""
+    ids, _ = oracle.route(tok.logits, w.top_k)
+    rng = np.random.default_rng(seed)
+    toks = gh.sample_tokens(w.T, max(1, n // (w.top_k + w.S)), seed)
+    pairs = [(int(e), int(t)) for t in toks for e in ids[t]]
+    pairs += [(w.E + s, int(t)) for t in toks for s in range(w.S)]
+    if w.twobit_frac > 0:  # make sure 2-bit experts are covered
+        tb = np.nonzero(synth.twobit_experts(w))[0]
+        pairs += [(int(e), int(rng.integers(w.T))) for e in tb[:4]]
+    pairs.sort()
+    slots = np.array([p[0] for p in pairs], np.int32)
+    tokens = np.array([p[1] for p in pairs], np.int32)
+    return slots, tokens
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_gemm1_partials_bit_exact(name):
+    w = synth.WORKLOADS[name]
+    tok = synth.make_tokens(w)
+    bank = gh.bank_of(w)
+    w13, _, _, _ = gh.device_bank(w)
+    slots, tokens = _sample_pairs(w, tok, 96)
+    d = gh.dims(w)
+    n = slots.shape[0]
+    p1 = torch.empty((n, 2 * w.I, w.H // w.group), dtype=torch.int32, device="cuda:0")
+    ws = binding.alloc_workspace(binding.partials_workspace_size(d, n), "cuda:0")
+    binding.moe_w4a8_gemm1_partials(gh.to_dev(tok.x_q), w13, d, gh.to_dev(tokens), gh.to_dev(slots), p1, ws)
+    torch.cuda.synchronize()
+    got = p1.cpu().numpy()
+    for r in range(n):
+        ref = oracle.partials(tok.x_q[tokens[r]], bank.w13[slots[r]], w.group)
+        assert np.array_equal(got[r], ref), f"pair {r}: token {tokens[r]} slot {slots[r]}"
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_gemm2_partials_bit_exact(name):
+    w = synth.WORKLOADS[name]
+    tok = synth.make_tokens(w)
+    bank = gh.bank_of(w)
+    _, _, w2, _ = gh.device_bank(w)
+    slots, _ = _sample_pairs(w, tok, 96, seed=1)
+    n = slots.shape[0]
+    rng = np.random.default_rng(2)
+    h_q = rng.integers(-127, 128, size=(n, w.I)).astype(np.int8)
+    h_q[0, :] = 127
+    if n > 1:
+        h_q[1, :] = -127
+    d = gh.dims(w)
+    p2 = torch.empty((n, w.H, w.I // w.group), dtype=torch.int32, device="cuda:0")
+    ws = binding.alloc_workspace(binding.partials_workspace_size(d, n), "cuda:0")
+    binding.moe_w4a8_gemm2_partials(gh.to_dev(h_q), w2, d, gh.to_dev(slots), p2, ws)
+    torch.cuda.synchronize()
+    got = p2.cpu().numpy()
+    for r in range(n):
+        ref = oracle.partials(h_q[r], bank.w2[slots[r]], w.group)
+        assert np.array_equal(got[r], ref), f"pair {r}: slot {slots[r]}"
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_forward_matches_oracle(name):
+    w = synth.WORKLOADS[name]
+    tok = synth.make_tokens(w)
+    bank = gh.bank_of(w)
+    out = gh.run_forward(w, tok)
+    sel = gh.sample_tokens(w.T, 48)
+    ref = gh.oracle_out(w, tok, bank, sel)
+    gh.assert_output_close(out[sel], ref, name)
+    assert np.all(np.isfinite(out))
+    again = gh.run_forward(w, tok)
+    assert np.array_equal(out, again), "two runs differ"
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_t4", "decode_verify_t12"])
+def test_requantised_intermediate(name):
+    w = synth.WORKLOADS[name]
+    tok = synth.make_tokens(w)
+    bank = gh.bank_of(w)
+    w13, s13, w2, s2 = gh.device_bank(w)
+    d = gh.dims(w)
+    P = w.T * (w.top_k + w.S)
+    out = torch.empty((w.T, w.H), dtype=torch.float32, device="cuda:0")
+    h_q = torch.empty((P, w.I), dtype=torch.int8, device="cuda:0")
+    s_h = torch.empty(P, dtype=torch.float32, device="cuda:0")
+    y = torch.empty((P, w.H), dtype=torch.float32, device="cuda:0")
+    ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), "cuda:0")
+    binding.moe_w4a8_forward_debug(gh.to_dev(tok.x_q), gh.to_dev(tok.x_scale), gh.to_dev(tok.logits), w13, s13, w2,
+                                   s2, d, out, ws, h_q, s_h, y)
+    torch.cuda.synchronize()
+    h_q, s_h, y = h_q.cpu().numpy(), s_h.cpu().numpy(), y.cpu().numpy()
+    ids, _ = oracle.route(tok.logits, w.top_k)
+    _, _, _, inv = oracle.permute(ids, w.E)
+    od = oracle.dims(w.T, w.H, w.I, w.E, w.S, w.top_k, w.group)
+    flips = 0
+    for t in range(w.T):
+        rows = [(int(inv[t * w.top_k + j]), int(ids[t, j])) for j in range(w.top_k)]
+        rows += [(w.T * w.top_k + s * w.T + t, w.E + s) for s in range(w.S)]
+        for row, slot in rows:
+            hq_ref, sh_ref, y_ref = oracle.pair_output(od, tok.x_q, tok.x_scale, bank.w13, bank.s13, bank.w2,
+                                                       bank.s2, t, slot)
+            assert abs(s_h[row] - sh_ref) <= 1e-5 * sh_ref
+            diff = h_q[row].astype(int) - hq_ref.astype(int)
+            assert np.all(np.abs(diff) <= 1)
+            if diff.any():
+                # only at half-step boundaries of the oracle's own value
+                _, _, h = oracle.hidden(tok.x_q[t], tok.x_scale[t], bank.w13[slot], bank.s13[slot], w.group)
+                frac = np.abs(np.abs(h[diff != 0] / sh_ref) % 1.0 - 0.5)
+                assert np.all(frac < 1e-3), frac
+                flips += int(np.count_nonzero(diff))
+            scale = np.max(np.abs(y_ref)) + 1e-30
+            assert np.max(np.abs(y[row] - y_ref)) <= 2e-2 * scale
+    assert flips <= 1e-3 * P * w.I
+
+
+# ------------------------------------------------------------------ edge cases
+
+SMALL = synth.Workload("small_s1", T=16, H=256, I=128, E=8, S=1, top_k=2, group=64)
+
+
+@pytest.mark.parametrize("T", [1, 2, 37, 64, 65, 130, 257])
+def test_ragged_batch_sizes(T):
+    w = SMALL.with_tokens(T)
+    tok = synth.make_tokens(w)
+    out = gh.run_forward(w, tok)
+    gh.assert_output_close(out, gh.oracle_out(w, tok, gh.bank_of(w)), f"T={T}")
+
+
+@pytest.mark.parametrize("k", [1, 8])
+def test_top_k_extremes(k):
+    w = synth.Workload("k", T=40, H=256, I=128, E=8, S=0, top_k=k, group=64)
+    tok = synth.make_tokens(w)
+    gh.assert_output_close(gh.run_forward(w, tok), gh.oracle_out(w, tok, gh.bank_of(w)), f"k={k}")
+
+
+def test_single_expert_dense_case():
+    w = synth.Workload("dense", T=70, H=256, I=128, E=1, S=0, top_k=1, group=128)
+    tok = synth.make_tokens(w)
+    gh.assert_output_close(gh.run_forward(w, tok), gh.oracle_out(w, tok, gh.bank_of(w)), "E=1")
+
+
+def test_all_tokens_on_one_expert_spans_many_tiles():
+    w = SMALL.with_tokens(300)
+    tok = synth.make_tokens(w)
+    tok.logits[:, 5] = 50.0
+    out = gh.run_forward(w, tok)
+    gh.assert_output_close(out, gh.oracle_out(w, tok, gh.bank_of(w)), "one hot expert")
+
+
+def test_zero_weight_expert_and_zero_token():
+    w = SMALL.with_tokens(33)
+    tok = synth.make_tokens(w)
+    b = gh.bank_of(w)
+    bank = synth.Bank(b.w13.copy(), b.s13.copy(), b.w2.copy(), b.s2.copy(), b.twobit)
+    for a in (bank.w13, bank.s13, bank.w2, bank.s2):
+        a[3] = 0
+    tok.x_q[4] = 0
+    tok.x_scale[4] = 0.0
+    dev_bank = tuple(gh.to_dev(a) for a in (bank.w13, bank.s13, bank.w2, bank.s2))
+    out = gh.run_forward(w, tok, dev_bank)
+    ref = gh.oracle_out(w, tok, bank)
+    gh.assert_output_close(out, ref, "zero expert")
+    assert np.array_equal(out[4], np.zeros(w.H, np.float32))  # zero activations give exactly zero
+
+
+def test_empty_batch_leaves_output_untouched():
+    w = SMALL.with_tokens(0)
+    w13, s13, w2, s2 = gh.device_bank(w)
+    d = gh.dims(w)
+    out = torch.empty((0, w.H), dtype=torch.float32, device="cuda:0")
+    e = lambda *s, dt=torch.float32: torch.empty(s, dtype=dt, device="cuda:0")  # noqa: E731
+    ws = binding.alloc_workspace(256, "cuda:0")
+    binding.moe_w4a8_forward(e(0, w.H, dt=torch.int8), e(0), e(0, w.E), w13, s13, w2, s2, d, out, ws)
+    torch.cuda.synchronize()
