@@ -15,7 +15,8 @@ CPU implementation.
 from __future__ import annotations
 
 __all__ = ["moe_w4a8_forward", "moe_w4a8_route", "moe_w4a8_gemm1_partials", "moe_w4a8_gemm2_partials",
-           "moe_w4a8_workspace_size", "moe_w4a8_version", "moe_w4a8_status_string", "Dims", "MoeError"]
+           "moe_w4a8_workspace_size", "moe_w4a8_version", "moe_w4a8_status_string", "moe_w4a8_forward_noalloc",
+           "Dims", "MoeError"]
 
 
 def __getattr__(name):

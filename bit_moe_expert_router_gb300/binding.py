@@ -15,6 +15,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_w4a8.so")
 ABI_VERSION = 1
+NOALLOC_SCRATCH_BYTES = 16 << 20
 _lib = None
 
 
@@ -50,8 +51,9 @@ def _load():
     lib.moe_w4a8_route.argtypes = [p, dp, p, p, p, p, p, p, p, sz, p]
     lib.moe_w4a8_gemm1_partials.argtypes = [p, p, dp, p, p, i64, p, p, sz, p]
     lib.moe_w4a8_gemm2_partials.argtypes = [p, p, dp, p, i64, p, p, sz, p]
+    lib.moe_w4a8_forward_noalloc.argtypes = [p, p, p, p, p, p, p, dp, p, p]
     for name in ("moe_w4a8_forward", "moe_w4a8_forward_debug", "moe_w4a8_route", "moe_w4a8_gemm1_partials",
-                 "moe_w4a8_gemm2_partials"):
+                 "moe_w4a8_gemm2_partials", "moe_w4a8_forward_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.moe_w4a8_version() != ABI_VERSION:
         raise RuntimeError(f"{LIB_PATH}: ABI version {lib.moe_w4a8_version()} != {ABI_VERSION}")
@@ -145,6 +147,23 @@ def moe_w4a8_forward(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_pack
     _check("moe_w4a8_forward", _load().moe_w4a8_forward(
         _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
         _ptr(w2_scale), ctypes.byref(d), _ptr(out), wp, wb, _stream(out.device)))
+    return out
+
+
+def moe_w4a8_forward_noalloc(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d: Dims,
+                             out):
+    """The layer using the library's built-in scratch array instead of a workspace.
+
+    For callers that cannot allocate device memory when they run the layer
+    (runtimes that own all device memory, or hot paths where cudaMalloc is
+    not allowed).  Calls on one device share the array, so calls that may
+    overlap on the GPU must be serialised; layers needing more than
+    NOALLOC_SCRATCH_BYTES of intermediates are rejected.
+    """
+    _check_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out)
+    _check("moe_w4a8_forward_noalloc", _load().moe_w4a8_forward_noalloc(
+        _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
+        _ptr(w2_scale), ctypes.byref(d), _ptr(out), _stream(out.device)))
     return out
 
 

@@ -3,6 +3,8 @@
 // runs in the kernels of route.cu and gemm_mma.cu.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "kernels.h"
 #include "moe_w4a8.h"
 
@@ -305,4 +307,47 @@ MOE_API int moe_w4a8_gemm2_partials(const int8_t* h_q, const uint8_t* w2_packed,
     g2.p2 = p2;
     MOE_CUDA(moe::launch_gemm2(moe::Gemm2Mode::kPartials, g2, static_cast<int>(L.max_tiles), st));
     return MOE_OK;
+}
+
+// ------------------------------------------------------------------ no-alloc variant
+// The scratch array of moe_w4a8_forward_noalloc.  Host code must not pass
+// `g_noalloc_scratch` itself to a kernel (on the host it names a stand-in,
+// not device memory); its device address is looked up once per device.
+namespace {
+constexpr size_t kNoAllocBytes = MOE_W4A8_NOALLOC_SCRATCH_BYTES;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (first call per device resolves it).
+int noalloc_scratch(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) return MOE_ERR_CUDA;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return MOE_OK;
+}
+}  // namespace
+
+MOE_API int moe_w4a8_forward_noalloc(const int8_t* x_q, const float* x_scale, const float* router_logits,
+                                     const uint8_t* w13_packed, const float* w13_scale, const uint8_t* w2_packed,
+                                     const float* w2_scale, const moe_dims_t* d, float* out, void* stream) {
+    MOE_TRY(check_dims(d));
+    MOE_TRY(check_ptrs({w13_packed, w13_scale, w2_packed, w2_scale}));
+    if (d->T == 0) return MOE_OK;
+    MOE_TRY(check_ptrs({x_q, x_scale, router_logits, out}));
+    const WsLayout L = layout_of(d);
+    if (L.total > kNoAllocBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    void* ws = nullptr;
+    MOE_TRY(noalloc_scratch(&ws));
+    return run_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out, L,
+                     views(ws, L), static_cast<cudaStream_t>(stream));
 }

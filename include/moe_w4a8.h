@@ -159,6 +159,44 @@ int moe_w4a8_gemm2_partials(const int8_t* h_q, const uint8_t* w2_packed, const m
                             const int32_t* pair_slot, int64_t n_pairs,
                             int32_t* p2, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Bytes of the library's built-in scratch array used by
+ * moe_w4a8_forward_noalloc (16 MiB).
+ */
+#define MOE_W4A8_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * moe_w4a8_forward without a caller-supplied workspace.  (The pages have no
+ * counterpart; this is a library convenience.)
+ *
+ * For callers that cannot allocate device memory when they run the layer:
+ * plugin hosts and inference runtimes that own all device memory and hand
+ * out only the tensors they manage, code that must not call cudaMalloc on
+ * its hot path (it synchronises the device and can fail under memory
+ * pressure), or embedded runtimes that allocate everything once at start-up.
+ * The intermediates live in one fixed array inside the library, of
+ * MOE_W4A8_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the
+ * library holds until the process exits.  This call allocates nothing and
+ * calls no allocating routine.
+ *
+ * Arguments, layouts, errors and the result are those of moe_w4a8_forward;
+ * the caller still passes the inputs and `out`.  Layers whose
+ * moe_w4a8_workspace_size(d) exceeds the array return
+ * MOE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued (for the 512-expert
+ * decode layer, H=2048, I=512, top-10, one shared expert, that is T > ~128).
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before capturing any stream into a
+ * CUDA graph.  All calls on a device share the one array: two calls whose
+ * kernels may overlap on the GPU (different streams without ordering
+ * between them) race and produce wrong results; serialise them.  Nothing
+ * from a previous call is reused -- each call initialises what it reads.
+ */
+int moe_w4a8_forward_noalloc(const int8_t* x_q, const float* x_scale, const float* router_logits,
+                             const uint8_t* w13_packed, const float* w13_scale,
+                             const uint8_t* w2_packed, const float* w2_scale,
+                             const moe_dims_t* d, float* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
