@@ -14,14 +14,19 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_w4a8.so")
-ABI_VERSION = 1
+ABI_VERSION = 2
+ENGINE_AUTO, ENGINE_GROUPED, ENGINE_DECODE = -1, 0, 1
 NOALLOC_SCRATCH_BYTES = 16 << 20
 _lib = None
 
 
 class MoeError(RuntimeError):
     def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn} failed with status {status}: {_load().moe_w4a8_status_string(status).decode()}")
+        lib = _load()
+        msg = f"{fn} failed with status {status}: {lib.moe_w4a8_status_string(status).decode()}"
+        if status == 4:
+            msg += f" [{lib.moe_w4a8_last_error().decode()}]"
+        super().__init__(msg)
         self.status = status
 
 
@@ -44,16 +49,23 @@ def _load():
     lib.moe_w4a8_version.restype = ctypes.c_int
     lib.moe_w4a8_status_string.argtypes = [ctypes.c_int]
     lib.moe_w4a8_status_string.restype = ctypes.c_char_p
+    lib.moe_w4a8_last_error.restype = ctypes.c_char_p
     lib.moe_w4a8_workspace_size.argtypes = [dp]
     lib.moe_w4a8_workspace_size.restype = sz
     lib.moe_w4a8_forward.argtypes = [p, p, p, p, p, p, p, dp, p, p, sz, p]
-    lib.moe_w4a8_forward_debug.argtypes = [p, p, p, p, p, p, p, dp, p, p, p, p, p, sz, p]
+    ci = ctypes.c_int
+    lib.moe_w4a8_forward_debug.argtypes = [p, p, p, p, p, p, p, dp, p, p, p, p, ci, p, sz, p]
     lib.moe_w4a8_route.argtypes = [p, dp, p, p, p, p, p, p, p, sz, p]
-    lib.moe_w4a8_gemm1_partials.argtypes = [p, p, dp, p, p, i64, p, p, sz, p]
-    lib.moe_w4a8_gemm2_partials.argtypes = [p, p, dp, p, i64, p, p, sz, p]
+    lib.moe_w4a8_gemm1_partials.argtypes = [p, p, dp, p, p, i64, p, ci, p, sz, p]
+    lib.moe_w4a8_gemm2_partials.argtypes = [p, p, dp, p, i64, p, ci, p, sz, p]
+    lib.moe_w4a8_device_status.argtypes = [p, sz, p]
+    lib.moe_w4a8_engine_for.argtypes = [dp]
+    lib.moe_w4a8_engine_for.restype = ctypes.c_int
+    lib.moe_w4a8_selftest_barrier_timeout.argtypes = [p, sz, p]
     lib.moe_w4a8_forward_noalloc.argtypes = [p, p, p, p, p, p, p, dp, p, p]
     for name in ("moe_w4a8_forward", "moe_w4a8_forward_debug", "moe_w4a8_route", "moe_w4a8_gemm1_partials",
-                 "moe_w4a8_gemm2_partials", "moe_w4a8_forward_noalloc"):
+                 "moe_w4a8_gemm2_partials", "moe_w4a8_forward_noalloc", "moe_w4a8_device_status",
+                 "moe_w4a8_selftest_barrier_timeout"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.moe_w4a8_version() != ABI_VERSION:
         raise RuntimeError(f"{LIB_PATH}: ABI version {lib.moe_w4a8_version()} != {ABI_VERSION}")
@@ -97,6 +109,11 @@ def moe_w4a8_version() -> int:
 
 def moe_w4a8_status_string(status: int) -> str:
     return _load().moe_w4a8_status_string(status).decode()
+
+
+def moe_w4a8_engine_for(d: Dims) -> int:
+    """ENGINE_DECODE or ENGINE_GROUPED: what moe_w4a8_forward runs for these sizes on the current device."""
+    return _load().moe_w4a8_engine_for(ctypes.byref(d))
 
 
 def moe_w4a8_workspace_size(d: Dims) -> int:
@@ -168,7 +185,7 @@ def moe_w4a8_forward_noalloc(x_q, x_scale, router_logits, w13_packed, w13_scale,
 
 
 def moe_w4a8_forward_debug(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d: Dims, out,
-                           workspace, h_q=None, s_h=None, y=None):
+                           workspace, h_q=None, s_h=None, y=None, engine: int = ENGINE_AUTO):
     _check_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out)
     P = d.T * (d.top_k + d.n_shared)
     if h_q is not None:
@@ -180,7 +197,8 @@ def moe_w4a8_forward_debug(x_q, x_scale, router_logits, w13_packed, w13_scale, w
     wp, wb = _ws_view(workspace)
     _check("moe_w4a8_forward_debug", _load().moe_w4a8_forward_debug(
         _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
-        _ptr(w2_scale), ctypes.byref(d), _ptr(out), _ptr(h_q), _ptr(s_h), _ptr(y), wp, wb, _stream(out.device)))
+        _ptr(w2_scale), ctypes.byref(d), _ptr(out), _ptr(h_q), _ptr(s_h), _ptr(y), engine, wp, wb,
+        _stream(out.device)))
     return out
 
 
@@ -198,7 +216,8 @@ def moe_w4a8_route(router_logits, d: Dims, topk_ids, topk_w, counts, offsets, pe
         _ptr(perm), _ptr(inv), wp, wb, _stream(router_logits.device)))
 
 
-def moe_w4a8_gemm1_partials(x_q, w13_packed, d: Dims, pair_token, pair_slot, p1, workspace):
+def moe_w4a8_gemm1_partials(x_q, w13_packed, d: Dims, pair_token, pair_slot, p1, workspace,
+                            engine: int = ENGINE_GROUPED):
     n = pair_slot.shape[0]
     _need(x_q, "x_q", torch.int8, (d.T, d.H))
     _need(w13_packed, "w13_packed", torch.uint8, _bank_shapes(d)[0])
@@ -207,11 +226,11 @@ def moe_w4a8_gemm1_partials(x_q, w13_packed, d: Dims, pair_token, pair_slot, p1,
     _need(p1, "p1", torch.int32, (n, 2 * d.I, d.H // d.group))
     wp, wb = _ws_view(workspace)
     _check("moe_w4a8_gemm1_partials", _load().moe_w4a8_gemm1_partials(
-        _ptr(x_q), _ptr(w13_packed), ctypes.byref(d), _ptr(pair_token), _ptr(pair_slot), n, _ptr(p1), wp, wb,
-        _stream(p1.device)))
+        _ptr(x_q), _ptr(w13_packed), ctypes.byref(d), _ptr(pair_token), _ptr(pair_slot), n, _ptr(p1), engine, wp,
+        wb, _stream(p1.device)))
 
 
-def moe_w4a8_gemm2_partials(h_q, w2_packed, d: Dims, pair_slot, p2, workspace):
+def moe_w4a8_gemm2_partials(h_q, w2_packed, d: Dims, pair_slot, p2, workspace, engine: int = ENGINE_GROUPED):
     n = pair_slot.shape[0]
     _need(h_q, "h_q", torch.int8, (n, d.I))
     _need(w2_packed, "w2_packed", torch.uint8, _bank_shapes(d)[2])
@@ -219,7 +238,21 @@ def moe_w4a8_gemm2_partials(h_q, w2_packed, d: Dims, pair_slot, p2, workspace):
     _need(p2, "p2", torch.int32, (n, d.H, d.I // d.group))
     wp, wb = _ws_view(workspace)
     _check("moe_w4a8_gemm2_partials", _load().moe_w4a8_gemm2_partials(
-        _ptr(h_q), _ptr(w2_packed), ctypes.byref(d), _ptr(pair_slot), n, _ptr(p2), wp, wb, _stream(p2.device)))
+        _ptr(h_q), _ptr(w2_packed), ctypes.byref(d), _ptr(pair_slot), n, _ptr(p2), engine, wp, wb,
+        _stream(p2.device)))
+
+
+def moe_w4a8_selftest_barrier_timeout(workspace: torch.Tensor):
+    """Enqueue the bounded-wait self-test (see the C header); read the result with moe_w4a8_device_status."""
+    wp, wb = _ws_view(workspace)
+    _check("moe_w4a8_selftest_barrier_timeout",
+           _load().moe_w4a8_selftest_barrier_timeout(wp, wb, _stream(workspace.device)))
+
+
+def moe_w4a8_device_status(workspace: torch.Tensor) -> int:
+    """Synchronises the current stream and returns the status word of the last call (0 = ok, 5 = timeout)."""
+    wp, wb = _ws_view(workspace)
+    return _load().moe_w4a8_device_status(wp, wb, _stream(workspace.device))
 
 
 class Layer:

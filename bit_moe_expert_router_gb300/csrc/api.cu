@@ -3,8 +3,10 @@
 // runs in the kernels of route.cu and gemm_mma.cu.
 #include <cuda_runtime.h>
 
+#include <cstdio>
 #include <mutex>
 
+#include "decode.h"
 #include "kernels.h"
 #include "moe_w4a8.h"
 
@@ -43,14 +45,20 @@ int check_ws(const WsLayout& L, const void* ws, size_t bytes) {
     return MOE_OK;
 }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+thread_local char g_last_error[256] = "";
+
+int cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return MOE_OK;
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+}
 
 #define MOE_TRY(expr)                          \
     do {                                       \
         int _rc = (expr);                      \
         if (_rc != MOE_OK) return _rc;         \
     } while (0)
-#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+#define MOE_CUDA(expr) MOE_TRY(cuda_status((expr), #expr))
 
 struct Views {
     moe::Header* hdr;
@@ -102,10 +110,49 @@ moe::SortArgs sort_args(const Views& v, const int32_t* ids, int64_t T, int64_t k
     return a;
 }
 
+// The fused decode engine's plan for a forward call, if the sizes fit it.
+bool decode_forward_plan(const moe_dims_t* d, moe::DecodePlan* pl) {
+    return moe::decode_plan(d->T, d->H, d->I, d->E, d->n_shared, d->top_k, d->group, 0, moe::DecodeMode::kForward,
+                            moe::decode_grid(), moe::decode_max_smem(), pl);
+}
+
+int run_decode(const int8_t* x_q, const float* x_scale, const float* logits, const uint8_t* w13, const float* s13,
+               const uint8_t* w2, const float* s2, const moe_dims_t* d, float* out, const Views& v,
+               const moe::DecodePlan& pl, float* y_debug, cudaStream_t st) {
+    moe::DecodeArgs a{};
+    a.x_q = x_q;
+    a.x_scale = x_scale;
+    a.logits = logits;
+    a.w13 = w13;
+    a.s13 = s13;
+    a.w2 = w2;
+    a.s2 = s2;
+    a.T = static_cast<int>(d->T);
+    a.H = static_cast<int>(d->H);
+    a.I = static_cast<int>(d->I);
+    a.E = static_cast<int>(d->E);
+    a.S = static_cast<int>(d->n_shared);
+    a.k = static_cast<int>(d->top_k);
+    a.g = static_cast<int>(d->group);
+    a.out = out;
+    a.hdr = v.hdr;
+    a.h = v.h;
+    a.amax = v.amax;
+    a.y = y_debug;
+    MOE_CUDA(moe::launch_decode(moe::DecodeMode::kForward, a, pl, moe::decode_grid(), st));
+    return MOE_OK;
+}
+
 // route + permute + gemm1 + gemm2 + combine on the workspace views.
 int run_layer(const int8_t* x_q, const float* x_scale, const float* logits, const uint8_t* w13, const float* s13,
               const uint8_t* w2, const float* s2, const moe_dims_t* d, float* out, const WsLayout& L, const Views& v,
-              cudaStream_t st) {
+              cudaStream_t st, int engine = MOE_ENGINE_AUTO, float* y_debug = nullptr) {
+    if (engine != MOE_ENGINE_GROUPED) {
+        moe::DecodePlan pl;
+        if (decode_forward_plan(d, &pl))
+            return run_decode(x_q, x_scale, logits, w13, s13, w2, s2, d, out, v, pl, y_debug, st);
+        if (engine == MOE_ENGINE_DECODE) return MOE_ERR_UNSUPPORTED;
+    }
     MOE_CUDA(moe::launch_route_topk(logits, d->T, d->E, d->top_k, v.ids, v.wts, st));
     MOE_CUDA(moe::launch_sort(sort_args(v, v.ids, d->T, d->top_k, d->E, d->n_shared, L.P), st));
 
@@ -154,12 +201,15 @@ int run_layer(const int8_t* x_q, const float* x_scale, const float* logits, cons
     c.S = d->n_shared;
     c.out = out;
     MOE_CUDA(moe::launch_combine(c, st));
+    if (y_debug) MOE_CUDA(cudaMemcpyAsync(y_debug, v.y, sizeof(float) * L.P * d->H, cudaMemcpyDeviceToDevice, st));
     return MOE_OK;
 }
 
 }  // namespace
 
 MOE_API int moe_w4a8_version(void) { return MOE_W4A8_ABI_VERSION; }
+
+MOE_API const char* moe_w4a8_last_error(void) { return g_last_error; }
 
 MOE_API const char* moe_w4a8_status_string(int status) {
     switch (status) {
@@ -176,6 +226,12 @@ MOE_API const char* moe_w4a8_status_string(int status) {
 MOE_API size_t moe_w4a8_workspace_size(const moe_dims_t* d) {
     if (check_dims(d) != MOE_OK) return 0;
     return layout_of(d).total;
+}
+
+MOE_API int moe_w4a8_engine_for(const moe_dims_t* d) {
+    if (check_dims(d) != MOE_OK) return -1;
+    moe::DecodePlan pl;
+    return decode_forward_plan(d, &pl) ? MOE_ENGINE_DECODE : MOE_ENGINE_GROUPED;
 }
 
 MOE_API int moe_w4a8_forward(const int8_t* x_q, const float* x_scale, const float* router_logits,
@@ -195,7 +251,7 @@ MOE_API int moe_w4a8_forward(const int8_t* x_q, const float* x_scale, const floa
 MOE_API int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, const float* router_logits,
                                    const uint8_t* w13_packed, const float* w13_scale, const uint8_t* w2_packed,
                                    const float* w2_scale, const moe_dims_t* d, float* out, int8_t* h_q, float* s_h,
-                                   float* y, void* workspace, size_t workspace_bytes, void* stream) {
+                                   float* y, int engine, void* workspace, size_t workspace_bytes, void* stream) {
     MOE_TRY(check_dims(d));
     MOE_TRY(check_ptrs({w13_packed, w13_scale, w2_packed, w2_scale}));
     if (d->T == 0) return MOE_OK;
@@ -206,9 +262,10 @@ MOE_API int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, cons
     MOE_TRY(check_ws(L, workspace, workspace_bytes));
     const Views v = views(workspace, L);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    MOE_TRY(run_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out, L, v, st));
+    if (engine < MOE_ENGINE_AUTO || engine > MOE_ENGINE_DECODE) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(run_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out, L, v, st,
+                      engine, y));
     if (h_q || s_h) MOE_CUDA(moe::launch_requant_copy(v.h, v.amax, L.P, d->I, h_q, s_h, st));
-    if (y) MOE_CUDA(cudaMemcpyAsync(y, v.y, sizeof(float) * L.P * d->H, cudaMemcpyDeviceToDevice, st));
     return MOE_OK;
 }
 
@@ -251,15 +308,53 @@ int group_pairs(const moe_dims_t* d, const int32_t* pair_token, const int32_t* p
 }
 }  // namespace
 
+// The decode engine's integer core on an explicit pair list (phase 1 or phase 2 alone).
+int decode_partials(moe::DecodeMode mode, const moe_dims_t* d, const int8_t* x_or_hq, const uint8_t* w,
+                    const int32_t* pair_token, const int32_t* pair_slot, int64_t n_pairs, int32_t* p, void* workspace,
+                    size_t workspace_bytes, cudaStream_t st) {
+    const int64_t T = mode == moe::DecodeMode::kGemm1Partials ? d->T : 0;
+    moe::DecodePlan pl;
+    if (!moe::decode_plan(T, d->H, d->I, d->E, 0, 1, d->group, n_pairs, mode, moe::decode_grid(),
+                          moe::decode_max_smem(), &pl))
+        return MOE_ERR_UNSUPPORTED;
+    const WsLayout L = moe::ws_layout(n_pairs, d->H, d->I, d->E + d->n_shared, 0, 1);
+    MOE_TRY(check_ws(L, workspace, workspace_bytes));
+    Views v = views(workspace, L);
+    moe::DecodeArgs a{};
+    a.x_q = mode == moe::DecodeMode::kGemm1Partials ? x_or_hq : nullptr;
+    a.h_q_in = mode == moe::DecodeMode::kGemm2Partials ? x_or_hq : nullptr;
+    a.w13 = w;
+    a.w2 = w;
+    a.T = static_cast<int>(T);
+    a.H = static_cast<int>(d->H);
+    a.I = static_cast<int>(d->I);
+    a.E = static_cast<int>(d->E + d->n_shared);
+    a.S = 0;
+    a.k = 1;
+    a.g = static_cast<int>(d->group);
+    a.pair_token = pair_token;
+    a.pair_slot = pair_slot;
+    a.n_pairs = static_cast<int>(n_pairs);
+    a.p1 = p;
+    a.p2 = p;
+    a.hdr = v.hdr;
+    MOE_CUDA(moe::launch_decode(mode, a, pl, moe::decode_grid(), st));
+    return MOE_OK;
+}
+
 MOE_API int moe_w4a8_gemm1_partials(const int8_t* x_q, const uint8_t* w13_packed, const moe_dims_t* d,
                                     const int32_t* pair_token, const int32_t* pair_slot, int64_t n_pairs, int32_t* p1,
-                                    void* workspace, size_t workspace_bytes, void* stream) {
+                                    int engine, void* workspace, size_t workspace_bytes, void* stream) {
     MOE_TRY(check_dims(d));
     if (n_pairs < 0 || n_pairs >= (int64_t(1) << 24)) return MOE_ERR_INVALID_ARG;
+    if (engine < MOE_ENGINE_AUTO || engine > MOE_ENGINE_DECODE) return MOE_ERR_INVALID_ARG;
     if (n_pairs == 0) return MOE_OK;
     if (d->E + d->n_shared > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED;
     MOE_TRY(check_ptrs({x_q, w13_packed, pair_token, pair_slot, p1}));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (engine == MOE_ENGINE_DECODE)
+        return decode_partials(moe::DecodeMode::kGemm1Partials, d, x_q, w13_packed, pair_token, pair_slot, n_pairs,
+                               p1, workspace, workspace_bytes, st);
     WsLayout L;
     Views v;
     MOE_TRY(group_pairs(d, pair_token, pair_slot, n_pairs, workspace, workspace_bytes, st, &L, &v));
@@ -282,14 +377,18 @@ MOE_API int moe_w4a8_gemm1_partials(const int8_t* x_q, const uint8_t* w13_packed
 }
 
 MOE_API int moe_w4a8_gemm2_partials(const int8_t* h_q, const uint8_t* w2_packed, const moe_dims_t* d,
-                                    const int32_t* pair_slot, int64_t n_pairs, int32_t* p2, void* workspace,
-                                    size_t workspace_bytes, void* stream) {
+                                    const int32_t* pair_slot, int64_t n_pairs, int32_t* p2, int engine,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
     MOE_TRY(check_dims(d));
     if (n_pairs < 0 || n_pairs >= (int64_t(1) << 24)) return MOE_ERR_INVALID_ARG;
+    if (engine < MOE_ENGINE_AUTO || engine > MOE_ENGINE_DECODE) return MOE_ERR_INVALID_ARG;
     if (n_pairs == 0) return MOE_OK;
     if (d->E + d->n_shared > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED;
     MOE_TRY(check_ptrs({h_q, w2_packed, pair_slot, p2}));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (engine == MOE_ENGINE_DECODE)
+        return decode_partials(moe::DecodeMode::kGemm2Partials, d, h_q, w2_packed, pair_slot, pair_slot, n_pairs, p2,
+                               workspace, workspace_bytes, st);
     WsLayout L;
     Views v;
     MOE_TRY(group_pairs(d, pair_slot, pair_slot, n_pairs, workspace, workspace_bytes, st, &L, &v));
@@ -306,6 +405,23 @@ MOE_API int moe_w4a8_gemm2_partials(const int8_t* h_q, const uint8_t* w2_packed,
     g2.hdr = v.hdr;
     g2.p2 = p2;
     MOE_CUDA(moe::launch_gemm2(moe::Gemm2Mode::kPartials, g2, static_cast<int>(L.max_tiles), st));
+    return MOE_OK;
+}
+
+MOE_API int moe_w4a8_device_status(const void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < sizeof(moe::Header))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t status = 0;
+    MOE_CUDA(cudaMemcpyAsync(&status, workspace, sizeof(status), cudaMemcpyDeviceToHost, st));
+    MOE_CUDA(cudaStreamSynchronize(st));
+    return (status & moe::kDevTimeout) ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+}
+
+MOE_API int moe_w4a8_selftest_barrier_timeout(void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < sizeof(moe::Header))
+        return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(moe::launch_barrier_timeout_probe(static_cast<moe::Header*>(workspace), static_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
 

@@ -1,0 +1,56 @@
+// Fused decode engine (decode.cu): launcher interface.
+#pragma once
+
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kDecodeMaxT = 32;        // tokens per launch
+constexpr int kDecodeMaxPairs = 512;   // routed (or listed) pair rows per launch
+constexpr int kMaxI = 2048;            // expert intermediate size
+
+enum class DecodeMode { kForward, kGemm1Partials, kGemm2Partials };
+
+struct DecodeArgs {
+    const int8_t* x_q;
+    const float* x_scale;
+    const float* logits;
+    const uint8_t* w13;
+    const float* s13;
+    const uint8_t* w2;
+    const float* s2;
+    int T, H, I, E, S, k, g;
+    // pair-list modes (pairs sorted by slot)
+    const int32_t* pair_token;
+    const int32_t* pair_slot;
+    int n_pairs;
+    const int8_t* h_q_in;    // [n_pairs][I] (gemm2 partials)
+    // outputs
+    float* out;              // [T][H]
+    int32_t* p1;             // [n_pairs][2I][H/g]
+    int32_t* p2;             // [n_pairs][H][I/g]
+    // workspace
+    Header* hdr;
+    float* h;                // [P][I]
+    uint32_t* amax;          // [P] row maxima (debug copies; may be null)
+    float* y;                // [P][H] (debug copies; may be null)
+};
+
+// Byte offsets of the shared-memory arrays of one launch.
+struct DecodePlan {
+    int rows_pc;      // down-projection output rows per CTA
+    int smem_slots;   // slots whose down-projection slice is staged in shared memory
+    int smem_bytes;
+    int off_bar, off_flags, off_ids, off_wts, off_pos, off_pair_of, off_row_tok, off_slot_e, off_slot_row0,
+        off_slot_cnt, off_n_slots, off_xs, off_sh, off_x, off_hq, off_y, off_w2s;
+};
+
+bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t k, int64_t g, int64_t n_pairs,
+                 DecodeMode mode, int grid, int max_smem, DecodePlan* out);
+bool decode_shape_supported(int64_t H, int64_t I);
+int decode_grid();
+int decode_max_smem();
+cudaError_t launch_decode(DecodeMode mode, const DecodeArgs& a, const DecodePlan& pl, int grid, cudaStream_t st);
+cudaError_t launch_barrier_timeout_probe(Header* hdr, cudaStream_t st);
+
+}  // namespace moe

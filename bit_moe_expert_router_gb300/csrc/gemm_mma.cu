@@ -424,7 +424,8 @@ int grid_for(K kernel, int smem_bytes, int64_t max_work) {
         if (it != cache.end()) {
             per_sm = it->second;
         } else {
-            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+            // one limit per kernel: the largest stage size any group width needs
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * stage_bytes(kMaxGroup));
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem_bytes);
             per_sm = std::max(per_sm, 1);
             cache[key] = per_sm;

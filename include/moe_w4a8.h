@@ -60,9 +60,10 @@
  * MOE_ERR_INVALID_ARG for a null or misaligned pointer (16-byte alignment
  * is required for every array), non-positive sizes, top_k outside [1, E],
  * g not a multiple of 32, or H or I not a multiple of g;
- * MOE_ERR_UNSUPPORTED for sizes beyond the kernels' limits (E + S > 4096,
- * top_k > 32, g > 256); MOE_ERR_WORKSPACE_TOO_SMALL; MOE_ERR_CUDA if a
- * launch is rejected.  Errors that occur while the kernels run surface at
+ * MOE_ERR_UNSUPPORTED for sizes beyond the kernels' limits (E > 1024,
+ * S > 8, top_k > 32, g > 256, I not a multiple of 64, H not a multiple of
+ * 128, T > 2^24); MOE_ERR_WORKSPACE_TOO_SMALL; MOE_ERR_CUDA if a launch is
+ * rejected.  Errors that occur while the kernels run surface at
  * the caller's next synchronisation, as for any CUDA work.  T = 0 is valid
  * and enqueues nothing.
  */
@@ -76,7 +77,15 @@
 extern "C" {
 #endif
 
-#define MOE_W4A8_ABI_VERSION 1
+#define MOE_W4A8_ABI_VERSION 2
+
+/* Engines (the `engine` argument of the checking entry points).  AUTO picks
+ * what moe_w4a8_forward picks: the fused decode engine when the batch fits
+ * it (T <= 32, T*k <= 512 pairs, H a multiple of 1024, I a multiple of
+ * 512, I/g a multiple of 4), the grouped tensor-core engine otherwise. */
+#define MOE_ENGINE_AUTO (-1)
+#define MOE_ENGINE_GROUPED 0
+#define MOE_ENGINE_DECODE 1
 
 typedef enum {
     MOE_OK = 0,
@@ -99,9 +108,19 @@ int moe_w4a8_version(void);
 /* Static text for a status code (never NULL). */
 const char* moe_w4a8_status_string(int status);
 
+/* The CUDA error behind this thread's most recent MOE_ERR_CUDA (the failing
+ * call and CUDA's message), or "" if there was none.  Never NULL. */
+const char* moe_w4a8_last_error(void);
+
 /* Bytes of workspace moe_w4a8_forward and moe_w4a8_route need for `d`
  * (0 if `d` is invalid).  Host call, no device work. */
 size_t moe_w4a8_workspace_size(const moe_dims_t* d);
+
+/* The engine moe_w4a8_forward uses for `d` on the current device
+ * (MOE_ENGINE_DECODE or MOE_ENGINE_GROUPED), or -1 if `d` is invalid.
+ * The decode engine is one kernel launch per call (after a 16-byte memset
+ * of its barrier counters); the grouped engine is seven launches. */
+int moe_w4a8_engine_for(const moe_dims_t* d);
 
 /*
  * The whole layer: route, permute, gemm1 + act + requant, gemm2, combine.
@@ -126,38 +145,62 @@ int moe_w4a8_route(const float* router_logits, const moe_dims_t* d,
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * The layer with its intermediates exposed, for checking: runs exactly the
- * kernels of moe_w4a8_forward and additionally copies out h_q int8
- * [P][I] and s_h float [P] (P = T*k + T*S pair rows, in pair-row order), and
- * Y float [P][H] (the per-pair down-projection outputs).  Any of the three
- * may be NULL.
+ * The layer with its intermediates exposed, for checking: with engine =
+ * MOE_ENGINE_AUTO it runs exactly the kernels of moe_w4a8_forward (another
+ * engine value forces that engine; MOE_ERR_UNSUPPORTED if the sizes do not
+ * fit it) and additionally copies out h_q int8 [P][I] and s_h float [P]
+ * (P = T*k + T*S pair rows, in pair-row order), and Y float [P][H] (the
+ * per-pair down-projection outputs).  Any of the three may be NULL.
  */
 int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, const float* router_logits,
                            const uint8_t* w13_packed, const float* w13_scale,
                            const uint8_t* w2_packed, const float* w2_scale,
                            const moe_dims_t* d, float* out, int8_t* h_q, float* s_h, float* y,
-                           void* workspace, size_t workspace_bytes, void* stream);
+                           int engine, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Int32 partial sums of the gate/up projection for an explicit list of
- * pairs, through the same grouped-GEMM main loop as moe_w4a8_forward:
- * for pair r (token pair_token[r], bank slot pair_slot[r], both int32
- * device arrays of n_pairs entries), p1[r][n][q] = P1 for n < 2I, q < H/g.
- * The pairs are grouped by slot internally; pair_slot must be sorted
- * ascending.  workspace as for moe_w4a8_forward.
+ * pairs, through the main loop of the chosen engine (MOE_ENGINE_GROUPED or
+ * MOE_ENGINE_DECODE; AUTO means GROUPED): for pair r (token pair_token[r],
+ * bank slot pair_slot[r], both int32 device arrays of n_pairs entries),
+ * p1[r][n][q] = P1 for n < 2I, q < H/g.  pair_slot must be sorted
+ * ascending.  Workspace: moe_w4a8_workspace_size of the dims with T =
+ * n_pairs, top_k = 1, E = E + S, n_shared = 0.
  */
 int moe_w4a8_gemm1_partials(const int8_t* x_q, const uint8_t* w13_packed, const moe_dims_t* d,
                             const int32_t* pair_token, const int32_t* pair_slot, int64_t n_pairs,
-                            int32_t* p1, void* workspace, size_t workspace_bytes, void* stream);
+                            int32_t* p1, int engine, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Int32 partial sums of the down projection for given int8 rows: for pair
  * r with activation row h_q[r][:] (int8 [n_pairs][I]) and bank slot
- * pair_slot[r] (sorted ascending), p2[r][n][q] = P2 for n < H, q < I/g.
+ * pair_slot[r] (sorted ascending), p2[r][n][q] = P2 for n < H, q < I/g,
+ * through the chosen engine's main loop (as for moe_w4a8_gemm1_partials).
  */
 int moe_w4a8_gemm2_partials(const int8_t* h_q, const uint8_t* w2_packed, const moe_dims_t* d,
                             const int32_t* pair_slot, int64_t n_pairs,
-                            int32_t* p2, void* workspace, size_t workspace_bytes, void* stream);
+                            int32_t* p2, int engine, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Device-side status of the last call that used `workspace`: synchronises
+ * `stream`, then reads the status word the kernels keep at the start of the
+ * workspace.  MOE_OK, or MOE_ERR_DEVICE_TIMEOUT if one of the engine's
+ * bounded waits (the decode engine's grid barrier or its bulk-copy wait,
+ * about one second each) ran out -- the kernels then skip the rest of the
+ * work and the output is not valid.  A diagnostic call (it blocks the host);
+ * not for the hot loop.
+ */
+int moe_w4a8_device_status(const void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Self-test of the bounded device waits: enqueues a two-CTA kernel in
+ * which one CTA waits at the decode engine's grid barrier for a CTA that
+ * never arrives.  The wait gives up after its limit (about a second) and
+ * records the timeout in the workspace status word, so a following
+ * moe_w4a8_device_status returns MOE_ERR_DEVICE_TIMEOUT; nothing faults and
+ * the context stays usable.  workspace: at least 256 bytes, 256-aligned.
+ */
+int moe_w4a8_selftest_barrier_timeout(void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Bytes of the library's built-in scratch array used by

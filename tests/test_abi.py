@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     names = _declared_symbols()
     assert {"moe_w4a8_forward", "moe_w4a8_route", "moe_w4a8_workspace_size", "moe_w4a8_version",
             "moe_w4a8_status_string", "moe_w4a8_gemm1_partials", "moe_w4a8_gemm2_partials",
-            "moe_w4a8_forward_debug"} <= names
+            "moe_w4a8_forward_debug", "moe_w4a8_device_status"} <= names
 
 
 def test_library_exports_every_declared_symbol(cuda_lib, lib):
@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(cuda_lib, lib):
 
 def test_version_and_status_strings(lib):
     from bit_moe_expert_router_gb300 import binding
-    assert lib.moe_w4a8_version() == binding.ABI_VERSION == 1
+    assert lib.moe_w4a8_version() == binding.ABI_VERSION == 2
     for s in range(6):
         assert binding.moe_w4a8_status_string(s)
     assert binding.moe_w4a8_status_string(99) == "unknown status"
@@ -109,3 +109,18 @@ def test_empty_batch_is_a_no_op(lib):
     # T = 0: valid, nothing enqueued, activations may be null
     assert lib.moe_w4a8_forward(None, None, None, fake, fake, fake, fake, ctypes.byref(d), None, None, 0, None) == 0
     assert lib.moe_w4a8_route(None, ctypes.byref(d), None, None, None, None, None, None, None, 0, None) == 0
+
+
+def test_engine_and_status_arguments_are_checked(lib):
+    from bit_moe_expert_router_gb300 import binding
+    d = binding.dims_of(4, 2048, 512, 512, 1, 10, 128)
+    fake = ctypes.c_void_p(0x100000)
+    need = lib.moe_w4a8_workspace_size(ctypes.byref(d))
+    # an engine outside {-1, 0, 1} is rejected before anything is enqueued
+    assert lib.moe_w4a8_forward_debug(*[fake] * 7, ctypes.byref(d), fake, None, None, None, 7, fake, need, None) == 1
+    assert lib.moe_w4a8_gemm1_partials(fake, fake, ctypes.byref(d), fake, fake, 3, fake, 2, fake, need, None) == 1
+    assert lib.moe_w4a8_gemm2_partials(fake, fake, ctypes.byref(d), fake, 3, fake, -2, fake, need, None) == 1
+    # the status query needs an aligned workspace of at least the header
+    assert lib.moe_w4a8_device_status(None, 1024, None) == 1
+    assert lib.moe_w4a8_device_status(ctypes.c_void_p(0x100010), 1024, None) == 1
+    assert lib.moe_w4a8_device_status(fake, 16, None) == 1

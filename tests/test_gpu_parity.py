@@ -102,9 +102,18 @@ def _sample_pairs(w, tok, n, seed=0):
     return slots, tokens
 
 
-@pytest.mark.parametrize("name", ALL)
-def test_gemm1_partials_bit_exact(name):
-    w = synth.WORKLOADS[name]
+# engine 0 = grouped tensor-core engine (any size), 1 = fused decode engine (T <= 32)
+PARTIALS_CASES = [(n, 0) for n in ALL] + [("decode_t4", 1), ("decode_verify_t12", 1), ("dec_small", 1)]
+DEC_SMALL = synth.Workload("dec_small", T=8, H=1024, I=512, E=16, S=1, top_k=4, group=128)
+
+
+def _workload(name):
+    return DEC_SMALL if name == "dec_small" else synth.WORKLOADS[name]
+
+
+@pytest.mark.parametrize("name,engine", PARTIALS_CASES)
+def test_gemm1_partials_bit_exact(name, engine):
+    w = _workload(name)
     tok = synth.make_tokens(w)
     bank = gh.bank_of(w)
     w13, _, _, _ = gh.device_bank(w)
@@ -113,7 +122,7 @@ def test_gemm1_partials_bit_exact(name):
     n = slots.shape[0]
     p1 = torch.empty((n, 2 * w.I, w.H // w.group), dtype=torch.int32, device="cuda:0")
     ws = binding.alloc_workspace(binding.partials_workspace_size(d, n), "cuda:0")
-    binding.moe_w4a8_gemm1_partials(gh.to_dev(tok.x_q), w13, d, gh.to_dev(tokens), gh.to_dev(slots), p1, ws)
+    binding.moe_w4a8_gemm1_partials(gh.to_dev(tok.x_q), w13, d, gh.to_dev(tokens), gh.to_dev(slots), p1, ws, engine)
     torch.cuda.synchronize()
     got = p1.cpu().numpy()
     for r in range(n):
@@ -121,9 +130,9 @@ def test_gemm1_partials_bit_exact(name):
         assert np.array_equal(got[r], ref), f"pair {r}: token {tokens[r]} slot {slots[r]}"
 
 
-@pytest.mark.parametrize("name", ALL)
-def test_gemm2_partials_bit_exact(name):
-    w = synth.WORKLOADS[name]
+@pytest.mark.parametrize("name,engine", PARTIALS_CASES)
+def test_gemm2_partials_bit_exact(name, engine):
+    w = _workload(name)
     tok = synth.make_tokens(w)
     bank = gh.bank_of(w)
     _, _, w2, _ = gh.device_bank(w)
@@ -137,7 +146,7 @@ def test_gemm2_partials_bit_exact(name):
     d = gh.dims(w)
     p2 = torch.empty((n, w.H, w.I // w.group), dtype=torch.int32, device="cuda:0")
     ws = binding.alloc_workspace(binding.partials_workspace_size(d, n), "cuda:0")
-    binding.moe_w4a8_gemm2_partials(gh.to_dev(h_q), w2, d, gh.to_dev(slots), p2, ws)
+    binding.moe_w4a8_gemm2_partials(gh.to_dev(h_q), w2, d, gh.to_dev(slots), p2, ws, engine)
     torch.cuda.synchronize()
     got = p2.cpu().numpy()
     for r in range(n):
@@ -159,9 +168,10 @@ def test_forward_matches_oracle(name):
     assert np.array_equal(out, again), "two runs differ"
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode_t4", "decode_verify_t12"])
-def test_requantised_intermediate(name):
-    w = synth.WORKLOADS[name]
+@pytest.mark.parametrize("name,engine", [("tiny", -1), ("decode_t4", 0), ("decode_t4", 1),
+                                         ("decode_verify_t12", 0), ("decode_verify_t12", 1), ("dec_small", 1)])
+def test_requantised_intermediate(name, engine):
+    w = _workload(name)
     tok = synth.make_tokens(w)
     bank = gh.bank_of(w)
     w13, s13, w2, s2 = gh.device_bank(w)
@@ -173,8 +183,11 @@ def test_requantised_intermediate(name):
     y = torch.empty((P, w.H), dtype=torch.float32, device="cuda:0")
     ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), "cuda:0")
     binding.moe_w4a8_forward_debug(gh.to_dev(tok.x_q), gh.to_dev(tok.x_scale), gh.to_dev(tok.logits), w13, s13, w2,
-                                   s2, d, out, ws, h_q, s_h, y)
+                                   s2, d, out, ws, h_q, s_h, y, engine=engine)
     torch.cuda.synchronize()
+    assert binding.moe_w4a8_device_status(ws) == 0
+    ref_out = gh.oracle_out(w, tok, bank)
+    gh.assert_output_close(out.cpu().numpy(), ref_out, f"{name} engine {engine}")
     h_q, s_h, y = h_q.cpu().numpy(), s_h.cpu().numpy(), y.cpu().numpy()
     ids, _ = oracle.route(tok.logits, w.top_k)
     _, _, _, inv = oracle.permute(ids, w.E)
@@ -259,3 +272,75 @@ def test_empty_batch_leaves_output_untouched():
     ws = binding.alloc_workspace(256, "cuda:0")
     binding.moe_w4a8_forward(e(0, w.H, dt=torch.int8), e(0), e(0, w.E), w13, s13, w2, s2, d, out, ws)
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ fused decode engine
+
+def _forward_engine(w, tok, engine, bank_dev=None):
+    w13, s13, w2, s2 = bank_dev if bank_dev is not None else gh.device_bank(w)
+    d = gh.dims(w)
+    out = torch.full((w.T, w.H), float("nan"), dtype=torch.float32, device="cuda:0")
+    ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), "cuda:0")
+    binding.moe_w4a8_forward_debug(gh.to_dev(tok.x_q), gh.to_dev(tok.x_scale), gh.to_dev(tok.logits), w13, s13, w2,
+                                   s2, d, out, ws, engine=engine)
+    torch.cuda.synchronize()
+    assert binding.moe_w4a8_device_status(ws) == 0
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 17, 32])
+def test_decode_engine_ragged_batches(T):
+    w = DEC_SMALL.with_tokens(T)
+    tok = synth.make_tokens(w)
+    out = _forward_engine(w, tok, 1)
+    gh.assert_output_close(out, gh.oracle_out(w, tok, gh.bank_of(w)), f"decode T={T}")
+
+
+@pytest.mark.parametrize("k,S", [(1, 0), (16, 1), (4, 0), (4, 2)])
+def test_decode_engine_top_k_and_shared(k, S):
+    w = synth.Workload("dk", T=9, H=1024, I=512, E=16, S=S, top_k=k, group=64)
+    tok = synth.make_tokens(w)
+    out = _forward_engine(w, tok, 1)
+    gh.assert_output_close(out, gh.oracle_out(w, tok, gh.bank_of(w)), f"decode k={k} S={S}")
+
+
+def test_decode_engine_matches_grouped_engine_on_large_bank_shape():
+    w = synth.WORKLOADS["large_bank_t2048"].with_tokens(6)
+    tok = synth.make_tokens(w)
+    a = _forward_engine(w, tok, 1)
+    b = _forward_engine(w, tok, 0)
+    ref = gh.oracle_out(w, tok, gh.bank_of(w))
+    gh.assert_output_close(a, ref, "decode engine, large bank")
+    gh.assert_output_close(b, ref, "grouped engine, large bank")
+
+
+def test_decode_engine_is_deterministic_and_auto_selected():
+    w = synth.WORKLOADS["decode_t4"]
+    tok = synth.make_tokens(w, batch=3)
+    a = _forward_engine(w, tok, 1)
+    b = _forward_engine(w, tok, -1)
+    assert np.array_equal(a, b)
+
+
+def test_decode_engine_rejects_batches_beyond_its_limits():
+    w = DEC_SMALL.with_tokens(33)
+    tok = synth.make_tokens(w)
+    with pytest.raises(binding.MoeError) as e:
+        _forward_engine(w, tok, 1)
+    assert e.value.status == 2
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    w = synth.WORKLOADS["decode_t4"]
+    d = gh.dims(w)
+    ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), "cuda:0")
+    binding.moe_w4a8_selftest_barrier_timeout(ws)
+    assert binding.moe_w4a8_device_status(ws) == 5
+    # the same workspace and context serve a normal call afterwards
+    tok = synth.make_tokens(w)
+    w13, s13, w2, s2 = gh.device_bank(w)
+    out = torch.empty((w.T, w.H), dtype=torch.float32, device="cuda:0")
+    binding.moe_w4a8_forward(gh.to_dev(tok.x_q), gh.to_dev(tok.x_scale), gh.to_dev(tok.logits), w13, s13, w2, s2, d,
+                             out, ws)
+    assert binding.moe_w4a8_device_status(ws) == 0
+    gh.assert_output_close(out.cpu().numpy(), gh.oracle_out(w, tok, gh.bank_of(w)), "after timeout")
