@@ -4,53 +4,58 @@
 // packed weights ("Two 96 GB Ascend cards run Qwen3.8 Flash-Next", section 3:
 // keep the W4 bank packed and do the work on the device; section 5: no host
 // round trips inside the token loop, fused operators for decode steps made of
-// many small launches).  One launch does everything, streaming each touched
-// expert's bytes from HBM exactly once:
+// many small launches).  One launch does everything and streams each touched
+// expert's bytes from HBM once:
 //
-//   phase 0  every CTA routes all T tokens itself (same deterministic result
-//            in every CTA, so no exchange is needed), sorts the pairs stably
-//            by expert into pair rows, builds the slot table (touched experts
-//            in ascending order, then the shared experts), stages the
-//            activations in shared memory, and starts TMA bulk copies of its
-//            own slice of the down-projection bank (its output rows, every
-//            touched slot) into shared memory (L2 prefetch for what does not
-//            fit).
-//   phase 1  gate/up projection: the (slot, intermediate index) units are split
-//            evenly over all warps of the grid; a warp streams the unit's gate
-//            row and up row (16-byte loads, round-robin over lanes), unpacks the
-//            nibbles in registers and accumulates with dp4a; each K group's
-//            exact int32 partial is folded into fp32 with its scale, then
+//   phase 0  every CTA routes all T tokens itself (the same deterministic
+//            result in every CTA, so nothing is exchanged), sorts the pairs
+//            stably by expert into pair rows, builds the slot table (touched
+//            experts ascending, then the shared experts), stages the
+//            activations in shared memory and prefetches its own slice of
+//            the down-projection bank (its output rows of every touched
+//            slot) into L2 so that phase 2 reads it from there.
+//   phase 1  gate/up projection with dp4a on the CUDA cores: units of two
+//            intermediate indices (2 gate rows + the 2 matching up rows) of
+//            one slot; the units are split into contiguous ranges of equal
+//            cost over all warps (cost = streaming + per-token work, so the
+//            always-on shared expert's multi-token units weigh more).  A warp
+//            keeps up to four units of 16-byte loads in flight in
+//            registers; each lane covers a 64-value K piece, folds its exact
+//            int32 piece sum with the piece's group scale, and a 4-row
+//            reduce-scatter across the warp (6 shuffles) gives the row sums;
 //            h = SiLU(G_gate) * G_up goes to the workspace.
-//   barrier  one grid-wide barrier (bounded wait; on timeout the status word
-//            records it and the CTAs leave after their copies have landed).
+//   barrier  one grid-wide barrier (bounded wait; on timeout the status
+//            word records it and the CTAs leave).
 //   phase 2  every CTA requantises all pair rows (row max -> s_h, RNE codes)
-//            into shared memory, runs the down projection for its output rows
-//            of every touched slot from the staged slice (half-warp per weight
-//            row), and combines out[t][n] = sum_j w[t][j] Y[(t,j)][n] + shared
-//            in a fixed order -- no atomics, deterministic.
+//            into shared memory, runs the down projection for its output
+//            rows of every touched slot (units of 8 rows, 16-value K piece
+//            per lane, 8-row reduce-scatter), and combines
+//            out[t][n] = sum_j w[t][j] Y[(t,j)][n] + shared in a fixed order:
+//            no atomics, deterministic.
 //
-// The same kernel also serves the partials entry points (phase 1 or phase 2
-// alone, pairs given as a list instead of routed) so the bit-exact int32
-// checks run through this engine's integer core.
+// The same kernel serves the partials entry points (phase 1 or phase 2
+// alone, pairs given as a list instead of routed); there each K group's
+// int32 partial is summed in integers over the lanes of the group, so the
+// bit-exact checks run through this engine's integer core.
 //
-// Nibble unpack as in the grouped engine: a nibble moved into the high half
-// of its byte is an int8 lane holding 16 * code; dp4a gives 16 * P exactly.
-// Activations are stored in shared memory with each 8-byte group split into
-// its even and odd elements, matching the unpack's even/odd output words.
+// Unpack: a nibble moved into the high half of its byte is an int8 lane
+// holding 16 * code (unpack_int4x8_x16), so dp4a sums are 16x and exact;
+// the unpack yields even and odd elements, and the activations are stored
+// with every 8-byte group split into its even and odd elements to match.
 #include <math.h>
 
 #include <algorithm>
 #include <map>
 #include <mutex>
-#include <tuple>
 
 #include "decode.h"
 
 namespace moe {
 namespace {
 
-constexpr int kThreadsD = 512;
+constexpr int kThreadsD = 256;
 constexpr int kWarpsD = kThreadsD / 32;
+
 // Bounded waits: give up after about one second of wall-clock time (the
 // global timer), with an iteration cap as a second bound.
 constexpr uint64_t kWaitNs = 1000000000ull;
@@ -70,43 +75,13 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
     return v;
 }
 
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+__device__ __forceinline__ uint2 ld_nc8(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
 }
 
-// Bounded wait for the TMA transactions of phase `parity`; false on timeout.
-__device__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    const uint64_t t0 = global_ns();
-    for (uint32_t it = 0; it < kSpinCap; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitNs) break;
-        __nanosleep(128);
-    }
-    return false;
-}
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p)); }
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
     uint32_t v;
@@ -148,31 +123,34 @@ __device__ bool grid_barrier(Header* hdr, uint32_t k) {
 // (v, e) beats (bv, be): larger value, or equal value and lower index.
 __device__ __forceinline__ bool beats(float v, int e, float bv, int be) { return v > bv || (v == bv && e < be); }
 
-// One warp routes token t: ids/w of its k selected experts into shared memory.
-__device__ void route_token_warp(const float* __restrict__ l, int E, int k, int* ids, float* wts) {
+// Top-k of one warp's share of a token's candidates, largest first (ties to
+// the lower expert index).  Lane `lane` holds candidates j = 0..NJ-1 (value
+// v[j], expert id id[j], -inf/INT_MAX when absent) and keeps its own best
+// remaining candidate, so each round is one warp argmax plus a rescan by
+// the winning lane only.  Selected (value, id) pairs land in out_v/out_e
+// (lane s holds the s-th).
+template <int NJ>
+__device__ __forceinline__ void warp_topk(const float (&v)[NJ], const int (&id)[NJ], int k, float& out_v, int& out_e) {
     const int lane = threadIdx.x & 31;
-    float v[kMaxExperts / 32];
     uint32_t taken = 0;
-    const int nj = (E + 31) / 32;
+    auto local_best = [&](float& bv, int& be) {
+        bv = -INFINITY;
+        be = INT32_MAX;
 #pragma unroll
-    for (int j = 0; j < kMaxExperts / 32; ++j) {
-        const int e = lane + 32 * j;
-        v[j] = (j < nj && e < E) ? __ldg(l + e) : -INFINITY;
-        if (!(j < nj && e < E)) taken |= 1u << j;
-    }
-    float my_v = 0.f;
-    int my_e = 0;
-    for (int s = 0; s < k; ++s) {
-        float bv = -INFINITY;
-        int be = INT32_MAX;
-#pragma unroll
-        for (int j = 0; j < kMaxExperts / 32; ++j) {
-            const int e = lane + 32 * j;
-            if (!(taken >> j & 1u) && beats(v[j], e, bv, be)) {
+        for (int j = 0; j < NJ; ++j)
+            if (!(taken >> j & 1u) && beats(v[j], id[j], bv, be)) {
                 bv = v[j];
-                be = e;
+                be = id[j];
             }
-        }
+    };
+    float lv;
+    int le;
+    local_best(lv, le);
+    out_v = -INFINITY;
+    out_e = INT32_MAX;
+    for (int s = 0; s < k; ++s) {
+        float bv = lv;
+        int be = le;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
@@ -182,80 +160,139 @@ __device__ void route_token_warp(const float* __restrict__ l, int E, int k, int*
                 be = oe;
             }
         }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        if (lane == s) {
-            my_v = bv;
-            my_e = be;
-        }
-    }
-    const float m = __shfl_sync(0xffffffffu, my_v, 0);
-    const float ex = lane < k ? expf(my_v - m) : 0.0f;
-    float sum = ex;
+        if (le == be && be != INT32_MAX) {  // this lane held the winner: drop it, rescan
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (lane < k) {
-        ids[lane] = my_e;
-        wts[lane] = ex / sum;
+            for (int j = 0; j < NJ; ++j)
+                if (id[j] == be) taken |= 1u << j;
+            local_best(lv, le);
+        }
+        if (lane == s) {
+            out_v = bv;
+            out_e = be;
+        }
     }
 }
 
-// Eight int8 values -> (even elements word, odd elements word).
-__device__ __forceinline__ uint2 split_even_odd(uint32_t w0, uint32_t w1) {
-    uint2 r;
-    r.x = __byte_perm(w0, w1, 0x6420);
-    r.y = __byte_perm(w0, w1, 0x7531);
+// Routing of all T tokens by the CTA's warps: each token's experts are
+// split over `wpt` warps (interleaved), each finds the top-k of its share,
+// and one warp per token merges the wpt * k candidates.  The result equals
+// the top-k over all experts (every global top-k expert is in its share's
+// top-k).  ids/wts: [T][k]; cand_v/cand_e: [T][wpt][k] scratch.
+__device__ void route_all(const float* __restrict__ logits, int T, int E, int k, int* ids, float* wts, float* cand_v,
+                          int* cand_e) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int wpt = 1;
+    while (wpt * 2 * T <= nw && wpt < 8 && 32 * wpt * 2 <= E) wpt *= 2;
+    constexpr int NJ = kMaxExperts / 32;
+    for (int job = warp; job < T * wpt; job += nw) {
+        const int t = job / wpt, sub = job % wpt;
+        float v[NJ];
+        int id[NJ];
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const int e = sub * 32 + lane + 32 * wpt * j;
+            const bool in = e < E;
+            v[j] = in ? __ldg(logits + static_cast<int64_t>(t) * E + e) : -INFINITY;
+            id[j] = in ? e : INT32_MAX;
+        }
+        float ov;
+        int oe;
+        warp_topk<NJ>(v, id, k, ov, oe);
+        if (lane < k) {
+            cand_v[(t * wpt + sub) * k + lane] = ov;
+            cand_e[(t * wpt + sub) * k + lane] = oe;
+        }
+    }
+    __syncthreads();
+    for (int t = warp; t < T; t += nw) {
+        constexpr int NM = 8;  // wpt * k <= 8 * 32 candidates, 8 per lane
+        float v[NM];
+        int id[NM];
+#pragma unroll
+        for (int j = 0; j < NM; ++j) {
+            const int c = lane + 32 * j;
+            const bool in = c < wpt * k;
+            v[j] = in ? cand_v[t * wpt * k + c] : -INFINITY;
+            id[j] = in ? cand_e[t * wpt * k + c] : INT32_MAX;
+        }
+        float my_v;
+        int my_e;
+        warp_topk<NM>(v, id, k, my_v, my_e);
+        // softmax over the selected logits, relative to the largest (selected first)
+        const float m = __shfl_sync(0xffffffffu, my_v, 0);
+        const float ex = lane < k ? expf(my_v - m) : 0.0f;
+        float sum = ex;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (lane < k) {
+            ids[t * k + lane] = my_e;
+            wts[t * k + lane] = ex / sum;
+        }
+    }
+}
+
+// 16 int8 -> the same 16 bytes with each 8-byte group split into its even
+// elements (first word) and odd elements (second word).
+__device__ __forceinline__ uint4 split16(uint4 v) {
+    uint4 r;
+    r.x = __byte_perm(v.x, v.y, 0x6420);
+    r.y = __byte_perm(v.x, v.y, 0x7531);
+    r.z = __byte_perm(v.z, v.w, 0x6420);
+    r.w = __byte_perm(v.z, v.w, 0x7531);
     return r;
 }
 
-// 16 int8 (uint4) -> same 16 bytes with each 8-byte group split even|odd.
-__device__ __forceinline__ uint4 split16(uint4 v) {
-    const uint2 a = split_even_odd(v.x, v.y), b = split_even_odd(v.z, v.w);
-    return make_uint4(a.x, a.y, b.x, b.y);
+// 16 * (dot of 8 packed codes `w` with the 8 split activation bytes xe|xo) + acc.
+__device__ __forceinline__ int dot8(uint32_t w, uint32_t xe, uint32_t xo, int acc) {
+    uint32_t e, o;
+    unpack_int4x8_x16(w, e, o);
+    acc = __dp4a(static_cast<int>(xe), static_cast<int>(e), acc);
+    return __dp4a(static_cast<int>(xo), static_cast<int>(o), acc);
 }
 
-// dp4a over one packed 16-byte weight chunk (32 codes) against 32 activation
-// bytes stored split (xa: codes 0..15, xb: codes 16..31).
-__device__ __forceinline__ int dot_chunk(const uint4 w, const uint4 xa, const uint4 xb, int acc) {
-    uint32_t e, o;
-    unpack_int4x8_x16(w.x, e, o);
-    acc = __dp4a(static_cast<int>(xa.x), static_cast<int>(e), acc);
-    acc = __dp4a(static_cast<int>(xa.y), static_cast<int>(o), acc);
-    unpack_int4x8_x16(w.y, e, o);
-    acc = __dp4a(static_cast<int>(xa.z), static_cast<int>(e), acc);
-    acc = __dp4a(static_cast<int>(xa.w), static_cast<int>(o), acc);
-    unpack_int4x8_x16(w.z, e, o);
-    acc = __dp4a(static_cast<int>(xb.x), static_cast<int>(e), acc);
-    acc = __dp4a(static_cast<int>(xb.y), static_cast<int>(o), acc);
-    unpack_int4x8_x16(w.w, e, o);
-    acc = __dp4a(static_cast<int>(xb.z), static_cast<int>(e), acc);
-    acc = __dp4a(static_cast<int>(xb.w), static_cast<int>(o), acc);
-    return acc;
+// 16 * dot of 32 packed codes (uint4) with 32 split activation bytes (two uint4).
+__device__ __forceinline__ int dot32(const uint4& w, const uint4& xa, const uint4& xb) {
+    int acc = dot8(w.x, xa.x, xa.y, 0);
+    acc = dot8(w.y, xa.z, xa.w, acc);
+    acc = dot8(w.z, xb.x, xb.y, acc);
+    return dot8(w.w, xb.z, xb.w, acc);
+}
+
+// Requantisation code of h with scale s and reciprocal rs: RNE(h / s) in
+// IEEE fp32.  h * rs is within 2^-23 relative of h / s (|h / s| <= 127),
+// so it rounds to the same integer unless it lies within 1e-4 of a
+// half-integer; only then is the exact division computed.
+__device__ __forceinline__ int requant_code_fast(float h, float s, float rs) {
+    if (!(s > 0.0f)) return 0;
+    const float f = h * rs;
+    const float d = fabsf(f - floorf(f) - 0.5f);
+    float q = d < 1e-4f ? rintf(__fdiv_rn(h, s)) : rintf(f);
+    q = fminf(fmaxf(q, -127.0f), 127.0f);
+    return static_cast<int>(q);
 }
 
 struct Smem {
-    uint64_t* bar;
-    int* flags;       // [0] abort
-    int* ids;         // [T*k]
-    float* wts;       // [T*k]
-    int* pos;         // [T*k] pair -> row
-    int* pair_of;     // [T*k] row -> pair
+    int* ids;         // [rows]
+    float* wts;       // [rows]
+    int* pos;         // [rows] pair -> row
+    int* pair_of;     // [rows] row -> pair
     int* row_tok;     // [P]
     int* slot_e;      // [MS]
     int* slot_row0;   // [MS]
     int* slot_cnt;    // [MS]
+    int* slot_cum;    // [MS + 1] phase-1 cost prefix
     int* n_slots;     // [1]
     float* xs;        // [T]
     float* sh;        // [P]
-    uint8_t* x;       // [T*H] phase-1 layout
-    uint8_t* hq;      // [P*I] phase-2 layout
-    float* y;         // [P*rows_pc]
-    uint8_t* w2s;     // [smem_slots][slot_bytes]
+    uint8_t* x;       // [T][H + 16] split layout
+    uint8_t* hq;      // [P][I + 16] split layout
+    float* y;         // [P][rows_pc]
+    float* cand_v;    // [T][8][k] routing candidates
+    int* cand_e;      // [T][8][k]
 };
 
 __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
     Smem s;
-    s.bar = reinterpret_cast<uint64_t*>(base + pl.off_bar);
-    s.flags = reinterpret_cast<int*>(base + pl.off_flags);
     s.ids = reinterpret_cast<int*>(base + pl.off_ids);
     s.wts = reinterpret_cast<float*>(base + pl.off_wts);
     s.pos = reinterpret_cast<int*>(base + pl.off_pos);
@@ -264,41 +301,50 @@ __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
     s.slot_e = reinterpret_cast<int*>(base + pl.off_slot_e);
     s.slot_row0 = reinterpret_cast<int*>(base + pl.off_slot_row0);
     s.slot_cnt = reinterpret_cast<int*>(base + pl.off_slot_cnt);
+    s.slot_cum = reinterpret_cast<int*>(base + pl.off_slot_cum);
     s.n_slots = reinterpret_cast<int*>(base + pl.off_n_slots);
     s.xs = reinterpret_cast<float*>(base + pl.off_xs);
     s.sh = reinterpret_cast<float*>(base + pl.off_sh);
     s.x = base + pl.off_x;
     s.hq = base + pl.off_hq;
     s.y = reinterpret_cast<float*>(base + pl.off_y);
-    s.w2s = base + pl.off_w2s;
+    s.cand_v = reinterpret_cast<float*>(base + pl.off_cand_v);
+    s.cand_e = reinterpret_cast<int*>(base + pl.off_cand_e);
     return s;
 }
 
-template <DecodeMode MODE, int C1, int C2>
+// Phase-1 cost of one unit of a slot with `cnt` tokens (streaming + per-token work).
+__device__ __forceinline__ int unit_cost(int cnt) { return 4 + cnt; }
+
+// PC1 = H / 2048 (64-value pieces per lane per row), PC2 = I / 512 (16-value pieces per lane per row).
+template <DecodeMode MODE, int PC1, int PC2>
 __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, DecodePlan pl) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const Smem s = carve(smem_raw, pl);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = a.T, H = a.H, I = a.I, k = a.k, g = a.g;
-    const int lpg1 = g / 32;                 // lanes per K group (one 16-byte chunk = 32 codes per lane)
-    // C1 = H / 1024: phase-1 chunks per lane per row; C2 = I / 512: phase-2 chunks per lane per row
     const int ng1 = H / g, ng2 = I / g;
+    const int XS = H + 16, HQS = I + 16;
     const bool routed = MODE == DecodeMode::kForward;
 
     // ---------------------------------------------------------------- phase 0
-    if (tid == 0) {
-        s.flags[0] = 0;
-        if (MODE == DecodeMode::kForward) mbar_init(s.bar, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
     int n_rows;  // routed/listed pair rows before the shared rows
     if (routed) {
-        for (int t = warp; t < T; t += kWarpsD)
-            route_token_warp(a.logits + static_cast<int64_t>(t) * a.E, a.E, k, s.ids + t * k, s.wts + t * k);
+        route_all(a.logits, T, a.E, k, s.ids, s.wts, s.cand_v, s.cand_e);
         n_rows = T * k;
     } else {
         n_rows = a.n_pairs;  // listed pairs; out-of-range slots and tokens are clamped (never read out of bounds)
         for (int r = tid; r < n_rows; r += kThreadsD) s.ids[r] = min(max(a.pair_slot[r], 0), a.E - 1);
+    }
+    // activations: [t][H + 16], each 8-byte group split even|odd (independent of routing)
+    if (MODE != DecodeMode::kGemm2Partials) {
+        const int per_tok = H / 16;
+        for (int o = tid; o < T * per_tok; o += kThreadsD) {
+            const int t = o / per_tok, c = o % per_tok;
+            const uint4 v = *reinterpret_cast<const uint4*>(a.x_q + static_cast<int64_t>(t) * H + 16 * c);
+            *reinterpret_cast<uint4*>(s.x + t * XS + 16 * c) = split16(v);
+        }
+        for (int t = tid; t < T; t += kThreadsD) s.xs[t] = routed ? a.x_scale[t] : 1.0f;
     }
     __syncthreads();
     // stable rank of each pair by expert id (n_rows <= kDecodeMaxPairs)
@@ -311,7 +357,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         }
         s.pos[i] = p;
         s.pair_of[p] = i;
-        s.row_tok[p] = routed ? i / k : (MODE == DecodeMode::kGemm1Partials ? min(max(a.pair_token[i], 0), T - 1) : 0);
+        s.row_tok[p] = routed ? i / k : (MODE == DecodeMode::kGemm1Partials ? min(max(a.pair_token[i], 0), T - 1) : p);
     }
     const int S = routed ? a.S : 0;
     for (int r = tid; r < T * S; r += kThreadsD) s.row_tok[n_rows + r] = r % T;
@@ -341,289 +387,292 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         const int end = u + 1 < n_routed_slots ? s.slot_row0[u + 1] : (u < n_routed_slots ? n_rows : T);
         s.slot_cnt[u] = u < n_routed_slots ? end - s.slot_row0[u] : T;
     }
-    // activations in the phase-1 layout: [t][chunk j][half][lane][16 B], each 8-byte group split even|odd
-    if (MODE != DecodeMode::kGemm2Partials) {
-        const int per_tok = H / 16;
-        for (int o = tid; o < T * per_tok; o += kThreadsD) {
-            const int t = o / per_tok, c = o % per_tok;
-            const int j = c / 64, half = (c / 32) % 2, l = c % 32;
-            const int k0 = 32 * (32 * j + l) + 16 * half;
-            const uint4 v = *reinterpret_cast<const uint4*>(a.x_q + static_cast<int64_t>(t) * H + k0);
-            *reinterpret_cast<uint4*>(s.x + static_cast<int64_t>(t) * H + c * 16) = split16(v);
-        }
-        for (int t = tid; t < T; t += kThreadsD) s.xs[t] = routed ? a.x_scale[t] : 1.0f;
-    }
     __syncthreads();
+    if (tid == 0) {  // phase-1 cost prefix over slots (n_slots <= a few hundred)
+        int c = 0;
+        for (int u = 0; u < n_slots; ++u) {
+            s.slot_cum[u] = c;
+            c += (I / 2) * unit_cost(s.slot_cnt[u]);
+        }
+        s.slot_cum[n_slots] = c;
+    }
 
-    // phase-2 slice of this CTA and its staging
+    // this CTA's down-projection slice: rows [n0, n0 + nrows) of every slot.  Its
+    // 128-byte lines are prefetched into L2 during phase 1, a few per unit, so
+    // the requests queue behind the phase-1 loads instead of stalling here.
     const int n0 = blockIdx.x * pl.rows_pc;
     const int nrows = max(0, min(pl.rows_pc, H - n0));
-    const int slot_w_bytes = pl.rows_pc * (I / 2), slot_s_bytes = pl.rows_pc * ng2 * 4;
-    const int n_smem = MODE == DecodeMode::kForward ? min(n_slots, pl.smem_slots) : 0;
-    if (MODE == DecodeMode::kForward && tid == 0) {
-        if (nrows > 0 && n_smem > 0) {
-            const uint32_t wb = nrows * (I / 2), sb = nrows * ng2 * 4;
-            mbar_arrive_expect_tx(s.bar, static_cast<uint32_t>(n_smem) * (wb + sb));
-            for (int u = 0; u < n_smem; ++u) {
-                const int64_t e = s.slot_e[u];
-                uint8_t* dst = s.w2s + static_cast<int64_t>(u) * (slot_w_bytes + slot_s_bytes);
-                bulk_g2s(dst, a.w2 + (e * H + n0) * (I / 2), wb, s.bar);
-                bulk_g2s(dst + slot_w_bytes, a.s2 + (e * H + n0) * ng2, sb, s.bar);
-            }
-        } else {
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(s.bar)) : "memory");
-        }
-        for (int u = n_smem; u < n_slots && nrows > 0; ++u) {
+    const int lines_w = (nrows * (I / 2) + 127) / 128, lines_s = (nrows * ng2 * 4 + 127) / 128;
+    const int n_lines = MODE == DecodeMode::kForward && nrows > 0 ? n_slots * (lines_w + lines_s) : 0;
+    int next_line = warp * 32 + lane;  // this thread's next line (stride kThreadsD)
+    auto prefetch_some = [&]() {
+        if (next_line < n_lines) {
+            const int u = next_line / (lines_w + lines_s), c = next_line % (lines_w + lines_s);
             const int64_t e = s.slot_e[u];
-            bulk_prefetch_l2(a.w2 + (e * H + n0) * (I / 2), nrows * (I / 2));
-            bulk_prefetch_l2(a.s2 + (e * H + n0) * ng2, nrows * ng2 * 4);
+            if (c < lines_w) prefetch_l2(a.w2 + (e * H + n0) * static_cast<int64_t>(I / 2) + 128 * c);
+            else prefetch_l2(reinterpret_cast<const uint8_t*>(a.s2 + (e * H + n0) * ng2) + 128 * (c - lines_w));
+            next_line += kThreadsD;
         }
-    }
+    };
+    __syncthreads();
 
     // ---------------------------------------------------------------- phase 1
     if (MODE != DecodeMode::kGemm2Partials) {
-        const int64_t N1 = static_cast<int64_t>(n_slots) * I;
+        constexpr int DEPTH = PC1 == 1 ? 4 : 2;  // units of loads in flight per warp
+        const int upe = I / 2;                    // units per slot
+        const int64_t Ctot = s.slot_cum[n_slots];
         const int64_t W = static_cast<int64_t>(gridDim.x) * kWarpsD;
         const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarpsD + warp;
-        const int64_t U0 = gw * N1 / W, U1 = (gw + 1) * N1 / W;
-        constexpr int kMaxC1 = C1;
-        uint4 wg[kMaxC1], wu[kMaxC1];
-        float sg[kMaxC1], su[kMaxC1];
-        auto load_unit = [&](int64_t U, uint4* g_, uint4* u_, float* sg_, float* su_) {
-            const int u = static_cast<int>(U / I), i = static_cast<int>(U % I);
-            const int64_t e = s.slot_e[u];
-            const uint8_t* rg = a.w13 + (e * 2 * I + i) * static_cast<int64_t>(H / 2);
-            const uint8_t* ru = rg + static_cast<int64_t>(I) * (H / 2);
-#pragma unroll
-            for (int j = 0; j < kMaxC1; ++j)
-                if (j < C1) {
-                    g_[j] = ld_stream16(rg + 16 * (32 * j + lane));
-                    u_[j] = ld_stream16(ru + 16 * (32 * j + lane));
-                    if (MODE == DecodeMode::kForward) {
-                        const int q = (32 * (32 * j + lane)) / g;
-                        sg_[j] = __ldg(a.s13 + (e * 2 * I + i) * ng1 + q);
-                        su_[j] = __ldg(a.s13 + (e * 2 * I + I + i) * ng1 + q);
-                    }
-                }
-        };
-        if (U0 < U1) load_unit(U0, wg, wu, sg, su);
-        for (int64_t U = U0; U < U1; ++U) {
-            uint4 cg[kMaxC1], cu[kMaxC1];
-            float csg[kMaxC1], csu[kMaxC1];
-#pragma unroll
-            for (int j = 0; j < kMaxC1; ++j) {
-                cg[j] = wg[j];
-                cu[j] = wu[j];
-                csg[j] = sg[j];
-                csu[j] = su[j];
+        // this warp's cost range -> unit range [Ua, Ub) over the flattened (slot, unit) space
+        auto unit_at = [&](int64_t cpos) -> int64_t {
+            int lo = 0, hi = n_slots;  // last slot with cum <= cpos
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) / 2;
+                if (s.slot_cum[mid] <= cpos) lo = mid;
+                else hi = mid;
             }
-            if (U + 1 < U1) load_unit(U + 1, wg, wu, sg, su);
-            const int u = static_cast<int>(U / I), i = static_cast<int>(U % I);
-            const int row0 = s.slot_row0[u], cnt = s.slot_cnt[u];
-            for (int m = 0; m < cnt; ++m) {
-                const int r = row0 + m;
-                const int t = s.row_tok[r];
-                int ag[kMaxC1], au[kMaxC1];
+            const int c = unit_cost(s.slot_cnt[lo]);
+            int64_t within = (cpos - s.slot_cum[lo] + c - 1) / c;
+            if (within > upe) within = upe;
+            return static_cast<int64_t>(lo) * upe + within;
+        };
+        const int64_t Ua = unit_at(gw * Ctot / W), Ub = unit_at((gw + 1) * Ctot / W);
+        const int nun = static_cast<int>(Ub - Ua);
+
+        uint4 wr[DEPTH][4][PC1][2];
+        float sr[DEPTH][4][PC1];
+        auto issue = [&](int un, int d) {
+            const int64_t U = Ua + un;
+            const int u = static_cast<int>(U / upe), ip = static_cast<int>(U % upe);
+            const int64_t e = s.slot_e[u];
 #pragma unroll
-                for (int j = 0; j < kMaxC1; ++j)
-                    if (j < C1) {
-                        const uint8_t* xp = s.x + static_cast<int64_t>(t) * H + j * 1024 + lane * 16;
-                        const uint4 xa = *reinterpret_cast<const uint4*>(xp);
-                        const uint4 xb = *reinterpret_cast<const uint4*>(xp + 512);
-                        ag[j] = dot_chunk(cg[j], xa, xb, 0);
-                        au[j] = dot_chunk(cu[j], xa, xb, 0);
+            for (int r = 0; r < 4; ++r) {
+                const int64_t row = e * 2 * I + (r >= 2 ? I : 0) + 2 * ip + (r & 1);
+                const uint8_t* wp = a.w13 + row * (H / 2);
+#pragma unroll
+                for (int j = 0; j < PC1; ++j) {
+                    wr[d][r][j][0] = ld_stream16(wp + 32 * (lane + 32 * j));
+                    wr[d][r][j][1] = ld_stream16(wp + 32 * (lane + 32 * j) + 16);
+                    if (MODE == DecodeMode::kForward) sr[d][r][j] = __ldg(a.s13 + row * ng1 + (64 * (lane + 32 * j)) / g);
+                }
+            }
+        };
+#pragma unroll
+        for (int d = 0; d < DEPTH; ++d)
+            if (d < nun) issue(d, d);
+        const int lpg = g / 64;  // lanes per K group
+        for (int base = 0; base < nun; base += DEPTH) {
+#pragma unroll
+            for (int d = 0; d < DEPTH; ++d) {
+                const int un = base + d;
+                if (un >= nun) break;
+                const uint4(&w)[4][PC1][2] = wr[d];
+                const float(&sc)[4][PC1] = sr[d];
+                const int64_t U = Ua + un;
+                const int u = static_cast<int>(U / upe), ip = static_cast<int>(U % upe);
+                const int row0 = s.slot_row0[u], cnt = s.slot_cnt[u];
+                for (int m = 0; m < cnt; ++m) {
+                    const int prow = row0 + m;
+                    const int t = s.row_tok[prow];
+                    int P[4][PC1];
+#pragma unroll
+                    for (int j = 0; j < PC1; ++j) {
+                        const uint8_t* xp = s.x + t * XS + 64 * (lane + 32 * j);
+                        const uint4 x0 = *reinterpret_cast<const uint4*>(xp);
+                        const uint4 x1 = *reinterpret_cast<const uint4*>(xp + 16);
+                        const uint4 x2 = *reinterpret_cast<const uint4*>(xp + 32);
+                        const uint4 x3 = *reinterpret_cast<const uint4*>(xp + 48);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            P[r][j] = dot32(w[r][j][0], x0, x1) + dot32(w[r][j][1], x2, x3);
                     }
-                // sum the lanes of each K group (consecutive lanes)
-                for (int off = 1; off < lpg1; off <<= 1)
+                    if (MODE == DecodeMode::kGemm1Partials) {
 #pragma unroll
-                    for (int j = 0; j < kMaxC1; ++j)
-                        if (j < C1) {
-                            ag[j] += __shfl_xor_sync(0xffffffffu, ag[j], off);
-                            au[j] += __shfl_xor_sync(0xffffffffu, au[j], off);
-                        }
-                const bool leader = (lane % lpg1) == 0;
-                if (MODE == DecodeMode::kGemm1Partials) {
-                    if (leader) {
-                        int32_t* dst = a.p1 + static_cast<int64_t>(r) * (2 * I) * ng1;
+                        for (int r = 0; r < 4; ++r)
 #pragma unroll
-                        for (int j = 0; j < kMaxC1; ++j)
-                            if (j < C1) {
-                                const int q = (32 * (32 * j + lane)) / g;
-                                dst[static_cast<int64_t>(i) * ng1 + q] = ag[j] >> 4;
-                                dst[static_cast<int64_t>(I + i) * ng1 + q] = au[j] >> 4;
+                            for (int j = 0; j < PC1; ++j) {
+                                int v = P[r][j];
+                                for (int off = 1; off < lpg; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                                if ((lane % lpg) == 0) {
+                                    const int64_t wrow = (r >= 2 ? I : 0) + 2 * ip + (r & 1);
+                                    a.p1[(static_cast<int64_t>(prow) * 2 * I + wrow) * ng1 + (64 * (lane + 32 * j)) / g] =
+                                        v >> 4;
+                                }
                             }
+                        continue;
                     }
-                    continue;
-                }
-                float vg = 0.f, vu = 0.f;
-                if (leader) {
+                    float v[4];
 #pragma unroll
-                    for (int j = 0; j < kMaxC1; ++j)
-                        if (j < C1) {
-                            vg = fmaf(static_cast<float>(ag[j] >> 4), csg[j], vg);
-                            vu = fmaf(static_cast<float>(au[j] >> 4), csu[j], vu);
-                        }
-                }
+                    for (int r = 0; r < 4; ++r) {
+                        v[r] = 0.f;
 #pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    vg += __shfl_xor_sync(0xffffffffu, vg, off);
-                    vu += __shfl_xor_sync(0xffffffffu, vu, off);
+                        for (int j = 0; j < PC1; ++j) v[r] = fmaf(static_cast<float>(P[r][j] >> 4), sc[r][j], v[r]);
+                    }
+                    // reduce-scatter of the 4 row sums: lane keeps row 2*bit4 + bit3
+                    const bool b4 = lane & 16, b3 = lane & 8;
+                    float k0 = b4 ? v[2] : v[0], k1 = b4 ? v[3] : v[1];
+                    const float s0 = b4 ? v[0] : v[2], s1 = b4 ? v[1] : v[3];
+                    k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+                    k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+                    float kk = b3 ? k1 : k0;
+                    kk += __shfl_xor_sync(0xffffffffu, b3 ? k0 : k1, 8);
+                    kk += __shfl_xor_sync(0xffffffffu, kk, 4);
+                    kk += __shfl_xor_sync(0xffffffffu, kk, 2);
+                    kk += __shfl_xor_sync(0xffffffffu, kk, 1);
+                    const float upv = __shfl_xor_sync(0xffffffffu, kk, 16);  // up row of the same index
+                    if (!b4 && (lane & 7) == 0) {
+                        const float xs = s.xs[t];
+                        a.h[static_cast<int64_t>(prow) * I + 2 * ip + (b3 ? 1 : 0)] = silu_f32(kk * xs) * (upv * xs);
+                    }
                 }
-                if (lane == 0) {
-                    const float xs = s.xs[t];
-                    a.h[static_cast<int64_t>(r) * I + i] = silu_f32(vg * xs) * (vu * xs);
-                }
+                if (un + DEPTH < nun) issue(un + DEPTH, d);  // refill this ring slot
+                prefetch_some();
             }
         }
     }
+    while (next_line < n_lines) prefetch_some();  // whatever phase 1 did not cover
     if (MODE == DecodeMode::kGemm1Partials) return;
 
     // ---------------------------------------------------------------- barrier
-    bool ok = true;
-    if (MODE == DecodeMode::kForward) ok = grid_barrier(a.hdr, 1);
-    if (!ok) {
-        // leave only once this CTA's own bulk copies have landed
-        if (tid == 0 && n_smem > 0 && nrows > 0) mbar_wait_bounded(s.bar, 0);
-        __syncthreads();
-        return;
-    }
+    if (MODE == DecodeMode::kForward && !grid_barrier(a.hdr, 1)) return;
 
     // ---------------------------------------------------------------- phase 2
     const int P = n_rows + T * S;
-    // (a) int8 rows in the phase-2 layout: [p][chunk j][half][lane 0..15][16 B]
     if (MODE == DecodeMode::kForward) {
-        for (int p = warp; p < P; p += kWarpsD) {
-            const float* hrow = a.h + static_cast<int64_t>(p) * I;
-            float v[C2][16];
-            float m = 0.f;
-            const int nout = I / 16 / 32;  // 16-byte outputs per lane
+        // (a) requantise every pair row: warp per row, lane per 16 values of each 512-value chunk
+        constexpr int RB = PC2 == 1 ? 2 : 1;  // rows in flight per warp
+        for (int p0 = warp; p0 < P; p0 += RB * kWarpsD) {
+            float v[RB][PC2][16];
+            float m[RB];
 #pragma unroll
-            for (int c = 0; c < C2; ++c)
-                if (c < nout) {
-                    const int o = lane + 32 * c;
-                    const int j = o / 32, half = (o / 16) % 2, l = o % 16;
-                    const int k0 = 32 * (16 * j + l) + 16 * half;
+            for (int b = 0; b < RB; ++b) {
+                m[b] = 0.f;
+                const int p = p0 + b * kWarpsD;
+                if (p >= P) break;
+                const float* hrow = a.h + static_cast<int64_t>(p) * I;
+#pragma unroll
+                for (int c = 0; c < PC2; ++c)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const float4 f = __ldcg(reinterpret_cast<const float4*>(hrow + k0 + 4 * q));
-                        v[c][4 * q] = f.x;
-                        v[c][4 * q + 1] = f.y;
-                        v[c][4 * q + 2] = f.z;
-                        v[c][4 * q + 3] = f.w;
+                        const float4 f = __ldcg(reinterpret_cast<const float4*>(hrow + 16 * lane + 512 * c + 4 * q));
+                        v[b][c][4 * q] = f.x;
+                        v[b][c][4 * q + 1] = f.y;
+                        v[b][c][4 * q + 2] = f.z;
+                        v[b][c][4 * q + 3] = f.w;
                     }
+            }
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) m = fmaxf(m, fabsf(v[c][q]));
-                }
+            for (int b = 0; b < RB; ++b) {
+                const int p = p0 + b * kWarpsD;
+                if (p >= P) break;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            const float sc = requant_scale(__float_as_uint(m));
+                for (int c = 0; c < PC2; ++c)
 #pragma unroll
-            for (int c = 0; c < C2; ++c)
-                if (c < nout) {
-                    const int o = lane + 32 * c;
+                    for (int q = 0; q < 16; ++q) m[b] = fmaxf(m[b], fabsf(v[b][c][q]));
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) m[b] = fmaxf(m[b], __shfl_xor_sync(0xffffffffu, m[b], off));
+                const float sc = requant_scale(__float_as_uint(m[b]));
+                const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+#pragma unroll
+                for (int c = 0; c < PC2; ++c) {
                     uint32_t wds[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        wds[q] = (requant_code(v[c][4 * q], sc) & 0xFF) |
-                                 ((requant_code(v[c][4 * q + 1], sc) & 0xFF) << 8) |
-                                 ((requant_code(v[c][4 * q + 2], sc) & 0xFF) << 16) |
-                                 ((static_cast<uint32_t>(requant_code(v[c][4 * q + 3], sc)) & 0xFF) << 24);
-                    *reinterpret_cast<uint4*>(s.hq + static_cast<int64_t>(p) * I + o * 16) =
+                        wds[q] = (requant_code_fast(v[b][c][4 * q], sc, rs) & 0xFF) |
+                                 ((requant_code_fast(v[b][c][4 * q + 1], sc, rs) & 0xFF) << 8) |
+                                 ((requant_code_fast(v[b][c][4 * q + 2], sc, rs) & 0xFF) << 16) |
+                                 ((static_cast<uint32_t>(requant_code_fast(v[b][c][4 * q + 3], sc, rs)) & 0xFF) << 24);
+                    *reinterpret_cast<uint4*>(s.hq + p * HQS + 16 * lane + 512 * c) =
                         split16(make_uint4(wds[0], wds[1], wds[2], wds[3]));
                 }
-            if (lane == 0) {
-                s.sh[p] = sc;
-                if (a.amax && blockIdx.x == 0) a.amax[p] = __float_as_uint(m);
+                if (lane == 0) {
+                    s.sh[p] = sc;
+                    if (a.amax && blockIdx.x == 0) a.amax[p] = __float_as_uint(m[b]);
+                }
             }
         }
     } else {  // kGemm2Partials: rows given as int8
         const int per_row = I / 16;
         for (int o = tid; o < P * per_row; o += kThreadsD) {
             const int p = o / per_row, c = o % per_row;
-            const int j = c / 32, half = (c / 16) % 2, l = c % 16;
-            const int k0 = 32 * (16 * j + l) + 16 * half;
-            const uint4 v = *reinterpret_cast<const uint4*>(a.h_q_in + static_cast<int64_t>(p) * I + k0);
-            *reinterpret_cast<uint4*>(s.hq + static_cast<int64_t>(p) * I + c * 16) = split16(v);
+            const uint4 v = *reinterpret_cast<const uint4*>(a.h_q_in + static_cast<int64_t>(p) * I + 16 * c);
+            *reinterpret_cast<uint4*>(s.hq + p * HQS + 16 * c) = split16(v);
         }
     }
     __syncthreads();
-    if (MODE == DecodeMode::kForward && n_smem > 0 && nrows > 0) {
-        if (tid == 0 && !mbar_wait_bounded(s.bar, 0)) {
-            atomicOr(&a.hdr->status, kDevTimeout);
-            s.flags[0] = 1;
-        }
-        __syncthreads();
-        if (s.flags[0]) {
-            if (tid == 0) mbar_wait_bounded(s.bar, 0);
-            __syncthreads();
-            return;
-        }
-    }
     if (nrows == 0) return;
 
-    // (b) down projection: half-warp teams over (slot, row) units
+    // (b) down projection: units of (slot, 8 output rows), lane per 16-value K piece per 512-value chunk
     {
-        const int team = warp * 2 + (lane >> 4), n_teams = kWarpsD * 2, l = lane & 15;
-        const unsigned hmask = 0xFFFFu << (lane & 16);
-        const int lpg2 = g / 32;
-        const int n_units = n_slots * nrows;
-        constexpr int kMaxC2 = C2;
-        for (int U = team; U < n_units; U += n_teams) {
-            const int u = U / nrows, r = U % nrows;
+        const int ntile = (nrows + 7) / 8;
+        const int n_units = n_slots * ntile;
+        const int lpg2 = g / 16;  // lanes per K group
+        for (int U = warp; U < n_units; U += kWarpsD) {
+            const int u = U / ntile, r8 = 8 * (U % ntile);
             const int64_t e = s.slot_e[u];
-            uint4 w[kMaxC2];
-            float sc[kMaxC2];
-#pragma unroll
-            for (int j = 0; j < kMaxC2; ++j)
-                if (j < C2) {
-                    const int q = (32 * (16 * j + l)) / g;
-                    if (u < n_smem) {
-                        const uint8_t* base = s.w2s + static_cast<int64_t>(u) * (slot_w_bytes + slot_s_bytes);
-                        w[j] = *reinterpret_cast<const uint4*>(base + r * (I / 2) + 16 * (16 * j + l));
-                        sc[j] = reinterpret_cast<const float*>(base + slot_w_bytes)[r * ng2 + q];
-                    } else {
-                        const uint8_t* row = a.w2 + (e * H + n0 + r) * static_cast<int64_t>(I / 2);
-                        w[j] = *reinterpret_cast<const uint4*>(row + 16 * (16 * j + l));
-                        sc[j] = MODE == DecodeMode::kForward ? __ldg(a.s2 + (e * H + n0 + r) * ng2 + q) : 0.f;
-                    }
-                }
             const int row0 = s.slot_row0[u], cnt = s.slot_cnt[u];
+            uint2 w[8][PC2];
+            float sc[8][PC2];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int rr = min(r8 + r, nrows - 1);
+                const int64_t row = e * H + n0 + rr;
+#pragma unroll
+                for (int c = 0; c < PC2; ++c) {
+                    w[r][c] = ld_nc8(a.w2 + row * (I / 2) + 8 * lane + 256 * c);
+                    sc[r][c] = MODE == DecodeMode::kForward ? __ldg(a.s2 + row * ng2 + (16 * lane + 512 * c) / g) : 0.f;
+                }
+            }
             for (int m = 0; m < cnt; ++m) {
                 const int p = row0 + m;
-                int acc[kMaxC2];
+                int Pr[8][PC2];
 #pragma unroll
-                for (int j = 0; j < kMaxC2; ++j)
-                    if (j < C2) {
-                        const uint8_t* xp = s.hq + static_cast<int64_t>(p) * I + j * 512 + l * 16;
-                        acc[j] = dot_chunk(w[j], *reinterpret_cast<const uint4*>(xp),
-                                           *reinterpret_cast<const uint4*>(xp + 256), 0);
-                    }
-                for (int off = 1; off < lpg2; off <<= 1)
+                for (int c = 0; c < PC2; ++c) {
+                    const uint4 xq = *reinterpret_cast<const uint4*>(s.hq + p * HQS + 16 * lane + 512 * c);
 #pragma unroll
-                    for (int j = 0; j < kMaxC2; ++j)
-                        if (j < C2) acc[j] += __shfl_xor_sync(hmask, acc[j], off);
-                const bool leader = (l % lpg2) == 0;
+                    for (int r = 0; r < 8; ++r) Pr[r][c] = dot8(w[r][c].y, xq.z, xq.w, dot8(w[r][c].x, xq.x, xq.y, 0));
+                }
                 if (MODE == DecodeMode::kGemm2Partials) {
-                    if (leader) {
-                        int32_t* dst = a.p2 + (static_cast<int64_t>(p) * H + n0 + r) * ng2;
 #pragma unroll
-                        for (int j = 0; j < kMaxC2; ++j)
-                            if (j < C2) dst[(32 * (16 * j + l)) / g] = acc[j] >> 4;
-                    }
+                    for (int r = 0; r < 8; ++r)
+#pragma unroll
+                        for (int c = 0; c < PC2; ++c) {
+                            int v = Pr[r][c];
+                            for (int off = 1; off < lpg2; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                            if ((lane % lpg2) == 0 && r8 + r < nrows)
+                                a.p2[(static_cast<int64_t>(p) * H + n0 + r8 + r) * ng2 + (16 * lane + 512 * c) / g] = v >> 4;
+                        }
                     continue;
                 }
-                float v = 0.f;
-                if (leader) {
+                float v[8];
 #pragma unroll
-                    for (int j = 0; j < kMaxC2; ++j)
-                        if (j < C2) v = fmaf(static_cast<float>(acc[j] >> 4), sc[j], v);
+                for (int r = 0; r < 8; ++r) {
+                    v[r] = 0.f;
+#pragma unroll
+                    for (int c = 0; c < PC2; ++c) v[r] = fmaf(static_cast<float>(Pr[r][c] >> 4), sc[r][c], v[r]);
                 }
+                // reduce-scatter of 8 row sums: lane keeps row 4*bit4 + 2*bit3 + bit2
+                const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+                float k4[4];
 #pragma unroll
-                for (int off = 1; off < 16; off <<= 1) v += __shfl_xor_sync(hmask, v, off);
-                if (l == 0) {
-                    const float yv = v * s.sh[p];
-                    s.y[p * pl.rows_pc + r] = yv;
-                    if (a.y) a.y[static_cast<int64_t>(p) * H + n0 + r] = yv;
+                for (int q = 0; q < 4; ++q) {
+                    const float keep = b4 ? v[4 + q] : v[q], send = b4 ? v[q] : v[4 + q];
+                    k4[q] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                }
+                float k2[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const float keep = b3 ? k4[2 + q] : k4[q], send = b3 ? k4[q] : k4[2 + q];
+                    k2[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                }
+                float kk = (b2 ? k2[1] : k2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? k2[0] : k2[1], 4);
+                kk += __shfl_xor_sync(0xffffffffu, kk, 2);
+                kk += __shfl_xor_sync(0xffffffffu, kk, 1);
+                const int r = (b4 ? 4 : 0) + (b3 ? 2 : 0) + (b2 ? 1 : 0);
+                if ((lane & 3) == 0 && r8 + r < nrows) {
+                    const float yv = kk * s.sh[p];
+                    s.y[p * pl.rows_pc + r8 + r] = yv;
+                    if (a.y) a.y[static_cast<int64_t>(p) * H + n0 + r8 + r] = yv;
                 }
             }
         }
@@ -650,59 +699,9 @@ __global__ void barrier_timeout_probe_kernel(Header* hdr) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-}  // namespace
-
-// Shared-memory plan of one launch (host side; the kernel reads the offsets).
-bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t k, int64_t g, int64_t n_pairs,
-                 DecodeMode mode, int grid, int max_smem, DecodePlan* out) {
-    if (!decode_shape_supported(H, I) || I > kMaxI || (I / g) % 4 != 0 || g % 32 != 0 || g > 1024) return false;
-    if (E > kMaxExperts) return false;
-    const int64_t rows = mode == DecodeMode::kForward ? T * k : n_pairs;
-    const int64_t Sx = mode == DecodeMode::kForward ? S : 0;
-    const int64_t P = rows + T * Sx;
-    if (T > kDecodeMaxT || rows > kDecodeMaxPairs || P > kDecodeMaxPairs + kDecodeMaxT * kMaxShared) return false;
-    const int64_t MS = rows + Sx;
-    DecodePlan pl{};
-    pl.rows_pc = static_cast<int>((H + grid - 1) / grid);
-    pl.rows_pc = (pl.rows_pc + 1) / 2 * 2;
-    size_t o = 0;
-    auto take = [&](size_t bytes, size_t al) {
-        o = align_up(o, al);
-        size_t at = o;
-        o += bytes;
-        return static_cast<int>(at);
-    };
-    pl.off_bar = take(8, 8);
-    pl.off_flags = take(16, 16);
-    pl.off_ids = take(4 * rows, 16);
-    pl.off_wts = take(4 * rows, 16);
-    pl.off_pos = take(4 * rows, 16);
-    pl.off_pair_of = take(4 * rows, 16);
-    pl.off_row_tok = take(4 * P, 16);
-    pl.off_slot_e = take(4 * MS, 16);
-    pl.off_slot_row0 = take(4 * MS, 16);
-    pl.off_slot_cnt = take(4 * MS, 16);
-    pl.off_n_slots = take(16, 16);
-    pl.off_xs = take(4 * T, 16);
-    pl.off_sh = take(4 * P, 16);
-    pl.off_x = take(mode == DecodeMode::kGemm2Partials ? 0 : T * H, 128);
-    pl.off_hq = take(mode == DecodeMode::kGemm1Partials ? 0 : P * I, 128);
-    pl.off_y = take(mode == DecodeMode::kForward ? 4 * P * pl.rows_pc : 0, 16);
-    pl.off_w2s = static_cast<int>(align_up(o, 128));
-    const size_t slot_bytes = static_cast<size_t>(pl.rows_pc) * (I / 2) + static_cast<size_t>(pl.rows_pc) * (I / g) * 4;
-    const size_t fixed = pl.off_w2s;
-    if (fixed > static_cast<size_t>(max_smem)) return false;
-    int64_t fit = mode == DecodeMode::kForward ? static_cast<int64_t>((max_smem - fixed) / slot_bytes) : 0;
-    pl.smem_slots = static_cast<int>(std::min<int64_t>(fit, MS));
-    pl.smem_bytes = static_cast<int>(fixed + pl.smem_slots * slot_bytes);
-    *out = pl;
-    return true;
-}
-
-namespace {
-template <DecodeMode MODE, int C1, int C2>
+template <DecodeMode MODE, int PC1, int PC2>
 cudaError_t launch_mode(const DecodeArgs& a, const DecodePlan& pl, int grid, cudaStream_t st) {
-    auto kern = decode_kernel<MODE, C1, C2>;
+    auto kern = decode_kernel<MODE, PC1, PC2>;
     // The dynamic shared memory limit is one value per kernel: set it once per
     // device to the largest size any plan may ask for.
     static std::mutex mu;
@@ -731,13 +730,63 @@ cudaError_t launch_mode(const DecodeArgs& a, const DecodePlan& pl, int grid, cud
     return cudaLaunchKernelEx(&cfg, kern, a, pl);
 }
 
-template <int C1, int C2>
+template <int PC1, int PC2>
 cudaError_t launch_shape(DecodeMode mode, const DecodeArgs& a, const DecodePlan& pl, int grid, cudaStream_t st) {
-    if (mode == DecodeMode::kForward) return launch_mode<DecodeMode::kForward, C1, C2>(a, pl, grid, st);
-    if (mode == DecodeMode::kGemm1Partials) return launch_mode<DecodeMode::kGemm1Partials, C1, C2>(a, pl, grid, st);
-    return launch_mode<DecodeMode::kGemm2Partials, C1, C2>(a, pl, grid, st);
+    if (mode == DecodeMode::kForward) return launch_mode<DecodeMode::kForward, PC1, PC2>(a, pl, grid, st);
+    if (mode == DecodeMode::kGemm1Partials) return launch_mode<DecodeMode::kGemm1Partials, PC1, PC2>(a, pl, grid, st);
+    return launch_mode<DecodeMode::kGemm2Partials, PC1, PC2>(a, pl, grid, st);
 }
+
 }  // namespace
+
+// (H / 2048, I / 512) shapes the engine is compiled for.
+bool decode_shape_supported(int64_t H, int64_t I) {
+    if (H % 2048 != 0 || I % 512 != 0) return false;
+    const int64_t p1 = H / 2048, p2 = I / 512;
+    return (p1 == 1 || p1 == 2) && (p2 == 1 || p2 == 3);
+}
+
+// Shared-memory plan of one launch (host side; the kernel reads the offsets).
+bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t k, int64_t g, int64_t n_pairs,
+                 DecodeMode mode, int grid, int max_smem, DecodePlan* out) {
+    if (!decode_shape_supported(H, I) || g % 64 != 0 || g > 512 || E > kMaxExperts) return false;
+    const int64_t rows = mode == DecodeMode::kForward ? T * k : n_pairs;
+    const int64_t Sx = mode == DecodeMode::kForward ? S : 0;
+    const int64_t P = rows + T * Sx;
+    if (T > kDecodeMaxT || rows > kDecodeMaxPairs || P > kDecodeMaxPairs + kDecodeMaxT * kMaxShared) return false;
+    if (mode != DecodeMode::kForward && rows < 1) return false;
+    const int64_t MS = rows + Sx;
+    DecodePlan pl{};
+    pl.rows_pc = static_cast<int>((H + grid - 1) / grid);
+    size_t o = 0;
+    auto take = [&](size_t bytes, size_t al) {
+        o = align_up(o, al);
+        size_t at = o;
+        o += bytes;
+        return static_cast<int>(at);
+    };
+    pl.off_ids = take(4 * rows, 16);
+    pl.off_wts = take(4 * rows, 16);
+    pl.off_pos = take(4 * rows, 16);
+    pl.off_pair_of = take(4 * rows, 16);
+    pl.off_row_tok = take(4 * P, 16);
+    pl.off_slot_e = take(4 * MS, 16);
+    pl.off_slot_row0 = take(4 * MS, 16);
+    pl.off_slot_cnt = take(4 * MS, 16);
+    pl.off_slot_cum = take(4 * (MS + 1), 16);
+    pl.off_n_slots = take(16, 16);
+    pl.off_xs = take(4 * T, 16);
+    pl.off_sh = take(4 * P, 16);
+    pl.off_x = take(mode == DecodeMode::kGemm2Partials ? 0 : T * (H + 16), 128);
+    pl.off_hq = take(mode == DecodeMode::kGemm1Partials ? 0 : P * (I + 16), 128);
+    pl.off_y = take(mode == DecodeMode::kForward ? 4 * P * pl.rows_pc : 0, 16);
+    pl.off_cand_v = take(mode == DecodeMode::kForward ? 4 * T * 8 * k : 0, 16);
+    pl.off_cand_e = take(mode == DecodeMode::kForward ? 4 * T * 8 * k : 0, 16);
+    pl.smem_bytes = static_cast<int>(align_up(o, 128));
+    if (pl.smem_bytes > max_smem) return false;
+    *out = pl;
+    return true;
+}
 
 int decode_grid() { return num_sms(); }
 
@@ -754,24 +803,16 @@ int decode_max_smem() {
     return cached[dev];
 }
 
-// (H / 1024, I / 512) shapes the engine is compiled for.
-bool decode_shape_supported(int64_t H, int64_t I) {
-    if (H % 1024 != 0 || I % 512 != 0) return false;
-    const int64_t c1 = H / 1024, c2 = I / 512;
-    return (c2 == 1 && (c1 == 1 || c1 == 2 || c1 == 4)) || (c2 == 3 && (c1 == 2 || c1 == 4));
-}
-
 cudaError_t launch_decode(DecodeMode mode, const DecodeArgs& a, const DecodePlan& pl, int grid, cudaStream_t st) {
     if (mode == DecodeMode::kForward) {
         cudaError_t e = cudaMemsetAsync(a.hdr, 0, 16, st);  // status and barrier counters
         if (e != cudaSuccess) return e;
     }
-    const int c1 = a.H / 1024, c2 = a.I / 512;
-    if (c2 == 1 && c1 == 1) return launch_shape<1, 1>(mode, a, pl, grid, st);
-    if (c2 == 1 && c1 == 2) return launch_shape<2, 1>(mode, a, pl, grid, st);
-    if (c2 == 1 && c1 == 4) return launch_shape<4, 1>(mode, a, pl, grid, st);
-    if (c2 == 3 && c1 == 2) return launch_shape<2, 3>(mode, a, pl, grid, st);
-    if (c2 == 3 && c1 == 4) return launch_shape<4, 3>(mode, a, pl, grid, st);
+    const int p1 = a.H / 2048, p2 = a.I / 512;
+    if (p1 == 1 && p2 == 1) return launch_shape<1, 1>(mode, a, pl, grid, st);
+    if (p1 == 2 && p2 == 1) return launch_shape<2, 1>(mode, a, pl, grid, st);
+    if (p1 == 1 && p2 == 3) return launch_shape<1, 3>(mode, a, pl, grid, st);
+    if (p1 == 2 && p2 == 3) return launch_shape<2, 3>(mode, a, pl, grid, st);
     return cudaErrorInvalidValue;
 }
 

@@ -104,7 +104,7 @@ def _sample_pairs(w, tok, n, seed=0):
 
 # engine 0 = grouped tensor-core engine (any size), 1 = fused decode engine (T <= 32)
 PARTIALS_CASES = [(n, 0) for n in ALL] + [("decode_t4", 1), ("decode_verify_t12", 1), ("dec_small", 1)]
-DEC_SMALL = synth.Workload("dec_small", T=8, H=1024, I=512, E=16, S=1, top_k=4, group=128)
+DEC_SMALL = synth.Workload("dec_small", T=8, H=2048, I=512, E=16, S=1, top_k=4, group=128)
 
 
 def _workload(name):
@@ -298,7 +298,7 @@ def test_decode_engine_ragged_batches(T):
 
 @pytest.mark.parametrize("k,S", [(1, 0), (16, 1), (4, 0), (4, 2)])
 def test_decode_engine_top_k_and_shared(k, S):
-    w = synth.Workload("dk", T=9, H=1024, I=512, E=16, S=S, top_k=k, group=64)
+    w = synth.Workload("dk", T=9, H=2048, I=512, E=16, S=S, top_k=k, group=64)
     tok = synth.make_tokens(w)
     out = _forward_engine(w, tok, 1)
     gh.assert_output_close(out, gh.oracle_out(w, tok, gh.bank_of(w)), f"decode k={k} S={S}")
