@@ -62,6 +62,9 @@ int cuda_status(cudaError_t e, const char* what) {
 
 struct Views {
     moe::Header* hdr;
+    uint32_t* flags;
+    int8_t* hq;
+    float* sh;
     int32_t *ids, *seg_cnt, *seg_off, *perm, *inv, *row_token, *chunk_counts, *tile_slot, *tile_row0;
     float *wts, *h, *y;
     uint32_t* amax;
@@ -70,6 +73,9 @@ struct Views {
 Views views(void* ws, const WsLayout& L) {
     Views v;
     v.hdr = moe::ws_at<moe::Header>(ws, L.hdr);
+    v.flags = moe::ws_at<uint32_t>(ws, L.flags);
+    v.hq = moe::ws_at<int8_t>(ws, L.hq);
+    v.sh = moe::ws_at<float>(ws, L.sh);
     v.ids = moe::ws_at<int32_t>(ws, L.ids);
     v.wts = moe::ws_at<float>(ws, L.wts);
     v.seg_cnt = moe::ws_at<int32_t>(ws, L.seg_cnt);
@@ -136,6 +142,9 @@ int run_decode(const int8_t* x_q, const float* x_scale, const float* logits, con
     a.g = static_cast<int>(d->group);
     a.out = out;
     a.hdr = v.hdr;
+    a.flags = v.flags;
+    a.hq_g = v.hq;
+    a.sh_g = v.sh;
     a.h = v.h;
     a.amax = v.amax;
     a.y = y_debug;

@@ -123,52 +123,69 @@ __device__ bool grid_barrier(Header* hdr, uint32_t k) {
 // (v, e) beats (bv, be): larger value, or equal value and lower index.
 __device__ __forceinline__ bool beats(float v, int e, float bv, int be) { return v > bv || (v == bv && e < be); }
 
-// Top-k of one warp's share of a token's candidates, largest first (ties to
-// the lower expert index).  Lane `lane` holds candidates j = 0..NJ-1 (value
-// v[j], expert id id[j], -inf/INT_MAX when absent) and keeps its own best
-// remaining candidate, so each round is one warp argmax plus a rescan by
-// the winning lane only.  Selected (value, id) pairs land in out_v/out_e
-// (lane s holds the s-th).
+// Order-preserving 32-bit key of a float: larger float -> larger key; -0.0
+// and +0.0 map to the same key (the sum with +0.0 turns -0.0 into +0.0).
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(v + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// (key a, id ia) ranks before (key b, id ib): larger key, or equal key and lower id.
+__device__ __forceinline__ bool ranks_before(uint32_t a, uint32_t ia, uint32_t b, uint32_t ib) {
+    return a > b || (a == b && ia < ib);
+}
+
+// Top-k of a warp's candidates, largest first (ties to the lower id).  Each
+// lane holds NJ candidates (key 0 / id 0xFFFFFFFF when absent), sorts them
+// once (bitonic network in registers), then each round takes the warp
+// maximum of the lanes' heads with two redux operations (max key, then min
+// id among the lanes holding it) and the winning lane pops its head.  Lane s
+// receives the s-th selected (key, id).
 template <int NJ>
-__device__ __forceinline__ void warp_topk(const float (&v)[NJ], const int (&id)[NJ], int k, float& out_v, int& out_e) {
+__device__ __forceinline__ void warp_topk(uint32_t (&key)[NJ], uint32_t (&id)[NJ], int k, uint32_t& out_key,
+                                          uint32_t& out_id) {
     const int lane = threadIdx.x & 31;
-    uint32_t taken = 0;
-    auto local_best = [&](float& bv, int& be) {
-        bv = -INFINITY;
-        be = INT32_MAX;
 #pragma unroll
-        for (int j = 0; j < NJ; ++j)
-            if (!(taken >> j & 1u) && beats(v[j], id[j], bv, be)) {
-                bv = v[j];
-                be = id[j];
+    for (int k2 = 2; k2 <= NJ; k2 <<= 1)
+#pragma unroll
+        for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1)
+#pragma unroll
+            for (int i = 0; i < NJ; ++i) {
+                const int l = i ^ j2;
+                if (l > i) {
+                    const bool want_i_first = (i & k2) == 0;
+                    const bool i_first = ranks_before(key[i], id[i], key[l], id[l]);
+                    if (i_first != want_i_first) {
+                        const uint32_t tk = key[i], ti = id[i];
+                        key[i] = key[l];
+                        id[i] = id[l];
+                        key[l] = tk;
+                        id[l] = ti;
+                    }
+                }
             }
-    };
-    float lv;
-    int le;
-    local_best(lv, le);
-    out_v = -INFINITY;
-    out_e = INT32_MAX;
+    // the first half of a bitonic sort per k2 level sorts descending when
+    // (i & NJ) == 0, which holds for every i < NJ: the list is descending.
+    out_key = 0;
+    out_id = 0xFFFFFFFFu;
     for (int s = 0; s < k; ++s) {
-        float bv = lv;
-        int be = le;
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, key[0]);
+        const uint32_t mi = __reduce_min_sync(0xffffffffu, key[0] == mk ? id[0] : 0xFFFFFFFFu);
+        if (key[0] == mk && id[0] == mi) {  // this lane holds the winner: pop it
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            if (beats(ov, oe, bv, be)) {
-                bv = ov;
-                be = oe;
+            for (int j = 0; j + 1 < NJ; ++j) {
+                key[j] = key[j + 1];
+                id[j] = id[j + 1];
             }
-        }
-        if (le == be && be != INT32_MAX) {  // this lane held the winner: drop it, rescan
-#pragma unroll
-            for (int j = 0; j < NJ; ++j)
-                if (id[j] == be) taken |= 1u << j;
-            local_best(lv, le);
+            key[NJ - 1] = 0;
+            id[NJ - 1] = 0xFFFFFFFFu;
         }
         if (lane == s) {
-            out_v = bv;
-            out_e = be;
+            out_key = mk;
+            out_id = mi;
         }
     }
 }
@@ -177,55 +194,53 @@ __device__ __forceinline__ void warp_topk(const float (&v)[NJ], const int (&id)[
 // split over `wpt` warps (interleaved), each finds the top-k of its share,
 // and one warp per token merges the wpt * k candidates.  The result equals
 // the top-k over all experts (every global top-k expert is in its share's
-// top-k).  ids/wts: [T][k]; cand_v/cand_e: [T][wpt][k] scratch.
-__device__ void route_all(const float* __restrict__ logits, int T, int E, int k, int* ids, float* wts, float* cand_v,
-                          int* cand_e) {
+// top-k).  ids/wts: [T][k]; cand_k/cand_i: [T][wpt][k] scratch.
+template <int NJ>
+__device__ void route_all(const float* __restrict__ logits, int T, int E, int k, int* ids, float* wts,
+                          uint32_t* cand_k, uint32_t* cand_i) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     int wpt = 1;
     while (wpt * 2 * T <= nw && wpt < 8 && 32 * wpt * 2 <= E) wpt *= 2;
-    constexpr int NJ = kMaxExperts / 32;
+    while (32 * NJ * wpt < E) wpt *= 2;  // each lane holds at most NJ candidates
     for (int job = warp; job < T * wpt; job += nw) {
         const int t = job / wpt, sub = job % wpt;
-        float v[NJ];
-        int id[NJ];
+        uint32_t key[NJ], id[NJ];
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
             const int e = sub * 32 + lane + 32 * wpt * j;
             const bool in = e < E;
-            v[j] = in ? __ldg(logits + static_cast<int64_t>(t) * E + e) : -INFINITY;
-            id[j] = in ? e : INT32_MAX;
+            key[j] = in ? order_key(__ldg(logits + static_cast<int64_t>(t) * E + e)) : 0u;
+            id[j] = in ? static_cast<uint32_t>(e) : 0xFFFFFFFFu;
         }
-        float ov;
-        int oe;
-        warp_topk<NJ>(v, id, k, ov, oe);
+        uint32_t ok, oi;
+        warp_topk<NJ>(key, id, k, ok, oi);
         if (lane < k) {
-            cand_v[(t * wpt + sub) * k + lane] = ov;
-            cand_e[(t * wpt + sub) * k + lane] = oe;
+            cand_k[(t * wpt + sub) * k + lane] = ok;
+            cand_i[(t * wpt + sub) * k + lane] = oi;
         }
     }
     __syncthreads();
     for (int t = warp; t < T; t += nw) {
-        constexpr int NM = 8;  // wpt * k <= 8 * 32 candidates, 8 per lane
-        float v[NM];
-        int id[NM];
+        constexpr int NM = 8;  // wpt * k <= 8 * 32 candidates
+        uint32_t key[NM], id[NM];
 #pragma unroll
         for (int j = 0; j < NM; ++j) {
             const int c = lane + 32 * j;
             const bool in = c < wpt * k;
-            v[j] = in ? cand_v[t * wpt * k + c] : -INFINITY;
-            id[j] = in ? cand_e[t * wpt * k + c] : INT32_MAX;
+            key[j] = in ? cand_k[t * wpt * k + c] : 0u;
+            id[j] = in ? cand_i[t * wpt * k + c] : 0xFFFFFFFFu;
         }
-        float my_v;
-        int my_e;
-        warp_topk<NM>(v, id, k, my_v, my_e);
+        uint32_t mk, mi;
+        warp_topk<NM>(key, id, k, mk, mi);
         // softmax over the selected logits, relative to the largest (selected first)
+        const float my_v = key_value(mk);
         const float m = __shfl_sync(0xffffffffu, my_v, 0);
         const float ex = lane < k ? expf(my_v - m) : 0.0f;
         float sum = ex;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
         if (lane < k) {
-            ids[t * k + lane] = my_e;
+            ids[t * k + lane] = static_cast<int>(mi);
             wts[t * k + lane] = ex / sum;
         }
     }
@@ -287,8 +302,9 @@ struct Smem {
     uint8_t* x;       // [T][H + 16] split layout
     uint8_t* hq;      // [P][I + 16] split layout
     float* y;         // [P][rows_pc]
-    float* cand_v;    // [T][8][k] routing candidates
-    int* cand_e;      // [T][8][k]
+    uint32_t* cand_k; // [T][8][k] routing candidates (order keys)
+    uint32_t* cand_i; // [T][8][k] (expert ids)
+    uint8_t* w2s;     // [smem_slots][slot_stride] staged down-projection slices
 };
 
 __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
@@ -308,13 +324,59 @@ __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
     s.x = base + pl.off_x;
     s.hq = base + pl.off_hq;
     s.y = reinterpret_cast<float*>(base + pl.off_y);
-    s.cand_v = reinterpret_cast<float*>(base + pl.off_cand_v);
-    s.cand_e = reinterpret_cast<int*>(base + pl.off_cand_e);
+    s.cand_k = reinterpret_cast<uint32_t*>(base + pl.off_cand_v);
+    s.cand_i = reinterpret_cast<uint32_t*>(base + pl.off_cand_e);
+    s.w2s = base + pl.off_w2s;
     return s;
 }
 
-// Phase-1 cost of one unit of a slot with `cnt` tokens (streaming + per-token work).
-__device__ __forceinline__ int unit_cost(int cnt) { return 4 + cnt; }
+// Requantise the pair rows of one slot (all its units are done): row max
+// -> s_h, RNE codes, stored split even|odd to hq_g, scales to sh_g.  One
+// warp; lane owns 16 consecutive values of every 512-value chunk.
+template <int PC2>
+__device__ void requant_slot(const DecodeArgs& a, int row0, int cnt) {
+    const int lane = threadIdx.x & 31, I = a.I;
+    for (int m = 0; m < cnt; ++m) {
+        const int p = row0 + m;
+        const float* hrow = a.h + static_cast<int64_t>(p) * I;
+        float v[PC2][16];
+        float mx = 0.f;
+#pragma unroll
+        for (int c = 0; c < PC2; ++c)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 f = __ldcg(reinterpret_cast<const float4*>(hrow + 16 * lane + 512 * c + 4 * q));
+                v[c][4 * q] = f.x;
+                v[c][4 * q + 1] = f.y;
+                v[c][4 * q + 2] = f.z;
+                v[c][4 * q + 3] = f.w;
+            }
+#pragma unroll
+        for (int c = 0; c < PC2; ++c)
+#pragma unroll
+            for (int q = 0; q < 16; ++q) mx = fmaxf(mx, fabsf(v[c][q]));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float sc = requant_scale(__float_as_uint(mx));
+        const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+#pragma unroll
+        for (int c = 0; c < PC2; ++c) {
+            uint32_t wds[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                wds[q] = (requant_code_fast(v[c][4 * q], sc, rs) & 0xFF) |
+                         ((requant_code_fast(v[c][4 * q + 1], sc, rs) & 0xFF) << 8) |
+                         ((requant_code_fast(v[c][4 * q + 2], sc, rs) & 0xFF) << 16) |
+                         ((static_cast<uint32_t>(requant_code_fast(v[c][4 * q + 3], sc, rs)) & 0xFF) << 24);
+            *reinterpret_cast<uint4*>(a.hq_g + static_cast<int64_t>(p) * I + 16 * lane + 512 * c) =
+                split16(make_uint4(wds[0], wds[1], wds[2], wds[3]));
+        }
+        if (lane == 0) {
+            a.sh_g[p] = sc;
+            if (a.amax) a.amax[p] = __float_as_uint(mx);
+        }
+    }
+}
 
 // PC1 = H / 2048 (64-value pieces per lane per row), PC2 = I / 512 (16-value pieces per lane per row).
 template <DecodeMode MODE, int PC1, int PC2>
@@ -325,12 +387,13 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     const int T = a.T, H = a.H, I = a.I, k = a.k, g = a.g;
     const int ng1 = H / g, ng2 = I / g;
     const int XS = H + 16, HQS = I + 16;
+    const int RS = I / 2 + 16;  // staged down-projection row stride
     const bool routed = MODE == DecodeMode::kForward;
 
     // ---------------------------------------------------------------- phase 0
     int n_rows;  // routed/listed pair rows before the shared rows
     if (routed) {
-        route_all(a.logits, T, a.E, k, s.ids, s.wts, s.cand_v, s.cand_e);
+        route_all<16>(a.logits, T, a.E, k, s.ids, s.wts, s.cand_k, s.cand_i);
         n_rows = T * k;
     } else {
         n_rows = a.n_pairs;  // listed pairs; out-of-range slots and tokens are clamped (never read out of bounds)
@@ -388,62 +451,62 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         s.slot_cnt[u] = u < n_routed_slots ? end - s.slot_row0[u] : T;
     }
     __syncthreads();
-    if (tid == 0) {  // phase-1 cost prefix over slots (n_slots <= a few hundred)
-        int c = 0;
-        for (int u = 0; u < n_slots; ++u) {
-            s.slot_cum[u] = c;
-            c += (I / 2) * unit_cost(s.slot_cnt[u]);
-        }
-        s.slot_cum[n_slots] = c;
-    }
 
-    // this CTA's down-projection slice: rows [n0, n0 + nrows) of every slot.  Its
-    // 128-byte lines are prefetched into L2 during phase 1, a few per unit, so
+    // This CTA's down-projection slice (rows [n0, n0 + nrows) of every slot):
+    // the first n_smem slots are copied into shared memory with cp.async, the
+    // rest warmed in L2.  Each thread issues a few copies per phase-1 unit, so
     // the requests queue behind the phase-1 loads instead of stalling here.
     const int n0 = blockIdx.x * pl.rows_pc;
     const int nrows = max(0, min(pl.rows_pc, H - n0));
+    const int n_smem = MODE == DecodeMode::kForward && nrows > 0 ? min(n_slots, pl.smem_slots) : 0;
+    const int slot_stride = pl.rows_pc * RS + pl.rows_pc * ng2 * 4;
+    const int wch = I / 32, sch = ng2 / 4;  // 16-byte chunks per row: weights, scales
+    const int per_slot = nrows * (wch + sch);
+    const int n_copies = n_smem * per_slot;
     const int lines_w = (nrows * (I / 2) + 127) / 128, lines_s = (nrows * ng2 * 4 + 127) / 128;
-    const int n_lines = MODE == DecodeMode::kForward && nrows > 0 ? n_slots * (lines_w + lines_s) : 0;
-    int next_line = warp * 32 + lane;  // this thread's next line (stride kThreadsD)
-    auto prefetch_some = [&]() {
-        if (next_line < n_lines) {
-            const int u = next_line / (lines_w + lines_s), c = next_line % (lines_w + lines_s);
-            const int64_t e = s.slot_e[u];
-            if (c < lines_w) prefetch_l2(a.w2 + (e * H + n0) * static_cast<int64_t>(I / 2) + 128 * c);
-            else prefetch_l2(reinterpret_cast<const uint8_t*>(a.s2 + (e * H + n0) * ng2) + 128 * (c - lines_w));
-            next_line += kThreadsD;
+    const int n_lines = MODE == DecodeMode::kForward && nrows > 0 ? (n_slots - n_smem) * (lines_w + lines_s) : 0;
+    int next_job = tid;  // this thread's next copy / prefetch (stride kThreadsD)
+    auto stage_some = [&](int budget) {
+        for (int b = 0; b < budget && next_job < n_copies + n_lines; ++b, next_job += kThreadsD) {
+            if (next_job < n_copies) {
+                const int u = next_job / per_slot, c = next_job % per_slot;
+                const int64_t e = s.slot_e[u];
+                uint8_t* base = s.w2s + u * slot_stride;
+                if (c < nrows * wch) {
+                    const int r = c / wch, q = c % wch;
+                    cp_async16(base + r * RS + 16 * q, a.w2 + (e * H + n0 + r) * static_cast<int64_t>(I / 2) + 16 * q);
+                } else {
+                    const int c2 = c - nrows * wch;
+                    cp_async16(base + pl.rows_pc * RS + 16 * c2, a.s2 + (e * H + n0) * ng2 + 4 * c2);
+                }
+            } else {
+                const int o = next_job - n_copies;
+                const int u = n_smem + o / (lines_w + lines_s), c = o % (lines_w + lines_s);
+                const int64_t e = s.slot_e[u];
+                if (c < lines_w) prefetch_l2(a.w2 + (e * H + n0) * static_cast<int64_t>(I / 2) + 128 * c);
+                else prefetch_l2(reinterpret_cast<const uint8_t*>(a.s2 + (e * H + n0) * ng2) + 128 * (c - lines_w));
+            }
         }
+        cp_async_commit();
     };
-    __syncthreads();
 
     // ---------------------------------------------------------------- phase 1
     if (MODE != DecodeMode::kGemm2Partials) {
         constexpr int DEPTH = PC1 == 1 ? 4 : 2;  // units of loads in flight per warp
         const int upe = I / 2;                    // units per slot
-        const int64_t Ctot = s.slot_cum[n_slots];
-        const int64_t W = static_cast<int64_t>(gridDim.x) * kWarpsD;
-        const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarpsD + warp;
-        // this warp's cost range -> unit range [Ua, Ub) over the flattened (slot, unit) space
-        auto unit_at = [&](int64_t cpos) -> int64_t {
-            int lo = 0, hi = n_slots;  // last slot with cum <= cpos
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) / 2;
-                if (s.slot_cum[mid] <= cpos) lo = mid;
-                else hi = mid;
-            }
-            const int c = unit_cost(s.slot_cnt[lo]);
-            int64_t within = (cpos - s.slot_cum[lo] + c - 1) / c;
-            if (within > upe) within = upe;
-            return static_cast<int64_t>(lo) * upe + within;
-        };
-        const int64_t Ua = unit_at(gw * Ctot / W), Ub = unit_at((gw + 1) * Ctot / W);
-        const int nun = static_cast<int>(Ub - Ua);
+        const int n_units = n_slots * upe;
+        const int W = static_cast<int>(gridDim.x) * kWarpsD;
+        const int gw = static_cast<int>(blockIdx.x) * kWarpsD + warp;
+        // units go round-robin over all warps of the grid, so the slots
+        // complete in order while phase 1 progresses
+        const int nun = gw < n_units ? (n_units - gw + W - 1) / W : 0;
+        const int stage_budget = (n_copies + n_lines + kThreadsD - 1) / kThreadsD / max(nun, 1) + 1;
 
         uint4 wr[DEPTH][4][PC1][2];
         float sr[DEPTH][4][PC1];
         auto issue = [&](int un, int d) {
-            const int64_t U = Ua + un;
-            const int u = static_cast<int>(U / upe), ip = static_cast<int>(U % upe);
+            const int U = gw + un * W;
+            const int u = U / upe, ip = U % upe;
             const int64_t e = s.slot_e[u];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -468,8 +531,8 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                 if (un >= nun) break;
                 const uint4(&w)[4][PC1][2] = wr[d];
                 const float(&sc)[4][PC1] = sr[d];
-                const int64_t U = Ua + un;
-                const int u = static_cast<int>(U / upe), ip = static_cast<int>(U % upe);
+                const int U = gw + un * W;
+                const int u = U / upe, ip = U % upe;
                 const int row0 = s.slot_row0[u], cnt = s.slot_cnt[u];
                 for (int m = 0; m < cnt; ++m) {
                     const int prow = row0 + m;
@@ -526,153 +589,96 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                     }
                 }
                 if (un + DEPTH < nun) issue(un + DEPTH, d);  // refill this ring slot
-                prefetch_some();
+                if (MODE == DecodeMode::kForward) stage_some(stage_budget);
+            }
+        }
+        if (MODE == DecodeMode::kForward) {
+            // count this warp's finished units per slot (one fence for all of
+            // them); the warp that completes a slot requantises its pair rows
+            __threadfence();
+            __syncwarp();
+            for (int un = 0; un < nun; ++un) {
+                const int u = (gw + un * W) / upe;
+                int last = 0;
+                if (lane == 0) last = atomicAdd(&a.flags[u], 1u) + 1 == static_cast<unsigned>(upe);
+                if (__shfl_sync(0xffffffffu, last, 0)) {
+                    __threadfence();
+                    requant_slot<PC2>(a, s.slot_row0[u], s.slot_cnt[u]);
+                }
             }
         }
     }
-    while (next_line < n_lines) prefetch_some();  // whatever phase 1 did not cover
     if (MODE == DecodeMode::kGemm1Partials) return;
+    if (MODE == DecodeMode::kForward) stage_some(1 << 30);  // whatever phase 1 did not cover
 
     // ---------------------------------------------------------------- barrier
-    if (MODE == DecodeMode::kForward && !grid_barrier(a.hdr, 1)) return;
+    if (MODE == DecodeMode::kForward && !grid_barrier(a.hdr, 1)) {
+        cp_async_wait<0>();  // this thread's own copies land before the CTA leaves
+        __syncthreads();
+        return;
+    }
 
     // ---------------------------------------------------------------- phase 2
     const int P = n_rows + T * S;
-    if (MODE == DecodeMode::kForward) {
-        // (a) requantise every pair row: warp per row, lane per 16 values of each 512-value chunk
-        constexpr int RB = PC2 == 1 ? 2 : 1;  // rows in flight per warp
-        for (int p0 = warp; p0 < P; p0 += RB * kWarpsD) {
-            float v[RB][PC2][16];
-            float m[RB];
-#pragma unroll
-            for (int b = 0; b < RB; ++b) {
-                m[b] = 0.f;
-                const int p = p0 + b * kWarpsD;
-                if (p >= P) break;
-                const float* hrow = a.h + static_cast<int64_t>(p) * I;
-#pragma unroll
-                for (int c = 0; c < PC2; ++c)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 f = __ldcg(reinterpret_cast<const float4*>(hrow + 16 * lane + 512 * c + 4 * q));
-                        v[b][c][4 * q] = f.x;
-                        v[b][c][4 * q + 1] = f.y;
-                        v[b][c][4 * q + 2] = f.z;
-                        v[b][c][4 * q + 3] = f.w;
-                    }
-            }
-#pragma unroll
-            for (int b = 0; b < RB; ++b) {
-                const int p = p0 + b * kWarpsD;
-                if (p >= P) break;
-#pragma unroll
-                for (int c = 0; c < PC2; ++c)
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) m[b] = fmaxf(m[b], fabsf(v[b][c][q]));
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) m[b] = fmaxf(m[b], __shfl_xor_sync(0xffffffffu, m[b], off));
-                const float sc = requant_scale(__float_as_uint(m[b]));
-                const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
-#pragma unroll
-                for (int c = 0; c < PC2; ++c) {
-                    uint32_t wds[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        wds[q] = (requant_code_fast(v[b][c][4 * q], sc, rs) & 0xFF) |
-                                 ((requant_code_fast(v[b][c][4 * q + 1], sc, rs) & 0xFF) << 8) |
-                                 ((requant_code_fast(v[b][c][4 * q + 2], sc, rs) & 0xFF) << 16) |
-                                 ((static_cast<uint32_t>(requant_code_fast(v[b][c][4 * q + 3], sc, rs)) & 0xFF) << 24);
-                    *reinterpret_cast<uint4*>(s.hq + p * HQS + 16 * lane + 512 * c) =
-                        split16(make_uint4(wds[0], wds[1], wds[2], wds[3]));
-                }
-                if (lane == 0) {
-                    s.sh[p] = sc;
-                    if (a.amax && blockIdx.x == 0) a.amax[p] = __float_as_uint(m[b]);
-                }
-            }
-        }
-    } else {  // kGemm2Partials: rows given as int8
+    {
+        // (a) the requantised rows (already split even|odd) into shared memory
         const int per_row = I / 16;
+        const int8_t* src = MODE == DecodeMode::kForward ? a.hq_g : a.h_q_in;
         for (int o = tid; o < P * per_row; o += kThreadsD) {
             const int p = o / per_row, c = o % per_row;
-            const uint4 v = *reinterpret_cast<const uint4*>(a.h_q_in + static_cast<int64_t>(p) * I + 16 * c);
-            *reinterpret_cast<uint4*>(s.hq + p * HQS + 16 * c) = split16(v);
+            if (MODE == DecodeMode::kForward) {
+                cp_async16(s.hq + p * HQS + 16 * c, src + static_cast<int64_t>(p) * I + 16 * c);
+            } else {
+                const uint4 v = *reinterpret_cast<const uint4*>(src + static_cast<int64_t>(p) * I + 16 * c);
+                *reinterpret_cast<uint4*>(s.hq + p * HQS + 16 * c) = split16(v);
+            }
         }
+        if (MODE == DecodeMode::kForward)
+            for (int p = tid; p < P; p += kThreadsD) s.sh[p] = __ldcg(a.sh_g + p);
+        cp_async_commit();
     }
+    cp_async_wait<0>();
     __syncthreads();
     if (nrows == 0) return;
 
-    // (b) down projection: units of (slot, 8 output rows), lane per 16-value K piece per 512-value chunk
+    // (b) down projection: one lane per (slot, output row); the lane runs the
+    // whole K = I dot product for each token of the slot (no cross-lane sums)
     {
-        const int ntile = (nrows + 7) / 8;
-        const int n_units = n_slots * ntile;
-        const int lpg2 = g / 16;  // lanes per K group
-        for (int U = warp; U < n_units; U += kWarpsD) {
-            const int u = U / ntile, r8 = 8 * (U % ntile);
+        const int n_items = n_slots * nrows;
+        for (int L = tid; L < n_items; L += kThreadsD) {
+            const int u = L / nrows, r = L % nrows;
             const int64_t e = s.slot_e[u];
             const int row0 = s.slot_row0[u], cnt = s.slot_cnt[u];
-            uint2 w[8][PC2];
-            float sc[8][PC2];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int rr = min(r8 + r, nrows - 1);
-                const int64_t row = e * H + n0 + rr;
-#pragma unroll
-                for (int c = 0; c < PC2; ++c) {
-                    w[r][c] = ld_nc8(a.w2 + row * (I / 2) + 8 * lane + 256 * c);
-                    sc[r][c] = MODE == DecodeMode::kForward ? __ldg(a.s2 + row * ng2 + (16 * lane + 512 * c) / g) : 0.f;
-                }
-            }
+            const bool in_smem = u < n_smem;
+            const uint8_t* wrow = in_smem ? s.w2s + u * slot_stride + r * RS
+                                          : a.w2 + (e * H + n0 + r) * static_cast<int64_t>(I / 2);
+            const float* srow = in_smem ? reinterpret_cast<const float*>(s.w2s + u * slot_stride + pl.rows_pc * RS) + r * ng2
+                                        : a.s2 + (e * H + n0 + r) * ng2;
             for (int m = 0; m < cnt; ++m) {
                 const int p = row0 + m;
-                int Pr[8][PC2];
-#pragma unroll
-                for (int c = 0; c < PC2; ++c) {
-                    const uint4 xq = *reinterpret_cast<const uint4*>(s.hq + p * HQS + 16 * lane + 512 * c);
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) Pr[r][c] = dot8(w[r][c].y, xq.z, xq.w, dot8(w[r][c].x, xq.x, xq.y, 0));
+                const uint8_t* xrow = s.hq + p * HQS;
+                float acc = 0.f;
+                for (int q = 0; q < ng2; ++q) {
+                    int P = 0;
+                    for (int c = 0; c < g / 32; ++c) {  // 32 codes (16 packed bytes) per step
+                        const int kb = q * (g / 2) + 16 * c;
+                        const uint4 wv = in_smem ? *reinterpret_cast<const uint4*>(wrow + kb)
+                                                 : ld_stream16(wrow + kb);
+                        const uint4 xa = *reinterpret_cast<const uint4*>(xrow + 2 * kb);
+                        const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 2 * kb + 16);
+                        P += dot32(wv, xa, xb);
+                    }
+                    if (MODE == DecodeMode::kGemm2Partials) {
+                        a.p2[(static_cast<int64_t>(p) * H + n0 + r) * ng2 + q] = P >> 4;
+                    } else {
+                        const float sc = in_smem ? srow[q] : __ldg(srow + q);
+                        acc = fmaf(static_cast<float>(P >> 4), sc, acc);
+                    }
                 }
-                if (MODE == DecodeMode::kGemm2Partials) {
-#pragma unroll
-                    for (int r = 0; r < 8; ++r)
-#pragma unroll
-                        for (int c = 0; c < PC2; ++c) {
-                            int v = Pr[r][c];
-                            for (int off = 1; off < lpg2; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                            if ((lane % lpg2) == 0 && r8 + r < nrows)
-                                a.p2[(static_cast<int64_t>(p) * H + n0 + r8 + r) * ng2 + (16 * lane + 512 * c) / g] = v >> 4;
-                        }
-                    continue;
-                }
-                float v[8];
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    v[r] = 0.f;
-#pragma unroll
-                    for (int c = 0; c < PC2; ++c) v[r] = fmaf(static_cast<float>(Pr[r][c] >> 4), sc[r][c], v[r]);
-                }
-                // reduce-scatter of 8 row sums: lane keeps row 4*bit4 + 2*bit3 + bit2
-                const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-                float k4[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float keep = b4 ? v[4 + q] : v[q], send = b4 ? v[q] : v[4 + q];
-                    k4[q] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-                }
-                float k2[2];
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const float keep = b3 ? k4[2 + q] : k4[q], send = b3 ? k4[q] : k4[2 + q];
-                    k2[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-                }
-                float kk = (b2 ? k2[1] : k2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? k2[0] : k2[1], 4);
-                kk += __shfl_xor_sync(0xffffffffu, kk, 2);
-                kk += __shfl_xor_sync(0xffffffffu, kk, 1);
-                const int r = (b4 ? 4 : 0) + (b3 ? 2 : 0) + (b2 ? 1 : 0);
-                if ((lane & 3) == 0 && r8 + r < nrows) {
-                    const float yv = kk * s.sh[p];
-                    s.y[p * pl.rows_pc + r8 + r] = yv;
-                    if (a.y) a.y[static_cast<int64_t>(p) * H + n0 + r8 + r] = yv;
+                if (MODE == DecodeMode::kForward) {
+                    const float yv = acc * s.sh[p];
+                    s.y[p * pl.rows_pc + r] = yv;
+                    if (a.y) a.y[static_cast<int64_t>(p) * H + n0 + r] = yv;
                 }
             }
         }
@@ -749,7 +755,7 @@ bool decode_shape_supported(int64_t H, int64_t I) {
 // Shared-memory plan of one launch (host side; the kernel reads the offsets).
 bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t k, int64_t g, int64_t n_pairs,
                  DecodeMode mode, int grid, int max_smem, DecodePlan* out) {
-    if (!decode_shape_supported(H, I) || g % 64 != 0 || g > 512 || E > kMaxExperts) return false;
+    if (!decode_shape_supported(H, I) || g % 64 != 0 || g > 512 || (I / g) % 4 != 0 || E > kMaxExperts) return false;
     const int64_t rows = mode == DecodeMode::kForward ? T * k : n_pairs;
     const int64_t Sx = mode == DecodeMode::kForward ? S : 0;
     const int64_t P = rows + T * Sx;
@@ -782,8 +788,14 @@ bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t 
     pl.off_y = take(mode == DecodeMode::kForward ? 4 * P * pl.rows_pc : 0, 16);
     pl.off_cand_v = take(mode == DecodeMode::kForward ? 4 * T * 8 * k : 0, 16);
     pl.off_cand_e = take(mode == DecodeMode::kForward ? 4 * T * 8 * k : 0, 16);
-    pl.smem_bytes = static_cast<int>(align_up(o, 128));
-    if (pl.smem_bytes > max_smem) return false;
+    pl.off_w2s = static_cast<int>(align_up(o, 128));
+    const size_t slot_bytes =
+        static_cast<size_t>(pl.rows_pc) * (I / 2 + 16) + static_cast<size_t>(pl.rows_pc) * (I / g) * 4;
+    const size_t fixed = pl.off_w2s;
+    if (fixed > static_cast<size_t>(max_smem)) return false;
+    const int64_t fit = mode == DecodeMode::kForward ? static_cast<int64_t>((max_smem - fixed) / slot_bytes) : 0;
+    pl.smem_slots = static_cast<int>(std::min<int64_t>(fit, MS));
+    pl.smem_bytes = static_cast<int>(fixed + pl.smem_slots * slot_bytes);
     *out = pl;
     return true;
 }
@@ -805,7 +817,8 @@ int decode_max_smem() {
 
 cudaError_t launch_decode(DecodeMode mode, const DecodeArgs& a, const DecodePlan& pl, int grid, cudaStream_t st) {
     if (mode == DecodeMode::kForward) {
-        cudaError_t e = cudaMemsetAsync(a.hdr, 0, 16, st);  // status and barrier counters
+        // status, barrier counters and the per-slot counters that follow the header
+        cudaError_t e = cudaMemsetAsync(a.hdr, 0, sizeof(Header) + sizeof(uint32_t) * kFlagWords, st);
         if (e != cudaSuccess) return e;
     }
     const int p1 = a.H / 2048, p2 = a.I / 512;

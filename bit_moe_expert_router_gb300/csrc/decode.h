@@ -6,7 +6,7 @@
 namespace moe {
 
 constexpr int kDecodeMaxT = 32;        // tokens per launch
-constexpr int kDecodeMaxPairs = 512;   // routed (or listed) pair rows per launch
+constexpr int kDecodeMaxPairs = 512;   // routed (or listed) pair rows per launch (< kFlagWords slots)
 constexpr int kMaxI = 2048;            // expert intermediate size (I / 512 in {1, 3})
 
 enum class DecodeMode { kForward, kGemm1Partials, kGemm2Partials };
@@ -31,6 +31,9 @@ struct DecodeArgs {
     int32_t* p2;             // [n_pairs][H][I/g]
     // workspace
     Header* hdr;
+    uint32_t* flags;         // [kFlagWords] per-slot counters, cleared before the launch
+    int8_t* hq_g;            // [P][I] requantised rows (split layout)
+    float* sh_g;             // [P] their scales
     float* h;                // [P][I]
     uint32_t* amax;          // [P] row maxima (debug copies; may be null)
     float* y;                // [P][H] (debug copies; may be null)
@@ -39,9 +42,10 @@ struct DecodeArgs {
 // Byte offsets of the shared-memory arrays of one launch.
 struct DecodePlan {
     int rows_pc;      // down-projection output rows per CTA
+    int smem_slots;   // slots whose down-projection slice is staged in shared memory
     int smem_bytes;
     int off_ids, off_wts, off_pos, off_pair_of, off_row_tok, off_slot_e, off_slot_row0, off_slot_cnt, off_slot_cum,
-        off_n_slots, off_xs, off_sh, off_x, off_hq, off_y, off_cand_v, off_cand_e;
+        off_n_slots, off_xs, off_sh, off_x, off_hq, off_y, off_cand_v, off_cand_e, off_w2s;
 };
 
 bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t k, int64_t g, int64_t n_pairs,
