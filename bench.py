@@ -49,6 +49,8 @@ def _args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--banks", type=int, default=N_BANKS,
+                   help="bank copies rotated between steps (fewer: a smaller case for profiler captures)")
     return p.parse_args()
 
 
@@ -152,8 +154,9 @@ def run_ours(a):
     d = binding.dims_of(w.T, w.H, w.I, w.E, w.S, w.top_k, w.group)
 
     bank = synth.make_bank(w)
+    bank_mb = sum(x.nbytes for x in (bank.w13, bank.s13, bank.w2, bank.s2)) / 1e6
     banks = []
-    for _ in range(N_BANKS):
+    for _ in range(a.banks):
         banks.append(tuple(torch.from_numpy(x).to(dev) for x in (bank.w13, bank.s13, bank.w2, bank.s2)))
     batches = [synth.make_tokens(w, batch=rank * N_BATCHES + b) for b in range(N_BATCHES)]
     dev_batches = [tuple(torch.from_numpy(x).to(dev) for x in (t.x_q, t.x_scale, t.logits)) for t in batches]
@@ -166,7 +169,7 @@ def run_ours(a):
 
     def step(i):
         x_q, x_s, lg = dev_batches[i % N_BATCHES]
-        w13, s13, w2, s2 = banks[i % N_BANKS]
+        w13, s13, w2, s2 = banks[i % len(banks)]
         binding.moe_w4a8_forward(x_q, x_s, lg, w13, s13, w2, s2, d, out, ws)
 
     stream = torch.cuda.Stream(dev)
@@ -237,7 +240,7 @@ def run_ours(a):
     def e2e_step(i):
         for src, dst in zip(host_in[i % N_BATCHES], dx):
             dst.copy_(src, non_blocking=True)
-        w13, s13, w2, s2 = banks[i % N_BANKS]
+        w13, s13, w2, s2 = banks[i % len(banks)]
         binding.moe_w4a8_forward(dx[0], dx[1], dx[2], w13, s13, w2, s2, d, out, ws)
         host_out.copy_(out, non_blocking=True)
 
@@ -273,7 +276,7 @@ def run_ours(a):
         "data": "synthetic (seeded generator: bf16 N(0,1) activations -> int8, N(0,0.02) weights -> int4 g128)",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "n_shared": w.S, "top_k": w.top_k,
                    "group": w.group, "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: {N_BANKS} bank copies x 857 MB and {N_BATCHES} token batches rotated",
+                   "l2": f"inputs larger than L2: {len(banks)} bank copies x {bank_mb:.0f} MB and {N_BATCHES} token batches rotated",
                    "timing": f"CUDA graph of {GRAPH_STEPS} steps replayed; events on the launching stream"},
         "plain_launch_ms_per_step": plain_ms_per_step,
         "e2e": {"value": w.T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,

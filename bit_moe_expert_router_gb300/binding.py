@@ -14,8 +14,8 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_w4a8.so")
-ABI_VERSION = 2
-ENGINE_AUTO, ENGINE_GROUPED, ENGINE_DECODE = -1, 0, 1
+ABI_VERSION = 3
+ENGINE_AUTO, ENGINE_GROUPED, ENGINE_DECODE, ENGINE_TCGEN05 = -1, 0, 1, 2
 NOALLOC_SCRATCH_BYTES = 16 << 20
 _lib = None
 
@@ -52,6 +52,8 @@ def _load():
     lib.moe_w4a8_last_error.restype = ctypes.c_char_p
     lib.moe_w4a8_workspace_size.argtypes = [dp]
     lib.moe_w4a8_workspace_size.restype = sz
+    lib.moe_w4a8_partials_workspace_size.argtypes = [dp, i64]
+    lib.moe_w4a8_partials_workspace_size.restype = sz
     lib.moe_w4a8_forward.argtypes = [p, p, p, p, p, p, p, dp, p, p, sz, p]
     ci = ctypes.c_int
     lib.moe_w4a8_forward_debug.argtypes = [p, p, p, p, p, p, p, dp, p, p, p, p, ci, p, sz, p]
@@ -112,7 +114,7 @@ def moe_w4a8_status_string(status: int) -> str:
 
 
 def moe_w4a8_engine_for(d: Dims) -> int:
-    """ENGINE_DECODE or ENGINE_GROUPED: what moe_w4a8_forward runs for these sizes on the current device."""
+    """ENGINE_DECODE, ENGINE_TCGEN05 or ENGINE_GROUPED: what moe_w4a8_forward runs for these sizes on the current device."""
     return _load().moe_w4a8_engine_for(ctypes.byref(d))
 
 
@@ -123,9 +125,15 @@ def moe_w4a8_workspace_size(d: Dims) -> int:
     return n
 
 
-def partials_workspace_size(d: Dims, n_pairs: int) -> int:
+def moe_w4a8_partials_workspace_size(d: Dims, n_pairs: int) -> int:
     """Workspace of moe_w4a8_gemm{1,2}_partials for n_pairs pairs."""
-    return moe_w4a8_workspace_size(Dims(max(n_pairs, 1), d.H, d.I, d.E + d.n_shared, 0, 1, d.group))
+    n = _load().moe_w4a8_partials_workspace_size(ctypes.byref(d), n_pairs)
+    if n == 0:
+        raise MoeError("moe_w4a8_partials_workspace_size", 1)
+    return n
+
+
+partials_workspace_size = moe_w4a8_partials_workspace_size
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:

@@ -1,14 +1,17 @@
 // C ABI of the routed-expert W4A8 MoE layer: argument checks, workspace
-// carving and the launch sequence.  Host code only; every step of the layer
-// runs in the kernels of route.cu and gemm_mma.cu.
+// carving, engine choice and the launch sequences.  Host code only; every
+// step of the layer runs in the kernels of route.cu, gemm_mma.cu, decode.cu
+// and prefill_tc.cu.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <mutex>
 
 #include "decode.h"
 #include "kernels.h"
 #include "moe_w4a8.h"
+#include "prefill.h"
 
 #define MOE_API extern "C" __attribute__((visibility("default")))
 
@@ -39,6 +42,13 @@ int check_ptrs(std::initializer_list<const void*> ptrs) {
 
 WsLayout layout_of(const moe_dims_t* d) { return moe::ws_layout(d->T, d->H, d->I, d->E, d->n_shared, d->top_k); }
 
+// Workspace of the partials entry points: the grouping of n_pairs pairs
+// over E + S slots, plus fp16 copies of the T activation rows.
+WsLayout partials_layout(const moe_dims_t* d, int64_t n_pairs) {
+    return moe::ws_layout(std::max<int64_t>(n_pairs, 1), d->H, d->I, d->E + d->n_shared, 0, 1, d->T);
+}
+
+
 int check_ws(const WsLayout& L, const void* ws, size_t bytes) {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
     if (bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -63,18 +73,17 @@ int cuda_status(cudaError_t e, const char* what) {
 struct Views {
     moe::Header* hdr;
     uint32_t* flags;
-    int8_t* hq;
     float* sh;
     int32_t *ids, *seg_cnt, *seg_off, *perm, *inv, *row_token, *chunk_counts, *tile_slot, *tile_row0;
     float *wts, *h, *y;
     uint32_t* amax;
+    __half *x16, *h16;
 };
 
 Views views(void* ws, const WsLayout& L) {
     Views v;
     v.hdr = moe::ws_at<moe::Header>(ws, L.hdr);
     v.flags = moe::ws_at<uint32_t>(ws, L.flags);
-    v.hq = moe::ws_at<int8_t>(ws, L.hq);
     v.sh = moe::ws_at<float>(ws, L.sh);
     v.ids = moe::ws_at<int32_t>(ws, L.ids);
     v.wts = moe::ws_at<float>(ws, L.wts);
@@ -89,6 +98,8 @@ Views views(void* ws, const WsLayout& L) {
     v.amax = moe::ws_at<uint32_t>(ws, L.amax);
     v.h = moe::ws_at<float>(ws, L.h);
     v.y = moe::ws_at<float>(ws, L.y);
+    v.x16 = moe::ws_at<__half>(ws, L.x16);
+    v.h16 = moe::ws_at<__half>(ws, L.h16);
     return v;
 }
 
@@ -142,9 +153,7 @@ int run_decode(const int8_t* x_q, const float* x_scale, const float* logits, con
     a.g = static_cast<int>(d->group);
     a.out = out;
     a.hdr = v.hdr;
-    a.flags = v.flags;
-    a.hq_g = v.hq;
-    a.sh_g = v.sh;
+    a.row_max = v.flags;
     a.h = v.h;
     a.amax = v.amax;
     a.y = y_debug;
@@ -152,18 +161,68 @@ int run_decode(const int8_t* x_q, const float* x_scale, const float* logits, con
     return MOE_OK;
 }
 
+int combine_out(const moe_dims_t* d, float* out, const WsLayout& L, const Views& v, float* y_debug, cudaStream_t st);
+
+bool tc_fits(const moe_dims_t* d) {
+    return moe::tc_supported(d->H, d->I, d->group) && d->E + d->n_shared <= moe::kTcMaxSlots;
+}
+
+moe::TcArgs tc_args(const uint8_t* w, const float* ws, int64_t rows_per_slot, int64_t K, const moe_dims_t* d,
+                    const __half* b, const int32_t* b_row, int64_t b_rows, const float* b_scale, const Views& v,
+                    int n_slots) {
+    moe::TcArgs a{};
+    a.w = w;
+    a.ws = ws;
+    a.rows_per_slot = rows_per_slot;
+    a.K = K;
+    a.g = static_cast<int>(d->group);
+    a.I = d->I;
+    a.H = d->H;
+    a.b = b;
+    a.b_row = b_row;
+    a.b_rows = b_rows;
+    a.b_scale = b_scale;
+    a.seg_off = v.seg_off;
+    a.seg_cnt = v.seg_cnt;
+    a.n_slots = n_slots;
+    a.hdr = v.hdr;
+    return a;
+}
+
+// gemm1 + act, requant, gemm2 on the tcgen05 engine (routing and grouping done).
+int run_tc_gemms(const int8_t* x_q, const float* x_scale, const uint8_t* w13, const float* s13, const uint8_t* w2,
+                 const float* s2, const moe_dims_t* d, const WsLayout& L, const Views& v, cudaStream_t st) {
+    const int n_slots = static_cast<int>(d->E + d->n_shared);
+    MOE_CUDA(moe::launch_prep_x16(x_q, d->T, d->H, v.x16, st));
+    moe::TcArgs g1 = tc_args(w13, s13, 2 * d->I, d->H, d, v.x16, v.row_token, d->T, x_scale, v, n_slots);
+    g1.h = v.h;
+    g1.amax = v.amax;
+    MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kGateUp, g1, st));
+    MOE_CUDA(moe::launch_prep_h16(v.h, v.amax, nullptr, L.P, d->I, v.h16, v.sh, st));
+    moe::TcArgs g2 = tc_args(w2, s2, d->H, d->I, d, v.h16, nullptr, L.P, v.sh, v, n_slots);
+    g2.y = v.y;
+    MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kDown, g2, st));
+    return MOE_OK;
+}
+
 // route + permute + gemm1 + gemm2 + combine on the workspace views.
 int run_layer(const int8_t* x_q, const float* x_scale, const float* logits, const uint8_t* w13, const float* s13,
               const uint8_t* w2, const float* s2, const moe_dims_t* d, float* out, const WsLayout& L, const Views& v,
               cudaStream_t st, int engine = MOE_ENGINE_AUTO, float* y_debug = nullptr) {
-    if (engine != MOE_ENGINE_GROUPED) {
+    if (engine == MOE_ENGINE_AUTO || engine == MOE_ENGINE_DECODE) {
         moe::DecodePlan pl;
         if (decode_forward_plan(d, &pl))
             return run_decode(x_q, x_scale, logits, w13, s13, w2, s2, d, out, v, pl, y_debug, st);
         if (engine == MOE_ENGINE_DECODE) return MOE_ERR_UNSUPPORTED;
     }
+    const bool tc = engine == MOE_ENGINE_TCGEN05 || (engine == MOE_ENGINE_AUTO && tc_fits(d));
+    if (tc && !tc_fits(d)) return MOE_ERR_UNSUPPORTED;
     MOE_CUDA(moe::launch_route_topk(logits, d->T, d->E, d->top_k, v.ids, v.wts, st));
     MOE_CUDA(moe::launch_sort(sort_args(v, v.ids, d->T, d->top_k, d->E, d->n_shared, L.P), st));
+    if (tc) {
+        MOE_TRY(run_tc_gemms(x_q, x_scale, w13, s13, w2, s2, d, L, v, st));
+        return combine_out(d, out, L, v, y_debug, st);
+    }
 
     moe::Gemm1Args g1{};
     g1.x_q = x_q;
@@ -199,7 +258,10 @@ int run_layer(const int8_t* x_q, const float* x_scale, const float* logits, cons
     g2.hdr = v.hdr;
     g2.y = v.y;
     MOE_CUDA(moe::launch_gemm2(moe::Gemm2Mode::kOutput, g2, static_cast<int>(L.max_tiles), st));
+    return combine_out(d, out, L, v, y_debug, st);
+}
 
+int combine_out(const moe_dims_t* d, float* out, const WsLayout& L, const Views& v, float* y_debug, cudaStream_t st) {
     moe::CombineArgs c{};
     c.y = v.y;
     c.wts = v.wts;
@@ -237,10 +299,16 @@ MOE_API size_t moe_w4a8_workspace_size(const moe_dims_t* d) {
     return layout_of(d).total;
 }
 
+MOE_API size_t moe_w4a8_partials_workspace_size(const moe_dims_t* d, int64_t n_pairs) {
+    if (check_dims(d) != MOE_OK || n_pairs < 0) return 0;
+    return partials_layout(d, n_pairs).total;
+}
+
 MOE_API int moe_w4a8_engine_for(const moe_dims_t* d) {
     if (check_dims(d) != MOE_OK) return -1;
     moe::DecodePlan pl;
-    return decode_forward_plan(d, &pl) ? MOE_ENGINE_DECODE : MOE_ENGINE_GROUPED;
+    if (decode_forward_plan(d, &pl)) return MOE_ENGINE_DECODE;
+    return tc_fits(d) ? MOE_ENGINE_TCGEN05 : MOE_ENGINE_GROUPED;
 }
 
 MOE_API int moe_w4a8_forward(const int8_t* x_q, const float* x_scale, const float* router_logits,
@@ -271,7 +339,7 @@ MOE_API int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, cons
     MOE_TRY(check_ws(L, workspace, workspace_bytes));
     const Views v = views(workspace, L);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (engine < MOE_ENGINE_AUTO || engine > MOE_ENGINE_DECODE) return MOE_ERR_INVALID_ARG;
+    if (engine < MOE_ENGINE_AUTO || engine > MOE_ENGINE_TCGEN05) return MOE_ERR_INVALID_ARG;
     MOE_TRY(run_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out, L, v, st,
                       engine, y));
     if (h_q || s_h) MOE_CUDA(moe::launch_requant_copy(v.h, v.amax, L.P, d->I, h_q, s_h, st));
@@ -303,11 +371,10 @@ namespace {
 // counting sort over E + S slots with one "expert" per pair.
 int group_pairs(const moe_dims_t* d, const int32_t* pair_token, const int32_t* pair_slot, int64_t n_pairs,
                 void* workspace, size_t workspace_bytes, cudaStream_t st, WsLayout* L_out, Views* v_out) {
-    const int64_t slots = d->E + d->n_shared;
-    const WsLayout L = moe::ws_layout(n_pairs, d->H, d->I, slots, 0, 1);
+    const WsLayout L = partials_layout(d, n_pairs);
     MOE_TRY(check_ws(L, workspace, workspace_bytes));
     Views v = views(workspace, L);
-    moe::SortArgs a = sort_args(v, pair_slot, n_pairs, 1, slots, 0, L.P);
+    moe::SortArgs a = sort_args(v, pair_slot, n_pairs, 1, d->E + d->n_shared, 0, L.P);
     a.tok_map = pair_token;
     a.amax = nullptr;
     MOE_CUDA(moe::launch_sort(a, st));
@@ -326,7 +393,7 @@ int decode_partials(moe::DecodeMode mode, const moe_dims_t* d, const int8_t* x_o
     if (!moe::decode_plan(T, d->H, d->I, d->E, 0, 1, d->group, n_pairs, mode, moe::decode_grid(),
                           moe::decode_max_smem(), &pl))
         return MOE_ERR_UNSUPPORTED;
-    const WsLayout L = moe::ws_layout(n_pairs, d->H, d->I, d->E + d->n_shared, 0, 1);
+    const WsLayout L = partials_layout(d, n_pairs);
     MOE_TRY(check_ws(L, workspace, workspace_bytes));
     Views v = views(workspace, L);
     moe::DecodeArgs a{};
@@ -356,7 +423,7 @@ MOE_API int moe_w4a8_gemm1_partials(const int8_t* x_q, const uint8_t* w13_packed
                                     int engine, void* workspace, size_t workspace_bytes, void* stream) {
     MOE_TRY(check_dims(d));
     if (n_pairs < 0 || n_pairs >= (int64_t(1) << 24)) return MOE_ERR_INVALID_ARG;
-    if (engine < MOE_ENGINE_AUTO || engine > MOE_ENGINE_DECODE) return MOE_ERR_INVALID_ARG;
+    if (engine < MOE_ENGINE_AUTO || engine > MOE_ENGINE_TCGEN05) return MOE_ERR_INVALID_ARG;
     if (n_pairs == 0) return MOE_OK;
     if (d->E + d->n_shared > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED;
     MOE_TRY(check_ptrs({x_q, w13_packed, pair_token, pair_slot, p1}));
@@ -367,6 +434,15 @@ MOE_API int moe_w4a8_gemm1_partials(const int8_t* x_q, const uint8_t* w13_packed
     WsLayout L;
     Views v;
     MOE_TRY(group_pairs(d, pair_token, pair_slot, n_pairs, workspace, workspace_bytes, st, &L, &v));
+    const int n_slots = static_cast<int>(d->E + d->n_shared);
+    if (engine == MOE_ENGINE_TCGEN05) {
+        if (!tc_fits(d)) return MOE_ERR_UNSUPPORTED;
+        MOE_CUDA(moe::launch_prep_x16(x_q, d->T, d->H, v.x16, st));
+        moe::TcArgs a = tc_args(w13_packed, nullptr, 2 * d->I, d->H, d, v.x16, v.row_token, d->T, nullptr, v, n_slots);
+        a.partials = p1;
+        MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kGateUpPartials, a, st));
+        return MOE_OK;
+    }
     moe::Gemm1Args g1{};
     g1.x_q = x_q;
     g1.w13 = w13_packed;
@@ -390,7 +466,7 @@ MOE_API int moe_w4a8_gemm2_partials(const int8_t* h_q, const uint8_t* w2_packed,
                                     void* workspace, size_t workspace_bytes, void* stream) {
     MOE_TRY(check_dims(d));
     if (n_pairs < 0 || n_pairs >= (int64_t(1) << 24)) return MOE_ERR_INVALID_ARG;
-    if (engine < MOE_ENGINE_AUTO || engine > MOE_ENGINE_DECODE) return MOE_ERR_INVALID_ARG;
+    if (engine < MOE_ENGINE_AUTO || engine > MOE_ENGINE_TCGEN05) return MOE_ERR_INVALID_ARG;
     if (n_pairs == 0) return MOE_OK;
     if (d->E + d->n_shared > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED;
     MOE_TRY(check_ptrs({h_q, w2_packed, pair_slot, p2}));
@@ -401,6 +477,15 @@ MOE_API int moe_w4a8_gemm2_partials(const int8_t* h_q, const uint8_t* w2_packed,
     WsLayout L;
     Views v;
     MOE_TRY(group_pairs(d, pair_slot, pair_slot, n_pairs, workspace, workspace_bytes, st, &L, &v));
+    const int n_slots = static_cast<int>(d->E + d->n_shared);
+    if (engine == MOE_ENGINE_TCGEN05) {
+        if (!tc_fits(d)) return MOE_ERR_UNSUPPORTED;
+        MOE_CUDA(moe::launch_prep_h16(nullptr, nullptr, h_q, n_pairs, d->I, v.h16, nullptr, st));
+        moe::TcArgs a = tc_args(w2_packed, nullptr, d->H, d->I, d, v.h16, nullptr, n_pairs, nullptr, v, n_slots);
+        a.partials = p2;
+        MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kDownPartials, a, st));
+        return MOE_OK;
+    }
     moe::Gemm2Args g2{};
     g2.h_q = h_q;
     g2.w2 = w2_packed;

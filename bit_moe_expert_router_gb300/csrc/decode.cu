@@ -10,28 +10,28 @@
 //   phase 0  every CTA routes all T tokens itself (the same deterministic
 //            result in every CTA, so nothing is exchanged), sorts the pairs
 //            stably by expert into pair rows, builds the slot table (touched
-//            experts ascending, then the shared experts), stages the
-//            activations in shared memory and prefetches its own slice of
-//            the down-projection bank (its output rows of every touched
-//            slot) into L2 so that phase 2 reads it from there.
+//            experts ascending, then the shared experts) and stages the
+//            activations in shared memory.
 //   phase 1  gate/up projection with dp4a on the CUDA cores: units of two
 //            intermediate indices (2 gate rows + the 2 matching up rows) of
-//            one slot; the units are split into contiguous ranges of equal
-//            cost over all warps (cost = streaming + per-token work, so the
-//            always-on shared expert's multi-token units weigh more).  A warp
+//            one slot, dealt round-robin over all warps of the grid.  A warp
 //            keeps up to four units of 16-byte loads in flight in
 //            registers; each lane covers a 64-value K piece, folds its exact
 //            int32 piece sum with the piece's group scale, and a 4-row
 //            reduce-scatter across the warp (6 shuffles) gives the row sums;
-//            h = SiLU(G_gate) * G_up goes to the workspace.
+//            h = SiLU(G_gate) * G_up goes to the workspace and |h| into the
+//            row's running maximum (fire-and-forget atomic max).  Meanwhile
+//            each CTA copies its slice of the down-projection bank (its
+//            output rows of every touched slot) into shared memory, or warms
+//            it in L2 where shared memory runs out.
 //   barrier  one grid-wide barrier (bounded wait; on timeout the status
 //            word records it and the CTAs leave).
-//   phase 2  every CTA requantises all pair rows (row max -> s_h, RNE codes)
-//            into shared memory, runs the down projection for its output
-//            rows of every touched slot (units of 8 rows, 16-value K piece
-//            per lane, 8-row reduce-scatter), and combines
+//   phase 2  every CTA requantises all pair rows from h and the row maxima
+//            (s_h = max/127, RNE codes) into shared memory, runs the down
+//            projection for its output rows of every touched slot (one lane
+//            per (slot, row), whole-K dot product), and combines
 //            out[t][n] = sum_j w[t][j] Y[(t,j)][n] + shared in a fixed order:
-//            no atomics, deterministic.
+//            no atomics on the output, deterministic.
 //
 // The same kernel serves the partials entry points (phase 1 or phase 2
 // alone, pairs given as a list instead of routed); there each K group's
@@ -54,6 +54,7 @@ namespace moe {
 namespace {
 
 constexpr int kThreadsD = 256;
+static_assert(kDecodeMaxPairs + kDecodeMaxT * kMaxShared <= kFlagWords, "row maxima live in the cleared words");
 constexpr int kWarpsD = kThreadsD / 32;
 
 // Bounded waits: give up after about one second of wall-clock time (the
@@ -330,54 +331,6 @@ __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
     return s;
 }
 
-// Requantise the pair rows of one slot (all its units are done): row max
-// -> s_h, RNE codes, stored split even|odd to hq_g, scales to sh_g.  One
-// warp; lane owns 16 consecutive values of every 512-value chunk.
-template <int PC2>
-__device__ void requant_slot(const DecodeArgs& a, int row0, int cnt) {
-    const int lane = threadIdx.x & 31, I = a.I;
-    for (int m = 0; m < cnt; ++m) {
-        const int p = row0 + m;
-        const float* hrow = a.h + static_cast<int64_t>(p) * I;
-        float v[PC2][16];
-        float mx = 0.f;
-#pragma unroll
-        for (int c = 0; c < PC2; ++c)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 f = __ldcg(reinterpret_cast<const float4*>(hrow + 16 * lane + 512 * c + 4 * q));
-                v[c][4 * q] = f.x;
-                v[c][4 * q + 1] = f.y;
-                v[c][4 * q + 2] = f.z;
-                v[c][4 * q + 3] = f.w;
-            }
-#pragma unroll
-        for (int c = 0; c < PC2; ++c)
-#pragma unroll
-            for (int q = 0; q < 16; ++q) mx = fmaxf(mx, fabsf(v[c][q]));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const float sc = requant_scale(__float_as_uint(mx));
-        const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
-#pragma unroll
-        for (int c = 0; c < PC2; ++c) {
-            uint32_t wds[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                wds[q] = (requant_code_fast(v[c][4 * q], sc, rs) & 0xFF) |
-                         ((requant_code_fast(v[c][4 * q + 1], sc, rs) & 0xFF) << 8) |
-                         ((requant_code_fast(v[c][4 * q + 2], sc, rs) & 0xFF) << 16) |
-                         ((static_cast<uint32_t>(requant_code_fast(v[c][4 * q + 3], sc, rs)) & 0xFF) << 24);
-            *reinterpret_cast<uint4*>(a.hq_g + static_cast<int64_t>(p) * I + 16 * lane + 512 * c) =
-                split16(make_uint4(wds[0], wds[1], wds[2], wds[3]));
-        }
-        if (lane == 0) {
-            a.sh_g[p] = sc;
-            if (a.amax) a.amax[p] = __float_as_uint(mx);
-        }
-    }
-}
-
 // PC1 = H / 2048 (64-value pieces per lane per row), PC2 = I / 512 (16-value pieces per lane per row).
 template <DecodeMode MODE, int PC1, int PC2>
 __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, DecodePlan pl) {
@@ -585,26 +538,13 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                     const float upv = __shfl_xor_sync(0xffffffffu, kk, 16);  // up row of the same index
                     if (!b4 && (lane & 7) == 0) {
                         const float xs = s.xs[t];
-                        a.h[static_cast<int64_t>(prow) * I + 2 * ip + (b3 ? 1 : 0)] = silu_f32(kk * xs) * (upv * xs);
+                        const float hv = silu_f32(kk * xs) * (upv * xs);
+                        a.h[static_cast<int64_t>(prow) * I + 2 * ip + (b3 ? 1 : 0)] = hv;
+                        atomicMax(a.row_max + prow, __float_as_uint(fabsf(hv)));
                     }
                 }
                 if (un + DEPTH < nun) issue(un + DEPTH, d);  // refill this ring slot
                 if (MODE == DecodeMode::kForward) stage_some(stage_budget);
-            }
-        }
-        if (MODE == DecodeMode::kForward) {
-            // count this warp's finished units per slot (one fence for all of
-            // them); the warp that completes a slot requantises its pair rows
-            __threadfence();
-            __syncwarp();
-            for (int un = 0; un < nun; ++un) {
-                const int u = (gw + un * W) / upe;
-                int last = 0;
-                if (lane == 0) last = atomicAdd(&a.flags[u], 1u) + 1 == static_cast<unsigned>(upe);
-                if (__shfl_sync(0xffffffffu, last, 0)) {
-                    __threadfence();
-                    requant_slot<PC2>(a, s.slot_row0[u], s.slot_cnt[u]);
-                }
             }
         }
     }
@@ -621,21 +561,51 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     // ---------------------------------------------------------------- phase 2
     const int P = n_rows + T * S;
     {
-        // (a) the requantised rows (already split even|odd) into shared memory
+        // (a) the requantised rows, split even|odd, into shared memory: every
+        // CTA requantises all P rows itself from h (L2) and the row maxima
         const int per_row = I / 16;
-        const int8_t* src = MODE == DecodeMode::kForward ? a.hq_g : a.h_q_in;
-        for (int o = tid; o < P * per_row; o += kThreadsD) {
-            const int p = o / per_row, c = o % per_row;
-            if (MODE == DecodeMode::kForward) {
-                cp_async16(s.hq + p * HQS + 16 * c, src + static_cast<int64_t>(p) * I + 16 * c);
-            } else {
-                const uint4 v = *reinterpret_cast<const uint4*>(src + static_cast<int64_t>(p) * I + 16 * c);
+        if (MODE == DecodeMode::kForward) {
+            for (int p = tid; p < P; p += kThreadsD) {
+                const uint32_t mb = __ldcg(a.row_max + p);
+                s.sh[p] = requant_scale(mb);
+                if (a.amax && blockIdx.x == 0) a.amax[p] = mb;
+            }
+            __syncthreads();
+            const int n_chunks = P * per_row;
+            for (int o0 = tid; o0 < n_chunks; o0 += 2 * kThreadsD) {
+                float4 f[2][4];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    const int o = min(o0 + b * kThreadsD, n_chunks - 1);
+                    const float4* src = reinterpret_cast<const float4*>(a.h + static_cast<int64_t>(o / per_row) * I +
+                                                                        16 * (o % per_row));
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) f[b][q] = __ldcg(src + q);
+                }
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    const int o = o0 + b * kThreadsD;
+                    if (o >= n_chunks) break;
+                    const int p = o / per_row, c = o % per_row;
+                    const float sc = s.sh[p];
+                    const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+                    uint32_t wds[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        wds[q] = (requant_code_fast(f[b][q].x, sc, rs) & 0xFF) |
+                                 ((requant_code_fast(f[b][q].y, sc, rs) & 0xFF) << 8) |
+                                 ((requant_code_fast(f[b][q].z, sc, rs) & 0xFF) << 16) |
+                                 ((static_cast<uint32_t>(requant_code_fast(f[b][q].w, sc, rs)) & 0xFF) << 24);
+                    *reinterpret_cast<uint4*>(s.hq + p * HQS + 16 * c) = split16(make_uint4(wds[0], wds[1], wds[2], wds[3]));
+                }
+            }
+        } else {
+            for (int o = tid; o < P * per_row; o += kThreadsD) {
+                const int p = o / per_row, c = o % per_row;
+                const uint4 v = *reinterpret_cast<const uint4*>(a.h_q_in + static_cast<int64_t>(p) * I + 16 * c);
                 *reinterpret_cast<uint4*>(s.hq + p * HQS + 16 * c) = split16(v);
             }
         }
-        if (MODE == DecodeMode::kForward)
-            for (int p = tid; p < P; p += kThreadsD) s.sh[p] = __ldcg(a.sh_g + p);
-        cp_async_commit();
     }
     cp_async_wait<0>();
     __syncthreads();

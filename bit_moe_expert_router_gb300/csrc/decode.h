@@ -31,9 +31,7 @@ struct DecodeArgs {
     int32_t* p2;             // [n_pairs][H][I/g]
     // workspace
     Header* hdr;
-    uint32_t* flags;         // [kFlagWords] per-slot counters, cleared before the launch
-    int8_t* hq_g;            // [P][I] requantised rows (split layout)
-    float* sh_g;             // [P] their scales
+    uint32_t* row_max;       // [P] running max |h| per pair row (float bits), cleared before the launch
     float* h;                // [P][I]
     uint32_t* amax;          // [P] row maxima (debug copies; may be null)
     float* y;                // [P][H] (debug copies; may be null)

@@ -1,0 +1,545 @@
+// Tensor-core (tcgen05) engine of the W4A8 MoE layer for large batches.
+//
+// The grouped expert projections are dense contractions once the tokens are
+// grouped per expert ("Two 96 GB Ascend cards run Qwen3.8 Flash-Next",
+// section 3: grouped expert projections on the matrix unit, blocked
+// reduction, W4A8, weights kept packed).  GB300 has no int8 tcgen05 MMA, so
+// the operands go to the fp16 MMA (kind::f16): int4 codes and int8 values
+// are exact in fp16, each product is exact in the fp32 accumulator and a
+// 128-value K group sums to |P| <= 128 * 127 * 8 < 2^24, so every group's
+// accumulator holds the exact int32 partial.  One group is accumulated per
+// TMEM buffer and folded into fp32 registers with its weight scale by the
+// epilogue warps while the tensor core fills the other buffer.
+//
+// Tile: M = 128 weight rows x N <= 128 tokens of one bank slot, one K
+// group (128 values) per pipeline stage, 3 stages in shared memory in the
+// 128-byte-swizzled K-major layout the MMA reads.  Gate/up tiles interleave
+// the rows (tile row 2j = gate row i, 2j + 1 = up row i, i = 64 m + j), so
+// the SiLU(gate) * up product pairs neighbouring lanes.  The MMA width N is
+// the token count of the tile rounded up to 16.  Persistent CTAs (one per
+// SM) walk the (slot, token tile, weight tile) items with the weight tile
+// fastest, so the CTAs working at one time share the token tile in L2.
+//
+// Nine warps: three of them share one SM sub-partition, whose 16K-register
+// file then caps a thread at 168 registers (the launch bound below).
+// Warp roles: warps 0-3 epilogue (TMEM lanes 32w..32w+31 = tile rows),
+// warps 4-7 producers (thread = tile row: unpack 64 packed bytes of its
+// weight row into fp16, cp.async its token row's 256 bytes), warp 8 issues
+// the MMAs (one thread) and owns the TMEM allocation.  Every wait is
+// bounded; a timeout sets the status word and every role leaves cleanly.
+//
+// K order: the weight unpack turns a packed word (codes 0..7) into fp16
+// pairs (0,4) (1,5) (2,6) (3,7); the token rows are converted to fp16 in
+// the same order by the prep kernels, so both operands agree on K.
+#include <math.h>
+
+#include <algorithm>
+#include <map>
+#include <mutex>
+
+#include "prefill.h"
+
+namespace moe {
+namespace {
+
+constexpr int kTcThreads = 288;
+constexpr int kNS = 3;
+constexpr int kTileN = 128;
+constexpr int kAtom = 16384;                 // 128 rows x 128 bytes
+constexpr int kStageA = 2 * kAtom, kStageB = 2 * kAtom, kStage = kStageA + kStageB;
+constexpr int kMaxSlotsTc = kTcMaxSlots + 1;
+constexpr int kSmemTc = kNS * kStage + 128 * 4 + 128 * 4 + (kMaxSlotsTc + 16) * 4 + 256 + 1024;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+struct Ctl {
+    volatile int* abort;
+    Header* hdr;
+};
+
+// Bounded wait for phase `parity` of `bar`; false if the CTA aborted or the
+// wait ran out (then the abort flag and the status word are set).
+__device__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctl& c) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31) == 31) {
+            if (*c.abort) return false;
+            const uint64_t t = global_ns();
+            if (t0 == 0) {
+                t0 = t;
+            } else if (t - t0 > kWaitNs) {
+                *c.abort = 1;
+                atomicOr(&c.hdr->status, kDevTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// kind::f16 instruction descriptor: fp32 accumulator, fp16 A and B, both
+// K-major, M = 128, N = n (a multiple of 16, at most 128).
+__device__ __forceinline__ uint32_t idesc_f16(int n) {
+    return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+        "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ld_nc16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Eight packed int4 codes (element e at bits 4e) -> fp16 pairs (0,4) (1,5) (2,6) (3,7).
+// A nibble n in offset binary (n ^ 8 = code + 8) placed in an fp16 0x6400 | n
+// is 1024 + code + 8; subtracting 1032 leaves the code exactly.
+__device__ __forceinline__ uint4 unpack_int4_f16(uint32_t w) {
+    const uint32_t o = w ^ 0x88888888u;
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+    uint32_t r[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t bits = ((o >> (4 * e)) & 0x000F000Fu) | 0x64006400u;
+        const __half2 hv = __hsub2(*reinterpret_cast<const __half2*>(&bits), bias);
+        r[e] = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+__device__ __forceinline__ uint32_t swz(int atom_row, int chunk) {  // byte offset in a 128 x 128 B atom
+    return static_cast<uint32_t>(atom_row * 128 + (((chunk & 7) ^ (atom_row & 7)) << 4));
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n)); }
+
+// Named barrier that also ORs a predicate over its threads: every thread gets the same answer.
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %3, 0;\n bar.red.or.pred q, %1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(id), "r"(n), "r"(v ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
+
+struct Item {
+    int slot, tt, mt, row0, ntok;
+};
+
+template <TcMode MODE>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_mt) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stages = smem;
+    float* colf = reinterpret_cast<float*>(smem + kNS * kStage);  // [128] B-row scales of the item
+    int* colp = reinterpret_cast<int*>(colf + 128);               // [128] pair rows of the item
+    int* prefix = colp + 128;                                     // [kMaxSlotsTc + 1] items before each slot
+    uint64_t* bars = reinterpret_cast<uint64_t*>(prefix + kMaxSlotsTc + 16);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + kNS;
+    uint64_t* accf = bars + 2 * kNS;
+    uint64_t* acce = accf + 2;
+    uint64_t* done = acce + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+    int* warp_sums = abort_flag + 1;  // [kTcThreads / 32 + 1]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr bool gateup = MODE == TcMode::kGateUp || MODE == TcMode::kGateUpPartials;
+    constexpr bool partials = MODE == TcMode::kGateUpPartials || MODE == TcMode::kDownPartials;
+    const int64_t K = a.K, rows_per_slot = a.rows_per_slot;
+    const int ksteps = static_cast<int>(K / 128), spg = a.g / 128, ngrp = static_cast<int>(K / a.g);
+    const Ctl ctl{abort_flag, a.hdr};
+
+    if (tid == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(full + s, 256);  // 128 producer arrivals + 128 cp.async completions
+            mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf + b, 1);
+            mbar_init(acce + b, 128);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp == 8) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tmem_holder)),
+                     "r"(256));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+    }
+    // items of each slot -> exclusive prefix (every CTA computes it)
+    {
+        const int per = (a.n_slots + kTcThreads - 1) / kTcThreads;
+        const int u0 = min(a.n_slots, tid * per), u1 = min(a.n_slots, (tid + 1) * per);
+        int local = 0;
+        for (int u = u0; u < u1; ++u) local += ((a.seg_cnt[u] + kTileN - 1) / kTileN) * n_mt;
+        int incl = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) warp_sums[warp] = incl;
+        __syncthreads();
+        if (tid == 0) {
+            int run = 0;
+            for (int w2 = 0; w2 < kTcThreads / 32; ++w2) {
+                const int v = warp_sums[w2];
+                warp_sums[w2] = run;
+                run += v;
+            }
+            warp_sums[kTcThreads / 32] = run;
+        }
+        __syncthreads();
+        int run = warp_sums[warp] + incl - local;
+        for (int u = u0; u < u1; ++u) {
+            prefix[u] = run;
+            run += ((a.seg_cnt[u] + kTileN - 1) / kTileN) * n_mt;
+        }
+        if (tid == 0) prefix[a.n_slots] = warp_sums[kTcThreads / 32];
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const int total = prefix[a.n_slots];
+
+    auto decode_item = [&](int item) {
+        int lo = 0, hi = a.n_slots;  // last slot whose first item is <= item
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (prefix[mid] <= item) lo = mid;
+            else hi = mid;
+        }
+        Item it;
+        it.slot = lo;
+        const int local = item - prefix[lo];
+        it.tt = local / n_mt;
+        it.mt = local % n_mt;
+        it.row0 = a.seg_off[lo] + kTileN * it.tt;
+        it.ntok = min(kTileN, a.seg_off[lo] + a.seg_cnt[lo] - it.row0);
+        return it;
+    };
+    // bank row of tile row r (gate/up: gate and up rows interleaved)
+    auto weight_row = [&](int mt, int r) -> int64_t {
+        if (gateup) return ((r & 1) ? a.I : 0) + 64 * mt + (r >> 1);
+        return static_cast<int64_t>(128) * mt + r;
+    };
+
+    if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ producers
+        const int pt = tid - 128;
+        int use = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+            const Item it = decode_item(item);
+            const uint8_t* asrc = a.w + (static_cast<int64_t>(it.slot) * rows_per_slot + weight_row(it.mt, pt)) * (K / 2);
+            int64_t brow = pt < it.ntok ? (a.b_row ? a.b_row[it.row0 + pt] : it.row0 + pt) : -1;
+            const bool bvalid = brow >= 0 && brow < a.b_rows;
+            const __half* bsrc = a.b + (bvalid ? brow : 0) * K;
+            for (int ks = 0; ks < ksteps; ++ks, ++use) {
+                const int s = use % kNS;
+                if (!wait_bar(empty + s, ((use / kNS) & 1) ^ 1, ctl)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* As = stages + s * kStage;
+                uint8_t* Bs = As + kStageA;
+#pragma unroll
+                for (int w = 0; w < 16; ++w)
+                    cp_async16(Bs + (w >> 3) * kAtom + swz(pt, w), bsrc + 128 * ks + 8 * w, bvalid ? 16 : 0);
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(full + s))
+                             : "memory");
+                const uint4* ap = reinterpret_cast<const uint4*>(asrc + 64 * ks);
+                uint4 raw[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) raw[q] = ld_nc16(ap + q);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t words[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        const int w = 4 * q + wi;
+                        *reinterpret_cast<uint4*>(As + (w >> 3) * kAtom + swz(pt, w)) = unpack_int4_f16(words[wi]);
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                mbar_arrive(full + s);
+            }
+        }
+        cp_async_wait<0>();
+    } else if (warp == 8) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int use = 0, grp = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+                const Item it = decode_item(item);
+                const uint32_t idesc = idesc_f16((it.ntok + 15) & ~15);
+                for (int ks = 0; ks < ksteps; ++ks, ++use) {
+                    const int s = use % kNS;
+                    const int sub = ks % spg;
+                    const int b = grp & 1;
+                    if (!wait_bar(full + s, (use / kNS) & 1, ctl) ||
+                        (sub == 0 && !wait_bar(acce + b, ((grp >> 1) & 1) ^ 1, ctl))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(stages + s * kStage), b0 = a0 + kStageA;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * kAtom + 32 * (kk & 3);
+                        mma_f16(tmem + b * 128, sdesc(a0 + off), sdesc(b0 + off), idesc, (sub > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(empty + s);
+                    if (sub == spg - 1) {
+                        mma_commit(accf + b);
+                        ++grp;
+                    }
+                }
+            }
+            mma_commit(done);  // arrives once every MMA issued above has completed
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(done, 0)) {
+                if (global_ns() - t0 > kWaitNs) {
+                    atomicOr(&a.hdr->status, kDevTimeout);
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int r = tid;  // TMEM lane = tile row
+        int grp = 0;
+        for (int item = blockIdx.x; item < total; item += gridDim.x) {
+            const Item it = decode_item(item);
+            if (r < it.ntok) {
+                const int p = it.row0 + r;
+                colp[r] = p;
+                if (!partials) colf[r] = gateup ? a.b_scale[a.b_row ? a.b_row[p] : p] : a.b_scale[p];
+            }
+            named_bar(1, 128);
+            const int64_t wrow = weight_row(it.mt, r);
+            const float* srow = a.ws + (static_cast<int64_t>(it.slot) * rows_per_slot + wrow) * ngrp;
+            float acc[kTileN];
+#pragma unroll
+            for (int c = 0; c < kTileN; ++c) acc[c] = 0.f;
+            bool ok = true;
+            for (int gq = 0; gq < ngrp; ++gq, ++grp) {
+                const int b = grp & 1;
+                const float sc = partials ? 0.f : __ldg(srow + gq);
+                if (!wait_bar(accf + b, (grp >> 1) & 1, ctl)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int i = 0; i < kTileN / 32; ++i) {
+                    if (32 * i >= it.ntok) break;
+                    uint32_t v[32];
+                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + b * 128 + 32 * i, v);
+                    if (partials) {
+                        int32_t* dst = a.partials + wrow * ngrp + gq;
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            if (32 * i + c < it.ntok)
+                                dst[static_cast<int64_t>(colp[32 * i + c]) * rows_per_slot * ngrp] =
+                                    __float2int_rn(__uint_as_float(v[c]));
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) acc[32 * i + c] = fmaf(__uint_as_float(v[c]), sc, acc[32 * i + c]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(acce + b);
+            }
+            if (ok && MODE == TcMode::kGateUp) {
+                const int64_t i = 64 * it.mt + (r >> 1);
+#pragma unroll
+                for (int c = 0; c < kTileN; ++c) {
+                    const float other = __shfl_xor_sync(0xffffffffu, acc[c], 1);  // up value (even lanes)
+                    float hv = 0.f;
+                    if (c < it.ntok && !(r & 1)) {
+                        const float xs = colf[c];
+                        hv = silu_f32(acc[c] * xs) * (other * xs);
+                        a.h[static_cast<int64_t>(colp[c]) * a.I + i] = hv;
+                    }
+                    const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
+                    if (lane == 0 && c < it.ntok) atomicMax(a.amax + colp[c], m);
+                }
+            } else if (ok && MODE == TcMode::kDown) {
+                const int64_t n = 128 * it.mt + r;
+#pragma unroll
+                for (int c = 0; c < kTileN; ++c)
+                    if (c < it.ntok) a.y[static_cast<int64_t>(colp[c]) * a.H + n] = acc[c] * colf[c];
+            }
+            // colf / colp are reused by the next item; leave together if any thread gave up
+            if (named_bar_or(1, 128, !ok)) break;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(256));
+    }
+}
+
+// x_q int8 -> fp16 in the engine's K order (pairs (0,4)(1,5)(2,6)(3,7) per 8 values).
+__global__ void prep_x16_kernel(const int8_t* __restrict__ x, int64_t n8, __half* __restrict__ out) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint2 v = *reinterpret_cast<const uint2*>(x + 8 * i);
+        const int8_t* b = reinterpret_cast<const int8_t*>(&v);
+        __half2 o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = __halves2half2(__int2half_rn(b[e]), __int2half_rn(b[e + 4]));
+        *reinterpret_cast<uint4*>(out + 8 * i) = *reinterpret_cast<const uint4*>(o);
+    }
+}
+
+// h fp32 -> requantised codes (fp32 decision, IEEE division) as fp16 in the engine's K order, plus s_h.
+__global__ void prep_h16_kernel(const float* __restrict__ h, const uint32_t* __restrict__ amax,
+                                const int8_t* __restrict__ hq_in, int64_t P, int64_t I, __half* __restrict__ out,
+                                float* __restrict__ s_h) {
+    const int64_t n8 = P * I / 8;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row = (8 * i) / I;
+        int code[8];
+        if (amax) {
+            const float s = requant_scale(amax[row]);
+            const float4 f0 = *reinterpret_cast<const float4*>(h + 8 * i);
+            const float4 f1 = *reinterpret_cast<const float4*>(h + 8 * i + 4);
+            const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) code[e] = requant_code(f[e], s);
+            if ((8 * i) % I == 0 && s_h) s_h[row] = s;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) code[e] = hq_in[8 * i + e];
+        }
+        __half2 o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = __halves2half2(__int2half_rn(code[e]), __int2half_rn(code[e + 4]));
+        *reinterpret_cast<uint4*>(out + 8 * i) = *reinterpret_cast<const uint4*>(o);
+    }
+}
+
+template <TcMode MODE>
+cudaError_t launch_mode_tc(const TcArgs& a, int n_mt, cudaStream_t st) {
+    auto kern = tc_gemm_kernel<MODE>;
+    static std::mutex mu;
+    static std::map<int, bool> attr_set;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set.count(dev)) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+            if (e != cudaSuccess) return e;
+            attr_set[dev] = true;
+        }
+    }
+    kern<<<num_sms(), kTcThreads, kSmemTc, st>>>(a, n_mt);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(int64_t H, int64_t I, int64_t g) {
+    return g % 128 == 0 && H % 128 == 0 && I % 128 == 0 && H >= 128 && I >= 128;
+}
+
+cudaError_t launch_tc_gemm(TcMode mode, const TcArgs& a, cudaStream_t st) {
+    if (a.n_slots < 1 || a.n_slots > kTcMaxSlots) return cudaErrorInvalidValue;
+    const bool gateup = mode == TcMode::kGateUp || mode == TcMode::kGateUpPartials;
+    const int n_mt = static_cast<int>(gateup ? a.I / 64 : a.H / 128);
+    switch (mode) {
+        case TcMode::kGateUp: return launch_mode_tc<TcMode::kGateUp>(a, n_mt, st);
+        case TcMode::kDown: return launch_mode_tc<TcMode::kDown>(a, n_mt, st);
+        case TcMode::kGateUpPartials: return launch_mode_tc<TcMode::kGateUpPartials>(a, n_mt, st);
+        default: return launch_mode_tc<TcMode::kDownPartials>(a, n_mt, st);
+    }
+}
+
+cudaError_t launch_prep_x16(const int8_t* x_q, int64_t T, int64_t H, __half* x16, cudaStream_t st) {
+    const int64_t n8 = T * H / 8;
+    const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, static_cast<int64_t>(num_sms()) * 8);
+    prep_x16_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(x_q, n8, x16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep_h16(const float* h, const uint32_t* amax, const int8_t* hq_in, int64_t P, int64_t I,
+                            __half* h16, float* s_h, cudaStream_t st) {
+    const int64_t n8 = P * I / 8;
+    const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, static_cast<int64_t>(num_sms()) * 8);
+    prep_h16_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(h, amax, hq_in, P, I, h16,
+                                                                                          s_h);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

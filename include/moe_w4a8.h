@@ -77,15 +77,22 @@
 extern "C" {
 #endif
 
-#define MOE_W4A8_ABI_VERSION 2
+#define MOE_W4A8_ABI_VERSION 3
 
 /* Engines (the `engine` argument of the checking entry points).  AUTO picks
  * what moe_w4a8_forward picks: the fused decode engine when the batch fits
- * it (T <= 32, T*k <= 512 pairs, H a multiple of 1024, I a multiple of
- * 512, I/g a multiple of 4), the grouped tensor-core engine otherwise. */
+ * it (T <= 32, T*k <= 512 pairs, H = 2048 or 4096, I = 512 or 1536, g a
+ * multiple of 64 with I/g a multiple of 4), else the tcgen05 engine when g
+ * is a multiple of 128, else the grouped mma.sync engine.
+ *   GROUPED  grouped GEMMs on the legacy int8 mma.sync path (any valid dims)
+ *   DECODE   one cooperative kernel per call, dp4a on the CUDA cores
+ *   TCGEN05  grouped GEMMs on the fifth-generation tensor cores (tcgen05.mma,
+ *            fp16 operands holding the exact int4 / int8 values, accumulator
+ *            in tensor memory; g a multiple of 128) */
 #define MOE_ENGINE_AUTO (-1)
 #define MOE_ENGINE_GROUPED 0
 #define MOE_ENGINE_DECODE 1
+#define MOE_ENGINE_TCGEN05 2
 
 typedef enum {
     MOE_OK = 0,
@@ -116,10 +123,15 @@ const char* moe_w4a8_last_error(void);
  * (0 if `d` is invalid).  Host call, no device work. */
 size_t moe_w4a8_workspace_size(const moe_dims_t* d);
 
+/* Bytes of workspace moe_w4a8_gemm1_partials and moe_w4a8_gemm2_partials
+ * need for `d` and n_pairs pairs (0 if `d` is invalid or n_pairs < 0). */
+size_t moe_w4a8_partials_workspace_size(const moe_dims_t* d, int64_t n_pairs);
+
 /* The engine moe_w4a8_forward uses for `d` on the current device
- * (MOE_ENGINE_DECODE or MOE_ENGINE_GROUPED), or -1 if `d` is invalid.
- * The decode engine is one kernel launch per call (after a 16-byte memset
- * of its barrier counters); the grouped engine is seven launches. */
+ * (MOE_ENGINE_DECODE, MOE_ENGINE_TCGEN05 or MOE_ENGINE_GROUPED), or -1 if
+ * `d` is invalid.  The decode engine is one kernel launch per call (after
+ * a memset of its barrier counters); the grouped engines are seven or
+ * eight launches. */
 int moe_w4a8_engine_for(const moe_dims_t* d);
 
 /*
@@ -160,12 +172,12 @@ int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, const float*
 
 /*
  * Int32 partial sums of the gate/up projection for an explicit list of
- * pairs, through the main loop of the chosen engine (MOE_ENGINE_GROUPED or
- * MOE_ENGINE_DECODE; AUTO means GROUPED): for pair r (token pair_token[r],
- * bank slot pair_slot[r], both int32 device arrays of n_pairs entries),
- * p1[r][n][q] = P1 for n < 2I, q < H/g.  pair_slot must be sorted
- * ascending.  Workspace: moe_w4a8_workspace_size of the dims with T =
- * n_pairs, top_k = 1, E = E + S, n_shared = 0.
+ * pairs, through the main loop of the chosen engine (MOE_ENGINE_GROUPED,
+ * MOE_ENGINE_DECODE or MOE_ENGINE_TCGEN05; AUTO means GROUPED): for pair r
+ * (token pair_token[r], bank slot pair_slot[r], both int32 device arrays
+ * of n_pairs entries), p1[r][n][q] = P1 for n < 2I, q < H/g.  pair_slot
+ * must be sorted ascending; a pair_token outside [0, T) reads a zero row.
+ * Workspace: moe_w4a8_partials_workspace_size(d, n_pairs) bytes.
  */
 int moe_w4a8_gemm1_partials(const int8_t* x_q, const uint8_t* w13_packed, const moe_dims_t* d,
                             const int32_t* pair_token, const int32_t* pair_slot, int64_t n_pairs,

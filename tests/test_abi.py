@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(cuda_lib, lib):
 
 def test_version_and_status_strings(lib):
     from bit_moe_expert_router_gb300 import binding
-    assert lib.moe_w4a8_version() == binding.ABI_VERSION == 2
+    assert lib.moe_w4a8_version() == binding.ABI_VERSION == 3
     for s in range(6):
         assert binding.moe_w4a8_status_string(s)
     assert binding.moe_w4a8_status_string(99) == "unknown status"
@@ -102,6 +102,19 @@ def test_null_and_misaligned_pointers_are_rejected(lib):
     assert lib.moe_w4a8_route(fake, ctypes.byref(d), fake, fake, fake, fake, fake, None, fake, need, None) == 1
 
 
+def test_partials_workspace_covers_grouping_and_fp16_rows(lib):
+    from bit_moe_expert_router_gb300 import binding
+    d = binding.dims_of(64, 2048, 512, 512, 1, 10, 128)
+    small, big = (binding.moe_w4a8_partials_workspace_size(d, n) for n in (8, 4096))
+    assert small % 256 == 0 and small < big
+    # the fp16 copy of the T activation rows and of the n_pairs down-projection rows
+    assert small >= 2 * d.T * d.H + 2 * 8 * d.I
+    assert big >= 4096 * (d.I + d.H) * 4 + 2 * 4096 * d.I
+    assert lib.moe_w4a8_partials_workspace_size(ctypes.byref(d), -1) == 0
+    d.group = 48
+    assert lib.moe_w4a8_partials_workspace_size(ctypes.byref(d), 8) == 0
+
+
 def test_empty_batch_is_a_no_op(lib):
     from bit_moe_expert_router_gb300 import binding
     d = binding.dims_of(0, 256, 128, 8, 0, 2, 64)
@@ -116,9 +129,9 @@ def test_engine_and_status_arguments_are_checked(lib):
     d = binding.dims_of(4, 2048, 512, 512, 1, 10, 128)
     fake = ctypes.c_void_p(0x100000)
     need = lib.moe_w4a8_workspace_size(ctypes.byref(d))
-    # an engine outside {-1, 0, 1} is rejected before anything is enqueued
+    # an engine outside {-1, 0, 1, 2} is rejected before anything is enqueued
     assert lib.moe_w4a8_forward_debug(*[fake] * 7, ctypes.byref(d), fake, None, None, None, 7, fake, need, None) == 1
-    assert lib.moe_w4a8_gemm1_partials(fake, fake, ctypes.byref(d), fake, fake, 3, fake, 2, fake, need, None) == 1
+    assert lib.moe_w4a8_gemm1_partials(fake, fake, ctypes.byref(d), fake, fake, 3, fake, 3, fake, need, None) == 1
     assert lib.moe_w4a8_gemm2_partials(fake, fake, ctypes.byref(d), fake, 3, fake, -2, fake, need, None) == 1
     # the status query needs an aligned workspace of at least the header
     assert lib.moe_w4a8_device_status(None, 1024, None) == 1

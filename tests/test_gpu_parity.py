@@ -102,13 +102,20 @@ def _sample_pairs(w, tok, n, seed=0):
     return slots, tokens
 
 
-# engine 0 = grouped tensor-core engine (any size), 1 = fused decode engine (T <= 32)
-PARTIALS_CASES = [(n, 0) for n in ALL] + [("decode_t4", 1), ("decode_verify_t12", 1), ("dec_small", 1)]
+# engine 0 = grouped mma.sync engine (any size), 1 = fused decode engine (T <= 32),
+# 2 = tcgen05 engine (g a multiple of 128)
 DEC_SMALL = synth.Workload("dec_small", T=8, H=2048, I=512, E=16, S=1, top_k=4, group=128)
+TC_SMALL = synth.Workload("tc_small", T=300, H=256, I=128, E=8, S=1, top_k=2, group=128)
+TC_ODD = synth.Workload("tc_odd", T=150, H=384, I=384, E=6, S=0, top_k=3, group=128)
+TC_G256 = synth.Workload("tc_g256", T=140, H=512, I=256, E=4, S=1, top_k=2, group=256)
+EXTRA = {w.name: w for w in (DEC_SMALL, TC_SMALL, TC_ODD, TC_G256)}
+PARTIALS_CASES = ([(n, 0) for n in ALL] + [("decode_t4", 1), ("decode_verify_t12", 1), ("dec_small", 1)] +
+                  [(n, 2) for n in ("prefill_t8192", "large_bank_t2048", "decode_t4", "tc_small", "tc_odd",
+                                    "tc_g256")])
 
 
 def _workload(name):
-    return DEC_SMALL if name == "dec_small" else synth.WORKLOADS[name]
+    return EXTRA[name] if name in EXTRA else synth.WORKLOADS[name]
 
 
 @pytest.mark.parametrize("name,engine", PARTIALS_CASES)
@@ -169,7 +176,8 @@ def test_forward_matches_oracle(name):
 
 
 @pytest.mark.parametrize("name,engine", [("tiny", -1), ("decode_t4", 0), ("decode_t4", 1),
-                                         ("decode_verify_t12", 0), ("decode_verify_t12", 1), ("dec_small", 1)])
+                                         ("decode_verify_t12", 0), ("decode_verify_t12", 1), ("dec_small", 1),
+                                         ("decode_t4", 2), ("tc_small", 2), ("tc_odd", 2), ("tc_g256", 2)])
 def test_requantised_intermediate(name, engine):
     w = _workload(name)
     tok = synth.make_tokens(w)
@@ -344,3 +352,57 @@ def test_bounded_wait_reports_timeout_and_context_survives():
                              out, ws)
     assert binding.moe_w4a8_device_status(ws) == 0
     gh.assert_output_close(out.cpu().numpy(), gh.oracle_out(w, tok, gh.bank_of(w)), "after timeout")
+
+
+# ------------------------------------------------------------------ tcgen05 engine
+
+@pytest.mark.parametrize("T", [1, 2, 37, 129, 300])
+def test_tcgen05_engine_ragged_batches(T):
+    w = TC_SMALL.with_tokens(T)
+    tok = synth.make_tokens(w)
+    out = _forward_engine(w, tok, 2)
+    gh.assert_output_close(out, gh.oracle_out(w, tok, gh.bank_of(w)), f"tcgen05 T={T}")
+
+
+@pytest.mark.parametrize("name", ["tc_odd", "tc_g256"])
+def test_tcgen05_engine_shapes(name):
+    w = EXTRA[name]
+    tok = synth.make_tokens(w)
+    out = _forward_engine(w, tok, 2)
+    gh.assert_output_close(out, gh.oracle_out(w, tok, gh.bank_of(w)), name)
+
+
+def test_tcgen05_engine_one_expert_spans_many_token_tiles():
+    w = TC_SMALL.with_tokens(700)
+    tok = synth.make_tokens(w)
+    tok.logits[:, 5] = 50.0
+    out = _forward_engine(w, tok, 2)
+    gh.assert_output_close(out, gh.oracle_out(w, tok, gh.bank_of(w)), "one hot expert")
+
+
+def test_tcgen05_engine_matches_grouped_engine_on_large_bank():
+    w = synth.WORKLOADS["large_bank_t2048"].with_tokens(200)
+    tok = synth.make_tokens(w)
+    a = _forward_engine(w, tok, 2)
+    b = _forward_engine(w, tok, 0)
+    sel = gh.sample_tokens(w.T, 24)
+    ref = gh.oracle_out(w, tok, gh.bank_of(w), sel)
+    gh.assert_output_close(a[sel], ref, "tcgen05 engine, large bank")
+    gh.assert_output_close(b[sel], ref, "grouped engine, large bank")
+    again = _forward_engine(w, tok, 2)
+    assert np.array_equal(a, again), "two runs differ"
+
+
+def test_tcgen05_engine_is_auto_selected_for_large_batches():
+    assert binding.moe_w4a8_engine_for(gh.dims(synth.WORKLOADS["prefill_t8192"])) == 2
+    assert binding.moe_w4a8_engine_for(gh.dims(synth.WORKLOADS["large_bank_t2048"])) == 2
+    assert binding.moe_w4a8_engine_for(gh.dims(synth.WORKLOADS["decode_t4"])) == 1
+    assert binding.moe_w4a8_engine_for(gh.dims(synth.WORKLOADS["tiny"])) == 0  # g = 64
+
+
+def test_tcgen05_engine_rejects_groups_it_does_not_tile():
+    w = SMALL.with_tokens(8)  # g = 64
+    tok = synth.make_tokens(w)
+    with pytest.raises(binding.MoeError) as e:
+        _forward_engine(w, tok, 2)
+    assert e.value.status == 2
