@@ -49,6 +49,7 @@ def _args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--batches", type=int, default=N_BATCHES, help="token batches rotated between steps")
     p.add_argument("--banks", type=int, default=N_BANKS,
                    help="bank copies rotated between steps (fewer: a smaller case for profiler captures)")
     return p.parse_args()
@@ -158,17 +159,19 @@ def run_ours(a):
     banks = []
     for _ in range(a.banks):
         banks.append(tuple(torch.from_numpy(x).to(dev) for x in (bank.w13, bank.s13, bank.w2, bank.s2)))
-    batches = [synth.make_tokens(w, batch=rank * N_BATCHES + b) for b in range(N_BATCHES)]
+    batches = [synth.make_tokens(w, batch=rank * a.batches + b) for b in range(a.batches)]
     dev_batches = [tuple(torch.from_numpy(x).to(dev) for x in (t.x_q, t.x_scale, t.logits)) for t in batches]
     ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), dev)
     out = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
     alg_bytes, per_expert = _touched_bytes(w, [t.logits for t in batches])
     engine = binding.moe_w4a8_engine_for(d)
-    kernel_label = ("decode_kernel (fused, one launch per step; timed with its 16-byte barrier memset)"
-                    if engine == binding.ENGINE_DECODE else "whole step (7 kernels of the grouped engine)")
+    kernel_label = {binding.ENGINE_DECODE: "decode_kernel (fused, one launch per step; timed with its barrier memset)",
+                    binding.ENGINE_TCGEN05: "whole step (9 kernels of the tcgen05 engine)",
+                    binding.ENGINE_GROUPED: "whole step (7 kernels of the grouped engine)"}[engine]
+    launches_per_step = {binding.ENGINE_DECODE: 1, binding.ENGINE_TCGEN05: 9, binding.ENGINE_GROUPED: 7}[engine]
 
     def step(i):
-        x_q, x_s, lg = dev_batches[i % N_BATCHES]
+        x_q, x_s, lg = dev_batches[i % len(dev_batches)]
         w13, s13, w2, s2 = banks[i % len(banks)]
         binding.moe_w4a8_forward(x_q, x_s, lg, w13, s13, w2, s2, d, out, ws)
 
@@ -238,7 +241,7 @@ def run_ours(a):
     n_e2e = min(a.steps, 2000)
 
     def e2e_step(i):
-        for src, dst in zip(host_in[i % N_BATCHES], dx):
+        for src, dst in zip(host_in[i % len(host_in)], dx):
             dst.copy_(src, non_blocking=True)
         w13, s13, w2, s2 = banks[i % len(banks)]
         binding.moe_w4a8_forward(dx[0], dx[1], dx[2], w13, s13, w2, s2, d, out, ws)
@@ -276,12 +279,12 @@ def run_ours(a):
         "data": "synthetic (seeded generator: bf16 N(0,1) activations -> int8, N(0,0.02) weights -> int4 g128)",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "n_shared": w.S, "top_k": w.top_k,
                    "group": w.group, "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: {len(banks)} bank copies x {bank_mb:.0f} MB and {N_BATCHES} token batches rotated",
+                   "l2": f"inputs larger than L2: {len(banks)} bank copies x {bank_mb:.0f} MB and {len(batches)} token batches rotated",
                    "timing": f"CUDA graph of {GRAPH_STEPS} steps replayed; events on the launching stream"},
         "plain_launch_ms_per_step": plain_ms_per_step,
         "e2e": {"value": w.T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": a.steps * (1 if engine == binding.ENGINE_DECODE else 7),
+        "gpu_launches": a.steps * launches_per_step,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None, "peak_source": peak_kind,
                      "kernel": kernel_label, "algorithmic_bytes_per_step": alg_bytes,

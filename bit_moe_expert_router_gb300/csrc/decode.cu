@@ -8,13 +8,17 @@
 // expert's bytes from HBM once:
 //
 //   phase 0  every CTA routes all T tokens itself (the same deterministic
-//            result in every CTA, so nothing is exchanged), sorts the pairs
+//            result in every CTA, so nothing is exchanged; one warp per token,
+//            a threshold from the lanes' maxima, then exact ranking of the
+//            few candidates above it), sorts the pairs
 //            stably by expert into pair rows, builds the slot table (touched
 //            experts ascending, then the shared experts) and stages the
 //            activations in shared memory.
 //   phase 1  gate/up projection with dp4a on the CUDA cores: units of two
 //            intermediate indices (2 gate rows + the 2 matching up rows) of
-//            one slot, dealt round-robin over all warps of the grid.  A warp
+//            one slot; each warp takes a contiguous unit range of equal cost
+//            (streaming + per-token work, so the always-on shared expert's
+//            multi-token units weigh more).  A warp
 //            keeps up to four units of 16-byte loads in flight in
 //            registers; each lane covers a 64-value K piece, folds its exact
 //            int32 piece sum with the piece's group scale, and a 4-row
@@ -76,12 +80,6 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
     return v;
 }
 
-__device__ __forceinline__ uint2 ld_nc8(const void* p) {
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p)); }
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
@@ -121,9 +119,6 @@ __device__ bool grid_barrier(Header* hdr, uint32_t k) {
     return ok_s != 0;
 }
 
-// (v, e) beats (bv, be): larger value, or equal value and lower index.
-__device__ __forceinline__ bool beats(float v, int e, float bv, int be) { return v > bv || (v == bv && e < be); }
-
 // Order-preserving 32-bit key of a float: larger float -> larger key; -0.0
 // and +0.0 map to the same key (the sum with +0.0 turns -0.0 into +0.0).
 __device__ __forceinline__ uint32_t order_key(float v) {
@@ -139,111 +134,128 @@ __device__ __forceinline__ bool ranks_before(uint32_t a, uint32_t ia, uint32_t b
     return a > b || (a == b && ia < ib);
 }
 
-// Top-k of a warp's candidates, largest first (ties to the lower id).  Each
-// lane holds NJ candidates (key 0 / id 0xFFFFFFFF when absent), sorts them
-// once (bitonic network in registers), then each round takes the warp
-// maximum of the lanes' heads with two redux operations (max key, then min
-// id among the lanes holding it) and the winning lane pops its head.  Lane s
-// receives the s-th selected (key, id).
-template <int NJ>
-__device__ __forceinline__ void warp_topk(uint32_t (&key)[NJ], uint32_t (&id)[NJ], int k, uint32_t& out_key,
-                                          uint32_t& out_id) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int k2 = 2; k2 <= NJ; k2 <<= 1)
-#pragma unroll
-        for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1)
-#pragma unroll
-            for (int i = 0; i < NJ; ++i) {
-                const int l = i ^ j2;
-                if (l > i) {
-                    const bool want_i_first = (i & k2) == 0;
-                    const bool i_first = ranks_before(key[i], id[i], key[l], id[l]);
-                    if (i_first != want_i_first) {
-                        const uint32_t tk = key[i], ti = id[i];
-                        key[i] = key[l];
-                        id[i] = id[l];
-                        key[l] = tk;
-                        id[l] = ti;
-                    }
-                }
-            }
-    // the first half of a bitonic sort per k2 level sorts descending when
-    // (i & NJ) == 0, which holds for every i < NJ: the list is descending.
-    out_key = 0;
-    out_id = 0xFFFFFFFFu;
-    for (int s = 0; s < k; ++s) {
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, key[0]);
-        const uint32_t mi = __reduce_min_sync(0xffffffffu, key[0] == mk ? id[0] : 0xFFFFFFFFu);
-        if (key[0] == mk && id[0] == mi) {  // this lane holds the winner: pop it
-#pragma unroll
-            for (int j = 0; j + 1 < NJ; ++j) {
-                key[j] = key[j + 1];
-                id[j] = id[j + 1];
-            }
-            key[NJ - 1] = 0;
-            id[NJ - 1] = 0xFFFFFFFFu;
-        }
-        if (lane == s) {
-            out_key = mk;
-            out_id = mi;
-        }
-    }
-}
+// Routing of all T tokens, one warp per token (tokens dealt over the
+// CTA's warps).  Lane l holds the order keys of experts l, l + 32, ...
+// (NJ * 32 >= E).  Exact top-k in (key desc, id asc) order:
+//  1. tau = the k-th best of the 32 lanes' best elements (bitonic sort of
+//     the lane maxima across the warp).  At least k elements rank at or
+//     before tau, so the top-k all do: the candidates are those elements.
+//  2. up to kCand candidates are compacted into shared memory and each is
+//     ranked against all of them; rank < k is selected at that position.
+//  3. more candidates than that (heavily skewed or tied logits): k rounds
+//     of a warp arg-max over the elements not yet taken.
+// Then the weights: softmax over the k selected logits, relative to the
+// largest.  ids/wts: [T][k]; cand_k/cand_i: kCand per warp.
+constexpr int kCand = 64;
 
-// Routing of all T tokens by the CTA's warps: each token's experts are
-// split over `wpt` warps (interleaved), each finds the top-k of its share,
-// and one warp per token merges the wpt * k candidates.  The result equals
-// the top-k over all experts (every global top-k expert is in its share's
-// top-k).  ids/wts: [T][k]; cand_k/cand_i: [T][wpt][k] scratch.
 template <int NJ>
-__device__ void route_all(const float* __restrict__ logits, int T, int E, int k, int* ids, float* wts,
-                          uint32_t* cand_k, uint32_t* cand_i) {
+__device__ void route_tokens(const float* __restrict__ logits, int T, int E, int k, int* ids, float* wts,
+                             uint32_t* cand_k, uint32_t* cand_i) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    int wpt = 1;
-    while (wpt * 2 * T <= nw && wpt < 8 && 32 * wpt * 2 <= E) wpt *= 2;
-    while (32 * NJ * wpt < E) wpt *= 2;  // each lane holds at most NJ candidates
-    for (int job = warp; job < T * wpt; job += nw) {
-        const int t = job / wpt, sub = job % wpt;
-        uint32_t key[NJ], id[NJ];
+    uint32_t* ck = cand_k + warp * kCand;
+    uint32_t* ci = cand_i + warp * kCand;
+    for (int t = warp; t < T; t += nw) {
+        uint32_t key[NJ];
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
-            const int e = sub * 32 + lane + 32 * wpt * j;
-            const bool in = e < E;
-            key[j] = in ? order_key(__ldg(logits + static_cast<int64_t>(t) * E + e)) : 0u;
-            id[j] = in ? static_cast<uint32_t>(e) : 0xFFFFFFFFu;
+            const int e = lane + 32 * j;
+            key[j] = e < E ? order_key(__ldg(logits + static_cast<int64_t>(t) * E + e)) : 0u;
         }
-        uint32_t ok, oi;
-        warp_topk<NJ>(key, id, k, ok, oi);
-        if (lane < k) {
-            cand_k[(t * wpt + sub) * k + lane] = ok;
-            cand_i[(t * wpt + sub) * k + lane] = oi;
-        }
-    }
-    __syncthreads();
-    for (int t = warp; t < T; t += nw) {
-        constexpr int NM = 8;  // wpt * k <= 8 * 32 candidates
-        uint32_t key[NM], id[NM];
+        // this lane's best (ids grow with j, so strict > keeps the lowest id on ties)
+        uint32_t sk = key[0], si = lane < E ? static_cast<uint32_t>(lane) : 0xFFFFFFFFu;
 #pragma unroll
-        for (int j = 0; j < NM; ++j) {
-            const int c = lane + 32 * j;
-            const bool in = c < wpt * k;
-            key[j] = in ? cand_k[t * wpt * k + c] : 0u;
-            id[j] = in ? cand_i[t * wpt * k + c] : 0xFFFFFFFFu;
+        for (int j = 1; j < NJ; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E && key[j] > sk) {
+                sk = key[j];
+                si = static_cast<uint32_t>(e);
+            }
         }
-        uint32_t mk, mi;
-        warp_topk<NM>(key, id, k, mk, mi);
-        // softmax over the selected logits, relative to the largest (selected first)
-        const float my_v = key_value(mk);
+        // bitonic sort of the 32 lane maxima, best first
+#pragma unroll
+        for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                const uint32_t ok = __shfl_xor_sync(0xffffffffu, sk, stride);
+                const uint32_t oi = __shfl_xor_sync(0xffffffffu, si, stride);
+                const bool lower = (lane & stride) == 0;
+                const bool desc = (lane & size) == 0 || size == 32;
+                const bool mine_first = ranks_before(sk, si, ok, oi);
+                if (mine_first != (lower == desc)) {
+                    sk = ok;
+                    si = oi;
+                }
+            }
+        const uint32_t tk = __shfl_sync(0xffffffffu, sk, k - 1), ti = __shfl_sync(0xffffffffu, si, k - 1);
+        // candidates: elements ranking at or before (tk, ti)
+        uint32_t cmask = 0;
+        int cnt = 0;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const int e = lane + 32 * j;
+            const bool in = e < E && (key[j] > tk || (key[j] == tk && static_cast<uint32_t>(e) <= ti));
+            cmask |= static_cast<uint32_t>(in) << j;
+            cnt += in;
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (total <= kCand) {
+            int o = incl - cnt;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j)
+                if (cmask >> j & 1u) {
+                    ck[o] = key[j];
+                    ci[o] = static_cast<uint32_t>(lane + 32 * j);
+                    ++o;
+                }
+            __syncwarp();
+            for (int c = lane; c < total; c += 32) {
+                const uint32_t mk = ck[c], mi = ci[c];
+                int rank = 0;
+                for (int u = 0; u < total; ++u) rank += ranks_before(ck[u], ci[u], mk, mi);
+                if (rank < k) {
+                    ids[t * k + rank] = static_cast<int>(mi);
+                    wts[t * k + rank] = key_value(mk);
+                }
+            }
+        } else {
+            uint32_t taken = 0;
+            for (int r = 0; r < k; ++r) {
+                uint32_t bk = 0, bi = 0xFFFFFFFFu;
+                int bj = -1;
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const int e = lane + 32 * j;
+                    if (e < E && !(taken >> j & 1u) && (bj < 0 || key[j] > bk)) {
+                        bk = key[j];
+                        bi = static_cast<uint32_t>(e);
+                        bj = j;
+                    }
+                }
+                const uint32_t mk = __reduce_max_sync(0xffffffffu, bj >= 0 ? bk : 0u);
+                const uint32_t mi = __reduce_min_sync(0xffffffffu, (bj >= 0 && bk == mk) ? bi : 0xFFFFFFFFu);
+                if (bj >= 0 && bi == mi) taken |= 1u << bj;
+                if (lane == 0) {
+                    ids[t * k + r] = static_cast<int>(mi);
+                    wts[t * k + r] = key_value(mk);
+                }
+            }
+        }
+        __syncwarp();
+        // softmax over the selected logits, relative to the largest (position 0)
+        const float my_v = lane < k ? wts[t * k + lane] : 0.0f;
         const float m = __shfl_sync(0xffffffffu, my_v, 0);
         const float ex = lane < k ? expf(my_v - m) : 0.0f;
         float sum = ex;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        if (lane < k) {
-            ids[t * k + lane] = static_cast<int>(mi);
-            wts[t * k + lane] = ex / sum;
-        }
+        if (lane < k) wts[t * k + lane] = ex / sum;
+        __syncwarp();
     }
 }
 
@@ -303,8 +315,10 @@ struct Smem {
     uint8_t* x;       // [T][H + 16] split layout
     uint8_t* hq;      // [P][I + 16] split layout
     float* y;         // [P][rows_pc]
-    uint32_t* cand_k; // [T][8][k] routing candidates (order keys)
-    uint32_t* cand_i; // [T][8][k] (expert ids)
+    uint32_t* cand_k; // [warps][kCand] routing candidates (order keys)
+    uint32_t* cand_i; // [warps][kCand] (expert ids)
+    int* first;       // [rows] pair is the first of its expert (by pair index)
+    int* eqc;         // [rows] pairs with the same expert
     uint8_t* w2s;     // [smem_slots][slot_stride] staged down-projection slices
 };
 
@@ -327,9 +341,14 @@ __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
     s.y = reinterpret_cast<float*>(base + pl.off_y);
     s.cand_k = reinterpret_cast<uint32_t*>(base + pl.off_cand_v);
     s.cand_i = reinterpret_cast<uint32_t*>(base + pl.off_cand_e);
+    s.first = reinterpret_cast<int*>(base + pl.off_first);
+    s.eqc = reinterpret_cast<int*>(base + pl.off_eqc);
     s.w2s = base + pl.off_w2s;
     return s;
 }
+
+// Phase-1 cost of one unit of a slot with `cnt` tokens (streaming + per-token work).
+__device__ __forceinline__ int unit_cost(int cnt) { return 4 + cnt; }
 
 // PC1 = H / 2048 (64-value pieces per lane per row), PC2 = I / 512 (16-value pieces per lane per row).
 template <DecodeMode MODE, int PC1, int PC2>
@@ -346,7 +365,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     // ---------------------------------------------------------------- phase 0
     int n_rows;  // routed/listed pair rows before the shared rows
     if (routed) {
-        route_all<16>(a.logits, T, a.E, k, s.ids, s.wts, s.cand_k, s.cand_i);
+        route_tokens<kMaxExperts / 32>(a.logits, T, a.E, k, s.ids, s.wts, s.cand_k, s.cand_i);
         n_rows = T * k;
     } else {
         n_rows = a.n_pairs;  // listed pairs; out-of-range slots and tokens are clamped (never read out of bounds)
@@ -363,45 +382,66 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         for (int t = tid; t < T; t += kThreadsD) s.xs[t] = routed ? a.x_scale[t] : 1.0f;
     }
     __syncthreads();
-    // stable rank of each pair by expert id (n_rows <= kDecodeMaxPairs)
+    // stable rank of each pair by expert id (n_rows <= kDecodeMaxPairs), whether
+    // it is its expert's first pair, and how many pairs share its expert
     for (int i = tid; i < n_rows; i += kThreadsD) {
         const int e = s.ids[i];
-        int p = 0;
+        int p = 0, eq = 0;
+        bool first = true;
         for (int j = 0; j < n_rows; ++j) {
             const int f = s.ids[j];
             p += (f < e) || (f == e && j < i);
+            eq += f == e;
+            first = first && !(f == e && j < i);
         }
         s.pos[i] = p;
         s.pair_of[p] = i;
         s.row_tok[p] = routed ? i / k : (MODE == DecodeMode::kGemm1Partials ? min(max(a.pair_token[i], 0), T - 1) : p);
+        s.first[i] = first;
+        s.eqc[i] = eq;
     }
     const int S = routed ? a.S : 0;
     for (int r = tid; r < T * S; r += kThreadsD) s.row_tok[n_rows + r] = r % T;
     __syncthreads();
-    for (int r = tid; r < n_rows; r += kThreadsD) {
-        const int e = s.ids[s.pair_of[r]];
-        if (r == 0 || s.ids[s.pair_of[r - 1]] != e) {
-            int u = 0;
-            for (int q = 1; q <= r; ++q) u += s.ids[s.pair_of[q]] != s.ids[s.pair_of[q - 1]];
-            s.slot_e[u] = e;
-            s.slot_row0[u] = r;
-        }
+    // slot table: touched experts ascending (slot = number of smaller touched
+    // experts), then the shared experts
+    for (int i = tid; i < n_rows; i += kThreadsD) {
+        if (!s.first[i]) continue;
+        const int e = s.ids[i];
+        int u = 0;
+        for (int j = 0; j < n_rows; ++j) u += s.first[j] && s.ids[j] < e;
+        s.slot_e[u] = e;
+        s.slot_row0[u] = s.pos[i];
+        s.slot_cnt[u] = s.eqc[i];
     }
-    if (tid == 0) {
+    if (warp == 0) {
         int nr = 0;
-        for (int q = 0; q < n_rows; ++q) nr += (q == 0 || s.ids[s.pair_of[q]] != s.ids[s.pair_of[q - 1]]);
-        for (int sh = 0; sh < S; ++sh) {
+        for (int b0 = 0; b0 < n_rows; b0 += 32)
+            nr += __popc(__ballot_sync(0xffffffffu, b0 + lane < n_rows && s.first[b0 + lane]));
+        for (int sh = lane; sh < S; sh += 32) {
             s.slot_e[nr + sh] = a.E + sh;
             s.slot_row0[nr + sh] = n_rows + sh * T;
+            s.slot_cnt[nr + sh] = T;
         }
-        s.n_slots[0] = nr + S;
+        if (lane == 0) s.n_slots[0] = nr + S;
     }
     __syncthreads();
     const int n_slots = s.n_slots[0];
-    const int n_routed_slots = n_slots - S;
-    for (int u = tid; u < n_slots; u += kThreadsD) {
-        const int end = u + 1 < n_routed_slots ? s.slot_row0[u + 1] : (u < n_routed_slots ? n_rows : T);
-        s.slot_cnt[u] = u < n_routed_slots ? end - s.slot_row0[u] : T;
+    if (warp == 0) {  // phase-1 cost prefix over slots (streaming + per-token work), warp scan
+        int run = 0;
+        for (int b0 = 0; b0 < n_slots; b0 += 32) {
+            const int u = b0 + lane;
+            const int c = u < n_slots ? (I / 2) * unit_cost(s.slot_cnt[u]) : 0;
+            int incl = c;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            if (u < n_slots) s.slot_cum[u] = run + incl - c;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) s.slot_cum[n_slots] = run;
     }
     __syncthreads();
 
@@ -447,19 +487,32 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     if (MODE != DecodeMode::kGemm2Partials) {
         constexpr int DEPTH = PC1 == 1 ? 4 : 2;  // units of loads in flight per warp
         const int upe = I / 2;                    // units per slot
-        const int n_units = n_slots * upe;
-        const int W = static_cast<int>(gridDim.x) * kWarpsD;
-        const int gw = static_cast<int>(blockIdx.x) * kWarpsD + warp;
-        // units go round-robin over all warps of the grid, so the slots
-        // complete in order while phase 1 progresses
-        const int nun = gw < n_units ? (n_units - gw + W - 1) / W : 0;
+        // each warp takes a contiguous unit range of equal cost: a CTA's warps
+        // stream neighbouring rows, and few slots (pages) per SM
+        const int64_t Ctot = s.slot_cum[n_slots];
+        const int64_t W = static_cast<int64_t>(gridDim.x) * kWarpsD;
+        const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarpsD + warp;
+        auto unit_at = [&](int64_t cpos) -> int64_t {
+            int lo = 0, hi = n_slots;  // last slot with cum <= cpos
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) / 2;
+                if (s.slot_cum[mid] <= cpos) lo = mid;
+                else hi = mid;
+            }
+            const int c = unit_cost(s.slot_cnt[lo]);
+            int64_t within = (cpos - s.slot_cum[lo] + c - 1) / c;
+            if (within > upe) within = upe;
+            return static_cast<int64_t>(lo) * upe + within;
+        };
+        const int64_t Ua = unit_at(gw * Ctot / W), Ub = unit_at((gw + 1) * Ctot / W);
+        const int nun = static_cast<int>(Ub - Ua);
         const int stage_budget = (n_copies + n_lines + kThreadsD - 1) / kThreadsD / max(nun, 1) + 1;
 
         uint4 wr[DEPTH][4][PC1][2];
         float sr[DEPTH][4][PC1];
         auto issue = [&](int un, int d) {
-            const int U = gw + un * W;
-            const int u = U / upe, ip = U % upe;
+            const int64_t U = Ua + un;
+            const int u = static_cast<int>(U / upe), ip = static_cast<int>(U % upe);
             const int64_t e = s.slot_e[u];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -484,8 +537,8 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                 if (un >= nun) break;
                 const uint4(&w)[4][PC1][2] = wr[d];
                 const float(&sc)[4][PC1] = sr[d];
-                const int U = gw + un * W;
-                const int u = U / upe, ip = U % upe;
+                const int64_t U = Ua + un;
+                const int u = static_cast<int>(U / upe), ip = static_cast<int>(U % upe);
                 const int row0 = s.slot_row0[u], cnt = s.slot_cnt[u];
                 for (int m = 0; m < cnt; ++m) {
                     const int prow = row0 + m;
@@ -756,8 +809,10 @@ bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t 
     pl.off_x = take(mode == DecodeMode::kGemm2Partials ? 0 : T * (H + 16), 128);
     pl.off_hq = take(mode == DecodeMode::kGemm1Partials ? 0 : P * (I + 16), 128);
     pl.off_y = take(mode == DecodeMode::kForward ? 4 * P * pl.rows_pc : 0, 16);
-    pl.off_cand_v = take(mode == DecodeMode::kForward ? 4 * T * 8 * k : 0, 16);
-    pl.off_cand_e = take(mode == DecodeMode::kForward ? 4 * T * 8 * k : 0, 16);
+    pl.off_cand_v = take(mode == DecodeMode::kForward ? 4 * kWarpsD * kCand : 0, 16);
+    pl.off_cand_e = take(mode == DecodeMode::kForward ? 4 * kWarpsD * kCand : 0, 16);
+    pl.off_first = take(4 * rows, 16);
+    pl.off_eqc = take(4 * rows, 16);
     pl.off_w2s = static_cast<int>(align_up(o, 128));
     const size_t slot_bytes =
         static_cast<size_t>(pl.rows_pc) * (I / 2 + 16) + static_cast<size_t>(pl.rows_pc) * (I / g) * 4;

@@ -48,7 +48,9 @@ constexpr int kTileN = 128;
 constexpr int kAtom = 16384;                 // 128 rows x 128 bytes
 constexpr int kStageA = 2 * kAtom, kStageB = 2 * kAtom, kStage = kStageA + kStageB;
 constexpr int kMaxSlotsTc = kTcMaxSlots + 1;
-constexpr int kSmemTc = kNS * kStage + 128 * 4 + 128 * 4 + (kMaxSlotsTc + 16) * 4 + 256 + 1024;
+constexpr int kRaw = 3;                      // packed weight rows in flight ahead of the unpack
+constexpr int kRawStage = 128 * 64;          // 128 rows x 64 packed bytes (128 codes)
+constexpr int kSmemTc = kNS * kStage + kRaw * kRawStage + 128 * 4 + 128 * 4 + (kMaxSlotsTc + 16) * 4 + 256 + 1024;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -189,7 +191,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
-    float* colf = reinterpret_cast<float*>(smem + kNS * kStage);  // [128] B-row scales of the item
+    uint8_t* raw = smem + kNS * kStage;                           // [kRaw][128][64] packed weight rows
+    float* colf = reinterpret_cast<float*>(raw + kRaw * kRawStage);  // [128] B-row scales of the item
     int* colp = reinterpret_cast<int*>(colf + 128);               // [128] pair rows of the item
     int* prefix = colp + 128;                                     // [kMaxSlotsTc + 1] items before each slot
     uint64_t* bars = reinterpret_cast<uint64_t*>(prefix + kMaxSlotsTc + 16);
@@ -288,12 +291,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
 
     if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ producers
+        // Each thread owns tile row pt.  Its packed weight bytes for use
+        // u + kRaw are copied (cp.async) into the raw ring while use u is
+        // unpacked, so the unpack never waits for HBM; it waits only for
+        // its own copies (cp.async.wait_group), no cross-thread sync.
         const int pt = tid - 128;
+        int l_item = blockIdx.x, l_ks = 0;  // next use whose raw bytes are fetched
+        const uint8_t* l_src = nullptr;
+        if (l_item < total) {
+            const Item it = decode_item(l_item);
+            l_src = a.w + (static_cast<int64_t>(it.slot) * rows_per_slot + weight_row(it.mt, pt)) * (K / 2);
+        }
+        int l_use = 0;
+        auto fetch_next = [&]() {
+            if (l_item < total) {
+                uint8_t* dst = raw + (l_use % kRaw) * kRawStage + pt * 64;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) cp_async16(dst + 16 * q, l_src + 64 * l_ks + 16 * q);
+                ++l_use;
+                if (++l_ks == ksteps) {
+                    l_ks = 0;
+                    l_item += gridDim.x;
+                    if (l_item < total) {
+                        const Item it = decode_item(l_item);
+                        l_src = a.w + (static_cast<int64_t>(it.slot) * rows_per_slot + weight_row(it.mt, pt)) * (K / 2);
+                    }
+                }
+            }
+            cp_async_commit();  // one group per call, empty or not, so the group count stays aligned
+        };
+#pragma unroll
+        for (int d = 0; d < kRaw; ++d) fetch_next();
         int use = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
             const Item it = decode_item(item);
-            const uint8_t* asrc = a.w + (static_cast<int64_t>(it.slot) * rows_per_slot + weight_row(it.mt, pt)) * (K / 2);
             int64_t brow = pt < it.ntok ? (a.b_row ? a.b_row[it.row0 + pt] : it.row0 + pt) : -1;
             const bool bvalid = brow >= 0 && brow < a.b_rows;
             const __half* bsrc = a.b + (bvalid ? brow : 0) * K;
@@ -310,19 +342,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                     cp_async16(Bs + (w >> 3) * kAtom + swz(pt, w), bsrc + 128 * ks + 8 * w, bvalid ? 16 : 0);
                 asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(full + s))
                              : "memory");
-                const uint4* ap = reinterpret_cast<const uint4*>(asrc + 64 * ks);
-                uint4 raw[4];
+                cp_async_wait<kRaw - 1>();  // this use's raw bytes (fetched kRaw calls ago) have landed
+                const uint4* rp = reinterpret_cast<const uint4*>(raw + (use % kRaw) * kRawStage + pt * 64);
+                uint4 rw[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) raw[q] = ld_nc16(ap + q);
+                for (int q = 0; q < 4; ++q) rw[q] = rp[q];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const uint32_t words[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+                    const uint32_t words[4] = {rw[q].x, rw[q].y, rw[q].z, rw[q].w};
 #pragma unroll
                     for (int wi = 0; wi < 4; ++wi) {
                         const int w = 4 * q + wi;
                         *reinterpret_cast<uint4*>(As + (w >> 3) * kAtom + swz(pt, w)) = unpack_int4_f16(words[wi]);
                     }
                 }
+                // the raw slot just consumed is refilled kRaw uses ahead (after its
+                // bytes were used: no copy may overwrite them before they are read)
+                asm volatile("" ::: "memory");
+                fetch_next();
                 asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
                 mbar_arrive(full + s);
             }
@@ -416,18 +453,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                 mbar_arrive(acce + b);
             }
             if (ok && MODE == TcMode::kGateUp) {
+                // lanes 2j (gate) and 2j+1 (up) hold index i for every column: for a
+                // column pair (c0, c1) the even lane finishes c0 and the odd lane c1
                 const int64_t i = 64 * it.mt + (r >> 1);
+                const bool odd = r & 1;
 #pragma unroll
-                for (int c = 0; c < kTileN; ++c) {
-                    const float other = __shfl_xor_sync(0xffffffffu, acc[c], 1);  // up value (even lanes)
+                for (int c0 = 0; c0 < kTileN; c0 += 2) {
+                    const int c = c0 + (odd ? 1 : 0);
+                    const float other = __shfl_xor_sync(0xffffffffu, odd ? acc[c0] : acc[c0 + 1], 1);
+                    const float gate = odd ? other : acc[c0], up = odd ? acc[c0 + 1] : other;
                     float hv = 0.f;
-                    if (c < it.ntok && !(r & 1)) {
+                    if (c < it.ntok) {
                         const float xs = colf[c];
-                        hv = silu_f32(acc[c] * xs) * (other * xs);
+                        hv = silu_f32(gate * xs) * (up * xs);
                         a.h[static_cast<int64_t>(colp[c]) * a.I + i] = hv;
                     }
-                    const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
-                    if (lane == 0 && c < it.ntok) atomicMax(a.amax + colp[c], m);
+                    const uint32_t hb = __float_as_uint(fabsf(hv));
+                    const uint32_t m0 = __reduce_max_sync(0xffffffffu, odd ? 0u : hb);
+                    const uint32_t m1 = __reduce_max_sync(0xffffffffu, odd ? hb : 0u);
+                    if (lane == 0 && c0 < it.ntok) atomicMax(a.amax + colp[c0], m0);
+                    if (lane == 1 && c0 + 1 < it.ntok) atomicMax(a.amax + colp[c0 + 1], m1);
                 }
             } else if (ok && MODE == TcMode::kDown) {
                 const int64_t n = 128 * it.mt + r;

@@ -130,8 +130,8 @@ size_t moe_w4a8_partials_workspace_size(const moe_dims_t* d, int64_t n_pairs);
 /* The engine moe_w4a8_forward uses for `d` on the current device
  * (MOE_ENGINE_DECODE, MOE_ENGINE_TCGEN05 or MOE_ENGINE_GROUPED), or -1 if
  * `d` is invalid.  The decode engine is one kernel launch per call (after
- * a memset of its barrier counters); the grouped engines are seven or
- * eight launches. */
+ * a memset of its barrier counters); the grouped mma.sync engine is seven
+ * launches, the tcgen05 engine nine. */
 int moe_w4a8_engine_for(const moe_dims_t* d);
 
 /*
