@@ -196,7 +196,6 @@ int run_tc_gemms(const int8_t* x_q, const float* x_scale, const uint8_t* w13, co
     MOE_CUDA(moe::launch_prep_x16(x_q, d->T, d->H, v.x16, st));
     moe::TcArgs g1 = tc_args(w13, s13, 2 * d->I, d->H, d, v.x16, v.row_token, d->T, x_scale, v, n_slots);
     g1.h = v.h;
-    g1.amax = v.amax;
     MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kGateUp, g1, st));
     MOE_CUDA(moe::launch_prep_h16(v.h, v.amax, nullptr, L.P, d->I, v.h16, v.sh, st));
     moe::TcArgs g2 = tc_args(w2, s2, d->H, d->I, d, v.h16, nullptr, L.P, v.sh, v, n_slots);

@@ -30,7 +30,7 @@ struct TcArgs {
     int n_slots;
     // outputs
     float* h;                 // [P][I]        gate/up
-    uint32_t* amax;           // [P]           gate/up (row maxima of |h|, atomicMax)
+    uint32_t* amax;           // [P]           unused by the kernel (row maxima come from prep_h16)
     float* y;                 // [P][H]        down
     int32_t* partials;        // [P][rows_per_slot][K/g]  partials modes
     Header* hdr;              // status word for the bounded waits
@@ -41,9 +41,9 @@ cudaError_t launch_tc_gemm(TcMode mode, const TcArgs& a, cudaStream_t st);
 
 // x_q int8 [T][H] -> fp16 [T][H] in the engine's K order.
 cudaError_t launch_prep_x16(const int8_t* x_q, int64_t T, int64_t H, __half* x16, cudaStream_t st);
-// h fp32 [P][I] -> requantised codes as fp16 [P][I] (engine K order) and s_h [P]
-// (amax null: h_q given as int8 in `hq_in` instead, scales untouched).
-cudaError_t launch_prep_h16(const float* h, const uint32_t* amax, const int8_t* hq_in, int64_t P, int64_t I,
-                            __half* h16, float* s_h, cudaStream_t st);
+// h fp32 [P][I] -> row maxima of |h| (amax bits [P]), s_h [P] and the requantised codes as fp16
+// [P][I] in the engine's K order; with h null, the int8 codes `hq_in` [P][I] are converted as given.
+cudaError_t launch_prep_h16(const float* h, uint32_t* amax, const int8_t* hq_in, int64_t P, int64_t I, __half* h16,
+                            float* s_h, cudaStream_t st);
 
 }  // namespace moe

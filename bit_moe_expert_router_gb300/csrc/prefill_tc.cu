@@ -20,12 +20,12 @@
 // SM) walk the (slot, token tile, weight tile) items with the weight tile
 // fastest, so the CTAs working at one time share the token tile in L2.
 //
-// Nine warps: three of them share one SM sub-partition, whose 16K-register
-// file then caps a thread at 168 registers (the launch bound below).
-// Warp roles: warps 0-3 epilogue (TMEM lanes 32w..32w+31 = tile rows),
-// warps 4-7 producers (thread = tile row: unpack 64 packed bytes of its
-// weight row into fp16, cp.async its token row's 256 bytes), warp 8 issues
-// the MMAs (one thread) and owns the TMEM allocation.  Every wait is
+// Thirteen warps (four of them share one SM sub-partition, whose 16K-register
+// file then caps a thread at 128 registers).  Warp roles: warps 0-7
+// epilogue (warp w: TMEM lanes 32 (w % 4) .. +31 = tile rows, columns
+// 64 (w / 4) .. +63), warps 8-11 producers (thread = tile row: unpack 64
+// packed bytes of its weight row into fp16, cp.async its token row's 256
+// bytes), warp 12 issues the MMAs (one thread) and owns the TMEM allocation.  Every wait is
 // bounded; a timeout sets the status word and every role leaves cleanly.
 //
 // K order: the weight unpack turns a packed word (codes 0..7) into fp16
@@ -42,12 +42,18 @@
 namespace moe {
 namespace {
 
-constexpr int kTcThreads = 288;
+constexpr int kEpiWarps = 8;                 // two per TMEM lane quarter, 64 columns each
+constexpr int kProdWarps = 4;
+constexpr int kMmaWarp = kEpiWarps + kProdWarps;
+constexpr int kTcThreads = 32 * (kMmaWarp + 1);
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kHalfN = 64;                   // columns per epilogue warp
 constexpr int kNS = 3;
 constexpr int kTileN = 128;
 constexpr int kAtom = 16384;                 // 128 rows x 128 bytes
 constexpr int kStageA = 2 * kAtom, kStageB = 2 * kAtom, kStage = kStageA + kStageB;
 constexpr int kMaxSlotsTc = kTcMaxSlots + 1;
+constexpr int kAcc = 4;                      // accumulator buffers in tensor memory (128 columns each)
 constexpr int kRaw = 3;                      // packed weight rows in flight ahead of the unpack
 constexpr int kRawStage = 128 * 64;          // 128 rows x 64 packed bytes (128 codes)
 constexpr int kSmemTc = kNS * kStage + kRaw * kRawStage + 128 * 4 + 128 * 4 + (kMaxSlotsTc + 16) * 4 + 256 + 1024;
@@ -141,6 +147,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
 
+__device__ __forceinline__ float ld_nc_f32(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];\n" : "=f"(v) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ uint4 ld_nc16(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
@@ -199,8 +211,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
     uint64_t* full = bars;
     uint64_t* empty = bars + kNS;
     uint64_t* accf = bars + 2 * kNS;
-    uint64_t* acce = accf + 2;
-    uint64_t* done = acce + 2;
+    uint64_t* acce = accf + kAcc;
+    uint64_t* done = acce + kAcc;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     int* warp_sums = abort_flag + 1;  // [kTcThreads / 32 + 1]
@@ -217,17 +229,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
             mbar_init(full + s, 256);  // 128 producer arrivals + 128 cp.async completions
             mbar_init(empty + s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kAcc; ++b) {
             mbar_init(accf + b, 1);
-            mbar_init(acce + b, 128);
+            mbar_init(acce + b, kEpiThreads);
         }
         mbar_init(done, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
-    if (warp == 8) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tmem_holder)),
-                     "r"(256));
+                     "r"(kAcc * 128));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
     // items of each slot -> exclusive prefix (every CTA computes it)
@@ -289,13 +301,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
         return static_cast<int64_t>(128) * mt + r;
     };
 
-    if (warp >= 4 && warp < 8) {
+    if (warp >= kEpiWarps && warp < kMmaWarp) {
         // ------------------------------------------------------------ producers
         // Each thread owns tile row pt.  Its packed weight bytes for use
         // u + kRaw are copied (cp.async) into the raw ring while use u is
         // unpacked, so the unpack never waits for HBM; it waits only for
         // its own copies (cp.async.wait_group), no cross-thread sync.
-        const int pt = tid - 128;
+        const int pt = tid - kEpiThreads;
+        // 16-byte chunk q of row pt sits at chunk q ^ rsw: eight consecutive rows
+        // (64 bytes apart) then hit eight different bank groups
+        const int rsw = (pt >> 1) & 3;
         int l_item = blockIdx.x, l_ks = 0;  // next use whose raw bytes are fetched
         const uint8_t* l_src = nullptr;
         if (l_item < total) {
@@ -307,7 +322,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
             if (l_item < total) {
                 uint8_t* dst = raw + (l_use % kRaw) * kRawStage + pt * 64;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) cp_async16(dst + 16 * q, l_src + 64 * l_ks + 16 * q);
+                for (int q = 0; q < 4; ++q) cp_async16(dst + 16 * (q ^ rsw), l_src + 64 * l_ks + 16 * q);
                 ++l_use;
                 if (++l_ks == ksteps) {
                     l_ks = 0;
@@ -346,7 +361,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                 const uint4* rp = reinterpret_cast<const uint4*>(raw + (use % kRaw) * kRawStage + pt * 64);
                 uint4 rw[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) rw[q] = rp[q];
+                for (int q = 0; q < 4; ++q) rw[q] = rp[q ^ rsw];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const uint32_t words[4] = {rw[q].x, rw[q].y, rw[q].z, rw[q].w};
@@ -365,7 +380,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
             }
         }
         cp_async_wait<0>();
-    } else if (warp == 8) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             int use = 0, grp = 0;
@@ -376,9 +391,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                 for (int ks = 0; ks < ksteps; ++ks, ++use) {
                     const int s = use % kNS;
                     const int sub = ks % spg;
-                    const int b = grp & 1;
+                    const int b = grp % kAcc;
                     if (!wait_bar(full + s, (use / kNS) & 1, ctl) ||
-                        (sub == 0 && !wait_bar(acce + b, ((grp >> 1) & 1) ^ 1, ctl))) {
+                        (sub == 0 && !wait_bar(acce + b, ((grp / kAcc) & 1) ^ 1, ctl))) {
                         ok = false;
                         break;
                     }
@@ -408,41 +423,48 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        const int r = tid;  // TMEM lane = tile row
+        // warp w: TMEM lanes 32 (w % 4) .. +31 (tile rows), columns 64 (w / 4) .. +63
+        const int quarter = warp & 3, c_base = kHalfN * (warp >> 2);
+        const int r = 32 * quarter + lane;  // tile row
         int grp = 0;
         for (int item = blockIdx.x; item < total; item += gridDim.x) {
             const Item it = decode_item(item);
-            if (r < it.ntok) {
-                const int p = it.row0 + r;
-                colp[r] = p;
-                if (!partials) colf[r] = gateup ? a.b_scale[a.b_row ? a.b_row[p] : p] : a.b_scale[p];
+            if (tid < it.ntok) {
+                const int p = it.row0 + tid;
+                colp[tid] = p;
+                if (!partials) colf[tid] = gateup ? a.b_scale[a.b_row ? a.b_row[p] : p] : a.b_scale[p];
             }
-            named_bar(1, 128);
+            named_bar(1, kEpiThreads);
+            const int nloc = min(kHalfN, it.ntok - c_base);  // this warp's live columns (may be <= 0)
             const int64_t wrow = weight_row(it.mt, r);
             const float* srow = a.ws + (static_cast<int64_t>(it.slot) * rows_per_slot + wrow) * ngrp;
-            float acc[kTileN];
+            float acc[kHalfN];
 #pragma unroll
-            for (int c = 0; c < kTileN; ++c) acc[c] = 0.f;
+            for (int c = 0; c < kHalfN; ++c) acc[c] = 0.f;
             bool ok = true;
+            // group scales two groups ahead (volatile loads: issued before the waits)
+            float sc1 = partials ? 0.f : ld_nc_f32(srow), sc2 = (partials || ngrp < 2) ? 0.f : ld_nc_f32(srow + 1);
             for (int gq = 0; gq < ngrp; ++gq, ++grp) {
-                const int b = grp & 1;
-                const float sc = partials ? 0.f : __ldg(srow + gq);
-                if (!wait_bar(accf + b, (grp >> 1) & 1, ctl)) {
+                const int b = grp % kAcc;
+                const float sc = sc1;
+                sc1 = sc2;
+                if (!partials && gq + 2 < ngrp) sc2 = ld_nc_f32(srow + gq + 2);
+                if (!wait_bar(accf + b, (grp / kAcc) & 1, ctl)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int i = 0; i < kTileN / 32; ++i) {
-                    if (32 * i >= it.ntok) break;
+                for (int i = 0; i < kHalfN / 32; ++i) {
+                    if (32 * i >= nloc) break;
                     uint32_t v[32];
-                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + b * 128 + 32 * i, v);
+                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + b * 128 + c_base + 32 * i, v);
                     if (partials) {
                         int32_t* dst = a.partials + wrow * ngrp + gq;
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
-                            if (32 * i + c < it.ntok)
-                                dst[static_cast<int64_t>(colp[32 * i + c]) * rows_per_slot * ngrp] =
+                            if (32 * i + c < nloc)
+                                dst[static_cast<int64_t>(colp[c_base + 32 * i + c]) * rows_per_slot * ngrp] =
                                     __float2int_rn(__uint_as_float(v[c]));
                     } else {
 #pragma unroll
@@ -458,38 +480,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                 const int64_t i = 64 * it.mt + (r >> 1);
                 const bool odd = r & 1;
 #pragma unroll
-                for (int c0 = 0; c0 < kTileN; c0 += 2) {
+                for (int c0 = 0; c0 < kHalfN; c0 += 2) {
                     const int c = c0 + (odd ? 1 : 0);
                     const float other = __shfl_xor_sync(0xffffffffu, odd ? acc[c0] : acc[c0 + 1], 1);
                     const float gate = odd ? other : acc[c0], up = odd ? acc[c0 + 1] : other;
-                    float hv = 0.f;
-                    if (c < it.ntok) {
-                        const float xs = colf[c];
-                        hv = silu_f32(gate * xs) * (up * xs);
-                        a.h[static_cast<int64_t>(colp[c]) * a.I + i] = hv;
+                    if (c < nloc) {
+                        const float xs = colf[c_base + c];
+                        a.h[static_cast<int64_t>(colp[c_base + c]) * a.I + i] = silu_f32(gate * xs) * (up * xs);
                     }
-                    const uint32_t hb = __float_as_uint(fabsf(hv));
-                    const uint32_t m0 = __reduce_max_sync(0xffffffffu, odd ? 0u : hb);
-                    const uint32_t m1 = __reduce_max_sync(0xffffffffu, odd ? hb : 0u);
-                    if (lane == 0 && c0 < it.ntok) atomicMax(a.amax + colp[c0], m0);
-                    if (lane == 1 && c0 + 1 < it.ntok) atomicMax(a.amax + colp[c0 + 1], m1);
                 }
             } else if (ok && MODE == TcMode::kDown) {
                 const int64_t n = 128 * it.mt + r;
 #pragma unroll
-                for (int c = 0; c < kTileN; ++c)
-                    if (c < it.ntok) a.y[static_cast<int64_t>(colp[c]) * a.H + n] = acc[c] * colf[c];
+                for (int c = 0; c < kHalfN; ++c)
+                    if (c < nloc) a.y[static_cast<int64_t>(colp[c_base + c]) * a.H + n] = acc[c] * colf[c_base + c];
             }
             // colf / colp are reused by the next item; leave together if any thread gave up
-            if (named_bar_or(1, 128, !ok)) break;
+            if (named_bar_or(1, kEpiThreads, !ok)) break;
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(256));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kAcc * 128));
     }
 }
 
@@ -506,31 +521,52 @@ __global__ void prep_x16_kernel(const int8_t* __restrict__ x, int64_t n8, __half
     }
 }
 
-// h fp32 -> requantised codes (fp32 decision, IEEE division) as fp16 in the engine's K order, plus s_h.
-__global__ void prep_h16_kernel(const float* __restrict__ h, const uint32_t* __restrict__ amax,
+// h fp32 -> requantised codes as fp16 in the engine's K order, one warp per
+// pair row: the row maximum of |h| (-> amax bits and s_h = max / 127), then
+// the codes (fp32 decision, IEEE division).  With hq_in (no h) the int8
+// codes are converted as given.
+__global__ void prep_h16_kernel(const float* __restrict__ h, uint32_t* __restrict__ amax,
                                 const int8_t* __restrict__ hq_in, int64_t P, int64_t I, __half* __restrict__ out,
                                 float* __restrict__ s_h) {
-    const int64_t n8 = P * I / 8;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t row = (8 * i) / I;
-        int code[8];
-        if (amax) {
-            const float s = requant_scale(amax[row]);
-            const float4 f0 = *reinterpret_cast<const float4*>(h + 8 * i);
-            const float4 f1 = *reinterpret_cast<const float4*>(h + 8 * i + 4);
-            const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) code[e] = requant_code(f[e], s);
-            if ((8 * i) % I == 0 && s_h) s_h[row] = s;
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) code[e] = hq_in[8 * i + e];
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); row < P; row += nw) {
+        const float* hr = h ? h + row * I : nullptr;
+        float s = 0.f;
+        if (hr) {
+            float m = 0.f;
+            for (int64_t k = 8 * lane; k < I; k += 256) {
+                const float4 f0 = *reinterpret_cast<const float4*>(hr + k);
+                const float4 f1 = *reinterpret_cast<const float4*>(hr + k + 4);
+                m = fmaxf(m, fmaxf(fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f0.z), fabsf(f0.w))),
+                                   fmaxf(fmaxf(fabsf(f1.x), fabsf(f1.y)), fmaxf(fabsf(f1.z), fabsf(f1.w)))));
+            }
+            m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
+            s = requant_scale(__float_as_uint(m));
+            if (lane == 0) {
+                if (amax) amax[row] = __float_as_uint(m);
+                if (s_h) s_h[row] = s;
+            }
         }
-        __half2 o[4];
+        for (int64_t k = 8 * lane; k < I; k += 256) {
+            int code[8];
+            if (hr) {
+                const float4 f0 = *reinterpret_cast<const float4*>(hr + k);
+                const float4 f1 = *reinterpret_cast<const float4*>(hr + k + 4);
+                const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[e] = __halves2half2(__int2half_rn(code[e]), __int2half_rn(code[e + 4]));
-        *reinterpret_cast<uint4*>(out + 8 * i) = *reinterpret_cast<const uint4*>(o);
+                for (int e = 0; e < 8; ++e) code[e] = requant_code(f[e], s);
+            } else {
+                const uint2 v = *reinterpret_cast<const uint2*>(hq_in + row * I + k);
+                const int8_t* b = reinterpret_cast<const int8_t*>(&v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) code[e] = b[e];
+            }
+            __half2 o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = __halves2half2(__int2half_rn(code[e]), __int2half_rn(code[e + 4]));
+            *reinterpret_cast<uint4*>(out + row * I + k) = *reinterpret_cast<const uint4*>(o);
+        }
     }
 }
 
@@ -578,10 +614,9 @@ cudaError_t launch_prep_x16(const int8_t* x_q, int64_t T, int64_t H, __half* x16
     return cudaGetLastError();
 }
 
-cudaError_t launch_prep_h16(const float* h, const uint32_t* amax, const int8_t* hq_in, int64_t P, int64_t I,
-                            __half* h16, float* s_h, cudaStream_t st) {
-    const int64_t n8 = P * I / 8;
-    const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, static_cast<int64_t>(num_sms()) * 8);
+cudaError_t launch_prep_h16(const float* h, uint32_t* amax, const int8_t* hq_in, int64_t P, int64_t I, __half* h16,
+                            float* s_h, cudaStream_t st) {
+    const int64_t blocks = std::min<int64_t>((P + 7) / 8, static_cast<int64_t>(num_sms()) * 8);
     prep_h16_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(h, amax, hq_in, P, I, h16,
                                                                                           s_h);
     return cudaGetLastError();
