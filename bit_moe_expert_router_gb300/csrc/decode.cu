@@ -290,11 +290,16 @@ __device__ __forceinline__ int dot32(const uint4& w, const uint4& xa, const uint
 // IEEE fp32.  h * rs is within 2^-23 relative of h / s (|h / s| <= 127),
 // so it rounds to the same integer unless it lies within 1e-4 of a
 // half-integer; only then is the exact division computed.
+// The rare exact path, kept out of line (the run-once code of a launch is
+// fetched cold, so it is kept small).
+__device__ __noinline__ float rint_div_exact(float h, float s) { return rintf(__fdiv_rn(h, s)); }
+
 __device__ __forceinline__ int requant_code_fast(float h, float s, float rs) {
     if (!(s > 0.0f)) return 0;
     const float f = h * rs;
     const float d = fabsf(f - floorf(f) - 0.5f);
-    float q = d < 1e-4f ? rintf(__fdiv_rn(h, s)) : rintf(f);
+    float q = rintf(f);
+    if (d < 1e-4f) q = rint_div_exact(h, s);
     q = fminf(fmaxf(q, -127.0f), 127.0f);
     return static_cast<int>(q);
 }
@@ -319,6 +324,7 @@ struct Smem {
     uint32_t* cand_i; // [warps][kCand] (expert ids)
     int* first;       // [rows] pair is the first of its expert (by pair index)
     int* eqc;         // [rows] pairs with the same expert
+    float* wmax;      // [warps][P] each warp's running max |h| per pair row
     uint8_t* w2s;     // [smem_slots][slot_stride] staged down-projection slices
 };
 
@@ -343,6 +349,7 @@ __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
     s.cand_i = reinterpret_cast<uint32_t*>(base + pl.off_cand_e);
     s.first = reinterpret_cast<int*>(base + pl.off_first);
     s.eqc = reinterpret_cast<int*>(base + pl.off_eqc);
+    s.wmax = reinterpret_cast<float*>(base + pl.off_wmax);
     s.w2s = base + pl.off_w2s;
     return s;
 }
@@ -365,7 +372,8 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     // ---------------------------------------------------------------- phase 0
     int n_rows;  // routed/listed pair rows before the shared rows
     if (routed) {
-        route_tokens<kMaxExperts / 32>(a.logits, T, a.E, k, s.ids, s.wts, s.cand_k, s.cand_i);
+        if (a.E <= 512) route_tokens<16>(a.logits, T, a.E, k, s.ids, s.wts, s.cand_k, s.cand_i);
+        else route_tokens<kMaxExperts / 32>(a.logits, T, a.E, k, s.ids, s.wts, s.cand_k, s.cand_i);
         n_rows = T * k;
     } else {
         n_rows = a.n_pairs;  // listed pairs; out-of-range slots and tokens are clamped (never read out of bounds)
@@ -402,6 +410,9 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     }
     const int S = routed ? a.S : 0;
     for (int r = tid; r < T * S; r += kThreadsD) s.row_tok[n_rows + r] = r % T;
+    const int P_all = n_rows + T * S;
+    if (MODE == DecodeMode::kForward)
+        for (int i = tid; i < kWarpsD * P_all; i += kThreadsD) s.wmax[i] = 0.f;
     __syncthreads();
     // slot table: touched experts ascending (slot = number of smaller touched
     // experts), then the shared experts
@@ -589,11 +600,17 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                     kk += __shfl_xor_sync(0xffffffffu, kk, 2);
                     kk += __shfl_xor_sync(0xffffffffu, kk, 1);
                     const float upv = __shfl_xor_sync(0xffffffffu, kk, 16);  // up row of the same index
+                    float hm = 0.f;
                     if (!b4 && (lane & 7) == 0) {
                         const float xs = s.xs[t];
                         const float hv = silu_f32(kk * xs) * (upv * xs);
                         a.h[static_cast<int64_t>(prow) * I + 2 * ip + (b3 ? 1 : 0)] = hv;
-                        atomicMax(a.row_max + prow, __float_as_uint(fabsf(hv)));
+                        hm = fabsf(hv);
+                    }
+                    if (MODE == DecodeMode::kForward) {
+                        // this warp's running maximum of the row (lane 0 owns the warp's entry)
+                        hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 8));
+                        if (lane == 0) s.wmax[warp * P_all + prow] = fmaxf(s.wmax[warp * P_all + prow], hm);
                     }
                 }
                 if (un + DEPTH < nun) issue(un + DEPTH, d);  // refill this ring slot
@@ -602,7 +619,15 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         }
     }
     if (MODE == DecodeMode::kGemm1Partials) return;
-    if (MODE == DecodeMode::kForward) stage_some(1 << 30);  // whatever phase 1 did not cover
+    if (MODE == DecodeMode::kForward) {
+        stage_some(1 << 30);  // whatever phase 1 did not cover
+        __syncthreads();
+        for (int p = tid; p < P_all; p += kThreadsD) {
+            float m = 0.f;
+            for (int w = 0; w < kWarpsD; ++w) m = fmaxf(m, s.wmax[w * P_all + p]);
+            if (m > 0.f) atomicMax(a.row_max + p, __float_as_uint(m));
+        }
+    }
 
     // ---------------------------------------------------------------- barrier
     if (MODE == DecodeMode::kForward && !grid_barrier(a.hdr, 1)) {
@@ -624,11 +649,12 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                 if (a.amax && blockIdx.x == 0) a.amax[p] = mb;
             }
             __syncthreads();
+            // 4 chunks (16 values each) per thread at a time, all 16 loads issued first
             const int n_chunks = P * per_row;
-            for (int o0 = tid; o0 < n_chunks; o0 += 2 * kThreadsD) {
-                float4 f[2][4];
+            for (int o0 = tid; o0 < n_chunks; o0 += 4 * kThreadsD) {
+                float4 f[4][4];
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
+                for (int b = 0; b < 4; ++b) {
                     const int o = min(o0 + b * kThreadsD, n_chunks - 1);
                     const float4* src = reinterpret_cast<const float4*>(a.h + static_cast<int64_t>(o / per_row) * I +
                                                                         16 * (o % per_row));
@@ -636,7 +662,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                     for (int q = 0; q < 4; ++q) f[b][q] = __ldcg(src + q);
                 }
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
+                for (int b = 0; b < 4; ++b) {
                     const int o = o0 + b * kThreadsD;
                     if (o >= n_chunks) break;
                     const int p = o / per_row, c = o % per_row;
@@ -644,11 +670,12 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                     const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
                     uint32_t wds[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        wds[q] = (requant_code_fast(f[b][q].x, sc, rs) & 0xFF) |
-                                 ((requant_code_fast(f[b][q].y, sc, rs) & 0xFF) << 8) |
-                                 ((requant_code_fast(f[b][q].z, sc, rs) & 0xFF) << 16) |
-                                 ((static_cast<uint32_t>(requant_code_fast(f[b][q].w, sc, rs)) & 0xFF) << 24);
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 v = f[b][q];
+                        wds[q] = (requant_code_fast(v.x, sc, rs) & 0xFF) | ((requant_code_fast(v.y, sc, rs) & 0xFF) << 8) |
+                                 ((requant_code_fast(v.z, sc, rs) & 0xFF) << 16) |
+                                 ((static_cast<uint32_t>(requant_code_fast(v.w, sc, rs)) & 0xFF) << 24);
+                    }
                     *reinterpret_cast<uint4*>(s.hq + p * HQS + 16 * c) = split16(make_uint4(wds[0], wds[1], wds[2], wds[3]));
                 }
             }
@@ -813,6 +840,7 @@ bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t 
     pl.off_cand_e = take(mode == DecodeMode::kForward ? 4 * kWarpsD * kCand : 0, 16);
     pl.off_first = take(4 * rows, 16);
     pl.off_eqc = take(4 * rows, 16);
+    pl.off_wmax = take(mode == DecodeMode::kForward ? 4 * kWarpsD * P : 0, 16);
     pl.off_w2s = static_cast<int>(align_up(o, 128));
     const size_t slot_bytes =
         static_cast<size_t>(pl.rows_pc) * (I / 2 + 16) + static_cast<size_t>(pl.rows_pc) * (I / g) * 4;
