@@ -147,6 +147,7 @@ __device__ __forceinline__ bool ranks_before(uint32_t a, uint32_t ia, uint32_t b
 // Then the weights: softmax over the k selected logits, relative to the
 // largest.  ids/wts: [T][k]; cand_k/cand_i: kCand per warp.
 constexpr int kCand = 64;
+constexpr int kStagePosMax = 4;  // down-projection staging: copy positions per thread and slot
 
 template <int NJ>
 __device__ void route_tokens(const float* __restrict__ logits, int T, int E, int k, int* ids, float* wts,
@@ -458,37 +459,60 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
 
     // This CTA's down-projection slice (rows [n0, n0 + nrows) of every slot):
     // the first n_smem slots are copied into shared memory with cp.async, the
-    // rest warmed in L2.  Each thread issues a few copies per phase-1 unit, so
-    // the requests queue behind the phase-1 loads instead of stalling here.
+    // rest warmed in L2.  Thread tid owns the same copy positions (row, 16-byte
+    // piece) in every slot -- computed once -- and walks the slots a few per
+    // phase-1 unit, so the requests queue behind the phase-1 loads.
     const int n0 = blockIdx.x * pl.rows_pc;
     const int nrows = max(0, min(pl.rows_pc, H - n0));
     const int n_smem = MODE == DecodeMode::kForward && nrows > 0 ? min(n_slots, pl.smem_slots) : 0;
     const int slot_stride = pl.rows_pc * RS + pl.rows_pc * ng2 * 4;
-    const int wch = I / 32, sch = ng2 / 4;  // 16-byte chunks per row: weights, scales
+    const int wch = I / 32, sch = ng2 / 4;  // 16-byte pieces per row: weights, scales
     const int per_slot = nrows * (wch + sch);
-    const int n_copies = n_smem * per_slot;
     const int lines_w = (nrows * (I / 2) + 127) / 128, lines_s = (nrows * ng2 * 4 + 127) / 128;
-    const int n_lines = MODE == DecodeMode::kForward && nrows > 0 ? (n_slots - n_smem) * (lines_w + lines_s) : 0;
-    int next_job = tid;  // this thread's next copy / prefetch (stride kThreadsD)
-    auto stage_some = [&](int budget) {
-        for (int b = 0; b < budget && next_job < n_copies + n_lines; ++b, next_job += kThreadsD) {
-            if (next_job < n_copies) {
-                const int u = next_job / per_slot, c = next_job % per_slot;
-                const int64_t e = s.slot_e[u];
-                uint8_t* base = s.w2s + u * slot_stride;
-                if (c < nrows * wch) {
-                    const int r = c / wch, q = c % wch;
-                    cp_async16(base + r * RS + 16 * q, a.w2 + (e * H + n0 + r) * static_cast<int64_t>(I / 2) + 16 * q);
-                } else {
-                    const int c2 = c - nrows * wch;
-                    cp_async16(base + pl.rows_pc * RS + 16 * c2, a.s2 + (e * H + n0) * ng2 + 4 * c2);
-                }
+    const int n_lines_slot = lines_w + lines_s;
+    // this thread's positions in a slot: up to kStagePos copy pieces and one prefetch line
+    constexpr int kStagePos = kStagePosMax;
+    int pos_dst[kStagePos];
+    int64_t pos_src[kStagePos];  // byte offset from the slot's first row (weights) or its scales
+    bool pos_scale[kStagePos];
+    int n_pos = 0;
+#pragma unroll
+    for (int i = 0; i < kStagePos; ++i) {
+        const int c = tid + kThreadsD * i;
+        pos_dst[i] = 0;
+        pos_src[i] = 0;
+        pos_scale[i] = false;
+        if (c < per_slot) {
+            n_pos = i + 1;
+            if (c < nrows * wch) {
+                const int r = c / wch, q = c % wch;
+                pos_dst[i] = r * RS + 16 * q;
+                pos_src[i] = static_cast<int64_t>(r) * (I / 2) + 16 * q;
             } else {
-                const int o = next_job - n_copies;
-                const int u = n_smem + o / (lines_w + lines_s), c = o % (lines_w + lines_s);
-                const int64_t e = s.slot_e[u];
-                if (c < lines_w) prefetch_l2(a.w2 + (e * H + n0) * static_cast<int64_t>(I / 2) + 128 * c);
-                else prefetch_l2(reinterpret_cast<const uint8_t*>(a.s2 + (e * H + n0) * ng2) + 128 * (c - lines_w));
+                const int c2 = c - nrows * wch;
+                pos_dst[i] = pl.rows_pc * RS + 16 * c2;
+                pos_src[i] = 16 * c2;
+                pos_scale[i] = true;
+            }
+        }
+    }
+    const bool line_is_w = tid < lines_w;
+    const int64_t line_off = line_is_w ? 128 * tid : 128 * (tid - lines_w);
+    const bool has_line = tid < n_lines_slot && MODE == DecodeMode::kForward && nrows > 0;
+    int next_slot = 0;  // next slot this thread stages (copies or warms)
+    auto stage_some = [&](int budget) {
+        for (int b = 0; b < budget && next_slot < n_slots; ++b, ++next_slot) {
+            const int u = next_slot;
+            const int64_t e = s.slot_e[u];
+            const uint8_t* wsrc = a.w2 + (e * H + n0) * static_cast<int64_t>(I / 2);
+            const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(a.s2 + (e * H + n0) * ng2);
+            if (u < n_smem) {
+                uint8_t* base = s.w2s + u * slot_stride;
+#pragma unroll
+                for (int i = 0; i < kStagePos; ++i)
+                    if (i < n_pos) cp_async16(base + pos_dst[i], (pos_scale[i] ? ssrc : wsrc) + pos_src[i]);
+            } else if (has_line) {
+                prefetch_l2((line_is_w ? wsrc : ssrc) + line_off);
             }
         }
         cp_async_commit();
@@ -517,7 +541,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         };
         const int64_t Ua = unit_at(gw * Ctot / W), Ub = unit_at((gw + 1) * Ctot / W);
         const int nun = static_cast<int>(Ub - Ua);
-        const int stage_budget = (n_copies + n_lines + kThreadsD - 1) / kThreadsD / max(nun, 1) + 1;
+        const int stage_budget = MODE == DecodeMode::kForward ? n_slots / max(nun, 1) + 1 : 0;
 
         uint4 wr[DEPTH][4][PC1][2];
         float sr[DEPTH][4][PC1];
@@ -846,7 +870,10 @@ bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t 
         static_cast<size_t>(pl.rows_pc) * (I / 2 + 16) + static_cast<size_t>(pl.rows_pc) * (I / g) * 4;
     const size_t fixed = pl.off_w2s;
     if (fixed > static_cast<size_t>(max_smem)) return false;
-    const int64_t fit = mode == DecodeMode::kForward ? static_cast<int64_t>((max_smem - fixed) / slot_bytes) : 0;
+    // the staging gives each thread at most kStagePos copy positions per slot
+    const int64_t copies_per_slot = static_cast<int64_t>(pl.rows_pc) * (I / 32 + (I / g) / 4);
+    const bool stageable = copies_per_slot <= static_cast<int64_t>(kStagePosMax) * kThreadsD;
+    const int64_t fit = mode == DecodeMode::kForward && stageable ? static_cast<int64_t>((max_smem - fixed) / slot_bytes) : 0;
     pl.smem_slots = static_cast<int>(std::min<int64_t>(fit, MS));
     pl.smem_bytes = static_cast<int>(fixed + pl.smem_slots * slot_bytes);
     *out = pl;

@@ -162,18 +162,30 @@ __device__ __forceinline__ uint4 ld_nc16(const void* p) {
 }
 
 // Eight packed int4 codes (element e at bits 4e) -> fp16 pairs (0,4) (1,5) (2,6) (3,7).
-// A nibble n in offset binary (n ^ 8 = code + 8) placed in an fp16 0x6400 | n
-// is 1024 + code + 8; subtracting 1032 leaves the code exactly.
+// A nibble n of a two's-complement code c satisfies n ^ 8 = c + 8.  Placed in
+// the low 4 mantissa bits of fp16 0x6400 (1024) it gives 1024 + c + 8, so
+// subtracting 1032 leaves c; placed 4 bits higher it gives 1024 + 16 (c + 8),
+// and x / 16 - 72 = c (one exact fma).  Each (w & mask) ^ (0x6400.. | 8-bit)
+// is a single three-input logic op.
 __device__ __forceinline__ uint4 unpack_int4_f16(uint32_t w) {
-    const uint32_t o = w ^ 0x88888888u;
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+    const __half2 sub = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+    const __half2 s16 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));   // 1/16
+    const __half2 b72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));   // -72
+    const uint32_t w8 = w >> 8;
+    uint32_t p[4];
+    p[0] = (w & 0x000F000Fu) ^ 0x64086408u;
+    p[1] = (w & 0x00F000F0u) ^ 0x64806480u;
+    p[2] = (w8 & 0x000F000Fu) ^ 0x64086408u;
+    p[3] = (w8 & 0x00F000F0u) ^ 0x64806480u;
     uint32_t r[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const uint32_t bits = ((o >> (4 * e)) & 0x000F000Fu) | 0x64006400u;
-        const __half2 hv = __hsub2(*reinterpret_cast<const __half2*>(&bits), bias);
-        r[e] = *reinterpret_cast<const uint32_t*>(&hv);
-    }
+    const __half2 h0 = __hsub2(*reinterpret_cast<const __half2*>(&p[0]), sub);
+    const __half2 h1 = __hfma2(*reinterpret_cast<const __half2*>(&p[1]), s16, b72);
+    const __half2 h2 = __hsub2(*reinterpret_cast<const __half2*>(&p[2]), sub);
+    const __half2 h3 = __hfma2(*reinterpret_cast<const __half2*>(&p[3]), s16, b72);
+    r[0] = *reinterpret_cast<const uint32_t*>(&h0);
+    r[1] = *reinterpret_cast<const uint32_t*>(&h1);
+    r[2] = *reinterpret_cast<const uint32_t*>(&h2);
+    r[3] = *reinterpret_cast<const uint32_t*>(&h3);
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
