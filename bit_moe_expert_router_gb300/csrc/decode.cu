@@ -18,16 +18,18 @@
 //            intermediate indices (2 gate rows + the 2 matching up rows) of
 //            one slot; each warp takes a contiguous unit range of equal cost
 //            (streaming + per-token work, so the always-on shared expert's
-//            multi-token units weigh more).  A warp
-//            keeps up to four units of 16-byte loads in flight in
-//            registers; each lane covers a 64-value K piece, folds its exact
-//            int32 piece sum with the piece's group scale, and a 4-row
-//            reduce-scatter across the warp (6 shuffles) gives the row sums;
-//            h = SiLU(G_gate) * G_up goes to the workspace and |h| into the
-//            row's running maximum (fire-and-forget atomic max).  Meanwhile
-//            each CTA copies its slice of the down-projection bank (its
-//            output rows of every touched slot) into shared memory, or warms
-//            it in L2 where shared memory runs out.
+//            multi-token units weigh more).  A warp keeps up to three units
+//            of 16-byte loads in flight in registers (lane l loads pieces
+//            l, l + 32, ... of each row, so each warp load reads 512
+//            contiguous bytes); each lane folds the exact int32 sum of each
+//            32-value piece with its group scale, and a 4-row reduce-scatter
+//            across the warp (6 shuffles) gives the row sums; h = SiLU(G_gate)
+//            * G_up goes to the workspace and |h| into the warp's running row
+//            maximum in shared memory (merged into the global row maxima once
+//            per CTA at the end of the phase).  Meanwhile each CTA copies its
+//            slice of the down-projection bank (its output rows of every
+//            touched slot) into shared memory, or warms it in L2 where shared
+//            memory runs out.
 //   barrier  one grid-wide barrier (bounded wait; on timeout the status
 //            word records it and the CTAs leave).
 //   phase 2  every CTA requantises all pair rows from h and the row maxima
@@ -520,7 +522,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
 
     // ---------------------------------------------------------------- phase 1
     if (MODE != DecodeMode::kGemm2Partials) {
-        constexpr int DEPTH = PC1 == 1 ? 4 : 2;  // units of loads in flight per warp
+        constexpr int DEPTH = PC1 == 1 ? 3 : 2;  // units of loads in flight per warp
         const int upe = I / 2;                    // units per slot
         // each warp takes a contiguous unit range of equal cost: a CTA's warps
         // stream neighbouring rows, and few slots (pages) per SM
@@ -543,8 +545,11 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         const int nun = static_cast<int>(Ub - Ua);
         const int stage_budget = MODE == DecodeMode::kForward ? n_slots / max(nun, 1) + 1 : 0;
 
-        uint4 wr[DEPTH][4][PC1][2];
-        float sr[DEPTH][4][PC1];
+        // lane l owns the 16-byte pieces l + 32 p of each row (32 codes each, p <
+        // NP): every load instruction of a warp reads 512 contiguous bytes
+        constexpr int NP = 2 * PC1;
+        uint4 wr[DEPTH][4][NP];
+        float sr[DEPTH][4][NP];
         auto issue = [&](int un, int d) {
             const int64_t U = Ua + un;
             const int u = static_cast<int>(U / upe), ip = static_cast<int>(U % upe);
@@ -554,52 +559,48 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                 const int64_t row = e * 2 * I + (r >= 2 ? I : 0) + 2 * ip + (r & 1);
                 const uint8_t* wp = a.w13 + row * (H / 2);
 #pragma unroll
-                for (int j = 0; j < PC1; ++j) {
-                    wr[d][r][j][0] = ld_stream16(wp + 32 * (lane + 32 * j));
-                    wr[d][r][j][1] = ld_stream16(wp + 32 * (lane + 32 * j) + 16);
-                    if (MODE == DecodeMode::kForward) sr[d][r][j] = __ldg(a.s13 + row * ng1 + (64 * (lane + 32 * j)) / g);
+                for (int p = 0; p < NP; ++p) {
+                    wr[d][r][p] = ld_stream16(wp + 16 * lane + 512 * p);
+                    if (MODE == DecodeMode::kForward) sr[d][r][p] = __ldg(a.s13 + row * ng1 + (32 * lane + 1024 * p) / g);
                 }
             }
         };
 #pragma unroll
         for (int d = 0; d < DEPTH; ++d)
             if (d < nun) issue(d, d);
-        const int lpg = g / 64;  // lanes per K group
+        const int lpg = g / 32;  // lanes per K group (per piece index)
         for (int base = 0; base < nun; base += DEPTH) {
 #pragma unroll
             for (int d = 0; d < DEPTH; ++d) {
                 const int un = base + d;
                 if (un >= nun) break;
-                const uint4(&w)[4][PC1][2] = wr[d];
-                const float(&sc)[4][PC1] = sr[d];
+                const uint4(&w)[4][NP] = wr[d];
+                const float(&sc)[4][NP] = sr[d];
                 const int64_t U = Ua + un;
                 const int u = static_cast<int>(U / upe), ip = static_cast<int>(U % upe);
                 const int row0 = s.slot_row0[u], cnt = s.slot_cnt[u];
                 for (int m = 0; m < cnt; ++m) {
                     const int prow = row0 + m;
                     const int t = s.row_tok[prow];
-                    int P[4][PC1];
+                    int P[4][NP];
 #pragma unroll
-                    for (int j = 0; j < PC1; ++j) {
-                        const uint8_t* xp = s.x + t * XS + 64 * (lane + 32 * j);
+                    for (int p = 0; p < NP; ++p) {
+                        const uint8_t* xp = s.x + t * XS + 32 * lane + 1024 * p;
                         const uint4 x0 = *reinterpret_cast<const uint4*>(xp);
                         const uint4 x1 = *reinterpret_cast<const uint4*>(xp + 16);
-                        const uint4 x2 = *reinterpret_cast<const uint4*>(xp + 32);
-                        const uint4 x3 = *reinterpret_cast<const uint4*>(xp + 48);
 #pragma unroll
-                        for (int r = 0; r < 4; ++r)
-                            P[r][j] = dot32(w[r][j][0], x0, x1) + dot32(w[r][j][1], x2, x3);
+                        for (int r = 0; r < 4; ++r) P[r][p] = dot32(w[r][p], x0, x1);
                     }
                     if (MODE == DecodeMode::kGemm1Partials) {
 #pragma unroll
                         for (int r = 0; r < 4; ++r)
 #pragma unroll
-                            for (int j = 0; j < PC1; ++j) {
-                                int v = P[r][j];
+                            for (int p = 0; p < NP; ++p) {
+                                int v = P[r][p];
                                 for (int off = 1; off < lpg; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
                                 if ((lane % lpg) == 0) {
                                     const int64_t wrow = (r >= 2 ? I : 0) + 2 * ip + (r & 1);
-                                    a.p1[(static_cast<int64_t>(prow) * 2 * I + wrow) * ng1 + (64 * (lane + 32 * j)) / g] =
+                                    a.p1[(static_cast<int64_t>(prow) * 2 * I + wrow) * ng1 + (32 * lane + 1024 * p) / g] =
                                         v >> 4;
                                 }
                             }
@@ -610,7 +611,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                     for (int r = 0; r < 4; ++r) {
                         v[r] = 0.f;
 #pragma unroll
-                        for (int j = 0; j < PC1; ++j) v[r] = fmaf(static_cast<float>(P[r][j] >> 4), sc[r][j], v[r]);
+                        for (int p = 0; p < NP; ++p) v[r] = fmaf(static_cast<float>(P[r][p] >> 4), sc[r][p], v[r]);
                     }
                     // reduce-scatter of the 4 row sums: lane keeps row 2*bit4 + bit3
                     const bool b4 = lane & 16, b3 = lane & 8;

@@ -12,21 +12,28 @@
 // epilogue warps while the tensor core fills the other buffer.
 //
 // Tile: M = 128 weight rows x N <= 128 tokens of one bank slot, one K
-// group (128 values) per pipeline stage, 3 stages in shared memory in the
-// 128-byte-swizzled K-major layout the MMA reads.  Gate/up tiles interleave
-// the rows (tile row 2j = gate row i, 2j + 1 = up row i, i = 64 m + j), so
-// the SiLU(gate) * up product pairs neighbouring lanes.  The MMA width N is
-// the token count of the tile rounded up to 16.  Persistent CTAs (one per
-// SM) walk the (slot, token tile, weight tile) items with the weight tile
-// fastest, so the CTAs working at one time share the token tile in L2.
+// group (128 values) per pipeline stage, 4 stages.  The A operand (the
+// unpacked weights, fp16) goes to tensor memory -- each producer thread
+// writes its row's 64 columns into its own lane with tcgen05.st -- and the
+// B operand (token rows, fp16) to shared memory in the 128-byte-swizzled
+// K-major layout the MMA reads; A thus never passes through shared memory,
+// whose bandwidth the MMA's B reads and the B copies then share alone.
+// Gate/up tiles interleave the rows (tile row 2j = gate row i, 2j + 1 = up
+// row i, i = 64 m + j), so the SiLU(gate) * up product pairs neighbouring
+// lanes.  The MMA width N is the token count of the tile rounded up to 16.
+// Persistent CTAs (one per SM) walk the (slot, token tile, weight tile)
+// items with the weight tile fastest, so the CTAs working at one time share
+// the token tile in L2.  Tensor memory: 2 accumulators x 128 columns + 4 A
+// stages x 64 columns = all 512 columns.
 //
 // Thirteen warps (four of them share one SM sub-partition, whose 16K-register
 // file then caps a thread at 128 registers).  Warp roles: warps 0-7
 // epilogue (warp w: TMEM lanes 32 (w % 4) .. +31 = tile rows, columns
 // 64 (w / 4) .. +63), warps 8-11 producers (thread = tile row: unpack 64
-// packed bytes of its weight row into fp16, cp.async its token row's 256
-// bytes), warp 12 issues the MMAs (one thread) and owns the TMEM allocation.  Every wait is
-// bounded; a timeout sets the status word and every role leaves cleanly.
+// packed bytes of its weight row into fp16 and store them to its TMEM lane,
+// cp.async its token row's 256 bytes), warp 12 issues the MMAs (one thread)
+// and owns the TMEM allocation.  Every wait is bounded; a timeout sets the
+// status word and every role leaves cleanly.
 //
 // K order: the weight unpack turns a packed word (codes 0..7) into fp16
 // pairs (0,4) (1,5) (2,6) (3,7); the token rows are converted to fp16 in
@@ -48,15 +55,18 @@ constexpr int kMmaWarp = kEpiWarps + kProdWarps;
 constexpr int kTcThreads = 32 * (kMmaWarp + 1);
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kHalfN = 64;                   // columns per epilogue warp
-constexpr int kNS = 3;
+constexpr int kNS = 4;                       // pipeline stages: A in tensor memory, B in shared memory
 constexpr int kTileN = 128;
 constexpr int kAtom = 16384;                 // 128 rows x 128 bytes
-constexpr int kStageA = 2 * kAtom, kStageB = 2 * kAtom, kStage = kStageA + kStageB;
+constexpr int kStage = 2 * kAtom;             // B: 128 token rows x 128 fp16 (two swizzled atoms)
+constexpr int kACols = 64;                   // A: 128 rows x 128 fp16 = 64 tensor-memory columns per stage
 constexpr int kMaxSlotsTc = kTcMaxSlots + 1;
-constexpr int kAcc = 4;                      // accumulator buffers in tensor memory (128 columns each)
+constexpr int kAcc = 2;                      // accumulator buffers in tensor memory (128 columns each)
+constexpr int kTmemCols = 512;               // kAcc * 128 accumulator columns + kNS * kACols A columns
 constexpr int kRaw = 3;                      // packed weight rows in flight ahead of the unpack
 constexpr int kRawStage = 128 * 64;          // 128 rows x 64 packed bytes (128 codes)
-constexpr int kSmemTc = kNS * kStage + kRaw * kRawStage + 128 * 4 + 128 * 4 + (kMaxSlotsTc + 16) * 4 + 256 + 1024;
+constexpr int kSmemTc =
+    kNS * kStage + kRaw * kRawStage + 128 * 4 + 128 * 4 + 2 * 128 * 4 + (kMaxSlotsTc + 16) * 4 + 256 + 1024;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -128,6 +138,13 @@ __device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
         "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
+// Same MMA with the A operand read from tensor memory (lane = row, K along the columns).
+__device__ __forceinline__ void mma_f16_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
                  : "memory");
@@ -151,6 +168,23 @@ __device__ __forceinline__ float ld_nc_f32(const float* p) {
     float v;
     asm volatile("ld.global.nc.f32 %0, [%1];\n" : "=f"(v) : "l"(p));
     return v;
+}
+
+// 64 consecutive 32-bit tensor-memory columns of this thread's lane <- v; waits for the store.
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&v)[64]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,"
+        "%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
+        "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};\n" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]), "r"(v[32]), "r"(v[33]), "r"(v[34]), "r"(v[35]), "r"(v[36]),
+        "r"(v[37]), "r"(v[38]), "r"(v[39]), "r"(v[40]), "r"(v[41]), "r"(v[42]), "r"(v[43]), "r"(v[44]), "r"(v[45]),
+        "r"(v[46]), "r"(v[47]), "r"(v[48]), "r"(v[49]), "r"(v[50]), "r"(v[51]), "r"(v[52]), "r"(v[53]), "r"(v[54]),
+        "r"(v[55]), "r"(v[56]), "r"(v[57]), "r"(v[58]), "r"(v[59]), "r"(v[60]), "r"(v[61]), "r"(v[62]), "r"(v[63])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
 __device__ __forceinline__ uint4 ld_nc16(const void* p) {
@@ -218,7 +252,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
     uint8_t* raw = smem + kNS * kStage;                           // [kRaw][128][64] packed weight rows
     float* colf = reinterpret_cast<float*>(raw + kRaw * kRawStage);  // [128] B-row scales of the item
     int* colp = reinterpret_cast<int*>(colf + 128);               // [128] pair rows of the item
-    int* prefix = colp + 128;                                     // [kMaxSlotsTc + 1] items before each slot
+    int* brow_tab = colp + 128;                                   // [2][128] B rows of an item (-1: none)
+    int* prefix = brow_tab + 2 * 128;                             // [kMaxSlotsTc + 1] items before each slot
     uint64_t* bars = reinterpret_cast<uint64_t*>(prefix + kMaxSlotsTc + 16);
     uint64_t* full = bars;
     uint64_t* empty = bars + kNS;
@@ -251,7 +286,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
     }
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tmem_holder)),
-                     "r"(kAcc * 128));
+                     "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
     // items of each slot -> exclusive prefix (every CTA computes it)
@@ -349,24 +384,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
         };
 #pragma unroll
         for (int d = 0; d < kRaw; ++d) fetch_next();
-        int use = 0;
+        int use = 0, item_n = 0;
         bool ok = true;
-        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        for (int item = blockIdx.x; item < total; item += gridDim.x) {
             const Item it = decode_item(item);
-            int64_t brow = pt < it.ntok ? (a.b_row ? a.b_row[it.row0 + pt] : it.row0 + pt) : -1;
-            const bool bvalid = brow >= 0 && brow < a.b_rows;
-            const __half* bsrc = a.b + (bvalid ? brow : 0) * K;
+            // B rows of this item, shared by the four producer warps: a warp's
+            // copy instruction covers two whole 256-byte row segments (16 lanes
+            // per row), not 32 scattered pieces.  Double-buffered by item parity;
+            // the barrier orders this item's writes after every producer thread
+            // finished the item two back, and makes a give-up unanimous.
+            {
+                const int64_t brow = pt < it.ntok ? (a.b_row ? a.b_row[it.row0 + pt] : it.row0 + pt) : -1;
+                brow_tab[(item_n & 1) * 128 + pt] = (brow >= 0 && brow < a.b_rows) ? static_cast<int>(brow) : -1;
+                if (named_bar_or(2, 128, !ok)) break;
+            }
+            const int* btab = brow_tab + (item_n & 1) * 128;
+            ++item_n;
             for (int ks = 0; ks < ksteps; ++ks, ++use) {
                 const int s = use % kNS;
                 if (!wait_bar(empty + s, ((use / kNS) & 1) ^ 1, ctl)) {
                     ok = false;
                     break;
                 }
-                uint8_t* As = stages + s * kStage;
-                uint8_t* Bs = As + kStageA;
+                tc_fence_after();  // the stage's previous MMAs (which read its A columns) are complete
+                uint8_t* Bs = stages + s * kStage;
+                const int pw = warp - kEpiWarps, chunk = lane & 15;
 #pragma unroll
-                for (int w = 0; w < 16; ++w)
-                    cp_async16(Bs + (w >> 3) * kAtom + swz(pt, w), bsrc + 128 * ks + 8 * w, bvalid ? 16 : 0);
+                for (int i = 0; i < 16; ++i) {
+                    const int row = 32 * pw + 2 * i + (lane >> 4);
+                    const int br = btab[row];
+                    cp_async16(Bs + (chunk >> 3) * kAtom + swz(row, chunk),
+                               a.b + static_cast<int64_t>(br >= 0 ? br : 0) * K + 128 * ks + 8 * chunk, br >= 0 ? 16 : 0);
+                }
                 asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(full + s))
                              : "memory");
                 cp_async_wait<kRaw - 1>();  // this use's raw bytes (fetched kRaw calls ago) have landed
@@ -374,20 +423,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                 uint4 rw[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) rw[q] = rp[q ^ rsw];
+                // unpacked row -> this thread's tensor-memory lane, 64 columns of
+                // fp16 pairs (column c holds K positions 2c, 2c + 1 of the stage)
+                uint32_t av[64];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const uint32_t words[4] = {rw[q].x, rw[q].y, rw[q].z, rw[q].w};
 #pragma unroll
                     for (int wi = 0; wi < 4; ++wi) {
-                        const int w = 4 * q + wi;
-                        *reinterpret_cast<uint4*>(As + (w >> 3) * kAtom + swz(pt, w)) = unpack_int4_f16(words[wi]);
+                        const uint4 u4 = unpack_int4_f16(words[wi]);
+                        const int c = 4 * (4 * q + wi);
+                        av[c] = u4.x;
+                        av[c + 1] = u4.y;
+                        av[c + 2] = u4.z;
+                        av[c + 3] = u4.w;
                     }
                 }
+                tmem_st64(tmem + (static_cast<uint32_t>(32 * (warp - kEpiWarps)) << 16) + kAcc * 128 + kACols * s, av);
                 // the raw slot just consumed is refilled kRaw uses ahead (after its
                 // bytes were used: no copy may overwrite them before they are read)
                 asm volatile("" ::: "memory");
                 fetch_next();
-                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                tc_fence_before();
                 mbar_arrive(full + s);
             }
         }
@@ -410,11 +467,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(stages + s * kStage), b0 = a0 + kStageA;
+                    const uint32_t b0 = smem_u32(stages + s * kStage);
+                    const uint32_t ta = tmem + kAcc * 128 + kACols * s;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
+                    for (int kk = 0; kk < 8; ++kk) {  // K = 16 per MMA: 8 A columns, 32 B of a B row
                         const uint32_t off = (kk >> 2) * kAtom + 32 * (kk & 3);
-                        mma_f16(tmem + b * 128, sdesc(a0 + off), sdesc(b0 + off), idesc, (sub > 0 || kk > 0) ? 1u : 0u);
+                        mma_f16_ta(tmem + b * 128, ta + 8 * kk, sdesc(b0 + off), idesc, (sub > 0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(empty + s);
                     if (sub == spg - 1) {
@@ -516,7 +574,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kAcc * 128));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
     }
 }
 
