@@ -73,6 +73,7 @@ int cuda_status(cudaError_t e, const char* what) {
 struct Views {
     moe::Header* hdr;
     uint32_t* flags;
+    int8_t* hq;
     float* sh;
     int32_t *ids, *seg_cnt, *seg_off, *perm, *inv, *row_token, *chunk_counts, *tile_slot, *tile_row0;
     float *wts, *h, *y;
@@ -84,6 +85,7 @@ Views views(void* ws, const WsLayout& L) {
     Views v;
     v.hdr = moe::ws_at<moe::Header>(ws, L.hdr);
     v.flags = moe::ws_at<uint32_t>(ws, L.flags);
+    v.hq = moe::ws_at<int8_t>(ws, L.hq);
     v.sh = moe::ws_at<float>(ws, L.sh);
     v.ids = moe::ws_at<int32_t>(ws, L.ids);
     v.wts = moe::ws_at<float>(ws, L.wts);
@@ -154,6 +156,8 @@ int run_decode(const int8_t* x_q, const float* x_scale, const float* logits, con
     a.out = out;
     a.hdr = v.hdr;
     a.row_max = v.flags;
+    a.hq_g = v.hq;
+    a.sh_g = v.sh;
     a.h = v.h;
     a.amax = v.amax;
     a.y = y_debug;

@@ -36,7 +36,7 @@ constexpr int kFlagWords = 1024;  // per-call words after the header, cleared wi
 struct WsLayout {
     int64_t Tk = 0, P = 0, n_chunks = 0, max_tiles = 0, slots = 0;
     size_t hdr = 0, flags = 0, ids = 0, wts = 0, seg_cnt = 0, seg_off = 0, perm = 0, inv = 0, row_token = 0,
-           chunk_counts = 0, tile_slot = 0, tile_row0 = 0, amax = 0, h = 0, sh = 0, y = 0, x16 = 0, h16 = 0,
+           chunk_counts = 0, tile_slot = 0, tile_row0 = 0, amax = 0, h = 0, hq = 0, sh = 0, y = 0, x16 = 0, h16 = 0,
            total = 0;
 };
 
@@ -66,6 +66,7 @@ inline WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S,
     L.tile_row0 = take(sizeof(int32_t) * L.max_tiles);
     L.amax = take(sizeof(uint32_t) * L.P);
     L.h = take(sizeof(float) * L.P * I);
+    L.hq = take(static_cast<size_t>(L.P) * I);
     L.sh = take(sizeof(float) * L.P);
     L.y = take(sizeof(float) * L.P * H);
     L.x16 = take(2 * static_cast<size_t>(Tx < 0 ? T : Tx) * H);  // tcgen05 engine operands (fp16)

@@ -373,6 +373,15 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     const bool routed = MODE == DecodeMode::kForward;
 
     // ---------------------------------------------------------------- phase 0
+    // the first activation pieces are loaded now, so their latency overlaps the routing
+    constexpr int kXPre = 4;
+    const int per_tok = H / 16, n_xp = MODE == DecodeMode::kGemm2Partials ? 0 : T * per_tok;
+    uint4 xpre[kXPre];
+#pragma unroll
+    for (int i = 0; i < kXPre; ++i) {
+        const int o = tid + kThreadsD * i;
+        if (o < n_xp) xpre[i] = *reinterpret_cast<const uint4*>(a.x_q + static_cast<int64_t>(o / per_tok) * H + 16 * (o % per_tok));
+    }
     int n_rows;  // routed/listed pair rows before the shared rows
     if (routed) {
         if (a.E <= 512) route_tokens<16>(a.logits, T, a.E, k, s.ids, s.wts, s.cand_k, s.cand_i);
@@ -384,8 +393,12 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     }
     // activations: [t][H + 16], each 8-byte group split even|odd (independent of routing)
     if (MODE != DecodeMode::kGemm2Partials) {
-        const int per_tok = H / 16;
-        for (int o = tid; o < T * per_tok; o += kThreadsD) {
+#pragma unroll
+        for (int i = 0; i < kXPre; ++i) {
+            const int o = tid + kThreadsD * i;
+            if (o < n_xp) *reinterpret_cast<uint4*>(s.x + (o / per_tok) * XS + 16 * (o % per_tok)) = split16(xpre[i]);
+        }
+        for (int o = tid + kThreadsD * kXPre; o < n_xp; o += kThreadsD) {
             const int t = o / per_tok, c = o % per_tok;
             const uint4 v = *reinterpret_cast<const uint4*>(a.x_q + static_cast<int64_t>(t) * H + 16 * c);
             *reinterpret_cast<uint4*>(s.x + t * XS + 16 * c) = split16(v);
@@ -663,53 +676,53 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
 
     // ---------------------------------------------------------------- phase 2
     const int P = n_rows + T * S;
-    {
-        // (a) the requantised rows, split even|odd, into shared memory: every
-        // CTA requantises all P rows itself from h (L2) and the row maxima
-        const int per_row = I / 16;
-        if (MODE == DecodeMode::kForward) {
-            for (int p = tid; p < P; p += kThreadsD) {
-                const uint32_t mb = __ldcg(a.row_max + p);
-                s.sh[p] = requant_scale(mb);
-                if (a.amax && blockIdx.x == 0) a.amax[p] = mb;
+    const int per_row = I / 16;
+    if (MODE == DecodeMode::kForward) {
+        // (a) requantisation, spread over the grid: row p goes to CTA p % grid,
+        // one warp per row -- s_h from the row maximum, RNE codes -- stored
+        // split even|odd to the workspace; a second grid barrier publishes them
+        for (int p = static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) * warp; p < P;
+             p += static_cast<int>(gridDim.x) * kWarpsD) {
+            const uint32_t mb = __ldcg(a.row_max + p);
+            const float sc = requant_scale(mb);
+            const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+            if (lane == 0) {
+                a.sh_g[p] = sc;
+                if (a.amax) a.amax[p] = mb;
             }
+#pragma unroll
+            for (int c2 = 0; c2 < PC2; ++c2) {  // 16 values per lane per 512-value chunk
+                const float4* src = reinterpret_cast<const float4*>(a.h + static_cast<int64_t>(p) * I + 512 * c2 + 16 * lane);
+                float4 f[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) f[q] = __ldcg(src + q);
+                uint32_t wds[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    wds[q] = (requant_code_fast(f[q].x, sc, rs) & 0xFF) | ((requant_code_fast(f[q].y, sc, rs) & 0xFF) << 8) |
+                             ((requant_code_fast(f[q].z, sc, rs) & 0xFF) << 16) |
+                             ((static_cast<uint32_t>(requant_code_fast(f[q].w, sc, rs)) & 0xFF) << 24);
+                *reinterpret_cast<uint4*>(a.hq_g + static_cast<int64_t>(p) * I + 512 * c2 + 16 * lane) =
+                    split16(make_uint4(wds[0], wds[1], wds[2], wds[3]));
+            }
+        }
+        if (!grid_barrier(a.hdr, 2)) {
+            cp_async_wait<0>();
             __syncthreads();
-            // 4 chunks (16 values each) per thread at a time, all 16 loads issued first
-            const int n_chunks = P * per_row;
-            for (int o0 = tid; o0 < n_chunks; o0 += 4 * kThreadsD) {
-                float4 f[4][4];
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int o = min(o0 + b * kThreadsD, n_chunks - 1);
-                    const float4* src = reinterpret_cast<const float4*>(a.h + static_cast<int64_t>(o / per_row) * I +
-                                                                        16 * (o % per_row));
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) f[b][q] = __ldcg(src + q);
-                }
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int o = o0 + b * kThreadsD;
-                    if (o >= n_chunks) break;
-                    const int p = o / per_row, c = o % per_row;
-                    const float sc = s.sh[p];
-                    const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
-                    uint32_t wds[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 v = f[b][q];
-                        wds[q] = (requant_code_fast(v.x, sc, rs) & 0xFF) | ((requant_code_fast(v.y, sc, rs) & 0xFF) << 8) |
-                                 ((requant_code_fast(v.z, sc, rs) & 0xFF) << 16) |
-                                 ((static_cast<uint32_t>(requant_code_fast(v.w, sc, rs)) & 0xFF) << 24);
-                    }
-                    *reinterpret_cast<uint4*>(s.hq + p * HQS + 16 * c) = split16(make_uint4(wds[0], wds[1], wds[2], wds[3]));
-                }
-            }
-        } else {
-            for (int o = tid; o < P * per_row; o += kThreadsD) {
-                const int p = o / per_row, c = o % per_row;
-                const uint4 v = *reinterpret_cast<const uint4*>(a.h_q_in + static_cast<int64_t>(p) * I + 16 * c);
-                *reinterpret_cast<uint4*>(s.hq + p * HQS + 16 * c) = split16(v);
-            }
+            return;
+        }
+        // (b) every CTA copies all P requantised rows (already split) and their scales
+        for (int o = tid; o < P * per_row; o += kThreadsD) {
+            const int p = o / per_row, c = o % per_row;
+            cp_async16(s.hq + p * HQS + 16 * c, a.hq_g + static_cast<int64_t>(p) * I + 16 * c);
+        }
+        for (int p = tid; p < P; p += kThreadsD) s.sh[p] = __ldcg(a.sh_g + p);
+        cp_async_commit();
+    } else {
+        for (int o = tid; o < P * per_row; o += kThreadsD) {
+            const int p = o / per_row, c = o % per_row;
+            const uint4 v = *reinterpret_cast<const uint4*>(a.h_q_in + static_cast<int64_t>(p) * I + 16 * c);
+            *reinterpret_cast<uint4*>(s.hq + p * HQS + 16 * c) = split16(v);
         }
     }
     cp_async_wait<0>();

@@ -32,6 +32,8 @@ struct DecodeArgs {
     // workspace
     Header* hdr;
     uint32_t* row_max;       // [P] running max |h| per pair row (float bits), cleared before the launch
+    int8_t* hq_g;            // [P][I] requantised rows, each 8-byte group split even|odd
+    float* sh_g;             // [P] their scales
     float* h;                // [P][I]
     uint32_t* amax;          // [P] row maxima (debug copies; may be null)
     float* y;                // [P][H] (debug copies; may be null)
