@@ -144,6 +144,27 @@ def _touched_bytes(w, logits_batches):
     return float(np.mean(tot)), per_expert
 
 
+# DRAM traffic per launch of the decode kernel, from an ncu capture of the
+# decode workload (dram__bytes_read.sum + dram__bytes_write.sum), valid only
+# for the kernel source it was taken on: the file records the SHA-1 of
+# csrc/decode.cu at capture time, and a changed kernel reports null.
+TRAFFIC_FILE = os.path.join(REPO, "bit_moe_expert_router_gb300", "ncu_traffic.json")
+
+
+def _decode_traffic(workload: str):
+    import hashlib
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get("decode_kernel", {})
+        with open(os.path.join(REPO, "bit_moe_expert_router_gb300", "csrc", "decode.cu"), "rb") as f:
+            sha = hashlib.sha1(f.read()).hexdigest()
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha1") != sha or rec.get("workload") != workload:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
 def run_ours(a):
     import torch
     from bit_moe_expert_router_gb300 import binding, synth
@@ -286,7 +307,8 @@ def run_ours(a):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": a.steps * launches_per_step,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "peak_source": peak_kind,
+                     "traffic": _decode_traffic(w.name) if engine == binding.ENGINE_DECODE else None,
+                     "peak_source": peak_kind,
                      "kernel": kernel_label, "algorithmic_bytes_per_step": alg_bytes,
                      "bytes_per_touched_expert": per_expert},
         "clocks": clk,

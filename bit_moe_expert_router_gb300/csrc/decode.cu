@@ -84,6 +84,30 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p)); }
 
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// global to shared memory, its completion counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
@@ -131,6 +155,23 @@ __device__ __forceinline__ float key_value(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// Bounded wait for the first phase of the slice-copy barrier; false (and the
+// status word set) if it runs out.
+__device__ bool w2_wait(uint64_t* bar, Header* hdr) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, 0)) return true;
+        if ((it & 15) == 15) {
+            const uint64_t t = global_ns();
+            if (t0 == 0) t0 = t;
+            if (t - t0 > kWaitNs || it > kSpinCap) {
+                atomicOr(&hdr->status, kDevTimeout);
+                return false;
+            }
+        }
+    }
+}
+
 // (key a, id ia) ranks before (key b, id ib): larger key, or equal key and lower id.
 __device__ __forceinline__ bool ranks_before(uint32_t a, uint32_t ia, uint32_t b, uint32_t ib) {
     return a > b || (a == b && ia < ib);
@@ -149,7 +190,6 @@ __device__ __forceinline__ bool ranks_before(uint32_t a, uint32_t ia, uint32_t b
 // Then the weights: softmax over the k selected logits, relative to the
 // largest.  ids/wts: [T][k]; cand_k/cand_i: kCand per warp.
 constexpr int kCand = 64;
-constexpr int kStagePosMax = 4;  // down-projection staging: copy positions per thread and slot
 
 template <int NJ>
 __device__ void route_tokens(const float* __restrict__ logits, int T, int E, int k, int* ids, float* wts,
@@ -328,6 +368,7 @@ struct Smem {
     int* first;       // [rows] pair is the first of its expert (by pair index)
     int* eqc;         // [rows] pairs with the same expert
     float* wmax;      // [warps][P] each warp's running max |h| per pair row
+    uint64_t* w2bar;  // completion of the down-projection slice copies
     uint8_t* w2s;     // [smem_slots][slot_stride] staged down-projection slices
 };
 
@@ -353,6 +394,7 @@ __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
     s.first = reinterpret_cast<int*>(base + pl.off_first);
     s.eqc = reinterpret_cast<int*>(base + pl.off_eqc);
     s.wmax = reinterpret_cast<float*>(base + pl.off_wmax);
+    s.w2bar = reinterpret_cast<uint64_t*>(base + pl.off_w2bar);
     s.w2s = base + pl.off_w2s;
     return s;
 }
@@ -371,6 +413,11 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     const int XS = H + 16, HQS = I + 16;
     const int RS = I / 2 + 16;  // staged down-projection row stride
     const bool routed = MODE == DecodeMode::kForward;
+
+    if (tid == 0) {
+        mbar_init(s.w2bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
 
     // ---------------------------------------------------------------- phase 0
     // the first activation pieces are loaded now, so their latency overlaps the routing
@@ -473,64 +520,36 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     __syncthreads();
 
     // This CTA's down-projection slice (rows [n0, n0 + nrows) of every slot):
-    // the first n_smem slots are copied into shared memory with cp.async, the
-    // rest warmed in L2.  Thread tid owns the same copy positions (row, 16-byte
-    // piece) in every slot -- computed once -- and walks the slots a few per
-    // phase-1 unit, so the requests queue behind the phase-1 loads.
+    // the first n_smem slots are copied into shared memory by the bulk-copy
+    // engine (one copy per row, so the rows keep their padded stride, and one
+    // for the scales; completion on one mbarrier), the rest warmed in L2.
+    // Lane 0 of warp w stages slots w, w + 8, ..., a few per phase-1 unit.
     const int n0 = blockIdx.x * pl.rows_pc;
     const int nrows = max(0, min(pl.rows_pc, H - n0));
     const int n_smem = MODE == DecodeMode::kForward && nrows > 0 ? min(n_slots, pl.smem_slots) : 0;
     const int slot_stride = pl.rows_pc * RS + pl.rows_pc * ng2 * 4;
-    const int wch = I / 32, sch = ng2 / 4;  // 16-byte pieces per row: weights, scales
-    const int per_slot = nrows * (wch + sch);
     const int lines_w = (nrows * (I / 2) + 127) / 128, lines_s = (nrows * ng2 * 4 + 127) / 128;
-    const int n_lines_slot = lines_w + lines_s;
-    // this thread's positions in a slot: up to kStagePos copy pieces and one prefetch line
-    constexpr int kStagePos = kStagePosMax;
-    int pos_dst[kStagePos];
-    int64_t pos_src[kStagePos];  // byte offset from the slot's first row (weights) or its scales
-    bool pos_scale[kStagePos];
-    int n_pos = 0;
-#pragma unroll
-    for (int i = 0; i < kStagePos; ++i) {
-        const int c = tid + kThreadsD * i;
-        pos_dst[i] = 0;
-        pos_src[i] = 0;
-        pos_scale[i] = false;
-        if (c < per_slot) {
-            n_pos = i + 1;
-            if (c < nrows * wch) {
-                const int r = c / wch, q = c % wch;
-                pos_dst[i] = r * RS + 16 * q;
-                pos_src[i] = static_cast<int64_t>(r) * (I / 2) + 16 * q;
-            } else {
-                const int c2 = c - nrows * wch;
-                pos_dst[i] = pl.rows_pc * RS + 16 * c2;
-                pos_src[i] = 16 * c2;
-                pos_scale[i] = true;
-            }
-        }
-    }
-    const bool line_is_w = tid < lines_w;
-    const int64_t line_off = line_is_w ? 128 * tid : 128 * (tid - lines_w);
-    const bool has_line = tid < n_lines_slot && MODE == DecodeMode::kForward && nrows > 0;
-    int next_slot = 0;  // next slot this thread stages (copies or warms)
+    if (tid == 0 && n_smem > 0)  // every staged byte counted before any copy can land
+        mbar_expect_tx(s.w2bar, static_cast<uint32_t>(n_smem * nrows * (I / 2 + ng2 * 4)));
+    __syncthreads();
+    int next_slot = warp;  // next slot this warp stages (copies or warms)
     auto stage_some = [&](int budget) {
-        for (int b = 0; b < budget && next_slot < n_slots; ++b, ++next_slot) {
+        for (int b = 0; b < budget && next_slot < n_slots; ++b, next_slot += kWarpsD) {
             const int u = next_slot;
             const int64_t e = s.slot_e[u];
             const uint8_t* wsrc = a.w2 + (e * H + n0) * static_cast<int64_t>(I / 2);
             const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(a.s2 + (e * H + n0) * ng2);
             if (u < n_smem) {
-                uint8_t* base = s.w2s + u * slot_stride;
-#pragma unroll
-                for (int i = 0; i < kStagePos; ++i)
-                    if (i < n_pos) cp_async16(base + pos_dst[i], (pos_scale[i] ? ssrc : wsrc) + pos_src[i]);
-            } else if (has_line) {
-                prefetch_l2((line_is_w ? wsrc : ssrc) + line_off);
+                if (lane == 0) {
+                    uint8_t* base = s.w2s + u * slot_stride;
+                    for (int r = 0; r < nrows; ++r) bulk_g2s(base + r * RS, wsrc + r * (I / 2), I / 2, s.w2bar);
+                    bulk_g2s(base + pl.rows_pc * RS, ssrc, nrows * ng2 * 4, s.w2bar);
+                }
+            } else {
+                for (int c = lane; c < lines_w + lines_s; c += 32)
+                    prefetch_l2(c < lines_w ? wsrc + 128 * c : ssrc + 128 * (c - lines_w));
             }
         }
-        cp_async_commit();
     };
 
     // ---------------------------------------------------------------- phase 1
@@ -556,7 +575,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         };
         const int64_t Ua = unit_at(gw * Ctot / W), Ub = unit_at((gw + 1) * Ctot / W);
         const int nun = static_cast<int>(Ub - Ua);
-        const int stage_budget = MODE == DecodeMode::kForward ? n_slots / max(nun, 1) + 1 : 0;
+        const int stage_budget = MODE == DecodeMode::kForward ? (n_slots + kWarpsD - 1) / kWarpsD / max(nun, 1) + 1 : 0;
 
         // lane l owns the 16-byte pieces l + 32 p of each row (32 codes each, p <
         // NP): every load instruction of a warp reads 512 contiguous bytes
@@ -669,7 +688,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
 
     // ---------------------------------------------------------------- barrier
     if (MODE == DecodeMode::kForward && !grid_barrier(a.hdr, 1)) {
-        cp_async_wait<0>();  // this thread's own copies land before the CTA leaves
+        if (n_smem > 0) w2_wait(s.w2bar, a.hdr);  // the CTA's bulk copies land before it leaves
         __syncthreads();
         return;
     }
@@ -707,7 +726,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
             }
         }
         if (!grid_barrier(a.hdr, 2)) {
-            cp_async_wait<0>();
+            if (n_smem > 0) w2_wait(s.w2bar, a.hdr);
             __syncthreads();
             return;
         }
@@ -726,6 +745,10 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         }
     }
     cp_async_wait<0>();
+    if (MODE == DecodeMode::kForward && n_smem > 0 && !w2_wait(s.w2bar, a.hdr)) {
+        __syncthreads();
+        return;
+    }
     __syncthreads();
     if (nrows == 0) return;
 
@@ -879,15 +902,13 @@ bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t 
     pl.off_first = take(4 * rows, 16);
     pl.off_eqc = take(4 * rows, 16);
     pl.off_wmax = take(mode == DecodeMode::kForward ? 4 * kWarpsD * P : 0, 16);
+    pl.off_w2bar = take(8, 16);
     pl.off_w2s = static_cast<int>(align_up(o, 128));
     const size_t slot_bytes =
         static_cast<size_t>(pl.rows_pc) * (I / 2 + 16) + static_cast<size_t>(pl.rows_pc) * (I / g) * 4;
     const size_t fixed = pl.off_w2s;
     if (fixed > static_cast<size_t>(max_smem)) return false;
-    // the staging gives each thread at most kStagePos copy positions per slot
-    const int64_t copies_per_slot = static_cast<int64_t>(pl.rows_pc) * (I / 32 + (I / g) / 4);
-    const bool stageable = copies_per_slot <= static_cast<int64_t>(kStagePosMax) * kThreadsD;
-    const int64_t fit = mode == DecodeMode::kForward && stageable ? static_cast<int64_t>((max_smem - fixed) / slot_bytes) : 0;
+    const int64_t fit = mode == DecodeMode::kForward ? static_cast<int64_t>((max_smem - fixed) / slot_bytes) : 0;
     pl.smem_slots = static_cast<int>(std::min<int64_t>(fit, MS));
     pl.smem_bytes = static_cast<int>(fixed + pl.smem_slots * slot_bytes);
     *out = pl;
