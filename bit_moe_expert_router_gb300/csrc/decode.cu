@@ -59,7 +59,7 @@
 namespace moe {
 namespace {
 
-constexpr int kThreadsD = 256;
+constexpr int kThreadsD = 512;
 static_assert(kDecodeMaxPairs + kDecodeMaxT * kMaxShared <= kFlagWords, "row maxima live in the cleared words");
 constexpr int kWarpsD = kThreadsD / 32;
 
@@ -523,7 +523,8 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     // the first n_smem slots are copied into shared memory by the bulk-copy
     // engine (one copy per row, so the rows keep their padded stride, and one
     // for the scales; completion on one mbarrier), the rest warmed in L2.
-    // Lane 0 of warp w stages slots w, w + 8, ..., a few per phase-1 unit.
+    // Warp w stages slots w, w + 8, ..., a few per phase-1 unit (lane r issues
+    // row r's copy).
     const int n0 = blockIdx.x * pl.rows_pc;
     const int nrows = max(0, min(pl.rows_pc, H - n0));
     const int n_smem = MODE == DecodeMode::kForward && nrows > 0 ? min(n_slots, pl.smem_slots) : 0;
@@ -540,10 +541,10 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
             const uint8_t* wsrc = a.w2 + (e * H + n0) * static_cast<int64_t>(I / 2);
             const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(a.s2 + (e * H + n0) * ng2);
             if (u < n_smem) {
-                if (lane == 0) {
-                    uint8_t* base = s.w2s + u * slot_stride;
-                    for (int r = 0; r < nrows; ++r) bulk_g2s(base + r * RS, wsrc + r * (I / 2), I / 2, s.w2bar);
-                    bulk_g2s(base + pl.rows_pc * RS, ssrc, nrows * ng2 * 4, s.w2bar);
+                uint8_t* base = s.w2s + u * slot_stride;
+                for (int r = lane; r <= nrows; r += 32) {  // lane r: row r; lane nrows: the scales
+                    if (r < nrows) bulk_g2s(base + r * RS, wsrc + r * (I / 2), I / 2, s.w2bar);
+                    else bulk_g2s(base + pl.rows_pc * RS, ssrc, nrows * ng2 * 4, s.w2bar);
                 }
             } else {
                 for (int c = lane; c < lines_w + lines_s; c += 32)
@@ -554,7 +555,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
 
     // ---------------------------------------------------------------- phase 1
     if (MODE != DecodeMode::kGemm2Partials) {
-        constexpr int DEPTH = PC1 == 1 ? 3 : 2;  // units of loads in flight per warp
+        constexpr int DEPTH = PC1 == 1 ? 2 : 1;  // units of loads in flight per warp
         const int upe = I / 2;                    // units per slot
         // each warp takes a contiguous unit range of equal cost: a CTA's warps
         // stream neighbouring rows, and few slots (pages) per SM
