@@ -368,6 +368,7 @@ struct Smem {
     int* first;       // [rows] pair is the first of its expert (by pair index)
     int* eqc;         // [rows] pairs with the same expert
     float* wmax;      // [warps][P] each warp's running max |h| per pair row
+    int* row_slot;    // [P] slot of each pair row
     uint64_t* w2bar;  // completion of the down-projection slice copies
     uint8_t* w2s;     // [smem_slots][slot_stride] staged down-projection slices
 };
@@ -394,6 +395,7 @@ __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
     s.first = reinterpret_cast<int*>(base + pl.off_first);
     s.eqc = reinterpret_cast<int*>(base + pl.off_eqc);
     s.wmax = reinterpret_cast<float*>(base + pl.off_wmax);
+    s.row_slot = reinterpret_cast<int*>(base + pl.off_row_slot);
     s.w2bar = reinterpret_cast<uint64_t*>(base + pl.off_w2bar);
     s.w2s = base + pl.off_w2s;
     return s;
@@ -501,6 +503,8 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     }
     __syncthreads();
     const int n_slots = s.n_slots[0];
+    for (int u = warp; u < n_slots; u += kWarpsD)  // pair row -> its slot
+        for (int m = lane; m < s.slot_cnt[u]; m += 32) s.row_slot[s.slot_row0[u] + m] = u;
     if (warp == 0) {  // phase-1 cost prefix over slots (streaming + per-token work), warp scan
         int run = 0;
         for (int b0 = 0; b0 < n_slots; b0 += 32) {
@@ -753,45 +757,42 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     __syncthreads();
     if (nrows == 0) return;
 
-    // (b) down projection: one lane per (slot, output row); the lane runs the
-    // whole K = I dot product for each token of the slot (no cross-lane sums)
+    // (b) down projection: one thread per (pair row, output row), running the
+    // whole K = I dot product of the row's slot (no cross-lane sums); the
+    // threads of one pair row share its activation row (broadcast reads)
     {
-        const int n_items = n_slots * nrows;
+        const int n_items = P * nrows;
         for (int L = tid; L < n_items; L += kThreadsD) {
-            const int u = L / nrows, r = L % nrows;
+            const int p = L / nrows, r = L % nrows;
+            const int u = s.row_slot[p];
             const int64_t e = s.slot_e[u];
-            const int row0 = s.slot_row0[u], cnt = s.slot_cnt[u];
             const bool in_smem = u < n_smem;
             const uint8_t* wrow = in_smem ? s.w2s + u * slot_stride + r * RS
                                           : a.w2 + (e * H + n0 + r) * static_cast<int64_t>(I / 2);
             const float* srow = in_smem ? reinterpret_cast<const float*>(s.w2s + u * slot_stride + pl.rows_pc * RS) + r * ng2
                                         : a.s2 + (e * H + n0 + r) * ng2;
-            for (int m = 0; m < cnt; ++m) {
-                const int p = row0 + m;
-                const uint8_t* xrow = s.hq + p * HQS;
-                float acc = 0.f;
-                for (int q = 0; q < ng2; ++q) {
-                    int P = 0;
-                    for (int c = 0; c < g / 32; ++c) {  // 32 codes (16 packed bytes) per step
-                        const int kb = q * (g / 2) + 16 * c;
-                        const uint4 wv = in_smem ? *reinterpret_cast<const uint4*>(wrow + kb)
-                                                 : ld_stream16(wrow + kb);
-                        const uint4 xa = *reinterpret_cast<const uint4*>(xrow + 2 * kb);
-                        const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 2 * kb + 16);
-                        P += dot32(wv, xa, xb);
-                    }
-                    if (MODE == DecodeMode::kGemm2Partials) {
-                        a.p2[(static_cast<int64_t>(p) * H + n0 + r) * ng2 + q] = P >> 4;
-                    } else {
-                        const float sc = in_smem ? srow[q] : __ldg(srow + q);
-                        acc = fmaf(static_cast<float>(P >> 4), sc, acc);
-                    }
+            const uint8_t* xrow = s.hq + p * HQS;
+            float acc = 0.f;
+            for (int q = 0; q < ng2; ++q) {
+                int Pq = 0;
+                for (int c = 0; c < g / 32; ++c) {  // 32 codes (16 packed bytes) per step
+                    const int kb = q * (g / 2) + 16 * c;
+                    const uint4 wv = in_smem ? *reinterpret_cast<const uint4*>(wrow + kb) : ld_stream16(wrow + kb);
+                    const uint4 xa = *reinterpret_cast<const uint4*>(xrow + 2 * kb);
+                    const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 2 * kb + 16);
+                    Pq += dot32(wv, xa, xb);
                 }
-                if (MODE == DecodeMode::kForward) {
-                    const float yv = acc * s.sh[p];
-                    s.y[p * pl.rows_pc + r] = yv;
-                    if (a.y) a.y[static_cast<int64_t>(p) * H + n0 + r] = yv;
+                if (MODE == DecodeMode::kGemm2Partials) {
+                    a.p2[(static_cast<int64_t>(p) * H + n0 + r) * ng2 + q] = Pq >> 4;
+                } else {
+                    const float sc = in_smem ? srow[q] : __ldg(srow + q);
+                    acc = fmaf(static_cast<float>(Pq >> 4), sc, acc);
                 }
+            }
+            if (MODE == DecodeMode::kForward) {
+                const float yv = acc * s.sh[p];
+                s.y[p * pl.rows_pc + r] = yv;
+                if (a.y) a.y[static_cast<int64_t>(p) * H + n0 + r] = yv;
             }
         }
     }
@@ -904,6 +905,7 @@ bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t 
     pl.off_eqc = take(4 * rows, 16);
     pl.off_wmax = take(mode == DecodeMode::kForward ? 4 * kWarpsD * P : 0, 16);
     pl.off_w2bar = take(8, 16);
+    pl.off_row_slot = take(4 * P, 16);
     pl.off_w2s = static_cast<int>(align_up(o, 128));
     const size_t slot_bytes =
         static_cast<size_t>(pl.rows_pc) * (I / 2 + 16) + static_cast<size_t>(pl.rows_pc) * (I / g) * 4;

@@ -31,13 +31,16 @@
 // epilogue (warp w: TMEM lanes 32 (w % 4) .. +31 = tile rows, columns
 // 64 (w / 4) .. +63), warps 8-11 producers (thread = tile row: unpack 64
 // packed bytes of its weight row into fp16 and store them to its TMEM lane,
-// cp.async its token row's 256 bytes), warp 12 issues the MMAs (one thread)
+// and copy the stage's token rows: cp.async for gathered rows, TMA tiles
+// issued by warp 8 for contiguous ones), warp 12 issues the MMAs (one thread)
 // and owns the TMEM allocation.  Every wait is bounded; a timeout sets the
 // status word and every role leaves cleanly.
 //
 // K order: the weight unpack turns a packed word (codes 0..7) into fp16
 // pairs (0,4) (1,5) (2,6) (3,7); the token rows are converted to fp16 in
 // the same order by the prep kernels, so both operands agree on K.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 
 #include <algorithm>
@@ -133,16 +136,24 @@ __device__ __forceinline__ uint32_t idesc_f16(int n) {
     return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-// Same MMA with the A operand read from tensor memory (lane = row, K along the columns).
+// MMA with the A operand read from tensor memory (lane = row, K along the columns)
+// and B from shared memory (descriptor).
 __device__ __forceinline__ void mma_f16_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+// TMA: one box (64 fp16 x 128 rows from column x, row y) -> 16 KB of shared memory.
+__device__ __forceinline__ void tma_tile2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -187,13 +198,6 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&v)[64
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
-__device__ __forceinline__ uint4 ld_nc16(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 // Eight packed int4 codes (element e at bits 4e) -> fp16 pairs (0,4) (1,5) (2,6) (3,7).
 // A nibble n of a two's-complement code c satisfies n ^ 8 = c + 8.  Placed in
@@ -223,6 +227,7 @@ __device__ __forceinline__ uint4 unpack_int4_f16(uint32_t w) {
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+
 __device__ __forceinline__ uint32_t swz(int atom_row, int chunk) {  // byte offset in a 128 x 128 B atom
     return static_cast<uint32_t>(atom_row * 128 + (((chunk & 7) ^ (atom_row & 7)) << 4));
 }
@@ -245,7 +250,7 @@ struct Item {
 };
 
 template <TcMode MODE>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_mt) {
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_mt, const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
@@ -273,7 +278,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
 
     if (tid == 0) {
         for (int s = 0; s < kNS; ++s) {
-            mbar_init(full + s, 256);  // 128 producer arrivals + 128 cp.async completions
+            // 128 producer arrivals + 128 cp.async completions (gathered B) or
+            // + the TMA tiles' expect-tx arrival (contiguous B)
+            mbar_init(full + s, a.b_row ? 256 : 129);
             mbar_init(empty + s, 1);
         }
         for (int b = 0; b < kAcc; ++b) {
@@ -408,16 +415,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                 }
                 tc_fence_after();  // the stage's previous MMAs (which read its A columns) are complete
                 uint8_t* Bs = stages + s * kStage;
-                const int pw = warp - kEpiWarps, chunk = lane & 15;
+                // B, the 128 token rows of the stage.  Gathered rows (gate/up):
+                // cp.async by the four producer warps, a warp instruction covering
+                // two whole 256-byte row segments (16 lanes per row); contiguous
+                // rows (down): two 2-D TMA tiles (one per 128-byte-swizzled atom)
+                // issued by producer warp 0.
+                if (a.b_row) {
+                    const int pw = warp - kEpiWarps, chunk = lane & 15;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int row = 32 * pw + 2 * i + (lane >> 4);
-                    const int br = btab[row];
-                    cp_async16(Bs + (chunk >> 3) * kAtom + swz(row, chunk),
-                               a.b + static_cast<int64_t>(br >= 0 ? br : 0) * K + 128 * ks + 8 * chunk, br >= 0 ? 16 : 0);
+                    for (int i = 0; i < 16; ++i) {
+                        const int row = 32 * pw + 2 * i + (lane >> 4);
+                        const int br = btab[row];
+                        cp_async16(Bs + (chunk >> 3) * kAtom + swz(row, chunk),
+                                   a.b + static_cast<int64_t>(br >= 0 ? br : 0) * K + 128 * ks + 8 * chunk,
+                                   br >= 0 ? 16 : 0);
+                    }
+                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(full + s))
+                                 : "memory");
+                } else if (warp == kEpiWarps && lane == 0) {
+                    mbar_expect_tx(full + s, kStage);
+#pragma unroll
+                    for (int at = 0; at < 2; ++at) tma_tile2d(Bs + at * kAtom, &bmap, 128 * ks + 64 * at, it.row0, full + s);
                 }
-                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(full + s))
-                             : "memory");
                 cp_async_wait<kRaw - 1>();  // this use's raw bytes (fetched kRaw calls ago) have landed
                 const uint4* rp = reinterpret_cast<const uint4*>(raw + (use % kRaw) * kRawStage + pt * 64);
                 uint4 rw[4];
@@ -640,6 +659,34 @@ __global__ void prep_h16_kernel(const float* __restrict__ h, uint32_t* __restric
     }
 }
 
+// Tensor map of contiguous B rows (fp16 [b_rows][K]) for the TMA unit:
+// boxes of 64 columns (128 bytes, the swizzle span) by 128 rows; rows past
+// the end read zeros.
+cudaError_t make_bmap(const TcArgs& a, CUtensorMap* map) {
+    using Encode = PFN_cuTensorMapEncodeTiled_v12000;
+    static Encode encode = nullptr;
+    static std::mutex mu;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q{};
+            cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess) return e;
+            if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
+            encode = reinterpret_cast<Encode>(fn);
+        }
+    }
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.b_rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K) * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(a.b), dims, strides, box, elem,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <TcMode MODE>
 cudaError_t launch_mode_tc(const TcArgs& a, int n_mt, cudaStream_t st) {
     auto kern = tc_gemm_kernel<MODE>;
@@ -655,7 +702,12 @@ cudaError_t launch_mode_tc(const TcArgs& a, int n_mt, cudaStream_t st) {
             attr_set[dev] = true;
         }
     }
-    kern<<<num_sms(), kTcThreads, kSmemTc, st>>>(a, n_mt);
+    alignas(64) CUtensorMap bmap{};  // used only for contiguous B rows
+    if (!a.b_row) {
+        cudaError_t e = make_bmap(a, &bmap);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<num_sms(), kTcThreads, kSmemTc, st>>>(a, n_mt, bmap);
     return cudaGetLastError();
 }
 
