@@ -43,9 +43,9 @@ int check_ptrs(std::initializer_list<const void*> ptrs) {
 WsLayout layout_of(const moe_dims_t* d) { return moe::ws_layout(d->T, d->H, d->I, d->E, d->n_shared, d->top_k); }
 
 // Workspace of the partials entry points: the grouping of n_pairs pairs
-// over E + S slots, plus fp16 copies of the T activation rows.
+// over E + S slots, plus the fp16 activation rows of the pairs.
 WsLayout partials_layout(const moe_dims_t* d, int64_t n_pairs) {
-    return moe::ws_layout(std::max<int64_t>(n_pairs, 1), d->H, d->I, d->E + d->n_shared, 0, 1, d->T);
+    return moe::ws_layout(std::max<int64_t>(n_pairs, 1), d->H, d->I, d->E + d->n_shared, 0, 1);
 }
 
 
@@ -197,8 +197,9 @@ moe::TcArgs tc_args(const uint8_t* w, const float* ws, int64_t rows_per_slot, in
 int run_tc_gemms(const int8_t* x_q, const float* x_scale, const uint8_t* w13, const float* s13, const uint8_t* w2,
                  const float* s2, const moe_dims_t* d, const WsLayout& L, const Views& v, cudaStream_t st) {
     const int n_slots = static_cast<int>(d->E + d->n_shared);
-    MOE_CUDA(moe::launch_prep_x16(x_q, d->T, d->H, v.x16, st));
-    moe::TcArgs g1 = tc_args(w13, s13, 2 * d->I, d->H, d, v.x16, v.row_token, d->T, x_scale, v, n_slots);
+    // the activations gathered by pair row, so the gate/up B tiles are contiguous rows
+    MOE_CUDA(moe::launch_prep_x16(x_q, d->T, d->H, v.row_token, L.P, v.x16, st));
+    moe::TcArgs g1 = tc_args(w13, s13, 2 * d->I, d->H, d, v.x16, v.row_token, L.P, x_scale, v, n_slots);
     g1.h = v.h;
     MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kGateUp, g1, st));
     MOE_CUDA(moe::launch_prep_h16(v.h, v.amax, nullptr, L.P, d->I, v.h16, v.sh, st));
@@ -440,8 +441,8 @@ MOE_API int moe_w4a8_gemm1_partials(const int8_t* x_q, const uint8_t* w13_packed
     const int n_slots = static_cast<int>(d->E + d->n_shared);
     if (engine == MOE_ENGINE_TCGEN05) {
         if (!tc_fits(d)) return MOE_ERR_UNSUPPORTED;
-        MOE_CUDA(moe::launch_prep_x16(x_q, d->T, d->H, v.x16, st));
-        moe::TcArgs a = tc_args(w13_packed, nullptr, 2 * d->I, d->H, d, v.x16, v.row_token, d->T, nullptr, v, n_slots);
+        MOE_CUDA(moe::launch_prep_x16(x_q, d->T, d->H, v.row_token, L.P, v.x16, st));
+        moe::TcArgs a = tc_args(w13_packed, nullptr, 2 * d->I, d->H, d, v.x16, nullptr, L.P, nullptr, v, n_slots);
         a.partials = p1;
         MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kGateUpPartials, a, st));
         return MOE_OK;

@@ -42,8 +42,7 @@ struct WsLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Tx: rows of the fp16 activation copy (default T).
-inline WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t k, int64_t Tx = -1) {
+inline WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t k) {
     WsLayout L;
     L.Tk = T * k;
     L.P = T * k + T * S;
@@ -69,7 +68,7 @@ inline WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S,
     L.hq = take(static_cast<size_t>(L.P) * I);
     L.sh = take(sizeof(float) * L.P);
     L.y = take(sizeof(float) * L.P * H);
-    L.x16 = take(2 * static_cast<size_t>(Tx < 0 ? T : Tx) * H);  // tcgen05 engine operands (fp16)
+    L.x16 = take(2 * static_cast<size_t>(L.P) * H);  // tcgen05 engine operands (fp16): activations by pair row
     L.h16 = take(2 * static_cast<size_t>(L.P) * I);
     L.total = o;
     return L;

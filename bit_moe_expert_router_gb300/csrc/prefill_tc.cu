@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
         for (int s = 0; s < kNS; ++s) {
             // 128 producer arrivals + 128 cp.async completions (gathered B) or
             // + the TMA tiles' expect-tx arrival (contiguous B)
-            mbar_init(full + s, a.b_row ? 256 : 129);
+            mbar_init(full + s, a.b_gather ? 256 : 129);
             mbar_init(empty + s, 1);
         }
         for (int b = 0; b < kAcc; ++b) {
@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
             // the barrier orders this item's writes after every producer thread
             // finished the item two back, and makes a give-up unanimous.
             {
-                const int64_t brow = pt < it.ntok ? (a.b_row ? a.b_row[it.row0 + pt] : it.row0 + pt) : -1;
+                const int64_t brow = pt < it.ntok ? (a.b_gather ? a.b_gather[it.row0 + pt] : it.row0 + pt) : -1;
                 brow_tab[(item_n & 1) * 128 + pt] = (brow >= 0 && brow < a.b_rows) ? static_cast<int>(brow) : -1;
                 if (named_bar_or(2, 128, !ok)) break;
             }
@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                 // two whole 256-byte row segments (16 lanes per row); contiguous
                 // rows (down): two 2-D TMA tiles (one per 128-byte-swizzled atom)
                 // issued by producer warp 0.
-                if (a.b_row) {
+                if (a.b_gather) {
                     const int pw = warp - kEpiWarps, chunk = lane & 15;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -598,10 +598,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
 }
 
 // x_q int8 -> fp16 in the engine's K order (pairs (0,4)(1,5)(2,6)(3,7) per 8 values).
-__global__ void prep_x16_kernel(const int8_t* __restrict__ x, int64_t n8, __half* __restrict__ out) {
+// x_q int8 -> fp16 rows in the engine's K order (pairs (0,4)(1,5)(2,6)(3,7) per
+// 8 values); out row r is token row_token[r] (null: r), zeros for a token
+// outside [0, T).
+__global__ void prep_x16_kernel(const int8_t* __restrict__ x, int64_t T, int64_t H, const int32_t* __restrict__ row_token,
+                                int64_t n8, __half* __restrict__ out) {
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const uint2 v = *reinterpret_cast<const uint2*>(x + 8 * i);
+        const int64_t r = (8 * i) / H, c = (8 * i) % H;
+        const int64_t t = row_token ? row_token[r] : r;
+        uint2 v = make_uint2(0u, 0u);
+        if (t >= 0 && t < T) v = *reinterpret_cast<const uint2*>(x + t * H + c);
         const int8_t* b = reinterpret_cast<const int8_t*>(&v);
         __half2 o[4];
 #pragma unroll
@@ -703,7 +710,7 @@ cudaError_t launch_mode_tc(const TcArgs& a, int n_mt, cudaStream_t st) {
         }
     }
     alignas(64) CUtensorMap bmap{};  // used only for contiguous B rows
-    if (!a.b_row) {
+    if (!a.b_gather) {
         cudaError_t e = make_bmap(a, &bmap);
         if (e != cudaSuccess) return e;
     }
@@ -729,10 +736,11 @@ cudaError_t launch_tc_gemm(TcMode mode, const TcArgs& a, cudaStream_t st) {
     }
 }
 
-cudaError_t launch_prep_x16(const int8_t* x_q, int64_t T, int64_t H, __half* x16, cudaStream_t st) {
-    const int64_t n8 = T * H / 8;
+cudaError_t launch_prep_x16(const int8_t* x_q, int64_t T, int64_t H, const int32_t* row_token, int64_t rows, __half* x16,
+                            cudaStream_t st) {
+    const int64_t n8 = rows * H / 8;
     const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, static_cast<int64_t>(num_sms()) * 8);
-    prep_x16_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(x_q, n8, x16);
+    prep_x16_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(x_q, T, H, row_token, n8, x16);
     return cudaGetLastError();
 }
 
