@@ -18,11 +18,10 @@
 //            intermediate indices (2 gate rows + the 2 matching up rows) of
 //            one slot; each warp takes a contiguous unit range of equal cost
 //            (streaming + per-token work, so the always-on shared expert's
-//            multi-token units weigh more).  A warp keeps the next unit's
-//            16-byte loads in flight in registers while it computes (16 warps
-//            per SM hide the rest of the latency; lane l loads pieces l,
+//            multi-token units weigh more).  A warp loads one unit at a
+//            time into registers (16-byte loads; lane l loads pieces l,
 //            l + 32, ... of each row, so each warp load reads 512 contiguous
-//            bytes); each lane folds the exact int32 sum of each
+//            bytes) -- the other 15 warps of the SM cover its latency; each lane folds the exact int32 sum of each
 //            32-value piece with its group scale, and a 4-row reduce-scatter
 //            across the warp (6 shuffles) gives the row sums; h = SiLU(G_gate)
 //            * G_up goes to the workspace and |h| into the warp's running row
@@ -560,7 +559,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
 
     // ---------------------------------------------------------------- phase 1
     if (MODE != DecodeMode::kGemm2Partials) {
-        constexpr int DEPTH = 1;  // units of loads in flight per warp (16 warps per SM hide the latency)
+        constexpr int DEPTH = 1;  // units loaded per warp at a time (the SM's other warps hide the latency)
         const int upe = I / 2;                    // units per slot
         // each warp takes a contiguous unit range of equal cost: a CTA's warps
         // stream neighbouring rows, and few slots (pages) per SM
