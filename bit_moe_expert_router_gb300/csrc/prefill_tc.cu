@@ -156,6 +156,10 @@ __device__ __forceinline__ void tma_tile2d(void* dst, const CUtensorMap* map, in
         : "memory");
 }
 
+// SiLU in fast fp32 (hardware exp2 approximation and fast reciprocal divide,
+// a few ulp from z / (1 + exp(-z))).
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
                  : "memory");
@@ -357,33 +361,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
 
     if (warp >= kEpiWarps && warp < kMmaWarp) {
         // ------------------------------------------------------------ producers
-        // Each thread owns tile row pt.  Its packed weight bytes for use
+        // Each thread owns tile row pt.  The packed weight bytes for use
         // u + kRaw are copied (cp.async) into the raw ring while use u is
-        // unpacked, so the unpack never waits for HBM; it waits only for
-        // its own copies (cp.async.wait_group), no cross-thread sync.
+        // unpacked, so the unpack never waits for HBM.  The copies are
+        // coalesced within the warp (4 lanes per row, 8 rows of 64 contiguous
+        // bytes per instruction), so a lane waits for its own copies and then
+        // syncs the warp before reading its row.
         const int pt = tid - kEpiThreads;
+        const int pw = warp - kEpiWarps;
         // 16-byte chunk q of row pt sits at chunk q ^ rsw: eight consecutive rows
         // (64 bytes apart) then hit eight different bank groups
         const int rsw = (pt >> 1) & 3;
         int l_item = blockIdx.x, l_ks = 0;  // next use whose raw bytes are fetched
-        const uint8_t* l_src = nullptr;
+        const uint8_t* l_slot = nullptr;    // its slot's packed rows
+        int l_mt = 0;
         if (l_item < total) {
             const Item it = decode_item(l_item);
-            l_src = a.w + (static_cast<int64_t>(it.slot) * rows_per_slot + weight_row(it.mt, pt)) * (K / 2);
+            l_slot = a.w + static_cast<int64_t>(it.slot) * rows_per_slot * (K / 2);
+            l_mt = it.mt;
         }
         int l_use = 0;
+        const int piece = lane & 3;
         auto fetch_next = [&]() {
             if (l_item < total) {
-                uint8_t* dst = raw + (l_use % kRaw) * kRawStage + pt * 64;
+                uint8_t* dst = raw + (l_use % kRaw) * kRawStage;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) cp_async16(dst + 16 * (q ^ rsw), l_src + 64 * l_ks + 16 * q);
+                for (int q = 0; q < 4; ++q) {  // rows 32 pw + 8 q .. + 7, 4 lanes per row
+                    const int row = 32 * pw + 8 * q + (lane >> 2);
+                    const int rs = (row >> 1) & 3;
+                    cp_async16(dst + row * 64 + 16 * (piece ^ rs),
+                               l_slot + weight_row(l_mt, row) * (K / 2) + 64 * l_ks + 16 * piece);
+                }
                 ++l_use;
                 if (++l_ks == ksteps) {
                     l_ks = 0;
                     l_item += gridDim.x;
                     if (l_item < total) {
                         const Item it = decode_item(l_item);
-                        l_src = a.w + (static_cast<int64_t>(it.slot) * rows_per_slot + weight_row(it.mt, pt)) * (K / 2);
+                        l_slot = a.w + static_cast<int64_t>(it.slot) * rows_per_slot * (K / 2);
+                        l_mt = it.mt;
                     }
                 }
             }
@@ -421,7 +437,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                 // rows (down): two 2-D TMA tiles (one per 128-byte-swizzled atom)
                 // issued by producer warp 0.
                 if (a.b_gather) {
-                    const int pw = warp - kEpiWarps, chunk = lane & 15;
+                    const int chunk = lane & 15;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int row = 32 * pw + 2 * i + (lane >> 4);
@@ -437,7 +453,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
 #pragma unroll
                     for (int at = 0; at < 2; ++at) tma_tile2d(Bs + at * kAtom, &bmap, 128 * ks + 64 * at, it.row0, full + s);
                 }
-                cp_async_wait<kRaw - 1>();  // this use's raw bytes (fetched kRaw calls ago) have landed
+                cp_async_wait<kRaw - 1>();  // this lane's copies for this use (issued kRaw calls ago) have landed
+                __syncwarp();               // ... and the other lanes' copies of this warp's rows
                 const uint4* rp = reinterpret_cast<const uint4*>(raw + (use % kRaw) * kRawStage + pt * 64);
                 uint4 rw[4];
 #pragma unroll
@@ -459,9 +476,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                     }
                 }
                 tmem_st64(tmem + (static_cast<uint32_t>(32 * (warp - kEpiWarps)) << 16) + kAcc * 128 + kACols * s, av);
-                // the raw slot just consumed is refilled kRaw uses ahead (after its
-                // bytes were used: no copy may overwrite them before they are read)
-                asm volatile("" ::: "memory");
+                // the raw slot just consumed is refilled kRaw uses ahead, after every
+                // lane of the warp has read its row from it
+                __syncwarp();
                 fetch_next();
                 tc_fence_before();
                 mbar_arrive(full + s);
@@ -575,7 +592,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                     const float gate = odd ? other : acc[c0], up = odd ? acc[c0 + 1] : other;
                     if (c < nloc) {
                         const float xs = colf[c_base + c];
-                        a.h[static_cast<int64_t>(colp[c_base + c]) * a.I + i] = silu_f32(gate * xs) * (up * xs);
+                        a.h[static_cast<int64_t>(colp[c_base + c]) * a.I + i] = silu_fast(gate * xs) * (up * xs);
                     }
                 }
             } else if (ok && MODE == TcMode::kDown) {
