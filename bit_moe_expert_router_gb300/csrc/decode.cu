@@ -9,9 +9,8 @@
 //
 //   phase 0  every CTA routes all T tokens itself (the same deterministic
 //            result in every CTA, so nothing is exchanged; one warp per token,
-//            a threshold from the lanes' maxima, then exact ranking of the
-//            few candidates above it), sorts the pairs
-//            stably by expert into pair rows, builds the slot table (touched
+//            k rounds of a warp arg-max), sorts the pairs stably by expert
+//            into pair rows, builds the slot table (touched
 //            experts ascending, then the shared experts) and stages the
 //            activations in shared memory.
 //   phase 1  gate/up projection with dp4a on the CUDA cores: units of two
@@ -172,121 +171,52 @@ __device__ bool w2_wait(uint64_t* bar, Header* hdr) {
     }
 }
 
-// (key a, id ia) ranks before (key b, id ib): larger key, or equal key and lower id.
-__device__ __forceinline__ bool ranks_before(uint32_t a, uint32_t ia, uint32_t b, uint32_t ib) {
-    return a > b || (a == b && ia < ib);
-}
-
 // Routing of all T tokens, one warp per token (tokens dealt over the
 // CTA's warps).  Lane l holds the order keys of experts l, l + 32, ...
-// (NJ * 32 >= E).  Exact top-k in (key desc, id asc) order:
-//  1. tau = the k-th best of the 32 lanes' best elements (bitonic sort of
-//     the lane maxima across the warp).  At least k elements rank at or
-//     before tau, so the top-k all do: the candidates are those elements.
-//  2. up to kCand candidates are compacted into shared memory and each is
-//     ranked against all of them; rank < k is selected at that position.
-//  3. more candidates than that (heavily skewed or tied logits): k rounds
-//     of a warp arg-max over the elements not yet taken.
-// Then the weights: softmax over the k selected logits, relative to the
-// largest.  ids/wts: [T][k]; cand_k/cand_i: kCand per warp.
-constexpr int kCand = 64;
-
+// (NJ * 32 >= E).  Exact top-k in (key desc, id asc) order by k rounds of a
+// warp arg-max: each lane keeps its best untaken (key, id) -- strict > over
+// its keys keeps the lowest id on ties -- the round's winner is the largest
+// key, lowest id among the lanes holding it, and only the winning lane
+// rescans its keys.  The code is short on purpose: it runs once per launch
+// and is fetched cold.  Then the weights: softmax over the k selected
+// logits, relative to the largest.  ids/wts: [T][k].
 template <int NJ>
-__device__ void route_tokens(const float* __restrict__ logits, int T, int E, int k, int* ids, float* wts,
-                             uint32_t* cand_k, uint32_t* cand_i) {
+__device__ void route_tokens(const float* __restrict__ logits, int T, int E, int k, int* ids, float* wts) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    uint32_t* ck = cand_k + warp * kCand;
-    uint32_t* ci = cand_i + warp * kCand;
     for (int t = warp; t < T; t += nw) {
         uint32_t key[NJ];
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
             const int e = lane + 32 * j;
+            // 0 is below every finite key, and k <= E real experts are always left
             key[j] = e < E ? order_key(__ldg(logits + static_cast<int64_t>(t) * E + e)) : 0u;
         }
-        // this lane's best (ids grow with j, so strict > keeps the lowest id on ties)
-        uint32_t sk = key[0], si = lane < E ? static_cast<uint32_t>(lane) : 0xFFFFFFFFu;
+        uint32_t bk = 0;
+        int bj = 0;
+        auto lane_best = [&]() {
+            bk = key[0];
+            bj = 0;
 #pragma unroll
-        for (int j = 1; j < NJ; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E && key[j] > sk) {
-                sk = key[j];
-                si = static_cast<uint32_t>(e);
+            for (int j = 1; j < NJ; ++j)
+                if (key[j] > bk) {
+                    bk = key[j];
+                    bj = j;
+                }
+        };
+        lane_best();
+        for (int r = 0; r < k; ++r) {
+            const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+            const uint32_t mine = static_cast<uint32_t>(lane + 32 * bj);
+            const uint32_t mi = __reduce_min_sync(0xffffffffu, bk == mk ? mine : 0xFFFFFFFFu);
+            if (lane == 0) {
+                ids[t * k + r] = static_cast<int>(mi);
+                wts[t * k + r] = key_value(mk);
             }
-        }
-        // bitonic sort of the 32 lane maxima, best first
+            if (mine == mi) {  // the winner drops the taken key and rescans
 #pragma unroll
-        for (int size = 2; size <= 32; size <<= 1)
-#pragma unroll
-            for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                const uint32_t ok = __shfl_xor_sync(0xffffffffu, sk, stride);
-                const uint32_t oi = __shfl_xor_sync(0xffffffffu, si, stride);
-                const bool lower = (lane & stride) == 0;
-                const bool desc = (lane & size) == 0 || size == 32;
-                const bool mine_first = ranks_before(sk, si, ok, oi);
-                if (mine_first != (lower == desc)) {
-                    sk = ok;
-                    si = oi;
-                }
-            }
-        const uint32_t tk = __shfl_sync(0xffffffffu, sk, k - 1), ti = __shfl_sync(0xffffffffu, si, k - 1);
-        // candidates: elements ranking at or before (tk, ti)
-        uint32_t cmask = 0;
-        int cnt = 0;
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-            const int e = lane + 32 * j;
-            const bool in = e < E && (key[j] > tk || (key[j] == tk && static_cast<uint32_t>(e) <= ti));
-            cmask |= static_cast<uint32_t>(in) << j;
-            cnt += in;
-        }
-        int incl = cnt;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
-        }
-        const int total = __shfl_sync(0xffffffffu, incl, 31);
-        if (total <= kCand) {
-            int o = incl - cnt;
-#pragma unroll
-            for (int j = 0; j < NJ; ++j)
-                if (cmask >> j & 1u) {
-                    ck[o] = key[j];
-                    ci[o] = static_cast<uint32_t>(lane + 32 * j);
-                    ++o;
-                }
-            __syncwarp();
-            for (int c = lane; c < total; c += 32) {
-                const uint32_t mk = ck[c], mi = ci[c];
-                int rank = 0;
-                for (int u = 0; u < total; ++u) rank += ranks_before(ck[u], ci[u], mk, mi);
-                if (rank < k) {
-                    ids[t * k + rank] = static_cast<int>(mi);
-                    wts[t * k + rank] = key_value(mk);
-                }
-            }
-        } else {
-            uint32_t taken = 0;
-            for (int r = 0; r < k; ++r) {
-                uint32_t bk = 0, bi = 0xFFFFFFFFu;
-                int bj = -1;
-#pragma unroll
-                for (int j = 0; j < NJ; ++j) {
-                    const int e = lane + 32 * j;
-                    if (e < E && !(taken >> j & 1u) && (bj < 0 || key[j] > bk)) {
-                        bk = key[j];
-                        bi = static_cast<uint32_t>(e);
-                        bj = j;
-                    }
-                }
-                const uint32_t mk = __reduce_max_sync(0xffffffffu, bj >= 0 ? bk : 0u);
-                const uint32_t mi = __reduce_min_sync(0xffffffffu, (bj >= 0 && bk == mk) ? bi : 0xFFFFFFFFu);
-                if (bj >= 0 && bi == mi) taken |= 1u << bj;
-                if (lane == 0) {
-                    ids[t * k + r] = static_cast<int>(mi);
-                    wts[t * k + r] = key_value(mk);
-                }
+                for (int j = 0; j < NJ; ++j)
+                    if (j == bj) key[j] = 0u;
+                lane_best();
             }
         }
         __syncwarp();
@@ -363,8 +293,6 @@ struct Smem {
     uint8_t* x;       // [T][H + 16] split layout
     uint8_t* hq;      // [P][I + 16] split layout
     float* y;         // [P][rows_pc]
-    uint32_t* cand_k; // [warps][kCand] routing candidates (order keys)
-    uint32_t* cand_i; // [warps][kCand] (expert ids)
     int* first;       // [rows] pair is the first of its expert (by pair index)
     int* eqc;         // [rows] pairs with the same expert
     float* wmax;      // [warps][P] each warp's running max |h| per pair row
@@ -390,8 +318,6 @@ __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
     s.x = base + pl.off_x;
     s.hq = base + pl.off_hq;
     s.y = reinterpret_cast<float*>(base + pl.off_y);
-    s.cand_k = reinterpret_cast<uint32_t*>(base + pl.off_cand_v);
-    s.cand_i = reinterpret_cast<uint32_t*>(base + pl.off_cand_e);
     s.first = reinterpret_cast<int*>(base + pl.off_first);
     s.eqc = reinterpret_cast<int*>(base + pl.off_eqc);
     s.wmax = reinterpret_cast<float*>(base + pl.off_wmax);
@@ -410,10 +336,13 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const Smem s = carve(smem_raw, pl);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int T = a.T, H = a.H, I = a.I, k = a.k, g = a.g;
+    // the shape is a template parameter (the host checks a.H and a.I against it),
+    // so the index arithmetic below divides by constants
+    constexpr int H = 2048 * PC1, I = 512 * PC2;
+    const int T = a.T, k = a.k, g = a.g;
     const int ng1 = H / g, ng2 = I / g;
-    const int XS = H + 16, HQS = I + 16;
-    const int RS = I / 2 + 16;  // staged down-projection row stride
+    constexpr int XS = H + 16, HQS = I + 16;
+    constexpr int RS = I / 2 + 16;  // staged down-projection row stride
     const bool routed = MODE == DecodeMode::kForward;
 
     if (tid == 0) {
@@ -424,7 +353,8 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     // ---------------------------------------------------------------- phase 0
     // the first activation pieces are loaded now, so their latency overlaps the routing
     constexpr int kXPre = 4;
-    const int per_tok = H / 16, n_xp = MODE == DecodeMode::kGemm2Partials ? 0 : T * per_tok;
+    constexpr int per_tok = H / 16;
+    const int n_xp = MODE == DecodeMode::kGemm2Partials ? 0 : T * per_tok;
     uint4 xpre[kXPre];
 #pragma unroll
     for (int i = 0; i < kXPre; ++i) {
@@ -433,8 +363,8 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     }
     int n_rows;  // routed/listed pair rows before the shared rows
     if (routed) {
-        if (a.E <= 512) route_tokens<16>(a.logits, T, a.E, k, s.ids, s.wts, s.cand_k, s.cand_i);
-        else route_tokens<kMaxExperts / 32>(a.logits, T, a.E, k, s.ids, s.wts, s.cand_k, s.cand_i);
+        if (a.E <= 512) route_tokens<16>(a.logits, T, a.E, k, s.ids, s.wts);
+        else route_tokens<kMaxExperts / 32>(a.logits, T, a.E, k, s.ids, s.wts);
         n_rows = T * k;
     } else {
         n_rows = a.n_pairs;  // listed pairs; out-of-range slots and tokens are clamped (never read out of bounds)
@@ -587,6 +517,10 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         constexpr int NP = 2 * PC1;
         uint4 wr[DEPTH][4][NP];
         float sr[DEPTH][4][NP];
+        // K group of piece p of this lane, (32 lane + 1024 p) / g, by a multiply and
+        // a shift: with m = ceil(2^24 / g), floor(n m / 2^24) = floor(n / g) for n g < 2^24
+        const uint32_t gmag = ((1u << 24) + static_cast<uint32_t>(g) - 1) / static_cast<uint32_t>(g);
+        auto gq = [&](int p) { return static_cast<int>((static_cast<uint32_t>(32 * lane + 1024 * p) * gmag) >> 24); };
         auto issue = [&](int un, int d) {
             const int64_t U = Ua + un;
             const int u = static_cast<int>(U / upe), ip = static_cast<int>(U % upe);
@@ -598,7 +532,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
 #pragma unroll
                 for (int p = 0; p < NP; ++p) {
                     wr[d][r][p] = ld_stream16(wp + 16 * lane + 512 * p);
-                    if (MODE == DecodeMode::kForward) sr[d][r][p] = __ldg(a.s13 + row * ng1 + (32 * lane + 1024 * p) / g);
+                    if (MODE == DecodeMode::kForward) sr[d][r][p] = __ldg(a.s13 + row * ng1 + gq(p));
                 }
             }
         };
@@ -637,8 +571,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                                 for (int off = 1; off < lpg; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
                                 if ((lane % lpg) == 0) {
                                     const int64_t wrow = (r >= 2 ? I : 0) + 2 * ip + (r & 1);
-                                    a.p1[(static_cast<int64_t>(prow) * 2 * I + wrow) * ng1 + (32 * lane + 1024 * p) / g] =
-                                        v >> 4;
+                                    a.p1[(static_cast<int64_t>(prow) * 2 * I + wrow) * ng1 + gq(p)] = v >> 4;
                                 }
                             }
                         continue;
@@ -717,17 +650,18 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
 #pragma unroll
             for (int c2 = 0; c2 < PC2; ++c2) {  // 16 values per lane per 512-value chunk
                 const float4* src = reinterpret_cast<const float4*>(a.h + static_cast<int64_t>(p) * I + 512 * c2 + 16 * lane);
-                float4 f[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) f[q] = __ldcg(src + q);
-                uint32_t wds[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    wds[q] = (requant_code_fast(f[q].x, sc, rs) & 0xFF) | ((requant_code_fast(f[q].y, sc, rs) & 0xFF) << 8) |
-                             ((requant_code_fast(f[q].z, sc, rs) & 0xFF) << 16) |
-                             ((static_cast<uint32_t>(requant_code_fast(f[q].w, sc, rs)) & 0xFF) << 24);
-                *reinterpret_cast<uint4*>(a.hq_g + static_cast<int64_t>(p) * I + 512 * c2 + 16 * lane) =
-                    split16(make_uint4(wds[0], wds[1], wds[2], wds[3]));
+                uint2* dst = reinterpret_cast<uint2*>(a.hq_g + static_cast<int64_t>(p) * I + 512 * c2 + 16 * lane);
+#pragma unroll 1
+                for (int q = 0; q < 2; ++q) {  // 8 values -> one 8-byte group, split even|odd (a loop: run-once code stays short)
+                    const float4 f0 = __ldcg(src + 2 * q), f1 = __ldcg(src + 2 * q + 1);
+                    const uint32_t w0 = (requant_code_fast(f0.x, sc, rs) & 0xFF) | ((requant_code_fast(f0.y, sc, rs) & 0xFF) << 8) |
+                                        ((requant_code_fast(f0.z, sc, rs) & 0xFF) << 16) |
+                                        ((static_cast<uint32_t>(requant_code_fast(f0.w, sc, rs)) & 0xFF) << 24);
+                    const uint32_t w1 = (requant_code_fast(f1.x, sc, rs) & 0xFF) | ((requant_code_fast(f1.y, sc, rs) & 0xFF) << 8) |
+                                        ((requant_code_fast(f1.z, sc, rs) & 0xFF) << 16) |
+                                        ((static_cast<uint32_t>(requant_code_fast(f1.w, sc, rs)) & 0xFF) << 24);
+                    dst[q] = make_uint2(__byte_perm(w0, w1, 0x6420), __byte_perm(w0, w1, 0x7531));
+                }
             }
         }
         if (!grid_barrier(a.hdr, 2)) {
@@ -899,8 +833,6 @@ bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t 
     pl.off_x = take(mode == DecodeMode::kGemm2Partials ? 0 : T * (H + 16), 128);
     pl.off_hq = take(mode == DecodeMode::kGemm1Partials ? 0 : P * (I + 16), 128);
     pl.off_y = take(mode == DecodeMode::kForward ? 4 * P * pl.rows_pc : 0, 16);
-    pl.off_cand_v = take(mode == DecodeMode::kForward ? 4 * kWarpsD * kCand : 0, 16);
-    pl.off_cand_e = take(mode == DecodeMode::kForward ? 4 * kWarpsD * kCand : 0, 16);
     pl.off_first = take(4 * rows, 16);
     pl.off_eqc = take(4 * rows, 16);
     pl.off_wmax = take(mode == DecodeMode::kForward ? 4 * kWarpsD * P : 0, 16);
@@ -940,6 +872,7 @@ cudaError_t launch_decode(DecodeMode mode, const DecodeArgs& a, const DecodePlan
         if (e != cudaSuccess) return e;
     }
     const int p1 = a.H / 2048, p2 = a.I / 512;
+    if (a.H != 2048 * p1 || a.I != 512 * p2) return cudaErrorInvalidValue;  // the kernel's shape is compiled in
     if (p1 == 1 && p2 == 1) return launch_shape<1, 1>(mode, a, pl, grid, st);
     if (p1 == 2 && p2 == 1) return launch_shape<2, 1>(mode, a, pl, grid, st);
     if (p1 == 1 && p2 == 3) return launch_shape<1, 3>(mode, a, pl, grid, st);

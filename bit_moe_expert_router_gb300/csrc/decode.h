@@ -45,7 +45,7 @@ struct DecodePlan {
     int smem_slots;   // slots whose down-projection slice is staged in shared memory
     int smem_bytes;
     int off_ids, off_wts, off_pos, off_pair_of, off_row_tok, off_slot_e, off_slot_row0, off_slot_cnt, off_slot_cum,
-        off_n_slots, off_xs, off_sh, off_x, off_hq, off_y, off_cand_v, off_cand_e, off_first, off_eqc, off_wmax, off_w2bar, off_row_slot, off_w2s;
+        off_n_slots, off_xs, off_sh, off_x, off_hq, off_y, off_first, off_eqc, off_wmax, off_w2bar, off_row_slot, off_w2s;
 };
 
 bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t k, int64_t g, int64_t n_pairs,

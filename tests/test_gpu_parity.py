@@ -108,8 +108,9 @@ DEC_SMALL = synth.Workload("dec_small", T=8, H=2048, I=512, E=16, S=1, top_k=4, 
 TC_SMALL = synth.Workload("tc_small", T=300, H=256, I=128, E=8, S=1, top_k=2, group=128)
 TC_ODD = synth.Workload("tc_odd", T=150, H=384, I=384, E=6, S=0, top_k=3, group=128)
 TC_G256 = synth.Workload("tc_g256", T=140, H=512, I=256, E=4, S=1, top_k=2, group=256)
-EXTRA = {w.name: w for w in (DEC_SMALL, TC_SMALL, TC_ODD, TC_G256)}
-PARTIALS_CASES = ([(n, 0) for n in ALL] + [("decode_t4", 1), ("decode_verify_t12", 1), ("dec_small", 1)] +
+DEC_G64 = synth.Workload("dec_g64", T=6, H=2048, I=512, E=8, S=1, top_k=3, group=64)
+EXTRA = {w.name: w for w in (DEC_SMALL, TC_SMALL, TC_ODD, TC_G256, DEC_G64)}
+PARTIALS_CASES = ([(n, 0) for n in ALL] + [("decode_t4", 1), ("decode_verify_t12", 1), ("dec_small", 1), ("dec_g64", 1)] +
                   [(n, 2) for n in ("prefill_t8192", "large_bank_t2048", "decode_t4", "tc_small", "tc_odd",
                                     "tc_g256")])
 
@@ -310,6 +311,21 @@ def test_decode_engine_top_k_and_shared(k, S):
     tok = synth.make_tokens(w)
     out = _forward_engine(w, tok, 1)
     gh.assert_output_close(out, gh.oracle_out(w, tok, gh.bank_of(w)), f"decode k={k} S={S}")
+
+
+@pytest.mark.parametrize("E", [64, 600])
+def test_decode_engine_routes_planted_ties(E):
+    """The fused kernel's own routing on massively tied logits (E > 512 takes its wide path)."""
+    w = synth.Workload("dties", T=12, H=2048, I=512, E=E, S=1, top_k=6, group=128)
+    tok = synth.make_tokens(w)
+    rng = np.random.default_rng(7)
+    lg = rng.integers(-2, 3, size=(w.T, w.E)).astype(np.float32)
+    lg[rng.random(lg.shape) < 0.2] = -0.0
+    lg[0, :] = 0.0
+    lg[1, :] = -0.0
+    tok.logits[...] = lg
+    out = _forward_engine(w, tok, 1)
+    gh.assert_output_close(out, gh.oracle_out(w, tok, gh.bank_of(w)), f"decode ties E={E}")
 
 
 def test_decode_engine_matches_grouped_engine_on_large_bank_shape():
