@@ -26,9 +26,8 @@ constexpr uint32_t kDevTimeout = 1;
 struct Header {
     uint32_t status;        // kDevOk / kDevTimeout
     uint32_t n_tiles;       // grouped-GEMM m-tiles of this call
-    uint32_t bar_arrive;    // grid barrier: arrivals (fused decode kernel)
-    uint32_t bar_gen;       // grid barrier: completed barriers
-    uint32_t pad[60];
+    uint32_t bar_arrive;    // grid barriers: arrivals so far (fused decode kernel)
+    uint32_t pad[61];
 };
 
 constexpr int kFlagWords = 1024;  // per-call words after the header, cleared with it (decode: row maxima)

@@ -113,29 +113,28 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
     return v;
 }
 
-// Grid-wide barrier number `k` (1-based) of this launch; the counters start
-// at zero (cleared before the launch).  Bounded: false on timeout.
+// Grid-wide barrier number `k` (1-based) of this launch; the arrival counter
+// starts at zero (cleared before the launch).  Each CTA adds its arrival and
+// polls the counter itself until all k * grid arrivals are in (one L2 round
+// trip less than a separate release word written by the last arriver).
+// Bounded: false on timeout.
 __device__ bool grid_barrier(Header* hdr, uint32_t k) {
     __shared__ int ok_s;
     __syncthreads();
     if (threadIdx.x == 0) {
         int ok = 1;
         __threadfence();
-        const uint32_t old = atomicAdd(&hdr->bar_arrive, 1u);
-        if (old == k * gridDim.x - 1) {
-            __threadfence();
-            atomicExch(&hdr->bar_gen, k);
-        } else {
-            const uint64_t t0 = global_ns();
-            uint32_t it = 0;
-            while (ld_acquire(&hdr->bar_gen) < k) {
-                if (++it > kSpinCap || global_ns() - t0 > kWaitNs) {
-                    atomicOr(&hdr->status, kDevTimeout);
-                    ok = 0;
-                    break;
-                }
-                __nanosleep(32);
+        atomicAdd(&hdr->bar_arrive, 1u);
+        const uint32_t target = k * gridDim.x;
+        const uint64_t t0 = global_ns();
+        uint32_t it = 0;
+        while (ld_acquire(&hdr->bar_arrive) < target) {
+            if (++it > kSpinCap || global_ns() - t0 > kWaitNs) {
+                atomicOr(&hdr->status, kDevTimeout);
+                ok = 0;
+                break;
             }
+            __nanosleep(32);
         }
         __threadfence();
         ok_s = ok;
@@ -179,10 +178,10 @@ __device__ bool w2_wait(uint64_t* bar, Header* hdr) {
 // key, lowest id among the lanes holding it, and only the winning lane
 // rescans its keys.  The code is short on purpose: it runs once per launch
 // and is fetched cold.  Then the weights: softmax over the k selected
-// logits, relative to the largest.  ids/wts: [T][k].
+// logits, relative to the largest.  ids/wts: [T][k]; warps 0 .. nw-1 take part.
 template <int NJ>
-__device__ void route_tokens(const float* __restrict__ logits, int T, int E, int k, int* ids, float* wts) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+__device__ void route_tokens(const float* __restrict__ logits, int T, int E, int k, int* ids, float* wts, int nw) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int t = warp; t < T; t += nw) {
         uint32_t key[NJ];
 #pragma unroll
@@ -351,38 +350,34 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     }
 
     // ---------------------------------------------------------------- phase 0
-    // the first activation pieces are loaded now, so their latency overlaps the routing
-    constexpr int kXPre = 4;
+    // Warps 0 .. nrw-1 route (one token each at a time); the others stage the
+    // activations meanwhile ([t][H + 16], each 8-byte group split even|odd).
+    // When every warp routes, every thread stages afterwards.
     constexpr int per_tok = H / 16;
     const int n_xp = MODE == DecodeMode::kGemm2Partials ? 0 : T * per_tok;
-    uint4 xpre[kXPre];
-#pragma unroll
-    for (int i = 0; i < kXPre; ++i) {
-        const int o = tid + kThreadsD * i;
-        if (o < n_xp) xpre[i] = *reinterpret_cast<const uint4*>(a.x_q + static_cast<int64_t>(o / per_tok) * H + 16 * (o % per_tok));
-    }
+    const int nrw = routed ? min(T, kWarpsD) : 0;
     int n_rows;  // routed/listed pair rows before the shared rows
     if (routed) {
-        if (a.E <= 512) route_tokens<16>(a.logits, T, a.E, k, s.ids, s.wts);
-        else route_tokens<kMaxExperts / 32>(a.logits, T, a.E, k, s.ids, s.wts);
+        if (warp < nrw) {
+            if (a.E <= 512) route_tokens<16>(a.logits, T, a.E, k, s.ids, s.wts, nrw);
+            else route_tokens<kMaxExperts / 32>(a.logits, T, a.E, k, s.ids, s.wts, nrw);
+        }
         n_rows = T * k;
     } else {
         n_rows = a.n_pairs;  // listed pairs; out-of-range slots and tokens are clamped (never read out of bounds)
         for (int r = tid; r < n_rows; r += kThreadsD) s.ids[r] = min(max(a.pair_slot[r], 0), a.E - 1);
     }
-    // activations: [t][H + 16], each 8-byte group split even|odd (independent of routing)
     if (MODE != DecodeMode::kGemm2Partials) {
-#pragma unroll
-        for (int i = 0; i < kXPre; ++i) {
-            const int o = tid + kThreadsD * i;
-            if (o < n_xp) *reinterpret_cast<uint4*>(s.x + (o / per_tok) * XS + 16 * (o % per_tok)) = split16(xpre[i]);
+        const int st0 = nrw < kWarpsD ? 32 * nrw : 0, nst = kThreadsD - st0;
+        if (tid >= st0) {
+#pragma unroll 4
+            for (int o = tid - st0; o < n_xp; o += nst) {
+                const int t = o / per_tok, c = o % per_tok;
+                const uint4 v = *reinterpret_cast<const uint4*>(a.x_q + static_cast<int64_t>(t) * H + 16 * c);
+                *reinterpret_cast<uint4*>(s.x + t * XS + 16 * c) = split16(v);
+            }
+            for (int t = tid - st0; t < T; t += nst) s.xs[t] = routed ? a.x_scale[t] : 1.0f;
         }
-        for (int o = tid + kThreadsD * kXPre; o < n_xp; o += kThreadsD) {
-            const int t = o / per_tok, c = o % per_tok;
-            const uint4 v = *reinterpret_cast<const uint4*>(a.x_q + static_cast<int64_t>(t) * H + 16 * c);
-            *reinterpret_cast<uint4*>(s.x + t * XS + 16 * c) = split16(v);
-        }
-        for (int t = tid; t < T; t += kThreadsD) s.xs[t] = routed ? a.x_scale[t] : 1.0f;
     }
     __syncthreads();
     // stable rank of each pair by expert id (n_rows <= kDecodeMaxPairs), whether
@@ -391,6 +386,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         const int e = s.ids[i];
         int p = 0, eq = 0;
         bool first = true;
+#pragma unroll 4
         for (int j = 0; j < n_rows; ++j) {
             const int f = s.ids[j];
             p += (f < e) || (f == e && j < i);
@@ -415,6 +411,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         if (!s.first[i]) continue;
         const int e = s.ids[i];
         int u = 0;
+#pragma unroll 4
         for (int j = 0; j < n_rows; ++j) u += s.first[j] && s.ids[j] < e;
         s.slot_e[u] = e;
         s.slot_row0[u] = s.pos[i];
@@ -640,6 +637,12 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         // split even|odd to the workspace; a second grid barrier publishes them
         for (int p = static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) * warp; p < P;
              p += static_cast<int>(gridDim.x) * kWarpsD) {
+            // the row's h values and its maximum in one round trip (PC2 = 1: 16 values
+            // per lane; larger I: the rest per chunk below)
+            const float4* src0 = reinterpret_cast<const float4*>(a.h + static_cast<int64_t>(p) * I + 16 * lane);
+            float4 f[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) f[q] = __ldcg(src0 + q);
             const uint32_t mb = __ldcg(a.row_max + p);
             const float sc = requant_scale(mb);
             const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
@@ -649,11 +652,15 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
             }
 #pragma unroll
             for (int c2 = 0; c2 < PC2; ++c2) {  // 16 values per lane per 512-value chunk
-                const float4* src = reinterpret_cast<const float4*>(a.h + static_cast<int64_t>(p) * I + 512 * c2 + 16 * lane);
+                if (c2 > 0) {
+                    const float4* src = reinterpret_cast<const float4*>(a.h + static_cast<int64_t>(p) * I + 512 * c2 + 16 * lane);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) f[q] = __ldcg(src + q);
+                }
                 uint2* dst = reinterpret_cast<uint2*>(a.hq_g + static_cast<int64_t>(p) * I + 512 * c2 + 16 * lane);
-#pragma unroll 1
-                for (int q = 0; q < 2; ++q) {  // 8 values -> one 8-byte group, split even|odd (a loop: run-once code stays short)
-                    const float4 f0 = __ldcg(src + 2 * q), f1 = __ldcg(src + 2 * q + 1);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {  // 8 values -> one 8-byte group, split even|odd
+                    const float4 f0 = f[2 * q], f1 = f[2 * q + 1];
                     const uint32_t w0 = (requant_code_fast(f0.x, sc, rs) & 0xFF) | ((requant_code_fast(f0.y, sc, rs) & 0xFF) << 8) |
                                         ((requant_code_fast(f0.z, sc, rs) & 0xFF) << 16) |
                                         ((static_cast<uint32_t>(requant_code_fast(f0.w, sc, rs)) & 0xFF) << 24);
