@@ -14,7 +14,7 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_w4a8.so")
-ABI_VERSION = 3
+ABI_VERSION = 4
 ENGINE_AUTO, ENGINE_GROUPED, ENGINE_DECODE, ENGINE_TCGEN05 = -1, 0, 1, 2
 NOALLOC_SCRATCH_BYTES = 16 << 20
 _lib = None
@@ -65,9 +65,12 @@ def _load():
     lib.moe_w4a8_engine_for.restype = ctypes.c_int
     lib.moe_w4a8_selftest_barrier_timeout.argtypes = [p, sz, p]
     lib.moe_w4a8_forward_noalloc.argtypes = [p, p, p, p, p, p, p, dp, p, p]
+    lib.moe_w4a8_forward_host_workspace_size.argtypes = [dp]
+    lib.moe_w4a8_forward_host_workspace_size.restype = sz
+    lib.moe_w4a8_forward_host.argtypes = [p, p, p, p, p, p, p, dp, p, p, sz, p]
     for name in ("moe_w4a8_forward", "moe_w4a8_forward_debug", "moe_w4a8_route", "moe_w4a8_gemm1_partials",
                  "moe_w4a8_gemm2_partials", "moe_w4a8_forward_noalloc", "moe_w4a8_device_status",
-                 "moe_w4a8_selftest_barrier_timeout"):
+                 "moe_w4a8_selftest_barrier_timeout", "moe_w4a8_forward_host"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.moe_w4a8_version() != ABI_VERSION:
         raise RuntimeError(f"{LIB_PATH}: ABI version {lib.moe_w4a8_version()} != {ABI_VERSION}")
@@ -172,6 +175,46 @@ def moe_w4a8_forward(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_pack
     _check("moe_w4a8_forward", _load().moe_w4a8_forward(
         _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
         _ptr(w2_scale), ctypes.byref(d), _ptr(out), wp, wb, _stream(out.device)))
+    return out
+
+
+def moe_w4a8_forward_host_workspace_size(d: Dims) -> int:
+    """Workspace of moe_w4a8_forward_host (the layer's plus the staged inputs and output)."""
+    n = _load().moe_w4a8_forward_host_workspace_size(ctypes.byref(d))
+    if n == 0:
+        raise MoeError("moe_w4a8_forward_host_workspace_size", 1)
+    return n
+
+
+def _need_host(t, name, dtype, shape):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if t.is_cuda or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be a contiguous CPU tensor of shape {tuple(shape)}")
+
+
+def moe_w4a8_forward_host(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d: Dims, out,
+                          workspace: torch.Tensor):
+    """The layer with x_q, x_scale, router_logits and out in host memory (CPU tensors).
+
+    Pinned tensors are read and written in place by the kernels (no copy
+    engine transfers); pageable ones go through asynchronous copies.  The
+    call is asynchronous on the current stream of the workspace's device:
+    synchronise it before reading `out` or reusing the inputs.
+    """
+    s13, s13s, s2, s2s = _bank_shapes(d)
+    _need_host(x_q, "x_q", torch.int8, (d.T, d.H))
+    _need_host(x_scale, "x_scale", torch.float32, (d.T,))
+    _need_host(router_logits, "router_logits", torch.float32, (d.T, d.E))
+    _need_host(out, "out", torch.float32, (d.T, d.H))
+    _need(w13_packed, "w13_packed", torch.uint8, s13)
+    _need(w13_scale, "w13_scale", torch.float32, s13s)
+    _need(w2_packed, "w2_packed", torch.uint8, s2)
+    _need(w2_scale, "w2_scale", torch.float32, s2s)
+    wp, wb = _ws_view(workspace)
+    _check("moe_w4a8_forward_host", _load().moe_w4a8_forward_host(
+        _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
+        _ptr(w2_scale), ctypes.byref(d), _ptr(out), wp, wb, _stream(workspace.device)))
     return out
 
 

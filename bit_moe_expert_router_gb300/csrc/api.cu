@@ -329,6 +329,105 @@ MOE_API int moe_w4a8_forward(const int8_t* x_q, const float* x_scale, const floa
                      views(workspace, L), static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Staging area after the layer's workspace: x_q, x_scale, logits, out.
+struct HostStage {
+    size_t x_q, x_scale, logits, out, total;
+};
+HostStage host_stage_of(const moe_dims_t* d, const WsLayout& L) {
+    HostStage h;
+    h.x_q = align256(L.total);
+    h.x_scale = h.x_q + align256(static_cast<size_t>(d->T) * d->H);
+    h.logits = h.x_scale + align256(sizeof(float) * d->T);
+    h.out = h.logits + align256(sizeof(float) * d->T * d->E);
+    h.total = h.out + align256(sizeof(float) * d->T * d->H);
+    return h;
+}
+
+// Where a caller's host-side buffer lives: 1 = page-locked host memory
+// mapped into the device address space (*dev = its device address),
+// 2 = device or managed memory (*dev = p), 0 = pageable host memory,
+// -1 = the runtime could not classify it.
+int host_buffer_kind(const void* p, void** dev) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    if (a.type == cudaMemoryTypeHost) {
+        if (!a.devicePointer) return 0;
+        *dev = a.devicePointer;
+        return 1;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+        *dev = const_cast<void*>(p);
+        return 2;
+    }
+    return 0;
+}
+
+}  // namespace
+
+MOE_API size_t moe_w4a8_forward_host_workspace_size(const moe_dims_t* d) {
+    if (check_dims(d) != MOE_OK) return 0;
+    return host_stage_of(d, layout_of(d)).total;
+}
+
+MOE_API int moe_w4a8_forward_host(const int8_t* x_q, const float* x_scale, const float* router_logits,
+                                  const uint8_t* w13_packed, const float* w13_scale, const uint8_t* w2_packed,
+                                  const float* w2_scale, const moe_dims_t* d, float* out, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    MOE_TRY(check_dims(d));
+    MOE_TRY(check_ptrs({w13_packed, w13_scale, w2_packed, w2_scale}));
+    if (d->T == 0) return MOE_OK;
+    MOE_TRY(check_ptrs({x_q, x_scale, router_logits, out}));
+    const WsLayout L = layout_of(d);
+    const HostStage hs = host_stage_of(d, L);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < hs.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+    // classify every buffer before anything is enqueued
+    const void* src[3] = {x_q, x_scale, router_logits};
+    const size_t bytes[3] = {static_cast<size_t>(d->T) * d->H, sizeof(float) * d->T, sizeof(float) * d->T * d->E};
+    const size_t off[3] = {hs.x_q, hs.x_scale, hs.logits};
+    int kind[3];
+    void* dev[3] = {nullptr, nullptr, nullptr};
+    for (int b = 0; b < 3; ++b)
+        if ((kind[b] = host_buffer_kind(src[b], &dev[b])) < 0) return MOE_ERR_INVALID_ARG;
+    void* out_dev = nullptr;
+    const int out_kind = host_buffer_kind(out, &out_dev);
+    if (out_kind < 0) return MOE_ERR_INVALID_ARG;
+
+    const void* in_dev[3];
+    moe::StageArgs sa{};
+    for (int b = 0; b < 3; ++b) {
+        if (kind[b] == 2) {  // device-accessible memory: used in place
+            in_dev[b] = dev[b];
+        } else if (kind[b] == 1) {  // mapped page-locked memory: one kernel reads it over the host link
+            sa.src[b] = dev[b];
+            sa.dst[b] = ws + off[b];
+            sa.bytes[b] = static_cast<int64_t>(bytes[b]);
+            in_dev[b] = ws + off[b];
+        } else {  // pageable: the driver stages the copy
+            MOE_CUDA(cudaMemcpyAsync(ws + off[b], src[b], bytes[b], cudaMemcpyHostToDevice, st));
+            in_dev[b] = ws + off[b];
+        }
+    }
+    MOE_CUDA(moe::launch_stage_copy(sa, st));
+    float* layer_out = out_kind == 0 ? reinterpret_cast<float*>(ws + hs.out) : static_cast<float*>(out_dev);
+    MOE_TRY(run_layer(static_cast<const int8_t*>(in_dev[0]), static_cast<const float*>(in_dev[1]),
+                      static_cast<const float*>(in_dev[2]), w13_packed, w13_scale, w2_packed, w2_scale, d, layer_out, L,
+                      views(workspace, L), st));
+    if (out_kind == 0)
+        MOE_CUDA(cudaMemcpyAsync(out, layer_out, sizeof(float) * d->T * d->H, cudaMemcpyDeviceToHost, st));
+    return MOE_OK;
+}
+
 MOE_API int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, const float* router_logits,
                                    const uint8_t* w13_packed, const float* w13_scale, const uint8_t* w2_packed,
                                    const float* w2_scale, const moe_dims_t* d, float* out, int8_t* h_q, float* s_h,

@@ -38,6 +38,17 @@ struct SortArgs {
 };
 cudaError_t launch_sort(const SortArgs& a, cudaStream_t st);
 
+// Copy of up to kStageBufs buffers (byte counts multiples of 4, addresses
+// 16-byte aligned) by one kernel; sources may be host memory mapped into
+// the device address space, read once over the host link.
+constexpr int kStageBufs = 3;
+struct StageArgs {
+    const void* src[kStageBufs];
+    void* dst[kStageBufs];
+    int64_t bytes[kStageBufs];
+};
+cudaError_t launch_stage_copy(const StageArgs& a, cudaStream_t st);
+
 enum class Gemm1Mode { kHidden, kPartials };
 enum class Gemm2Mode { kOutput, kPartials };
 

@@ -15,6 +15,8 @@
 #include <float.h>
 #include <math.h>
 
+#include <algorithm>
+
 #include "kernels.h"
 
 namespace moe {
@@ -243,6 +245,32 @@ cudaError_t launch_sort(const SortArgs& a, cudaStream_t st) {
     }
     scan_kernel<<<1, 1024, 0, st>>>(a, n_chunks);
     if (n_chunks > 0) scatter_kernel<<<static_cast<unsigned>(n_chunks), 32, hist_bytes, st>>>(a, n);
+    return cudaGetLastError();
+}
+
+// Grid-stride copy of the staged buffers: 16-byte words, then the 4-byte tail.
+__global__ void stage_copy_kernel(StageArgs a) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+#pragma unroll
+    for (int b = 0; b < kStageBufs; ++b) {
+        const int64_t n16 = a.bytes[b] / 16, n4 = a.bytes[b] / 4;
+        const uint4* s16 = static_cast<const uint4*>(a.src[b]);
+        uint4* d16 = static_cast<uint4*>(a.dst[b]);
+        for (int64_t i = i0; i < n16; i += stride) d16[i] = s16[i];
+        const uint32_t* s4 = static_cast<const uint32_t*>(a.src[b]);
+        uint32_t* d4 = static_cast<uint32_t*>(a.dst[b]);
+        for (int64_t i = 4 * n16 + i0; i < n4; i += stride) d4[i] = s4[i];
+    }
+}
+
+cudaError_t launch_stage_copy(const StageArgs& a, cudaStream_t st) {
+    int64_t total = 0;
+    for (int b = 0; b < kStageBufs; ++b) total += a.bytes[b];
+    if (total == 0) return cudaSuccess;
+    // about 32 KB per block, at most a wave of 152 blocks
+    const int64_t blocks = std::min<int64_t>(std::max<int64_t>(total / 32768, 1), 152);
+    stage_copy_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 

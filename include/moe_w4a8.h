@@ -77,7 +77,7 @@
 extern "C" {
 #endif
 
-#define MOE_W4A8_ABI_VERSION 3
+#define MOE_W4A8_ABI_VERSION 4
 
 /* Engines (the `engine` argument of the checking entry points).  AUTO picks
  * what moe_w4a8_forward picks: the fused decode engine when the batch fits
@@ -251,6 +251,42 @@ int moe_w4a8_forward_noalloc(const int8_t* x_q, const float* x_scale, const floa
                              const uint8_t* w13_packed, const float* w13_scale,
                              const uint8_t* w2_packed, const float* w2_scale,
                              const moe_dims_t* d, float* out, void* stream);
+
+/*
+ * Bytes of device workspace moe_w4a8_forward_host needs for `d`: the
+ * moe_w4a8_forward workspace plus room for the staged inputs and output
+ * (0 if `d` is invalid).  Host call, no device work.
+ */
+size_t moe_w4a8_forward_host_workspace_size(const moe_dims_t* d);
+
+/*
+ * moe_w4a8_forward with the activations, scales, logits and output in HOST
+ * memory (the weights and the workspace stay device memory).  (The pages
+ * have no counterpart; this is the step a host-side caller makes each
+ * decode step, with the transfers done by the library.)
+ *
+ * x_q, x_scale, router_logits, out: host pointers, layouts as for
+ * moe_w4a8_forward, 16-byte aligned.  Page-locked memory mapped into the
+ * device address space (cudaHostAlloc / cudaMallocHost / pinned tensors;
+ * with unified addressing every such allocation is mapped) is used in place: one
+ * small kernel reads the inputs over the host link into the workspace, and
+ * the layer writes `out` directly into host memory -- no copy engine
+ * transfers.  Pageable memory is accepted too: it goes through
+ * cudaMemcpyAsync (staged by the driver, which may block the calling
+ * thread).  Device or managed memory is used as is.
+ *
+ * As with any asynchronous transfer, the inputs must stay unchanged and
+ * `out` must not be read until `stream` has passed this call (synchronise
+ * the stream or an event recorded after it).  workspace: device memory of
+ * at least moe_w4a8_forward_host_workspace_size(d) bytes, 256-byte aligned.
+ * Errors as for moe_w4a8_forward; a pointer the runtime cannot classify
+ * (cudaPointerGetAttributes fails) is MOE_ERR_INVALID_ARG.
+ */
+int moe_w4a8_forward_host(const int8_t* x_q, const float* x_scale, const float* router_logits,
+                          const uint8_t* w13_packed, const float* w13_scale,
+                          const uint8_t* w2_packed, const float* w2_scale,
+                          const moe_dims_t* d, float* out,
+                          void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -31,7 +31,8 @@ def test_header_declares_the_entry_points():
     names = _declared_symbols()
     assert {"moe_w4a8_forward", "moe_w4a8_route", "moe_w4a8_workspace_size", "moe_w4a8_version",
             "moe_w4a8_status_string", "moe_w4a8_gemm1_partials", "moe_w4a8_gemm2_partials",
-            "moe_w4a8_forward_debug", "moe_w4a8_device_status"} <= names
+            "moe_w4a8_forward_debug", "moe_w4a8_device_status", "moe_w4a8_forward_host",
+            "moe_w4a8_forward_host_workspace_size"} <= names
 
 
 def test_library_exports_every_declared_symbol(cuda_lib, lib):
@@ -47,7 +48,7 @@ def test_library_exports_every_declared_symbol(cuda_lib, lib):
 
 def test_version_and_status_strings(lib):
     from bit_moe_expert_router_gb300 import binding
-    assert lib.moe_w4a8_version() == binding.ABI_VERSION == 3
+    assert lib.moe_w4a8_version() == binding.ABI_VERSION == 4
     for s in range(6):
         assert binding.moe_w4a8_status_string(s)
     assert binding.moe_w4a8_status_string(99) == "unknown status"
@@ -137,3 +138,25 @@ def test_engine_and_status_arguments_are_checked(lib):
     assert lib.moe_w4a8_device_status(None, 1024, None) == 1
     assert lib.moe_w4a8_device_status(ctypes.c_void_p(0x100010), 1024, None) == 1
     assert lib.moe_w4a8_device_status(fake, 16, None) == 1
+
+
+def test_host_buffer_entry_checks_before_touching_memory(lib):
+    from bit_moe_expert_router_gb300 import binding
+    d = binding.dims_of(4, 2048, 512, 512, 1, 10, 128)
+    need = lib.moe_w4a8_workspace_size(ctypes.byref(d))
+    need_host = lib.moe_w4a8_forward_host_workspace_size(ctypes.byref(d))
+    # the staged inputs (T*H int8, T floats, T*E floats) and output (T*H floats) on top, 256-aligned
+    assert need_host % 256 == 0
+    assert need_host >= need + d.T * d.H + 4 * d.T + 4 * d.T * d.E + 4 * d.T * d.H
+    d_bad = binding.dims_of(4, 2048, 512, 512, 1, 10, 48)
+    assert lib.moe_w4a8_forward_host_workspace_size(ctypes.byref(d_bad)) == 0
+    fake = ctypes.c_void_p(0x100000)       # never dereferenced: the checks fail first
+    odd = ctypes.c_void_p(0x100008)
+    args = [fake] * 7
+    assert lib.moe_w4a8_forward_host(odd, *args[1:], ctypes.byref(d), fake, fake, need_host, None) == 1
+    assert lib.moe_w4a8_forward_host(*args, ctypes.byref(d), None, fake, need_host, None) == 1
+    assert lib.moe_w4a8_forward_host(*args, ctypes.byref(d), fake, ctypes.c_void_p(0x100010), need_host, None) == 1
+    # the plain layer workspace is not enough: the staging area comes on top
+    assert lib.moe_w4a8_forward_host(*args, ctypes.byref(d), fake, fake, need, None) == 3
+    d0 = binding.dims_of(0, 2048, 512, 512, 1, 10, 128)
+    assert lib.moe_w4a8_forward_host(None, None, None, fake, fake, fake, fake, ctypes.byref(d0), None, None, 0, None) == 0

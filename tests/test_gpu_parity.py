@@ -422,3 +422,28 @@ def test_tcgen05_engine_rejects_groups_it_does_not_tile():
     with pytest.raises(binding.MoeError) as e:
         _forward_engine(w, tok, 2)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("name,pinned_in,pinned_out", [("decode_t4", True, True), ("decode_t4", False, False),
+                                                       ("decode_t4", True, False), ("tc_small", True, True),
+                                                       ("small_s1", False, True)])
+def test_forward_host_buffers_match_device_forward(name, pinned_in, pinned_out):
+    """Host-resident activations/logits/output: the same kernels, so the same bits as the device call."""
+    w = _workload(name) if name in EXTRA else (SMALL if name == "small_s1" else synth.WORKLOADS[name])
+    tok = synth.make_tokens(w)
+    d = gh.dims(w)
+    w13, s13, w2, s2 = gh.device_bank(w)
+    ws = binding.alloc_workspace(binding.moe_w4a8_forward_host_workspace_size(d), "cuda:0")
+    dev_out = torch.empty((w.T, w.H), dtype=torch.float32, device="cuda:0")
+    binding.moe_w4a8_forward(gh.to_dev(tok.x_q), gh.to_dev(tok.x_scale), gh.to_dev(tok.logits), w13, s13, w2, s2, d,
+                             dev_out, ws)
+    host_in = [torch.from_numpy(a.copy()) for a in (tok.x_q, tok.x_scale, tok.logits)]
+    if pinned_in:
+        host_in = [t.pin_memory() for t in host_in]
+    host_out = torch.full((w.T, w.H), float("nan"), dtype=torch.float32)
+    if pinned_out:
+        host_out = host_out.pin_memory()
+    binding.moe_w4a8_forward_host(*host_in, w13, s13, w2, s2, d, host_out, ws)
+    torch.cuda.synchronize()
+    assert binding.moe_w4a8_device_status(ws) == 0
+    assert torch.equal(host_out, dev_out.cpu())
