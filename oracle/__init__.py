@@ -41,6 +41,8 @@ def _load():
     lib.orc_hidden.restype = None
     lib.orc_requant.argtypes = [p, i64, p, p]
     lib.orc_requant.restype = None
+    lib.orc_quantize_bf16.argtypes = [p, i64, i64, p, p]
+    lib.orc_quantize_bf16.restype = None
     lib.orc_down.argtypes = [p, ctypes.c_float, p, p, i64, i64, i64, p, p]
     lib.orc_down.restype = None
     lib.orc_pair_output.argtypes = [ctypes.POINTER(Dims), p, p, p, p, p, p, i64, i64, p, p, p]
@@ -126,6 +128,16 @@ def requant(h: np.ndarray):
     sh = np.empty(1, np.float32)
     _load().orc_requant(_p(h), h.shape[0], _p(hq), _p(sh))
     return hq, float(sh[0])
+
+
+def quantize_bf16(x_bits: np.ndarray):
+    """S0 of bf16 activations (uint16 bit patterns [T][H]) -> (x_q int8 [T][H], x_scale float32 [T])."""
+    x_bits = _c(x_bits, np.uint16)
+    T, H = x_bits.shape
+    x_q = np.empty((T, H), np.int8)
+    x_scale = np.empty(T, np.float32)
+    _load().orc_quantize_bf16(_p(x_bits), T, H, _p(x_q), _p(x_scale))
+    return x_q, x_scale
 
 
 def down(hq, sh, w2e, s2e, group):

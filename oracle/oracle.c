@@ -182,6 +182,39 @@ void orc_requant(const double* h, int64_t I, int8_t* hq, float* sh) {
     }
 }
 
+/*
+ * S0, the activations' quantisation, for callers that hand the layer bf16
+ * activations: per token, s = max_h |x[t][h]| / 127 and
+ * q = clamp(RNE(x / s), -127, 127), an all-zero row giving s = 0 and q = 0
+ * (the same per-token symmetric int8 recipe as the workloads' inputs).
+ * x holds bf16 bit patterns; each is widened exactly to fp32 (the 16 bits
+ * become the high half of the fp32 word).  The integer decision is taken in
+ * fp32, the precision of the device kernels: fp32 maximum, fp32 division
+ * by 127, fp32 division x / s, round half to even.
+ */
+void orc_quantize_bf16(const uint16_t* x, int64_t T, int64_t H, int8_t* x_q, float* x_scale) {
+    for (int64_t t = 0; t < T; ++t) {
+        float amax = 0.0f;
+        for (int64_t h = 0; h < H; ++h) {
+            uint32_t bits = (uint32_t)x[t * H + h] << 16;
+            float v;
+            memcpy(&v, &bits, sizeof v);
+            if (fabsf(v) > amax) amax = fabsf(v);
+        }
+        float s = amax / 127.0f;
+        x_scale[t] = s;
+        for (int64_t h = 0; h < H; ++h) {
+            uint32_t bits = (uint32_t)x[t * H + h] << 16;
+            float v;
+            memcpy(&v, &bits, sizeof v);
+            float q = (s > 0.0f) ? rintf(v / s) : 0.0f;
+            if (q > 127.0f) q = 127.0f;
+            if (q < -127.0f) q = -127.0f;
+            x_q[t * H + h] = (int8_t)q;
+        }
+    }
+}
+
 /* gemm2 for one pair: Y[n] = s_h * sum_q s2[n][q] * P2[n][q]; P2 optional [H][I/g]. */
 void orc_down(const int8_t* hq, float sh, const uint8_t* w2e, const float* s2e,
               int64_t H, int64_t I, int64_t g, int32_t* P2, double* y) {

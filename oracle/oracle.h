@@ -20,6 +20,7 @@ double orc_silu(double z);
 void orc_hidden(const int8_t* x, float x_scale, const uint8_t* w13e, const float* s13e,
                 int64_t H, int64_t I, int64_t g, int32_t* P1, double* G, double* h);
 void orc_requant(const double* h, int64_t I, int8_t* hq, float* sh);
+void orc_quantize_bf16(const uint16_t* x, int64_t T, int64_t H, int8_t* x_q, float* x_scale);
 void orc_down(const int8_t* hq, float sh, const uint8_t* w2e, const float* s2e,
               int64_t H, int64_t I, int64_t g, int32_t* P2, double* y);
 void orc_pair_output(const orc_dims_t* d, const int8_t* x_q, const float* x_scale,

@@ -381,3 +381,57 @@ def test_zipf_bias_skews_expert_load():
     ids, _ = oracle.route(synth.make_tokens(w).logits, w.top_k)
     counts = np.sort(np.bincount(ids.ravel(), minlength=w.E))[::-1]
     assert counts[0] > 0.5 * w.T and counts[w.E // 2] == 0
+
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of fp32 values that are exact in bf16 (checked)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0), "value not exact in bf16"
+    return (u >> 16).astype(np.uint16)
+
+
+def test_s0_quantisation_golden_rows():
+    """Hand-worked rows (scales powers of two, half-way cases): exact codes and scales."""
+    rows = []
+    for line in open(os.path.join(GOLDEN, "s0_quant_bf16.txt")):
+        line = line.split("#")[0].split()
+        if line:
+            rows.append((line[0], [float(v) for v in line[1:]]))
+    xs = [v for k, v in rows if k == "x"]
+    ss = [v[0] for k, v in rows if k == "s"]
+    qs = [v for k, v in rows if k == "q"]
+    assert len(xs) == len(ss) == len(qs) == 5
+    x_q, x_scale = oracle.quantize_bf16(_bf16_bits(np.array(xs, np.float32)))
+    assert np.array_equal(x_scale, np.array(ss, np.float32))
+    assert np.array_equal(x_q, np.array(qs, np.int8))
+
+
+def test_s0_quantisation_matches_the_generators_own_quantiser():
+    """Two independent implementations of the same recipe agree bit for bit."""
+    for name in ("tiny", "decode_t4", "decode_verify_t12", "large_bank_t2048"):
+        w = synth.WORKLOADS[name].with_tokens(min(synth.WORKLOADS[name].T, 64))
+        tok = synth.make_tokens(w)
+        x_q, x_scale = oracle.quantize_bf16(_bf16_bits(synth.bf16_activations(w)))
+        assert np.array_equal(x_scale, tok.x_scale), name
+        assert np.array_equal(x_q, tok.x_q), name
+
+
+def test_s0_quantisation_invariants():
+    rng = np.random.default_rng(11)
+    T, H = 40, 256
+    x = (rng.standard_normal((T, H)) * np.exp(rng.uniform(-20, 20, size=(T, 1)))).astype(np.float32)
+    x = (x.view(np.uint32) & 0xFFFF0000).view(np.float32)  # truncate to bf16
+    x[3] = 0.0
+    x[4] = -0.0
+    x[5, :] = 0.0
+    x[5, 17] = -3.0
+    x_q, s = oracle.quantize_bf16(_bf16_bits(x))
+    assert s[3] == 0 and s[4] == 0 and not x_q[3].any() and not x_q[4].any()
+    live = s > 0
+    assert np.all(np.abs(x_q.astype(int)) <= 127)
+    assert np.all(np.abs(x_q[live].astype(int)).max(axis=1) == 127)
+    assert x_q[5, 17] == -127 and np.count_nonzero(x_q[5]) == 1
+    # each code is the nearest integer to x / s (within fp32 rounding of the division)
+    err = np.abs(x_q[live].astype(np.float64) - x[live].astype(np.float64) / s[live, None].astype(np.float64))
+    assert np.all(err <= 0.5 + 1e-5)
