@@ -68,9 +68,12 @@ def _load():
     lib.moe_w4a8_forward_host_workspace_size.argtypes = [dp]
     lib.moe_w4a8_forward_host_workspace_size.restype = sz
     lib.moe_w4a8_forward_host.argtypes = [p, p, p, p, p, p, p, dp, p, p, sz, p]
+    lib.moe_w4a8_forward_bf16_workspace_size.argtypes = [dp]
+    lib.moe_w4a8_forward_bf16_workspace_size.restype = sz
+    lib.moe_w4a8_forward_bf16.argtypes = [p, p, p, p, p, p, dp, p, p, sz, p]
     for name in ("moe_w4a8_forward", "moe_w4a8_forward_debug", "moe_w4a8_route", "moe_w4a8_gemm1_partials",
                  "moe_w4a8_gemm2_partials", "moe_w4a8_forward_noalloc", "moe_w4a8_device_status",
-                 "moe_w4a8_selftest_barrier_timeout", "moe_w4a8_forward_host"):
+                 "moe_w4a8_selftest_barrier_timeout", "moe_w4a8_forward_host", "moe_w4a8_forward_bf16"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.moe_w4a8_version() != ABI_VERSION:
         raise RuntimeError(f"{LIB_PATH}: ABI version {lib.moe_w4a8_version()} != {ABI_VERSION}")
@@ -215,6 +218,32 @@ def moe_w4a8_forward_host(x_q, x_scale, router_logits, w13_packed, w13_scale, w2
     _check("moe_w4a8_forward_host", _load().moe_w4a8_forward_host(
         _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
         _ptr(w2_scale), ctypes.byref(d), _ptr(out), wp, wb, _stream(workspace.device)))
+    return out
+
+
+def moe_w4a8_forward_bf16_workspace_size(d: Dims) -> int:
+    """Workspace of moe_w4a8_forward_bf16 (the layer's plus the quantised activations)."""
+    n = _load().moe_w4a8_forward_bf16_workspace_size(ctypes.byref(d))
+    if n == 0:
+        raise MoeError("moe_w4a8_forward_bf16_workspace_size", 1)
+    return n
+
+
+def moe_w4a8_forward_bf16(x_bf16, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d: Dims, out,
+                          workspace: torch.Tensor):
+    """The layer from bf16 activations [T, H]: the per-token int8 quantisation runs on the device."""
+    s13, s13s, s2, s2s = _bank_shapes(d)
+    _need(x_bf16, "x_bf16", torch.bfloat16, (d.T, d.H))
+    _need(router_logits, "router_logits", torch.float32, (d.T, d.E))
+    _need(w13_packed, "w13_packed", torch.uint8, s13)
+    _need(w13_scale, "w13_scale", torch.float32, s13s)
+    _need(w2_packed, "w2_packed", torch.uint8, s2)
+    _need(w2_scale, "w2_scale", torch.float32, s2s)
+    _need(out, "out", torch.float32, (d.T, d.H))
+    wp, wb = _ws_view(workspace)
+    _check("moe_w4a8_forward_bf16", _load().moe_w4a8_forward_bf16(
+        _ptr(x_bf16), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed), _ptr(w2_scale),
+        ctypes.byref(d), _ptr(out), wp, wb, _stream(out.device)))
     return out
 
 

@@ -137,10 +137,11 @@ bool decode_forward_plan(const moe_dims_t* d, moe::DecodePlan* pl) {
 
 int run_decode(const int8_t* x_q, const float* x_scale, const float* logits, const uint8_t* w13, const float* s13,
                const uint8_t* w2, const float* s2, const moe_dims_t* d, float* out, const Views& v,
-               const moe::DecodePlan& pl, float* y_debug, cudaStream_t st) {
+               const moe::DecodePlan& pl, float* y_debug, cudaStream_t st, const uint16_t* x_bf16 = nullptr) {
     moe::DecodeArgs a{};
     a.x_q = x_q;
     a.x_scale = x_scale;
+    a.x_bf16 = x_bf16;
     a.logits = logits;
     a.w13 = w13;
     a.s13 = s13;
@@ -426,6 +427,46 @@ MOE_API int moe_w4a8_forward_host(const int8_t* x_q, const float* x_scale, const
     if (out_kind == 0)
         MOE_CUDA(cudaMemcpyAsync(out, layer_out, sizeof(float) * d->T * d->H, cudaMemcpyDeviceToHost, st));
     return MOE_OK;
+}
+
+namespace {
+// Staging area of moe_w4a8_forward_bf16 after the layer's workspace: x_q [T][H], x_scale [T].
+size_t bf16_stage_xq(const WsLayout& L) { return align256(L.total); }
+size_t bf16_stage_xs(const moe_dims_t* d, const WsLayout& L) {
+    return bf16_stage_xq(L) + align256(static_cast<size_t>(d->T) * d->H);
+}
+size_t bf16_stage_total(const moe_dims_t* d, const WsLayout& L) {
+    return bf16_stage_xs(d, L) + align256(sizeof(float) * d->T);
+}
+}  // namespace
+
+MOE_API size_t moe_w4a8_forward_bf16_workspace_size(const moe_dims_t* d) {
+    if (check_dims(d) != MOE_OK) return 0;
+    return bf16_stage_total(d, layout_of(d));
+}
+
+MOE_API int moe_w4a8_forward_bf16(const uint16_t* x_bf16, const float* router_logits, const uint8_t* w13_packed,
+                                  const float* w13_scale, const uint8_t* w2_packed, const float* w2_scale,
+                                  const moe_dims_t* d, float* out, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+    MOE_TRY(check_dims(d));
+    MOE_TRY(check_ptrs({w13_packed, w13_scale, w2_packed, w2_scale}));
+    if (d->T == 0) return MOE_OK;
+    MOE_TRY(check_ptrs({x_bf16, router_logits, out}));
+    const WsLayout L = layout_of(d);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < bf16_stage_total(d, L)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const Views v = views(workspace, L);
+    moe::DecodePlan pl;
+    if (decode_forward_plan(d, &pl))  // the fused kernel quantises the activations itself
+        return run_decode(nullptr, nullptr, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out, v, pl,
+                          nullptr, st, x_bf16);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int8_t* x_q = reinterpret_cast<int8_t*>(ws + bf16_stage_xq(L));
+    float* x_scale = reinterpret_cast<float*>(ws + bf16_stage_xs(d, L));
+    MOE_CUDA(moe::launch_quantize_bf16(x_bf16, d->T, d->H, x_q, x_scale, st));
+    return run_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out, L, v, st);
 }
 
 MOE_API int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, const float* router_logits,

@@ -367,7 +367,50 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         n_rows = a.n_pairs;  // listed pairs; out-of-range slots and tokens are clamped (never read out of bounds)
         for (int r = tid; r < n_rows; r += kThreadsD) s.ids[r] = min(max(a.pair_slot[r], 0), a.E - 1);
     }
-    if (MODE != DecodeMode::kGemm2Partials) {
+    if (MODE == DecodeMode::kForward && a.x_bf16) {
+        // S0 on the device: the warps that do not route quantise the bf16
+        // activations (s = max|x| / 127, q = RNE(x / s) decided in fp32, clamped
+        // to +-127; zero row: s = 0, q = 0) into the split staging layout.  wpt
+        // warps share a token: each finds the row maximum itself (no sync) and
+        // codes the 8-value groups i = part, part + wpt, ... of every lane
+        // (group lane + 32 i).  Codes come from x * (1/s) with the exact
+        // division only near a half-step, as in the requantisation.
+        constexpr int NV = H / 256;  // 8-value groups per lane
+        const int w0 = nrw < kWarpsD ? nrw : 0, nws = kWarpsD - w0;
+        const int wpt = max(1, min(NV, nws / max(T, 1))), ntw = nws / wpt, rel = warp - w0;
+        if (warp >= w0 && rel < ntw * wpt)
+            for (int t = rel / wpt; t < T; t += ntw) {
+                const int part = rel % wpt;
+                const uint4* xr = reinterpret_cast<const uint4*>(a.x_bf16 + static_cast<int64_t>(t) * H);
+                float amax = 0.f;
+#pragma unroll 4
+                for (int i = 0; i < NV; ++i) {
+                    const uint4 v = xr[lane + 32 * i];
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wv[j] << 16)), fabsf(__uint_as_float(wv[j] & 0xFFFF0000u))));
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+                const float sc = __fdiv_rn(amax, 127.0f);
+                const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+                if (lane == 0 && part == 0) s.xs[t] = sc;
+                for (int i = part; i < NV; i += wpt) {
+                    const uint4 v = xr[lane + 32 * i];
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t b = (j & 1) ? (wv[j >> 1] & 0xFFFF0000u) : (wv[j >> 1] << 16);
+                        packed[j >> 2] |= (static_cast<uint32_t>(requant_code_fast(__uint_as_float(b), sc, rs)) & 0xFFu)
+                                          << (8 * (j & 3));
+                    }
+                    *reinterpret_cast<uint2*>(s.x + t * XS + 8 * (lane + 32 * i)) =
+                        make_uint2(__byte_perm(packed[0], packed[1], 0x6420), __byte_perm(packed[0], packed[1], 0x7531));
+                }
+            }
+    } else if (MODE != DecodeMode::kGemm2Partials) {
         const int st0 = nrw < kWarpsD ? 32 * nrw : 0, nst = kThreadsD - st0;
         if (tid >= st0) {
 #pragma unroll 4

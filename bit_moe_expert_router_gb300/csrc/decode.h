@@ -14,6 +14,7 @@ enum class DecodeMode { kForward, kGemm1Partials, kGemm2Partials };
 struct DecodeArgs {
     const int8_t* x_q;
     const float* x_scale;
+    const uint16_t* x_bf16;  // forward: bf16 activations [T][H] quantised in the kernel (x_q / x_scale unused), or null
     const float* logits;
     const uint8_t* w13;
     const float* s13;

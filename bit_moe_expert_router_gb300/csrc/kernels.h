@@ -49,6 +49,11 @@ struct StageArgs {
 };
 cudaError_t launch_stage_copy(const StageArgs& a, cudaStream_t st);
 
+// S0 of bf16 activations [T][H] (bit patterns): per token s = max|x| / 127,
+// q = clamp(RNE(x / s), -127, 127) in IEEE fp32; an all-zero row gives s = 0.
+cudaError_t launch_quantize_bf16(const uint16_t* x, int64_t T, int64_t H, int8_t* x_q, float* x_scale,
+                                 cudaStream_t st);
+
 enum class Gemm1Mode { kHidden, kPartials };
 enum class Gemm2Mode { kOutput, kPartials };
 

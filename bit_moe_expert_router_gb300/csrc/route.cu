@@ -274,4 +274,48 @@ cudaError_t launch_stage_copy(const StageArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// One warp per token: the row maximum, then the codes (8 values per step).
+__global__ void quantize_bf16_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int8_t* __restrict__ x_q,
+                                     float* __restrict__ x_scale) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + t * H);
+    const int64_t n8 = H / 8;  // H is a multiple of 128
+    float amax = 0.f;
+    for (int64_t i = lane; i < n8; i += 32) {
+        const uint4 v = xr[i];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wv[j] << 16)), fabsf(__uint_as_float(wv[j] & 0xFFFF0000u))));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float sc = __fdiv_rn(amax, 127.0f);
+    if (lane == 0) x_scale[t] = sc;
+    uint2* qr = reinterpret_cast<uint2*>(x_q + t * H);
+    for (int64_t i = lane; i < n8; i += 32) {
+        const uint4 v = xr[i];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t b = (j & 1) ? (wv[j >> 1] & 0xFFFF0000u) : (wv[j >> 1] << 16);
+            float q = sc > 0.0f ? rintf(__fdiv_rn(__uint_as_float(b), sc)) : 0.0f;
+            q = fminf(fmaxf(q, -127.0f), 127.0f);
+            packed[j >> 2] |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xFFu) << (8 * (j & 3));
+        }
+        qr[i] = make_uint2(packed[0], packed[1]);
+    }
+}
+
+cudaError_t launch_quantize_bf16(const uint16_t* x, int64_t T, int64_t H, int8_t* x_q, float* x_scale,
+                                 cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    const int warps = 8;
+    quantize_bf16_kernel<<<static_cast<unsigned>((T + warps - 1) / warps), 32 * warps, 0, st>>>(x, T, H, x_q, x_scale);
+    return cudaGetLastError();
+}
+
 }  // namespace moe

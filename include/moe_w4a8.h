@@ -288,6 +288,33 @@ int moe_w4a8_forward_host(const int8_t* x_q, const float* x_scale, const float* 
                           const moe_dims_t* d, float* out,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace moe_w4a8_forward_bf16 needs for `d` (the
+ * moe_w4a8_forward workspace plus T*H + 4T bytes, each area 256-aligned;
+ * 0 if `d` is invalid).  Host call, no device work. */
+size_t moe_w4a8_forward_bf16_workspace_size(const moe_dims_t* d);
+
+/*
+ * The layer from bf16 activations: S0, the per-token quantisation, runs on
+ * the device as part of the call (section 5 of the page: keep the decode
+ * step's work on the device, no host round trips).  x_bf16: device array
+ * [T][H] of bf16 bit patterns (16-byte aligned).  Per token t:
+ * x_scale[t] = max_h |x[t][h]| / 127 and x_q[t][h] = clamp(RNE(x[t][h] /
+ * x_scale[t]), -127, 127), decided in IEEE fp32 (an all-zero row gives
+ * x_scale = 0 and x_q = 0) -- the per-token symmetric int8 activations that
+ * moe_w4a8_forward takes -- then the layer as moe_w4a8_forward.  The decode
+ * engine quantises inside its single kernel (the warps that do not route
+ * do it while the others route); the other engines run one quantisation
+ * kernel first.  Same codes as the recipe, so the result equals
+ * moe_w4a8_forward on the quantised activations bit for bit.
+ * workspace: at least moe_w4a8_forward_bf16_workspace_size(d) bytes,
+ * 256-byte aligned.  Other arguments and errors as for moe_w4a8_forward.
+ */
+int moe_w4a8_forward_bf16(const uint16_t* x_bf16, const float* router_logits,
+                          const uint8_t* w13_packed, const float* w13_scale,
+                          const uint8_t* w2_packed, const float* w2_scale,
+                          const moe_dims_t* d, float* out,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

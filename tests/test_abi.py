@@ -32,7 +32,8 @@ def test_header_declares_the_entry_points():
     assert {"moe_w4a8_forward", "moe_w4a8_route", "moe_w4a8_workspace_size", "moe_w4a8_version",
             "moe_w4a8_status_string", "moe_w4a8_gemm1_partials", "moe_w4a8_gemm2_partials",
             "moe_w4a8_forward_debug", "moe_w4a8_device_status", "moe_w4a8_forward_host",
-            "moe_w4a8_forward_host_workspace_size"} <= names
+            "moe_w4a8_forward_host_workspace_size", "moe_w4a8_forward_bf16",
+            "moe_w4a8_forward_bf16_workspace_size"} <= names
 
 
 def test_library_exports_every_declared_symbol(cuda_lib, lib):
@@ -160,3 +161,19 @@ def test_host_buffer_entry_checks_before_touching_memory(lib):
     assert lib.moe_w4a8_forward_host(*args, ctypes.byref(d), fake, fake, need, None) == 3
     d0 = binding.dims_of(0, 2048, 512, 512, 1, 10, 128)
     assert lib.moe_w4a8_forward_host(None, None, None, fake, fake, fake, fake, ctypes.byref(d0), None, None, 0, None) == 0
+
+
+def test_bf16_entry_checks_its_arguments(lib):
+    from bit_moe_expert_router_gb300 import binding
+    d = binding.dims_of(4, 2048, 512, 512, 1, 10, 128)
+    need = lib.moe_w4a8_workspace_size(ctypes.byref(d))
+    need_bf16 = lib.moe_w4a8_forward_bf16_workspace_size(ctypes.byref(d))
+    assert need_bf16 % 256 == 0 and need_bf16 >= need + d.T * d.H + 4 * d.T
+    fake = ctypes.c_void_p(0x100000)       # never dereferenced: the checks fail first
+    w = [fake] * 4
+    assert lib.moe_w4a8_forward_bf16(None, fake, *w, ctypes.byref(d), fake, fake, need_bf16, None) == 1
+    assert lib.moe_w4a8_forward_bf16(ctypes.c_void_p(0x100008), fake, *w, ctypes.byref(d), fake, fake, need_bf16,
+                                     None) == 1
+    assert lib.moe_w4a8_forward_bf16(fake, fake, *w, ctypes.byref(d), fake, fake, need, None) == 3
+    d0 = binding.dims_of(0, 2048, 512, 512, 1, 10, 128)
+    assert lib.moe_w4a8_forward_bf16(None, None, *w, ctypes.byref(d0), None, None, 0, None) == 0

@@ -447,3 +447,34 @@ def test_forward_host_buffers_match_device_forward(name, pinned_in, pinned_out):
     torch.cuda.synchronize()
     assert binding.moe_w4a8_device_status(ws) == 0
     assert torch.equal(host_out, dev_out.cpu())
+
+
+@pytest.mark.parametrize("name", ["decode_t4", "decode_verify_t12", "dec_small", "dec_g64", "large_bank_t2048",
+                                  "tc_small", "small_s1"])
+def test_forward_bf16_quantises_on_device_bit_exactly(name):
+    """S0 on the device: the same codes as the oracle's S0, so the same output bits as moe_w4a8_forward."""
+    if name == "small_s1":
+        w = SMALL
+    elif name == "large_bank_t2048":
+        w = synth.WORKLOADS[name].with_tokens(6)  # the decode engine at H = 4096
+    else:
+        w = _workload(name)
+    xb = synth.bf16_activations(w)
+    xb[0, :] = 0.0                      # an all-zero token: s = 0, codes 0
+    if w.T > 1:
+        xb[1, 5] = -3.0 * np.abs(xb[1]).max()  # the row maximum at a negative value
+    bits = (np.ascontiguousarray(xb, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    x_q, x_scale = oracle.quantize_bf16(bits)
+    assert x_scale[0] == 0 and not x_q[0].any()
+    tok = synth.make_tokens(w)
+    d = gh.dims(w)
+    w13, s13, w2, s2 = gh.device_bank(w)
+    ws = binding.alloc_workspace(binding.moe_w4a8_forward_bf16_workspace_size(d), "cuda:0")
+    ref = torch.empty((w.T, w.H), dtype=torch.float32, device="cuda:0")
+    binding.moe_w4a8_forward(gh.to_dev(x_q), gh.to_dev(x_scale), gh.to_dev(tok.logits), w13, s13, w2, s2, d, ref, ws)
+    out = torch.full((w.T, w.H), float("nan"), dtype=torch.float32, device="cuda:0")
+    x_dev = torch.from_numpy(bits.view(np.int16)).to("cuda:0").view(torch.bfloat16)
+    binding.moe_w4a8_forward_bf16(x_dev, gh.to_dev(tok.logits), w13, s13, w2, s2, d, out, ws)
+    torch.cuda.synchronize()
+    assert binding.moe_w4a8_device_status(ws) == 0
+    assert torch.equal(out, ref)
