@@ -478,3 +478,34 @@ def test_forward_bf16_quantises_on_device_bit_exactly(name):
     torch.cuda.synchronize()
     assert binding.moe_w4a8_device_status(ws) == 0
     assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("name", ["decode_t4", "tc_small"])
+def test_layer_call_captures_into_a_cuda_graph(name):
+    """The call enqueues kernels only (no sync, no allocation): a captured graph replays it on new inputs."""
+    w = _workload(name) if name in EXTRA else synth.WORKLOADS[name]
+    d = gh.dims(w)
+    w13, s13, w2, s2 = gh.device_bank(w)
+    ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), "cuda:0")
+    toks = [synth.make_tokens(w, batch=b) for b in range(3)]
+    x_q, x_s, lg = (gh.to_dev(a) for a in (toks[0].x_q, toks[0].x_scale, toks[0].logits))
+    out = torch.empty((w.T, w.H), dtype=torch.float32, device="cuda:0")
+    eager = []
+    for t in toks:
+        o = torch.empty_like(out)
+        binding.moe_w4a8_forward(gh.to_dev(t.x_q), gh.to_dev(t.x_scale), gh.to_dev(t.logits), w13, s13, w2, s2, d, o, ws)
+        eager.append(o)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            binding.moe_w4a8_forward(x_q, x_s, lg, w13, s13, w2, s2, d, out, ws)
+    for b in (1, 2, 0):
+        x_q.copy_(gh.to_dev(toks[b].x_q))
+        x_s.copy_(gh.to_dev(toks[b].x_scale))
+        lg.copy_(gh.to_dev(toks[b].logits))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager[b]), f"replay on batch {b}"
+    assert binding.moe_w4a8_device_status(ws) == 0
