@@ -115,6 +115,7 @@ class Bank:
     w2: np.ndarray    # uint8 [slots, H, I/2]
     s2: np.ndarray    # float32 [slots, H, I/g]
     twobit: np.ndarray  # bool [slots]: expert quantised to the 2-bit code range
+    slot_bits: np.ndarray = None  # uint8 [slots]: storage width of each slot (4, or 2 for true 2-bit packing)
 
 
 @dataclasses.dataclass
@@ -148,8 +149,21 @@ def twobit_experts(w: Workload) -> np.ndarray:
     return flags
 
 
-def make_bank(w: Workload, with_codes: bool = False):
-    """The packed bank; with_codes also returns the int8 codes (w13 [slots,2I,H], w2 [slots,H,I])."""
+def pack2_rows(codes: np.ndarray, row_bytes: int) -> np.ndarray:
+    """Rows of 2-bit codes [rows, K] (values in [-2, 1]) packed 4 per byte, low bits first, into rows of
+    row_bytes bytes (the first K/4 bytes; the rest zero)."""
+    c = (codes.astype(np.int16) & 0x3).astype(np.uint8).reshape(codes.shape[0], -1, 4)
+    out = np.zeros((codes.shape[0], row_bytes), np.uint8)
+    out[:, :codes.shape[1] // 4] = c[:, :, 0] | (c[:, :, 1] << 2) | (c[:, :, 2] << 4) | (c[:, :, 3] << 6)
+    return out
+
+
+def make_bank(w: Workload, with_codes: bool = False, pack2: bool = False):
+    """The packed bank; with_codes also returns the int8 codes (w13 [slots,2I,H], w2 [slots,H,I]).
+
+    pack2: the 2-bit experts are stored with true 2-bit packing (4 codes per byte in the first half of each
+    row) and slot_bits marks them 2; otherwise every slot uses the int4 packing (slot_bits all 4).
+    """
     lib = _load()
     H, I, g, slots = w.H, w.I, w.group, w.slots
     w13 = np.empty((slots, 2 * I, H // 2), dtype=np.uint8)
@@ -159,13 +173,21 @@ def make_bank(w: Workload, with_codes: bool = False):
     c13 = np.empty((slots, 2 * I, H), dtype=np.int8) if with_codes else None
     c2 = np.empty((slots, H, I), dtype=np.int8) if with_codes else None
     twobit = twobit_experts(w)
+    slot_bits = np.full(slots, 4, np.uint8)
     for e in range(slots):
         qmax, qlo, qhi = (2, -2, 1) if twobit[e] else (7, -8, 7)
+        two = pack2 and twobit[e]
+        k13 = c13[e] if with_codes else (np.empty((2 * I, H), np.int8) if two else None)
+        k2 = c2[e] if with_codes else (np.empty((H, I), np.int8) if two else None)
         lib.synth_weight_matrix(w.seed, STREAM_W13, e, 2 * I, H, g, 0.02, qmax, qlo, qhi,
-                                _ptr(w13[e]), _ptr(s13[e]), _ptr(c13[e]) if with_codes else None)
+                                _ptr(w13[e]), _ptr(s13[e]), _ptr(k13) if k13 is not None else None)
         lib.synth_weight_matrix(w.seed, STREAM_W2, e, H, I, g, 0.02, qmax, qlo, qhi,
-                                _ptr(w2[e]), _ptr(s2[e]), _ptr(c2[e]) if with_codes else None)
-    bank = Bank(w13, s13, w2, s2, twobit)
+                                _ptr(w2[e]), _ptr(s2[e]), _ptr(k2) if k2 is not None else None)
+        if two:
+            w13[e] = pack2_rows(k13, H // 2)
+            w2[e] = pack2_rows(k2, I // 2)
+            slot_bits[e] = 2
+    bank = Bank(w13, s13, w2, s2, twobit, slot_bits)
     return (bank, c13, c2) if with_codes else bank
 
 

@@ -31,6 +31,9 @@ def _load():
     lib = ctypes.CDLL(LIB_PATH)
     i64, p = ctypes.c_int64, ctypes.c_void_p
     lib.orc_unpack.argtypes = [ctypes.c_uint8, ctypes.c_int]
+    lib.orc_unpack2.argtypes = [ctypes.c_uint8, ctypes.c_int]
+    lib.orc_partials_bits.argtypes = [p, i64, p, i64, i64, ctypes.c_int, p]
+    lib.orc_partials_bits.restype = None
     lib.orc_route.argtypes = [i64, i64, i64, p, p, p]
     lib.orc_permute.argtypes = [i64, i64, i64, p, p, p, p, p]
     lib.orc_partials.argtypes = [p, i64, p, i64, i64, p]
@@ -48,6 +51,7 @@ def _load():
     lib.orc_pair_output.argtypes = [ctypes.POINTER(Dims), p, p, p, p, p, p, i64, i64, p, p, p]
     lib.orc_pair_output.restype = None
     lib.orc_forward_tokens.argtypes = [ctypes.POINTER(Dims), p, p, p, p, p, p, p, i64, p, p]
+    lib.orc_forward_tokens_mixed.argtypes = [ctypes.POINTER(Dims), p, p, p, p, p, p, p, p, i64, p, p]
     _lib = lib
     return lib
 
@@ -92,15 +96,20 @@ def permute(ids: np.ndarray, E: int):
     return counts, offsets, perm, inv
 
 
-def partials(a: np.ndarray, W: np.ndarray, group: int) -> np.ndarray:
-    """int32 [rows, K/g] partials of int8 row a (K) against packed rows W [rows, K/2]."""
+def partials(a: np.ndarray, W: np.ndarray, group: int, bits: int = 4) -> np.ndarray:
+    """int32 [rows, K/g] partials of int8 row a (K) against packed rows W [rows, K/2] of `bits`-bit codes."""
     a = _c(a, np.int8)
     W = _c(W, np.uint8)
     K = a.shape[0]
     rows = W.shape[0]
     P = np.empty((rows, K // group), np.int32)
-    _load().orc_partials(_p(a), K, _p(W), rows, group, _p(P))
+    _load().orc_partials_bits(_p(a), K, _p(W), rows, group, bits, _p(P))
     return P
+
+
+def unpack2(byte: int, pos: int) -> int:
+    """The 2-bit code at position pos (0..3) of a packed byte."""
+    return _load().orc_unpack2(byte, pos)
 
 
 def silu(z: float) -> float:
@@ -169,14 +178,19 @@ def pair_output(d: Dims, x_q, x_scale, w13, s13, w2, s2, t: int, slot: int):
     return hq, float(sh[0]), y
 
 
-def forward_tokens(d: Dims, x_q, x_scale, logits, w13, s13, w2, s2, tokens=None) -> np.ndarray:
-    """Layer output (f64 [len(tokens), H]) for the listed tokens (all tokens if None)."""
+def forward_tokens(d: Dims, x_q, x_scale, logits, w13, s13, w2, s2, tokens=None, slot_bits=None) -> np.ndarray:
+    """Layer output (f64 [len(tokens), H]) for the listed tokens (all tokens if None).
+
+    slot_bits (optional uint8 [E+S], 2 or 4): each slot's code width (default: all 4).
+    """
     x_q, x_scale, w13, s13, w2, s2 = _layer_args(x_q, x_scale, w13, s13, w2, s2)
     logits = _c(logits, np.float32)
     tokens = np.arange(d.T, dtype=np.int64) if tokens is None else _c(tokens, np.int64)
+    bits = None if slot_bits is None else _c(slot_bits, np.uint8)
     out = np.empty((tokens.shape[0], d.H), np.float64)
-    if _load().orc_forward_tokens(ctypes.byref(d), _p(x_q), _p(x_scale), _p(logits), _p(w13), _p(s13),
-                                  _p(w2), _p(s2), tokens.shape[0], _p(tokens), _p(out)):
+    if _load().orc_forward_tokens_mixed(ctypes.byref(d), _p(x_q), _p(x_scale), _p(logits), _p(w13), _p(s13),
+                                        _p(w2), _p(s2), _p(bits) if bits is not None else None, tokens.shape[0],
+                                        _p(tokens), _p(out)):
         raise ValueError("orc_forward_tokens: invalid arguments")
     return out
 
@@ -185,4 +199,4 @@ def forward_workload(w, tokens_data, bank, tokens=None) -> np.ndarray:
     """forward_tokens for a synth Workload with its Tokens and Bank."""
     d = dims(w.T, w.H, w.I, w.E, w.S, w.top_k, w.group)
     return forward_tokens(d, tokens_data.x_q, tokens_data.x_scale, tokens_data.logits,
-                          bank.w13, bank.s13, bank.w2, bank.s2, tokens)
+                          bank.w13, bank.s13, bank.w2, bank.s2, tokens, getattr(bank, "slot_bits", None))

@@ -48,7 +48,23 @@ int orc_unpack(uint8_t byte, int high) {
     return v >= 8 ? v - 16 : v;
 }
 
-static int code_at(const uint8_t* row, int64_t k) { return orc_unpack(row[k >> 1], (int)(k & 1)); }
+/*
+ * Packed 2-bit storage (mixed 2/4-bit banks): element 4j + p sits in bits
+ * 2p, 2p+1 of byte j of the row, a two's-complement 2-bit number in [-2, 1]
+ * (the same low-bits-first order as the 4-bit packing).  A 2-bit row keeps
+ * the 4-bit row's length, K/2 bytes, of which the first K/4 hold the codes
+ * (reading: the storage of a slot does not depend on its width, so one bank
+ * array serves both; only the bytes read halve).
+ */
+int orc_unpack2(uint8_t byte, int pos) {
+    int v = (byte >> (2 * pos)) & 0x3;
+    return v >= 2 ? v - 4 : v;
+}
+
+/* Code k of a packed row of `bits` (4 or 2) bits per code. */
+static int code_at(const uint8_t* row, int64_t k, int bits) {
+    return bits == 2 ? orc_unpack2(row[k >> 2], (int)(k & 3)) : orc_unpack(row[k >> 1], (int)(k & 1));
+}
 
 /*
  * route: for each token choose k experts by repeated scans for the largest
@@ -116,16 +132,21 @@ int orc_permute(int64_t T, int64_t E, int64_t k, const int32_t* ids,
  * against `rows` packed weight rows of length K: P[n * (K/g) + q] =
  * sum over k in [q*g, (q+1)*g) of a[k] * code(W[n], k).  |P| <= g*127*8.
  */
-void orc_partials(const int8_t* a, int64_t K, const uint8_t* W, int64_t rows, int64_t g, int32_t* P) {
+void orc_partials_bits(const int8_t* a, int64_t K, const uint8_t* W, int64_t rows, int64_t g, int bits,
+                       int32_t* P) {
     int64_t ng = K / g;
     for (int64_t n = 0; n < rows; ++n) {
         const uint8_t* row = W + n * (K / 2);
         for (int64_t q = 0; q < ng; ++q) {
             int32_t acc = 0;
-            for (int64_t kk = q * g; kk < (q + 1) * g; ++kk) acc += (int32_t)a[kk] * code_at(row, kk);
+            for (int64_t kk = q * g; kk < (q + 1) * g; ++kk) acc += (int32_t)a[kk] * code_at(row, kk, bits);
             P[n * ng + q] = acc;
         }
     }
+}
+
+void orc_partials(const int8_t* a, int64_t K, const uint8_t* W, int64_t rows, int64_t g, int32_t* P) {
+    orc_partials_bits(a, K, W, rows, g, 4, P);
 }
 
 /* Dequantised row sums: out[n] = a_scale * sum_q s[n][q] * P[n][q] (fp64). */
@@ -146,16 +167,21 @@ double orc_silu(double z) { return z / (1.0 + exp(-z)); }
  * the plain concatenation gate-then-up).  P1 (optional) receives the int32
  * partials [2I][H/g].
  */
-void orc_hidden(const int8_t* x, float x_scale, const uint8_t* w13e, const float* s13e,
-                int64_t H, int64_t I, int64_t g, int32_t* P1, double* G, double* h) {
+static void hidden_bits(const int8_t* x, float x_scale, const uint8_t* w13e, const float* s13e,
+                        int64_t H, int64_t I, int64_t g, int bits, int32_t* P1, double* G, double* h) {
     int64_t ng = H / g;
     int32_t* P = P1 ? P1 : (int32_t*)malloc((size_t)(2 * I * ng) * sizeof(int32_t));
     double* Gv = G ? G : (double*)malloc((size_t)(2 * I) * sizeof(double));
-    orc_partials(x, H, w13e, 2 * I, g, P);
+    orc_partials_bits(x, H, w13e, 2 * I, g, bits, P);
     combine_groups(P, s13e, 2 * I, ng, (double)x_scale, Gv);
     for (int64_t i = 0; i < I; ++i) h[i] = orc_silu(Gv[i]) * Gv[I + i];
     if (!P1) free(P);
     if (!G) free(Gv);
+}
+
+void orc_hidden(const int8_t* x, float x_scale, const uint8_t* w13e, const float* s13e,
+                int64_t H, int64_t I, int64_t g, int32_t* P1, double* G, double* h) {
+    hidden_bits(x, x_scale, w13e, s13e, H, I, g, 4, P1, G, h);
 }
 
 /*
@@ -216,31 +242,45 @@ void orc_quantize_bf16(const uint16_t* x, int64_t T, int64_t H, int8_t* x_q, flo
 }
 
 /* gemm2 for one pair: Y[n] = s_h * sum_q s2[n][q] * P2[n][q]; P2 optional [H][I/g]. */
-void orc_down(const int8_t* hq, float sh, const uint8_t* w2e, const float* s2e,
-              int64_t H, int64_t I, int64_t g, int32_t* P2, double* y) {
+static void down_bits(const int8_t* hq, float sh, const uint8_t* w2e, const float* s2e,
+                      int64_t H, int64_t I, int64_t g, int bits, int32_t* P2, double* y) {
     int64_t ng = I / g;
     int32_t* P = P2 ? P2 : (int32_t*)malloc((size_t)(H * ng) * sizeof(int32_t));
-    orc_partials(hq, I, w2e, H, g, P);
+    orc_partials_bits(hq, I, w2e, H, g, bits, P);
     combine_groups(P, s2e, H, ng, (double)sh, y);
     if (!P2) free(P);
 }
 
-/* Y of one (token, slot) pair; hq/sh (optional) receive the requantised intermediate. */
-void orc_pair_output(const orc_dims_t* d, const int8_t* x_q, const float* x_scale,
-                     const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
-                     int64_t t, int64_t slot, int8_t* hq_out, float* sh_out, double* y) {
+void orc_down(const int8_t* hq, float sh, const uint8_t* w2e, const float* s2e,
+              int64_t H, int64_t I, int64_t g, int32_t* P2, double* y) {
+    down_bits(hq, sh, w2e, s2e, H, I, g, 4, P2, y);
+}
+
+/* Y of one (token, slot) pair; hq/sh (optional) receive the requantised intermediate;
+ * slot_bits (optional, [E+S], 2 or 4) gives each slot's code width (default 4). */
+static void pair_output_bits(const orc_dims_t* d, const int8_t* x_q, const float* x_scale,
+                             const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
+                             const uint8_t* slot_bits, int64_t t, int64_t slot, int8_t* hq_out, float* sh_out,
+                             double* y) {
     int64_t H = d->H, I = d->I, g = d->group;
+    int bits = slot_bits ? slot_bits[slot] : 4;
     double* h = (double*)malloc((size_t)I * sizeof(double));
     int8_t* hq = (int8_t*)malloc((size_t)I);
     float sh;
-    orc_hidden(x_q + t * H, x_scale[t], w13 + slot * (2 * I) * (H / 2), s13 + slot * (2 * I) * (H / g),
-               H, I, g, NULL, NULL, h);
+    hidden_bits(x_q + t * H, x_scale[t], w13 + slot * (2 * I) * (H / 2), s13 + slot * (2 * I) * (H / g),
+                H, I, g, bits, NULL, NULL, h);
     orc_requant(h, I, hq, &sh);
-    orc_down(hq, sh, w2 + slot * H * (I / 2), s2 + slot * H * (I / g), H, I, g, NULL, y);
+    down_bits(hq, sh, w2 + slot * H * (I / 2), s2 + slot * H * (I / g), H, I, g, bits, NULL, y);
     if (hq_out) memcpy(hq_out, hq, (size_t)I);
     if (sh_out) *sh_out = sh;
     free(h);
     free(hq);
+}
+
+void orc_pair_output(const orc_dims_t* d, const int8_t* x_q, const float* x_scale,
+                     const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
+                     int64_t t, int64_t slot, int8_t* hq_out, float* sh_out, double* y) {
+    pair_output_bits(d, x_q, x_scale, w13, s13, w2, s2, NULL, t, slot, hq_out, sh_out, y);
 }
 
 /*
@@ -250,9 +290,9 @@ void orc_pair_output(const orc_dims_t* d, const int8_t* x_q, const float* x_scal
  * + sum_s Y(t, E + s), summed in that fixed order in fp64.  Each token only
  * needs its own routing, so a sample of tokens costs only its own pairs.
  */
-int orc_forward_tokens(const orc_dims_t* d, const int8_t* x_q, const float* x_scale, const float* logits,
-                       const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
-                       int64_t n_sel, const int64_t* tokens, double* out) {
+int orc_forward_tokens_mixed(const orc_dims_t* d, const int8_t* x_q, const float* x_scale, const float* logits,
+                             const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
+                             const uint8_t* slot_bits, int64_t n_sel, const int64_t* tokens, double* out) {
     int64_t H = d->H, E = d->E, k = d->top_k;
     if (d->T < 0 || d->H < 1 || d->I < 1 || E < 1 || k < 1 || k > E || d->n_shared < 0 || d->group < 1 ||
         d->H % d->group || d->I % d->group || d->group % 2)
@@ -270,11 +310,11 @@ int orc_forward_tokens(const orc_dims_t* d, const int8_t* x_q, const float* x_sc
         if (orc_route(1, E, k, logits + t * E, ids, w)) bad = 1;
         for (int64_t n = 0; n < H; ++n) o[n] = 0.0;
         for (int64_t j = 0; j < k; ++j) {
-            orc_pair_output(d, x_q, x_scale, w13, s13, w2, s2, t, ids[j], NULL, NULL, y);
+            pair_output_bits(d, x_q, x_scale, w13, s13, w2, s2, slot_bits, t, ids[j], NULL, NULL, y);
             for (int64_t n = 0; n < H; ++n) o[n] += w[j] * y[n];
         }
         for (int64_t s = 0; s < d->n_shared; ++s) {
-            orc_pair_output(d, x_q, x_scale, w13, s13, w2, s2, t, E + s, NULL, NULL, y);
+            pair_output_bits(d, x_q, x_scale, w13, s13, w2, s2, slot_bits, t, E + s, NULL, NULL, y);
             for (int64_t n = 0; n < H; ++n) o[n] += y[n];
         }
         free(ids);
@@ -282,4 +322,10 @@ int orc_forward_tokens(const orc_dims_t* d, const int8_t* x_q, const float* x_sc
         free(y);
     }
     return bad;
+}
+
+int orc_forward_tokens(const orc_dims_t* d, const int8_t* x_q, const float* x_scale, const float* logits,
+                       const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
+                       int64_t n_sel, const int64_t* tokens, double* out) {
+    return orc_forward_tokens_mixed(d, x_q, x_scale, logits, w13, s13, w2, s2, NULL, n_sel, tokens, out);
 }

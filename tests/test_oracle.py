@@ -435,3 +435,64 @@ def test_s0_quantisation_invariants():
     # each code is the nearest integer to x / s (within fp32 rounding of the division)
     err = np.abs(x_q[live].astype(np.float64) - x[live].astype(np.float64) / s[live, None].astype(np.float64))
     assert np.all(err <= 0.5 + 1e-5)
+
+
+# ---------------------------------------------------------------- mixed 2/4-bit banks
+MIXED = synth.Workload("mixed_small", T=12, H=256, I=128, E=8, S=1, top_k=2, group=64, twobit_frac=0.5)
+
+
+def test_int2_unpack_golden_bytes():
+    n = 0
+    for line in open(os.path.join(GOLDEN, "int2_codes.txt")):
+        f = line.split("#")[0].split()
+        if not f:
+            continue
+        b = int(f[0], 16)
+        assert [oracle.unpack2(b, p) for p in range(4)] == [int(v) for v in f[1:]], f[0]
+        n += 1
+    assert n >= 12
+
+
+def _pack4_rows(codes):
+    """int4 packing written out from the format (element 2j low nibble, 2j+1 high nibble)."""
+    c = (codes.astype(np.int16) & 0xF).astype(np.uint8)
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
+def test_int2_partials_equal_int4_partials_and_brute_force():
+    rng = np.random.default_rng(21)
+    rows, K, g = 24, 512, 128
+    codes = rng.integers(-2, 2, size=(rows, K)).astype(np.int8)
+    codes[0, :] = -2
+    codes[1, :] = 1
+    a = rng.integers(-127, 128, size=K).astype(np.int8)
+    a[:64] = -127
+    p2 = oracle.partials(a, synth.pack2_rows(codes, K // 2), g, bits=2)
+    p4 = oracle.partials(a, _pack4_rows(codes), g, bits=4)
+    brute = np.einsum("nqk,qk->nq", codes.astype(np.int64).reshape(rows, K // g, g),
+                      a.astype(np.int64).reshape(K // g, g))
+    assert np.array_equal(p2, brute) and np.array_equal(p4, brute)
+
+
+def test_generator_true_2bit_bytes_unpack_to_its_codes():
+    bank, c13, c2 = synth.make_bank(MIXED, with_codes=True, pack2=True)
+    two = np.nonzero(bank.slot_bits == 2)[0]
+    assert len(two) >= 2 and np.all(bank.slot_bits[bank.slot_bits != 2] == 4)
+    assert np.array_equal(bank.slot_bits == 2, bank.twobit)
+    lut = np.array([[oracle.unpack2(b, p) for p in range(4)] for b in range(256)], np.int8)
+    for e in two:
+        got13 = lut[bank.w13[e][:, :MIXED.H // 4]].reshape(2 * MIXED.I, MIXED.H)
+        got2 = lut[bank.w2[e][:, :MIXED.I // 4]].reshape(MIXED.H, MIXED.I)
+        assert np.array_equal(got13, c13[e]) and np.array_equal(got2, c2[e])
+        assert not bank.w13[e][:, MIXED.H // 4:].any()  # the unused half of a 2-bit row
+
+
+def test_mixed_bank_layer_equals_the_same_codes_in_int4_storage():
+    tok = synth.make_tokens(MIXED)
+    b4 = synth.make_bank(MIXED)
+    b2 = synth.make_bank(MIXED, pack2=True)
+    assert np.array_equal(b4.s13, b2.s13) and not np.array_equal(b4.w13, b2.w13)
+    out4 = oracle.forward_workload(MIXED, tok, b4)
+    out2 = oracle.forward_workload(MIXED, tok, b2)
+    assert np.array_equal(out4, out2)
+    assert np.abs(out4).max() > 0
