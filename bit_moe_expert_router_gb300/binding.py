@@ -71,9 +71,11 @@ def _load():
     lib.moe_w4a8_forward_bf16_workspace_size.argtypes = [dp]
     lib.moe_w4a8_forward_bf16_workspace_size.restype = sz
     lib.moe_w4a8_forward_bf16.argtypes = [p, p, p, p, p, p, dp, p, p, sz, p]
+    lib.moe_w4a8_forward_w2w4.argtypes = [p, p, p, p, p, p, p, p, dp, p, p, sz, p]
     for name in ("moe_w4a8_forward", "moe_w4a8_forward_debug", "moe_w4a8_route", "moe_w4a8_gemm1_partials",
                  "moe_w4a8_gemm2_partials", "moe_w4a8_forward_noalloc", "moe_w4a8_device_status",
-                 "moe_w4a8_selftest_barrier_timeout", "moe_w4a8_forward_host", "moe_w4a8_forward_bf16"):
+                 "moe_w4a8_selftest_barrier_timeout", "moe_w4a8_forward_host", "moe_w4a8_forward_bf16",
+                 "moe_w4a8_forward_w2w4"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.moe_w4a8_version() != ABI_VERSION:
         raise RuntimeError(f"{LIB_PATH}: ABI version {lib.moe_w4a8_version()} != {ABI_VERSION}")
@@ -244,6 +246,22 @@ def moe_w4a8_forward_bf16(x_bf16, router_logits, w13_packed, w13_scale, w2_packe
     _check("moe_w4a8_forward_bf16", _load().moe_w4a8_forward_bf16(
         _ptr(x_bf16), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed), _ptr(w2_scale),
         ctypes.byref(d), _ptr(out), wp, wb, _stream(out.device)))
+    return out
+
+
+def moe_w4a8_forward_w2w4(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, slot_bits,
+                          d: Dims, out, workspace: torch.Tensor):
+    """The layer on a mixed 2/4-bit bank: slot_bits (uint8 CUDA tensor [E+S], 2 or 4) gives each slot's width.
+
+    2-bit slots hold four codes per byte in the first half of each row (see the header).  Decode-engine
+    sizes only.
+    """
+    _check_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out)
+    _need(slot_bits, "slot_bits", torch.uint8, (d.E + d.n_shared,))
+    wp, wb = _ws_view(workspace)
+    _check("moe_w4a8_forward_w2w4", _load().moe_w4a8_forward_w2w4(
+        _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
+        _ptr(w2_scale), _ptr(slot_bits), ctypes.byref(d), _ptr(out), wp, wb, _stream(out.device)))
     return out
 
 

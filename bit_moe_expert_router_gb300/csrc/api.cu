@@ -137,11 +137,13 @@ bool decode_forward_plan(const moe_dims_t* d, moe::DecodePlan* pl) {
 
 int run_decode(const int8_t* x_q, const float* x_scale, const float* logits, const uint8_t* w13, const float* s13,
                const uint8_t* w2, const float* s2, const moe_dims_t* d, float* out, const Views& v,
-               const moe::DecodePlan& pl, float* y_debug, cudaStream_t st, const uint16_t* x_bf16 = nullptr) {
+               const moe::DecodePlan& pl, float* y_debug, cudaStream_t st, const uint16_t* x_bf16 = nullptr,
+               const uint8_t* slot_bits = nullptr) {
     moe::DecodeArgs a{};
     a.x_q = x_q;
     a.x_scale = x_scale;
     a.x_bf16 = x_bf16;
+    a.slot_bits = slot_bits;
     a.logits = logits;
     a.w13 = w13;
     a.s13 = s13;
@@ -467,6 +469,23 @@ MOE_API int moe_w4a8_forward_bf16(const uint16_t* x_bf16, const float* router_lo
     float* x_scale = reinterpret_cast<float*>(ws + bf16_stage_xs(d, L));
     MOE_CUDA(moe::launch_quantize_bf16(x_bf16, d->T, d->H, x_q, x_scale, st));
     return run_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out, L, v, st);
+}
+
+MOE_API int moe_w4a8_forward_w2w4(const int8_t* x_q, const float* x_scale, const float* router_logits,
+                                  const uint8_t* w13_packed, const float* w13_scale, const uint8_t* w2_packed,
+                                  const float* w2_scale, const uint8_t* slot_bits, const moe_dims_t* d, float* out,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+    MOE_TRY(check_dims(d));
+    MOE_TRY(check_ptrs({w13_packed, w13_scale, w2_packed, w2_scale}));
+    if (!slot_bits) return MOE_ERR_INVALID_ARG;
+    if (d->T == 0) return MOE_OK;
+    MOE_TRY(check_ptrs({x_q, x_scale, router_logits, out}));
+    const WsLayout L = layout_of(d);
+    MOE_TRY(check_ws(L, workspace, workspace_bytes));
+    moe::DecodePlan pl;
+    if (!decode_forward_plan(d, &pl)) return MOE_ERR_UNSUPPORTED;  // mixed banks: the decode engine's sizes
+    return run_decode(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out,
+                      views(workspace, L), pl, nullptr, static_cast<cudaStream_t>(stream), nullptr, slot_bits);
 }
 
 MOE_API int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, const float* router_logits,

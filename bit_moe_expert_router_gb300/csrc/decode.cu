@@ -258,6 +258,37 @@ __device__ __forceinline__ int dot32(const uint4& w, const uint4& xa, const uint
     return dot8(w.w, xb.z, xb.w, acc);
 }
 
+// Sixteen packed 2-bit codes (element 4j + p in bits 2p, 2p+1 of byte j) ->
+// four int8 lane words holding 64 * code, in the split activation order:
+// e0 = elements 0,2,4,6; o0 = 1,3,5,7; e1 = 8,10,12,14; o1 = 9,11,13,15.
+// Each code is moved to bits 6-7 of its byte (byte_perm duplicates the
+// source byte into the two lanes it feeds).
+__device__ __forceinline__ void unpack_int2x16_x64(uint32_t w, uint32_t& e0, uint32_t& o0, uint32_t& e1, uint32_t& o1) {
+    const uint32_t t0 = __byte_perm(w, 0u, 0x1100), t1 = __byte_perm(w, 0u, 0x3322);
+    e0 = ((t0 << 6) & 0x00C000C0u) | ((t0 << 2) & 0xC000C000u);
+    o0 = ((t0 << 4) & 0x00C000C0u) | (t0 & 0xC000C000u);
+    e1 = ((t1 << 6) & 0x00C000C0u) | ((t1 << 2) & 0xC000C000u);
+    o1 = ((t1 << 4) & 0x00C000C0u) | (t1 & 0xC000C000u);
+}
+
+// 64 * dot of 64 packed 2-bit codes (uint4) with 64 split activation bytes (four uint4).
+__device__ __forceinline__ int dot64_2bit(const uint4& w, const uint4& xa, const uint4& xb, const uint4& xc,
+                                          const uint4& xd) {
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    const uint4 xv[4] = {xa, xb, xc, xd};
+    int acc = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t e0, o0, e1, o1;
+        unpack_int2x16_x64(wv[i], e0, o0, e1, o1);
+        acc = __dp4a(static_cast<int>(xv[i].x), static_cast<int>(e0), acc);
+        acc = __dp4a(static_cast<int>(xv[i].y), static_cast<int>(o0), acc);
+        acc = __dp4a(static_cast<int>(xv[i].z), static_cast<int>(e1), acc);
+        acc = __dp4a(static_cast<int>(xv[i].w), static_cast<int>(o1), acc);
+    }
+    return acc;
+}
+
 // Requantisation code of h with scale s and reciprocal rs: RNE(h / s) in
 // IEEE fp32.  h * rs is within 2^-23 relative of h / s (|h / s| <= 127),
 // so it rounds to the same integer unless it lies within 1e-4 of a
@@ -285,6 +316,7 @@ struct Smem {
     int* slot_e;      // [MS]
     int* slot_row0;   // [MS]
     int* slot_cnt;    // [MS]
+    int* slot_bw;     // [MS] code width of the slot (4, or 2 in a mixed bank)
     int* slot_cum;    // [MS + 1] phase-1 cost prefix
     int* n_slots;     // [1]
     float* xs;        // [T]
@@ -310,6 +342,7 @@ __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
     s.slot_e = reinterpret_cast<int*>(base + pl.off_slot_e);
     s.slot_row0 = reinterpret_cast<int*>(base + pl.off_slot_row0);
     s.slot_cnt = reinterpret_cast<int*>(base + pl.off_slot_cnt);
+    s.slot_bw = reinterpret_cast<int*>(base + pl.off_slot_bw);
     s.slot_cum = reinterpret_cast<int*>(base + pl.off_slot_cum);
     s.n_slots = reinterpret_cast<int*>(base + pl.off_n_slots);
     s.xs = reinterpret_cast<float*>(base + pl.off_xs);
@@ -327,10 +360,12 @@ __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
 }
 
 // Phase-1 cost of one unit of a slot with `cnt` tokens (streaming + per-token work).
-__device__ __forceinline__ int unit_cost(int cnt) { return 4 + cnt; }
+__device__ __forceinline__ int unit_cost(int cnt, int bits) { return (bits == 2 ? 2 : 4) + cnt; }
 
 // PC1 = H / 2048 (64-value pieces per lane per row), PC2 = I / 512 (16-value pieces per lane per row).
-template <DecodeMode MODE, int PC1, int PC2>
+// MIXED (forward only): the bank mixes 2-bit and 4-bit slots (a.slot_bits); the plain
+// instantiation carries none of the 2-bit code.
+template <DecodeMode MODE, int PC1, int PC2, bool MIXED = false>
 __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, DecodePlan pl) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const Smem s = carve(smem_raw, pl);
@@ -459,6 +494,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         s.slot_e[u] = e;
         s.slot_row0[u] = s.pos[i];
         s.slot_cnt[u] = s.eqc[i];
+        s.slot_bw[u] = (MIXED && a.slot_bits) ? (a.slot_bits[e] == 2 ? 2 : 4) : 4;
     }
     if (warp == 0) {
         int nr = 0;
@@ -468,6 +504,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
             s.slot_e[nr + sh] = a.E + sh;
             s.slot_row0[nr + sh] = n_rows + sh * T;
             s.slot_cnt[nr + sh] = T;
+            s.slot_bw[nr + sh] = (MIXED && a.slot_bits) ? (a.slot_bits[a.E + sh] == 2 ? 2 : 4) : 4;
         }
         if (lane == 0) s.n_slots[0] = nr + S;
     }
@@ -479,7 +516,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         int run = 0;
         for (int b0 = 0; b0 < n_slots; b0 += 32) {
             const int u = b0 + lane;
-            const int c = u < n_slots ? (I / 2) * unit_cost(s.slot_cnt[u]) : 0;
+            const int c = u < n_slots ? (I / 2) * unit_cost(s.slot_cnt[u], s.slot_bw[u]) : 0;
             int incl = c;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -503,9 +540,12 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     const int nrows = max(0, min(pl.rows_pc, H - n0));
     const int n_smem = MODE == DecodeMode::kForward && nrows > 0 ? min(n_slots, pl.smem_slots) : 0;
     const int slot_stride = pl.rows_pc * RS + pl.rows_pc * ng2 * 4;
-    const int lines_w = (nrows * (I / 2) + 127) / 128, lines_s = (nrows * ng2 * 4 + 127) / 128;
-    if (tid == 0 && n_smem > 0)  // every staged byte counted before any copy can land
-        mbar_expect_tx(s.w2bar, static_cast<uint32_t>(n_smem * nrows * (I / 2 + ng2 * 4)));
+    const int lines_s = (nrows * ng2 * 4 + 127) / 128;
+    if (tid == 0 && n_smem > 0) {  // every staged byte counted before any copy can land
+        uint32_t bytes = 0;  // a 2-bit slot's rows are copied at half length
+        for (int u = 0; u < n_smem; ++u) bytes += nrows * ((MIXED && s.slot_bw[u] == 2 ? I / 4 : I / 2) + ng2 * 4);
+        mbar_expect_tx(s.w2bar, bytes);
+    }
     __syncthreads();
     int next_slot = warp;  // next slot this warp stages (copies or warms)
     auto stage_some = [&](int budget) {
@@ -514,15 +554,17 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
             const int64_t e = s.slot_e[u];
             const uint8_t* wsrc = a.w2 + (e * H + n0) * static_cast<int64_t>(I / 2);
             const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(a.s2 + (e * H + n0) * ng2);
+            const int rb = MIXED && s.slot_bw[u] == 2 ? I / 4 : I / 2;  // bytes of a row that hold codes
             if (u < n_smem) {
                 uint8_t* base = s.w2s + u * slot_stride;
                 for (int r = lane; r <= nrows; r += 32) {  // lane r: row r; lane nrows: the scales
-                    if (r < nrows) bulk_g2s(base + r * RS, wsrc + r * (I / 2), I / 2, s.w2bar);
+                    if (r < nrows) bulk_g2s(base + r * RS, wsrc + r * (I / 2), rb, s.w2bar);
                     else bulk_g2s(base + pl.rows_pc * RS, ssrc, nrows * ng2 * 4, s.w2bar);
                 }
             } else {
+                const int lpr = rb / 128, lines_w = nrows * lpr;  // 128-byte lines of the code bytes of each row
                 for (int c = lane; c < lines_w + lines_s; c += 32)
-                    prefetch_l2(c < lines_w ? wsrc + 128 * c : ssrc + 128 * (c - lines_w));
+                    prefetch_l2(c < lines_w ? wsrc + (c / lpr) * (I / 2) + 128 * (c % lpr) : ssrc + 128 * (c - lines_w));
             }
         }
     };
@@ -543,7 +585,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                 if (s.slot_cum[mid] <= cpos) lo = mid;
                 else hi = mid;
             }
-            const int c = unit_cost(s.slot_cnt[lo]);
+            const int c = unit_cost(s.slot_cnt[lo], s.slot_bw[lo]);
             int64_t within = (cpos - s.slot_cum[lo] + c - 1) / c;
             if (within > upe) within = upe;
             return static_cast<int64_t>(lo) * upe + within;
@@ -561,18 +603,22 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         // a shift: with m = ceil(2^24 / g), floor(n m / 2^24) = floor(n / g) for n g < 2^24
         const uint32_t gmag = ((1u << 24) + static_cast<uint32_t>(g) - 1) / static_cast<uint32_t>(g);
         auto gq = [&](int p) { return static_cast<int>((static_cast<uint32_t>(32 * lane + 1024 * p) * gmag) >> 24); };
+        // a 2-bit row: lane l owns the 16-byte pieces l + 32 p (64 codes each, p < PC1)
+        auto gq2 = [&](int p) { return static_cast<int>((static_cast<uint32_t>(64 * lane + 2048 * p) * gmag) >> 24); };
         auto issue = [&](int un, int d) {
             const int64_t U = Ua + un;
             const int u = static_cast<int>(U / upe), ip = static_cast<int>(U % upe);
             const int64_t e = s.slot_e[u];
+            const bool two = MIXED && s.slot_bw[u] == 2;  // half the bytes per row
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int64_t row = e * 2 * I + (r >= 2 ? I : 0) + 2 * ip + (r & 1);
                 const uint8_t* wp = a.w13 + row * (H / 2);
 #pragma unroll
                 for (int p = 0; p < NP; ++p) {
+                    if (two && p >= PC1) break;
                     wr[d][r][p] = ld_stream16(wp + 16 * lane + 512 * p);
-                    if (MODE == DecodeMode::kForward) sr[d][r][p] = __ldg(a.s13 + row * ng1 + gq(p));
+                    if (MODE == DecodeMode::kForward) sr[d][r][p] = __ldg(a.s13 + row * ng1 + (two ? gq2(p) : gq(p)));
                 }
             }
         };
@@ -590,9 +636,36 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                 const int64_t U = Ua + un;
                 const int u = static_cast<int>(U / upe), ip = static_cast<int>(U % upe);
                 const int row0 = s.slot_row0[u], cnt = s.slot_cnt[u];
+                const bool two = MIXED && s.slot_bw[u] == 2;
                 for (int m = 0; m < cnt; ++m) {
                     const int prow = row0 + m;
                     const int t = s.row_tok[prow];
+                    float v[4];
+                    if (two) {  // 2-bit slot: 64 codes per piece, sums are 64 x the int32 partials
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) v[r] = 0.f;
+#pragma unroll
+                        for (int p = 0; p < PC1; ++p) {
+                            const uint4* xp = reinterpret_cast<const uint4*>(s.x + t * XS + 64 * lane + 2048 * p);
+                            int acc[4] = {0, 0, 0, 0};
+#pragma unroll 1
+                            for (int i = 0; i < 4; ++i) {  // word i: 16 codes against 16 activation bytes
+                                const uint4 xv = xp[i];
+#pragma unroll
+                                for (int r = 0; r < 4; ++r) {
+                                    const uint32_t wd = i == 0 ? w[r][p].x : i == 1 ? w[r][p].y : i == 2 ? w[r][p].z : w[r][p].w;
+                                    uint32_t e0, o0, e1, o1;
+                                    unpack_int2x16_x64(wd, e0, o0, e1, o1);
+                                    acc[r] = __dp4a(static_cast<int>(xv.x), static_cast<int>(e0), acc[r]);
+                                    acc[r] = __dp4a(static_cast<int>(xv.y), static_cast<int>(o0), acc[r]);
+                                    acc[r] = __dp4a(static_cast<int>(xv.z), static_cast<int>(e1), acc[r]);
+                                    acc[r] = __dp4a(static_cast<int>(xv.w), static_cast<int>(o1), acc[r]);
+                                }
+                            }
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) v[r] = fmaf(static_cast<float>(acc[r] >> 6), sc[r][p], v[r]);
+                        }
+                    } else {
                     int P[4][NP];
 #pragma unroll
                     for (int p = 0; p < NP; ++p) {
@@ -616,13 +689,13 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                             }
                         continue;
                     }
-                    float v[4];
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
                         v[r] = 0.f;
 #pragma unroll
                         for (int p = 0; p < NP; ++p) v[r] = fmaf(static_cast<float>(P[r][p] >> 4), sc[r][p], v[r]);
                     }
+                    }  // 4-bit slot
                     // reduce-scatter of the 4 row sums: lane keeps row 2*bit4 + bit3
                     const bool b4 = lane & 16, b3 = lane & 8;
                     float k0 = b4 ? v[2] : v[0], k1 = b4 ? v[3] : v[1];
@@ -756,15 +829,25 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
             const float* srow = in_smem ? reinterpret_cast<const float*>(s.w2s + u * slot_stride + pl.rows_pc * RS) + r * ng2
                                         : a.s2 + (e * H + n0 + r) * ng2;
             const uint8_t* xrow = s.hq + p * HQS;
+            const bool two = MIXED && s.slot_bw[u] == 2;
             float acc = 0.f;
             for (int q = 0; q < ng2; ++q) {
                 int Pq = 0;
-                for (int c = 0; c < g / 32; ++c) {  // 32 codes (16 packed bytes) per step
-                    const int kb = q * (g / 2) + 16 * c;
-                    const uint4 wv = in_smem ? *reinterpret_cast<const uint4*>(wrow + kb) : ld_stream16(wrow + kb);
-                    const uint4 xa = *reinterpret_cast<const uint4*>(xrow + 2 * kb);
-                    const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 2 * kb + 16);
-                    Pq += dot32(wv, xa, xb);
+                if (two) {
+                    for (int c = 0; c < g / 64; ++c) {  // 64 codes (16 packed bytes) per step
+                        const int kb = q * (g / 4) + 16 * c;
+                        const uint4 wv = in_smem ? *reinterpret_cast<const uint4*>(wrow + kb) : ld_stream16(wrow + kb);
+                        const uint4* xp = reinterpret_cast<const uint4*>(xrow + 4 * kb);
+                        Pq += dot64_2bit(wv, xp[0], xp[1], xp[2], xp[3]) >> 2;  // 16 x the partial, as below
+                    }
+                } else {
+                    for (int c = 0; c < g / 32; ++c) {  // 32 codes (16 packed bytes) per step
+                        const int kb = q * (g / 2) + 16 * c;
+                        const uint4 wv = in_smem ? *reinterpret_cast<const uint4*>(wrow + kb) : ld_stream16(wrow + kb);
+                        const uint4 xa = *reinterpret_cast<const uint4*>(xrow + 2 * kb);
+                        const uint4 xb = *reinterpret_cast<const uint4*>(xrow + 2 * kb + 16);
+                        Pq += dot32(wv, xa, xb);
+                    }
                 }
                 if (MODE == DecodeMode::kGemm2Partials) {
                     a.p2[(static_cast<int64_t>(p) * H + n0 + r) * ng2 + q] = Pq >> 4;
@@ -802,9 +885,9 @@ __global__ void barrier_timeout_probe_kernel(Header* hdr) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-template <DecodeMode MODE, int PC1, int PC2>
+template <DecodeMode MODE, int PC1, int PC2, bool MIXED = false>
 cudaError_t launch_mode(const DecodeArgs& a, const DecodePlan& pl, int grid, cudaStream_t st) {
-    auto kern = decode_kernel<MODE, PC1, PC2>;
+    auto kern = decode_kernel<MODE, PC1, PC2, MIXED>;
     // The dynamic shared memory limit is one value per kernel: set it once per
     // device to the largest size any plan may ask for.
     static std::mutex mu;
@@ -835,7 +918,9 @@ cudaError_t launch_mode(const DecodeArgs& a, const DecodePlan& pl, int grid, cud
 
 template <int PC1, int PC2>
 cudaError_t launch_shape(DecodeMode mode, const DecodeArgs& a, const DecodePlan& pl, int grid, cudaStream_t st) {
-    if (mode == DecodeMode::kForward) return launch_mode<DecodeMode::kForward, PC1, PC2>(a, pl, grid, st);
+    if (mode == DecodeMode::kForward)
+        return a.slot_bits ? launch_mode<DecodeMode::kForward, PC1, PC2, true>(a, pl, grid, st)
+                           : launch_mode<DecodeMode::kForward, PC1, PC2, false>(a, pl, grid, st);
     if (mode == DecodeMode::kGemm1Partials) return launch_mode<DecodeMode::kGemm1Partials, PC1, PC2>(a, pl, grid, st);
     return launch_mode<DecodeMode::kGemm2Partials, PC1, PC2>(a, pl, grid, st);
 }
@@ -876,6 +961,7 @@ bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t 
     pl.off_slot_e = take(4 * MS, 16);
     pl.off_slot_row0 = take(4 * MS, 16);
     pl.off_slot_cnt = take(4 * MS, 16);
+    pl.off_slot_bw = take(4 * MS, 16);
     pl.off_slot_cum = take(4 * (MS + 1), 16);
     pl.off_n_slots = take(16, 16);
     pl.off_xs = take(4 * T, 16);

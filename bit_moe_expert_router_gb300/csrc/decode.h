@@ -16,6 +16,7 @@ struct DecodeArgs {
     const float* x_scale;
     const uint16_t* x_bf16;  // forward: bf16 activations [T][H] quantised in the kernel (x_q / x_scale unused), or null
     const float* logits;
+    const uint8_t* slot_bits;  // forward: code width of each bank slot [E+S] (2 or 4), or null (all 4)
     const uint8_t* w13;
     const float* s13;
     const uint8_t* w2;
@@ -45,7 +46,7 @@ struct DecodePlan {
     int rows_pc;      // down-projection output rows per CTA
     int smem_slots;   // slots whose down-projection slice is staged in shared memory
     int smem_bytes;
-    int off_ids, off_wts, off_pos, off_pair_of, off_row_tok, off_slot_e, off_slot_row0, off_slot_cnt, off_slot_cum,
+    int off_ids, off_wts, off_pos, off_pair_of, off_row_tok, off_slot_e, off_slot_row0, off_slot_cnt, off_slot_bw, off_slot_cum,
         off_n_slots, off_xs, off_sh, off_x, off_hq, off_y, off_first, off_eqc, off_wmax, off_w2bar, off_row_slot, off_w2s;
 };
 

@@ -315,6 +315,31 @@ int moe_w4a8_forward_bf16(const uint16_t* x_bf16, const float* router_logits,
                           const moe_dims_t* d, float* out,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * The layer on a mixed 2/4-bit bank (the page's mixed W2/W4 expert
+ * checkpoint, section "GLM is my next, harder model", and the grouped mixed
+ * W2/W4 expert path of "Known issues and work in progress"): slot_bits, a
+ * device array of E+S bytes,
+ * gives each bank slot's code width, 4 or 2.  A 4-bit slot is stored as in
+ * moe_w4a8_forward.  A 2-bit slot keeps the same row length (K/2 bytes per
+ * row of K codes, both projections) but holds its codes in the first K/4
+ * bytes, four per byte: element 4j + p in bits 2p and 2p+1 of byte j, a
+ * two's-complement number in [-2, 1]; the rest of the row is never read.
+ * Scales are unchanged (one per row and group).  A 2-bit slot's code bytes
+ * -- what a decode step streams -- are half those of a 4-bit slot.
+ * Supported for the sizes the decode engine takes (T <= 32, T*k <= 512,
+ * H in {2048, 4096}, I in {512, 1536}, g a multiple of 64 with I/g a
+ * multiple of 4); otherwise MOE_ERR_UNSUPPORTED.  A null slot_bits is
+ * MOE_ERR_INVALID_ARG.  Other arguments, workspace (moe_w4a8_workspace_size)
+ * and errors as for moe_w4a8_forward; with every slot 4-bit the result
+ * equals moe_w4a8_forward's bit for bit.
+ */
+int moe_w4a8_forward_w2w4(const int8_t* x_q, const float* x_scale, const float* router_logits,
+                          const uint8_t* w13_packed, const float* w13_scale,
+                          const uint8_t* w2_packed, const float* w2_scale, const uint8_t* slot_bits,
+                          const moe_dims_t* d, float* out,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,7 @@ def test_header_declares_the_entry_points():
     assert {"moe_w4a8_forward", "moe_w4a8_route", "moe_w4a8_workspace_size", "moe_w4a8_version",
             "moe_w4a8_status_string", "moe_w4a8_gemm1_partials", "moe_w4a8_gemm2_partials",
             "moe_w4a8_forward_debug", "moe_w4a8_device_status", "moe_w4a8_forward_host",
-            "moe_w4a8_forward_host_workspace_size", "moe_w4a8_forward_bf16",
+            "moe_w4a8_forward_host_workspace_size", "moe_w4a8_forward_bf16", "moe_w4a8_forward_w2w4",
             "moe_w4a8_forward_bf16_workspace_size"} <= names
 
 
@@ -177,3 +177,17 @@ def test_bf16_entry_checks_its_arguments(lib):
     assert lib.moe_w4a8_forward_bf16(fake, fake, *w, ctypes.byref(d), fake, fake, need, None) == 3
     d0 = binding.dims_of(0, 2048, 512, 512, 1, 10, 128)
     assert lib.moe_w4a8_forward_bf16(None, None, *w, ctypes.byref(d0), None, None, 0, None) == 0
+
+
+def test_mixed_bank_entry_checks_its_arguments(lib):
+    from bit_moe_expert_router_gb300 import binding
+    d = binding.dims_of(4, 2048, 512, 512, 1, 10, 128)
+    need = lib.moe_w4a8_workspace_size(ctypes.byref(d))
+    fake = ctypes.c_void_p(0x100000)       # never dereferenced: the checks fail first
+    args = [fake] * 7
+    assert lib.moe_w4a8_forward_w2w4(*args, None, ctypes.byref(d), fake, fake, need, None) == 1
+    assert lib.moe_w4a8_forward_w2w4(*args, fake, ctypes.byref(d), fake, fake, need - 256, None) == 3
+    # sizes the decode engine does not take are refused before anything is enqueued
+    big = binding.dims_of(4096, 2048, 512, 512, 1, 10, 128)
+    need_big = lib.moe_w4a8_workspace_size(ctypes.byref(big))
+    assert lib.moe_w4a8_forward_w2w4(*args, fake, ctypes.byref(big), fake, fake, need_big, None) == 2
