@@ -130,9 +130,9 @@ moe::SortArgs sort_args(const Views& v, const int32_t* ids, int64_t T, int64_t k
 }
 
 // The fused decode engine's plan for a forward call, if the sizes fit it.
-bool decode_forward_plan(const moe_dims_t* d, moe::DecodePlan* pl) {
+bool decode_forward_plan(const moe_dims_t* d, moe::DecodePlan* pl, bool mixed = false) {
     return moe::decode_plan(d->T, d->H, d->I, d->E, d->n_shared, d->top_k, d->group, 0, moe::DecodeMode::kForward,
-                            moe::decode_grid(), moe::decode_max_smem(), pl);
+                            moe::decode_grid(), moe::decode_max_smem(), pl, mixed);
 }
 
 int run_decode(const int8_t* x_q, const float* x_scale, const float* logits, const uint8_t* w13, const float* s13,
@@ -483,7 +483,7 @@ MOE_API int moe_w4a8_forward_w2w4(const int8_t* x_q, const float* x_scale, const
     const WsLayout L = layout_of(d);
     MOE_TRY(check_ws(L, workspace, workspace_bytes));
     moe::DecodePlan pl;
-    if (!decode_forward_plan(d, &pl)) return MOE_ERR_UNSUPPORTED;  // mixed banks: the decode engine's sizes
+    if (!decode_forward_plan(d, &pl, true)) return MOE_ERR_UNSUPPORTED;  // mixed banks: the decode engine's sizes
     return run_decode(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out,
                       views(workspace, L), pl, nullptr, static_cast<cudaStream_t>(stream), nullptr, slot_bits);
 }

@@ -242,6 +242,17 @@ __device__ __forceinline__ uint4 split16(uint4 v) {
     return r;
 }
 
+// 16 int8 -> the same 16 bytes in mod-4 order: word p holds elements p, p + 4,
+// p + 8, p + 12 (the lanes a 2-bit word unpacks into with one shift and mask).
+__device__ __forceinline__ uint4 mod4_16(uint4 v) {
+    uint4 r;
+    r.x = __byte_perm(__byte_perm(v.x, v.y, 0x0040), __byte_perm(v.z, v.w, 0x0040), 0x5410);
+    r.y = __byte_perm(__byte_perm(v.x, v.y, 0x0051), __byte_perm(v.z, v.w, 0x0051), 0x5410);
+    r.z = __byte_perm(__byte_perm(v.x, v.y, 0x0062), __byte_perm(v.z, v.w, 0x0062), 0x5410);
+    r.w = __byte_perm(__byte_perm(v.x, v.y, 0x0073), __byte_perm(v.z, v.w, 0x0073), 0x5410);
+    return r;
+}
+
 // 16 * (dot of 8 packed codes `w` with the 8 split activation bytes xe|xo) + acc.
 __device__ __forceinline__ int dot8(uint32_t w, uint32_t xe, uint32_t xo, int acc) {
     uint32_t e, o;
@@ -322,6 +333,7 @@ struct Smem {
     float* xs;        // [T]
     float* sh;        // [P]
     uint8_t* x;       // [T][H + 16] split layout
+    uint8_t* xm;      // [T][H + 16] mod-4 layout (mixed banks only)
     uint8_t* hq;      // [P][I + 16] split layout
     float* y;         // [P][rows_pc]
     int* first;       // [rows] pair is the first of its expert (by pair index)
@@ -348,6 +360,7 @@ __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
     s.xs = reinterpret_cast<float*>(base + pl.off_xs);
     s.sh = reinterpret_cast<float*>(base + pl.off_sh);
     s.x = base + pl.off_x;
+    s.xm = base + pl.off_xm;
     s.hq = base + pl.off_hq;
     s.y = reinterpret_cast<float*>(base + pl.off_y);
     s.first = reinterpret_cast<int*>(base + pl.off_first);
@@ -402,7 +415,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         n_rows = a.n_pairs;  // listed pairs; out-of-range slots and tokens are clamped (never read out of bounds)
         for (int r = tid; r < n_rows; r += kThreadsD) s.ids[r] = min(max(a.pair_slot[r], 0), a.E - 1);
     }
-    if (MODE == DecodeMode::kForward && a.x_bf16) {
+    if (MODE == DecodeMode::kForward && !MIXED && a.x_bf16) {
         // S0 on the device: the warps that do not route quantise the bf16
         // activations (s = max|x| / 127, q = RNE(x / s) decided in fp32, clamped
         // to +-127; zero row: s = 0, q = 0) into the split staging layout.  wpt
@@ -453,6 +466,7 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                 const int t = o / per_tok, c = o % per_tok;
                 const uint4 v = *reinterpret_cast<const uint4*>(a.x_q + static_cast<int64_t>(t) * H + 16 * c);
                 *reinterpret_cast<uint4*>(s.x + t * XS + 16 * c) = split16(v);
+                if (MIXED) *reinterpret_cast<uint4*>(s.xm + t * XS + 16 * c) = mod4_16(v);
             }
             for (int t = tid - st0; t < T; t += nst) s.xs[t] = routed ? a.x_scale[t] : 1.0f;
         }
@@ -646,20 +660,19 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
                         for (int r = 0; r < 4; ++r) v[r] = 0.f;
 #pragma unroll
                         for (int p = 0; p < PC1; ++p) {
-                            const uint4* xp = reinterpret_cast<const uint4*>(s.x + t * XS + 64 * lane + 2048 * p);
+                            // activations in mod-4 order: lane word q of a 2-bit word is one shift and one mask
+                            const uint4* xp = reinterpret_cast<const uint4*>(s.xm + t * XS + 64 * lane + 2048 * p);
                             int acc[4] = {0, 0, 0, 0};
-#pragma unroll 1
+#pragma unroll
                             for (int i = 0; i < 4; ++i) {  // word i: 16 codes against 16 activation bytes
                                 const uint4 xv = xp[i];
 #pragma unroll
                                 for (int r = 0; r < 4; ++r) {
                                     const uint32_t wd = i == 0 ? w[r][p].x : i == 1 ? w[r][p].y : i == 2 ? w[r][p].z : w[r][p].w;
-                                    uint32_t e0, o0, e1, o1;
-                                    unpack_int2x16_x64(wd, e0, o0, e1, o1);
-                                    acc[r] = __dp4a(static_cast<int>(xv.x), static_cast<int>(e0), acc[r]);
-                                    acc[r] = __dp4a(static_cast<int>(xv.y), static_cast<int>(o0), acc[r]);
-                                    acc[r] = __dp4a(static_cast<int>(xv.z), static_cast<int>(e1), acc[r]);
-                                    acc[r] = __dp4a(static_cast<int>(xv.w), static_cast<int>(o1), acc[r]);
+                                    acc[r] = __dp4a(static_cast<int>(xv.x), static_cast<int>((wd << 6) & 0xC0C0C0C0u), acc[r]);
+                                    acc[r] = __dp4a(static_cast<int>(xv.y), static_cast<int>((wd << 4) & 0xC0C0C0C0u), acc[r]);
+                                    acc[r] = __dp4a(static_cast<int>(xv.z), static_cast<int>((wd << 2) & 0xC0C0C0C0u), acc[r]);
+                                    acc[r] = __dp4a(static_cast<int>(xv.w), static_cast<int>(wd & 0xC0C0C0C0u), acc[r]);
                                 }
                             }
 #pragma unroll
@@ -936,7 +949,7 @@ bool decode_shape_supported(int64_t H, int64_t I) {
 
 // Shared-memory plan of one launch (host side; the kernel reads the offsets).
 bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t k, int64_t g, int64_t n_pairs,
-                 DecodeMode mode, int grid, int max_smem, DecodePlan* out) {
+                 DecodeMode mode, int grid, int max_smem, DecodePlan* out, bool mixed) {
     if (!decode_shape_supported(H, I) || g % 64 != 0 || g > 512 || (I / g) % 4 != 0 || E > kMaxExperts) return false;
     const int64_t rows = mode == DecodeMode::kForward ? T * k : n_pairs;
     const int64_t Sx = mode == DecodeMode::kForward ? S : 0;
@@ -967,6 +980,7 @@ bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t 
     pl.off_xs = take(4 * T, 16);
     pl.off_sh = take(4 * P, 16);
     pl.off_x = take(mode == DecodeMode::kGemm2Partials ? 0 : T * (H + 16), 128);
+    pl.off_xm = take(mode == DecodeMode::kForward && mixed ? T * (H + 16) : 0, 128);
     pl.off_hq = take(mode == DecodeMode::kGemm1Partials ? 0 : P * (I + 16), 128);
     pl.off_y = take(mode == DecodeMode::kForward ? 4 * P * pl.rows_pc : 0, 16);
     pl.off_first = take(4 * rows, 16);

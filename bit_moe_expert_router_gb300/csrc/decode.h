@@ -47,11 +47,12 @@ struct DecodePlan {
     int smem_slots;   // slots whose down-projection slice is staged in shared memory
     int smem_bytes;
     int off_ids, off_wts, off_pos, off_pair_of, off_row_tok, off_slot_e, off_slot_row0, off_slot_cnt, off_slot_bw, off_slot_cum,
-        off_n_slots, off_xs, off_sh, off_x, off_hq, off_y, off_first, off_eqc, off_wmax, off_w2bar, off_row_slot, off_w2s;
+        off_n_slots, off_xs, off_sh, off_x, off_xm, off_hq, off_y, off_first, off_eqc, off_wmax, off_w2bar, off_row_slot, off_w2s;
 };
 
+// mixed: the forward kernel for mixed 2/4-bit banks (a second activation staging area).
 bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t k, int64_t g, int64_t n_pairs,
-                 DecodeMode mode, int grid, int max_smem, DecodePlan* out);
+                 DecodeMode mode, int grid, int max_smem, DecodePlan* out, bool mixed = false);
 bool decode_shape_supported(int64_t H, int64_t I);
 int decode_grid();
 int decode_max_smem();
