@@ -9,10 +9,10 @@
 // 128-value K group sums to |P| <= 128 * 127 * 8 < 2^24, so every group's
 // accumulator holds the exact int32 partial.  One group is accumulated per
 // TMEM buffer and folded into fp32 registers with its weight scale by the
-// epilogue warps while the tensor core fills the other buffer.
+// epilogue warps while the tensor core fills the next buffer.
 //
 // Tile: M = 128 weight rows x N <= 128 tokens of one bank slot, one K
-// group (128 values) per pipeline stage, 4 stages.  The A operand (the
+// group (128 values) per pipeline stage, 2 stages.  The A operand (the
 // unpacked weights, fp16) goes to tensor memory -- each producer thread
 // writes its row's 64 columns into its own lane with tcgen05.st -- and the
 // B operand (token rows, fp16) to shared memory in the 128-byte-swizzled
@@ -23,8 +23,11 @@
 // lanes.  The MMA width N is the token count of the tile rounded up to 16.
 // Persistent CTAs (one per SM) walk the (slot, token tile, weight tile)
 // items with the weight tile fastest, so the CTAs working at one time share
-// the token tile in L2.  Tensor memory: 2 accumulators x 128 columns + 4 A
-// stages x 64 columns = all 512 columns.
+// the token tile in L2.  Tensor memory: 3 accumulators x 128 columns + 2 A
+// stages x 64 columns = all 512 columns.  Three accumulators let the MMAs run
+// two groups into the next item while the epilogue finishes an item (SiLU or
+// scaling and the stores); that buys more than deeper A/B staging, since the
+// producers keep ahead of the MMAs with two stages.
 //
 // Thirteen warps (four of them share one SM sub-partition, whose 16K-register
 // file then caps a thread at 128 registers).  Warp roles: warps 0-7
@@ -58,19 +61,20 @@ constexpr int kMmaWarp = kEpiWarps + kProdWarps;
 constexpr int kTcThreads = 32 * (kMmaWarp + 1);
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kHalfN = 64;                   // columns per epilogue warp
-constexpr int kNS = 4;                       // pipeline stages: A in tensor memory, B in shared memory
+constexpr int kNS = 2;                       // pipeline stages: A in tensor memory, B in shared memory
 constexpr int kTileN = 128;
 constexpr int kAtom = 16384;                 // 128 rows x 128 bytes
 constexpr int kStage = 2 * kAtom;             // B: 128 token rows x 128 fp16 (two swizzled atoms)
 constexpr int kACols = 64;                   // A: 128 rows x 128 fp16 = 64 tensor-memory columns per stage
 constexpr int kMaxSlotsTc = kTcMaxSlots + 1;
-constexpr int kAcc = 2;                      // accumulator buffers in tensor memory (128 columns each)
+constexpr int kAcc = 3;                      // accumulator buffers in tensor memory (128 columns each)
 constexpr int kTmemCols = 512;               // kAcc * 128 accumulator columns + kNS * kACols A columns
 constexpr int kRaw = 3;                      // packed weight rows in flight ahead of the unpack
 constexpr int kRawStage = 128 * 64;          // 128 rows x 64 packed bytes (128 codes)
 constexpr int kSmemTc =
     kNS * kStage + kRaw * kRawStage + 128 * 4 + 128 * 4 + 2 * 128 * 4 + (kMaxSlotsTc + 16) * 4 + 256 + 1024;
 constexpr uint64_t kWaitNs = 2000000000ull;
+static_assert(kAcc * 128 + kNS * kACols <= kTmemCols, "tensor-memory columns");
 
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
