@@ -152,10 +152,23 @@ __global__ void __launch_bounds__(1024) scan_kernel(SortArgs a, int64_t n_chunks
     __shared__ int tiles[kMaxExperts + kMaxShared + 1];
     __shared__ int warp_sums[33];
     const int E = static_cast<int>(a.E), slots = static_cast<int>(a.E + a.S);
+    // per expert: exclusive prefix over the chunks, eight chunks' counts loaded at a time
+    // (independent loads in flight instead of a load-store chain)
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = 0;
-        for (int64_t c = 0; c < n_chunks; ++c) {
-            int v = a.chunk_counts[c * E + e];
+        int64_t c = 0;
+        for (; c + 8 <= n_chunks; c += 8) {
+            int v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = a.chunk_counts[(c + j) * E + e];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                a.chunk_counts[(c + j) * E + e] = run;
+                run += v[j];
+            }
+        }
+        for (; c < n_chunks; ++c) {
+            const int v = a.chunk_counts[c * E + e];
             a.chunk_counts[c * E + e] = run;
             run += v;
         }
@@ -176,8 +189,18 @@ __global__ void __launch_bounds__(1024) scan_kernel(SortArgs a, int64_t n_chunks
         a.seg_off[s] = off;
         if (a.offsets_out && s <= E) a.offsets_out[s] = off;
     }
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        for (int64_t c = 0; c < n_chunks; ++c) a.chunk_counts[c * E + e] += tot[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int base = tot[e];
+        int64_t c = 0;
+        for (; c + 8 <= n_chunks; c += 8) {
+            int v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = a.chunk_counts[(c + j) * E + e];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a.chunk_counts[(c + j) * E + e] = v[j] + base;
+        }
+        for (; c < n_chunks; ++c) a.chunk_counts[c * E + e] += base;
+    }
     for (int s = threadIdx.x; s < slots; s += blockDim.x) {
         int cnt = a.seg_cnt[s];
         int nt = (cnt + kTileM - 1) / kTileM;
@@ -199,9 +222,11 @@ __global__ void __launch_bounds__(32) scatter_kernel(SortArgs a, int64_t n) {
     for (int e = lane; e < a.E; e += 32) cursor[e] = a.chunk_counts[c * a.E + e];
     __syncwarp();
     const int64_t i0 = c * kChunk, i_end = min(n, i0 + kChunk);
+    int id_next = i0 + lane < i_end ? a.ids[i0 + lane] : -1;  // the next batch's ids are loaded one batch ahead
     for (int64_t base = i0; base < i_end; base += 32) {
         const int64_t i = base + lane;
-        const int id = i < i_end ? a.ids[i] : -1;
+        const int id = id_next;
+        id_next = base + 32 + lane < i_end ? a.ids[base + 32 + lane] : -1;
         const bool valid = static_cast<unsigned>(id) < static_cast<unsigned>(a.E);
         const int e = valid ? id : -1 - lane;  // absent or out-of-range lanes match nobody
         const uint32_t same = __match_any_sync(0xffffffffu, e);
