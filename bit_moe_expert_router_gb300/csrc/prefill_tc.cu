@@ -618,15 +618,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
     }
 }
 
-// x_q int8 -> fp16 in the engine's K order (pairs (0,4)(1,5)(2,6)(3,7) per 8 values).
 // x_q int8 -> fp16 rows in the engine's K order (pairs (0,4)(1,5)(2,6)(3,7) per
 // 8 values); out row r is token row_token[r] (null: r), zeros for a token
-// outside [0, T).
+// outside [0, T).  Idx: the type of the element index 8 i (32-bit when
+// rows * H fits, which keeps the row/column split a 32-bit division).
+template <typename Idx>
 __global__ void prep_x16_kernel(const int8_t* __restrict__ x, int64_t T, int64_t H, const int32_t* __restrict__ row_token,
                                 int64_t n8, __half* __restrict__ out) {
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = (8 * i) / H, c = (8 * i) % H;
+        const Idx i8 = static_cast<Idx>(8 * i), Hx = static_cast<Idx>(H);
+        const int64_t r = static_cast<int64_t>(i8 / Hx), c = static_cast<int64_t>(i8 % Hx);
         const int64_t t = row_token ? row_token[r] : r;
         uint2 v = make_uint2(0u, 0u);
         if (t >= 0 && t < T) v = *reinterpret_cast<const uint2*>(x + t * H + c);
@@ -761,7 +763,11 @@ cudaError_t launch_prep_x16(const int8_t* x_q, int64_t T, int64_t H, const int32
                             cudaStream_t st) {
     const int64_t n8 = rows * H / 8;
     const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, static_cast<int64_t>(num_sms()) * 8);
-    prep_x16_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(x_q, T, H, row_token, n8, x16);
+    const unsigned grid = static_cast<unsigned>(std::max<int64_t>(blocks, 1));
+    if (rows * H < (int64_t(1) << 32))
+        prep_x16_kernel<uint32_t><<<grid, 256, 0, st>>>(x_q, T, H, row_token, n8, x16);
+    else
+        prep_x16_kernel<uint64_t><<<grid, 256, 0, st>>>(x_q, T, H, row_token, n8, x16);
     return cudaGetLastError();
 }
 
