@@ -22,7 +22,6 @@ struct TcArgs {
     // B operand: fp16 rows (K order permuted inside 8-value groups), by pair row
     const __half* b;          // [rows][K]
     const int32_t* b_row;     // pair row -> row of b_scale (null: identity)
-    const int32_t* b_gather;  // pair row -> B row, gathered by cp.async (null: B row = pair row, TMA tiles)
     int64_t b_rows;           // rows of b; a B row outside [0, b_rows) reads zeros
     const float* b_scale;     // gate/up: per B row (x_scale); down: per pair row (s_h)
     // grouping of the pair rows by bank slot
@@ -31,7 +30,6 @@ struct TcArgs {
     int n_slots;
     // outputs
     float* h;                 // [P][I]        gate/up
-    uint32_t* amax;           // [P]           unused by the kernel (row maxima come from prep_h16)
     float* y;                 // [P][H]        down
     int32_t* partials;        // [P][rows_per_slot][K/g]  partials modes
     Header* hdr;              // status word for the bounded waits

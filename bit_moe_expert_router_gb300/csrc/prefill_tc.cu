@@ -33,9 +33,9 @@
 // file then caps a thread at 128 registers).  Warp roles: warps 0-7
 // epilogue (warp w: TMEM lanes 32 (w % 4) .. +31 = tile rows, columns
 // 64 (w / 4) .. +63), warps 8-11 producers (thread = tile row: unpack 64
-// packed bytes of its weight row into fp16 and store them to its TMEM lane,
-// and copy the stage's token rows: cp.async for gathered rows, TMA tiles
-// issued by warp 8 for contiguous ones), warp 12 issues the MMAs (one thread)
+// packed bytes of its weight row into fp16 and store them to its TMEM lane;
+// warp 8 also issues the stage's two TMA tiles of token rows), warp 12 issues
+// the MMAs (one thread)
 // and owns the TMEM allocation.  Every wait is bounded; a timeout sets the
 // status word and every role leaves cleanly.
 //
@@ -72,7 +72,7 @@ constexpr int kTmemCols = 512;               // kAcc * 128 accumulator columns +
 constexpr int kRaw = 3;                      // packed weight rows in flight ahead of the unpack
 constexpr int kRawStage = 128 * 64;          // 128 rows x 64 packed bytes (128 codes)
 constexpr int kSmemTc =
-    kNS * kStage + kRaw * kRawStage + 128 * 4 + 128 * 4 + 2 * 128 * 4 + (kMaxSlotsTc + 16) * 4 + 256 + 1024;
+    kNS * kStage + kRaw * kRawStage + 128 * 4 + 128 * 4 + (kMaxSlotsTc + 16) * 4 + 256 + 1024;
 constexpr uint64_t kWaitNs = 2000000000ull;
 static_assert(kAcc * 128 + kNS * kACols <= kTmemCols, "tensor-memory columns");
 
@@ -236,10 +236,6 @@ __device__ __forceinline__ uint4 unpack_int4_f16(uint32_t w) {
 }
 
 
-__device__ __forceinline__ uint32_t swz(int atom_row, int chunk) {  // byte offset in a 128 x 128 B atom
-    return static_cast<uint32_t>(atom_row * 128 + (((chunk & 7) ^ (atom_row & 7)) << 4));
-}
-
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n)); }
 
 // Named barrier that also ORs a predicate over its threads: every thread gets the same answer.
@@ -265,8 +261,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
     uint8_t* raw = smem + kNS * kStage;                           // [kRaw][128][64] packed weight rows
     float* colf = reinterpret_cast<float*>(raw + kRaw * kRawStage);  // [128] B-row scales of the item
     int* colp = reinterpret_cast<int*>(colf + 128);               // [128] pair rows of the item
-    int* brow_tab = colp + 128;                                   // [2][128] B rows of an item (-1: none)
-    int* prefix = brow_tab + 2 * 128;                             // [kMaxSlotsTc + 1] items before each slot
+    int* prefix = colp + 128;                                     // [kMaxSlotsTc + 1] items before each slot
     uint64_t* bars = reinterpret_cast<uint64_t*>(prefix + kMaxSlotsTc + 16);
     uint64_t* full = bars;
     uint64_t* empty = bars + kNS;
@@ -286,9 +281,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
 
     if (tid == 0) {
         for (int s = 0; s < kNS; ++s) {
-            // 128 producer arrivals + 128 cp.async completions (gathered B) or
-            // + the TMA tiles' expect-tx arrival (contiguous B)
-            mbar_init(full + s, a.b_gather ? 256 : 129);
+            // 128 producer arrivals (A in tensor memory) + the TMA tiles' expect-tx arrival (B)
+            mbar_init(full + s, 129);
             mbar_init(empty + s, 1);
         }
         for (int b = 0; b < kAcc; ++b) {
@@ -411,22 +405,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
         };
 #pragma unroll
         for (int d = 0; d < kRaw; ++d) fetch_next();
-        int use = 0, item_n = 0;
+        int use = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < total; item += gridDim.x) {
             const Item it = decode_item(item);
-            // B rows of this item, shared by the four producer warps: a warp's
-            // copy instruction covers two whole 256-byte row segments (16 lanes
-            // per row), not 32 scattered pieces.  Double-buffered by item parity;
-            // the barrier orders this item's writes after every producer thread
-            // finished the item two back, and makes a give-up unanimous.
-            {
-                const int64_t brow = pt < it.ntok ? (a.b_gather ? a.b_gather[it.row0 + pt] : it.row0 + pt) : -1;
-                brow_tab[(item_n & 1) * 128 + pt] = (brow >= 0 && brow < a.b_rows) ? static_cast<int>(brow) : -1;
-                if (named_bar_or(2, 128, !ok)) break;
-            }
-            const int* btab = brow_tab + (item_n & 1) * 128;
-            ++item_n;
+            if (named_bar_or(2, 128, !ok)) break;  // the four producer warps give up together
             for (int ks = 0; ks < ksteps; ++ks, ++use) {
                 const int s = use % kNS;
                 if (!wait_bar(empty + s, ((use / kNS) & 1) ^ 1, ctl)) {
@@ -435,24 +418,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                 }
                 tc_fence_after();  // the stage's previous MMAs (which read its A columns) are complete
                 uint8_t* Bs = stages + s * kStage;
-                // B, the 128 token rows of the stage.  Gathered rows (gate/up):
-                // cp.async by the four producer warps, a warp instruction covering
-                // two whole 256-byte row segments (16 lanes per row); contiguous
-                // rows (down): two 2-D TMA tiles (one per 128-byte-swizzled atom)
-                // issued by producer warp 0.
-                if (a.b_gather) {
-                    const int chunk = lane & 15;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int row = 32 * pw + 2 * i + (lane >> 4);
-                        const int br = btab[row];
-                        cp_async16(Bs + (chunk >> 3) * kAtom + swz(row, chunk),
-                                   a.b + static_cast<int64_t>(br >= 0 ? br : 0) * K + 128 * ks + 8 * chunk,
-                                   br >= 0 ? 16 : 0);
-                    }
-                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(full + s))
-                                 : "memory");
-                } else if (warp == kEpiWarps && lane == 0) {
+                // B, the 128 token rows of the stage (contiguous fp16 rows): two 2-D
+                // TMA tiles, one per 128-byte-swizzled atom, issued by producer warp 0
+                if (warp == kEpiWarps && lane == 0) {
                     mbar_expect_tx(full + s, kStage);
 #pragma unroll
                     for (int at = 0; at < 2; ++at) tma_tile2d(Bs + at * kAtom, &bmap, 128 * ks + 64 * at, it.row0, full + s);
@@ -732,11 +700,8 @@ cudaError_t launch_mode_tc(const TcArgs& a, int n_mt, cudaStream_t st) {
             attr_set[dev] = true;
         }
     }
-    alignas(64) CUtensorMap bmap{};  // used only for contiguous B rows
-    if (!a.b_gather) {
-        cudaError_t e = make_bmap(a, &bmap);
-        if (e != cudaSuccess) return e;
-    }
+    alignas(64) CUtensorMap bmap{};
+    if (cudaError_t e = make_bmap(a, &bmap); e != cudaSuccess) return e;
     kern<<<num_sms(), kTcThreads, kSmemTc, st>>>(a, n_mt, bmap);
     return cudaGetLastError();
 }
