@@ -66,6 +66,24 @@ def _dist_init(n):
     return rank, world
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time: every rank gets the same value (all-reduce MAX).
+
+    device: where the reduction tensor lives (a CUDA device for NCCL, None / CPU for gloo).
+    """
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms_total: float, steps: int) -> float:
+    """Units processed by all ranks per second, timed by the slowest rank (weak scaling: fixed units per rank)."""
+    return units_per_rank * world * steps / (ms_total * 1e-3)
+
+
 def _peaks():
     path = os.path.join(REPO, "MEASURED_PEAKS.json")
     try:
@@ -237,11 +255,7 @@ def run_ours(a):
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     clk = clocks.stop() if rank == 0 else None
     ms_per_step = ms / a.steps
 
@@ -287,7 +301,7 @@ def run_ours(a):
     achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
     line = {
         "metric": "W4A8 MoE layer tokens/s (decode, T=4)",
-        "value": w.T * world / (ms_per_step * 1e-3),
+        "value": whole_job_rate(w.T, world, ms, a.steps),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": a.steps,
