@@ -191,3 +191,36 @@ def test_mixed_bank_entry_checks_its_arguments(lib):
     big = binding.dims_of(4096, 2048, 512, 512, 1, 10, 128)
     need_big = lib.moe_w4a8_workspace_size(ctypes.byref(big))
     assert lib.moe_w4a8_forward_w2w4(*args, fake, ctypes.byref(big), fake, fake, need_big, None) == 2
+
+
+def test_plain_c_program_links_against_the_library(cuda_lib, tmp_path):
+    """The boundary is a C ABI: a C11 program includes the header, links the library and calls it
+    (host-side entry points only: no GPU is needed for these)."""
+    import shutil
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi_check.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "moe_w4a8.h"
+int main(void) {
+    moe_dims_t d = {4, 2048, 512, 512, 1, 10, 128};
+    moe_dims_t bad = {4, 2048, 512, 512, 1, 10, 48};
+    if (moe_w4a8_version() != MOE_W4A8_ABI_VERSION) return 1;
+    if (moe_w4a8_workspace_size(&d) == 0 || moe_w4a8_workspace_size(&bad) != 0) return 2;
+    if (moe_w4a8_forward_host_workspace_size(&d) <= moe_w4a8_workspace_size(&d)) return 3;
+    /* host-detected errors come back before anything is enqueued */
+    if (moe_w4a8_forward(NULL, NULL, NULL, NULL, NULL, NULL, NULL, &d, NULL, NULL, 0, NULL) != MOE_ERR_INVALID_ARG)
+        return 4;
+    printf("%s|%s\n", moe_w4a8_status_string(MOE_OK), moe_w4a8_status_string(MOE_ERR_WORKSPACE_TOO_SMALL));
+    return 0;
+}
+''')
+    exe = tmp_path / "abi_check"
+    libdir = os.path.dirname(cuda_lib)
+    libname = os.path.basename(cuda_lib)
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-pedantic", str(src), "-I", os.path.join(REPO, "include"),
+                    "-o", str(exe), os.path.join(libdir, libname), f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, (out.returncode, out.stderr)
+    assert out.stdout.strip() == "ok|workspace too small"
