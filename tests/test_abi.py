@@ -224,3 +224,35 @@ int main(void) {
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     assert out.returncode == 0, (out.returncode, out.stderr)
     assert out.stdout.strip() == "ok|workspace too small"
+
+
+def test_binding_checks_tensors_before_calling_the_library(lib):
+    """The Python binding refuses wrong dtypes, shapes, devices and layouts itself (no CUDA call)."""
+    import torch
+    from bit_moe_expert_router_gb300 import binding
+    d = binding.dims_of(4, 256, 128, 8, 1, 2, 64)
+    slots = d.E + d.n_shared
+    good = dict(x_q=torch.zeros(4, 256, dtype=torch.int8), x_scale=torch.zeros(4), logits=torch.zeros(4, 8),
+                w13=torch.zeros(slots, 256, 128, dtype=torch.uint8), s13=torch.zeros(slots, 256, 4),
+                w2=torch.zeros(slots, 256, 64, dtype=torch.uint8), s2=torch.zeros(slots, 256, 2),
+                out=torch.zeros(4, 256))
+    ws = torch.zeros(1024, dtype=torch.uint8)
+
+    def call(**over):
+        a = dict(good, **over)
+        return binding.moe_w4a8_forward(a["x_q"], a["x_scale"], a["logits"], a["w13"], a["s13"], a["w2"], a["s2"],
+                                        d, a["out"], ws)
+
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        call()                                                   # host tensors go through moe_w4a8_forward_host
+    with pytest.raises(TypeError, match="x_q: dtype"):
+        call(x_q=torch.zeros(4, 256))
+    with pytest.raises(ValueError, match="x_q is required"):
+        call(x_q=None)
+    # the host-buffer entry wants CPU activations and checks their shapes and layouts the same way
+    with pytest.raises(ValueError, match="router_logits must be a contiguous CPU tensor"):
+        binding.moe_w4a8_forward_host(good["x_q"], good["x_scale"], torch.zeros(8, 4).t(), good["w13"], good["s13"],
+                                      good["w2"], good["s2"], d, good["out"], ws)
+    with pytest.raises(ValueError, match="out must be a contiguous CPU tensor"):
+        binding.moe_w4a8_forward_host(good["x_q"], good["x_scale"], good["logits"], good["w13"], good["s13"],
+                                      good["w2"], good["s2"], d, torch.zeros(4, 255), ws)
