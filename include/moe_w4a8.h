@@ -330,7 +330,8 @@ int moe_w4a8_forward_bf16(const uint16_t* x_bf16, const float* router_logits,
  * Supported for the sizes the decode engine takes (T <= 32, T*k <= 512,
  * H in {2048, 4096}, I in {512, 1536}, g a multiple of 64 with I/g a
  * multiple of 4); otherwise MOE_ERR_UNSUPPORTED.  A null slot_bits is
- * MOE_ERR_INVALID_ARG.  Other arguments, workspace (moe_w4a8_workspace_size)
+ * MOE_ERR_INVALID_ARG (it needs no particular alignment; a value other than
+ * 2 is read as 4).  Other arguments, workspace (moe_w4a8_workspace_size)
  * and errors as for moe_w4a8_forward; with every slot 4-bit the result
  * equals moe_w4a8_forward's bit for bit.
  */
