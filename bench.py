@@ -358,24 +358,27 @@ def run_reference(a):
         return
     from bit_moe_expert_router_gb300 import synth
     import oracle
+    import numpy as np
     w = synth.WORKLOADS[a.workload]
     bank = synth.make_bank(w)
+    # warm-up on whole batches, which also measures the oracle's time per token
+    t_tok = None
     for b in range(max(a.warmup, 1)):
+        t0 = time.perf_counter()
         oracle.forward_workload(w, synth.make_tokens(w, batch=b), bank)
-    # each step is one batch; the run stops early once ~60 s of oracle time is spent
-    el, done = 0.0, 0
+        t_tok = (time.perf_counter() - t0) / w.T
+    # exactly a.steps steps; each step is a sample of the step's batch (its first n_tok tokens),
+    # sized so that the timed steps take about two minutes at most
+    n_tok = int(max(1, min(w.T, 120.0 / (a.steps * max(t_tok, 1e-9)))))
+    el = 0.0
     for b in range(a.steps):
         tok = synth.make_tokens(w, batch=max(a.warmup, 1) + b)
         t0 = time.perf_counter()
-        oracle.forward_workload(w, tok, bank)
+        oracle.forward_workload(w, tok, bank, np.arange(n_tok))
         el += time.perf_counter() - t0
-        done += 1
-        if el > 60.0:
-            break
-    a.steps = done
     ms = el * 1e3 / a.steps
-    cores = min(os.cpu_count() or 1, w.T)
-    val = w.T / (ms * 1e-3)
+    val = n_tok / (ms * 1e-3)
+    cores = min(os.cpu_count() or 1, n_tok)
     print(json.dumps({
         "impl": "reference", "metric": "W4A8 MoE layer tokens/s (decode, T=4)", "value": val, "unit": "tokens/s",
         "n_gpus": 1, "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -383,7 +386,7 @@ def run_reference(a):
         "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "n_shared": w.S, "top_k": w.top_k,
                    "group": w.group, "parallelism": "cpu"},
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{a.steps} batches of T={w.T}"},
+                         "sample": f"{a.steps} steps of {n_tok} of the T={w.T} tokens of a batch of {w.name}"},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
