@@ -9,10 +9,13 @@
 //
 //   phase 0  every CTA routes all T tokens itself (the same deterministic
 //            result in every CTA, so nothing is exchanged; one warp per token,
-//            k rounds of a warp arg-max), sorts the pairs stably by expert
-//            into pair rows, builds the slot table (touched
-//            experts ascending, then the shared experts) and stages the
-//            activations in shared memory.
+//            k rounds of a warp arg-max) while its other warps stage the
+//            activations in shared memory (int8 input split even|odd; bf16
+//            input quantised here first: S0, s = max|x| / 127, RNE codes);
+//            then it sorts the pairs stably by expert into pair rows and builds
+//            the slot table (touched experts ascending, then the shared
+//            experts; with each slot's code width for a mixed 2/4-bit bank)
+//            and a per-slot cost prefix.
 //   phase 1  gate/up projection with dp4a on the CUDA cores: units of two
 //            intermediate indices (2 gate rows + the 2 matching up rows) of
 //            one slot; each warp takes a contiguous unit range of equal cost
@@ -20,21 +23,27 @@
 //            multi-token units weigh more).  A warp loads one unit at a
 //            time into registers (16-byte loads; lane l loads pieces l,
 //            l + 32, ... of each row, so each warp load reads 512 contiguous
-//            bytes) -- the other 15 warps of the SM cover its latency; each lane folds the exact int32 sum of each
-//            32-value piece with its group scale, and a 4-row reduce-scatter
-//            across the warp (6 shuffles) gives the row sums; h = SiLU(G_gate)
-//            * G_up goes to the workspace and |h| into the warp's running row
-//            maximum in shared memory (merged into the global row maxima once
-//            per CTA at the end of the phase).  Meanwhile each CTA copies its
-//            slice of the down-projection bank (its output rows of every
-//            touched slot) into shared memory, or warms it in L2 where shared
-//            memory runs out.
-//   barrier  one grid-wide barrier (bounded wait; on timeout the status
-//            word records it and the CTAs leave).
-//   phase 2  every CTA requantises all pair rows from h and the row maxima
-//            (s_h = max/127, RNE codes) into shared memory, runs the down
-//            projection for its output rows of every touched slot (one lane
-//            per (slot, row), whole-K dot product), and combines
+//            bytes) -- the other 15 warps of the SM cover its latency; each
+//            lane folds the exact int32 sum of each piece with its group
+//            scale, and a 4-row reduce-scatter across the warp (6 shuffles)
+//            gives the row sums; h = SiLU(G_gate) * G_up goes to the workspace
+//            and |h| into the warp's running row maximum in shared memory
+//            (merged into the global row maxima with one atomic max per CTA
+//            and row at the end of the phase).  2-bit slots (the MIXED
+//            instantiation) load half-length rows and multiply them with a
+//            second, mod-4 ordered copy of the activations.  Meanwhile each CTA
+//            has the bulk-copy engine copy its slice of the down-projection
+//            bank (its output rows of every touched slot) into shared memory,
+//            or warms it in L2 where shared memory runs out.
+//   barrier  grid barrier 1 (each CTA adds its arrival and polls the count;
+//            bounded: on timeout the status word records it and the CTAs
+//            leave).
+//   phase 2  requantisation spread over the grid (row p on CTA p mod grid,
+//            one warp: s_h = max/127 from the row maximum, RNE codes) into the
+//            workspace; grid barrier 2; every CTA copies the P requantised
+//            rows into shared memory, runs the down projection for its output
+//            rows of every touched slot (one thread per (pair row, output
+//            row), whole-K dot product) and combines
 //            out[t][n] = sum_j w[t][j] Y[(t,j)][n] + shared in a fixed order:
 //            no atomics on the output, deterministic.
 //
