@@ -27,7 +27,8 @@ int check_dims(const moe_dims_t* d) {
         d->group < 32 || d->group % 32 != 0 || d->H % d->group != 0 || d->I % d->group != 0)
         return MOE_ERR_INVALID_ARG;
     if (d->E > moe::kMaxExperts || d->n_shared > moe::kMaxShared || d->top_k > moe::kMaxTopK ||
-        d->group > moe::kMaxGroup || d->I % 64 != 0 || d->H % 128 != 0)
+        d->group > moe::kMaxGroup || d->I % 64 != 0 || d->H % 128 != 0 || d->H > moe::kMaxDim ||
+        d->I > moe::kMaxDim)
         return MOE_ERR_UNSUPPORTED;
     const int64_t P = d->T * (d->top_k + d->n_shared);
     if (d->T > (int64_t(1) << 24) || P >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
@@ -307,7 +308,7 @@ MOE_API size_t moe_w4a8_workspace_size(const moe_dims_t* d) {
 }
 
 MOE_API size_t moe_w4a8_partials_workspace_size(const moe_dims_t* d, int64_t n_pairs) {
-    if (check_dims(d) != MOE_OK || n_pairs < 0) return 0;
+    if (check_dims(d) != MOE_OK || n_pairs < 0 || n_pairs >= (int64_t(1) << 24)) return 0;
     return partials_layout(d, n_pairs).total;
 }
 

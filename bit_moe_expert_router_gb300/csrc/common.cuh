@@ -15,6 +15,7 @@ constexpr int kMaxTopK = 32;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxShared = 8;
 constexpr int kMaxGroup = 256;
+constexpr int kMaxDim = 65536;  // largest H and I: keeps every workspace size far from overflow
 
 // Status word values written by device code into the workspace header.
 constexpr uint32_t kDevOk = 0;

@@ -62,7 +62,7 @@
  * g not a multiple of 32, or H or I not a multiple of g;
  * MOE_ERR_UNSUPPORTED for sizes beyond the kernels' limits (E > 1024,
  * S > 8, top_k > 32, g > 256, I not a multiple of 64, H not a multiple of
- * 128, T > 2^24); MOE_ERR_WORKSPACE_TOO_SMALL; MOE_ERR_CUDA if a launch is
+ * 128, H or I > 65536, T > 2^24); MOE_ERR_WORKSPACE_TOO_SMALL; MOE_ERR_CUDA if a launch is
  * rejected.  Errors that occur while the kernels run surface at
  * the caller's next synchronisation, as for any CUDA work.  T = 0 is valid
  * and enqueues nothing.
@@ -124,7 +124,8 @@ const char* moe_w4a8_last_error(void);
 size_t moe_w4a8_workspace_size(const moe_dims_t* d);
 
 /* Bytes of workspace moe_w4a8_gemm1_partials and moe_w4a8_gemm2_partials
- * need for `d` and n_pairs pairs (0 if `d` is invalid or n_pairs < 0). */
+ * need for `d` and n_pairs pairs (0 if `d` is invalid or n_pairs is
+ * outside [0, 2^24)). */
 size_t moe_w4a8_partials_workspace_size(const moe_dims_t* d, int64_t n_pairs);
 
 /* The engine moe_w4a8_forward uses for `d` on the current device

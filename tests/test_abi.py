@@ -72,6 +72,7 @@ def test_workspace_size_grows_with_tokens(lib):
     ("E", 0, 1), ("top_k", 0, 1), ("top_k", 9, 1), ("group", 48, 1), ("group", 0, 1), ("H", 200, 1),
     ("I", 96, 1), ("T", -1, 1), ("n_shared", -1, 1),
     ("E", 2048, 2), ("group", 512, 1), ("n_shared", 9, 2), ("H", 320, 2),
+    ("H", 1 << 17, 2), ("I", 1 << 17, 2), ("H", 1 << 40, 2),
 ])
 def test_bad_dims_are_rejected(lib, field, value, status):
     from bit_moe_expert_router_gb300 import binding
@@ -80,6 +81,15 @@ def test_bad_dims_are_rejected(lib, field, value, status):
     assert lib.moe_w4a8_workspace_size(ctypes.byref(d)) == 0
     rc = lib.moe_w4a8_forward(None, None, None, None, None, None, None, ctypes.byref(d), None, None, 0, None)
     assert rc == status
+
+
+def test_partials_workspace_size_follows_the_pair_limit(lib):
+    from bit_moe_expert_router_gb300 import binding
+    d = binding.dims_of(16, 256, 128, 8, 0, 2, 64)
+    assert lib.moe_w4a8_partials_workspace_size(ctypes.byref(d), ctypes.c_int64(0)) > 0
+    assert lib.moe_w4a8_partials_workspace_size(ctypes.byref(d), ctypes.c_int64((1 << 24) - 1)) > 0
+    assert lib.moe_w4a8_partials_workspace_size(ctypes.byref(d), ctypes.c_int64(1 << 24)) == 0
+    assert lib.moe_w4a8_partials_workspace_size(ctypes.byref(d), ctypes.c_int64(-1)) == 0
 
 
 def test_group_beyond_limit_is_unsupported(lib):
