@@ -96,6 +96,25 @@ def _stream(device) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+def _one_device(fn: str, tensors):
+    """The one CUDA device all of `tensors` (None entries skipped) live on."""
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) != 1:
+        raise ValueError(f"{fn}: the device tensors must share one device, got {sorted(map(str, devs))}")
+    return devs.pop()
+
+
+def _call(fn: str, tensors, *args):
+    """Calls entry point `fn` with `args` followed by the current stream of the
+    device `tensors` share, with that device current for the launches."""
+    dev = _one_device(fn, tensors)
+    if dev.index == torch.cuda.current_device():
+        _check(fn, getattr(_load(), fn)(*args, _stream(dev)))
+        return
+    with torch.cuda.device(dev):
+        _check(fn, getattr(_load(), fn)(*args, _stream(dev)))
+
+
 def _need(t, name, dtype, shape=None):
     if t is None:
         raise ValueError(f"{name} is required")
@@ -150,6 +169,7 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
 
 def _ws_view(ws: torch.Tensor):
     """(pointer, bytes) of the 256-byte aligned part of a uint8 workspace tensor."""
+    _need(ws, "workspace", torch.uint8)
     base = ws.data_ptr()
     aligned = (base + 255) & ~255
     return ctypes.c_void_p(aligned), ws.numel() - (aligned - base)
@@ -177,9 +197,10 @@ def moe_w4a8_forward(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_pack
                      workspace: torch.Tensor):
     _check_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out)
     wp, wb = _ws_view(workspace)
-    _check("moe_w4a8_forward", _load().moe_w4a8_forward(
-        _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
-        _ptr(w2_scale), ctypes.byref(d), _ptr(out), wp, wb, _stream(out.device)))
+    _call("moe_w4a8_forward", (x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, out,
+                               workspace),
+          _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
+          _ptr(w2_scale), ctypes.byref(d), _ptr(out), wp, wb)
     return out
 
 
@@ -217,9 +238,9 @@ def moe_w4a8_forward_host(x_q, x_scale, router_logits, w13_packed, w13_scale, w2
     _need(w2_packed, "w2_packed", torch.uint8, s2)
     _need(w2_scale, "w2_scale", torch.float32, s2s)
     wp, wb = _ws_view(workspace)
-    _check("moe_w4a8_forward_host", _load().moe_w4a8_forward_host(
-        _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
-        _ptr(w2_scale), ctypes.byref(d), _ptr(out), wp, wb, _stream(workspace.device)))
+    _call("moe_w4a8_forward_host", (w13_packed, w13_scale, w2_packed, w2_scale, workspace),
+          _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
+          _ptr(w2_scale), ctypes.byref(d), _ptr(out), wp, wb)
     return out
 
 
@@ -243,9 +264,10 @@ def moe_w4a8_forward_bf16(x_bf16, router_logits, w13_packed, w13_scale, w2_packe
     _need(w2_scale, "w2_scale", torch.float32, s2s)
     _need(out, "out", torch.float32, (d.T, d.H))
     wp, wb = _ws_view(workspace)
-    _check("moe_w4a8_forward_bf16", _load().moe_w4a8_forward_bf16(
-        _ptr(x_bf16), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed), _ptr(w2_scale),
-        ctypes.byref(d), _ptr(out), wp, wb, _stream(out.device)))
+    _call("moe_w4a8_forward_bf16", (x_bf16, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, out,
+                                    workspace),
+          _ptr(x_bf16), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed), _ptr(w2_scale),
+          ctypes.byref(d), _ptr(out), wp, wb)
     return out
 
 
@@ -259,9 +281,10 @@ def moe_w4a8_forward_w2w4(x_q, x_scale, router_logits, w13_packed, w13_scale, w2
     _check_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out)
     _need(slot_bits, "slot_bits", torch.uint8, (d.E + d.n_shared,))
     wp, wb = _ws_view(workspace)
-    _check("moe_w4a8_forward_w2w4", _load().moe_w4a8_forward_w2w4(
-        _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
-        _ptr(w2_scale), _ptr(slot_bits), ctypes.byref(d), _ptr(out), wp, wb, _stream(out.device)))
+    _call("moe_w4a8_forward_w2w4", (x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale,
+                                    slot_bits, out, workspace),
+          _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
+          _ptr(w2_scale), _ptr(slot_bits), ctypes.byref(d), _ptr(out), wp, wb)
     return out
 
 
@@ -276,9 +299,9 @@ def moe_w4a8_forward_noalloc(x_q, x_scale, router_logits, w13_packed, w13_scale,
     NOALLOC_SCRATCH_BYTES of intermediates are rejected.
     """
     _check_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out)
-    _check("moe_w4a8_forward_noalloc", _load().moe_w4a8_forward_noalloc(
-        _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
-        _ptr(w2_scale), ctypes.byref(d), _ptr(out), _stream(out.device)))
+    _call("moe_w4a8_forward_noalloc", (x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, out),
+          _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
+          _ptr(w2_scale), ctypes.byref(d), _ptr(out))
     return out
 
 
@@ -293,10 +316,10 @@ def moe_w4a8_forward_debug(x_q, x_scale, router_logits, w13_packed, w13_scale, w
     if y is not None:
         _need(y, "y", torch.float32, (P, d.H))
     wp, wb = _ws_view(workspace)
-    _check("moe_w4a8_forward_debug", _load().moe_w4a8_forward_debug(
-        _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
-        _ptr(w2_scale), ctypes.byref(d), _ptr(out), _ptr(h_q), _ptr(s_h), _ptr(y), engine, wp, wb,
-        _stream(out.device)))
+    _call("moe_w4a8_forward_debug", (x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, out,
+                                     h_q, s_h, y, workspace),
+          _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
+          _ptr(w2_scale), ctypes.byref(d), _ptr(out), _ptr(h_q), _ptr(s_h), _ptr(y), engine, wp, wb)
     return out
 
 
@@ -309,9 +332,9 @@ def moe_w4a8_route(router_logits, d: Dims, topk_ids, topk_w, counts, offsets, pe
     _need(perm, "perm", torch.int32, (d.T * d.top_k,))
     _need(inv, "inv", torch.int32, (d.T * d.top_k,))
     wp, wb = _ws_view(workspace)
-    _check("moe_w4a8_route", _load().moe_w4a8_route(
-        _ptr(router_logits), ctypes.byref(d), _ptr(topk_ids), _ptr(topk_w), _ptr(counts), _ptr(offsets),
-        _ptr(perm), _ptr(inv), wp, wb, _stream(router_logits.device)))
+    _call("moe_w4a8_route", (router_logits, topk_ids, topk_w, counts, offsets, perm, inv, workspace),
+          _ptr(router_logits), ctypes.byref(d), _ptr(topk_ids), _ptr(topk_w), _ptr(counts), _ptr(offsets),
+          _ptr(perm), _ptr(inv), wp, wb)
 
 
 def moe_w4a8_gemm1_partials(x_q, w13_packed, d: Dims, pair_token, pair_slot, p1, workspace,
@@ -323,9 +346,9 @@ def moe_w4a8_gemm1_partials(x_q, w13_packed, d: Dims, pair_token, pair_slot, p1,
     _need(pair_slot, "pair_slot", torch.int32, (n,))
     _need(p1, "p1", torch.int32, (n, 2 * d.I, d.H // d.group))
     wp, wb = _ws_view(workspace)
-    _check("moe_w4a8_gemm1_partials", _load().moe_w4a8_gemm1_partials(
-        _ptr(x_q), _ptr(w13_packed), ctypes.byref(d), _ptr(pair_token), _ptr(pair_slot), n, _ptr(p1), engine, wp,
-        wb, _stream(p1.device)))
+    _call("moe_w4a8_gemm1_partials", (x_q, w13_packed, pair_token, pair_slot, p1, workspace),
+          _ptr(x_q), _ptr(w13_packed), ctypes.byref(d), _ptr(pair_token), _ptr(pair_slot), n, _ptr(p1), engine, wp,
+          wb)
 
 
 def moe_w4a8_gemm2_partials(h_q, w2_packed, d: Dims, pair_slot, p2, workspace, engine: int = ENGINE_GROUPED):
@@ -335,22 +358,21 @@ def moe_w4a8_gemm2_partials(h_q, w2_packed, d: Dims, pair_slot, p2, workspace, e
     _need(pair_slot, "pair_slot", torch.int32, (n,))
     _need(p2, "p2", torch.int32, (n, d.H, d.I // d.group))
     wp, wb = _ws_view(workspace)
-    _check("moe_w4a8_gemm2_partials", _load().moe_w4a8_gemm2_partials(
-        _ptr(h_q), _ptr(w2_packed), ctypes.byref(d), _ptr(pair_slot), n, _ptr(p2), engine, wp, wb,
-        _stream(p2.device)))
+    _call("moe_w4a8_gemm2_partials", (h_q, w2_packed, pair_slot, p2, workspace),
+          _ptr(h_q), _ptr(w2_packed), ctypes.byref(d), _ptr(pair_slot), n, _ptr(p2), engine, wp, wb)
 
 
 def moe_w4a8_selftest_barrier_timeout(workspace: torch.Tensor):
     """Enqueue the bounded-wait self-test (see the C header); read the result with moe_w4a8_device_status."""
     wp, wb = _ws_view(workspace)
-    _check("moe_w4a8_selftest_barrier_timeout",
-           _load().moe_w4a8_selftest_barrier_timeout(wp, wb, _stream(workspace.device)))
+    _call("moe_w4a8_selftest_barrier_timeout", (workspace,), wp, wb)
 
 
 def moe_w4a8_device_status(workspace: torch.Tensor) -> int:
     """Synchronises the current stream and returns the status word of the last call (0 = ok, 5 = timeout)."""
     wp, wb = _ws_view(workspace)
-    return _load().moe_w4a8_device_status(wp, wb, _stream(workspace.device))
+    with torch.cuda.device(workspace.device):
+        return _load().moe_w4a8_device_status(wp, wb, _stream(workspace.device))
 
 
 class Layer:

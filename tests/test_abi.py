@@ -266,3 +266,61 @@ def test_binding_checks_tensors_before_calling_the_library(lib):
     with pytest.raises(ValueError, match="out must be a contiguous CPU tensor"):
         binding.moe_w4a8_forward_host(good["x_q"], good["x_scale"], good["logits"], good["w13"], good["s13"],
                                       good["w2"], good["s2"], d, torch.zeros(4, 255), ws)
+
+
+def test_binding_checks_the_workspace_and_the_device(lib):
+    """Every call needs a CUDA uint8 workspace and all device tensors on one device (checked before any call)."""
+    import torch
+    from bit_moe_expert_router_gb300 import binding
+    with pytest.raises(ValueError, match="workspace must be a CUDA tensor"):
+        binding._ws_view(torch.zeros(1024, dtype=torch.uint8))
+    with pytest.raises(TypeError, match="workspace: dtype"):
+        binding._ws_view(torch.zeros(1024))
+    a, b = torch.zeros(4), torch.zeros(4, device="meta")
+    assert binding._one_device("f", (a, None, a)) == a.device
+    with pytest.raises(ValueError, match="share one device"):
+        binding._one_device("moe_w4a8_forward", (a, None, b))
+
+
+def test_binding_calls_on_the_tensors_device_with_its_stream(monkeypatch):
+    """_call appends the current stream of the tensors' device, makes that device current only when it is
+    not, and turns a non-zero status into MoeError (fakes stand in for the library and the CUDA runtime)."""
+    import contextlib
+    import types
+    import torch
+    from bit_moe_expert_router_gb300 import binding
+    calls, switched = [], []
+
+    class FakeLib:
+        def moe_w4a8_forward(self, *args):
+            calls.append(args)
+            return self.status
+
+        def moe_w4a8_status_string(self, status):
+            return b"fake status"
+
+    lib = FakeLib()
+    monkeypatch.setattr(binding, "_load", lambda: lib)
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda dev: types.SimpleNamespace(cuda_stream=100 + dev.index))
+
+    @contextlib.contextmanager
+    def fake_device(dev):
+        switched.append(dev.index)
+        yield
+
+    monkeypatch.setattr(torch.cuda, "device", fake_device)
+    on = lambda i: types.SimpleNamespace(device=torch.device("cuda", i))  # noqa: E731
+
+    lib.status = 0
+    binding._call("moe_w4a8_forward", (on(0), None, on(0)), "a", "b")
+    assert calls[-1][:2] == ("a", "b") and calls[-1][2].value == 100 and switched == []
+    binding._call("moe_w4a8_forward", (on(1), on(1)), "c")
+    assert calls[-1][0] == "c" and calls[-1][1].value == 101 and switched == [1]
+    lib.status = 3
+    with pytest.raises(binding.MoeError):
+        binding._call("moe_w4a8_forward", (on(0),), "d")
+    n = len(calls)
+    with pytest.raises(ValueError, match="share one device"):
+        binding._call("moe_w4a8_forward", (on(0), on(1)), "e")
+    assert len(calls) == n                       # refused before the library is called
