@@ -324,3 +324,18 @@ def test_binding_calls_on_the_tensors_device_with_its_stream(monkeypatch):
     with pytest.raises(ValueError, match="share one device"):
         binding._call("moe_w4a8_forward", (on(0), on(1)), "e")
     assert len(calls) == n                       # refused before the library is called
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    """No CPU fallback: with the CUDA library absent every entry point raises before doing anything."""
+    import torch
+    from bit_moe_expert_router_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "libmoe_w4a8.so"))
+    d = binding.dims_of(4, 256, 128, 8, 0, 2, 64)
+    with pytest.raises(RuntimeError, match="is missing"):
+        binding.moe_w4a8_version()
+    with pytest.raises(RuntimeError, match="is missing"):
+        binding.moe_w4a8_workspace_size(d)
+    with pytest.raises(RuntimeError, match="is missing"):
+        binding.Layer(d, None, None, None, None, "cpu")
