@@ -339,3 +339,16 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
         binding.moe_w4a8_workspace_size(d)
     with pytest.raises(RuntimeError, match="is missing"):
         binding.Layer(d, None, None, None, None, "cpu")
+
+
+def test_engine_query_without_a_device_returns_cleanly(lib):
+    """Host-only: with no usable device the engine query still answers (the decode engine needs the
+    device's shared-memory size, so it is ruled out) and invalid sizes give -1."""
+    import torch
+    from bit_moe_expert_router_gb300 import binding
+    if torch.cuda.is_available():
+        pytest.skip("a device is visible")
+    d = binding.dims_of(4, 2048, 512, 512, 1, 10, 128)
+    assert binding.moe_w4a8_engine_for(d) in (binding.ENGINE_TCGEN05, binding.ENGINE_GROUPED)
+    d.group = 48
+    assert binding.moe_w4a8_engine_for(d) == -1
