@@ -352,3 +352,12 @@ def test_engine_query_without_a_device_returns_cleanly(lib):
     assert binding.moe_w4a8_engine_for(d) in (binding.ENGINE_TCGEN05, binding.ENGINE_GROUPED)
     d.group = 48
     assert binding.moe_w4a8_engine_for(d) == -1
+
+
+def test_binding_refuses_a_library_of_another_abi_version(monkeypatch, lib):
+    """The binding and the library move in lock-step: a different ABI version is refused at load."""
+    from bit_moe_expert_router_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "ABI_VERSION", lib.moe_w4a8_version() + 1)
+    with pytest.raises(RuntimeError, match="ABI version"):
+        binding._load()
