@@ -15,7 +15,6 @@ from __future__ import annotations
 
 import ctypes
 import dataclasses
-import math
 import os
 
 import numpy as np
