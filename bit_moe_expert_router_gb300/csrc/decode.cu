@@ -153,8 +153,11 @@ __device__ bool grid_barrier(Header* hdr, uint32_t k) {
 }
 
 // Order-preserving 32-bit key of a float: larger float -> larger key; -0.0
-// and +0.0 map to the same key (the sum with +0.0 turns -0.0 into +0.0).
+// and +0.0 map to the same key (the sum with +0.0 turns -0.0 into +0.0).  A
+// NaN gets key 1: below every number (-inf is 0x007FFFFF), above the 0 of a
+// taken or absent expert, so NaNs are picked last, by index.
 __device__ __forceinline__ uint32_t order_key(float v) {
+    if (v != v) return 1u;
     const uint32_t u = __float_as_uint(v + 0.0f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }

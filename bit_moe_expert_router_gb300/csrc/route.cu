@@ -22,9 +22,16 @@
 namespace moe {
 namespace {
 
-// (v, e) beats (bv, be): larger value, or equal value and lower index.
+// (v, e) beats (bv, be): larger value, or equal value and lower index; a NaN
+// ranks below every number (NaNs among themselves by index); be = INT32_MAX
+// is "no candidate yet", which anything beats.  So every token gets k
+// distinct experts whatever its logits hold.
 __device__ __forceinline__ bool beats(float v, int e, float bv, int be) {
-    return v > bv || (v == bv && e < be);
+    if (e == INT32_MAX) return false;
+    if (be == INT32_MAX) return true;
+    const bool vn = v != v, bn = bv != bv;
+    if (vn != bn) return bn;
+    return v > bv || ((v == bv || vn) && e < be);
 }
 
 template <int MAXJ>

@@ -69,7 +69,9 @@ static int code_at(const uint8_t* row, int64_t k, int bits) {
 /*
  * route: for each token choose k experts by repeated scans for the largest
  * remaining logit (a strictly larger value replaces the candidate, so equal
- * values keep the lower index; -0.0 and +0.0 compare equal).  Selecting on
+ * values keep the lower index; -0.0 and +0.0 compare equal).  A NaN logit
+ * ranks below every number and NaNs among themselves by index (reading: the
+ * page is silent on invalid logits; this keeps k distinct experts per token).  Selecting on
  * the logits picks the same set as selecting on the softmax probabilities,
  * because exp is increasing.  Weights: exp(l_j - m) / sum over the selected
  * of exp(l - m), m the largest selected logit -- the renormalised top-k of
@@ -85,7 +87,7 @@ int orc_route(int64_t T, int64_t E, int64_t k, const float* logits, int32_t* ids
             int64_t best = -1;
             for (int64_t e = 0; e < E; ++e) {
                 if (taken[e]) continue;
-                if (best < 0 || l[e] > l[best]) best = e;
+                if (best < 0 || l[e] > l[best] || (isnan(l[best]) && !isnan(l[e]))) best = e;
             }
             taken[best] = 1;
             ids[t * k + j] = (int32_t)best;

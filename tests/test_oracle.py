@@ -112,6 +112,24 @@ def test_route_k1_and_k_equals_E():
     assert np.max(np.abs(wE - np.take_along_axis(full, idsE, axis=1))) < 1e-12
 
 
+def test_route_orders_nan_logits_last():
+    """NaN ranks below every number (-inf included), NaNs by index: numpy's stable lexsort on (is NaN, -value)."""
+    rng = np.random.default_rng(11)
+    l = rng.standard_normal((40, 24)).astype(np.float32)
+    l[rng.random(l.shape) < 0.25] = np.nan
+    l[0, :] = np.nan                       # all NaN: the lowest indices
+    l[1, :5] = -np.inf
+    l[1, 5:] = np.nan                      # -inf before every NaN
+    l[2, 3] = np.inf
+    for k in (1, 5, 24):
+        ids, _ = oracle.route(l, k)
+        ref = np.stack([np.lexsort((np.where(np.isnan(r), 0.0, -r.astype(np.float64)), np.isnan(r)))[:k] for r in l])
+        assert np.array_equal(ids, ref), k
+        assert all(len(set(row)) == k for row in ids.tolist())
+    assert oracle.route(l, 3)[0][0].tolist() == [0, 1, 2]
+    assert oracle.route(l, 6)[0][1].tolist() == [0, 1, 2, 3, 4, 5]
+
+
 def test_route_rejects_bad_k():
     with pytest.raises(ValueError):
         oracle.route(np.zeros((2, 4), np.float32), 5)

@@ -19,7 +19,10 @@ MUTANTS = [
     ("int2 sign", "return v >= 2 ? v - 4 : v;", "return v;"),
     ("int2 field order", "int v = (byte >> (2 * pos)) & 0x3;", "int v = (byte >> (6 - 2 * pos)) & 0x3;"),
     ("int2 byte index", "orc_unpack2(row[k >> 2], (int)(k & 3))", "orc_unpack2(row[k >> 1], (int)(k & 3))"),
-    ("route tie to higher index", "if (best < 0 || l[e] > l[best]) best = e;", "if (best < 0 || l[e] >= l[best]) best = e;"),
+    ("route tie to higher index", "if (best < 0 || l[e] > l[best] || (isnan(l[best]) && !isnan(l[e]))) best = e;",
+     "if (best < 0 || l[e] >= l[best] || (isnan(l[best]) && !isnan(l[e]))) best = e;"),
+    ("route NaN first", "if (best < 0 || l[e] > l[best] || (isnan(l[best]) && !isnan(l[e]))) best = e;",
+     "if (best < 0 || l[e] > l[best]) best = e;"),
     ("group scale dropped", "out[n] = a_scale * acc;", "out[n] = acc;"),
     ("gate and up swapped", "h[i] = orc_silu(Gv[i]) * Gv[I + i];", "h[i] = orc_silu(Gv[I + i]) * Gv[i];"),
     ("SiLU sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
