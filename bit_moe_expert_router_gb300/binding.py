@@ -368,8 +368,15 @@ def moe_w4a8_selftest_barrier_timeout(workspace: torch.Tensor):
     _call("moe_w4a8_selftest_barrier_timeout", (workspace,), wp, wb)
 
 
-def moe_w4a8_device_status(workspace: torch.Tensor) -> int:
-    """Synchronises the current stream and returns the status word of the last call (0 = ok, 5 = timeout)."""
+def moe_w4a8_device_status(workspace: torch.Tensor | None, device=None) -> int:
+    """Synchronises the current stream and returns the status word of the last call (0 = ok, 5 = timeout).
+
+    workspace None: the status of the last moe_w4a8_forward_noalloc call on `device` (default: current device).
+    """
+    if workspace is None:
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        with torch.cuda.device(dev):
+            return _load().moe_w4a8_device_status(None, 0, _stream(dev))
     wp, wb = _ws_view(workspace)
     with torch.cuda.device(workspace.device):
         return _load().moe_w4a8_device_status(wp, wb, _stream(workspace.device))

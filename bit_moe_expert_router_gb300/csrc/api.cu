@@ -6,8 +6,6 @@
 
 #include <algorithm>
 #include <cstdio>
-#include <mutex>
-
 #include "decode.h"
 #include "kernels.h"
 #include "moe_w4a8.h"
@@ -176,8 +174,7 @@ bool tc_fits(const moe_dims_t* d) {
 }
 
 moe::TcArgs tc_args(const uint8_t* w, const float* ws, int64_t rows_per_slot, int64_t K, const moe_dims_t* d,
-                    const __half* b, const int32_t* b_row, int64_t b_rows, const float* b_scale, const Views& v,
-                    int n_slots) {
+                    const __half* b, int64_t b_rows, const float* b_scale, const Views& v, int n_slots) {
     moe::TcArgs a{};
     a.w = w;
     a.ws = ws;
@@ -187,29 +184,37 @@ moe::TcArgs tc_args(const uint8_t* w, const float* ws, int64_t rows_per_slot, in
     a.I = d->I;
     a.H = d->H;
     a.b = b;
-    a.b_row = b_row;
     a.b_rows = b_rows;
     a.b_scale = b_scale;
     a.seg_off = v.seg_off;
     a.seg_cnt = v.seg_cnt;
+    a.row_token = v.row_token;
     a.n_slots = n_slots;
     a.hdr = v.hdr;
     return a;
 }
 
-// gemm1 + act, requant, gemm2 on the tcgen05 engine (routing and grouping done).
+// gemm1 + act, requant, gemm2 and the combine on the tcgen05 engine (routing and grouping done).
+// y_debug: also the per-pair outputs Y in fp32.
 int run_tc_gemms(const int8_t* x_q, const float* x_scale, const uint8_t* w13, const float* s13, const uint8_t* w2,
-                 const float* s2, const moe_dims_t* d, const WsLayout& L, const Views& v, cudaStream_t st) {
+                 const float* s2, const moe_dims_t* d, float* out, const WsLayout& L, const Views& v, float* y_debug,
+                 cudaStream_t st) {
     const int n_slots = static_cast<int>(d->E + d->n_shared);
-    // the activations gathered by pair row, so the gate/up B tiles are contiguous rows
+    // the activations gathered by pair row (fp16, the engine's K order): contiguous B tiles for gate/up
     MOE_CUDA(moe::launch_prep_x16(x_q, d->T, d->H, v.row_token, L.P, v.x16, st));
-    moe::TcArgs g1 = tc_args(w13, s13, 2 * d->I, d->H, d, v.x16, v.row_token, L.P, x_scale, v, n_slots);
+    moe::TcArgs g1 = tc_args(w13, s13, 2 * d->I, d->H, d, v.x16, L.P, x_scale, v, n_slots);
     g1.h = v.h;
     MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kGateUp, g1, st));
     MOE_CUDA(moe::launch_prep_h16(v.h, v.amax, nullptr, L.P, d->I, v.h16, v.sh, st));
-    moe::TcArgs g2 = tc_args(w2, s2, d->H, d->I, d, v.h16, nullptr, L.P, v.sh, v, n_slots);
-    g2.y = v.y;
+    moe::TcArgs g2 = tc_args(w2, s2, d->H, d->I, d, v.h16, L.P, v.sh, v, n_slots);
+    __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(v.y);  // the Y area holds bf16 Y here
+    g2.yb = yb;
     MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kDown, g2, st));
+    MOE_CUDA(moe::launch_combine_bf16(yb, v.wts, v.inv, d->T, d->H, d->top_k, d->n_shared, out, st));
+    if (y_debug) {
+        g2.y = y_debug;
+        MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kDownY, g2, st));
+    }
     return MOE_OK;
 }
 
@@ -227,10 +232,7 @@ int run_layer(const int8_t* x_q, const float* x_scale, const float* logits, cons
     if (tc && !tc_fits(d)) return MOE_ERR_UNSUPPORTED;
     MOE_CUDA(moe::launch_route_topk(logits, d->T, d->E, d->top_k, v.ids, v.wts, st));
     MOE_CUDA(moe::launch_sort(sort_args(v, v.ids, d->T, d->top_k, d->E, d->n_shared, L.P), st));
-    if (tc) {
-        MOE_TRY(run_tc_gemms(x_q, x_scale, w13, s13, w2, s2, d, L, v, st));
-        return combine_out(d, out, L, v, y_debug, st);
-    }
+    if (tc) return run_tc_gemms(x_q, x_scale, w13, s13, w2, s2, d, out, L, v, y_debug, st);
 
     moe::Gemm1Args g1{};
     g1.x_q = x_q;
@@ -602,7 +604,7 @@ MOE_API int moe_w4a8_gemm1_partials(const int8_t* x_q, const uint8_t* w13_packed
     if (engine == MOE_ENGINE_TCGEN05) {
         if (!tc_fits(d)) return MOE_ERR_UNSUPPORTED;
         MOE_CUDA(moe::launch_prep_x16(x_q, d->T, d->H, v.row_token, L.P, v.x16, st));
-        moe::TcArgs a = tc_args(w13_packed, nullptr, 2 * d->I, d->H, d, v.x16, nullptr, L.P, nullptr, v, n_slots);
+        moe::TcArgs a = tc_args(w13_packed, nullptr, 2 * d->I, d->H, d, v.x16, L.P, nullptr, v, n_slots);
         a.partials = p1;
         MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kGateUpPartials, a, st));
         return MOE_OK;
@@ -645,7 +647,7 @@ MOE_API int moe_w4a8_gemm2_partials(const int8_t* h_q, const uint8_t* w2_packed,
     if (engine == MOE_ENGINE_TCGEN05) {
         if (!tc_fits(d)) return MOE_ERR_UNSUPPORTED;
         MOE_CUDA(moe::launch_prep_h16(nullptr, nullptr, h_q, n_pairs, d->I, v.h16, nullptr, st));
-        moe::TcArgs a = tc_args(w2_packed, nullptr, d->H, d->I, d, v.h16, nullptr, n_pairs, nullptr, v, n_slots);
+        moe::TcArgs a = tc_args(w2_packed, nullptr, d->H, d->I, d, v.h16, n_pairs, nullptr, v, n_slots);
         a.partials = p2;
         MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kDownPartials, a, st));
         return MOE_OK;
@@ -666,8 +668,18 @@ MOE_API int moe_w4a8_gemm2_partials(const int8_t* h_q, const uint8_t* w2_packed,
     return MOE_OK;
 }
 
+namespace {
+int noalloc_scratch(void** out);
+}  // namespace
+
 MOE_API int moe_w4a8_device_status(const void* workspace, size_t workspace_bytes, void* stream) {
-    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < sizeof(moe::Header))
+    void* scratch = nullptr;
+    if (!workspace) {  // the built-in array of moe_w4a8_forward_noalloc on the current device
+        MOE_TRY(noalloc_scratch(&scratch));
+        workspace = scratch;
+        workspace_bytes = MOE_W4A8_NOALLOC_SCRATCH_BYTES;
+    }
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < sizeof(moe::Header))
         return MOE_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint32_t status = 0;
@@ -686,27 +698,20 @@ MOE_API int moe_w4a8_selftest_barrier_timeout(void* workspace, size_t workspace_
 // ------------------------------------------------------------------ no-alloc variant
 // The scratch array of moe_w4a8_forward_noalloc.  Host code must not pass
 // `g_noalloc_scratch` itself to a kernel (on the host it names a stand-in,
-// not device memory); its device address is looked up once per device.
+// not device memory); its device address is looked up on every call, with
+// the calling device current, so a context that was reset and re-created
+// (the module reloaded, the array possibly moved) gets its new address.
 namespace {
 constexpr size_t kNoAllocBytes = MOE_W4A8_NOALLOC_SCRATCH_BYTES;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (first call per device resolves it).
+// Device address of the scratch array on the current device.  The first
+// lookup in a context loads the library's device code there.
 int noalloc_scratch(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-        void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p) return MOE_ERR_CUDA;
-        g_noalloc_addr[dev] = p;
-    }
-    *out = g_noalloc_addr[dev];
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return cuda_status(e == cudaSuccess ? cudaErrorInvalidSymbol : e, "cudaGetSymbolAddress");
+    *out = p;
     return MOE_OK;
 }
 }  // namespace

@@ -68,7 +68,8 @@ inline WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S,
     L.hq = take(static_cast<size_t>(L.P) * I);
     L.sh = take(sizeof(float) * L.P);
     L.y = take(sizeof(float) * L.P * H);
-    L.x16 = take(2 * static_cast<size_t>(L.P) * H);  // tcgen05 engine operands (fp16): activations by pair row
+    // tcgen05 engine operands (fp16), by pair row: the gathered activations and the requantised h
+    L.x16 = take(2 * static_cast<size_t>(L.P) * H);
     L.h16 = take(2 * static_cast<size_t>(L.P) * I);
     L.total = o;
     return L;

@@ -7,37 +7,50 @@
 // the operands go to the fp16 MMA (kind::f16): int4 codes and int8 values
 // are exact in fp16, each product is exact in the fp32 accumulator and a
 // 128-value K group sums to |P| <= 128 * 127 * 8 < 2^24, so every group's
-// accumulator holds the exact int32 partial.  One group is accumulated per
-// TMEM buffer and folded into fp32 registers with its weight scale by the
-// epilogue warps while the tensor core fills the next buffer.
+// accumulator holds the exact int32 partial.  Each group is accumulated in
+// its own tensor-memory buffer and folded into fp32 registers with its
+// weight scale by the epilogue warps while the tensor core fills the other
+// buffer.
 //
-// Tile: M = 128 weight rows x N <= 128 tokens of one bank slot, one K
-// group (128 values) per pipeline stage, 2 stages.  The A operand (the
-// unpacked weights, fp16) goes to tensor memory -- each producer thread
-// writes its row's 64 columns into its own lane with tcgen05.st -- and the
-// B operand (token rows, fp16) to shared memory in the 128-byte-swizzled
-// K-major layout the MMA reads; A thus never passes through shared memory,
-// whose bandwidth the MMA's B reads and the B copies then share alone.
-// Gate/up tiles interleave the rows (tile row 2j = gate row i, 2j + 1 = up
-// row i, i = 64 m + j), so the SiLU(gate) * up product pairs neighbouring
-// lanes.  The MMA width N is the token count of the tile rounded up to 16.
+// Tile: M = 128 weight rows x N <= 192 tokens of one bank slot, one K group
+// (128 values) per B stage.  An M = 128 MMA costs about the same
+// time for any N up to 192 on this GPU (~135 cycles with A in tensor memory),
+// so wide token tiles are what sets the tensor-pipe rate; 192 columns is the
+// widest that leaves two accumulators and two A stages in the 512 columns of
+// tensor memory (2 x 192 + 2 x 64).
+//   A (the unpacked weights, fp16): each producer warp copies the packed
+//     rows of its 32 tile rows for a stage (64 bytes each, cp.async, four
+//     lanes per row) into a 3-deep ring two stages ahead; each producer
+//     thread unpacks its row's 128 codes and writes them to its own
+//     tensor-memory lane with tcgen05.st, so A never passes through shared
+//     memory.  (TMA boxes of 64-byte rows measured slower: the TMA unit
+//     spends its time per row.)  Gate/up tiles interleave the rows (tile row 2j = gate row i,
+//     2j + 1 = up row i, i = 64 m + j): the SiLU(gate) * up product pairs
+//     neighbouring lanes.
+//   B (token rows, fp16, 128-byte-swizzled K-major atoms): contiguous rows
+//     by pair row -- the activations gathered per pair (gate/up) or the
+//     requantised h (down) -- loaded as two 2-D TMA tiles per stage by the MMA
+//     warp.  (Gathering the activation rows inside the kernel from a
+//     per-token table, by TMA tile::gather4 or by 16-byte cp.async copies,
+//     measured several times slower here: the row requests cost far more than
+//     the bytes.)  Three stages.
 // Persistent CTAs (one per SM) walk the (slot, token tile, weight tile)
 // items with the weight tile fastest, so the CTAs working at one time share
-// the token tile in L2.  Tensor memory: 3 accumulators x 128 columns + 2 A
-// stages x 64 columns = all 512 columns.  Three accumulators let the MMAs run
-// two groups into the next item while the epilogue finishes an item (SiLU or
-// scaling and the stores); that buys more than deeper A/B staging, since the
-// producers keep ahead of the MMAs with two stages.
+// the token rows in L2.  Every item costs the same MMA time (K / 16 MMAs of
+// any width), so a static round-robin deal balances the grid.
 //
-// Thirteen warps (four of them share one SM sub-partition, whose 16K-register
-// file then caps a thread at 128 registers).  Warp roles: warps 0-7
-// epilogue (warp w: TMEM lanes 32 (w % 4) .. +31 = tile rows, columns
-// 64 (w / 4) .. +63), warps 8-11 producers (thread = tile row: unpack 64
-// packed bytes of its weight row into fp16 and store them to its TMEM lane;
-// warp 8 also issues the stage's two TMA tiles of token rows), warp 12 issues
-// the MMAs (one thread)
-// and owns the TMEM allocation.  Every wait is bounded; a timeout sets the
-// status word and every role leaves cleanly.
+// Epilogue.  Gate/up: h = SiLU(x_scale G_gate) * (x_scale G_up) by pair row.
+// Down: Y = s_h * sum_q s2 P2 by pair row, stored in bf16 for the combine
+// kernel, which sums each token's pairs in a fixed order in fp32 (adding the
+// pairs into the output with device reductions instead measured several
+// times slower: the reductions of one tile outlast its MMAs many times over).
+//
+// Seventeen warps: 0-11 epilogue (warp w: TMEM lanes 32 (w % 4) .. +31 =
+// tile rows, columns 64 (w / 4) .. +63), 12-15 producers (thread = tile row
+// of A), 16 MMA issue and B tiles (one thread: a warp-wide wait costs a few
+// hundred cycles here, and the issuing loop has to stay well inside the MMA
+// time of a stage) and the tensor-memory allocation.  Every wait is
+// bounded; a timeout sets the status word and every role leaves cleanly.
 //
 // K order: the weight unpack turns a packed word (codes 0..7) into fp16
 // pairs (0,4) (1,5) (2,6) (3,7); the token rows are converted to fp16 in
@@ -55,26 +68,46 @@
 namespace moe {
 namespace {
 
-constexpr int kEpiWarps = 8;                 // two per TMEM lane quarter, 64 columns each
-constexpr int kProdWarps = 4;
-constexpr int kMmaWarp = kEpiWarps + kProdWarps;
+constexpr int kEpiWarps = 12;                // three per TMEM lane quarter, 64 columns each
+constexpr int kProdWarps = 4;                // one per TMEM lane quarter
+constexpr int kProdWarp0 = kEpiWarps;
+constexpr int kMmaWarp = kEpiWarps + kProdWarps;  // MMA issue and B tiles
 constexpr int kTcThreads = 32 * (kMmaWarp + 1);
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kHalfN = 64;                   // columns per epilogue warp
-constexpr int kNS = 2;                       // pipeline stages: A in tensor memory, B in shared memory
-constexpr int kTileN = 128;
-constexpr int kAtom = 16384;                 // 128 rows x 128 bytes
-constexpr int kStage = 2 * kAtom;             // B: 128 token rows x 128 fp16 (two swizzled atoms)
-constexpr int kACols = 64;                   // A: 128 rows x 128 fp16 = 64 tensor-memory columns per stage
-constexpr int kMaxSlotsTc = kTcMaxSlots + 1;
-constexpr int kAcc = 3;                      // accumulator buffers in tensor memory (128 columns each)
-constexpr int kTmemCols = 512;               // kAcc * 128 accumulator columns + kNS * kACols A columns
-constexpr int kRaw = 3;                      // packed weight rows in flight ahead of the unpack
+constexpr int kProdThreads = 32 * kProdWarps;
+constexpr int kColsW = 64;                   // accumulator columns per epilogue warp
+constexpr int kTileN = 192;                  // tokens per tile (MMA width <= 192)
+constexpr int kAcc = 2;                      // accumulators in tensor memory
+constexpr int kAStages = 2;                  // A stages in tensor memory: one K group (64 columns) each
+constexpr int kACols = 64;
+constexpr int kACol0 = kAcc * kTileN;        // first A column
+constexpr int kTmemCols = 512;
+constexpr int kBStages = 3;
+constexpr int kBAtom = kTileN * 128;         // 192 rows x 128 bytes (64 fp16 of K)
+constexpr int kBStage = 2 * kBAtom;          // 128 values of K
+constexpr int kRaw = 3;                      // packed weight stages in flight
+constexpr int kStageOut = kTileN * 256;      // output staging: 192 rows x 256 bytes (64 fp32 of h or 128 bf16 of Y)
 constexpr int kRawStage = 128 * 64;          // 128 rows x 64 packed bytes (128 codes)
-constexpr int kSmemTc =
-    kNS * kStage + kRaw * kRawStage + 128 * 4 + 128 * 4 + (kMaxSlotsTc + 16) * 4 + 256 + 1024;
+constexpr int kMaxSlotsTc = kTcMaxSlots + 1;
+// Shared-memory layout (byte offsets from the 1024-aligned base), one region after another.
+constexpr int kOffB = 0;                                        // [kBStages][2 atoms][192 rows][128 B]
+constexpr int kOffRaw = kOffB + kBStages * kBStage;             // [kRaw][128 rows][64 B], 64-byte swizzle
+constexpr int kOffOut = kOffRaw + kRaw * kRawStage;             // [192 rows][256 B] output tile staging
+constexpr int kOffColp = kOffOut + kStageOut;                   // int [2][192]: pair rows of the item (two items)
+constexpr int kOffColf = kOffColp + 2 * kTileN * 4;             // float [2][192]: their scales
+constexpr int kOffPrefix = kOffColf + 2 * kTileN * 4;           // int [kMaxSlotsTc + 1]: items before each slot
+constexpr int kOffBars = kOffPrefix + ((kMaxSlotsTc + 1) * 4 + 7) / 8 * 8;  // mbarriers, then small words
+constexpr int kBarWords = 2 * kAStages + 2 * kBStages + 2 * kAcc + 1;
+constexpr int kOffMisc = kOffBars + 8 * kBarWords;              // tmem holder, abort flag, warp sums
+constexpr int kSmemUsed = kOffMisc + 4 * (2 + 18);             // tmem holder, abort flag, 18 warp sums
+constexpr int kSmemTc = kSmemUsed + 1024;                      // + room to align the base to 1024 bytes
 constexpr uint64_t kWaitNs = 2000000000ull;
-static_assert(kAcc * 128 + kNS * kACols <= kTmemCols, "tensor-memory columns");
+static_assert(kAcc * kTileN + kAStages * kACols <= kTmemCols, "tensor-memory columns");
+static_assert(kEpiWarps * kColsW == 4 * kTileN, "epilogue warps cover the tile");
+static_assert(kSmemTc <= 227 * 1024, "shared memory");
+static_assert(kOffRaw % 1024 == 0 && kOffOut % 16 == 0 && kOffBars % 8 == 0, "region alignment");
+static_assert(kTcThreads / 32 + 1 <= 18, "warp sums fit the small words");
+static_assert(kRawStage == 128 * 64, "raw stage: 128 rows of 64 packed bytes");
 
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
@@ -96,6 +129,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
 struct Ctl {
@@ -135,7 +171,7 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
 }
 
 // kind::f16 instruction descriptor: fp32 accumulator, fp16 A and B, both
-// K-major, M = 128, N = n (a multiple of 16, at most 128).
+// K-major, M = 128, N = n (a multiple of 16).
 __device__ __forceinline__ uint32_t idesc_f16(int n) {
     return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | ((128u >> 4) << 24);
 }
@@ -148,10 +184,7 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t d, uint32_t a_tmem, uint64_t
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
 }
 
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-// TMA: one box (64 fp16 x 128 rows from column x, row y) -> 16 KB of shared memory.
+// TMA: 2-D box at (x, y) of `map` -> shared memory, completion counted on `bar`.
 __device__ __forceinline__ void tma_tile2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
@@ -159,7 +192,6 @@ __device__ __forceinline__ void tma_tile2d(void* dst, const CUtensorMap* map, in
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
-
 // SiLU in fast fp32 (hardware exp2 approximation and fast reciprocal divide,
 // a few ulp from z / (1 + exp(-z))).
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
@@ -171,17 +203,15 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+// 16 consecutive 32-bit tensor-memory columns of this thread's lane (no wait).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
-        "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
         : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
-          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
-          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
 __device__ __forceinline__ float ld_nc_f32(const float* p) {
     float v;
@@ -189,23 +219,18 @@ __device__ __forceinline__ float ld_nc_f32(const float* p) {
     return v;
 }
 
-// 64 consecutive 32-bit tensor-memory columns of this thread's lane <- v; waits for the store.
-__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&v)[64]) {
+// 32 consecutive 32-bit tensor-memory columns of this thread's lane <- v (no wait).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,"
-        "%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
-        "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};\n" ::"r"(taddr),
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+        "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
         "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
         "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]), "r"(v[32]), "r"(v[33]), "r"(v[34]), "r"(v[35]), "r"(v[36]),
-        "r"(v[37]), "r"(v[38]), "r"(v[39]), "r"(v[40]), "r"(v[41]), "r"(v[42]), "r"(v[43]), "r"(v[44]), "r"(v[45]),
-        "r"(v[46]), "r"(v[47]), "r"(v[48]), "r"(v[49]), "r"(v[50]), "r"(v[51]), "r"(v[52]), "r"(v[53]), "r"(v[54]),
-        "r"(v[55]), "r"(v[56]), "r"(v[57]), "r"(v[58]), "r"(v[59]), "r"(v[60]), "r"(v[61]), "r"(v[62]), "r"(v[63])
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
-
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
 // Eight packed int4 codes (element e at bits 4e) -> fp16 pairs (0,4) (1,5) (2,6) (3,7).
 // A nibble n of a two's-complement code c satisfies n ^ 8 = c + 8.  Placed in
@@ -213,7 +238,7 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&v)[64
 // subtracting 1032 leaves c; placed 4 bits higher it gives 1024 + 16 (c + 8),
 // and x / 16 - 72 = c (one exact fma).  Each (w & mask) ^ (0x6400.. | 8-bit)
 // is a single three-input logic op.
-__device__ __forceinline__ uint4 unpack_int4_f16(uint32_t w) {
+__device__ __forceinline__ void unpack_int4_f16(uint32_t w, uint32_t* r) {
     const __half2 sub = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
     const __half2 s16 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));   // 1/16
     const __half2 b72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));   // -72
@@ -223,7 +248,6 @@ __device__ __forceinline__ uint4 unpack_int4_f16(uint32_t w) {
     p[1] = (w & 0x00F000F0u) ^ 0x64806480u;
     p[2] = (w8 & 0x000F000Fu) ^ 0x64086408u;
     p[3] = (w8 & 0x00F000F0u) ^ 0x64806480u;
-    uint32_t r[4];
     const __half2 h0 = __hsub2(*reinterpret_cast<const __half2*>(&p[0]), sub);
     const __half2 h1 = __hfma2(*reinterpret_cast<const __half2*>(&p[1]), s16, b72);
     const __half2 h2 = __hsub2(*reinterpret_cast<const __half2*>(&p[2]), sub);
@@ -232,43 +256,57 @@ __device__ __forceinline__ uint4 unpack_int4_f16(uint32_t w) {
     r[1] = *reinterpret_cast<const uint32_t*>(&h1);
     r[2] = *reinterpret_cast<const uint32_t*>(&h2);
     r[3] = *reinterpret_cast<const uint32_t*>(&h3);
-    return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-
-__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n)); }
+// Named barriers of n threads.  The non-aligned forms (barrier.sync / barrier.red, not bar.*):
+// they are reached right after per-thread bounded spin waits, so a warp may arrive diverged, and
+// the compiler does not reconverge a warp before an inline-asm barrier.
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("barrier.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+}
 
 // Named barrier that also ORs a predicate over its threads: every thread gets the same answer.
 __device__ __forceinline__ bool named_bar_or(int id, int n, bool v) {
     uint32_t r;
     asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.u32 p, %3, 0;\n bar.red.or.pred q, %1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %3, 0;\n barrier.red.or.pred q, %1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
         : "=r"(r)
         : "r"(id), "r"(n), "r"(v ? 1u : 0u)
         : "memory");
     return r != 0;
 }
 
+
+
 struct Item {
     int slot, tt, mt, row0, ntok;
 };
 
+// Walks this CTA's (item, K step) uses in order.
+struct Cursor {
+    int item, ks;
+};
+
 template <TcMode MODE>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_mt, const __grid_constant__ CUtensorMap bmap) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_gemm_kernel(TcArgs a, int n_mt, const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* stages = smem;
-    uint8_t* raw = smem + kNS * kStage;                           // [kRaw][128][64] packed weight rows
-    float* colf = reinterpret_cast<float*>(raw + kRaw * kRawStage);  // [128] B-row scales of the item
-    int* colp = reinterpret_cast<int*>(colf + 128);               // [128] pair rows of the item
-    int* prefix = colp + 128;                                     // [kMaxSlotsTc + 1] items before each slot
-    uint64_t* bars = reinterpret_cast<uint64_t*>(prefix + kMaxSlotsTc + 16);
-    uint64_t* full = bars;
-    uint64_t* empty = bars + kNS;
-    uint64_t* accf = bars + 2 * kNS;
-    uint64_t* acce = accf + kAcc;
+    uint8_t* bstages = smem + kOffB;
+    uint8_t* raw = smem + kOffRaw;
+    uint8_t* outst = smem + kOffOut;
+    int* colp_buf = reinterpret_cast<int*>(smem + kOffColp);
+    float* colf_buf = reinterpret_cast<float*>(smem + kOffColf);
+    int* prefix = reinterpret_cast<int*>(smem + kOffPrefix);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+    uint64_t* a_full = bars;                     // [kAStages] 128 producer arrivals
+    uint64_t* a_empty = a_full + kAStages;       // [kAStages] MMA commit
+    uint64_t* b_full = a_empty + kAStages;       // [kBStages] expect-tx arrival + TMA bytes
+    uint64_t* b_empty = b_full + kBStages;       // [kBStages] MMA commit
+    uint64_t* accf = b_empty + kBStages;         // [kAcc] MMA commit at a group's end
+    uint64_t* acce = accf + kAcc;                // [kAcc] epilogue arrivals
     uint64_t* done = acce + kAcc;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     int* warp_sums = abort_flag + 1;  // [kTcThreads / 32 + 1]
 
@@ -280,10 +318,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
     const Ctl ctl{abort_flag, a.hdr};
 
     if (tid == 0) {
-        for (int s = 0; s < kNS; ++s) {
-            // 128 producer arrivals (A in tensor memory) + the TMA tiles' expect-tx arrival (B)
-            mbar_init(full + s, 129);
-            mbar_init(empty + s, 1);
+        for (int s = 0; s < kAStages; ++s) {
+            mbar_init(a_full + s, kProdThreads);
+            mbar_init(a_empty + s, 1);
+        }
+        for (int s = 0; s < kBStages; ++s) {
+            mbar_init(b_full + s, 1);  // expect-tx arrival + the TMA bytes
+            mbar_init(b_empty + s, 1);
         }
         for (int b = 0; b < kAcc; ++b) {
             mbar_init(accf + b, 1);
@@ -293,7 +334,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp) {  // (a converged warp; warp-aligned alloc)
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tmem_holder)),
                      "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
@@ -356,136 +397,138 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
         if (gateup) return ((r & 1) ? a.I : 0) + 64 * mt + (r >> 1);
         return static_cast<int64_t>(128) * mt + r;
     };
-
-    if (warp >= kEpiWarps && warp < kMmaWarp) {
-        // ------------------------------------------------------------ producers
-        // Each thread owns tile row pt.  The packed weight bytes for use
-        // u + kRaw are copied (cp.async) into the raw ring while use u is
-        // unpacked, so the unpack never waits for HBM.  The copies are
-        // coalesced within the warp (4 lanes per row, 8 rows of 64 contiguous
-        // bytes per instruction), so a lane waits for its own copies and then
-        // syncs the warp before reading its row.
-        const int pt = tid - kEpiThreads;
-        const int pw = warp - kEpiWarps;
-        // 16-byte chunk q of row pt sits at chunk q ^ rsw: eight consecutive rows
-        // (64 bytes apart) then hit eight different bank groups
-        const int rsw = (pt >> 1) & 3;
-        int l_item = blockIdx.x, l_ks = 0;  // next use whose raw bytes are fetched
-        const uint8_t* l_slot = nullptr;    // its slot's packed rows
-        int l_mt = 0;
-        if (l_item < total) {
-            const Item it = decode_item(l_item);
-            l_slot = a.w + static_cast<int64_t>(it.slot) * rows_per_slot * (K / 2);
-            l_mt = it.mt;
+    auto advance = [&](Cursor& c) {
+        if (++c.ks == ksteps) {
+            c.ks = 0;
+            c.item += gridDim.x;
         }
-        int l_use = 0;
+    };
+
+    if (warp >= kProdWarp0 && warp < kMmaWarp) {
+        // ------------------------------------------------------------ producers
+        // Thread pt owns tile row pt (TMEM lane pt).  Each warp copies the
+        // packed bytes of its 32 rows for use u + kRaw - 1 into the raw slot
+        // of use u - 1 (which every lane of the warp has read: the warp is
+        // past it), so the unpack never waits for HBM.
+        const int pw = warp - kProdWarp0;
+        const int pt = 32 * pw + lane;
+        const int rsw = (pt >> 1) & 3;  // 16-byte chunk q of row r sits at q ^ ((r >> 1) & 3): no bank conflicts
         const int piece = lane & 3;
-        auto fetch_next = [&]() {
-            if (l_item < total) {
+        Cursor lc{static_cast<int>(blockIdx.x), 0};
+        int l_use = 0, l_dec = -1;
+        Item l_it{};
+        auto fetch = [&]() {  // this warp's rows of use l_use into raw slot l_use % kRaw (one commit group)
+            if (lc.item < total) {
+                if (lc.item != l_dec) {
+                    l_it = decode_item(lc.item);
+                    l_dec = lc.item;
+                }
+                const uint8_t* wslot = a.w + static_cast<int64_t>(l_it.slot) * rows_per_slot * (K / 2);
                 uint8_t* dst = raw + (l_use % kRaw) * kRawStage;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {  // rows 32 pw + 8 q .. + 7, 4 lanes per row
+                for (int q = 0; q < 4; ++q) {  // rows 32 pw + 8 q .. + 7, four lanes per row (64 contiguous bytes)
                     const int row = 32 * pw + 8 * q + (lane >> 2);
-                    const int rs = (row >> 1) & 3;
-                    cp_async16(dst + row * 64 + 16 * (piece ^ rs),
-                               l_slot + weight_row(l_mt, row) * (K / 2) + 64 * l_ks + 16 * piece);
+                    cp_async16(dst + row * 64 + 16 * (piece ^ ((row >> 1) & 3)),
+                               wslot + weight_row(l_it.mt, row) * (K / 2) + 64 * lc.ks + 16 * piece);
                 }
-                ++l_use;
-                if (++l_ks == ksteps) {
-                    l_ks = 0;
-                    l_item += gridDim.x;
-                    if (l_item < total) {
-                        const Item it = decode_item(l_item);
-                        l_slot = a.w + static_cast<int64_t>(it.slot) * rows_per_slot * (K / 2);
-                        l_mt = it.mt;
-                    }
-                }
+                advance(lc);
             }
-            cp_async_commit();  // one group per call, empty or not, so the group count stays aligned
+            cp_async_commit();  // one group per use, empty or not, so the group count stays aligned
+            ++l_use;
         };
-#pragma unroll
-        for (int d = 0; d < kRaw; ++d) fetch_next();
-        int use = 0;
         bool ok = true;
-        for (int item = blockIdx.x; item < total; item += gridDim.x) {
-            const Item it = decode_item(item);
-            if (named_bar_or(2, 128, !ok)) break;  // the four producer warps give up together
+        for (int d = 0; d < kRaw - 1; ++d) fetch();
+        int use = 0;
+        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
             for (int ks = 0; ks < ksteps; ++ks, ++use) {
-                const int s = use % kNS;
-                if (!wait_bar(empty + s, ((use / kNS) & 1) ^ 1, ctl)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();  // the stage's previous MMAs (which read its A columns) are complete
-                uint8_t* Bs = stages + s * kStage;
-                // B, the 128 token rows of the stage (contiguous fp16 rows): two 2-D
-                // TMA tiles, one per 128-byte-swizzled atom, issued by producer warp 0
-                if (warp == kEpiWarps && lane == 0) {
-                    mbar_expect_tx(full + s, kStage);
-#pragma unroll
-                    for (int at = 0; at < 2; ++at) tma_tile2d(Bs + at * kAtom, &bmap, 128 * ks + 64 * at, it.row0, full + s);
-                }
-                cp_async_wait<kRaw - 1>();  // this lane's copies for this use (issued kRaw calls ago) have landed
-                __syncwarp();               // ... and the other lanes' copies of this warp's rows
+                fetch();                      // use + kRaw - 1 into the slot of use - 1
+                cp_async_wait<kRaw - 1>();    // this lane's copies for this use have landed
+                __syncwarp();                 // ... and the other lanes' copies of this warp's rows
                 const uint4* rp = reinterpret_cast<const uint4*>(raw + (use % kRaw) * kRawStage + pt * 64);
                 uint4 rw[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) rw[q] = rp[q ^ rsw];
-                // unpacked row -> this thread's tensor-memory lane, 64 columns of
-                // fp16 pairs (column c holds K positions 2c, 2c + 1 of the stage)
-                uint32_t av[64];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t words[4] = {rw[q].x, rw[q].y, rw[q].z, rw[q].w};
-#pragma unroll
-                    for (int wi = 0; wi < 4; ++wi) {
-                        const uint4 u4 = unpack_int4_f16(words[wi]);
-                        const int c = 4 * (4 * q + wi);
-                        av[c] = u4.x;
-                        av[c + 1] = u4.y;
-                        av[c + 2] = u4.z;
-                        av[c + 3] = u4.w;
-                    }
+                const int s = use % kAStages;
+                // warp-uniform outcome: the tensor-memory stores below are warp-aligned
+                if (!__all_sync(0xffffffffu, wait_bar(a_empty + s, ((use / kAStages) & 1) ^ 1, ctl))) {
+                    ok = false;
+                    break;
                 }
-                tmem_st64(tmem + (static_cast<uint32_t>(32 * (warp - kEpiWarps)) << 16) + kAcc * 128 + kACols * s, av);
-                // the raw slot just consumed is refilled kRaw uses ahead, after every
-                // lane of the warp has read its row from it
-                __syncwarp();
-                fetch_next();
+                tc_fence_after();  // the stage's previous MMAs (which read its A columns) are complete
+                // unpacked row -> this thread's tensor-memory lane, 64 columns of fp16
+                // pairs (column c holds K positions 2c, 2c + 1 of the stage)
+                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * pw) << 16) + kACol0 + kACols * s;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t av[32];
+                    const uint32_t words[8] = {rw[2 * h2].x, rw[2 * h2].y, rw[2 * h2].z, rw[2 * h2].w,
+                                               rw[2 * h2 + 1].x, rw[2 * h2 + 1].y, rw[2 * h2 + 1].z, rw[2 * h2 + 1].w};
+#pragma unroll
+                    for (int wi = 0; wi < 8; ++wi) unpack_int4_f16(words[wi], av + 4 * wi);
+                    tmem_st32(ta + 32 * h2, av);
+                }
+                tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(full + s);
+                mbar_arrive(a_full + s);
             }
         }
-        cp_async_wait<0>();
+        cp_async_wait<0>();  // no copy is left in flight when the CTA leaves
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ MMA issue + B tiles (lane 0)
+        // Use u: wait for its B tiles, a free accumulator (at a group's start)
+        // and its A stage; issue the 8 MMAs; then the B tiles of use u + 2 into
+        // the stage use u - 1 read.
         if (lane == 0) {
+            Cursor bc{static_cast<int>(blockIdx.x), 0};
+            int b_use = 0, b_issued = 0, b_dec = -1;
+            Item b_it{};
+            auto issue_b = [&]() -> bool {  // the B rows of use b_use into stage b_use % kBStages
+                if (bc.item < total) {
+                    const int s = b_use % kBStages;
+                    if (!wait_bar(b_empty + s, ((b_use / kBStages) & 1) ^ 1, ctl)) return false;
+                    if (bc.item != b_dec) {
+                        b_it = decode_item(bc.item);
+                        b_dec = bc.item;
+                    }
+                    uint8_t* Bs = bstages + s * kBStage;
+                    mbar_expect_tx(b_full + s, kBStage);
+                    tma_tile2d(Bs, &bmap, 128 * bc.ks, b_it.row0, b_full + s);
+                    tma_tile2d(Bs + kBAtom, &bmap, 128 * bc.ks + 64, b_it.row0, b_full + s);
+                    advance(bc);
+                    b_issued = b_use + 1;
+                }
+                ++b_use;
+                return true;
+            };
+            bool ok = issue_b() && issue_b();
             int use = 0, grp = 0;
-            bool ok = true;
             for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
                 const Item it = decode_item(item);
                 const uint32_t idesc = idesc_f16((it.ntok + 15) & ~15);
                 for (int ks = 0; ks < ksteps; ++ks, ++use) {
-                    const int s = use % kNS;
-                    const int sub = ks % spg;
-                    const int b = grp % kAcc;
-                    if (!wait_bar(full + s, (use / kNS) & 1, ctl) ||
-                        (sub == 0 && !wait_bar(acce + b, ((grp / kAcc) & 1) ^ 1, ctl))) {
+                    const int sa = use % kAStages, sb = use % kBStages, sub = ks % spg, b = grp % kAcc;
+                    if (!wait_bar(b_full + sb, (use / kBStages) & 1, ctl) ||
+                        (sub == 0 && !wait_bar(acce + b, ((grp / kAcc) & 1) ^ 1, ctl)) ||
+                        !wait_bar(a_full + sa, (use / kAStages) & 1, ctl)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t b0 = smem_u32(stages + s * kStage);
-                    const uint32_t ta = tmem + kAcc * 128 + kACols * s;
+                    const uint32_t b0 = smem_u32(bstages + sb * kBStage);
+                    const uint32_t tam = tmem + kACol0 + kACols * sa;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {  // K = 16 per MMA: 8 A columns, 32 B of a B row
-                        const uint32_t off = (kk >> 2) * kAtom + 32 * (kk & 3);
-                        mma_f16_ta(tmem + b * 128, ta + 8 * kk, sdesc(b0 + off), idesc, (sub > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(empty + s);
+                    for (int kk = 0; kk < 8; ++kk)  // K = 16 per MMA: 8 A columns, 32 bytes of a B row
+                        mma_f16_ta(tmem + b * kTileN, tam + 8 * kk, sdesc(b0 + (kk >> 2) * kBAtom + 32 * (kk & 3)), idesc,
+                                   (sub > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(a_empty + sa);
+                    mma_commit(b_empty + sb);
                     if (sub == spg - 1) {
                         mma_commit(accf + b);
                         ++grp;
+                    }
+                    if (!issue_b()) {
+                        ok = false;
+                        break;
                     }
                 }
             }
@@ -497,28 +540,58 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                     break;
                 }
             }
+            // after an abort: let the B tiles still in flight land before the CTA leaves
+            for (int u = use; u < b_issued; ++u) {
+                const uint64_t t1 = global_ns();
+                while (!mbar_try_wait(b_full + u % kBStages, (u / kBStages) & 1) && global_ns() - t1 < kWaitNs) {
+                }
+            }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
         // warp w: TMEM lanes 32 (w % 4) .. +31 (tile rows), columns 64 (w / 4) .. +63
-        const int quarter = warp & 3, c_base = kHalfN * (warp >> 2);
+        const int quarter = warp & 3, c_base = kColsW * (warp >> 2);
         const int r = 32 * quarter + lane;  // tile row
         int grp = 0;
-        for (int item = blockIdx.x; item < total; item += gridDim.x) {
-            const Item it = decode_item(item);
-            if (tid < it.ntok) {
-                const int p = it.row0 + tid;
-                colp[tid] = p;
-                if (!partials) colf[tid] = gateup ? a.b_scale[a.b_row ? a.b_row[p] : p] : a.b_scale[p];
+        // the pair rows and column scales of an item are loaded one item ahead (their global
+        // loads then overlap the previous item's groups) into the other half of colp / colf
+        auto load_cols = [&](int item, int& p_out, float& f_out) {
+            p_out = -1;
+            if (item < total && tid < kTileN) {
+                const Item nx = decode_item(item);
+                if (tid < nx.ntok) {
+                    const int p = nx.row0 + tid;
+                    p_out = p;
+                    f_out = MODE == TcMode::kGateUp ? __ldg(a.b_scale + __ldg(a.row_token + p))
+                                                    : (partials ? 0.f : __ldg(a.b_scale + p));
+                }
             }
+        };
+        {
+            int p0 = -1;
+            float f0 = 0.f;
+            load_cols(blockIdx.x, p0, f0);
+            if (p0 >= 0) {
+                colp_buf[tid] = p0;
+                colf_buf[tid] = f0;
+            }
+        }
+        int j = 0;  // this CTA's item count
+        for (int item = blockIdx.x; item < total; item += gridDim.x, ++j) {
+            const Item it = decode_item(item);
+            int* colp = colp_buf + (j & 1) * kTileN;
+            float* colf = colf_buf + (j & 1) * kTileN;
+            int np = -1;
+            float nf = 0.f;
+            load_cols(item + gridDim.x, np, nf);  // the next item's (consumed after this one)
             named_bar(1, kEpiThreads);
-            const int nloc = min(kHalfN, it.ntok - c_base);  // this warp's live columns (may be <= 0)
+            const int nloc = min(kColsW, it.ntok - c_base);  // this warp's live columns (may be <= 0)
             const int64_t wrow = weight_row(it.mt, r);
             const float* srow = a.ws + (static_cast<int64_t>(it.slot) * rows_per_slot + wrow) * ngrp;
-            float acc[kHalfN];
+            float acc[kColsW];
 #pragma unroll
-            for (int c = 0; c < kHalfN; ++c) acc[c] = 0.f;
+            for (int c = 0; c < kColsW; ++c) acc[c] = 0.f;
             bool ok = true;
             // group scales two groups ahead (volatile loads: issued before the waits)
             float sc1 = partials ? 0.f : ld_nc_f32(srow), sc2 = (partials || ngrp < 2) ? 0.f : ld_nc_f32(srow + 1);
@@ -527,54 +600,92 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
                 const float sc = sc1;
                 sc1 = sc2;
                 if (!partials && gq + 2 < ngrp) sc2 = ld_nc_f32(srow + gq + 2);
-                if (!wait_bar(accf + b, (grp / kAcc) & 1, ctl)) {
+                if (!__all_sync(0xffffffffu, wait_bar(accf + b, (grp / kAcc) & 1, ctl))) {  // loads below are warp-aligned
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const uint32_t tb = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + b * kTileN + c_base;
+                if (partials) {
+                    uint32_t v[16];
 #pragma unroll
-                for (int i = 0; i < kHalfN / 32; ++i) {
-                    if (32 * i >= nloc) break;
-                    uint32_t v[32];
-                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + b * 128 + c_base + 32 * i, v);
-                    if (partials) {
+                    for (int i = 0; i < kColsW / 16; ++i) {
+                        if (16 * i >= nloc) break;
+                        tmem_ld16(tb + 16 * i, v);
+                        tmem_ld_wait();
                         int32_t* dst = a.partials + wrow * ngrp + gq;
 #pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            if (32 * i + c < nloc)
-                                dst[static_cast<int64_t>(colp[c_base + 32 * i + c]) * rows_per_slot * ngrp] =
+                        for (int c = 0; c < 16; ++c)
+                            if (16 * i + c < nloc)
+                                dst[static_cast<int64_t>(colp[c_base + 16 * i + c]) * rows_per_slot * ngrp] =
                                     __float2int_rn(__uint_as_float(v[c]));
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) acc[32 * i + c] = fmaf(__uint_as_float(v[c]), sc, acc[32 * i + c]);
                     }
+                    tc_fence_before();
+                    mbar_arrive(acce + b);
+                } else {
+                    // 16 columns at a time (registers: 64 running sums + 16 loaded values)
+#pragma unroll
+                    for (int i = 0; i < kColsW / 16; ++i) {
+                        if (16 * i < nloc) {
+                            uint32_t v[16];
+                            tmem_ld16(tb + 16 * i, v);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) acc[16 * i + c] = fmaf(__uint_as_float(v[c]), sc, acc[16 * i + c]);
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(acce + b);
                 }
-                tc_fence_before();
-                mbar_arrive(acce + b);
             }
-            if (ok && MODE == TcMode::kGateUp) {
-                // lanes 2j (gate) and 2j+1 (up) hold index i for every column: for a
-                // column pair (c0, c1) the even lane finishes c0 and the odd lane c1
-                const int64_t i = 64 * it.mt + (r >> 1);
-                const bool odd = r & 1;
+            // every epilogue thread learns whether any gave up before the tile's shared output work
+            if (named_bar_or(1, kEpiThreads, !ok)) break;
+            if (MODE == TcMode::kGateUp || MODE == TcMode::kDown) {
+                // the tile's output rows (one per token column, 256 bytes each) are staged in shared
+                // memory and written with 16-byte stores: rows of h [P][I] (64 fp32 from 64 i) or of the
+                // bf16 Y [P][H] (128 n)
+                if (MODE == TcMode::kGateUp) {
+                    // lanes 2j (gate) and 2j+1 (up) hold index i for every column: for a
+                    // column pair (c0, c1) the even lane finishes c0 and the odd lane c1
+                    const int il = r >> 1;  // i - 64 mt
+                    const bool odd = r & 1;
 #pragma unroll
-                for (int c0 = 0; c0 < kHalfN; c0 += 2) {
-                    const int c = c0 + (odd ? 1 : 0);
-                    const float other = __shfl_xor_sync(0xffffffffu, odd ? acc[c0] : acc[c0 + 1], 1);
-                    const float gate = odd ? other : acc[c0], up = odd ? acc[c0 + 1] : other;
-                    if (c < nloc) {
-                        const float xs = colf[c_base + c];
-                        a.h[static_cast<int64_t>(colp[c_base + c]) * a.I + i] = silu_fast(gate * xs) * (up * xs);
+                    for (int c0 = 0; c0 < kColsW; c0 += 2) {
+                        const int c = c0 + (odd ? 1 : 0);
+                        const float other = __shfl_xor_sync(0xffffffffu, odd ? acc[c0] : acc[c0 + 1], 1);
+                        const float gate = odd ? other : acc[c0], up = odd ? acc[c0 + 1] : other;
+                        if (c < nloc) {
+                            const float xs = colf[c_base + c];
+                            reinterpret_cast<float*>(outst)[(c_base + c) * 64 + il] = silu_fast(gate * xs) * (up * xs);
+                        }
                     }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kColsW; ++c)
+                        if (c < nloc)
+                            reinterpret_cast<__nv_bfloat16*>(outst)[(c_base + c) * 128 + r] =
+                                __float2bfloat16_rn(acc[c] * colf[c_base + c]);
                 }
-            } else if (ok && MODE == TcMode::kDown) {
+                named_bar(1, kEpiThreads);
+                const int64_t ld = MODE == TcMode::kGateUp ? a.I * 4 : a.H * 2;  // global row pitch, bytes
+                const int64_t col0 = 256 * static_cast<int64_t>(it.mt);         // first byte of the tile in a row
+                uint8_t* gbase = MODE == TcMode::kGateUp ? reinterpret_cast<uint8_t*>(a.h) : reinterpret_cast<uint8_t*>(a.yb);
+                for (int q = tid; q < it.ntok * 16; q += kEpiThreads) {
+                    const int row = q >> 4, ch = q & 15;
+                    *reinterpret_cast<uint4*>(gbase + static_cast<int64_t>(colp[row]) * ld + col0 + 16 * ch) =
+                        reinterpret_cast<const uint4*>(outst)[q];
+                }
+            } else if (MODE == TcMode::kDownY) {
                 const int64_t n = 128 * it.mt + r;
 #pragma unroll
-                for (int c = 0; c < kHalfN; ++c)
+                for (int c = 0; c < kColsW; ++c)
                     if (c < nloc) a.y[static_cast<int64_t>(colp[c_base + c]) * a.H + n] = acc[c] * colf[c_base + c];
             }
-            // colf / colp are reused by the next item; leave together if any thread gave up
-            if (named_bar_or(1, kEpiThreads, !ok)) break;
+            if (np >= 0) {
+                colp_buf[((j + 1) & 1) * kTileN + tid] = np;
+                colf_buf[((j + 1) & 1) * kTileN + tid] = nf;
+            }
+            named_bar(1, kEpiThreads);  // the staging area is reused by the next item
         }
     }
 
@@ -587,9 +698,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(TcArgs a, int n_
 }
 
 // x_q int8 -> fp16 rows in the engine's K order (pairs (0,4)(1,5)(2,6)(3,7) per
-// 8 values); out row r is token row_token[r] (null: r), zeros for a token
-// outside [0, T).  Idx: the type of the element index 8 i (32-bit when
-// rows * H fits, which keeps the row/column split a 32-bit division).
+// 8 values); out row r is token row_token[r], zeros for a token outside
+// [0, T).  Idx: the type of the element index 8 i (32-bit when rows * H fits,
+// which keeps the row/column split a 32-bit division).
 template <typename Idx>
 __global__ void prep_x16_kernel(const int8_t* __restrict__ x, int64_t T, int64_t H, const int32_t* __restrict__ row_token,
                                 int64_t n8, __half* __restrict__ out) {
@@ -597,7 +708,7 @@ __global__ void prep_x16_kernel(const int8_t* __restrict__ x, int64_t T, int64_t
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const Idx i8 = static_cast<Idx>(8 * i), Hx = static_cast<Idx>(H);
         const int64_t r = static_cast<int64_t>(i8 / Hx), c = static_cast<int64_t>(i8 % Hx);
-        const int64_t t = row_token ? row_token[r] : r;
+        const int64_t t = row_token[r];
         uint2 v = make_uint2(0u, 0u);
         if (t >= 0 && t < T) v = *reinterpret_cast<const uint2*>(x + t * H + c);
         const int8_t* b = reinterpret_cast<const int8_t*>(&v);
@@ -657,32 +768,64 @@ __global__ void prep_h16_kernel(const float* __restrict__ h, uint32_t* __restric
     }
 }
 
-// Tensor map of contiguous B rows (fp16 [b_rows][K]) for the TMA unit:
-// boxes of 64 columns (128 bytes, the swizzle span) by 128 rows; rows past
-// the end read zeros.
-cudaError_t make_bmap(const TcArgs& a, CUtensorMap* map) {
-    using Encode = PFN_cuTensorMapEncodeTiled_v12000;
+using Encode = PFN_cuTensorMapEncodeTiled_v12000;
+
+cudaError_t get_encode(Encode* out) {
     static Encode encode = nullptr;
     static std::mutex mu;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!encode) {
-            void* fn = nullptr;
-            cudaDriverEntryPointQueryResult q{};
-            cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-            if (e != cudaSuccess) return e;
-            if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
-            encode = reinterpret_cast<Encode>(fn);
-        }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess) return e;
+        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
+        encode = reinterpret_cast<Encode>(fn);
     }
+    *out = encode;
+    return cudaSuccess;
+}
+
+// Tensor map of the B rows of one launch: fp16 [b_rows][K], boxes of 64 values by 192 rows,
+// 128-byte swizzle; rows past the end read zeros.
+cudaError_t make_bmap(const TcArgs& a, CUtensorMap* bmap) {
+    Encode encode = nullptr;
+    if (cudaError_t e = get_encode(&encode); e != cudaSuccess) return e;
+    const cuuint32_t elem[2] = {1, 1};
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.b_rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K) * 2};
-    const cuuint32_t box[2] = {64, 128};
-    const cuuint32_t elem[2] = {1, 1};
-    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(a.b), dims, strides, box, elem,
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTileN)};
+    const CUresult r = encode(bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(a.b), dims, strides, box, elem,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Fixed-order combine from bf16 Y: one thread per (token, 8 output columns).
+__global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* __restrict__ y,
+                                                           const float* __restrict__ wts, const int32_t* __restrict__ inv,
+                                                           int64_t T, int64_t H, int64_t k, int64_t S,
+                                                           float* __restrict__ out) {
+    const int64_t H8 = H / 8, Tk = T * k, total = T * H8;
+    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = idx / H8, n = (idx % H8) * 8;
+        float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        auto add_row = [&](int64_t row, float wj) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + row * H + n));
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                o[2 * e] = fmaf(wj, __uint_as_float(u[e] << 16), o[2 * e]);
+                o[2 * e + 1] = fmaf(wj, __uint_as_float(u[e] & 0xFFFF0000u), o[2 * e + 1]);
+            }
+        };
+        for (int64_t j = 0; j < k; ++j) add_row(inv[t * k + j], wts[t * k + j]);
+        for (int64_t sh = 0; sh < S; ++sh) add_row(Tk + sh * T + t, 1.0f);
+        float4* dst = reinterpret_cast<float4*>(out + t * H + n);
+        dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+    }
 }
 
 template <TcMode MODE>
@@ -714,11 +857,16 @@ bool tc_supported(int64_t H, int64_t I, int64_t g) {
 
 cudaError_t launch_tc_gemm(TcMode mode, const TcArgs& a, cudaStream_t st) {
     if (a.n_slots < 1 || a.n_slots > kTcMaxSlots) return cudaErrorInvalidValue;
+    // the weight rows are addressed as one 2-D tensor of int32 row coordinates
+    if (static_cast<int64_t>(a.n_slots) * a.rows_per_slot >= (int64_t(1) << 31) || a.b_rows < 1 ||
+        a.b_rows >= (int64_t(1) << 31))
+        return cudaErrorInvalidValue;
     const bool gateup = mode == TcMode::kGateUp || mode == TcMode::kGateUpPartials;
     const int n_mt = static_cast<int>(gateup ? a.I / 64 : a.H / 128);
     switch (mode) {
         case TcMode::kGateUp: return launch_mode_tc<TcMode::kGateUp>(a, n_mt, st);
         case TcMode::kDown: return launch_mode_tc<TcMode::kDown>(a, n_mt, st);
+        case TcMode::kDownY: return launch_mode_tc<TcMode::kDownY>(a, n_mt, st);
         case TcMode::kGateUpPartials: return launch_mode_tc<TcMode::kGateUpPartials>(a, n_mt, st);
         default: return launch_mode_tc<TcMode::kDownPartials>(a, n_mt, st);
     }
@@ -733,6 +881,15 @@ cudaError_t launch_prep_x16(const int8_t* x_q, int64_t T, int64_t H, const int32
         prep_x16_kernel<uint32_t><<<grid, 256, 0, st>>>(x_q, T, H, row_token, n8, x16);
     else
         prep_x16_kernel<uint64_t><<<grid, 256, 0, st>>>(x_q, T, H, row_token, n8, x16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bf16(const __nv_bfloat16* y, const float* wts, const int32_t* inv, int64_t T, int64_t H,
+                                int64_t k, int64_t S, float* out, cudaStream_t st) {
+    const int64_t total = T * H / 8;
+    if (total == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(num_sms()) * 16);
+    combine_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(y, wts, inv, T, H, k, S, out);
     return cudaGetLastError();
 }
 

@@ -201,7 +201,9 @@ int moe_w4a8_gemm2_partials(const int8_t* h_q, const uint8_t* w2_packed, const m
  * bounded waits (the decode engine's grid barrier or its bulk-copy wait,
  * about one second each) ran out -- the kernels then skip the rest of the
  * work and the output is not valid.  A diagnostic call (it blocks the host);
- * not for the hot loop.
+ * not for the hot loop.  With workspace NULL (workspace_bytes ignored) it
+ * reads the status word of the built-in array of moe_w4a8_forward_noalloc on
+ * the current device, i.e. of the last no-alloc call there.
  */
 int moe_w4a8_device_status(const void* workspace, size_t workspace_bytes, void* stream);
 
@@ -241,9 +243,12 @@ int moe_w4a8_selftest_barrier_timeout(void* workspace, size_t workspace_bytes, v
  * MOE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued (for the 512-expert
  * decode layer, H=2048, I=512, top-10, one shared expert, that is T > ~128).
  *
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before capturing any stream into a
- * CUDA graph.  All calls on a device share the one array: two calls whose
+ * Every call looks up the array's device address on the current device (so
+ * a context that was reset and re-created is served at the array's new
+ * address); the first lookup in a context loads the library's device code,
+ * so make the first call on a device before capturing any stream into a
+ * CUDA graph.  A bounded device wait that ran out inside a no-alloc call is
+ * reported by moe_w4a8_device_status(NULL, 0, stream).  All calls on a device share the one array: two calls whose
  * kernels may overlap on the GPU (different streams without ordering
  * between them) race and produce wrong results; serialise them.  Nothing
  * from a previous call is reused -- each call initialises what it reads.

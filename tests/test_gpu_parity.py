@@ -79,6 +79,23 @@ def test_route_planted_ties():
     _check_route(wE, logits[:50, :32].copy())
 
 
+def test_route_nan_logits_rank_last():
+    """NaN logits rank below every number (ties by index): k distinct experts per token, as the oracle."""
+    rng = np.random.default_rng(9)
+    w = synth.Workload("nan", T=200, H=256, I=128, E=96, S=0, top_k=7, group=64)
+    logits = rng.standard_normal((w.T, w.E)).astype(np.float32)
+    logits[rng.random(logits.shape) < 0.3] = np.nan
+    logits[0, :] = np.nan
+    logits[1, :4] = -np.inf
+    logits[1, 4:] = np.nan
+    got = _route_gpu(w, logits)
+    ids, _ = oracle.route(logits, w.top_k)
+    assert np.array_equal(got["ids"], ids)
+    assert all(len(set(r)) == w.top_k for r in got["ids"].tolist())
+    counts, offsets, perm, inv = oracle.permute(ids, w.E)
+    assert np.array_equal(got["perm"], perm) and np.array_equal(got["inv"], inv)
+
+
 def test_route_all_tokens_to_one_expert():
     w = synth.WORKLOADS["prefill_t8192"].with_tokens(3000)
     logits = synth.make_tokens(w).logits
@@ -135,7 +152,9 @@ def test_gemm1_partials_bit_exact(name, engine):
     got = p1.cpu().numpy()
     for r in range(n):
         ref = oracle.partials(tok.x_q[tokens[r]], bank.w13[slots[r]], w.group)
-        assert np.array_equal(got[r], ref), f"pair {r}: token {tokens[r]} slot {slots[r]}"
+        bad = np.argwhere(got[r] != ref)
+        assert bad.size == 0, (f"pair {r}: token {tokens[r]} slot {slots[r]}: {len(bad)} of {ref.size} differ, "
+                               f"first (row, group) {bad[:6].tolist()}")
 
 
 @pytest.mark.parametrize("name,engine", PARTIALS_CASES)
@@ -159,7 +178,8 @@ def test_gemm2_partials_bit_exact(name, engine):
     got = p2.cpu().numpy()
     for r in range(n):
         ref = oracle.partials(h_q[r], bank.w2[slots[r]], w.group)
-        assert np.array_equal(got[r], ref), f"pair {r}: slot {slots[r]}"
+        bad = np.argwhere(got[r] != ref)
+        assert bad.size == 0, f"pair {r}: slot {slots[r]}: {len(bad)} of {ref.size} differ, first {bad[:6].tolist()}"
 
 
 @pytest.mark.parametrize("name", ALL)
@@ -169,6 +189,13 @@ def test_forward_matches_oracle(name):
     bank = gh.bank_of(w)
     out = gh.run_forward(w, tok)
     sel = gh.sample_tokens(w.T, 48)
+    if w.T > 48:
+        # plus every token routed to the ten least-loaded touched experts (the skewed tail's partial tiles)
+        ids, _ = oracle.route(tok.logits, w.top_k)
+        counts = np.bincount(ids.ravel(), minlength=w.E)
+        tail = [e for e in np.argsort(counts, kind="stable") if counts[e] > 0][:10]
+        extra = np.nonzero(np.isin(ids, tail).any(axis=1))[0]
+        sel = np.union1d(sel, extra)
     ref = gh.oracle_out(w, tok, bank, sel)
     gh.assert_output_close(out[sel], ref, name)
     assert np.all(np.isfinite(out))
@@ -326,6 +353,27 @@ def test_decode_engine_routes_planted_ties(E):
     tok.logits[...] = lg
     out = _forward_engine(w, tok, 1)
     gh.assert_output_close(out, gh.oracle_out(w, tok, gh.bank_of(w)), f"decode ties E={E}")
+
+
+def test_decode_engine_ranks_nan_logits_last():
+    """NaN logits in the decode kernel's own routing: never chosen while k numbers remain, so those tokens
+    match the oracle; a token whose logits are all NaN gets the lowest k experts (NaN weights, NaN output)."""
+    w = synth.Workload("dnan", T=10, H=2048, I=512, E=64, S=1, top_k=6, group=128)
+    tok = synth.make_tokens(w)
+    orig = tok.logits.copy()
+    rng = np.random.default_rng(3)
+    tok.logits[rng.random(tok.logits.shape) < 0.4] = np.nan
+    tok.logits[2, :] = np.nan
+    tok.logits[3, :58] = np.nan  # exactly k numbers left
+    tok.logits[3, 58:] = orig[3, 58:]
+    assert all(np.count_nonzero(~np.isnan(tok.logits[t])) >= w.top_k for t in range(w.T) if t != 2)
+    out = _forward_engine(w, tok, 1)
+    ref = gh.oracle_out(w, tok, gh.bank_of(w))
+    ok = [t for t in range(w.T) if t != 2]
+    gh.assert_output_close(out[ok], ref[ok], "decode engine, NaN logits")
+    assert np.all(np.isnan(out[2])) and np.all(np.isnan(ref[2]))
+    ids, _ = oracle.route(tok.logits, w.top_k)
+    assert ids[2].tolist() == list(range(w.top_k)) and ids[3].tolist() == sorted(ids[3].tolist(), key=lambda e: -tok.logits[3, e])
 
 
 def test_decode_engine_matches_grouped_engine_on_large_bank_shape():

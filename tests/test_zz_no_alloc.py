@@ -30,6 +30,11 @@ def _lib(cuda_lib):
     binding._load()
 
 
+def _same(out, ref, what):
+    """The same kernels on the same inputs: the same bits."""
+    assert np.array_equal(out, ref), f"{what}: no-alloc output differs from moe_w4a8_forward"
+
+
 def _both(w, tok, bank_dev):
     w13, s13, w2, s2 = bank_dev
     d = gh.dims(w)
@@ -50,6 +55,9 @@ def test_noalloc_matches_forward_on_consecutive_calls():
     for batch in (0, 1):
         out, ref = _both(w, synth.make_tokens(w, batch=batch), bank_dev)
         gh.assert_output_close(out, ref.astype(np.float64), f"batch {batch}")
+        _same(out, ref, f"batch {batch}")
+        # the status word of the built-in array (a timed-out device wait would show here)
+        assert binding.moe_w4a8_device_status(None) == 0
 
 
 def test_noalloc_matches_forward_after_a_larger_layer():
@@ -57,9 +65,11 @@ def test_noalloc_matches_forward_after_a_larger_layer():
     w_big = synth.WORKLOADS["decode_t4"].with_tokens(64)
     out, ref = _both(w_big, synth.make_tokens(w_big), gh.device_bank(w_big))
     gh.assert_output_close(out, ref.astype(np.float64), "T=64")
+    _same(out, ref, "T=64")
     w_small = synth.WORKLOADS["tiny"]
     out, ref = _both(w_small, synth.make_tokens(w_small), gh.device_bank(w_small))
     gh.assert_output_close(out, ref.astype(np.float64), "tiny")
+    _same(out, ref, "tiny")
 
 
 def test_noalloc_rejects_layers_beyond_its_array():
