@@ -71,8 +71,9 @@ namespace {
 constexpr int kEpiWarps = 12;                // three per TMEM lane quarter, 64 columns each
 constexpr int kProdWarps = 4;                // one per TMEM lane quarter
 constexpr int kProdWarp0 = kEpiWarps;
-constexpr int kMmaWarp = kEpiWarps + kProdWarps;  // MMA issue and B tiles
-constexpr int kTcThreads = 32 * (kMmaWarp + 1);
+constexpr int kMmaWarp = kEpiWarps + kProdWarps;  // MMA issue and the tensor-memory allocation
+constexpr int kBWarp = kMmaWarp + 1;              // B tiles
+constexpr int kTcThreads = 32 * (kBWarp + 1);
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kProdThreads = 32 * kProdWarps;
 constexpr int kColsW = 64;                   // accumulator columns per epilogue warp
@@ -82,32 +83,31 @@ constexpr int kAStages = 2;                  // A stages in tensor memory: one K
 constexpr int kACols = 64;
 constexpr int kACol0 = kAcc * kTileN;        // first A column
 constexpr int kTmemCols = 512;
-constexpr int kBStages = 3;
+constexpr int kBStages = 4;
 constexpr int kBAtom = kTileN * 128;         // 192 rows x 128 bytes (64 fp16 of K)
 constexpr int kBStage = 2 * kBAtom;          // 128 values of K
 constexpr int kRaw = 3;                      // packed weight stages in flight
-constexpr int kStageOut = kTileN * 256;      // output staging: 192 rows x 256 bytes (64 fp32 of h or 128 bf16 of Y)
 constexpr int kRawStage = 128 * 64;          // 128 rows x 64 packed bytes (128 codes)
 constexpr int kMaxSlotsTc = kTcMaxSlots + 1;
+constexpr int kNumWarps = kTcThreads / 32;
 // Shared-memory layout (byte offsets from the 1024-aligned base), one region after another.
 constexpr int kOffB = 0;                                        // [kBStages][2 atoms][192 rows][128 B]
 constexpr int kOffRaw = kOffB + kBStages * kBStage;             // [kRaw][128 rows][64 B], 64-byte swizzle
-constexpr int kOffOut = kOffRaw + kRaw * kRawStage;             // [192 rows][256 B] output tile staging
-constexpr int kOffColp = kOffOut + kStageOut;                   // int [2][192]: pair rows of the item (two items)
+constexpr int kOffColp = kOffRaw + kRaw * kRawStage;            // int [2][192]: pair rows of the item (two items)
 constexpr int kOffColf = kOffColp + 2 * kTileN * 4;             // float [2][192]: their scales
 constexpr int kOffPrefix = kOffColf + 2 * kTileN * 4;           // int [kMaxSlotsTc + 1]: items before each slot
 constexpr int kOffBars = kOffPrefix + ((kMaxSlotsTc + 1) * 4 + 7) / 8 * 8;  // mbarriers, then small words
 constexpr int kBarWords = 2 * kAStages + 2 * kBStages + 2 * kAcc + 1;
 constexpr int kOffMisc = kOffBars + 8 * kBarWords;              // tmem holder, abort flag, warp sums
-constexpr int kSmemUsed = kOffMisc + 4 * (2 + 18);             // tmem holder, abort flag, 18 warp sums
+constexpr int kSmemUsed = kOffMisc + 4 * (2 + kNumWarps + 1);
 constexpr int kSmemTc = kSmemUsed + 1024;                      // + room to align the base to 1024 bytes
 constexpr uint64_t kWaitNs = 2000000000ull;
 static_assert(kAcc * kTileN + kAStages * kACols <= kTmemCols, "tensor-memory columns");
 static_assert(kEpiWarps * kColsW == 4 * kTileN, "epilogue warps cover the tile");
 static_assert(kSmemTc <= 227 * 1024, "shared memory");
-static_assert(kOffRaw % 1024 == 0 && kOffOut % 16 == 0 && kOffBars % 8 == 0, "region alignment");
-static_assert(kTcThreads / 32 + 1 <= 18, "warp sums fit the small words");
+static_assert(kOffRaw % 1024 == 0 && kOffColp % 16 == 0 && kOffBars % 8 == 0, "region alignment");
 static_assert(kRawStage == 128 * 64, "raw stage: 128 rows of 64 packed bytes");
+static_assert((kOffB + kBStages * kBStage) >> 4 < (1 << 14), "B stages addressable by a matrix descriptor");
 
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
@@ -294,7 +294,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* bstages = smem + kOffB;
     uint8_t* raw = smem + kOffRaw;
-    uint8_t* outst = smem + kOffOut;
     int* colp_buf = reinterpret_cast<int*>(smem + kOffColp);
     float* colf_buf = reinterpret_cast<float*>(smem + kOffColf);
     int* prefix = reinterpret_cast<int*>(smem + kOffPrefix);
@@ -308,7 +307,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* done = acce + kAcc;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
-    int* warp_sums = abort_flag + 1;  // [kTcThreads / 32 + 1]
+    int* warp_sums = abort_flag + 1;  // [kNumWarps + 1]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr bool gateup = MODE == TcMode::kGateUp || MODE == TcMode::kGateUpPartials;
@@ -474,37 +473,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         cp_async_wait<0>();  // no copy is left in flight when the CTA leaves
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issue + B tiles (lane 0)
-        // Use u: wait for its B tiles, a free accumulator (at a group's start)
-        // and its A stage; issue the 8 MMAs; then the B tiles of use u + 2 into
-        // the stage use u - 1 read.
+        // ------------------------------------------------------------ MMA issue (lane 0)
+        // Use u: wait for its B stage, a drained accumulator (at a group's
+        // start) and its A stage; issue its 8 MMAs; release both stages to
+        // the copies (and the accumulator to the epilogue at a group's end).
+        // Nothing else runs on this thread: its loop has to stay well inside
+        // the MMA time of a use.
         if (lane == 0) {
-            Cursor bc{static_cast<int>(blockIdx.x), 0};
-            int b_use = 0, b_issued = 0, b_dec = -1;
-            Item b_it{};
-            auto issue_b = [&]() -> bool {  // the B rows of use b_use into stage b_use % kBStages
-                if (bc.item < total) {
-                    const int s = b_use % kBStages;
-                    if (!wait_bar(b_empty + s, ((b_use / kBStages) & 1) ^ 1, ctl)) return false;
-                    if (bc.item != b_dec) {
-                        b_it = decode_item(bc.item);
-                        b_dec = bc.item;
-                    }
-                    uint8_t* Bs = bstages + s * kBStage;
-                    mbar_expect_tx(b_full + s, kBStage);
-                    tma_tile2d(Bs, &bmap, 128 * bc.ks, b_it.row0, b_full + s);
-                    tma_tile2d(Bs + kBAtom, &bmap, 128 * bc.ks + 64, b_it.row0, b_full + s);
-                    advance(bc);
-                    b_issued = b_use + 1;
-                }
-                ++b_use;
-                return true;
-            };
-            bool ok = issue_b() && issue_b();
+            bool ok = true;
             int use = 0, grp = 0;
+            const uint64_t bdesc0 = sdesc(smem_u32(bstages));
             for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-                const Item it = decode_item(item);
-                const uint32_t idesc = idesc_f16((it.ntok + 15) & ~15);
+                const uint32_t idesc = idesc_f16((decode_item(item).ntok + 15) & ~15);
                 for (int ks = 0; ks < ksteps; ++ks, ++use) {
                     const int sa = use % kAStages, sb = use % kBStages, sub = ks % spg, b = grp % kAcc;
                     if (!wait_bar(b_full + sb, (use / kBStages) & 1, ctl) ||
@@ -514,21 +494,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t b0 = smem_u32(bstages + sb * kBStage);
-                    const uint32_t tam = tmem + kACol0 + kACols * sa;
+                    // descriptor address field = byte address / 16: stage and K offsets add to it
+                    const uint64_t bd = bdesc0 + static_cast<uint64_t>((sb * kBStage) >> 4);
+                    const uint32_t ta = tmem + kACol0 + kACols * sa, td = tmem + b * kTileN;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)  // K = 16 per MMA: 8 A columns, 32 bytes of a B row
-                        mma_f16_ta(tmem + b * kTileN, tam + 8 * kk, sdesc(b0 + (kk >> 2) * kBAtom + 32 * (kk & 3)), idesc,
-                                   (sub > 0 || kk > 0) ? 1u : 0u);
+                        mma_f16_ta(td, ta + 8 * kk, bd + static_cast<uint64_t>(((kk >> 2) * kBAtom + 32 * (kk & 3)) >> 4),
+                                   idesc, (sub > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(a_empty + sa);
                     mma_commit(b_empty + sb);
                     if (sub == spg - 1) {
                         mma_commit(accf + b);
                         ++grp;
-                    }
-                    if (!issue_b()) {
-                        ok = false;
-                        break;
                     }
                 }
             }
@@ -540,8 +517,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     break;
                 }
             }
-            // after an abort: let the B tiles still in flight land before the CTA leaves
-            for (int u = use; u < b_issued; ++u) {
+        }
+        __syncwarp();
+    } else if (warp == kBWarp) {
+        // ------------------------------------------------------------ B tiles (lane 0)
+        // The token rows of use u go into stage u % kBStages once the MMAs of
+        // use u - kBStages have released it: two 2-D TMA tiles of 64 K values.
+        if (lane == 0) {
+            int use = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+                const int row0 = decode_item(item).row0;
+                for (int ks = 0; ks < ksteps; ++ks, ++use) {
+                    const int s = use % kBStages;
+                    if (!wait_bar(b_empty + s, ((use / kBStages) & 1) ^ 1, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* Bs = bstages + s * kBStage;
+                    mbar_expect_tx(b_full + s, kBStage);
+                    tma_tile2d(Bs, &bmap, 128 * ks, row0, b_full + s);
+                    tma_tile2d(Bs + kBAtom, &bmap, 128 * ks + 64, row0, b_full + s);
+                }
+            }
+            // every tile issued above lands before the CTA leaves (after an abort the MMA thread
+            // no longer waits for them): the last kBStages uses cover every stage still in flight
+            for (int u = max(0, use - kBStages); u < use; ++u) {
                 const uint64_t t1 = global_ns();
                 while (!mbar_try_wait(b_full + u % kBStages, (u / kBStages) & 1) && global_ns() - t1 < kWaitNs) {
                 }
@@ -578,21 +579,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
         int j = 0;  // this CTA's item count
+        bool ok = true;
         for (int item = blockIdx.x; item < total; item += gridDim.x, ++j) {
+            // Every epilogue thread learns whether any gave up; and every thread is done with
+            // item j - 1, so its column tables (the other half) may be refilled during item j.
+            if (named_bar_or(1, kEpiThreads, !ok)) break;
             const Item it = decode_item(item);
-            int* colp = colp_buf + (j & 1) * kTileN;
-            float* colf = colf_buf + (j & 1) * kTileN;
+            const int* colp = colp_buf + (j & 1) * kTileN;
+            const float* colf = colf_buf + (j & 1) * kTileN;
             int np = -1;
             float nf = 0.f;
             load_cols(item + gridDim.x, np, nf);  // the next item's (consumed after this one)
-            named_bar(1, kEpiThreads);
             const int nloc = min(kColsW, it.ntok - c_base);  // this warp's live columns (may be <= 0)
             const int64_t wrow = weight_row(it.mt, r);
             const float* srow = a.ws + (static_cast<int64_t>(it.slot) * rows_per_slot + wrow) * ngrp;
             float acc[kColsW];
 #pragma unroll
             for (int c = 0; c < kColsW; ++c) acc[c] = 0.f;
-            bool ok = true;
             // group scales two groups ahead (volatile loads: issued before the waits)
             float sc1 = partials ? 0.f : ld_nc_f32(srow), sc2 = (partials || ngrp < 2) ? 0.f : ld_nc_f32(srow + 1);
             for (int gq = 0; gq < ngrp; ++gq, ++grp) {
@@ -638,54 +641,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mbar_arrive(acce + b);
                 }
             }
-            // every epilogue thread learns whether any gave up before the tile's shared output work
-            if (named_bar_or(1, kEpiThreads, !ok)) break;
-            if (MODE == TcMode::kGateUp || MODE == TcMode::kDown) {
-                // the tile's output rows (one per token column, 256 bytes each) are staged in shared
-                // memory and written with 16-byte stores: rows of h [P][I] (64 fp32 from 64 i) or of the
-                // bf16 Y [P][H] (128 n)
-                if (MODE == TcMode::kGateUp) {
-                    // lanes 2j (gate) and 2j+1 (up) hold index i for every column: for a
-                    // column pair (c0, c1) the even lane finishes c0 and the odd lane c1
-                    const int il = r >> 1;  // i - 64 mt
-                    const bool odd = r & 1;
+            if (!ok) continue;  // (the barrier at the top ends the loop for every thread)
+            // Outputs straight from the registers: for one token column the lanes of a warp hold
+            // consecutive output features, so each store instruction writes 64-byte row pieces.
+            if (MODE == TcMode::kGateUp) {
+                // lanes 2j (gate) and 2j+1 (up) hold index i = 64 mt + j for every column: for a
+                // column pair (c0, c0 + 1) the even lane finishes c0 and the odd lane c0 + 1
+                float* hcol = a.h + 64 * static_cast<int64_t>(it.mt) + (r >> 1);
+                const bool odd = r & 1;
 #pragma unroll
-                    for (int c0 = 0; c0 < kColsW; c0 += 2) {
+                for (int c0 = 0; c0 < kColsW; c0 += 2) {
+                    if (c0 < nloc) {  // warp-uniform: the shuffle below is warp-wide
                         const int c = c0 + (odd ? 1 : 0);
                         const float other = __shfl_xor_sync(0xffffffffu, odd ? acc[c0] : acc[c0 + 1], 1);
                         const float gate = odd ? other : acc[c0], up = odd ? acc[c0 + 1] : other;
                         if (c < nloc) {
                             const float xs = colf[c_base + c];
-                            reinterpret_cast<float*>(outst)[(c_base + c) * 64 + il] = silu_fast(gate * xs) * (up * xs);
+                            hcol[static_cast<int64_t>(colp[c_base + c]) * a.I] = silu_fast(gate * xs) * (up * xs);
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < kColsW; ++c)
-                        if (c < nloc)
-                            reinterpret_cast<__nv_bfloat16*>(outst)[(c_base + c) * 128 + r] =
-                                __float2bfloat16_rn(acc[c] * colf[c_base + c]);
                 }
-                named_bar(1, kEpiThreads);
-                const int64_t ld = MODE == TcMode::kGateUp ? a.I * 4 : a.H * 2;  // global row pitch, bytes
-                const int64_t col0 = 256 * static_cast<int64_t>(it.mt);         // first byte of the tile in a row
-                uint8_t* gbase = MODE == TcMode::kGateUp ? reinterpret_cast<uint8_t*>(a.h) : reinterpret_cast<uint8_t*>(a.yb);
-                for (int q = tid; q < it.ntok * 16; q += kEpiThreads) {
-                    const int row = q >> 4, ch = q & 15;
-                    *reinterpret_cast<uint4*>(gbase + static_cast<int64_t>(colp[row]) * ld + col0 + 16 * ch) =
-                        reinterpret_cast<const uint4*>(outst)[q];
-                }
-            } else if (MODE == TcMode::kDownY) {
-                const int64_t n = 128 * it.mt + r;
+            } else if (MODE == TcMode::kDown || MODE == TcMode::kDownY) {
+                const int64_t n = 128 * static_cast<int64_t>(it.mt) + r;
 #pragma unroll
-                for (int c = 0; c < kColsW; ++c)
-                    if (c < nloc) a.y[static_cast<int64_t>(colp[c_base + c]) * a.H + n] = acc[c] * colf[c_base + c];
+                for (int c = 0; c < kColsW; ++c) {
+                    if (c < nloc) {
+                        const int64_t o = static_cast<int64_t>(colp[c_base + c]) * a.H + n;
+                        const float v = acc[c] * colf[c_base + c];
+                        if (MODE == TcMode::kDown) a.yb[o] = __float2bfloat16_rn(v);
+                        else a.y[o] = v;
+                    }
+                }
             }
             if (np >= 0) {
                 colp_buf[((j + 1) & 1) * kTileN + tid] = np;
                 colf_buf[((j + 1) & 1) * kTileN + tid] = nf;
             }
-            named_bar(1, kEpiThreads);  // the staging area is reused by the next item
         }
     }
 
