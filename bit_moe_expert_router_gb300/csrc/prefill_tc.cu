@@ -3,14 +3,28 @@
 // The grouped expert projections are dense contractions once the tokens are
 // grouped per expert ("Two 96 GB Ascend cards run Qwen3.8 Flash-Next",
 // section 3: grouped expert projections on the matrix unit, blocked
-// reduction, W4A8, weights kept packed).  GB300 has no int8 tcgen05 MMA, so
-// the operands go to the fp16 MMA (kind::f16): int4 codes and int8 values
-// are exact in fp16, each product is exact in the fp32 accumulator and a
-// 128-value K group sums to |P| <= 128 * 127 * 8 < 2^24, so every group's
-// accumulator holds the exact int32 partial.  Each group is accumulated in
-// its own tensor-memory buffer and folded into fp32 registers with its
-// weight scale by the epilogue warps while the tensor core fills the other
-// buffer.
+// reduction, W4A8, weights kept packed).  GB300 has no fast int8 tcgen05
+// MMA, so the operands go to the fp16 MMA (kind::f16).
+//
+// Two accumulation schedules:
+//   Exact (gate/up, and both partials modes): int4 codes and int8 values are
+//     exact in fp16, each product is exact in the fp32 accumulator and a
+//     128-value K group sums to |P| <= 128 * 127 * 8 < 2^24, so every group's
+//     accumulator holds the exact int32 partial.  Each group gets its own
+//     tensor-memory buffer; the epilogue folds it into fp32 registers with
+//     its weight scale (or writes the partial) while the tensor core fills
+//     the other buffer.  The requantised intermediate depends on h at the
+//     rounding level, so gate/up stays exact.
+//   Scaled (down): the producers multiply each code by its group's scale
+//     over the row's largest scale (a fraction of magnitude <= 1, rounded to
+//     fp16, then the product rounded to fp16: within 2^-10 relative of the
+//     dequantised weight) and one accumulator sums the item's whole K range;
+//     the epilogue multiplies the row's largest scale back once.  One drain
+//     per item instead of one per K group: the epilogue's work and its
+//     hand-offs with the MMA thread drop by the group count, and the output
+//     stores overlap the next item's MMAs.  The error enters the layer
+//     output directly (no requantisation after it), far inside the output
+//     tolerance.
 //
 // Tile: M = 128 weight rows x N <= 192 tokens of one bank slot, one K group
 // (128 values) per B stage.  An M = 128 MMA costs about the same
@@ -29,11 +43,11 @@
 //     neighbouring lanes.
 //   B (token rows, fp16, 128-byte-swizzled K-major atoms): contiguous rows
 //     by pair row -- the activations gathered per pair (gate/up) or the
-//     requantised h (down) -- loaded as two 2-D TMA tiles per stage by the MMA
-//     warp.  (Gathering the activation rows inside the kernel from a
-//     per-token table, by TMA tile::gather4 or by 16-byte cp.async copies,
-//     measured several times slower here: the row requests cost far more than
-//     the bytes.)  Three stages.
+//     requantised h (down) -- loaded as two 2-D TMA tiles per stage by a
+//     warp of its own, four stages deep.  (Gathering the activation rows
+//     inside the kernel from a per-token table, by TMA tile::gather4 or by
+//     16-byte cp.async copies, measured several times slower here: the row
+//     requests cost far more than the bytes.)
 // Persistent CTAs (one per SM) walk the (slot, token tile, weight tile)
 // items with the weight tile fastest, so the CTAs working at one time share
 // the token rows in L2.  Every item costs the same MMA time (K / 16 MMAs of
@@ -44,13 +58,18 @@
 // kernel, which sums each token's pairs in a fixed order in fp32 (adding the
 // pairs into the output with device reductions instead measured several
 // times slower: the reductions of one tile outlast its MMAs many times over).
+// Both are stored straight from the registers: for one token column a
+// warp's lanes hold consecutive output features, and a tile's pair rows are
+// consecutive.
 //
-// Seventeen warps: 0-11 epilogue (warp w: TMEM lanes 32 (w % 4) .. +31 =
+// Eighteen warps: 0-11 epilogue (warp w: TMEM lanes 32 (w % 4) .. +31 =
 // tile rows, columns 64 (w / 4) .. +63), 12-15 producers (thread = tile row
-// of A), 16 MMA issue and B tiles (one thread: a warp-wide wait costs a few
-// hundred cycles here, and the issuing loop has to stay well inside the MMA
-// time of a stage) and the tensor-memory allocation.  Every wait is
-// bounded; a timeout sets the status word and every role leaves cleanly.
+// of A), 16 MMA issue (one thread; the tensor-memory allocation is the
+// warp's) and 17 the B tiles (one thread).  The MMA thread does nothing but
+// wait, issue and commit: each instruction of a single thread costs tens of
+// cycles here and its loop has to stay inside the MMA time of a use.  Every
+// wait is bounded (the waiting thread sleeps in the barrier test); a timeout
+// sets the status word and every role leaves cleanly.
 //
 // K order: the weight unpack turns a packed word (codes 0..7) into fp16
 // pairs (0,4) (1,5) (2,6) (3,7); the token rows are converted to fp16 in
@@ -102,6 +121,7 @@ constexpr int kOffMisc = kOffBars + 8 * kBarWords;              // tmem holder, 
 constexpr int kSmemUsed = kOffMisc + 4 * (2 + kNumWarps + 1);
 constexpr int kSmemTc = kSmemUsed + 1024;                      // + room to align the base to 1024 bytes
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint32_t kSleepNs = 20000;  // longest sleep inside one barrier test
 static_assert(kAcc * kTileN + kAStages * kACols <= kTmemCols, "tensor-memory columns");
 static_assert(kEpiWarps * kColsW == 4 * kTileN, "epilogue warps cover the tile");
 static_assert(kSmemTc <= 227 * 1024, "shared memory");
@@ -130,6 +150,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// The same test, but the thread may sleep in the instruction for up to `ns` nanoseconds (it is
+// woken when the phase completes): a waiting warp then takes no issue slots from the warps
+// doing the work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
@@ -144,8 +176,8 @@ struct Ctl {
 __device__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctl& c) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31) == 31) {
+        if (mbar_wait_sleep(bar, parity, kSleepNs)) return true;
+        if ((it & 7) == 7) {
             if (*c.abort) return false;
             const uint64_t t = global_ns();
             if (t0 == 0) {
@@ -211,13 +243,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
           "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
         : "r"(taddr));
 }
+// 8 consecutive 32-bit tensor-memory columns of this thread's lane (no wait).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* v) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
-__device__ __forceinline__ float ld_nc_f32(const float* p) {
-    float v;
-    asm volatile("ld.global.nc.f32 %0, [%1];\n" : "=f"(v) : "l"(p));
-    return v;
-}
 
 // 32 consecutive 32-bit tensor-memory columns of this thread's lane <- v (no wait).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
@@ -258,6 +291,15 @@ __device__ __forceinline__ void unpack_int4_f16(uint32_t w, uint32_t* r) {
     r[3] = *reinterpret_cast<const uint32_t*>(&h3);
 }
 
+// Largest |scale| of a weight row's n groups (0 for an all-zero row).  The producers put each
+// group's scale into A as a fraction of it and the epilogue multiplies it back: both read the same
+// values, and a maximum does not depend on the order it is taken in.
+__device__ __forceinline__ float row_scale_max(const float* s, int n) {
+    float m = 0.f;
+    for (int g = 0; g < n; ++g) m = fmaxf(m, fabsf(__ldg(s + g)));
+    return m;
+}
+
 // Named barriers of n threads.  The non-aligned forms (barrier.sync / barrier.red, not bar.*):
 // they are reached right after per-thread bounded spin waits, so a warp may arrive diverged, and
 // the compiler does not reconverge a warp before an inline-asm barrier.
@@ -291,7 +333,9 @@ template <TcMode MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(TcArgs a, int n_mt, const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // (offset from the __shared__ array itself, not an integer cast: the compiler then keeps every
+    // access below in the shared state space and knows it cannot alias the global stores)
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* bstages = smem + kOffB;
     uint8_t* raw = smem + kOffRaw;
     int* colp_buf = reinterpret_cast<int*>(smem + kOffColp);
@@ -312,6 +356,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr bool gateup = MODE == TcMode::kGateUp || MODE == TcMode::kGateUpPartials;
     constexpr bool partials = MODE == TcMode::kGateUpPartials || MODE == TcMode::kDownPartials;
+    // Down projection outputs: the group scales ride in A and one accumulator sums the item's
+    // whole K range.  Every other mode keeps one exact int32 partial per K group.
+    constexpr bool scaled = MODE == TcMode::kDown || MODE == TcMode::kDownY;
     const int64_t K = a.K, rows_per_slot = a.rows_per_slot;
     const int ksteps = static_cast<int>(K / 128), spg = a.g / 128, ngrp = static_cast<int>(K / a.g);
     const Ctl ctl{abort_flag, a.hdr};
@@ -439,7 +486,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int d = 0; d < kRaw - 1; ++d) fetch();
         int use = 0;
         for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+            // Scaled (down) modes: A carries each code times its group's scale over the row's
+            // largest scale (|fraction| <= 1, so the fp16 product keeps 11 significant bits).
+            // Other modes: A is the bare code.
+            const float* srow = nullptr;
+            float inv = 0.f;
+            if (scaled) {
+                const Item it = decode_item(item);
+                srow = a.ws + (static_cast<int64_t>(it.slot) * rows_per_slot + weight_row(it.mt, pt)) * ngrp;
+                const float m = row_scale_max(srow, ngrp);
+                inv = m > 0.f ? 1.0f / m : 0.f;
+            }
             for (int ks = 0; ks < ksteps; ++ks, ++use) {
+                const float sg = scaled ? __ldg(srow + ks / spg) : 0.f;  // (loaded ahead of the waits)
                 fetch();                      // use + kRaw - 1 into the slot of use - 1
                 cp_async_wait<kRaw - 1>();    // this lane's copies for this use have landed
                 __syncwarp();                 // ... and the other lanes' copies of this warp's rows
@@ -464,6 +523,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                rw[2 * h2 + 1].x, rw[2 * h2 + 1].y, rw[2 * h2 + 1].z, rw[2 * h2 + 1].w};
 #pragma unroll
                     for (int wi = 0; wi < 8; ++wi) unpack_int4_f16(words[wi], av + 4 * wi);
+                    if (scaled) {
+                        const __half2 f2 = __float2half2_rn(sg * inv);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&av[e]), f2);
+                            av[e] = *reinterpret_cast<const uint32_t*>(&v);
+                        }
+                    }
                     tmem_st32(ta + 32 * h2, av);
                 }
                 tmem_st_wait();
@@ -482,11 +549,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             bool ok = true;
             int use = 0, grp = 0;
+            const int span = scaled ? ksteps : spg;  // uses summed in one accumulator
             const uint64_t bdesc0 = sdesc(smem_u32(bstages));
             for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
                 const uint32_t idesc = idesc_f16((decode_item(item).ntok + 15) & ~15);
                 for (int ks = 0; ks < ksteps; ++ks, ++use) {
-                    const int sa = use % kAStages, sb = use % kBStages, sub = ks % spg, b = grp % kAcc;
+                    const int sa = use % kAStages, sb = use % kBStages, sub = ks % span, b = grp % kAcc;
                     if (!wait_bar(b_full + sb, (use / kBStages) & 1, ctl) ||
                         (sub == 0 && !wait_bar(acce + b, ((grp / kAcc) & 1) ^ 1, ctl)) ||
                         !wait_bar(a_full + sa, (use / kAStages) & 1, ctl)) {
@@ -503,7 +571,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                    idesc, (sub > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(a_empty + sa);
                     mma_commit(b_empty + sb);
-                    if (sub == spg - 1) {
+                    if (sub == span - 1) {
                         mma_commit(accf + b);
                         ++grp;
                     }
@@ -593,23 +661,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int nloc = min(kColsW, it.ntok - c_base);  // this warp's live columns (may be <= 0)
             const int64_t wrow = weight_row(it.mt, r);
             const float* srow = a.ws + (static_cast<int64_t>(it.slot) * rows_per_slot + wrow) * ngrp;
-            float acc[kColsW];
-#pragma unroll
-            for (int c = 0; c < kColsW; ++c) acc[c] = 0.f;
-            // group scales two groups ahead (volatile loads: issued before the waits)
-            float sc1 = partials ? 0.f : ld_nc_f32(srow), sc2 = (partials || ngrp < 2) ? 0.f : ld_nc_f32(srow + 1);
-            for (int gq = 0; gq < ngrp; ++gq, ++grp) {
-                const int b = grp % kAcc;
-                const float sc = sc1;
-                sc1 = sc2;
-                if (!partials && gq + 2 < ngrp) sc2 = ld_nc_f32(srow + gq + 2);
-                if (!__all_sync(0xffffffffu, wait_bar(accf + b, (grp / kAcc) & 1, ctl))) {  // loads below are warp-aligned
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t tb = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + b * kTileN + c_base;
-                if (partials) {
+            if (partials) {
+                // one accumulator per K group: its exact int32 partial, by pair row
+                for (int gq = 0; gq < ngrp; ++gq, ++grp) {
+                    const int b = grp % kAcc;
+                    if (!__all_sync(0xffffffffu, wait_bar(accf + b, (grp / kAcc) & 1, ctl))) {  // loads are warp-aligned
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tb = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + b * kTileN + c_base;
                     uint32_t v[16];
 #pragma unroll
                     for (int i = 0; i < kColsW / 16; ++i) {
@@ -625,51 +686,101 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc_fence_before();
                     mbar_arrive(acce + b);
-                } else {
-                    // 16 columns at a time (registers: 64 running sums + 16 loaded values)
+                }
+            } else if (!scaled) {
+                // Gate/up: each K group's exact partial is folded into fp32 registers with its
+                // scale (scales two groups ahead: issued before the waits)
+                float acc[kColsW];
 #pragma unroll
-                    for (int i = 0; i < kColsW / 16; ++i) {
-                        if (16 * i < nloc) {
-                            uint32_t v[16];
-                            tmem_ld16(tb + 16 * i, v);
+                for (int c = 0; c < kColsW; ++c) acc[c] = 0.f;
+                float sc1 = __ldg(srow), sc2 = ngrp < 2 ? 0.f : __ldg(srow + 1);
+                for (int gq = 0; gq < ngrp; ++gq, ++grp) {
+                    const int b = grp % kAcc;
+                    const float sc = sc1;
+                    sc1 = sc2;
+                    if (gq + 2 < ngrp) sc2 = __ldg(srow + gq + 2);
+                    if (!__all_sync(0xffffffffu, wait_bar(accf + b, (grp / kAcc) & 1, ctl))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tb = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + b * kTileN + c_base;
+#pragma unroll
+                    for (int i = 0; i < kColsW / 8; ++i) {  // 8 columns at a time (64 running sums + 8 loaded)
+                        if (8 * i < nloc) {
+                            uint32_t v[8];
+                            tmem_ld8(tb + 8 * i, v);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) acc[16 * i + c] = fmaf(__uint_as_float(v[c]), sc, acc[16 * i + c]);
+                            for (int c = 0; c < 8; ++c) acc[8 * i + c] = fmaf(__uint_as_float(v[c]), sc, acc[8 * i + c]);
                         }
                     }
                     tc_fence_before();
                     mbar_arrive(acce + b);
                 }
-            }
-            if (!ok) continue;  // (the barrier at the top ends the loop for every thread)
-            // Outputs straight from the registers: for one token column the lanes of a warp hold
-            // consecutive output features, so each store instruction writes 64-byte row pieces.
-            if (MODE == TcMode::kGateUp) {
-                // lanes 2j (gate) and 2j+1 (up) hold index i = 64 mt + j for every column: for a
-                // column pair (c0, c0 + 1) the even lane finishes c0 and the odd lane c0 + 1
-                float* hcol = a.h + 64 * static_cast<int64_t>(it.mt) + (r >> 1);
+                if (!ok) continue;
+                // h straight from the registers: lanes 2j (gate) and 2j+1 (up) hold index
+                // i = 64 mt + j for every column; for a column pair (c0, c0 + 1) the even lane
+                // finishes c0 and the odd lane c0 + 1, so each store instruction writes two
+                // 64-byte row pieces.  The tile's pair rows are consecutive (row0 + column).
                 const bool odd = r & 1;
+                float* hp = a.h + static_cast<int64_t>(it.row0 + c_base + (odd ? 1 : 0)) * a.I + 64 * it.mt + (r >> 1);
 #pragma unroll
-                for (int c0 = 0; c0 < kColsW; c0 += 2) {
-                    if (c0 < nloc) {  // warp-uniform: the shuffle below is warp-wide
-                        const int c = c0 + (odd ? 1 : 0);
-                        const float other = __shfl_xor_sync(0xffffffffu, odd ? acc[c0] : acc[c0 + 1], 1);
-                        const float gate = odd ? other : acc[c0], up = odd ? acc[c0 + 1] : other;
-                        if (c < nloc) {
-                            const float xs = colf[c_base + c];
-                            hcol[static_cast<int64_t>(colp[c_base + c]) * a.I] = silu_fast(gate * xs) * (up * xs);
+                for (int q = 0; q < kColsW / 16; ++q) {
+                    if (16 * q < nloc) {  // warp-uniform: the shuffles below are warp-wide
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int c0 = 16 * q + 2 * e;
+                            const float xs = colf[c_base + c0 + (odd ? 1 : 0)];
+                            const float other = __shfl_xor_sync(0xffffffffu, odd ? acc[c0] : acc[c0 + 1], 1);
+                            const float gate = odd ? other : acc[c0], up = odd ? acc[c0 + 1] : other;
+                            if (c0 + (odd ? 1 : 0) < nloc) *hp = silu_fast(gate * xs) * (up * xs);
+                            hp += 2 * a.I;
                         }
                     }
                 }
-            } else if (MODE == TcMode::kDown || MODE == TcMode::kDownY) {
-                const int64_t n = 128 * static_cast<int64_t>(it.mt) + r;
+            } else {
+                // Down: one accumulator holds the item's whole K range in units of the row's
+                // largest scale.  It is read 16 columns at a time and handed back to the MMAs as
+                // soon as its last columns are in registers; Y goes straight from the registers:
+                // for one token column the lanes of a warp hold consecutive output features, so
+                // each store instruction writes a 64-byte row piece, and the tile's pair rows are
+                // consecutive (row0 + column).
+                const float smax = row_scale_max(srow, ngrp);
+                const int b = grp % kAcc;
+                ++grp;
+                if (!__all_sync(0xffffffffu, wait_bar(accf + b, ((grp - 1) / kAcc) & 1, ctl))) {
+                    ok = false;
+                    continue;
+                }
+                tc_fence_after();
+                const uint32_t tb = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + b * kTileN + c_base;
+                const int nq = nloc <= 0 ? 0 : min(kColsW / 16, (nloc + 15) / 16);  // chunks with live columns
+                if (nq == 0) {
+                    tc_fence_before();
+                    mbar_arrive(acce + b);
+                }
+                const int64_t o0 = static_cast<int64_t>(it.row0 + c_base) * a.H + 128 * static_cast<int64_t>(it.mt) + r;
 #pragma unroll
-                for (int c = 0; c < kColsW; ++c) {
-                    if (c < nloc) {
-                        const int64_t o = static_cast<int64_t>(colp[c_base + c]) * a.H + n;
-                        const float v = acc[c] * colf[c_base + c];
-                        if (MODE == TcMode::kDown) a.yb[o] = __float2bfloat16_rn(v);
-                        else a.y[o] = v;
+                for (int q = 0; q < kColsW / 16; ++q) {
+                    if (q < nq) {  // warp-uniform: the loads below are warp-wide
+                        uint32_t v[16];
+                        tmem_ld16(tb + 16 * q, v);
+                        tmem_ld_wait();
+                        if (q == nq - 1) {
+                            tc_fence_before();
+                            mbar_arrive(acce + b);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int c = 16 * q + e;
+                            const float yv = __uint_as_float(v[e]) * smax * colf[c_base + c];
+                            const int64_t o = o0 + static_cast<int64_t>(c) * a.H;
+                            if (c < nloc) {
+                                if (MODE == TcMode::kDown) a.yb[o] = __float2bfloat16_rn(yv);
+                                else a.y[o] = yv;
+                            }
+                        }
                     }
                 }
             }
