@@ -62,14 +62,16 @@
 // warp's lanes hold consecutive output features, and a tile's pair rows are
 // consecutive.
 //
-// Eighteen warps: 0-11 epilogue (warp w: TMEM lanes 32 (w % 4) .. +31 =
-// tile rows, columns 64 (w / 4) .. +63), 12-15 producers (thread = tile row
-// of A), 16 MMA issue (one thread; the tensor-memory allocation is the
-// warp's) and 17 the B tiles (one thread).  The MMA thread does nothing but
-// wait, issue and commit: each instruction of a single thread costs tens of
-// cycles here and its loop has to stay inside the MMA time of a use.  Every
-// wait is bounded (the waiting thread sleeps in the barrier test); a timeout
-// sets the status word and every role leaves cleanly.
+// Eighteen warps: 0 MMA issue (one thread; the tensor-memory allocation is
+// the warp's), 1 the B tiles (one thread), 2-5 producers (thread = tile row
+// of A, rows 32 (w % 4) .. +31) and 6-17 epilogue (warp w: TMEM lanes
+// 32 (w % 4) .. +31 = tile rows, columns 64 ((w - 6) / 4) .. +63).  The MMA
+// thread does nothing but wait, issue and commit, and it has the lowest
+// warp id: with busy warps beside it on its scheduler each of its
+// instructions otherwise waited tens of cycles, and its loop has to stay
+// inside the MMA time of a use.  Every wait is bounded (the waiting thread
+// sleeps in the barrier test); a timeout sets the status word and every role
+// leaves cleanly.
 //
 // K order: the weight unpack turns a packed word (codes 0..7) into fp16
 // pairs (0,4) (1,5) (2,6) (3,7); the token rows are converted to fp16 in
@@ -87,12 +89,17 @@
 namespace moe {
 namespace {
 
-constexpr int kEpiWarps = 12;                // three per TMEM lane quarter, 64 columns each
+// Roles by warp.  The single-thread roles come first: a warp scheduler that has several ready
+// warps favours the lower warp ids, and these threads' loops set the pace of everything else.
+// A warp reaches only the tensor-memory lane quarter warp % 4, so the four producer warps and
+// each group of four epilogue warps cover the four quarters in some order.
+constexpr int kMmaWarp = 0;                  // MMA issue and the tensor-memory allocation
+constexpr int kBWarp = 1;                    // B tiles
 constexpr int kProdWarps = 4;                // one per TMEM lane quarter
-constexpr int kProdWarp0 = kEpiWarps;
-constexpr int kMmaWarp = kEpiWarps + kProdWarps;  // MMA issue and the tensor-memory allocation
-constexpr int kBWarp = kMmaWarp + 1;              // B tiles
-constexpr int kTcThreads = 32 * (kBWarp + 1);
+constexpr int kProdWarp0 = 2;
+constexpr int kEpiWarps = 12;                // three per TMEM lane quarter, 64 columns each
+constexpr int kEpiWarp0 = kProdWarp0 + kProdWarps;
+constexpr int kTcThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kProdThreads = 32 * kProdWarps;
 constexpr int kColsW = 64;                   // accumulator columns per epilogue warp
@@ -115,15 +122,18 @@ constexpr int kOffRaw = kOffB + kBStages * kBStage;             // [kRaw][128 ro
 constexpr int kOffColp = kOffRaw + kRaw * kRawStage;            // int [2][192]: pair rows of the item (two items)
 constexpr int kOffColf = kOffColp + 2 * kTileN * 4;             // float [2][192]: their scales
 constexpr int kOffPrefix = kOffColf + 2 * kTileN * 4;           // int [kMaxSlotsTc + 1]: items before each slot
-constexpr int kOffBars = kOffPrefix + ((kMaxSlotsTc + 1) * 4 + 7) / 8 * 8;  // mbarriers, then small words
-constexpr int kBarWords = 2 * kAStages + 2 * kBStages + 2 * kAcc + 1;
+constexpr int kItab = 256;                                      // this CTA's first items, decoded once
+constexpr int kOffItab = kOffPrefix + ((kMaxSlotsTc + 1) * 4 + 7) / 8 * 8;  // ItemRec [kItab]
+constexpr int kOffBars = kOffItab + kItab * 8;                  // mbarriers, then small words
+constexpr int kBarWords = kAStages + 2 * kBStages + 2 * kAcc + 1;
 constexpr int kOffMisc = kOffBars + 8 * kBarWords;              // tmem holder, abort flag, warp sums
 constexpr int kSmemUsed = kOffMisc + 4 * (2 + kNumWarps + 1);
 constexpr int kSmemTc = kSmemUsed + 1024;                      // + room to align the base to 1024 bytes
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kSleepNs = 20000;  // longest sleep inside one barrier test
 static_assert(kAcc * kTileN + kAStages * kACols <= kTmemCols, "tensor-memory columns");
-static_assert(kEpiWarps * kColsW == 4 * kTileN, "epilogue warps cover the tile");
+static_assert(kEpiWarps * kColsW == 4 * kTileN && kEpiWarps % 4 == 0, "epilogue warps cover the tile");
+static_assert(kProdWarps == 4 && kEpiWarp0 == kProdWarp0 + kProdWarps, "four producers, one per lane quarter");
 static_assert(kSmemTc <= 227 * 1024, "shared memory");
 static_assert(kOffRaw % 1024 == 0 && kOffColp % 16 == 0 && kOffBars % 8 == 0, "region alignment");
 static_assert(kRawStage == 128 * 64, "raw stage: 128 rows of 64 packed bytes");
@@ -321,12 +331,19 @@ __device__ __forceinline__ bool named_bar_or(int id, int n, bool v) {
 
 
 struct Item {
-    int slot, tt, mt, row0, ntok;
+    int slot, mt, row0, ntok;
 };
+// A decoded item as kept in shared memory.
+struct ItemRec {
+    int row0;
+    int16_t slot;
+    uint8_t mt, ntok_m1;
+};
+static_assert(sizeof(ItemRec) == 8, "item record");
 
 // Walks this CTA's (item, K step) uses in order.
 struct Cursor {
-    int item, ks;
+    int item, ks, j;  // j: the item's index among this CTA's items
 };
 
 template <TcMode MODE>
@@ -341,12 +358,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int* colp_buf = reinterpret_cast<int*>(smem + kOffColp);
     float* colf_buf = reinterpret_cast<float*>(smem + kOffColf);
     int* prefix = reinterpret_cast<int*>(smem + kOffPrefix);
+    ItemRec* itab = reinterpret_cast<ItemRec*>(smem + kOffItab);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
-    uint64_t* a_full = bars;                     // [kAStages] 128 producer arrivals
-    uint64_t* a_empty = a_full + kAStages;       // [kAStages] MMA commit
-    uint64_t* b_full = a_empty + kAStages;       // [kBStages] expect-tx arrival + TMA bytes
-    uint64_t* b_empty = b_full + kBStages;       // [kBStages] MMA commit
-    uint64_t* accf = b_empty + kBStages;         // [kAcc] MMA commit at a group's end
+    // Use u: its A stage is u % kAStages, its B stage and its empty barrier u % kBStages.
+    uint64_t* a_full = bars;                     // [kAStages] 128 producer arrivals (the last after B landed)
+    uint64_t* b_full = a_full + kAStages;        // [kBStages] expect-tx arrival + TMA bytes
+    uint64_t* empty = b_full + kBStages;         // [kBStages] MMA commit: use u's A and B stages are read
+    uint64_t* accf = empty + kBStages;           // [kAcc] MMA commit at a group's end
     uint64_t* acce = accf + kAcc;                // [kAcc] epilogue arrivals
     uint64_t* done = acce + kAcc;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -364,13 +382,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const Ctl ctl{abort_flag, a.hdr};
 
     if (tid == 0) {
-        for (int s = 0; s < kAStages; ++s) {
-            mbar_init(a_full + s, kProdThreads);
-            mbar_init(a_empty + s, 1);
-        }
+        for (int s = 0; s < kAStages; ++s) mbar_init(a_full + s, kProdThreads);
         for (int s = 0; s < kBStages; ++s) {
             mbar_init(b_full + s, 1);  // expect-tx arrival + the TMA bytes
-            mbar_init(b_empty + s, 1);
+            mbar_init(empty + s, 1);
         }
         for (int b = 0; b < kAcc; ++b) {
             mbar_init(accf + b, 1);
@@ -432,10 +447,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         Item it;
         it.slot = lo;
         const int local = item - prefix[lo];
-        it.tt = local / n_mt;
         it.mt = local % n_mt;
-        it.row0 = a.seg_off[lo] + kTileN * it.tt;
+        it.row0 = a.seg_off[lo] + kTileN * (local / n_mt);
         it.ntok = min(kTileN, a.seg_off[lo] + a.seg_cnt[lo] - it.row0);
+        return it;
+    };
+    // This CTA's j-th item (item = blockIdx.x + j gridDim.x): its first kItab items are decoded
+    // once here, so the single-thread loops read one record instead of searching the prefix.
+    for (int j = tid; j < kItab; j += kTcThreads) {
+        const int item = static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x);
+        if (item < total) {
+            const Item it = decode_item(item);
+            itab[j] = ItemRec{it.row0, static_cast<int16_t>(it.slot), static_cast<uint8_t>(it.mt),
+                              static_cast<uint8_t>(it.ntok - 1)};
+        }
+    }
+    __syncthreads();
+    auto item_at = [&](int j, int item) -> Item {
+        if (j >= kItab) return decode_item(item);
+        const ItemRec rec = itab[j];
+        Item it;
+        it.slot = rec.slot;
+        it.mt = rec.mt;
+        it.row0 = rec.row0;
+        it.ntok = rec.ntok_m1 + 1;
         return it;
     };
     // bank row of tile row r (gate/up: gate and up rows interleaved)
@@ -447,26 +482,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (++c.ks == ksteps) {
             c.ks = 0;
             c.item += gridDim.x;
+            ++c.j;
         }
     };
 
-    if (warp >= kProdWarp0 && warp < kMmaWarp) {
+    if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
         // ------------------------------------------------------------ producers
         // Thread pt owns tile row pt (TMEM lane pt).  Each warp copies the
         // packed bytes of its 32 rows for use u + kRaw - 1 into the raw slot
         // of use u - 1 (which every lane of the warp has read: the warp is
         // past it), so the unpack never waits for HBM.
-        const int pw = warp - kProdWarp0;
+        const int pw = warp & 3;  // this warp's tensor-memory lane quarter = its 32 tile rows
         const int pt = 32 * pw + lane;
         const int rsw = (pt >> 1) & 3;  // 16-byte chunk q of row r sits at q ^ ((r >> 1) & 3): no bank conflicts
         const int piece = lane & 3;
-        Cursor lc{static_cast<int>(blockIdx.x), 0};
+        Cursor lc{static_cast<int>(blockIdx.x), 0, 0};
         int l_use = 0, l_dec = -1;
         Item l_it{};
         auto fetch = [&]() {  // this warp's rows of use l_use into raw slot l_use % kRaw (one commit group)
             if (lc.item < total) {
                 if (lc.item != l_dec) {
-                    l_it = decode_item(lc.item);
+                    l_it = item_at(lc.j, lc.item);
                     l_dec = lc.item;
                 }
                 const uint8_t* wslot = a.w + static_cast<int64_t>(l_it.slot) * rows_per_slot * (K / 2);
@@ -485,14 +521,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = true;
         for (int d = 0; d < kRaw - 1; ++d) fetch();
         int use = 0;
-        for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        for (int item = blockIdx.x, j = 0; item < total && ok; item += gridDim.x, ++j) {
             // Scaled (down) modes: A carries each code times its group's scale over the row's
             // largest scale (|fraction| <= 1, so the fp16 product keeps 11 significant bits).
             // Other modes: A is the bare code.
             const float* srow = nullptr;
             float inv = 0.f;
             if (scaled) {
-                const Item it = decode_item(item);
+                const Item it = item_at(j, item);
                 srow = a.ws + (static_cast<int64_t>(it.slot) * rows_per_slot + weight_row(it.mt, pt)) * ngrp;
                 const float m = row_scale_max(srow, ngrp);
                 inv = m > 0.f ? 1.0f / m : 0.f;
@@ -507,10 +543,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) rw[q] = rp[q ^ rsw];
                 const int s = use % kAStages;
-                // warp-uniform outcome: the tensor-memory stores below are warp-aligned
-                if (!__all_sync(0xffffffffu, wait_bar(a_empty + s, ((use / kAStages) & 1) ^ 1, ctl))) {
-                    ok = false;
-                    break;
+                // The A stage is free once the MMAs of use - kAStages have completed (warp-uniform
+                // outcome: the tensor-memory stores below are warp-aligned).
+                if (use >= kAStages) {
+                    const int v = use - kAStages;
+                    if (!__all_sync(0xffffffffu, wait_bar(empty + v % kBStages, (v / kBStages) & 1, ctl))) {
+                        ok = false;
+                        break;
+                    }
                 }
                 tc_fence_after();  // the stage's previous MMAs (which read its A columns) are complete
                 // unpacked row -> this thread's tensor-memory lane, 64 columns of fp16
@@ -534,6 +574,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tmem_st32(ta + 32 * h2, av);
                 }
                 tmem_st_wait();
+                // Thread 0 holds its arrival back until the use's B tiles have landed, so the MMA
+                // thread waits on one barrier per use.
+                if (!__all_sync(0xffffffffu, pt != 0 || wait_bar(b_full + use % kBStages, (use / kBStages) & 1, ctl))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_before();
                 mbar_arrive(a_full + s);
             }
@@ -551,13 +597,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int use = 0, grp = 0;
             const int span = scaled ? ksteps : spg;  // uses summed in one accumulator
             const uint64_t bdesc0 = sdesc(smem_u32(bstages));
-            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-                const uint32_t idesc = idesc_f16((decode_item(item).ntok + 15) & ~15);
+            for (int item = blockIdx.x, j = 0; item < total && ok; item += gridDim.x, ++j) {
+                const uint32_t idesc = idesc_f16((item_at(j, item).ntok + 15) & ~15);
                 for (int ks = 0; ks < ksteps; ++ks, ++use) {
                     const int sa = use % kAStages, sb = use % kBStages, sub = ks % span, b = grp % kAcc;
-                    if (!wait_bar(b_full + sb, (use / kBStages) & 1, ctl) ||
-                        (sub == 0 && !wait_bar(acce + b, ((grp / kAcc) & 1) ^ 1, ctl)) ||
-                        !wait_bar(a_full + sa, (use / kAStages) & 1, ctl)) {
+                    if (!wait_bar(a_full + sa, (use / kAStages) & 1, ctl) ||
+                        (sub == 0 && !wait_bar(acce + b, ((grp / kAcc) & 1) ^ 1, ctl))) {
                         ok = false;
                         break;
                     }
@@ -569,8 +614,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int kk = 0; kk < 8; ++kk)  // K = 16 per MMA: 8 A columns, 32 bytes of a B row
                         mma_f16_ta(td, ta + 8 * kk, bd + static_cast<uint64_t>(((kk >> 2) * kBAtom + 32 * (kk & 3)) >> 4),
                                    idesc, (sub > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(a_empty + sa);
-                    mma_commit(b_empty + sb);
+                    mma_commit(empty + sb);
                     if (sub == span - 1) {
                         mma_commit(accf + b);
                         ++grp;
@@ -594,11 +638,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             int use = 0;
             bool ok = true;
-            for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-                const int row0 = decode_item(item).row0;
+            for (int item = blockIdx.x, j = 0; item < total && ok; item += gridDim.x, ++j) {
+                const int row0 = item_at(j, item).row0;
                 for (int ks = 0; ks < ksteps; ++ks, ++use) {
                     const int s = use % kBStages;
-                    if (!wait_bar(b_empty + s, ((use / kBStages) & 1) ^ 1, ctl)) {
+                    if (!wait_bar(empty + s, ((use / kBStages) & 1) ^ 1, ctl)) {
                         ok = false;
                         break;
                     }
@@ -619,18 +663,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        // warp w: TMEM lanes 32 (w % 4) .. +31 (tile rows), columns 64 (w / 4) .. +63
-        const int quarter = warp & 3, c_base = kColsW * (warp >> 2);
+        // warp w: TMEM lanes 32 (w % 4) .. +31 (tile rows), columns 64 ((w - kEpiWarp0) / 4) .. +63
+        const int quarter = warp & 3, c_base = kColsW * ((warp - kEpiWarp0) >> 2);
         const int r = 32 * quarter + lane;  // tile row
+        const int et = tid - 32 * kEpiWarp0;  // epilogue thread index
         int grp = 0;
         // the pair rows and column scales of an item are loaded one item ahead (their global
         // loads then overlap the previous item's groups) into the other half of colp / colf
-        auto load_cols = [&](int item, int& p_out, float& f_out) {
+        auto load_cols = [&](int jj, int item, int& p_out, float& f_out) {
             p_out = -1;
-            if (item < total && tid < kTileN) {
-                const Item nx = decode_item(item);
-                if (tid < nx.ntok) {
-                    const int p = nx.row0 + tid;
+            if (item < total && et < kTileN) {
+                const Item nx = item_at(jj, item);
+                if (et < nx.ntok) {
+                    const int p = nx.row0 + et;
                     p_out = p;
                     f_out = MODE == TcMode::kGateUp ? __ldg(a.b_scale + __ldg(a.row_token + p))
                                                     : (partials ? 0.f : __ldg(a.b_scale + p));
@@ -640,10 +685,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         {
             int p0 = -1;
             float f0 = 0.f;
-            load_cols(blockIdx.x, p0, f0);
+            load_cols(0, blockIdx.x, p0, f0);
             if (p0 >= 0) {
-                colp_buf[tid] = p0;
-                colf_buf[tid] = f0;
+                colp_buf[et] = p0;
+                colf_buf[et] = f0;
             }
         }
         int j = 0;  // this CTA's item count
@@ -652,12 +697,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // Every epilogue thread learns whether any gave up; and every thread is done with
             // item j - 1, so its column tables (the other half) may be refilled during item j.
             if (named_bar_or(1, kEpiThreads, !ok)) break;
-            const Item it = decode_item(item);
+            const Item it = item_at(j, item);
             const int* colp = colp_buf + (j & 1) * kTileN;
             const float* colf = colf_buf + (j & 1) * kTileN;
             int np = -1;
             float nf = 0.f;
-            load_cols(item + gridDim.x, np, nf);  // the next item's (consumed after this one)
+            load_cols(j + 1, item + gridDim.x, np, nf);  // the next item's (consumed after this one)
             const int nloc = min(kColsW, it.ntok - c_base);  // this warp's live columns (may be <= 0)
             const int64_t wrow = weight_row(it.mt, r);
             const float* srow = a.ws + (static_cast<int64_t>(it.slot) * rows_per_slot + wrow) * ngrp;
@@ -785,8 +830,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             if (np >= 0) {
-                colp_buf[((j + 1) & 1) * kTileN + tid] = np;
-                colf_buf[((j + 1) & 1) * kTileN + tid] = nf;
+                colp_buf[((j + 1) & 1) * kTileN + et] = np;
+                colf_buf[((j + 1) & 1) * kTileN + et] = nf;
             }
         }
     }
@@ -954,7 +999,8 @@ cudaError_t launch_mode_tc(const TcArgs& a, int n_mt, cudaStream_t st) {
 }  // namespace
 
 bool tc_supported(int64_t H, int64_t I, int64_t g) {
-    return g % 128 == 0 && H % 128 == 0 && I % 128 == 0 && H >= 128 && I >= 128;
+    // (weight tiles per slot: I / 64 for gate/up, H / 128 for down, each indexed in 8 bits)
+    return g % 128 == 0 && H % 128 == 0 && I % 128 == 0 && H >= 128 && I >= 128 && I / 64 <= 256 && H / 128 <= 256;
 }
 
 cudaError_t launch_tc_gemm(TcMode mode, const TcArgs& a, cudaStream_t st) {
@@ -965,6 +1011,7 @@ cudaError_t launch_tc_gemm(TcMode mode, const TcArgs& a, cudaStream_t st) {
         return cudaErrorInvalidValue;
     const bool gateup = mode == TcMode::kGateUp || mode == TcMode::kGateUpPartials;
     const int n_mt = static_cast<int>(gateup ? a.I / 64 : a.H / 128);
+    if (n_mt < 1 || n_mt > 256) return cudaErrorInvalidValue;  // weight tile index kept in 8 bits
     switch (mode) {
         case TcMode::kGateUp: return launch_mode_tc<TcMode::kGateUp>(a, n_mt, st);
         case TcMode::kDown: return launch_mode_tc<TcMode::kDown>(a, n_mt, st);
