@@ -95,14 +95,9 @@ namespace {
 // each group of four epilogue warps cover the four quarters in some order.
 constexpr int kMmaWarp = 0;                  // MMA issue and the tensor-memory allocation
 constexpr int kBWarp = 1;                    // B tiles
-constexpr int kProdWarps = 4;                // one per TMEM lane quarter
-constexpr int kProdWarp0 = 2;
-constexpr int kEpiWarps = 12;                // three per TMEM lane quarter, 64 columns each
-constexpr int kEpiWarp0 = kProdWarp0 + kProdWarps;
-constexpr int kTcThreads = 32 * (kEpiWarp0 + kEpiWarps);
-constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kProdThreads = 32 * kProdWarps;
-constexpr int kColsW = 64;                   // accumulator columns per epilogue warp
+constexpr int kProdWarp0 = 2;                // producers, then the epilogue (split per mode below)
+constexpr int kNumWarps = 18;
+constexpr int kTcThreads = 32 * kNumWarps;
 constexpr int kTileN = 192;                  // tokens per tile (MMA width <= 192)
 constexpr int kAcc = 2;                      // accumulators in tensor memory
 constexpr int kAStages = 2;                  // A stages in tensor memory: one K group (64 columns) each
@@ -115,7 +110,6 @@ constexpr int kBStage = 2 * kBAtom;          // 128 values of K
 constexpr int kRaw = 3;                      // packed weight stages in flight
 constexpr int kRawStage = 128 * 64;          // 128 rows x 64 packed bytes (128 codes)
 constexpr int kMaxSlotsTc = kTcMaxSlots + 1;
-constexpr int kNumWarps = kTcThreads / 32;
 // Shared-memory layout (byte offsets from the 1024-aligned base), one region after another.
 constexpr int kOffB = 0;                                        // [kBStages][2 atoms][192 rows][128 B]
 constexpr int kOffRaw = kOffB + kBStages * kBStage;             // [kRaw][128 rows][64 B], 64-byte swizzle
@@ -132,8 +126,7 @@ constexpr int kSmemTc = kSmemUsed + 1024;                      // + room to alig
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kSleepNs = 20000;  // longest sleep inside one barrier test
 static_assert(kAcc * kTileN + kAStages * kACols <= kTmemCols, "tensor-memory columns");
-static_assert(kEpiWarps * kColsW == 4 * kTileN && kEpiWarps % 4 == 0, "epilogue warps cover the tile");
-static_assert(kProdWarps == 4 && kEpiWarp0 == kProdWarp0 + kProdWarps, "four producers, one per lane quarter");
+
 static_assert(kSmemTc <= 227 * 1024, "shared memory");
 static_assert(kOffRaw % 1024 == 0 && kOffColp % 16 == 0 && kOffBars % 8 == 0, "region alignment");
 static_assert(kRawStage == 128 * 64, "raw stage: 128 rows of 64 packed bytes");
@@ -330,6 +323,21 @@ __device__ __forceinline__ bool named_bar_or(int id, int n, bool v) {
 
 
 
+// Producer / epilogue split of the warps after the two single-thread roles.  The exact modes
+// drain the accumulator every K group, so their epilogue gets 12 warps (64 columns each); the
+// scaled (down) mode drains once per item and its producers carry the scaling, so it gets 8
+// producers (each quarter's rows split in two K halves) and 8 epilogue warps (96 columns each).
+template <TcMode M>
+struct Roles {
+    static constexpr bool scaled = M == TcMode::kDown || M == TcMode::kDownY;
+    static constexpr int prod = scaled ? 8 : 4;
+    static constexpr int epi0 = kProdWarp0 + prod;
+    static constexpr int epi = kNumWarps - epi0;
+    static constexpr int cols = 4 * kTileN / epi;  // accumulator columns per epilogue warp
+    static constexpr int parts = prod / 4;         // K parts of a stage, one per producer warp of a quarter
+    static_assert(prod % 4 == 0 && epi % 4 == 0 && cols % 16 == 0 && 4 * kTileN % epi == 0, "warp split");
+};
+
 struct Item {
     int slot, mt, row0, ntok;
 };
@@ -376,13 +384,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr bool partials = MODE == TcMode::kGateUpPartials || MODE == TcMode::kDownPartials;
     // Down projection outputs: the group scales ride in A and one accumulator sums the item's
     // whole K range.  Every other mode keeps one exact int32 partial per K group.
-    constexpr bool scaled = MODE == TcMode::kDown || MODE == TcMode::kDownY;
+    using R = Roles<MODE>;
+    constexpr bool scaled = R::scaled;
+    constexpr int kColsW = R::cols;
+    constexpr int kEpiThreads = 32 * R::epi;
     const int64_t K = a.K, rows_per_slot = a.rows_per_slot;
     const int ksteps = static_cast<int>(K / 128), spg = a.g / 128, ngrp = static_cast<int>(K / a.g);
     const Ctl ctl{abort_flag, a.hdr};
 
     if (tid == 0) {
-        for (int s = 0; s < kAStages; ++s) mbar_init(a_full + s, kProdThreads);
+        for (int s = 0; s < kAStages; ++s) mbar_init(a_full + s, 32 * R::prod);
         for (int s = 0; s < kBStages; ++s) {
             mbar_init(b_full + s, 1);  // expect-tx arrival + the TMA bytes
             mbar_init(empty + s, 1);
@@ -486,16 +497,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     };
 
-    if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
+    if (warp >= kProdWarp0 && warp < R::epi0) {
         // ------------------------------------------------------------ producers
-        // Thread pt owns tile row pt (TMEM lane pt).  Each warp copies the
-        // packed bytes of its 32 rows for use u + kRaw - 1 into the raw slot
-        // of use u - 1 (which every lane of the warp has read: the warp is
-        // past it), so the unpack never waits for HBM.
+        // Thread pt owns tile row pt (TMEM lane pt), and this warp K part kh of
+        // each stage (all of it, or one half).  Each warp copies its part of
+        // the packed bytes of its 32 rows for use u + kRaw - 1 into the raw
+        // slot of use u - 1 (which every lane of the warp has read: the warp
+        // is past it), so the unpack never waits for HBM.
+        constexpr int kPieces = 4 / R::parts;  // 16-byte pieces (32 codes) of a packed row per warp
         const int pw = warp & 3;  // this warp's tensor-memory lane quarter = its 32 tile rows
+        const int kh = (warp - kProdWarp0) >> 2;
         const int pt = 32 * pw + lane;
         const int rsw = (pt >> 1) & 3;  // 16-byte chunk q of row r sits at q ^ ((r >> 1) & 3): no bank conflicts
-        const int piece = lane & 3;
         Cursor lc{static_cast<int>(blockIdx.x), 0, 0};
         int l_use = 0, l_dec = -1;
         Item l_it{};
@@ -508,8 +521,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint8_t* wslot = a.w + static_cast<int64_t>(l_it.slot) * rows_per_slot * (K / 2);
                 uint8_t* dst = raw + (l_use % kRaw) * kRawStage;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {  // rows 32 pw + 8 q .. + 7, four lanes per row (64 contiguous bytes)
-                    const int row = 32 * pw + 8 * q + (lane >> 2);
+                for (int q = 0; q < kPieces; ++q) {  // kPieces lanes per row, contiguous 16-byte pieces
+                    const int idx = 32 * q + lane;
+                    const int row = 32 * pw + idx / kPieces, piece = kh * kPieces + idx % kPieces;
                     cp_async16(dst + row * 64 + 16 * (piece ^ ((row >> 1) & 3)),
                                wslot + weight_row(l_it.mt, row) * (K / 2) + 64 * lc.ks + 16 * piece);
                 }
@@ -539,9 +553,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 cp_async_wait<kRaw - 1>();    // this lane's copies for this use have landed
                 __syncwarp();                 // ... and the other lanes' copies of this warp's rows
                 const uint4* rp = reinterpret_cast<const uint4*>(raw + (use % kRaw) * kRawStage + pt * 64);
-                uint4 rw[4];
+                uint4 rw[kPieces];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) rw[q] = rp[q ^ rsw];
+                for (int q = 0; q < kPieces; ++q) rw[q] = rp[(kh * kPieces + q) ^ rsw];
                 const int s = use % kAStages;
                 // The A stage is free once the MMAs of use - kAStages have completed (warp-uniform
                 // outcome: the tensor-memory stores below are warp-aligned).
@@ -553,11 +567,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 tc_fence_after();  // the stage's previous MMAs (which read its A columns) are complete
-                // unpacked row -> this thread's tensor-memory lane, 64 columns of fp16
-                // pairs (column c holds K positions 2c, 2c + 1 of the stage)
-                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * pw) << 16) + kACol0 + kACols * s;
+                // unpacked row part -> this thread's tensor-memory lane, 32 columns of fp16 pairs
+                // per 64 codes (column c of the stage holds K positions 2c, 2c + 1)
+                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * pw) << 16) + kACol0 + kACols * s + 32 * kh * (kPieces / 2);
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
+                for (int h2 = 0; h2 < kPieces / 2; ++h2) {
                     uint32_t av[32];
                     const uint32_t words[8] = {rw[2 * h2].x, rw[2 * h2].y, rw[2 * h2].z, rw[2 * h2].w,
                                                rw[2 * h2 + 1].x, rw[2 * h2 + 1].y, rw[2 * h2 + 1].z, rw[2 * h2 + 1].w};
@@ -576,7 +590,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_st_wait();
                 // Thread 0 holds its arrival back until the use's B tiles have landed, so the MMA
                 // thread waits on one barrier per use.
-                if (!__all_sync(0xffffffffu, pt != 0 || wait_bar(b_full + use % kBStages, (use / kBStages) & 1, ctl))) {
+                if (!__all_sync(0xffffffffu, pt != 0 || kh != 0 || wait_bar(b_full + use % kBStages, (use / kBStages) & 1, ctl))) {
                     ok = false;
                     break;
                 }
@@ -663,10 +677,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        // warp w: TMEM lanes 32 (w % 4) .. +31 (tile rows), columns 64 ((w - kEpiWarp0) / 4) .. +63
-        const int quarter = warp & 3, c_base = kColsW * ((warp - kEpiWarp0) >> 2);
+        // warp w: TMEM lanes 32 (w % 4) .. +31 (tile rows), columns kColsW ((w - epi0) / 4) .. +kColsW - 1
+        const int quarter = warp & 3, c_base = kColsW * ((warp - R::epi0) >> 2);
         const int r = 32 * quarter + lane;  // tile row
-        const int et = tid - 32 * kEpiWarp0;  // epilogue thread index
+        const int et = tid - 32 * R::epi0;  // epilogue thread index
         int grp = 0;
         // the pair rows and column scales of an item are loaded one item ahead (their global
         // loads then overlap the previous item's groups) into the other half of colp / colf
