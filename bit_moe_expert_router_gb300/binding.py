@@ -58,6 +58,7 @@ def _load():
     ci = ctypes.c_int
     lib.moe_w4a8_forward_debug.argtypes = [p, p, p, p, p, p, p, dp, p, p, p, p, ci, p, sz, p]
     lib.moe_w4a8_route.argtypes = [p, dp, p, p, p, p, p, p, p, sz, p]
+    lib.moe_w4a8_debug_routing.argtypes = [dp, p, sz, p, p, p, p, p]
     lib.moe_w4a8_gemm1_partials.argtypes = [p, p, dp, p, p, i64, p, ci, p, sz, p]
     lib.moe_w4a8_gemm2_partials.argtypes = [p, p, dp, p, i64, p, ci, p, sz, p]
     lib.moe_w4a8_device_status.argtypes = [p, sz, p]
@@ -75,7 +76,7 @@ def _load():
     for name in ("moe_w4a8_forward", "moe_w4a8_forward_debug", "moe_w4a8_route", "moe_w4a8_gemm1_partials",
                  "moe_w4a8_gemm2_partials", "moe_w4a8_forward_noalloc", "moe_w4a8_device_status",
                  "moe_w4a8_selftest_barrier_timeout", "moe_w4a8_forward_host", "moe_w4a8_forward_bf16",
-                 "moe_w4a8_forward_w2w4"):
+                 "moe_w4a8_forward_w2w4", "moe_w4a8_debug_routing"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.moe_w4a8_version() != ABI_VERSION:
         raise RuntimeError(f"{LIB_PATH}: ABI version {lib.moe_w4a8_version()} != {ABI_VERSION}")
@@ -335,6 +336,17 @@ def moe_w4a8_route(router_logits, d: Dims, topk_ids, topk_w, counts, offsets, pe
     _call("moe_w4a8_route", (router_logits, topk_ids, topk_w, counts, offsets, perm, inv, workspace),
           _ptr(router_logits), ctypes.byref(d), _ptr(topk_ids), _ptr(topk_w), _ptr(counts), _ptr(offsets),
           _ptr(perm), _ptr(inv), wp, wb)
+
+
+def moe_w4a8_debug_routing(d: Dims, workspace, topk_ids, topk_w, perm, inv):
+    """The routing of the last moe_w4a8_forward_debug call on `workspace` (see the header)."""
+    _need(topk_ids, "topk_ids", torch.int32, (d.T, d.top_k))
+    _need(topk_w, "topk_w", torch.float32, (d.T, d.top_k))
+    _need(perm, "perm", torch.int32, (d.T * d.top_k,))
+    _need(inv, "inv", torch.int32, (d.T * d.top_k,))
+    wp, wb = _ws_view(workspace)
+    _call("moe_w4a8_debug_routing", (workspace, topk_ids, topk_w, perm, inv), ctypes.byref(d), wp, wb,
+          _ptr(topk_ids), _ptr(topk_w), _ptr(perm), _ptr(inv))
 
 
 def moe_w4a8_gemm1_partials(x_q, w13_packed, d: Dims, pair_token, pair_slot, p1, workspace,

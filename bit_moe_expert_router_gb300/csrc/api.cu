@@ -137,7 +137,7 @@ bool decode_forward_plan(const moe_dims_t* d, moe::DecodePlan* pl, bool mixed = 
 int run_decode(const int8_t* x_q, const float* x_scale, const float* logits, const uint8_t* w13, const float* s13,
                const uint8_t* w2, const float* s2, const moe_dims_t* d, float* out, const Views& v,
                const moe::DecodePlan& pl, float* y_debug, cudaStream_t st, const uint16_t* x_bf16 = nullptr,
-               const uint8_t* slot_bits = nullptr) {
+               const uint8_t* slot_bits = nullptr, bool route_debug = false) {
     moe::DecodeArgs a{};
     a.x_q = x_q;
     a.x_scale = x_scale;
@@ -163,6 +163,12 @@ int run_decode(const int8_t* x_q, const float* x_scale, const float* logits, con
     a.h = v.h;
     a.amax = v.amax;
     a.y = y_debug;
+    if (route_debug) {  // leave the routing in the workspace arrays the other engines fill
+        a.ids_out = v.ids;
+        a.wts_out = v.wts;
+        a.perm_out = v.perm;
+        a.inv_out = v.inv;
+    }
     MOE_CUDA(moe::launch_decode(moe::DecodeMode::kForward, a, pl, moe::decode_grid(), st));
     return MOE_OK;
 }
@@ -221,11 +227,12 @@ int run_tc_gemms(const int8_t* x_q, const float* x_scale, const uint8_t* w13, co
 // route + permute + gemm1 + gemm2 + combine on the workspace views.
 int run_layer(const int8_t* x_q, const float* x_scale, const float* logits, const uint8_t* w13, const float* s13,
               const uint8_t* w2, const float* s2, const moe_dims_t* d, float* out, const WsLayout& L, const Views& v,
-              cudaStream_t st, int engine = MOE_ENGINE_AUTO, float* y_debug = nullptr) {
+              cudaStream_t st, int engine = MOE_ENGINE_AUTO, float* y_debug = nullptr, bool route_debug = false) {
     if (engine == MOE_ENGINE_AUTO || engine == MOE_ENGINE_DECODE) {
         moe::DecodePlan pl;
         if (decode_forward_plan(d, &pl))
-            return run_decode(x_q, x_scale, logits, w13, s13, w2, s2, d, out, v, pl, y_debug, st);
+            return run_decode(x_q, x_scale, logits, w13, s13, w2, s2, d, out, v, pl, y_debug, st, nullptr, nullptr,
+                              route_debug);
         if (engine == MOE_ENGINE_DECODE) return MOE_ERR_UNSUPPORTED;
     }
     const bool tc = engine == MOE_ENGINE_TCGEN05 || (engine == MOE_ENGINE_AUTO && tc_fits(d));
@@ -507,8 +514,25 @@ MOE_API int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, cons
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (engine < MOE_ENGINE_AUTO || engine > MOE_ENGINE_TCGEN05) return MOE_ERR_INVALID_ARG;
     MOE_TRY(run_layer(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out, L, v, st,
-                      engine, y));
+                      engine, y, true));
     if (h_q || s_h) MOE_CUDA(moe::launch_requant_copy(v.h, v.amax, L.P, d->I, h_q, s_h, st));
+    return MOE_OK;
+}
+
+MOE_API int moe_w4a8_debug_routing(const moe_dims_t* d, const void* workspace, size_t workspace_bytes,
+                                   int32_t* topk_ids, float* topk_w, int32_t* perm, int32_t* inv, void* stream) {
+    MOE_TRY(check_dims(d));
+    if (d->T == 0) return MOE_OK;
+    MOE_TRY(check_ptrs({topk_ids, topk_w, perm, inv}));
+    const WsLayout L = layout_of(d);
+    MOE_TRY(check_ws(L, const_cast<void*>(workspace), workspace_bytes));
+    const Views v = views(const_cast<void*>(workspace), L);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t n = static_cast<size_t>(d->T * d->top_k);
+    MOE_CUDA(cudaMemcpyAsync(topk_ids, v.ids, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    MOE_CUDA(cudaMemcpyAsync(topk_w, v.wts, n * sizeof(float), cudaMemcpyDeviceToDevice, st));
+    MOE_CUDA(cudaMemcpyAsync(perm, v.perm, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    MOE_CUDA(cudaMemcpyAsync(inv, v.inv, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
     return MOE_OK;
 }
 

@@ -505,6 +505,14 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     }
     const int S = routed ? a.S : 0;
     for (int r = tid; r < T * S; r += kThreadsD) s.row_tok[n_rows + r] = r % T;
+    if (routed && blockIdx.x == 0 && a.ids_out) {  // debug copies of the routing (every CTA holds the same)
+        for (int i = tid; i < n_rows; i += kThreadsD) {
+            a.ids_out[i] = s.ids[i];
+            a.wts_out[i] = s.wts[i];
+            a.inv_out[i] = s.pos[i];
+            a.perm_out[s.pos[i]] = i;
+        }
+    }
     const int P_all = n_rows + T * S;
     if (MODE == DecodeMode::kForward)
         for (int i = tid; i < kWarpsD * P_all; i += kThreadsD) s.wmax[i] = 0.f;

@@ -39,6 +39,12 @@ struct DecodeArgs {
     float* h;                // [P][I]
     uint32_t* amax;          // [P] row maxima (debug copies; may be null)
     float* y;                // [P][H] (debug copies; may be null)
+    // the routing of the launch (debug copies, written by CTA 0; may be null): ids and weights
+    // [T][k], perm [T*k] (pair row -> pair) and inv [T*k] (pair -> pair row)
+    int32_t* ids_out;
+    float* wts_out;
+    int32_t* perm_out;
+    int32_t* inv_out;
 };
 
 // Byte offsets of the shared-memory arrays of one launch.

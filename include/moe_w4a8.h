@@ -172,6 +172,19 @@ int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, const float*
                            int engine, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The routing used by the last moe_w4a8_forward_debug call on `workspace`
+ * (any engine; the decode engine copies its own in-kernel routing there):
+ * topk_ids int32 [T][k] and topk_w float [T][k] in rank order (largest
+ * logit first, ties by lower expert id), perm int32 [T*k] (pair row ->
+ * pair index t*k + j) and inv int32 [T*k] (pair index -> pair row), as
+ * moe_w4a8_route returns them.  All four are device pointers; the copies
+ * are enqueued on `stream`.  The values are unspecified if no forward_debug
+ * call with the same dims has run on this workspace.
+ */
+int moe_w4a8_debug_routing(const moe_dims_t* d, const void* workspace, size_t workspace_bytes,
+                           int32_t* topk_ids, float* topk_w, int32_t* perm, int32_t* inv, void* stream);
+
+/*
  * Int32 partial sums of the gate/up projection for an explicit list of
  * pairs, through the main loop of the chosen engine (MOE_ENGINE_GROUPED,
  * MOE_ENGINE_DECODE or MOE_ENGINE_TCGEN05; AUTO means GROUPED): for pair r

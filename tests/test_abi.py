@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
             "moe_w4a8_status_string", "moe_w4a8_gemm1_partials", "moe_w4a8_gemm2_partials",
             "moe_w4a8_forward_debug", "moe_w4a8_device_status", "moe_w4a8_forward_host",
             "moe_w4a8_forward_host_workspace_size", "moe_w4a8_forward_bf16", "moe_w4a8_forward_w2w4",
-            "moe_w4a8_forward_bf16_workspace_size"} <= names
+            "moe_w4a8_forward_bf16_workspace_size", "moe_w4a8_debug_routing"} <= names
 
 
 def test_library_exports_every_declared_symbol(cuda_lib, lib):
@@ -112,6 +112,9 @@ def test_null_and_misaligned_pointers_are_rejected(lib):
     need = lib.moe_w4a8_workspace_size(ctypes.byref(d))
     assert lib.moe_w4a8_forward(*args, ctypes.byref(d), fake, fake, need - 256, None) == 3
     assert lib.moe_w4a8_route(fake, ctypes.byref(d), fake, fake, fake, fake, fake, None, fake, need, None) == 1
+    # the routing read-back: a null output, then a workspace too small
+    assert lib.moe_w4a8_debug_routing(ctypes.byref(d), fake, need, fake, None, fake, fake, None) == 1
+    assert lib.moe_w4a8_debug_routing(ctypes.byref(d), fake, need - 256, fake, fake, fake, fake, None) == 3
 
 
 def test_partials_workspace_covers_grouping_and_fp16_rows(lib):

@@ -355,6 +355,62 @@ def test_decode_engine_routes_planted_ties(E):
     gh.assert_output_close(out, gh.oracle_out(w, tok, gh.bank_of(w)), f"decode ties E={E}")
 
 
+def _debug_routing(w, tok, engine):
+    """Runs moe_w4a8_forward_debug on `engine` and reads back the routing it used."""
+    w13, s13, w2, s2 = gh.device_bank(w)
+    d = gh.dims(w)
+    dev = "cuda:0"
+    out = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+    ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), dev)
+    binding.moe_w4a8_forward_debug(gh.to_dev(tok.x_q), gh.to_dev(tok.x_scale), gh.to_dev(tok.logits), w13, s13, w2,
+                                   s2, d, out, ws, engine=engine)
+    got = dict(ids=torch.empty((w.T, w.top_k), dtype=torch.int32, device=dev),
+               w=torch.empty((w.T, w.top_k), dtype=torch.float32, device=dev),
+               perm=torch.empty(w.T * w.top_k, dtype=torch.int32, device=dev),
+               inv=torch.empty(w.T * w.top_k, dtype=torch.int32, device=dev))
+    binding.moe_w4a8_debug_routing(d, ws, got["ids"], got["w"], got["perm"], got["inv"])
+    torch.cuda.synchronize()
+    assert binding.moe_w4a8_device_status(ws) == 0
+    return {k_: v.cpu().numpy() for k_, v in got.items()}
+
+
+@pytest.mark.parametrize("name,engine", [("decode_t4", 1), ("decode_verify_t12", 1), ("dec_small", 1),
+                                         ("decode_t4", 0), ("tc_small", 2)])
+def test_engine_routing_is_the_oracles(name, engine):
+    """The routing each engine used inside the layer call (the decode kernel's own in-kernel top-k and pair
+    sort included): ids, permutation and inverse bit-exact against the oracle, weights within 2e-6."""
+    w = _workload(name)
+    tok = synth.make_tokens(w)
+    got = _debug_routing(w, tok, engine)
+    ids, wt = oracle.route(tok.logits, w.top_k)
+    _, _, perm, inv = oracle.permute(ids, w.E)
+    assert np.array_equal(got["ids"], ids)
+    assert np.array_equal(got["perm"], perm)
+    assert np.array_equal(got["inv"], inv)
+    assert np.max(np.abs(got["w"] - wt)) < 2e-6
+
+
+@pytest.mark.parametrize("E", [64, 600])
+def test_decode_engine_routing_of_planted_ties_is_the_oracles(E):
+    """Massively tied and signed-zero logits through the decode kernel's own routing (E > 512 takes its
+    wide path): ids and permutation bit-exact."""
+    w = synth.Workload("dties", T=12, H=2048, I=512, E=E, S=1, top_k=6, group=128)
+    tok = synth.make_tokens(w)
+    rng = np.random.default_rng(7)
+    lg = rng.integers(-2, 3, size=(w.T, w.E)).astype(np.float32)
+    lg[rng.random(lg.shape) < 0.2] = -0.0
+    lg[0, :] = 0.0
+    lg[1, :] = -0.0
+    tok.logits[...] = lg
+    got = _debug_routing(w, tok, 1)
+    ids, wt = oracle.route(tok.logits, w.top_k)
+    _, _, perm, inv = oracle.permute(ids, w.E)
+    assert np.array_equal(got["ids"], ids)
+    assert np.array_equal(got["perm"], perm)
+    assert np.array_equal(got["inv"], inv)
+    assert np.max(np.abs(got["w"] - wt)) < 2e-6
+
+
 def test_decode_engine_ranks_nan_logits_last():
     """NaN logits in the decode kernel's own routing: never chosen while k numbers remain, so those tokens
     match the oracle; a token whose logits are all NaN gets the lowest k experts (NaN weights, NaN output)."""
