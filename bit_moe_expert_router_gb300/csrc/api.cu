@@ -202,17 +202,20 @@ moe::TcArgs tc_args(const uint8_t* w, const float* ws, int64_t rows_per_slot, in
 
 // gemm1 + act, requant, gemm2 and the combine on the tcgen05 engine (routing and grouping done).
 // y_debug: also the per-pair outputs Y in fp32.
+// slot_bits: each slot's code width (2 or 4) of a mixed bank, or null.
 int run_tc_gemms(const int8_t* x_q, const float* x_scale, const uint8_t* w13, const float* s13, const uint8_t* w2,
                  const float* s2, const moe_dims_t* d, float* out, const WsLayout& L, const Views& v, float* y_debug,
-                 cudaStream_t st) {
+                 cudaStream_t st, const uint8_t* slot_bits = nullptr) {
     const int n_slots = static_cast<int>(d->E + d->n_shared);
     // the activations gathered by pair row (fp16, the engine's K order): contiguous B tiles for gate/up
     MOE_CUDA(moe::launch_prep_x16(x_q, d->T, d->H, v.row_token, L.P, v.x16, st));
     moe::TcArgs g1 = tc_args(w13, s13, 2 * d->I, d->H, d, v.x16, L.P, x_scale, v, n_slots);
+    g1.slot_bits = slot_bits;
     g1.h = v.h;
     MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kGateUp, g1, st));
     MOE_CUDA(moe::launch_prep_h16(v.h, v.amax, nullptr, L.P, d->I, v.h16, v.sh, st));
     moe::TcArgs g2 = tc_args(w2, s2, d->H, d->I, d, v.h16, L.P, v.sh, v, n_slots);
+    g2.slot_bits = slot_bits;
     __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(v.y);  // the Y area holds bf16 Y here
     g2.yb = yb;
     MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kDown, g2, st));
@@ -492,10 +495,17 @@ MOE_API int moe_w4a8_forward_w2w4(const int8_t* x_q, const float* x_scale, const
     MOE_TRY(check_ptrs({x_q, x_scale, router_logits, out}));
     const WsLayout L = layout_of(d);
     MOE_TRY(check_ws(L, workspace, workspace_bytes));
+    const Views v = views(workspace, L);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
     moe::DecodePlan pl;
-    if (!decode_forward_plan(d, &pl, true)) return MOE_ERR_UNSUPPORTED;  // mixed banks: the decode engine's sizes
-    return run_decode(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out,
-                      views(workspace, L), pl, nullptr, static_cast<cudaStream_t>(stream), nullptr, slot_bits);
+    if (decode_forward_plan(d, &pl, true))  // small batches: the decode engine
+        return run_decode(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out, v, pl,
+                          nullptr, st, nullptr, slot_bits);
+    if (!tc_fits(d)) return MOE_ERR_UNSUPPORTED;  // large batches: the tcgen05 engine's sizes
+    MOE_CUDA(moe::launch_route_topk(router_logits, d->T, d->E, d->top_k, v.ids, v.wts, st));
+    MOE_CUDA(moe::launch_sort(sort_args(v, v.ids, d->T, d->top_k, d->E, d->n_shared, L.P), st));
+    return run_tc_gemms(x_q, x_scale, w13_packed, w13_scale, w2_packed, w2_scale, d, out, L, v, nullptr, st,
+                        slot_bits);
 }
 
 MOE_API int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, const float* router_logits,

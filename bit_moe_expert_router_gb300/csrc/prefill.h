@@ -20,6 +20,8 @@ struct TcArgs {
     // A operand: packed int4 weight rows of every bank slot with their group scales
     const uint8_t* w;         // [slots][rows_per_slot][K/2]
     const float* ws;          // [slots][rows_per_slot][K/g]
+    const uint8_t* slot_bits; // code width of each slot (2 or 4), or null (all 4): a 2-bit row holds its
+                              // K codes in its first K/4 bytes, element 4j + p in bits 2p, 2p+1 of byte j
     int64_t rows_per_slot;    // 2I (gate/up) or H (down)
     int64_t K;                // H (gate/up) or I (down)
     int g;

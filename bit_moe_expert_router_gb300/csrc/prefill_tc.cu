@@ -294,6 +294,25 @@ __device__ __forceinline__ void unpack_int4_f16(uint32_t w, uint32_t* r) {
     r[3] = *reinterpret_cast<const uint32_t*>(&h3);
 }
 
+// Sixteen packed 2-bit codes (element 4j + p in bits 2p, 2p+1 of byte j, two's complement in
+// [-2, 1]) -> fp16 pairs (0,4) (1,5) (2,6) (3,7) of each 8, the same K order as the int4 unpack.  A
+// field f satisfies f ^ 2 = c + 2: in the low mantissa bits of fp16 0x6400 (1024) it gives
+// 1024 + c + 2, and subtracting 1026 leaves c.  Bytes 0 and 1 hold codes 0-3 and 4-7, so spreading
+// them to the two halves of a word lines each pair's codes up in one shift and one mask.
+__device__ __forceinline__ void unpack_int2_f16(uint32_t w, uint32_t* r) {
+    const __half2 sub = __halves2half2(__ushort_as_half(0x6402), __ushort_as_half(0x6402));  // 1026
+    const uint32_t y0 = __byte_perm(w, 0u, 0x4140), y1 = __byte_perm(w, 0u, 0x4342);  // bytes (0,1), (2,3) -> halves
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint32_t q0 = ((y0 >> (2 * p)) & 0x00030003u) ^ 0x64026402u;
+        const uint32_t q1 = ((y1 >> (2 * p)) & 0x00030003u) ^ 0x64026402u;
+        const __half2 h0 = __hsub2(*reinterpret_cast<const __half2*>(&q0), sub);
+        const __half2 h1 = __hsub2(*reinterpret_cast<const __half2*>(&q1), sub);
+        r[p] = *reinterpret_cast<const uint32_t*>(&h0);
+        r[4 + p] = *reinterpret_cast<const uint32_t*>(&h1);
+    }
+}
+
 // Largest |scale| of a weight row's n groups (0 for an all-zero row).  The producers put each
 // group's scale into A as a fraction of it and the epilogue multiplies it back: both read the same
 // values, and a maximum does not depend on the order it is taken in.
@@ -511,21 +530,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int rsw = (pt >> 1) & 3;  // 16-byte chunk q of row r sits at q ^ ((r >> 1) & 3): no bank conflicts
         Cursor lc{static_cast<int>(blockIdx.x), 0, 0};
         int l_use = 0, l_dec = -1;
+        bool l_two = false;  // the fetched item's slot holds 2-bit codes
         Item l_it{};
         auto fetch = [&]() {  // this warp's rows of use l_use into raw slot l_use % kRaw (one commit group)
             if (lc.item < total) {
                 if (lc.item != l_dec) {
                     l_it = item_at(lc.j, lc.item);
                     l_dec = lc.item;
+                    l_two = a.slot_bits && a.slot_bits[l_it.slot] == 2;
                 }
                 const uint8_t* wslot = a.w + static_cast<int64_t>(l_it.slot) * rows_per_slot * (K / 2);
                 uint8_t* dst = raw + (l_use % kRaw) * kRawStage;
+                if (!l_two) {
 #pragma unroll
-                for (int q = 0; q < kPieces; ++q) {  // kPieces lanes per row, contiguous 16-byte pieces
-                    const int idx = 32 * q + lane;
-                    const int row = 32 * pw + idx / kPieces, piece = kh * kPieces + idx % kPieces;
-                    cp_async16(dst + row * 64 + 16 * (piece ^ ((row >> 1) & 3)),
-                               wslot + weight_row(l_it.mt, row) * (K / 2) + 64 * lc.ks + 16 * piece);
+                    for (int q = 0; q < kPieces; ++q) {  // kPieces lanes per row, contiguous 16-byte pieces
+                        const int idx = 32 * q + lane;
+                        const int row = 32 * pw + idx / kPieces, piece = kh * kPieces + idx % kPieces;
+                        cp_async16(dst + row * 64 + 16 * (piece ^ ((row >> 1) & 3)),
+                                   wslot + weight_row(l_it.mt, row) * (K / 2) + 64 * lc.ks + 16 * piece);
+                    }
+                } else {
+                    // a 2-bit row holds a use's 128 codes in 32 bytes: this warp's K part is the first
+                    // kPieces / 2 of its pieces
+#pragma unroll
+                    for (int q = 0; q < kPieces; ++q) {
+                        const int idx = 32 * q + lane, lp = idx % kPieces;
+                        const int row = 32 * pw + idx / kPieces, piece = kh * kPieces + lp;
+                        if (lp < kPieces / 2)
+                            cp_async16(dst + row * 64 + 16 * (piece ^ ((row >> 1) & 3)),
+                                       wslot + weight_row(l_it.mt, row) * (K / 2) + 32 * lc.ks +
+                                           16 * (kh * (kPieces / 2) + lp));
+                    }
                 }
                 advance(lc);
             }
@@ -541,6 +576,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // Other modes: A is the bare code.
             const float* srow = nullptr;
             float inv = 0.f;
+            const bool two = a.slot_bits && a.slot_bits[item_at(j, item).slot] == 2;
             if (scaled) {
                 const Item it = item_at(j, item);
                 srow = a.ws + (static_cast<int64_t>(it.slot) * rows_per_slot + weight_row(it.mt, pt)) * ngrp;
@@ -573,10 +609,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int h2 = 0; h2 < kPieces / 2; ++h2) {
                     uint32_t av[32];
-                    const uint32_t words[8] = {rw[2 * h2].x, rw[2 * h2].y, rw[2 * h2].z, rw[2 * h2].w,
-                                               rw[2 * h2 + 1].x, rw[2 * h2 + 1].y, rw[2 * h2 + 1].z, rw[2 * h2 + 1].w};
+                    if (!two) {
+                        const uint32_t words[8] = {rw[2 * h2].x, rw[2 * h2].y, rw[2 * h2].z, rw[2 * h2].w,
+                                                   rw[2 * h2 + 1].x, rw[2 * h2 + 1].y, rw[2 * h2 + 1].z, rw[2 * h2 + 1].w};
 #pragma unroll
-                    for (int wi = 0; wi < 8; ++wi) unpack_int4_f16(words[wi], av + 4 * wi);
+                        for (int wi = 0; wi < 8; ++wi) unpack_int4_f16(words[wi], av + 4 * wi);
+                    } else {  // 64 2-bit codes of piece h2
+                        const uint32_t words[4] = {rw[h2].x, rw[h2].y, rw[h2].z, rw[h2].w};
+#pragma unroll
+                        for (int wi = 0; wi < 4; ++wi) unpack_int2_f16(words[wi], av + 8 * wi);
+                    }
                     if (scaled) {
                         const __half2 f2 = __float2half2_rn(sg * inv);
 #pragma unroll

@@ -346,9 +346,10 @@ int moe_w4a8_forward_bf16(const uint16_t* x_bf16, const float* router_logits,
  * two's-complement number in [-2, 1]; the rest of the row is never read.
  * Scales are unchanged (one per row and group).  A 2-bit slot's code bytes
  * -- what a decode step streams -- are half those of a 4-bit slot.
- * Supported for the sizes the decode engine takes (T <= 32, T*k <= 512,
- * H in {2048, 4096}, I in {512, 1536}, g a multiple of 64 with I/g a
- * multiple of 4); otherwise MOE_ERR_UNSUPPORTED.  A null slot_bits is
+ * Small batches run on the decode engine (T <= 32, T*k <= 512, H in
+ * {2048, 4096}, I in {512, 1536}, g a multiple of 64 with I/g a multiple
+ * of 4), larger ones on the tcgen05 engine (H and I multiples of 128, g a
+ * multiple of 128, E+S <= 1039); other sizes return MOE_ERR_UNSUPPORTED.  A null slot_bits is
  * MOE_ERR_INVALID_ARG (it needs no particular alignment; a value other than
  * 2 is read as 4).  Other arguments, workspace (moe_w4a8_workspace_size)
  * and errors as for moe_w4a8_forward; with every slot 4-bit the result

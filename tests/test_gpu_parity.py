@@ -650,3 +650,49 @@ def test_mixed_2bit_bank_on_the_decode_engine(name):
     binding.moe_w4a8_forward_w2w4(*x, w13, s13, w2, s2, all4, d, out, ws)
     torch.cuda.synchronize()
     assert np.array_equal(out.cpu().numpy(), ref)
+
+
+TC_MIXED = synth.Workload("tc_mixed", T=400, H=512, I=256, E=8, S=1, top_k=2, group=128, twobit_frac=0.5)
+
+
+@pytest.mark.parametrize("name", ["tc_mixed", "large_bank_t2048"])
+def test_mixed_2bit_bank_on_the_tcgen05_engine(name):
+    """A mixed 2/4-bit bank on the tcgen05 engine (batches past the decode engine's range): against the
+    oracle (every token of the small case; for the 2048-token large bank the 48 sampled tokens plus those
+    routed to the least-loaded experts), against the same codes in int4 storage, and bit for bit against
+    the int4 path when every slot is 4-bit."""
+    w = TC_MIXED if name == "tc_mixed" else synth.WORKLOADS[name]
+    tok = synth.make_tokens(w)
+    b2 = synth.make_bank(w, pack2=True)
+    assert (b2.slot_bits == 2).sum() >= 2
+    d = gh.dims(w)
+    assert binding.moe_w4a8_engine_for(d) == 2
+    dev = [gh.to_dev(a) for a in (b2.w13, b2.s13, b2.w2, b2.s2)]
+    bits = gh.to_dev(b2.slot_bits)
+    ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), "cuda:0")
+    x = [gh.to_dev(a) for a in (tok.x_q, tok.x_scale, tok.logits)]
+    out = torch.empty((w.T, w.H), dtype=torch.float32, device="cuda:0")
+    binding.moe_w4a8_forward_w2w4(*x, *dev, bits, d, out, ws)
+    torch.cuda.synchronize()
+    assert binding.moe_w4a8_device_status(ws) == 0
+    got = out.cpu().numpy()
+    sel = np.arange(w.T) if w.T <= 400 else gh.sample_tokens(w.T, 48)
+    if w.T > 400:
+        ids, _ = oracle.route(tok.logits, w.top_k)
+        counts = np.bincount(ids.ravel(), minlength=w.E)
+        tail = [e for e in np.argsort(counts, kind="stable") if counts[e] > 0][:6]
+        sel = np.union1d(sel, np.nonzero(np.isin(ids, tail).any(axis=1))[0][:48])
+    gh.assert_output_close(got[sel], oracle.forward_workload(w, tok, b2, sel), f"mixed bank {name} (tcgen05)")
+    # the same codes in int4 storage through the int4 path of the same engine
+    w13, s13, w2, s2 = gh.device_bank(w)
+    ref = torch.empty_like(out)
+    binding.moe_w4a8_forward(*x, w13, s13, w2, s2, d, ref, ws)
+    ref = ref.cpu().numpy()
+    rms = np.sqrt(np.mean(ref.astype(np.float64) ** 2))
+    # the same integer products; only a requantisation code one step apart at a half-step can differ
+    assert np.max(np.abs(got - ref)) <= 1e-3 * rms
+    all4 = torch.full((w.E + w.S,), 4, dtype=torch.uint8, device="cuda:0")
+    binding.moe_w4a8_forward_w2w4(*x, w13, s13, w2, s2, all4, d, out, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), ref)
+
