@@ -199,6 +199,20 @@ def touched_bytes(w, logits_batches):
     return float(np.mean(tot))
 
 
+def touched_bytes_mixed(w, logits_batches, slot_bits):
+    """touched_bytes for a bank whose 2-bit slots (slot_bits[e] == 2) are stored 4 codes per byte: such a
+    slot's code bytes halve, its scales stay."""
+    codes = w.H * (2 * w.I) // 2 + w.I * w.H // 2
+    tot = []
+    for lg in logits_batches:
+        ids = np.argsort(-lg, axis=1, kind="stable")[:, :w.top_k]
+        slots = list(np.unique(ids)) + [w.E + s for s in range(w.S)]
+        two = sum(1 for e in slots if slot_bits[e] == 2)
+        act = w.T * w.H + 4 * w.T + 4 * w.T * w.E + 4 * w.T * w.H
+        tot.append(len(slots) * per_expert_bytes(w) - two * codes // 2 + act)
+    return float(np.mean(tot))
+
+
 def step_ops(w) -> float:
     """Integer multiply-adds of one step counted as 2 ops each: every pair row's gate/up and down projections."""
     return float(w.pairs) * 2.0 * (2 * w.I * w.H + w.H * w.I)
@@ -352,6 +366,8 @@ def run_ours(a):
             ent["tokens_per_s"] = whole_job_rate(wx.T, world, msx, a.steps)
             ent["region_ms"] = {"median": msx, "min": mnx, "max": mxx, "repeats": a.repeats}
             ent["config"] = _config(wx, world)
+            if wx.twobit_frac > 0:
+                ent["mixed_2bit_storage"] = _mixed_entry(wx, dx, bx, stepx, a, stream, dev, binding, world)
             extra[name] = ent
             del wsx
             torch.cuda.empty_cache()
@@ -425,6 +441,37 @@ def _roofline_entry(w, ms_per_step, logits_batches, hbm_peak, tf_peak, peak_kind
                  "hbm_GBs": gbs, "hbm_frac": gbs / hbm_peak, "tensor_TOPs": tops, "tensor_frac": tops / tf_peak,
                  "roofline_ms": max(t_hbm, t_tc) * 1e3, "roofline_frac": max(t_hbm, t_tc) / t})
     return {"ms_per_step": ms_per_step, "engine": engine_name, "roofline": roof}
+
+
+def _mixed_entry(w, d, batches, step_int4, a, stream, dev, binding, world):
+    """The same workload with its 2-bit experts stored 4 codes per byte (moe_w4a8_forward_w2w4): time and
+    algorithmic bytes beside the int4 storage's (the same codes)."""
+    import torch
+    from bit_moe_expert_router_gb300 import synth
+    b2 = synth.make_bank(w, pack2=True)
+    bank = tuple(torch.from_numpy(x).to(dev) for x in (b2.w13, b2.s13, b2.w2, b2.s2))
+    bits = torch.from_numpy(b2.slot_bits).to(dev)
+    dev_batches = [tuple(torch.from_numpy(x).to(dev) for x in (t.x_q, t.x_scale, t.logits)) for t in batches]
+    ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), dev)
+    out = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+
+    def step(i):
+        x_q, x_s, lg = dev_batches[i % len(dev_batches)]
+        binding.moe_w4a8_forward_w2w4(x_q, x_s, lg, *bank, bits, d, out, ws)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(a.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize(dev)
+    ms, mn, mx = time_region(step, a.steps, a.repeats, stream, dev)
+    ms = max_over_ranks(ms, world, dev)
+    lgs = [t.logits for t in batches]
+    return {"ms_per_step": ms / a.steps, "algorithmic_bytes_per_step": touched_bytes_mixed(w, lgs, b2.slot_bits),
+            "int4_storage_bytes_per_step": touched_bytes(w, lgs),
+            "bank_bytes": int(b2.w13.nbytes + b2.s13.nbytes + b2.w2.nbytes + b2.s2.nbytes),
+            "note": "2-bit slots keep the int4 row length (codes in the first half of each row): the bytes read "
+                    "halve for those slots, the bank's storage does not",
+            "region_ms": {"median": ms, "min": mn, "max": mx, "repeats": a.repeats}}
 
 
 def _e2e(w, d, banks, batches, steps, stream, dev, binding):
