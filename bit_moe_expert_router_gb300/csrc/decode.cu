@@ -12,10 +12,13 @@
 //            k rounds of a warp arg-max) while its other warps stage the
 //            activations in shared memory (int8 input split even|odd; bf16
 //            input quantised here first: S0, s = max|x| / 127, RNE codes);
-//            then it sorts the pairs stably by expert into pair rows and builds
+//            then it groups the pairs stably by expert into pair rows and builds
 //            the slot table (touched experts ascending, then the shared
 //            experts; with each slot's code width for a mixed 2/4-bit bank)
-//            and a per-slot cost prefix.
+//            from per-expert token masks and expert presence bits (a pair's
+//            slot is a popcount of the presence bits below its expert, its row
+//            in the slot a popcount of its expert's mask below its token), and
+//            a per-slot cost prefix.
 //   phase 1  gate/up projection with dp4a on the CUDA cores: units of two
 //            intermediate indices (2 gate rows + the 2 matching up rows) of
 //            one slot; each warp takes a contiguous unit range of equal cost
@@ -483,27 +486,133 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
             for (int t = tid - st0; t < T; t += nst) s.xs[t] = routed ? a.x_scale[t] : 1.0f;
         }
     }
+    // routed: per-expert token masks and expert presence bits for the grouping below, in the
+    // requantised-row area (first written in phase 2)
+    uint32_t* emask = reinterpret_cast<uint32_t*>(s.hq);  // [E] bit t: token t picked the expert
+    uint32_t* pres = emask + a.E;                          // [EW] bit e: expert e was picked
+    int* pbase = reinterpret_cast<int*>(pres + (a.E + 31) / 32);  // [EW] experts picked in earlier words
+    const int EW = (a.E + 31) / 32;
+    if (routed)
+        for (int i = tid; i < a.E + EW; i += kThreadsD) emask[i] = 0u;
     __syncthreads();
-    // stable rank of each pair by expert id (n_rows <= kDecodeMaxPairs), whether
-    // it is its expert's first pair, and how many pairs share its expert
-    for (int i = tid; i < n_rows; i += kThreadsD) {
-        const int e = s.ids[i];
-        int p = 0, eq = 0;
-        bool first = true;
-#pragma unroll 4
-        for (int j = 0; j < n_rows; ++j) {
-            const int f = s.ids[j];
-            p += (f < e) || (f == e && j < i);
-            eq += f == e;
-            first = first && !(f == e && j < i);
-        }
-        s.pos[i] = p;
-        s.pair_of[p] = i;
-        s.row_tok[p] = routed ? i / k : (MODE == DecodeMode::kGemm1Partials ? min(max(a.pair_token[i], 0), T - 1) : p);
-        s.first[i] = first;
-        s.eqc[i] = eq;
-    }
     const int S = routed ? a.S : 0;
+    if (routed) {
+        // Grouping from bitmaps (T <= 32, and top-k picks an expert at most once per token): a pair's
+        // slot is the number of picked experts below its expert, its row within the slot the number
+        // of earlier tokens that picked the same expert -- the stable order by (expert, pair index).
+        for (int i = tid; i < n_rows; i += kThreadsD) {
+            const int e = s.ids[i];
+            atomicOr(emask + e, 1u << (i / k));
+            atomicOr(pres + (e >> 5), 1u << (e & 31));
+        }
+        __syncthreads();
+        if (warp == 0) {  // exclusive prefix of the presence popcounts; the shared slots after the routed ones
+            int run = 0;
+            for (int b0 = 0; b0 < EW; b0 += 32) {
+                const int wi = b0 + lane;
+                const int c = wi < EW ? __popc(pres[wi]) : 0;
+                int incl = c;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += o;
+                }
+                if (wi < EW) pbase[wi] = run + incl - c;
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            for (int sh = lane; sh < S; sh += 32) {
+                s.slot_e[run + sh] = a.E + sh;
+                s.slot_row0[run + sh] = n_rows + sh * T;
+                s.slot_cnt[run + sh] = T;
+                s.slot_bw[run + sh] = (MIXED && a.slot_bits) ? (a.slot_bits[a.E + sh] == 2 ? 2 : 4) : 4;
+            }
+            if (lane == 0) s.n_slots[0] = run + S;
+        }
+        __syncthreads();
+        for (int i = tid; i < n_rows; i += kThreadsD) {
+            const int e = s.ids[i], t = i / k;
+            const uint32_t m = emask[e];
+            const int u = pbase[e >> 5] + __popc(pres[e >> 5] & ((1u << (e & 31)) - 1u));
+            const int within = __popc(m & ((1u << t) - 1u));
+            if (within == 0) {
+                s.slot_e[u] = e;
+                s.slot_cnt[u] = __popc(m);
+                s.slot_bw[u] = (MIXED && a.slot_bits) ? (a.slot_bits[e] == 2 ? 2 : 4) : 4;
+            }
+            s.first[i] = u;  // (scratch here: the pair's slot and its rank within the slot)
+            s.eqc[i] = within;
+        }
+        __syncthreads();
+        if (warp == 0) {  // first pair row of each routed slot: exclusive prefix of the counts
+            const int nr = s.n_slots[0] - S;
+            int run = 0;
+            for (int b0 = 0; b0 < nr; b0 += 32) {
+                const int u = b0 + lane;
+                const int c = u < nr ? s.slot_cnt[u] : 0;
+                int incl = c;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += o;
+                }
+                if (u < nr) s.slot_row0[u] = run + incl - c;
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+        }
+        __syncthreads();
+        for (int i = tid; i < n_rows; i += kThreadsD) {
+            const int p = s.slot_row0[s.first[i]] + s.eqc[i];
+            s.pos[i] = p;
+            s.pair_of[p] = i;
+            s.row_tok[p] = i / k;
+        }
+    } else {
+        // stable rank of each pair by expert id (n_rows <= kDecodeMaxPairs), whether
+        // it is its expert's first pair, and how many pairs share its expert
+        for (int i = tid; i < n_rows; i += kThreadsD) {
+            const int e = s.ids[i];
+            int p = 0, eq = 0;
+            bool first = true;
+#pragma unroll 4
+            for (int j = 0; j < n_rows; ++j) {
+                const int f = s.ids[j];
+                p += (f < e) || (f == e && j < i);
+                eq += f == e;
+                first = first && !(f == e && j < i);
+            }
+            s.pos[i] = p;
+            s.pair_of[p] = i;
+            s.row_tok[p] = routed ? i / k : (MODE == DecodeMode::kGemm1Partials ? min(max(a.pair_token[i], 0), T - 1) : p);
+            s.first[i] = first;
+            s.eqc[i] = eq;
+        }
+        __syncthreads();
+        // slot table: touched experts ascending (slot = number of smaller touched
+        // experts), then the shared experts
+        for (int i = tid; i < n_rows; i += kThreadsD) {
+            if (!s.first[i]) continue;
+            const int e = s.ids[i];
+            int u = 0;
+#pragma unroll 4
+            for (int j = 0; j < n_rows; ++j) u += s.first[j] && s.ids[j] < e;
+            s.slot_e[u] = e;
+            s.slot_row0[u] = s.pos[i];
+            s.slot_cnt[u] = s.eqc[i];
+            s.slot_bw[u] = (MIXED && a.slot_bits) ? (a.slot_bits[e] == 2 ? 2 : 4) : 4;
+        }
+        if (warp == 0) {
+            int nr = 0;
+            for (int b0 = 0; b0 < n_rows; b0 += 32)
+                nr += __popc(__ballot_sync(0xffffffffu, b0 + lane < n_rows && s.first[b0 + lane]));
+            for (int sh = lane; sh < S; sh += 32) {
+                s.slot_e[nr + sh] = a.E + sh;
+                s.slot_row0[nr + sh] = n_rows + sh * T;
+                s.slot_cnt[nr + sh] = T;
+                s.slot_bw[nr + sh] = (MIXED && a.slot_bits) ? (a.slot_bits[a.E + sh] == 2 ? 2 : 4) : 4;
+            }
+            if (lane == 0) s.n_slots[0] = nr + S;
+        }
+    }
     for (int r = tid; r < T * S; r += kThreadsD) s.row_tok[n_rows + r] = r % T;
     if (routed && blockIdx.x == 0 && a.ids_out) {  // debug copies of the routing (every CTA holds the same)
         for (int i = tid; i < n_rows; i += kThreadsD) {
@@ -516,32 +625,6 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     const int P_all = n_rows + T * S;
     if (MODE == DecodeMode::kForward)
         for (int i = tid; i < kWarpsD * P_all; i += kThreadsD) s.wmax[i] = 0.f;
-    __syncthreads();
-    // slot table: touched experts ascending (slot = number of smaller touched
-    // experts), then the shared experts
-    for (int i = tid; i < n_rows; i += kThreadsD) {
-        if (!s.first[i]) continue;
-        const int e = s.ids[i];
-        int u = 0;
-#pragma unroll 4
-        for (int j = 0; j < n_rows; ++j) u += s.first[j] && s.ids[j] < e;
-        s.slot_e[u] = e;
-        s.slot_row0[u] = s.pos[i];
-        s.slot_cnt[u] = s.eqc[i];
-        s.slot_bw[u] = (MIXED && a.slot_bits) ? (a.slot_bits[e] == 2 ? 2 : 4) : 4;
-    }
-    if (warp == 0) {
-        int nr = 0;
-        for (int b0 = 0; b0 < n_rows; b0 += 32)
-            nr += __popc(__ballot_sync(0xffffffffu, b0 + lane < n_rows && s.first[b0 + lane]));
-        for (int sh = lane; sh < S; sh += 32) {
-            s.slot_e[nr + sh] = a.E + sh;
-            s.slot_row0[nr + sh] = n_rows + sh * T;
-            s.slot_cnt[nr + sh] = T;
-            s.slot_bw[nr + sh] = (MIXED && a.slot_bits) ? (a.slot_bits[a.E + sh] == 2 ? 2 : 4) : 4;
-        }
-        if (lane == 0) s.n_slots[0] = nr + S;
-    }
     __syncthreads();
     const int n_slots = s.n_slots[0];
     for (int u = warp; u < n_slots; u += kWarpsD)  // pair row -> its slot
@@ -1001,7 +1084,10 @@ bool decode_plan(int64_t T, int64_t H, int64_t I, int64_t E, int64_t S, int64_t 
     pl.off_sh = take(4 * P, 16);
     pl.off_x = take(mode == DecodeMode::kGemm2Partials ? 0 : T * (H + 16), 128);
     pl.off_xm = take(mode == DecodeMode::kForward && mixed ? T * (H + 16) : 0, 128);
-    pl.off_hq = take(mode == DecodeMode::kGemm1Partials ? 0 : P * (I + 16), 128);
+    // (the forward kernel's grouping uses this area as scratch before phase 2 writes it: E + 2 (E + 31) / 32 words)
+    pl.off_hq = take(mode == DecodeMode::kGemm1Partials ? 0
+                     : std::max<int64_t>(P * (I + 16), mode == DecodeMode::kForward ? 4 * (E + 2 * ((E + 31) / 32)) : 0),
+                     128);
     pl.off_y = take(mode == DecodeMode::kForward ? 4 * P * pl.rows_pc : 0, 16);
     pl.off_first = take(4 * rows, 16);
     pl.off_eqc = take(4 * rows, 16);
