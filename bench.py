@@ -347,6 +347,8 @@ def run_ours(a):
     e2e = None
     if not a.no_e2e:
         e2e = _e2e(w, d, banks, batches, a.steps, stream, dev, binding)
+    # the same workload with each batch's routing supplied (an expert-routing cache hit)
+    supplied = _supplied_routing_entry(w, d, banks, batches, a, stream, dev, binding, world)
 
     # ---------------------------------------------------------------- further workloads, same K steps
     extra = {}
@@ -402,6 +404,7 @@ def run_ours(a):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    line["routing_supplied"] = supplied
     if extra:
         line["workloads"] = extra
     if not a.no_cpu_baseline:
@@ -441,6 +444,38 @@ def _roofline_entry(w, ms_per_step, logits_batches, hbm_peak, tf_peak, peak_kind
                  "hbm_GBs": gbs, "hbm_frac": gbs / hbm_peak, "tensor_TOPs": tops, "tensor_frac": tops / tf_peak,
                  "roofline_ms": max(t_hbm, t_tc) * 1e3, "roofline_frac": max(t_hbm, t_tc) / t})
     return {"ms_per_step": ms_per_step, "engine": engine_name, "roofline": roof}
+
+
+def _supplied_routing_entry(w, d, banks, batches, a, stream, dev, binding, world):
+    """moe_w4a8_forward_routed with each batch's routing computed once beforehand (moe_w4a8_route, outside the
+    timed region): the step without its top-k, as a routing cache would serve it."""
+    import torch
+    dev_batches = [tuple(torch.from_numpy(x).to(dev) for x in (t.x_q, t.x_scale, t.logits)) for t in batches]
+    ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), dev)
+    routes = []
+    for x_q, x_s, lg in dev_batches:
+        ids = torch.empty((w.T, w.top_k), dtype=torch.int32, device=dev)
+        wts = torch.empty((w.T, w.top_k), dtype=torch.float32, device=dev)
+        ex = [torch.empty(n, dtype=torch.int32, device=dev) for n in (w.E, w.E + 1, w.T * w.top_k, w.T * w.top_k)]
+        binding.moe_w4a8_route(lg, d, ids, wts, *ex, ws)
+        routes.append((ids, wts))
+    out = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+
+    def step(i):
+        x_q, x_s, _ = dev_batches[i % len(dev_batches)]
+        ids, wts = routes[i % len(routes)]
+        w13, s13, w2, s2 = banks[i % len(banks)]
+        binding.moe_w4a8_forward_routed(x_q, x_s, ids, wts, w13, s13, w2, s2, d, out, ws)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(a.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize(dev)
+    ms, mn, mx = time_region(step, a.steps, a.repeats, stream, dev)
+    ms = max_over_ranks(ms, world, dev)
+    return {"ms_per_step": ms / a.steps, "value": whole_job_rate(w.T, world, ms, a.steps), "unit": "tokens/s",
+            "call": "moe_w4a8_forward_routed (routing of each batch computed beforehand by moe_w4a8_route)",
+            "region_ms": {"median": ms, "min": mn, "max": mx, "repeats": a.repeats}}
 
 
 def _mixed_entry(w, d, batches, step_int4, a, stream, dev, binding, world):

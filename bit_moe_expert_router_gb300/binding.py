@@ -59,6 +59,7 @@ def _load():
     lib.moe_w4a8_forward_debug.argtypes = [p, p, p, p, p, p, p, dp, p, p, p, p, ci, p, sz, p]
     lib.moe_w4a8_route.argtypes = [p, dp, p, p, p, p, p, p, p, sz, p]
     lib.moe_w4a8_debug_routing.argtypes = [dp, p, sz, p, p, p, p, p]
+    lib.moe_w4a8_forward_routed.argtypes = [p, p, p, p, p, p, p, p, dp, p, p, sz, p]
     lib.moe_w4a8_gemm1_partials.argtypes = [p, p, dp, p, p, i64, p, ci, p, sz, p]
     lib.moe_w4a8_gemm2_partials.argtypes = [p, p, dp, p, i64, p, ci, p, sz, p]
     lib.moe_w4a8_device_status.argtypes = [p, sz, p]
@@ -76,7 +77,7 @@ def _load():
     for name in ("moe_w4a8_forward", "moe_w4a8_forward_debug", "moe_w4a8_route", "moe_w4a8_gemm1_partials",
                  "moe_w4a8_gemm2_partials", "moe_w4a8_forward_noalloc", "moe_w4a8_device_status",
                  "moe_w4a8_selftest_barrier_timeout", "moe_w4a8_forward_host", "moe_w4a8_forward_bf16",
-                 "moe_w4a8_forward_w2w4", "moe_w4a8_debug_routing"):
+                 "moe_w4a8_forward_w2w4", "moe_w4a8_debug_routing", "moe_w4a8_forward_routed"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.moe_w4a8_version() != ABI_VERSION:
         raise RuntimeError(f"{LIB_PATH}: ABI version {lib.moe_w4a8_version()} != {ABI_VERSION}")
@@ -336,6 +337,27 @@ def moe_w4a8_route(router_logits, d: Dims, topk_ids, topk_w, counts, offsets, pe
     _call("moe_w4a8_route", (router_logits, topk_ids, topk_w, counts, offsets, perm, inv, workspace),
           _ptr(router_logits), ctypes.byref(d), _ptr(topk_ids), _ptr(topk_w), _ptr(counts), _ptr(offsets),
           _ptr(perm), _ptr(inv), wp, wb)
+
+
+def moe_w4a8_forward_routed(x_q, x_scale, topk_ids, topk_w, w13_packed, w13_scale, w2_packed, w2_scale, d: Dims,
+                            out, workspace):
+    """The layer with the routing supplied by the caller (see the header)."""
+    _need(x_q, "x_q", torch.int8, (d.T, d.H))
+    _need(x_scale, "x_scale", torch.float32, (d.T,))
+    _need(topk_ids, "topk_ids", torch.int32, (d.T, d.top_k))
+    _need(topk_w, "topk_w", torch.float32, (d.T, d.top_k))
+    w13s, s13s, w2s, s2s = _bank_shapes(d)
+    _need(w13_packed, "w13_packed", torch.uint8, w13s)
+    _need(w13_scale, "w13_scale", torch.float32, s13s)
+    _need(w2_packed, "w2_packed", torch.uint8, w2s)
+    _need(w2_scale, "w2_scale", torch.float32, s2s)
+    _need(out, "out", torch.float32, (d.T, d.H))
+    wp, wb = _ws_view(workspace)
+    _call("moe_w4a8_forward_routed", (x_q, x_scale, topk_ids, topk_w, w13_packed, w13_scale, w2_packed, w2_scale, out,
+                                      workspace),
+          _ptr(x_q), _ptr(x_scale), _ptr(topk_ids), _ptr(topk_w), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
+          _ptr(w2_scale), ctypes.byref(d), _ptr(out), wp, wb)
+    return out
 
 
 def moe_w4a8_debug_routing(d: Dims, workspace, topk_ids, topk_w, perm, inv):

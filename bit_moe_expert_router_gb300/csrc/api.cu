@@ -137,13 +137,16 @@ bool decode_forward_plan(const moe_dims_t* d, moe::DecodePlan* pl, bool mixed = 
 int run_decode(const int8_t* x_q, const float* x_scale, const float* logits, const uint8_t* w13, const float* s13,
                const uint8_t* w2, const float* s2, const moe_dims_t* d, float* out, const Views& v,
                const moe::DecodePlan& pl, float* y_debug, cudaStream_t st, const uint16_t* x_bf16 = nullptr,
-               const uint8_t* slot_bits = nullptr, bool route_debug = false) {
+               const uint8_t* slot_bits = nullptr, bool route_debug = false, const int32_t* ids_in = nullptr,
+               const float* wts_in = nullptr) {
     moe::DecodeArgs a{};
     a.x_q = x_q;
     a.x_scale = x_scale;
     a.x_bf16 = x_bf16;
     a.slot_bits = slot_bits;
     a.logits = logits;
+    a.ids_in = ids_in;
+    a.wts_in = wts_in;
     a.w13 = w13;
     a.s13 = s13;
     a.w2 = w2;
@@ -230,17 +233,19 @@ int run_tc_gemms(const int8_t* x_q, const float* x_scale, const uint8_t* w13, co
 // route + permute + gemm1 + gemm2 + combine on the workspace views.
 int run_layer(const int8_t* x_q, const float* x_scale, const float* logits, const uint8_t* w13, const float* s13,
               const uint8_t* w2, const float* s2, const moe_dims_t* d, float* out, const WsLayout& L, const Views& v,
-              cudaStream_t st, int engine = MOE_ENGINE_AUTO, float* y_debug = nullptr, bool route_debug = false) {
+              cudaStream_t st, int engine = MOE_ENGINE_AUTO, float* y_debug = nullptr, bool route_debug = false,
+              const int32_t* ids_in = nullptr, const float* wts_in = nullptr) {
     if (engine == MOE_ENGINE_AUTO || engine == MOE_ENGINE_DECODE) {
         moe::DecodePlan pl;
         if (decode_forward_plan(d, &pl))
             return run_decode(x_q, x_scale, logits, w13, s13, w2, s2, d, out, v, pl, y_debug, st, nullptr, nullptr,
-                              route_debug);
+                              route_debug, ids_in, wts_in);
         if (engine == MOE_ENGINE_DECODE) return MOE_ERR_UNSUPPORTED;
     }
     const bool tc = engine == MOE_ENGINE_TCGEN05 || (engine == MOE_ENGINE_AUTO && tc_fits(d));
     if (tc && !tc_fits(d)) return MOE_ERR_UNSUPPORTED;
-    MOE_CUDA(moe::launch_route_topk(logits, d->T, d->E, d->top_k, v.ids, v.wts, st));
+    if (ids_in) MOE_CUDA(moe::launch_route_supplied(ids_in, wts_in, d->T, d->E, d->top_k, v.ids, v.wts, st));
+    else MOE_CUDA(moe::launch_route_topk(logits, d->T, d->E, d->top_k, v.ids, v.wts, st));
     MOE_CUDA(moe::launch_sort(sort_args(v, v.ids, d->T, d->top_k, d->E, d->n_shared, L.P), st));
     if (tc) return run_tc_gemms(x_q, x_scale, w13, s13, w2, s2, d, out, L, v, y_debug, st);
 
@@ -527,6 +532,21 @@ MOE_API int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, cons
                       engine, y, true));
     if (h_q || s_h) MOE_CUDA(moe::launch_requant_copy(v.h, v.amax, L.P, d->I, h_q, s_h, st));
     return MOE_OK;
+}
+
+MOE_API int moe_w4a8_forward_routed(const int8_t* x_q, const float* x_scale, const int32_t* topk_ids,
+                                   const float* topk_w, const uint8_t* w13_packed, const float* w13_scale,
+                                   const uint8_t* w2_packed, const float* w2_scale, const moe_dims_t* d, float* out,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+    MOE_TRY(check_dims(d));
+    MOE_TRY(check_ptrs({w13_packed, w13_scale, w2_packed, w2_scale}));
+    if (d->T == 0) return MOE_OK;
+    MOE_TRY(check_ptrs({x_q, x_scale, topk_ids, topk_w, out}));
+    const WsLayout L = layout_of(d);
+    MOE_TRY(check_ws(L, workspace, workspace_bytes));
+    return run_layer(x_q, x_scale, nullptr, w13_packed, w13_scale, w2_packed, w2_scale, d, out, L,
+                     views(workspace, L), static_cast<cudaStream_t>(stream), MOE_ENGINE_AUTO, nullptr, false, topk_ids,
+                     topk_w);
 }
 
 MOE_API int moe_w4a8_debug_routing(const moe_dims_t* d, const void* workspace, size_t workspace_bytes,

@@ -418,10 +418,15 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     // When every warp routes, every thread stages afterwards.
     constexpr int per_tok = H / 16;
     const int n_xp = MODE == DecodeMode::kGemm2Partials ? 0 : T * per_tok;
-    const int nrw = routed ? min(T, kWarpsD) : 0;
+    const int nrw = routed && !a.ids_in ? min(T, kWarpsD) : 0;
     int n_rows;  // routed/listed pair rows before the shared rows
     if (routed) {
-        if (warp < nrw) {
+        if (a.ids_in) {  // routing supplied by the caller
+            for (int i = tid; i < T * k; i += kThreadsD) {
+                s.ids[i] = min(max(a.ids_in[i], 0), a.E - 1);
+                s.wts[i] = a.wts_in[i];
+            }
+        } else if (warp < nrw) {
             if (a.E <= 512) route_tokens<16>(a.logits, T, a.E, k, s.ids, s.wts, nrw);
             else route_tokens<kMaxExperts / 32>(a.logits, T, a.E, k, s.ids, s.wts, nrw);
         }
@@ -492,11 +497,13 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
     uint32_t* pres = emask + a.E;                          // [EW] bit e: expert e was picked
     int* pbase = reinterpret_cast<int*>(pres + (a.E + 31) / 32);  // [EW] experts picked in earlier words
     const int EW = (a.E + 31) / 32;
-    if (routed)
+    // (supplied routing may repeat an expert within a token: it takes the scans below)
+    const bool bitmaps = routed && !a.ids_in;
+    if (bitmaps)
         for (int i = tid; i < a.E + EW; i += kThreadsD) emask[i] = 0u;
     __syncthreads();
     const int S = routed ? a.S : 0;
-    if (routed) {
+    if (bitmaps) {
         // Grouping from bitmaps (T <= 32, and top-k picks an expert at most once per token): a pair's
         // slot is the number of picked experts below its expert, its row within the slot the number
         // of earlier tokens that picked the same expert -- the stable order by (expert, pair index).

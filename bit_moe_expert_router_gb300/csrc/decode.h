@@ -16,6 +16,8 @@ struct DecodeArgs {
     const float* x_scale;
     const uint16_t* x_bf16;  // forward: bf16 activations [T][H] quantised in the kernel (x_q / x_scale unused), or null
     const float* logits;
+    const int32_t* ids_in;   // forward: routing supplied by the caller ([T][k] ids, clamped to [0, E)), or null
+    const float* wts_in;     //          its weights [T][k] (logits unused)
     const uint8_t* slot_bits;  // forward: code width of each bank slot [E+S] (2 or 4), or null (all 4)
     const uint8_t* w13;
     const float* s13;

@@ -10,6 +10,9 @@
 namespace moe {
 
 // Router: ids/wts [T][k] from logits [T][E].
+// ids [T][k] <- ids_in clamped into [0, E), wts <- wts_in (a routing supplied by the caller).
+cudaError_t launch_route_supplied(const int32_t* ids_in, const float* wts_in, int64_t T, int64_t E, int64_t k,
+                                  int32_t* ids, float* wts, cudaStream_t st);
 cudaError_t launch_route_topk(const float* logits, int64_t T, int64_t E, int64_t k, int32_t* ids, float* wts,
                               cudaStream_t st);
 

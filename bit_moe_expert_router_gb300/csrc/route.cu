@@ -252,6 +252,27 @@ __global__ void __launch_bounds__(32) scatter_kernel(SortArgs a, int64_t n) {
 
 }  // namespace
 
+namespace {
+// Routing supplied by the caller: ids clamped into [0, E) (no expert id can address memory outside the
+// bank), weights as given.
+__global__ void route_supplied_kernel(const int32_t* __restrict__ ids_in, const float* __restrict__ wts_in, int64_t n,
+                                      int E, int32_t* __restrict__ ids, float* __restrict__ wts) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        ids[i] = min(max(ids_in[i], 0), E - 1);
+        wts[i] = wts_in[i];
+    }
+}
+}  // namespace
+
+cudaError_t launch_route_supplied(const int32_t* ids_in, const float* wts_in, int64_t T, int64_t E, int64_t k,
+                                  int32_t* ids, float* wts, cudaStream_t st) {
+    const int64_t n = T * k;
+    const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 1024));
+    route_supplied_kernel<<<std::max(blocks, 1u), 256, 0, st>>>(ids_in, wts_in, n, static_cast<int>(E), ids, wts);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_route_topk(const float* logits, int64_t T, int64_t E, int64_t k, int32_t* ids, float* wts,
                               cudaStream_t st) {
     const int warps = 8;

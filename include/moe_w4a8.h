@@ -172,6 +172,26 @@ int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, const float*
                            int engine, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The layer with the routing supplied by the caller -- an expert-routing
+ * cache (the page's serving notes name one among the optimisations measured
+ * at the API boundary, section 6): the ids and weights an earlier call
+ * computed for the same tokens (moe_w4a8_route, moe_w4a8_debug_routing) or
+ * any routing the caller keeps, so the call skips the top-k.  topk_ids
+ * int32 [T][k] (the expert of pair t*k + j; each row should hold k distinct
+ * experts -- an id outside [0, E) is clamped into it, and a repeated expert
+ * is grouped and weighted like any other pair, never read out of bounds) and
+ * topk_w float [T][k] (the pair weights, used as given), both 16-byte-aligned
+ * device arrays; router_logits are not needed.  Everything else (engines,
+ * workspace, errors) as for moe_w4a8_forward.  Given the routing
+ * moe_w4a8_forward computes for these inputs, the result equals its output
+ * bit for bit.
+ */
+int moe_w4a8_forward_routed(const int8_t* x_q, const float* x_scale, const int32_t* topk_ids, const float* topk_w,
+                            const uint8_t* w13_packed, const float* w13_scale,
+                            const uint8_t* w2_packed, const float* w2_scale,
+                            const moe_dims_t* d, float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * The routing used by the last moe_w4a8_forward_debug call on `workspace`
  * (any engine; the decode engine copies its own in-kernel routing there):
  * topk_ids int32 [T][k] and topk_w float [T][k] in rank order (largest

@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
             "moe_w4a8_status_string", "moe_w4a8_gemm1_partials", "moe_w4a8_gemm2_partials",
             "moe_w4a8_forward_debug", "moe_w4a8_device_status", "moe_w4a8_forward_host",
             "moe_w4a8_forward_host_workspace_size", "moe_w4a8_forward_bf16", "moe_w4a8_forward_w2w4",
-            "moe_w4a8_forward_bf16_workspace_size", "moe_w4a8_debug_routing"} <= names
+            "moe_w4a8_forward_bf16_workspace_size", "moe_w4a8_debug_routing", "moe_w4a8_forward_routed"} <= names
 
 
 def test_library_exports_every_declared_symbol(cuda_lib, lib):
@@ -115,6 +115,13 @@ def test_null_and_misaligned_pointers_are_rejected(lib):
     # the routing read-back: a null output, then a workspace too small
     assert lib.moe_w4a8_debug_routing(ctypes.byref(d), fake, need, fake, None, fake, fake, None) == 1
     assert lib.moe_w4a8_debug_routing(ctypes.byref(d), fake, need - 256, fake, fake, fake, fake, None) == 3
+    # the routed layer: no routing, then a misaligned weight array, then a workspace too small
+    assert lib.moe_w4a8_forward_routed(fake, fake, None, fake, *([fake] * 4), ctypes.byref(d), fake, fake, need,
+                                       None) == 1
+    assert lib.moe_w4a8_forward_routed(fake, fake, fake, odd, *([fake] * 4), ctypes.byref(d), fake, fake, need,
+                                       None) == 1
+    assert lib.moe_w4a8_forward_routed(fake, fake, fake, fake, *([fake] * 4), ctypes.byref(d), fake, fake,
+                                       need - 256, None) == 3
 
 
 def test_partials_workspace_covers_grouping_and_fp16_rows(lib):
@@ -202,8 +209,9 @@ def test_mixed_bank_entry_checks_its_arguments(lib):
     args = [fake] * 7
     assert lib.moe_w4a8_forward_w2w4(*args, None, ctypes.byref(d), fake, fake, need, None) == 1
     assert lib.moe_w4a8_forward_w2w4(*args, fake, ctypes.byref(d), fake, fake, need - 256, None) == 3
-    # sizes the decode engine does not take are refused before anything is enqueued
-    big = binding.dims_of(4096, 2048, 512, 512, 1, 10, 128)
+    # sizes neither the decode engine (T <= 32) nor the tcgen05 engine (g a multiple of 128) takes are
+    # refused before anything is enqueued
+    big = binding.dims_of(4096, 2048, 512, 512, 1, 10, 64)
     need_big = lib.moe_w4a8_workspace_size(ctypes.byref(big))
     assert lib.moe_w4a8_forward_w2w4(*args, fake, ctypes.byref(big), fake, fake, need_big, None) == 2
 

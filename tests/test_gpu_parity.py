@@ -696,3 +696,63 @@ def test_mixed_2bit_bank_on_the_tcgen05_engine(name):
     torch.cuda.synchronize()
     assert np.array_equal(out.cpu().numpy(), ref)
 
+
+def _routed_call(w, tok, ids, wts):
+    w13, s13, w2, s2 = gh.device_bank(w)
+    d = gh.dims(w)
+    out = torch.empty((w.T, w.H), dtype=torch.float32, device="cuda:0")
+    ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), "cuda:0")
+    binding.moe_w4a8_forward_routed(gh.to_dev(tok.x_q), gh.to_dev(tok.x_scale), gh.to_dev(ids.astype(np.int32)),
+                                    gh.to_dev(wts.astype(np.float32)), w13, s13, w2, s2, d, out, ws)
+    torch.cuda.synchronize()
+    assert binding.moe_w4a8_device_status(ws) == 0
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("name,engine", [("decode_t4", 1), ("decode_verify_t12", 1), ("tc_small", 2), ("tiny", 0)])
+def test_supplied_routing_reproduces_the_layer(name, engine):
+    """A routing cache hit: the routing a layer call computed, handed back through moe_w4a8_forward_routed,
+    gives that call's output bit for bit (each engine, its own routing); the oracle's routing gives the
+    oracle's output within the stated tolerance."""
+    w = _workload(name)
+    tok = synth.make_tokens(w)
+    assert binding.moe_w4a8_engine_for(gh.dims(w)) == engine
+    got = _debug_routing(w, tok, engine)
+    ref = _forward_engine(w, tok, engine)
+    out = _routed_call(w, tok, got["ids"], got["w"])
+    assert np.array_equal(out, ref)
+    ids, wt = oracle.route(tok.logits, w.top_k)
+    out_o = _routed_call(w, tok, ids, wt)
+    sel = gh.sample_tokens(w.T, 48)
+    gh.assert_output_close(out_o[sel], gh.oracle_out(w, tok, gh.bank_of(w), sel), f"{name} oracle routing supplied")
+
+
+@pytest.mark.parametrize("name", ["dec_small", "tc_small"])
+def test_supplied_routing_with_repeats_and_out_of_range_ids(name):
+    """Ids outside [0, E) are clamped and a token may name an expert twice: every pair is computed and
+    weighted as given (against the oracle's per-pair outputs summed in the same order)."""
+    w = _workload(name)
+    tok = synth.make_tokens(w)
+    rng = np.random.default_rng(3)
+    ids = rng.integers(0, w.E, size=(w.T, w.top_k)).astype(np.int64)
+    ids[0, :] = ids[0, 0]                      # one expert, k times
+    ids[1, 0] = -5
+    ids[1, -1] = w.E + 7
+    wts = rng.random((w.T, w.top_k)).astype(np.float32)
+    out = _routed_call(w, tok, ids, wts)
+    assert np.all(np.isfinite(out))
+    bank = gh.bank_of(w)
+    od = oracle.dims(w.T, w.H, w.I, w.E, w.S, w.top_k, w.group)
+    clamped = np.clip(ids, 0, w.E - 1)
+    for t in gh.sample_tokens(w.T, 12):
+        ref = np.zeros(w.H)
+        for j in range(w.top_k):
+            _, _, y = oracle.pair_output(od, tok.x_q, tok.x_scale, bank.w13, bank.s13, bank.w2, bank.s2, t,
+                                         int(clamped[t, j]))
+            ref += float(wts[t, j]) * y
+        for sh in range(w.S):
+            _, _, y = oracle.pair_output(od, tok.x_q, tok.x_scale, bank.w13, bank.s13, bank.w2, bank.s2, t, w.E + sh)
+            ref += y
+        rms = np.sqrt(np.mean(ref ** 2)) + 1e-30
+        assert np.max(np.abs(out[t] - ref)) <= 2e-2 * rms, f"token {t}"
+
