@@ -387,8 +387,9 @@ __device__ Smem carve(uint8_t* base, const DecodePlan& pl) {
     return s;
 }
 
-// Phase-1 cost of one unit of a slot with `cnt` tokens (streaming + per-token work).
-__device__ __forceinline__ int unit_cost(int cnt, int bits) { return (bits == 2 ? 2 : 4) + cnt; }
+// Phase-1 cost of one unit of a slot with `cnt` tokens (streaming + per-token work), in units fitted to
+// measured per-CTA phase times: a 4-token unit of a 4-bit slot takes ~2.1x a 1-token unit.
+__device__ __forceinline__ int unit_cost(int cnt, int bits) { return (bits == 2 ? 5 : 9) + 8 * cnt; }
 
 // PC1 = H / 2048 (64-value pieces per lane per row), PC2 = I / 512 (16-value pieces per lane per row).
 // MIXED (forward only): the bank mixes 2-bit and 4-bit slots (a.slot_bits); the plain
