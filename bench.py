@@ -314,7 +314,7 @@ def run_ours(a):
     # ---------------------------------------------------------------- headline workload
     w, d, banks, batches, step, _ = measure(a.workload, a.banks, a.batches, a.warmup)
     engine = binding.moe_w4a8_engine_for(d)
-    launches_per_step = {binding.ENGINE_DECODE: 1, binding.ENGINE_TCGEN05: 9, binding.ENGINE_GROUPED: 7}[engine]
+    launches_per_step = {binding.ENGINE_DECODE: 1, binding.ENGINE_TCGEN05: 10, binding.ENGINE_GROUPED: 8}[engine]
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     if rank == 0:
         clocks.start()

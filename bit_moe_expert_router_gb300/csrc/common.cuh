@@ -9,7 +9,7 @@
 namespace moe {
 
 constexpr int kWarp = 32;
-constexpr int kChunk = 1024;   // pairs per chunk of the counting sort
+constexpr int kChunk = 256;    // pairs per chunk of the counting sort (one scatter warp each)
 constexpr int kTileM = 64;     // pair rows per grouped-GEMM tile
 constexpr int kMaxTopK = 32;
 constexpr int kMaxExperts = 1024;

@@ -22,76 +22,132 @@
 namespace moe {
 namespace {
 
-// (v, e) beats (bv, be): larger value, or equal value and lower index; a NaN
-// ranks below every number (NaNs among themselves by index); be = INT32_MAX
-// is "no candidate yet", which anything beats.  So every token gets k
-// distinct experts whatever its logits hold.
-__device__ __forceinline__ bool beats(float v, int e, float bv, int be) {
-    if (e == INT32_MAX) return false;
-    if (be == INT32_MAX) return true;
-    const bool vn = v != v, bn = bv != bv;
-    if (vn != bn) return bn;
-    return v > bv || ((v == bv || vn) && e < be);
+// Order-preserving 32-bit key of a logit: a larger float gives a larger key, -0.0 and +0.0 the same
+// key, and a NaN key 1 -- below every number (-inf is 0x007FFFFF) and above the 0 of an absent
+// expert -- so NaNs rank last, among themselves by index.  key_value inverts it for numbers.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    if (v != v) return 1u;
+    const uint32_t u = __float_as_uint(v + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+constexpr int kRouteWarps = 8;  // tokens per block, one warp each
+constexpr int kRouteCand = 64;  // candidate keys a warp ranks directly
+
+// Top-k of each token by (key desc, id asc), one warp per token; lane l holds the keys of experts
+// l, l + 32, ...  Threshold: the k-th largest of the 32 lane maxima (k <= 32).  At least k keys reach
+// it, so every pick does, and so does every key better than a pick: the picks are the k best of the
+// keys >= the threshold, whose ranks among themselves are counted directly (a few more than k keys
+// qualify as a rule).  When more than kRouteCand qualify, k rounds of a warp-wide arg-max instead.
+// Weights: softmax over the k picked logits, relative to the largest.
 template <int MAXJ>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                         int32_t* __restrict__ ids, float* __restrict__ wts) {
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+__global__ void __launch_bounds__(32 * kRouteWarps) route_topk_kernel(const float* __restrict__ logits, int T, int E,
+                                                                     int k, int32_t* __restrict__ ids,
+                                                                     float* __restrict__ wts) {
+    __shared__ uint32_t cand_k[kRouteWarps][kRouteCand];
+    __shared__ int cand_i[kRouteWarps][kRouteCand];
+    __shared__ uint32_t picked[kRouteWarps][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * kRouteWarps + warp;
     if (t >= T) return;
     const float* l = logits + static_cast<int64_t>(t) * E;
-    float v[MAXJ];
+    uint32_t key[MAXJ];
 #pragma unroll
     for (int j = 0; j < MAXJ; ++j) {
-        int e = lane + 32 * j;
-        v[j] = e < E ? __ldg(l + e) : -FLT_MAX;
+        const int e = lane + 32 * j;
+        key[j] = e < E ? order_key(__ldg(l + e)) : 0u;
     }
-    uint32_t taken = 0;  // bit j: element lane + 32 j already selected (or absent)
+    uint32_t lm = key[0];
 #pragma unroll
-    for (int j = 0; j < MAXJ; ++j)
-        if (lane + 32 * j >= E) taken |= 1u << j;
-    float my_v = 0.0f;
+    for (int j = 1; j < MAXJ; ++j) lm = max(lm, key[j]);
+    int rk = 0;  // rank of this lane's maximum among the lanes' (ties by lane)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const uint32_t o = __shfl_sync(0xffffffffu, lm, j);
+        rk += o > lm || (o == lm && j < lane);
+    }
+    const uint32_t th = __shfl_sync(0xffffffffu, lm, __ffs(__ballot_sync(0xffffffffu, rk == k - 1)) - 1);
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < MAXJ; ++j) c += key[j] >= th;
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    const int C = __shfl_sync(0xffffffffu, incl, 31);
     int my_e = 0;
-    for (int s = 0; s < k; ++s) {
-        float bv = -INFINITY;
-        int be = INT32_MAX;
+    uint32_t my_k = 0;
+    if (C <= kRouteCand) {
+        int w = incl - c;
 #pragma unroll
-        for (int j = 0; j < MAXJ; ++j) {
-            int e = lane + 32 * j;
-            if (!(taken >> j & 1u) && beats(v[j], e, bv, be)) {
-                bv = v[j];
-                be = e;
+        for (int j = 0; j < MAXJ; ++j)
+            if (key[j] >= th) {
+                cand_k[warp][w] = key[j];
+                cand_i[warp][w] = lane + 32 * j;
+                ++w;
+            }
+        __syncwarp();
+        for (int i = lane; i < C; i += 32) {
+            const uint32_t kk = cand_k[warp][i];
+            const int ii = cand_i[warp][i];
+            int r = 0;
+            for (int j = 0; j < C; ++j) r += cand_k[warp][j] > kk || (cand_k[warp][j] == kk && cand_i[warp][j] < ii);
+            if (r < k) {
+                picked[warp][r] = kk;
+                ids[static_cast<int64_t>(t) * k + r] = ii;
             }
         }
+        __syncwarp();
+        if (lane < k) my_k = picked[warp][lane];
+    } else {
+        uint32_t bk = 0;
+        int bj = 0;
+        auto lane_best = [&]() {
+            bk = key[0];
+            bj = 0;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            if (beats(ov, oe, bv, be)) {
-                bv = ov;
-                be = oe;
+            for (int j = 1; j < MAXJ; ++j)
+                if (key[j] > bk) {
+                    bk = key[j];
+                    bj = j;
+                }
+        };
+        lane_best();
+        for (int r = 0; r < k; ++r) {
+            const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+            const uint32_t mine = static_cast<uint32_t>(lane + 32 * bj);
+            const uint32_t mi = __reduce_min_sync(0xffffffffu, bk == mk ? mine : 0xFFFFFFFFu);
+            if (lane == r) {
+                my_k = mk;
+                my_e = static_cast<int>(mi);
+            }
+            if (mine == mi) {  // the winner drops the taken key and rescans
+#pragma unroll
+                for (int j = 0; j < MAXJ; ++j)
+                    if (j == bj) key[j] = 0u;
+                lane_best();
             }
         }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        if (lane == s) {
-            my_v = bv;
-            my_e = be;
-        }
+        if (lane < k) ids[static_cast<int64_t>(t) * k + lane] = my_e;
     }
-    // softmax over the selected logits, relative to the largest (selected first)
+    // softmax over the selected logits, relative to the largest (position 0)
+    const float my_v = lane < k ? key_value(my_k) : 0.0f;
     const float m = __shfl_sync(0xffffffffu, my_v, 0);
-    float ex = lane < k ? expf(my_v - m) : 0.0f;
+    const float ex = lane < k ? expf(my_v - m) : 0.0f;
     float sum = ex;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (lane < k) {
-        ids[static_cast<int64_t>(t) * k + lane] = my_e;
-        wts[static_cast<int64_t>(t) * k + lane] = ex / sum;
-    }
+    if (lane < k) wts[static_cast<int64_t>(t) * k + lane] = ex / sum;
 }
 
-__global__ void __launch_bounds__(256) count_kernel(SortArgs a, int64_t n) {
+// Chunk c's expert histogram -> chunk_counts[e * n_chunks + c] (expert-major: one expert's counts over
+// the chunks are contiguous for the scan).
+__global__ void __launch_bounds__(256) count_kernel(SortArgs a, int64_t n, int64_t n_chunks) {
     extern __shared__ int hist[];
     for (int e = threadIdx.x; e < a.E; e += blockDim.x) hist[e] = 0;
     __syncthreads();
@@ -102,7 +158,7 @@ __global__ void __launch_bounds__(256) count_kernel(SortArgs a, int64_t n) {
         if (static_cast<unsigned>(e) < static_cast<unsigned>(a.E)) atomicAdd(&hist[e], 1);  // out-of-range ids are dropped
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < a.E; e += blockDim.x) a.chunk_counts[c * a.E + e] = hist[e];
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) a.chunk_counts[e * n_chunks + c] = hist[e];
     // side jobs spread over the grid: clear the row maxima, name the shared rows' tokens
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -154,33 +210,47 @@ __device__ int block_exclusive_scan(int* data, int n, int* warp_sums) {
     return total;
 }
 
+// Per expert, one warp: the exclusive prefix of its chunk counts (contiguous, expert-major) in place,
+// 256 chunks a step with each lane's 8 counts loaded together; the expert's total -> seg_cnt[e].
+__global__ void __launch_bounds__(256) chunk_scan_kernel(SortArgs a, int64_t n_chunks) {
+    const int lane = threadIdx.x & 31;
+    const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (e >= a.E) return;
+    int32_t* cc = a.chunk_counts + static_cast<int64_t>(e) * n_chunks;
+    int run = 0;
+    for (int64_t base = 0; base < n_chunks; base += 256) {
+        int v[8], loc = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int64_t c = base + 8 * lane + j;
+            v[j] = c < n_chunks ? cc[c] : 0;
+            loc += v[j];
+        }
+        int incl = loc;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        int r = run + incl - loc;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int64_t c = base + 8 * lane + j;
+            if (c < n_chunks) cc[c] = r;
+            r += v[j];
+        }
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) a.seg_cnt[e] = run;
+}
+
 __global__ void __launch_bounds__(1024) scan_kernel(SortArgs a, int64_t n_chunks) {
     __shared__ int tot[kMaxExperts + kMaxShared + 1];
     __shared__ int tiles[kMaxExperts + kMaxShared + 1];
     __shared__ int warp_sums[33];
     const int E = static_cast<int>(a.E), slots = static_cast<int>(a.E + a.S);
-    // per expert: exclusive prefix over the chunks, eight chunks' counts loaded at a time
-    // (independent loads in flight instead of a load-store chain)
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = 0;
-        int64_t c = 0;
-        for (; c + 8 <= n_chunks; c += 8) {
-            int v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = a.chunk_counts[(c + j) * E + e];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                a.chunk_counts[(c + j) * E + e] = run;
-                run += v[j];
-            }
-        }
-        for (; c < n_chunks; ++c) {
-            const int v = a.chunk_counts[c * E + e];
-            a.chunk_counts[c * E + e] = run;
-            run += v;
-        }
-        tot[e] = run;
-    }
+    // the experts' totals from chunk_scan_kernel (no chunks: none)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) tot[e] = n_chunks > 0 ? a.seg_cnt[e] : 0;
     for (int s = threadIdx.x; s < a.S; s += blockDim.x) tot[E + s] = static_cast<int>(a.T);
     __syncthreads();
     for (int s = threadIdx.x; s < slots; s += blockDim.x) {
@@ -196,18 +266,6 @@ __global__ void __launch_bounds__(1024) scan_kernel(SortArgs a, int64_t n_chunks
         a.seg_off[s] = off;
         if (a.offsets_out && s <= E) a.offsets_out[s] = off;
     }
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int base = tot[e];
-        int64_t c = 0;
-        for (; c + 8 <= n_chunks; c += 8) {
-            int v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = a.chunk_counts[(c + j) * E + e];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) a.chunk_counts[(c + j) * E + e] = v[j] + base;
-        }
-        for (; c < n_chunks; ++c) a.chunk_counts[c * E + e] += base;
-    }
     for (int s = threadIdx.x; s < slots; s += blockDim.x) {
         int cnt = a.seg_cnt[s];
         int nt = (cnt + kTileM - 1) / kTileM;
@@ -222,11 +280,12 @@ __global__ void __launch_bounds__(1024) scan_kernel(SortArgs a, int64_t n_chunks
     }
 }
 
-__global__ void __launch_bounds__(32) scatter_kernel(SortArgs a, int64_t n) {
+__global__ void __launch_bounds__(32) scatter_kernel(SortArgs a, int64_t n, int64_t n_chunks) {
     extern __shared__ int cursor[];
     const int lane = threadIdx.x;
     const int64_t c = blockIdx.x;
-    for (int e = lane; e < a.E; e += 32) cursor[e] = a.chunk_counts[c * a.E + e];
+    // the chunk's first row of each expert: the expert's segment offset + the earlier chunks' count
+    for (int e = lane; e < a.E; e += 32) cursor[e] = a.seg_off[e] + a.chunk_counts[e * n_chunks + c];
     __syncwarp();
     const int64_t i0 = c * kChunk, i_end = min(n, i0 + kChunk);
     int id_next = i0 + lane < i_end ? a.ids[i0 + lane] : -1;  // the next batch's ids are loaded one batch ahead
@@ -275,7 +334,7 @@ cudaError_t launch_route_supplied(const int32_t* ids_in, const float* wts_in, in
 
 cudaError_t launch_route_topk(const float* logits, int64_t T, int64_t E, int64_t k, int32_t* ids, float* wts,
                               cudaStream_t st) {
-    const int warps = 8;
+    const int warps = kRouteWarps;
     dim3 grid(static_cast<unsigned>((T + warps - 1) / warps)), block(32 * warps);
     const int Ti = static_cast<int>(T), Ei = static_cast<int>(E), ki = static_cast<int>(k);
     if (E <= 32) route_topk_kernel<1><<<grid, block, 0, st>>>(logits, Ti, Ei, ki, ids, wts);
@@ -292,12 +351,13 @@ cudaError_t launch_sort(const SortArgs& a, cudaStream_t st) {
     const int64_t n_chunks = (n + kChunk - 1) / kChunk;
     const size_t hist_bytes = sizeof(int) * a.E;
     if (n_chunks > 0) {
-        count_kernel<<<static_cast<unsigned>(n_chunks), 256, hist_bytes, st>>>(a, n);
+        count_kernel<<<static_cast<unsigned>(n_chunks), 256, hist_bytes, st>>>(a, n, n_chunks);
     } else if (a.amax) {
         cudaMemsetAsync(a.amax, 0, sizeof(uint32_t) * a.P, st);
     }
+    if (n_chunks > 0) chunk_scan_kernel<<<static_cast<unsigned>((a.E + 7) / 8), 256, 0, st>>>(a, n_chunks);
     scan_kernel<<<1, 1024, 0, st>>>(a, n_chunks);
-    if (n_chunks > 0) scatter_kernel<<<static_cast<unsigned>(n_chunks), 32, hist_bytes, st>>>(a, n);
+    if (n_chunks > 0) scatter_kernel<<<static_cast<unsigned>(n_chunks), 32, hist_bytes, st>>>(a, n, n_chunks);
     return cudaGetLastError();
 }
 
