@@ -27,11 +27,13 @@
 //     tolerance.
 //
 // Tile: M = 128 weight rows x N <= 192 tokens of one bank slot, one K group
-// (128 values) per B stage.  An M = 128 MMA costs about the same
-// time for any N up to 192 on this GPU (~135 cycles with A in tensor memory),
-// so wide token tiles are what sets the tensor-pipe rate; 192 columns is the
-// widest that leaves two accumulators and two A stages in the 512 columns of
-// tensor memory (2 x 192 + 2 x 64).
+// (128 values) per B stage.  An M = 128, K = 16 MMA takes N / 2 cycles for
+// N >= 64 on this GPU (64 at N = 128, 96 at N = 192, 128 at N = 256, A in
+// tensor or shared memory alike) and ~45 cycles below that; wide token
+// tiles spread each A stage (the unpack and its tensor-memory stores) and
+// each accumulator drain over more tokens.  192 columns is the widest that
+// leaves two accumulators and two A stages in the 512 columns of tensor
+// memory (2 x 192 + 2 x 64).
 //   A (the unpacked weights, fp16): each producer warp copies the packed
 //     rows of its 32 tile rows for a stage (64 bytes each, cp.async, four
 //     lanes per row) into a 3-deep ring two stages ahead; each producer
