@@ -479,12 +479,14 @@ def _supplied_routing_entry(w, d, banks, batches, a, stream, dev, binding, world
 
 
 def _mixed_entry(w, d, batches, step_int4, a, stream, dev, binding, world):
-    """The same workload with its 2-bit experts stored 4 codes per byte (moe_w4a8_forward_w2w4): time and
-    algorithmic bytes beside the int4 storage's (the same codes)."""
+    """The same workload with its 2-bit experts stored 4 codes per byte in compact storage (every slot's
+    rows at the slot's own width, moe_w4a8_forward_w2w4_compact): time, algorithmic bytes and bank size
+    beside the int4 storage's (the same codes)."""
     import torch
     from bit_moe_expert_router_gb300 import synth
     b2 = synth.make_bank(w, pack2=True)
-    bank = tuple(torch.from_numpy(x).to(dev) for x in (b2.w13, b2.s13, b2.w2, b2.s2))
+    w13c, o13, w2c, o2 = synth.compact_bank(b2)
+    bank = tuple(torch.from_numpy(x).to(dev) for x in (w13c, o13, b2.s13, w2c, o2, b2.s2))
     bits = torch.from_numpy(b2.slot_bits).to(dev)
     dev_batches = [tuple(torch.from_numpy(x).to(dev) for x in (t.x_q, t.x_scale, t.logits)) for t in batches]
     ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), dev)
@@ -492,7 +494,7 @@ def _mixed_entry(w, d, batches, step_int4, a, stream, dev, binding, world):
 
     def step(i):
         x_q, x_s, lg = dev_batches[i % len(dev_batches)]
-        binding.moe_w4a8_forward_w2w4(x_q, x_s, lg, *bank, bits, d, out, ws)
+        binding.moe_w4a8_forward_w2w4_compact(x_q, x_s, lg, *bank, bits, d, out, ws)
 
     with torch.cuda.stream(stream):
         for i in range(max(a.warmup, 3)):
@@ -501,11 +503,13 @@ def _mixed_entry(w, d, batches, step_int4, a, stream, dev, binding, world):
     ms, mn, mx = time_region(step, a.steps, a.repeats, stream, dev)
     ms = max_over_ranks(ms, world, dev)
     lgs = [t.logits for t in batches]
+    scales = int(b2.s13.nbytes + b2.s2.nbytes)
     return {"ms_per_step": ms / a.steps, "algorithmic_bytes_per_step": touched_bytes_mixed(w, lgs, b2.slot_bits),
             "int4_storage_bytes_per_step": touched_bytes(w, lgs),
-            "bank_bytes": int(b2.w13.nbytes + b2.s13.nbytes + b2.w2.nbytes + b2.s2.nbytes),
-            "note": "2-bit slots keep the int4 row length (codes in the first half of each row): the bytes read "
-                    "halve for those slots, the bank's storage does not",
+            "bank_bytes": int(w13c.nbytes + w2c.nbytes) + scales,
+            "int4_storage_bank_bytes": int(b2.w13.nbytes + b2.w2.nbytes) + scales,
+            "storage": "compact: every slot's rows at the slot's own width (2-bit rows K/4 bytes), slots back "
+                       "to back; one bank copy (the int4 line rotates copies to stay beyond L2)",
             "region_ms": {"median": ms, "min": mn, "max": mx, "repeats": a.repeats}}
 
 

@@ -74,10 +74,13 @@ def _load():
     lib.moe_w4a8_forward_bf16_workspace_size.restype = sz
     lib.moe_w4a8_forward_bf16.argtypes = [p, p, p, p, p, p, dp, p, p, sz, p]
     lib.moe_w4a8_forward_w2w4.argtypes = [p, p, p, p, p, p, p, p, dp, p, p, sz, p]
+    lib.moe_w4a8_mixed_bank_layout.argtypes = [p, dp, p, p, p, p]
+    lib.moe_w4a8_forward_w2w4_compact.argtypes = [p, p, p, p, p, p, p, p, p, p, dp, p, p, sz, p]
     for name in ("moe_w4a8_forward", "moe_w4a8_forward_debug", "moe_w4a8_route", "moe_w4a8_gemm1_partials",
                  "moe_w4a8_gemm2_partials", "moe_w4a8_forward_noalloc", "moe_w4a8_device_status",
                  "moe_w4a8_selftest_barrier_timeout", "moe_w4a8_forward_host", "moe_w4a8_forward_bf16",
-                 "moe_w4a8_forward_w2w4", "moe_w4a8_debug_routing", "moe_w4a8_forward_routed"):
+                 "moe_w4a8_forward_w2w4", "moe_w4a8_debug_routing", "moe_w4a8_forward_routed",
+                 "moe_w4a8_mixed_bank_layout", "moe_w4a8_forward_w2w4_compact"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.moe_w4a8_version() != ABI_VERSION:
         raise RuntimeError(f"{LIB_PATH}: ABI version {lib.moe_w4a8_version()} != {ABI_VERSION}")
@@ -287,6 +290,52 @@ def moe_w4a8_forward_w2w4(x_q, x_scale, router_logits, w13_packed, w13_scale, w2
                                     slot_bits, out, workspace),
           _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_scale), _ptr(w2_packed),
           _ptr(w2_scale), _ptr(slot_bits), ctypes.byref(d), _ptr(out), wp, wb)
+    return out
+
+
+def moe_w4a8_mixed_bank_layout(slot_bits, d: Dims):
+    """The compact layout of a mixed 2/4-bit bank, computed on the host.
+
+    slot_bits: uint8 CPU tensor [E+S] (2 or 4).  Returns (w13_off, w2_off, w13_bytes, w2_bytes): each slot's
+    byte offset in the gate/up and the down bank (int64 CPU tensors [E+S]) and the two banks' sizes.
+    """
+    _need_host(slot_bits, "slot_bits", torch.uint8, (d.E + d.n_shared,))
+    n = d.E + d.n_shared
+    o13 = torch.empty(n, dtype=torch.int64)
+    o2 = torch.empty(n, dtype=torch.int64)
+    b13, b2 = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check("moe_w4a8_mixed_bank_layout",
+           _load().moe_w4a8_mixed_bank_layout(_ptr(slot_bits), ctypes.byref(d), _ptr(o13), _ptr(o2),
+                                               ctypes.byref(b13), ctypes.byref(b2)))
+    return o13, o2, b13.value, b2.value
+
+
+def moe_w4a8_forward_w2w4_compact(x_q, x_scale, router_logits, w13_packed, w13_off, w13_scale, w2_packed, w2_off,
+                                  w2_scale, slot_bits, d: Dims, out, workspace: torch.Tensor):
+    """The layer on a mixed 2/4-bit bank in compact storage (see moe_w4a8_mixed_bank_layout).
+
+    w13_packed, w2_packed: uint8 CUDA tensors holding every slot's rows at the slot's own width; w13_off,
+    w2_off: int64 CUDA tensors [E+S], each slot's byte offset (multiples of 16).  Scales and slot_bits as
+    for moe_w4a8_forward_w2w4.
+    """
+    s13, s13s, s2, s2s = _bank_shapes(d)
+    n = d.E + d.n_shared
+    _need(x_q, "x_q", torch.int8, (d.T, d.H))
+    _need(x_scale, "x_scale", torch.float32, (d.T,))
+    _need(router_logits, "router_logits", torch.float32, (d.T, d.E))
+    _need(w13_packed, "w13_packed", torch.uint8)
+    _need(w13_off, "w13_off", torch.int64, (n,))
+    _need(w13_scale, "w13_scale", torch.float32, s13s)
+    _need(w2_packed, "w2_packed", torch.uint8)
+    _need(w2_off, "w2_off", torch.int64, (n,))
+    _need(w2_scale, "w2_scale", torch.float32, s2s)
+    _need(slot_bits, "slot_bits", torch.uint8, (n,))
+    _need(out, "out", torch.float32, (d.T, d.H))
+    wp, wb = _ws_view(workspace)
+    _call("moe_w4a8_forward_w2w4_compact", (x_q, x_scale, router_logits, w13_packed, w13_off, w13_scale, w2_packed,
+                                            w2_off, w2_scale, slot_bits, out, workspace),
+          _ptr(x_q), _ptr(x_scale), _ptr(router_logits), _ptr(w13_packed), _ptr(w13_off), _ptr(w13_scale),
+          _ptr(w2_packed), _ptr(w2_off), _ptr(w2_scale), _ptr(slot_bits), ctypes.byref(d), _ptr(out), wp, wb)
     return out
 
 

@@ -138,12 +138,14 @@ int run_decode(const int8_t* x_q, const float* x_scale, const float* logits, con
                const uint8_t* w2, const float* s2, const moe_dims_t* d, float* out, const Views& v,
                const moe::DecodePlan& pl, float* y_debug, cudaStream_t st, const uint16_t* x_bf16 = nullptr,
                const uint8_t* slot_bits = nullptr, bool route_debug = false, const int32_t* ids_in = nullptr,
-               const float* wts_in = nullptr) {
+               const float* wts_in = nullptr, const int64_t* w13_off = nullptr, const int64_t* w2_off = nullptr) {
     moe::DecodeArgs a{};
     a.x_q = x_q;
     a.x_scale = x_scale;
     a.x_bf16 = x_bf16;
     a.slot_bits = slot_bits;
+    a.w13_off = w13_off;
+    a.w2_off = w2_off;
     a.logits = logits;
     a.ids_in = ids_in;
     a.wts_in = wts_in;
@@ -208,17 +210,20 @@ moe::TcArgs tc_args(const uint8_t* w, const float* ws, int64_t rows_per_slot, in
 // slot_bits: each slot's code width (2 or 4) of a mixed bank, or null.
 int run_tc_gemms(const int8_t* x_q, const float* x_scale, const uint8_t* w13, const float* s13, const uint8_t* w2,
                  const float* s2, const moe_dims_t* d, float* out, const WsLayout& L, const Views& v, float* y_debug,
-                 cudaStream_t st, const uint8_t* slot_bits = nullptr) {
+                 cudaStream_t st, const uint8_t* slot_bits = nullptr, const int64_t* w13_off = nullptr,
+                 const int64_t* w2_off = nullptr) {
     const int n_slots = static_cast<int>(d->E + d->n_shared);
     // the activations gathered by pair row (fp16, the engine's K order): contiguous B tiles for gate/up
     MOE_CUDA(moe::launch_prep_x16(x_q, d->T, d->H, v.row_token, L.P, v.x16, st));
     moe::TcArgs g1 = tc_args(w13, s13, 2 * d->I, d->H, d, v.x16, L.P, x_scale, v, n_slots);
     g1.slot_bits = slot_bits;
+    g1.w_off = w13_off;
     g1.h = v.h;
     MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kGateUp, g1, st));
     MOE_CUDA(moe::launch_prep_h16(v.h, v.amax, nullptr, L.P, d->I, v.h16, v.sh, st));
     moe::TcArgs g2 = tc_args(w2, s2, d->H, d->I, d, v.h16, L.P, v.sh, v, n_slots);
     g2.slot_bits = slot_bits;
+    g2.w_off = w2_off;
     __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(v.y);  // the Y area holds bf16 Y here
     g2.yb = yb;
     MOE_CUDA(moe::launch_tc_gemm(moe::TcMode::kDown, g2, st));
@@ -511,6 +516,50 @@ MOE_API int moe_w4a8_forward_w2w4(const int8_t* x_q, const float* x_scale, const
     MOE_CUDA(moe::launch_sort(sort_args(v, v.ids, d->T, d->top_k, d->E, d->n_shared, L.P), st));
     return run_tc_gemms(x_q, x_scale, w13_packed, w13_scale, w2_packed, w2_scale, d, out, L, v, nullptr, st,
                         slot_bits);
+}
+
+MOE_API int moe_w4a8_mixed_bank_layout(const uint8_t* slot_bits, const moe_dims_t* d, int64_t* w13_off,
+                                       int64_t* w2_off, int64_t* w13_bytes, int64_t* w2_bytes) {
+    MOE_TRY(check_dims(d));
+    if (!slot_bits || !w13_off || !w2_off || !w13_bytes || !w2_bytes) return MOE_ERR_INVALID_ARG;
+    // (the dims checks keep H and I multiples of 64: every 2-bit row, and so every offset, is a multiple
+    // of 16 bytes)
+    int64_t o13 = 0, o2 = 0;
+    for (int64_t e = 0; e < d->E + d->n_shared; ++e) {
+        const bool two = slot_bits[e] == 2;
+        w13_off[e] = o13;
+        w2_off[e] = o2;
+        o13 += 2 * d->I * (two ? d->H / 4 : d->H / 2);
+        o2 += d->H * (two ? d->I / 4 : d->I / 2);
+    }
+    *w13_bytes = o13;
+    *w2_bytes = o2;
+    return MOE_OK;
+}
+
+MOE_API int moe_w4a8_forward_w2w4_compact(const int8_t* x_q, const float* x_scale, const float* router_logits,
+                                          const uint8_t* w13_packed, const int64_t* w13_off, const float* w13_scale,
+                                          const uint8_t* w2_packed, const int64_t* w2_off, const float* w2_scale,
+                                          const uint8_t* slot_bits, const moe_dims_t* d, float* out,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
+    MOE_TRY(check_dims(d));
+    MOE_TRY(check_ptrs({w13_packed, w13_scale, w2_packed, w2_scale}));
+    if (!slot_bits || !w13_off || !w2_off) return MOE_ERR_INVALID_ARG;
+    if (d->T == 0) return MOE_OK;
+    MOE_TRY(check_ptrs({x_q, x_scale, router_logits, out}));
+    const WsLayout L = layout_of(d);
+    MOE_TRY(check_ws(L, workspace, workspace_bytes));
+    const Views v = views(workspace, L);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    moe::DecodePlan pl;
+    if (decode_forward_plan(d, &pl, true))  // small batches: the decode engine
+        return run_decode(x_q, x_scale, router_logits, w13_packed, w13_scale, w2_packed, w2_scale, d, out, v, pl,
+                          nullptr, st, nullptr, slot_bits, false, nullptr, nullptr, w13_off, w2_off);
+    if (!tc_fits(d)) return MOE_ERR_UNSUPPORTED;  // large batches: the tcgen05 engine's sizes
+    MOE_CUDA(moe::launch_route_topk(router_logits, d->T, d->E, d->top_k, v.ids, v.wts, st));
+    MOE_CUDA(moe::launch_sort(sort_args(v, v.ids, d->T, d->top_k, d->E, d->n_shared, L.P), st));
+    return run_tc_gemms(x_q, x_scale, w13_packed, w13_scale, w2_packed, w2_scale, d, out, L, v, nullptr, st,
+                        slot_bits, w13_off, w2_off);
 }
 
 MOE_API int moe_w4a8_forward_debug(const int8_t* x_q, const float* x_scale, const float* router_logits,

@@ -155,6 +155,15 @@ __device__ bool grid_barrier(Header* hdr, uint32_t k) {
     return ok_s != 0;
 }
 
+// Byte offset of row r of slot e in a packed bank of `rows` rows per slot and
+// rb4 bytes per 4-bit row: the uniform layout (every row rb4 bytes), or the
+// compact one (slot e at off[e], low four bits cleared so every 16-byte load
+// stays aligned; rows at the slot's own width, rb4 / 2 for a 2-bit slot).
+__device__ __forceinline__ int64_t bank_row(const int64_t* off, int64_t e, int64_t rows, int64_t r, int64_t rb4,
+                                            bool two) {
+    return off ? (__ldg(off + e) & ~int64_t(15)) + r * (two ? rb4 / 2 : rb4) : (e * rows + r) * rb4;
+}
+
 // Order-preserving 32-bit key of a float: larger float -> larger key; -0.0
 // and +0.0 map to the same key (the sum with +0.0 turns -0.0 into +0.0).  A
 // NaN gets key 1: below every number (-inf is 0x007FFFFF), above the 0 of a
@@ -677,19 +686,22 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
         for (int b = 0; b < budget && next_slot < n_slots; ++b, next_slot += kWarpsD) {
             const int u = next_slot;
             const int64_t e = s.slot_e[u];
-            const uint8_t* wsrc = a.w2 + (e * H + n0) * static_cast<int64_t>(I / 2);
+            const bool two = MIXED && s.slot_bw[u] == 2;
+            const int64_t* off = MIXED ? a.w2_off : nullptr;
+            const uint8_t* wsrc = a.w2 + bank_row(off, e, H, n0, I / 2, two);
             const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(a.s2 + (e * H + n0) * ng2);
-            const int rb = MIXED && s.slot_bw[u] == 2 ? I / 4 : I / 2;  // bytes of a row that hold codes
+            const int rb = two ? I / 4 : I / 2;       // bytes of a row that hold codes
+            const int rstr = off && two ? I / 4 : I / 2;  // bytes from one row to the next
             if (u < n_smem) {
                 uint8_t* base = s.w2s + u * slot_stride;
                 for (int r = lane; r <= nrows; r += 32) {  // lane r: row r; lane nrows: the scales
-                    if (r < nrows) bulk_g2s(base + r * RS, wsrc + r * (I / 2), rb, s.w2bar);
+                    if (r < nrows) bulk_g2s(base + r * RS, wsrc + r * rstr, rb, s.w2bar);
                     else bulk_g2s(base + pl.rows_pc * RS, ssrc, nrows * ng2 * 4, s.w2bar);
                 }
             } else {
                 const int lpr = rb / 128, lines_w = nrows * lpr;  // 128-byte lines of the code bytes of each row
                 for (int c = lane; c < lines_w + lines_s; c += 32)
-                    prefetch_l2(c < lines_w ? wsrc + (c / lpr) * (I / 2) + 128 * (c % lpr) : ssrc + 128 * (c - lines_w));
+                    prefetch_l2(c < lines_w ? wsrc + (c / lpr) * rstr + 128 * (c % lpr) : ssrc + 128 * (c - lines_w));
             }
         }
     };
@@ -737,8 +749,8 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
             const bool two = MIXED && s.slot_bw[u] == 2;  // half the bytes per row
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-                const int64_t row = e * 2 * I + (r >= 2 ? I : 0) + 2 * ip + (r & 1);
-                const uint8_t* wp = a.w13 + row * (H / 2);
+                const int64_t rr = (r >= 2 ? I : 0) + 2 * ip + (r & 1), row = e * 2 * I + rr;
+                const uint8_t* wp = a.w13 + bank_row(MIXED ? a.w13_off : nullptr, e, 2 * I, rr, H / 2, two);
 #pragma unroll
                 for (int p = 0; p < NP; ++p) {
                     if (two && p >= PC1) break;
@@ -949,7 +961,8 @@ __global__ void __launch_bounds__(kThreadsD, 1) decode_kernel(DecodeArgs a, Deco
             const int64_t e = s.slot_e[u];
             const bool in_smem = u < n_smem;
             const uint8_t* wrow = in_smem ? s.w2s + u * slot_stride + r * RS
-                                          : a.w2 + (e * H + n0 + r) * static_cast<int64_t>(I / 2);
+                                          : a.w2 + bank_row(MIXED ? a.w2_off : nullptr, e, H, n0 + r, I / 2,
+                                                            MIXED && s.slot_bw[u] == 2);
             const float* srow = in_smem ? reinterpret_cast<const float*>(s.w2s + u * slot_stride + pl.rows_pc * RS) + r * ng2
                                         : a.s2 + (e * H + n0 + r) * ng2;
             const uint8_t* xrow = s.hq + p * HQS;

@@ -19,6 +19,8 @@ struct DecodeArgs {
     const int32_t* ids_in;   // forward: routing supplied by the caller ([T][k] ids, clamped to [0, E)), or null
     const float* wts_in;     //          its weights [T][k] (logits unused)
     const uint8_t* slot_bits;  // forward: code width of each bank slot [E+S] (2 or 4), or null (all 4)
+    const int64_t* w13_off;    // forward with slot_bits: compact storage, slot e's gate/up rows at w13 + w13_off[e]
+    const int64_t* w2_off;     //   and its down rows at w2 + w2_off[e], each row at its slot's width; or null
     const uint8_t* w13;
     const float* s13;
     const uint8_t* w2;

@@ -22,6 +22,8 @@ struct TcArgs {
     const float* ws;          // [slots][rows_per_slot][K/g]
     const uint8_t* slot_bits; // code width of each slot (2 or 4), or null (all 4): a 2-bit row holds its
                               // K codes in its first K/4 bytes, element 4j + p in bits 2p, 2p+1 of byte j
+    const int64_t* w_off;     // with slot_bits: compact storage, slot e's rows at w + w_off[e], each K/4
+                              // (2-bit) or K/2 (4-bit) bytes after the one before; or null (K/2 stride)
     int64_t rows_per_slot;    // 2I (gate/up) or H (down)
     int64_t K;                // H (gate/up) or I (down)
     int g;

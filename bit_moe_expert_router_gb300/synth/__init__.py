@@ -190,6 +190,30 @@ def make_bank(w: Workload, with_codes: bool = False, pack2: bool = False):
     return (bank, c13, c2) if with_codes else bank
 
 
+def compact_bank(bank: Bank):
+    """The same codes in compact storage: every slot's rows back to back at the slot's own width (K/4 bytes
+    per row for a 2-bit slot, K/2 for a 4-bit one), slots one after another in slot order.
+
+    Returns (w13 uint8 [bytes], w13_off int64 [slots], w2 uint8 [bytes], w2_off int64 [slots]): each slot's
+    byte offset in each flat bank.  Layout only: the bytes of a row are the uniform bank's, cut to the width.
+    """
+    bits = bank.slot_bits if bank.slot_bits is not None else np.full(bank.w13.shape[0], 4, np.uint8)
+
+    def flat(w):
+        parts, offs, pos = [], [], 0
+        for e in range(w.shape[0]):
+            rb = w.shape[2] // 2 if bits[e] == 2 else w.shape[2]
+            part = np.ascontiguousarray(w[e, :, :rb]).reshape(-1)
+            offs.append(pos)
+            parts.append(part)
+            pos += part.size
+        return np.concatenate(parts), np.asarray(offs, dtype=np.int64)
+
+    w13, o13 = flat(bank.w13)
+    w2, o2 = flat(bank.w2)
+    return w13, o13, w2, o2
+
+
 def logit_bias(w: Workload) -> np.ndarray:
     """fp64 [T, E] bias added to the N(0, sigma) router logits."""
     T, E = w.T, w.E

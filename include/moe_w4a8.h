@@ -381,6 +381,43 @@ int moe_w4a8_forward_w2w4(const int8_t* x_q, const float* x_scale, const float* 
                           const moe_dims_t* d, float* out,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Compact storage of a mixed 2/4-bit bank.  moe_w4a8_forward_w2w4 keeps a
+ * 2-bit slot at the int4 row length, so the bank takes the same HBM either
+ * way.  The compact layout puts each slot's rows back to back at the slot's
+ * own code width -- K/4 bytes per row for a 2-bit slot, K/2 for a 4-bit
+ * slot (same codes, same packing within a row) -- and the slots one after
+ * another in slot order, so a 2-bit expert takes half the bank bytes of a
+ * 4-bit one.  Host function, no device work: from slot_bits (HOST, E+S
+ * bytes, 2 or 4; any other value is read as 4) it writes each slot's byte
+ * offset in the gate/up bank and in the down bank (HOST int64 arrays of E+S
+ * entries) and each bank's size in bytes.  Every offset is a multiple of 16
+ * (H and I are multiples of 64).  Errors: MOE_ERR_INVALID_ARG for a null
+ * pointer; dims are checked as for moe_w4a8_forward (MOE_ERR_INVALID_ARG,
+ * MOE_ERR_UNSUPPORTED).
+ */
+int moe_w4a8_mixed_bank_layout(const uint8_t* slot_bits, const moe_dims_t* d, int64_t* w13_off, int64_t* w2_off,
+                               int64_t* w13_bytes, int64_t* w2_bytes);
+
+/*
+ * moe_w4a8_forward_w2w4 on a bank in compact storage: slot e's rows begin
+ * at w13_packed + w13_off[e] (2I rows of H codes) and w2_packed + w2_off[e]
+ * (H rows of I codes), DEVICE int64 arrays of E+S entries (for example the
+ * layout above), each row K/4 bytes (2-bit slot) or K/2 bytes (4-bit slot)
+ * after the one before.  Offsets must be multiples of 16 (the kernels clear
+ * their low four bits, so a wrong offset reads wrong bytes, never a
+ * misaligned address) and, like the bank pointers themselves, lie inside
+ * the caller's buffers: they are not checked.  Scales, slot_bits, engines,
+ * size limits and errors as for moe_w4a8_forward_w2w4 (null offsets:
+ * MOE_ERR_INVALID_ARG); the output equals moe_w4a8_forward_w2w4's on the
+ * same codes bit for bit.
+ */
+int moe_w4a8_forward_w2w4_compact(const int8_t* x_q, const float* x_scale, const float* router_logits,
+                                  const uint8_t* w13_packed, const int64_t* w13_off, const float* w13_scale,
+                                  const uint8_t* w2_packed, const int64_t* w2_off, const float* w2_scale,
+                                  const uint8_t* slot_bits, const moe_dims_t* d, float* out,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

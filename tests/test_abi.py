@@ -216,6 +216,59 @@ def test_mixed_bank_entry_checks_its_arguments(lib):
     assert lib.moe_w4a8_forward_w2w4(*args, fake, ctypes.byref(big), fake, fake, need_big, None) == 2
 
 
+def test_compact_mixed_bank_layout_matches_the_generators_compaction(lib):
+    """The host layout helper (no device work): the same per-slot offsets and bank sizes as the seeded
+    generator's own compaction of a mixed bank, and its argument checks."""
+    import numpy as np
+    import torch
+    from bit_moe_expert_router_gb300 import binding, synth
+    w = synth.Workload("layout_mixed", T=1, H=256, I=128, E=6, S=1, top_k=2, group=64, twobit_frac=0.5)
+    bank = synth.make_bank(w, pack2=True)
+    assert 0 < (bank.slot_bits == 2).sum() < w.E
+    w13c, o13, w2c, o2 = synth.compact_bank(bank)
+    d = binding.dims_of(w.T, w.H, w.I, w.E, w.S, w.top_k, w.group)
+    g13, g2, n13, n2 = binding.moe_w4a8_mixed_bank_layout(torch.from_numpy(bank.slot_bits.copy()), d)
+    assert np.array_equal(g13.numpy(), o13) and np.array_equal(g2.numpy(), o2)
+    assert (n13, n2) == (w13c.size, w2c.size)
+    assert np.all(g13.numpy() % 16 == 0) and np.all(g2.numpy() % 16 == 0)
+    # a 2-bit slot takes half the bytes of a 4-bit one in both banks
+    n4 = int((bank.slot_bits == 4).sum())
+    assert n13 == (2 * n4 + (w.E + w.S - n4)) * 2 * w.I * w.H // 4
+    # the compacted rows are the uniform rows cut to the slot's width
+    e2 = int(np.nonzero(bank.slot_bits == 2)[0][0])
+    row = w13c[o13[e2] + 3 * (w.H // 4): o13[e2] + 4 * (w.H // 4)]
+    assert np.array_equal(row, bank.w13[e2, 3, : w.H // 4])
+    bits = np.ascontiguousarray(bank.slot_bits)
+    i64 = ctypes.c_int64()
+    o = np.empty(w.E + w.S, np.int64)
+    assert lib.moe_w4a8_mixed_bank_layout(None, ctypes.byref(d), o.ctypes.data, o.ctypes.data, ctypes.byref(i64),
+                                          ctypes.byref(i64)) == 1
+    bad = binding.dims_of(1, 256, 96, 6, 1, 2, 32)  # I not a multiple of 64
+    assert lib.moe_w4a8_mixed_bank_layout(bits.ctypes.data, ctypes.byref(bad), o.ctypes.data, o.ctypes.data,
+                                          ctypes.byref(i64), ctypes.byref(i64)) == 2
+
+
+def test_compact_mixed_bank_entry_checks_its_arguments(lib):
+    from bit_moe_expert_router_gb300 import binding
+    d = binding.dims_of(4, 2048, 512, 512, 1, 10, 128)
+    need = lib.moe_w4a8_workspace_size(ctypes.byref(d))
+    fake = ctypes.c_void_p(0x100000)       # never dereferenced: the checks fail first
+    x = [fake] * 3
+    # null offsets or slot widths: invalid before anything is enqueued
+    assert lib.moe_w4a8_forward_w2w4_compact(*x, fake, None, fake, fake, fake, fake, fake, ctypes.byref(d), fake,
+                                             fake, need, None) == 1
+    assert lib.moe_w4a8_forward_w2w4_compact(*x, fake, fake, fake, fake, None, fake, fake, ctypes.byref(d), fake,
+                                             fake, need, None) == 1
+    assert lib.moe_w4a8_forward_w2w4_compact(*x, fake, fake, fake, fake, fake, fake, None, ctypes.byref(d), fake,
+                                             fake, need, None) == 1
+    assert lib.moe_w4a8_forward_w2w4_compact(*x, fake, fake, fake, fake, fake, fake, fake, ctypes.byref(d), fake,
+                                             fake, need - 256, None) == 3
+    big = binding.dims_of(4096, 2048, 512, 512, 1, 10, 64)
+    need_big = lib.moe_w4a8_workspace_size(ctypes.byref(big))
+    assert lib.moe_w4a8_forward_w2w4_compact(*x, fake, fake, fake, fake, fake, fake, fake, ctypes.byref(big), fake,
+                                             fake, need_big, None) == 2
+
+
 def test_plain_c_program_links_against_the_library(cuda_lib, tmp_path):
     """The boundary is a C ABI: a C11 program includes the header, links the library and calls it
     (host-side entry points only: no GPU is needed for these)."""

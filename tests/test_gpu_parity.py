@@ -697,6 +697,43 @@ def test_mixed_2bit_bank_on_the_tcgen05_engine(name):
     assert np.array_equal(out.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("name,T", [("dec_mixed", None), ("tc_mixed", None), ("large_bank_t2048", 6),
+                                    ("large_bank_t2048", None)])
+def test_compact_mixed_bank_reproduces_the_uniform_layout(name, T):
+    """Compact storage of a mixed 2/4-bit bank (each slot's rows at its own width, slots back to back, the
+    library's layout helper giving the offsets): bit for bit the output of the uniform layout on the same
+    codes -- on the decode engine (dec_mixed, 6 tokens of the large bank) and the tcgen05 engine (tc_mixed,
+    the 2048-token large bank) -- so the oracle checks of the uniform layout carry over; the small case is
+    also checked against the oracle directly."""
+    w = {"dec_mixed": DEC_MIXED, "tc_mixed": TC_MIXED}.get(name) or synth.WORKLOADS[name]
+    if T is not None:
+        w = w.with_tokens(T)
+    tok = synth.make_tokens(w)
+    b2 = synth.make_bank(w, pack2=True)
+    assert (b2.slot_bits == 2).sum() >= 2
+    d = gh.dims(w)
+    w13c, o13, w2c, o2 = synth.compact_bank(b2)
+    l13, l2, n13, n2 = binding.moe_w4a8_mixed_bank_layout(torch.from_numpy(b2.slot_bits.copy()), d)
+    assert np.array_equal(l13.numpy(), o13) and np.array_equal(l2.numpy(), o2) and (n13, n2) == (w13c.size, w2c.size)
+    assert w13c.size < b2.w13.size and w2c.size < b2.w2.size
+    x = [gh.to_dev(a) for a in (tok.x_q, tok.x_scale, tok.logits)]
+    s13, s2, bits = gh.to_dev(b2.s13), gh.to_dev(b2.s2), gh.to_dev(b2.slot_bits)
+    ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), "cuda:0")
+    ref = torch.empty((w.T, w.H), dtype=torch.float32, device="cuda:0")
+    binding.moe_w4a8_forward_w2w4(*x, gh.to_dev(b2.w13), s13, gh.to_dev(b2.w2), s2, bits, d, ref, ws)
+    torch.cuda.synchronize()
+    assert binding.moe_w4a8_device_status(ws) == 0
+    out = torch.full_like(ref, float("nan"))
+    binding.moe_w4a8_forward_w2w4_compact(*x, gh.to_dev(w13c), gh.to_dev(o13), s13, gh.to_dev(w2c), gh.to_dev(o2),
+                                          s2, bits, d, out, ws)
+    torch.cuda.synchronize()
+    assert binding.moe_w4a8_device_status(ws) == 0
+    got = out.cpu().numpy()
+    assert np.array_equal(got, ref.cpu().numpy())
+    if w.T <= 8:
+        gh.assert_output_close(got, oracle.forward_workload(w, tok, b2), f"compact mixed bank {name}")
+
+
 def _routed_call(w, tok, ids, wts):
     w13, s13, w2, s2 = gh.device_bank(w)
     d = gh.dims(w)
