@@ -1068,7 +1068,7 @@ cudaError_t launch_shape(DecodeMode mode, const DecodeArgs& a, const DecodePlan&
 bool decode_shape_supported(int64_t H, int64_t I) {
     if (H % 2048 != 0 || I % 512 != 0) return false;
     const int64_t p1 = H / 2048, p2 = I / 512;
-    return (p1 == 1 || p1 == 2) && (p2 == 1 || p2 == 3);
+    return (p1 == 1 || p1 == 2) && (p2 >= 1 && p2 <= 4);
 }
 
 // Shared-memory plan of one launch (host side; the kernel reads the offsets).
@@ -1152,8 +1152,12 @@ cudaError_t launch_decode(DecodeMode mode, const DecodeArgs& a, const DecodePlan
     if (a.H != 2048 * p1 || a.I != 512 * p2) return cudaErrorInvalidValue;  // the kernel's shape is compiled in
     if (p1 == 1 && p2 == 1) return launch_shape<1, 1>(mode, a, pl, grid, st);
     if (p1 == 2 && p2 == 1) return launch_shape<2, 1>(mode, a, pl, grid, st);
+    if (p1 == 1 && p2 == 2) return launch_shape<1, 2>(mode, a, pl, grid, st);
+    if (p1 == 2 && p2 == 2) return launch_shape<2, 2>(mode, a, pl, grid, st);
     if (p1 == 1 && p2 == 3) return launch_shape<1, 3>(mode, a, pl, grid, st);
     if (p1 == 2 && p2 == 3) return launch_shape<2, 3>(mode, a, pl, grid, st);
+    if (p1 == 1 && p2 == 4) return launch_shape<1, 4>(mode, a, pl, grid, st);
+    if (p1 == 2 && p2 == 4) return launch_shape<2, 4>(mode, a, pl, grid, st);
     return cudaErrorInvalidValue;
 }
 

@@ -81,7 +81,7 @@ extern "C" {
 
 /* Engines (the `engine` argument of the checking entry points).  AUTO picks
  * what moe_w4a8_forward picks: the fused decode engine when the batch fits
- * it (T <= 32, T*k <= 512 pairs, H = 2048 or 4096, I = 512 or 1536, g a
+ * it (T <= 32, T*k <= 512 pairs, H = 2048 or 4096, I = 512, 1024, 1536 or 2048, g a
  * multiple of 64 with I/g a multiple of 4), else the tcgen05 engine when g
  * is a multiple of 128, else the grouped mma.sync engine.
  *   GROUPED  grouped GEMMs on the legacy int8 mma.sync path (any valid dims)
@@ -367,7 +367,7 @@ int moe_w4a8_forward_bf16(const uint16_t* x_bf16, const float* router_logits,
  * Scales are unchanged (one per row and group).  A 2-bit slot's code bytes
  * -- what a decode step streams -- are half those of a 4-bit slot.
  * Small batches run on the decode engine (T <= 32, T*k <= 512, H in
- * {2048, 4096}, I in {512, 1536}, g a multiple of 64 with I/g a multiple
+ * {2048, 4096}, I in {512, 1024, 1536, 2048}, g a multiple of 64 with I/g a multiple
  * of 4), larger ones on the tcgen05 engine (H and I multiples of 128, g a
  * multiple of 128, E+S <= 1039); other sizes return MOE_ERR_UNSUPPORTED.  A null slot_bits is
  * MOE_ERR_INVALID_ARG (it needs no particular alignment; a value other than

@@ -442,6 +442,34 @@ def test_decode_engine_matches_grouped_engine_on_large_bank_shape():
     gh.assert_output_close(b, ref, "grouped engine, large bank")
 
 
+@pytest.mark.parametrize("H,I,T", [(2048, 1024, 5), (4096, 2048, 3), (2048, 2048, 9)])
+def test_decode_engine_intermediate_widths(H, I, T):
+    """The decode engine at intermediate widths I = 1024 and 2048 (both hidden sizes): auto-selected, and
+    within tolerance of the oracle, with a 2-bit-free and a mixed bank (the latter through the uniform and
+    the compact storage, bit for bit alike)."""
+    w = synth.Workload(f"dec_h{H}_i{I}", T=T, H=H, I=I, E=40, S=1, top_k=4, group=128, twobit_frac=0.25)
+    assert binding.moe_w4a8_engine_for(gh.dims(w)) == 1
+    tok = synth.make_tokens(w)
+    got = _forward_engine(w, tok, 1)
+    gh.assert_output_close(got, gh.oracle_out(w, tok, gh.bank_of(w)), f"decode engine H={H} I={I}")
+    b2 = synth.make_bank(w, pack2=True)
+    d = gh.dims(w)
+    x = [gh.to_dev(a) for a in (tok.x_q, tok.x_scale, tok.logits)]
+    s13, s2, bits = gh.to_dev(b2.s13), gh.to_dev(b2.s2), gh.to_dev(b2.slot_bits)
+    ws = binding.alloc_workspace(binding.moe_w4a8_workspace_size(d), "cuda:0")
+    out = torch.empty((w.T, w.H), dtype=torch.float32, device="cuda:0")
+    binding.moe_w4a8_forward_w2w4(*x, gh.to_dev(b2.w13), s13, gh.to_dev(b2.w2), s2, bits, d, out, ws)
+    w13c, o13, w2c, o2 = synth.compact_bank(b2)
+    outc = torch.full_like(out, float("nan"))
+    binding.moe_w4a8_forward_w2w4_compact(*x, gh.to_dev(w13c), gh.to_dev(o13), s13, gh.to_dev(w2c), gh.to_dev(o2),
+                                          s2, bits, d, outc, ws)
+    torch.cuda.synchronize()
+    assert binding.moe_w4a8_device_status(ws) == 0
+    mixed = out.cpu().numpy()
+    gh.assert_output_close(mixed, oracle.forward_workload(w, tok, b2), f"decode engine H={H} I={I}, mixed bank")
+    assert np.array_equal(outc.cpu().numpy(), mixed)
+
+
 def test_decode_engine_is_deterministic_and_auto_selected():
     w = synth.WORKLOADS["decode_t4"]
     tok = synth.make_tokens(w, batch=3)
