@@ -34,13 +34,17 @@
 // each accumulator drain over more tokens.  192 columns is the widest that
 // leaves two accumulators and two A stages in the 512 columns of tensor
 // memory (2 x 192 + 2 x 64).
-//   A (the unpacked weights, fp16): each producer warp copies the packed
-//     rows of its 32 tile rows for a stage (64 bytes each, cp.async, four
-//     lanes per row) into a 3-deep ring two stages ahead; each producer
-//     thread unpacks its row's 128 codes and writes them to its own
-//     tensor-memory lane with tcgen05.st, so A never passes through shared
-//     memory.  (TMA boxes of 64-byte rows measured slower: the TMA unit
-//     spends its time per row.)  Gate/up tiles interleave the rows (tile row 2j = gate row i,
+//   A (the unpacked weights, fp16): the packed rows of a stage (128 rows x
+//     64 bytes = 128 codes each) land in a 3-deep shared-memory ring: for an
+//     int4 bank as two 2-D TMA tiles of 64 rows (64-byte swizzle) issued by
+//     a loader warp of its own; for a mixed 2/4-bit or a compact bank as
+//     cp.async copies of each producer warp's 32 rows, two stages ahead.
+//     (The TMA tiles measured 5-7% faster per step than the cp.async copies;
+//     an earlier TMA version, whose tiles shared an issuing thread with the
+//     B tiles, measured slower.)  Each producer thread then unpacks its
+//     row's 128 codes and writes them to its own tensor-memory lane with
+//     tcgen05.st, so the unpacked A never passes through shared memory.
+//     Gate/up tiles interleave the rows (tile row 2j = gate row i,
 //     2j + 1 = up row i, i = 64 m + j): the SiLU(gate) * up product pairs
 //     neighbouring lanes.
 //   B (token rows, fp16, 128-byte-swizzled K-major atoms): contiguous rows
@@ -64,10 +68,12 @@
 // warp's lanes hold consecutive output features, and a tile's pair rows are
 // consecutive.
 //
-// Eighteen warps: 0 MMA issue (one thread; the tensor-memory allocation is
+// Nineteen warps: 0 MMA issue (one thread; the tensor-memory allocation is
 // the warp's), 1 the B tiles (one thread), 2-5 producers (thread = tile row
-// of A, rows 32 (w % 4) .. +31) and 6-17 epilogue (warp w: TMEM lanes
-// 32 (w % 4) .. +31 = tile rows, columns 64 ((w - 6) / 4) .. +63).  The MMA
+// of A, rows 32 (w % 4) .. +31; 2-9 for the down projection, two K halves
+// per row) and then the epilogue (warp w: TMEM lanes 32 (w % 4) .. +31 =
+// tile rows, a column range per group of four warps), 18 the A tiles (one
+// thread, int4 banks).  The MMA
 // thread does nothing but wait, issue and commit, and it has the lowest
 // warp id: with busy warps beside it on its scheduler each of its
 // instructions otherwise waited tens of cycles, and its loop has to stay
@@ -98,7 +104,8 @@ namespace {
 constexpr int kMmaWarp = 0;                  // MMA issue and the tensor-memory allocation
 constexpr int kBWarp = 1;                    // B tiles
 constexpr int kProdWarp0 = 2;                // producers, then the epilogue (split per mode below)
-constexpr int kNumWarps = 18;
+constexpr int kNumWarps = 19;
+constexpr int kAWarp = kNumWarps - 1;        // packed A tiles by TMA (int4 banks; idle otherwise)
 constexpr int kTcThreads = 32 * kNumWarps;
 constexpr int kTileN = 192;                  // tokens per tile (MMA width <= 192)
 constexpr int kAcc = 2;                      // accumulators in tensor memory
@@ -121,7 +128,7 @@ constexpr int kOffPrefix = kOffColf + 2 * kTileN * 4;           // int [kMaxSlot
 constexpr int kItab = 256;                                      // this CTA's first items, decoded once
 constexpr int kOffItab = kOffPrefix + ((kMaxSlotsTc + 1) * 4 + 7) / 8 * 8;  // ItemRec [kItab]
 constexpr int kOffBars = kOffItab + kItab * 8;                  // mbarriers, then small words
-constexpr int kBarWords = kAStages + 2 * kBStages + 2 * kAcc + 1;
+constexpr int kBarWords = kAStages + 2 * kBStages + 2 * kAcc + 1 + 2 * kRaw;
 constexpr int kOffMisc = kOffBars + 8 * kBarWords;              // tmem holder, abort flag, warp sums
 constexpr int kSmemUsed = kOffMisc + 4 * (2 + kNumWarps + 1);
 constexpr int kSmemTc = kSmemUsed + 1024;                      // + room to align the base to 1024 bytes
@@ -353,7 +360,7 @@ struct Roles {
     static constexpr bool scaled = M == TcMode::kDown || M == TcMode::kDownY;
     static constexpr int prod = scaled ? 8 : 4;
     static constexpr int epi0 = kProdWarp0 + prod;
-    static constexpr int epi = kNumWarps - epi0;
+    static constexpr int epi = kAWarp - epi0;
     static constexpr int cols = 4 * kTileN / epi;  // accumulator columns per epilogue warp
     static constexpr int parts = prod / 4;         // K parts of a stage, one per producer warp of a quarter
     static_assert(prod % 4 == 0 && epi % 4 == 0 && cols % 16 == 0 && 4 * kTileN % epi == 0, "warp split");
@@ -377,9 +384,12 @@ struct Cursor {
 
 // COMPACT: the bank is in compact storage (a.w_off); a variant of its own, so the producers' fetch
 // of the uniform layout keeps its shape (a run-time test there measured 1.5-2.5% slower).
-template <TcMode MODE, bool COMPACT = false>
+// TMA_A: the packed A tiles come by TMA (a loader warp of their own) instead of the producers'
+// cp.async copies; int4 banks in the uniform layout only (2-bit rows and compact slots keep cp.async).
+template <TcMode MODE, bool COMPACT = false, bool TMA_A = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    tc_gemm_kernel(TcArgs a, int n_mt, const __grid_constant__ CUtensorMap bmap) {
+    tc_gemm_kernel(TcArgs a, int n_mt, const __grid_constant__ CUtensorMap bmap,
+                   const __grid_constant__ CUtensorMap amap) {
     extern __shared__ uint8_t smem_raw[];
     // (offset from the __shared__ array itself, not an integer cast: the compiler then keeps every
     // access below in the shared state space and knows it cannot alias the global stores)
@@ -398,6 +408,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* accf = empty + kBStages;           // [kAcc] MMA commit at a group's end
     uint64_t* acce = accf + kAcc;                // [kAcc] epilogue arrivals
     uint64_t* done = acce + kAcc;
+    uint64_t* raw_full = done + 1;               // [kRaw] TMA_A: expect-tx arrival + the A tile bytes
+    uint64_t* raw_empty = raw_full + kRaw;       // [kRaw] TMA_A: the producers have read the stage
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     int* warp_sums = abort_flag + 1;  // [kNumWarps + 1]
@@ -426,6 +438,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(acce + b, kEpiThreads);
         }
         mbar_init(done, 1);
+        for (int r = 0; r < kRaw; ++r) {
+            mbar_init(raw_full + r, 1);
+            mbar_init(raw_empty + r, 32 * R::prod);
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -531,7 +547,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int pw = warp & 3;  // this warp's tensor-memory lane quarter = its 32 tile rows
         const int kh = (warp - kProdWarp0) >> 2;
         const int pt = 32 * pw + lane;
-        const int rsw = (pt >> 1) & 3;  // 16-byte chunk q of row r sits at q ^ ((r >> 1) & 3): no bank conflicts
+        // Row of the raw stage holding tile row pt: the tile row itself (cp.async copies), or, for
+        // TMA tiles, its place in the stage's two 64-row boxes (gate/up: gate rows, then up rows).
+        const int arow = TMA_A && gateup ? ((pt & 1) ? 64 : 0) + (pt >> 1) : pt;
+        const int rsw = (arow >> 1) & 3;  // 16-byte chunk q of row r sits at q ^ ((r >> 1) & 3): no bank
+                                          // conflicts (the TMA tiles' 64-byte swizzle is the same pattern)
         Cursor lc{static_cast<int>(blockIdx.x), 0, 0};
         int l_use = 0, l_dec = -1;
         bool l_two = false;  // the fetched item's slot holds 2-bit codes
@@ -578,7 +598,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ++l_use;
         };
         bool ok = true;
-        for (int d = 0; d < kRaw - 1; ++d) fetch();
+        if (!TMA_A)
+            for (int d = 0; d < kRaw - 1; ++d) fetch();
         int use = 0;
         for (int item = blockIdx.x, j = 0; item < total && ok; item += gridDim.x, ++j) {
             // Scaled (down) modes: A carries each code times its group's scale over the row's
@@ -595,10 +616,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             for (int ks = 0; ks < ksteps; ++ks, ++use) {
                 const float sg = scaled ? __ldg(srow + ks / spg) : 0.f;  // (loaded ahead of the waits)
-                fetch();                      // use + kRaw - 1 into the slot of use - 1
-                cp_async_wait<kRaw - 1>();    // this lane's copies for this use have landed
-                __syncwarp();                 // ... and the other lanes' copies of this warp's rows
-                const uint4* rp = reinterpret_cast<const uint4*>(raw + (use % kRaw) * kRawStage + pt * 64);
+                if (TMA_A) {  // the stage's tiles have landed
+                    if (!__all_sync(0xffffffffu, wait_bar(raw_full + use % kRaw, (use / kRaw) & 1, ctl))) {
+                        ok = false;
+                        break;
+                    }
+                } else {
+                    fetch();                      // use + kRaw - 1 into the slot of use - 1
+                    cp_async_wait<kRaw - 1>();    // this lane's copies for this use have landed
+                    __syncwarp();                 // ... and the other lanes' copies of this warp's rows
+                }
+                const uint4* rp = reinterpret_cast<const uint4*>(raw + (use % kRaw) * kRawStage + arow * 64);
                 uint4 rw[kPieces];
 #pragma unroll
                 for (int q = 0; q < kPieces; ++q) rw[q] = rp[(kh * kPieces + q) ^ rsw];
@@ -640,6 +668,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tmem_st32(ta + 32 * h2, av);
                 }
                 tmem_st_wait();
+                // TMA_A: the raw stage goes back to the loader only now that the unpack above has
+                // consumed the loaded words (an arrival right after the loads let the next tile's TMA
+                // write overtake loads still in flight: the async proxy is not ordered behind them)
+                if (TMA_A) mbar_arrive(raw_empty + use % kRaw);
                 // Thread 0 holds its arrival back until the use's B tiles have landed, so the MMA
                 // thread waits on one barrier per use.
                 if (!__all_sync(0xffffffffu, pt != 0 || kh != 0 || wait_bar(b_full + use % kBStages, (use / kBStages) & 1, ctl))) {
@@ -693,6 +725,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (global_ns() - t0 > kWaitNs) {
                     atomicOr(&a.hdr->status, kDevTimeout);
                     break;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kAWarp) {
+        // ------------------------------------------------------------ A tiles (lane 0, TMA_A)
+        // The packed rows of use u go into raw stage u % kRaw once the producers
+        // have read use u - kRaw from it: two 2-D TMA tiles of 64 rows x 64 bytes
+        // (128 codes), 64-byte swizzle (gate/up: the 64 gate rows, then the 64 up
+        // rows of the weight tile; down: rows 0-63 and 64-127).  A thread of its
+        // own: a thread's copies to one barrier measured as waiting for its
+        // copies to the barrier before.
+        if (TMA_A && lane == 0) {
+            int use = 0;
+            bool ok = true;
+            for (int item = blockIdx.x, j = 0; item < total && ok; item += gridDim.x, ++j) {
+                const Item it = item_at(j, item);
+                const int y0 = static_cast<int>(it.slot * rows_per_slot + (gateup ? 64 : 128) * it.mt);
+                const int y1 = gateup ? static_cast<int>(it.slot * rows_per_slot + a.I + 64 * it.mt) : y0 + 64;
+                for (int ks = 0; ks < ksteps; ++ks, ++use) {
+                    const int r = use % kRaw;
+                    if (use >= kRaw && !wait_bar(raw_empty + r, ((use / kRaw) & 1) ^ 1, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* dst = raw + r * kRawStage;
+                    mbar_expect_tx(raw_full + r, kRawStage);
+                    tma_tile2d(dst, &amap, 64 * ks, y0, raw_full + r);
+                    tma_tile2d(dst + 64 * 64, &amap, 64 * ks, y1, raw_full + r);
+                }
+            }
+            // every tile issued above lands before the CTA leaves
+            for (int u = max(0, use - kRaw); u < use; ++u) {
+                const uint64_t t1 = global_ns();
+                while (!mbar_try_wait(raw_full + u % kRaw, (u / kRaw) & 1) && global_ns() - t1 < kWaitNs) {
                 }
             }
         }
@@ -1014,6 +1081,22 @@ cudaError_t make_bmap(const TcArgs& a, CUtensorMap* bmap) {
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Packed weight rows of every slot as one 2-D uint8 tensor (K/2 bytes per row): 64-byte x 64-row
+// boxes, 64-byte swizzle (16-byte chunk q of box row r at q ^ ((r >> 1) & 3)).
+cudaError_t make_amap(const TcArgs& a, CUtensorMap* amap) {
+    Encode encode = nullptr;
+    if (cudaError_t e = get_encode(&encode); e != cudaSuccess) return e;
+    const cuuint32_t elem[2] = {1, 1};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K / 2),
+                                static_cast<cuuint64_t>(a.n_slots) * static_cast<cuuint64_t>(a.rows_per_slot)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K / 2)};
+    const cuuint32_t box[2] = {64, 64};
+    const CUresult r = encode(amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.w), dims, strides, box, elem,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Fixed-order combine from bf16 Y: one thread per (token, 8 output columns).
 __global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* __restrict__ y,
                                                            const float* __restrict__ wts, const int32_t* __restrict__ inv,
@@ -1041,9 +1124,9 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* 
     }
 }
 
-template <TcMode MODE, bool COMPACT = false>
+template <TcMode MODE, bool COMPACT = false, bool TMA_A = false>
 cudaError_t launch_mode_tc(const TcArgs& a, int n_mt, cudaStream_t st) {
-    auto kern = tc_gemm_kernel<MODE, COMPACT>;
+    auto kern = tc_gemm_kernel<MODE, COMPACT, TMA_A>;
     static std::mutex mu;
     static std::map<int, bool> attr_set;
     int dev = 0;
@@ -1058,7 +1141,10 @@ cudaError_t launch_mode_tc(const TcArgs& a, int n_mt, cudaStream_t st) {
     }
     alignas(64) CUtensorMap bmap{};
     if (cudaError_t e = make_bmap(a, &bmap); e != cudaSuccess) return e;
-    kern<<<num_sms(), kTcThreads, kSmemTc, st>>>(a, n_mt, bmap);
+    alignas(64) CUtensorMap amap{};
+    if (TMA_A)
+        if (cudaError_t e = make_amap(a, &amap); e != cudaSuccess) return e;
+    kern<<<num_sms(), kTcThreads, kSmemTc, st>>>(a, n_mt, bmap, amap);
     return cudaGetLastError();
 }
 
@@ -1079,14 +1165,21 @@ cudaError_t launch_tc_gemm(TcMode mode, const TcArgs& a, cudaStream_t st) {
     const int n_mt = static_cast<int>(gateup ? a.I / 64 : a.H / 128);
     if (n_mt < 1 || n_mt > 256) return cudaErrorInvalidValue;  // weight tile index kept in 8 bits
     switch (mode) {
+        // int4 banks: A tiles by TMA; mixed banks: the producers' copies (compact storage: its own variant)
         case TcMode::kGateUp:
-            return a.w_off ? launch_mode_tc<TcMode::kGateUp, true>(a, n_mt, st) : launch_mode_tc<TcMode::kGateUp>(a, n_mt, st);
+            return a.w_off ? launch_mode_tc<TcMode::kGateUp, true>(a, n_mt, st)
+                 : a.slot_bits ? launch_mode_tc<TcMode::kGateUp>(a, n_mt, st)
+                               : launch_mode_tc<TcMode::kGateUp, false, true>(a, n_mt, st);
         case TcMode::kDown:
-            return a.w_off ? launch_mode_tc<TcMode::kDown, true>(a, n_mt, st) : launch_mode_tc<TcMode::kDown>(a, n_mt, st);
+            return a.w_off ? launch_mode_tc<TcMode::kDown, true>(a, n_mt, st)
+                 : a.slot_bits ? launch_mode_tc<TcMode::kDown>(a, n_mt, st)
+                               : launch_mode_tc<TcMode::kDown, false, true>(a, n_mt, st);
         case TcMode::kDownY:
-            return a.w_off ? launch_mode_tc<TcMode::kDownY, true>(a, n_mt, st) : launch_mode_tc<TcMode::kDownY>(a, n_mt, st);
-        case TcMode::kGateUpPartials: return launch_mode_tc<TcMode::kGateUpPartials>(a, n_mt, st);
-        default: return launch_mode_tc<TcMode::kDownPartials>(a, n_mt, st);
+            return a.w_off ? launch_mode_tc<TcMode::kDownY, true>(a, n_mt, st)
+                 : a.slot_bits ? launch_mode_tc<TcMode::kDownY>(a, n_mt, st)
+                               : launch_mode_tc<TcMode::kDownY, false, true>(a, n_mt, st);
+        case TcMode::kGateUpPartials: return launch_mode_tc<TcMode::kGateUpPartials, false, true>(a, n_mt, st);
+        default: return launch_mode_tc<TcMode::kDownPartials, false, true>(a, n_mt, st);
     }
 }
 
