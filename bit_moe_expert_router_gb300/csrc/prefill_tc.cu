@@ -35,18 +35,17 @@
 // leaves two accumulators and two A stages in the 512 columns of tensor
 // memory (2 x 192 + 2 x 64).
 //   A (the unpacked weights, fp16): the packed rows of a stage (128 rows x
-//     64 bytes = 128 codes each) land in a 3-deep shared-memory ring: for an
-//     int4 bank as two 2-D TMA tiles of 64 rows (64-byte swizzle) issued by
-//     a loader warp of its own; for a mixed 2/4-bit or a compact bank as
-//     cp.async copies of each producer warp's 32 rows, two stages ahead.
-//     (The TMA tiles measured 5-7% faster per step than the cp.async copies;
-//     an earlier TMA version, whose tiles shared an issuing thread with the
-//     B tiles, measured slower.)  Each producer thread then unpacks its
-//     row's 128 codes and writes them to its own tensor-memory lane with
-//     tcgen05.st, so the unpacked A never passes through shared memory.
-//     Gate/up tiles interleave the rows (tile row 2j = gate row i,
-//     2j + 1 = up row i, i = 64 m + j): the SiLU(gate) * up product pairs
-//     neighbouring lanes.
+//     128 codes) land in a 3-deep shared-memory ring as two 2-D TMA tiles of
+//     64 rows, issued by a loader warp of their own (64-byte rows, 64-byte
+//     swizzle; a 2-bit slot's 32-byte rows, 32-byte swizzle, through a map of
+//     their own).  (The TMA tiles measured 5-7% faster per step than the
+//     producers' own cp.async copies; an earlier TMA version, whose tiles
+//     shared an issuing thread with the B tiles, measured slower.)  Each
+//     producer thread unpacks its row's 128 codes and writes them to its own
+//     tensor-memory lane with tcgen05.st, so the unpacked A never passes
+//     through shared memory.  Gate/up tiles interleave the rows (tile row
+//     2j = gate row i, 2j + 1 = up row i, i = 64 m + j): the SiLU(gate) * up
+//     product pairs neighbouring lanes.
 //   B (token rows, fp16, 128-byte-swizzled K-major atoms): contiguous rows
 //     by pair row -- the activations gathered per pair (gate/up) or the
 //     requantised h (down) -- loaded as two 2-D TMA tiles per stage by a
@@ -73,7 +72,7 @@
 // of A, rows 32 (w % 4) .. +31; 2-9 for the down projection, two K halves
 // per row) and then the epilogue (warp w: TMEM lanes 32 (w % 4) .. +31 =
 // tile rows, a column range per group of four warps), 18 the A tiles (one
-// thread, int4 banks).  The MMA
+// thread).  The MMA
 // thread does nothing but wait, issue and commit, and it has the lowest
 // warp id: with busy warps beside it on its scheduler each of its
 // instructions otherwise waited tens of cycles, and its loop has to stay
@@ -105,7 +104,7 @@ constexpr int kMmaWarp = 0;                  // MMA issue and the tensor-memory 
 constexpr int kBWarp = 1;                    // B tiles
 constexpr int kProdWarp0 = 2;                // producers, then the epilogue (split per mode below)
 constexpr int kNumWarps = 19;
-constexpr int kAWarp = kNumWarps - 1;        // packed A tiles by TMA (int4 banks; idle otherwise)
+constexpr int kAWarp = kNumWarps - 1;        // packed A tiles by TMA
 constexpr int kTcThreads = 32 * kNumWarps;
 constexpr int kTileN = 192;                  // tokens per tile (MMA width <= 192)
 constexpr int kAcc = 2;                      // accumulators in tensor memory
@@ -334,9 +333,6 @@ __device__ __forceinline__ float row_scale_max(const float* s, int n) {
 // Named barriers of n threads.  The non-aligned forms (barrier.sync / barrier.red, not bar.*):
 // they are reached right after per-thread bounded spin waits, so a warp may arrive diverged, and
 // the compiler does not reconverge a warp before an inline-asm barrier.
-__device__ __forceinline__ void named_bar(int id, int n) {
-    asm volatile("barrier.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
-}
 
 // Named barrier that also ORs a predicate over its threads: every thread gets the same answer.
 __device__ __forceinline__ bool named_bar_or(int id, int n, bool v) {
@@ -377,19 +373,12 @@ struct ItemRec {
 };
 static_assert(sizeof(ItemRec) == 8, "item record");
 
-// Walks this CTA's (item, K step) uses in order.
-struct Cursor {
-    int item, ks, j;  // j: the item's index among this CTA's items
-};
-
-// COMPACT: the bank is in compact storage (a.w_off); a variant of its own, so the producers' fetch
-// of the uniform layout keeps its shape (a run-time test there measured 1.5-2.5% slower).
-// TMA_A: the packed A tiles come by TMA (a loader warp of their own) instead of the producers'
-// cp.async copies; int4 banks in the uniform layout only (2-bit rows and compact slots keep cp.async).
-template <TcMode MODE, bool COMPACT = false, bool TMA_A = false>
+// COMPACT: the bank is in compact storage (a.w_off), a variant of its own (its A loader reads the
+// slots' offsets; the uniform layout's needs none).
+template <TcMode MODE, bool COMPACT = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(TcArgs a, int n_mt, const __grid_constant__ CUtensorMap bmap,
-                   const __grid_constant__ CUtensorMap amap) {
+                   const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap amap2) {
     extern __shared__ uint8_t smem_raw[];
     // (offset from the __shared__ array itself, not an integer cast: the compiler then keeps every
     // access below in the shared state space and knows it cannot alias the global stores)
@@ -408,8 +397,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* accf = empty + kBStages;           // [kAcc] MMA commit at a group's end
     uint64_t* acce = accf + kAcc;                // [kAcc] epilogue arrivals
     uint64_t* done = acce + kAcc;
-    uint64_t* raw_full = done + 1;               // [kRaw] TMA_A: expect-tx arrival + the A tile bytes
-    uint64_t* raw_empty = raw_full + kRaw;       // [kRaw] TMA_A: the producers have read the stage
+    uint64_t* raw_full = done + 1;               // [kRaw] expect-tx arrival + the A tile bytes
+    uint64_t* raw_empty = raw_full + kRaw;       // [kRaw] the producers have unpacked the stage
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     int* warp_sums = abort_flag + 1;  // [kNumWarps + 1]
@@ -528,78 +517,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (gateup) return ((r & 1) ? a.I : 0) + 64 * mt + (r >> 1);
         return static_cast<int64_t>(128) * mt + r;
     };
-    auto advance = [&](Cursor& c) {
-        if (++c.ks == ksteps) {
-            c.ks = 0;
-            c.item += gridDim.x;
-            ++c.j;
-        }
-    };
 
     if (warp >= kProdWarp0 && warp < R::epi0) {
         // ------------------------------------------------------------ producers
         // Thread pt owns tile row pt (TMEM lane pt), and this warp K part kh of
-        // each stage (all of it, or one half).  Each warp copies its part of
-        // the packed bytes of its 32 rows for use u + kRaw - 1 into the raw
-        // slot of use u - 1 (which every lane of the warp has read: the warp
-        // is past it), so the unpack never waits for HBM.
+        // each stage (all of it, or one half).  The packed rows of a use arrive
+        // in raw stage use % kRaw by TMA (the A loader warp); each thread reads
+        // its row's part into registers, unpacks it into its tensor-memory lane
+        // and only then releases the stage.
         constexpr int kPieces = 4 / R::parts;  // 16-byte pieces (32 codes) of a packed row per warp
         const int pw = warp & 3;  // this warp's tensor-memory lane quarter = its 32 tile rows
         const int kh = (warp - kProdWarp0) >> 2;
         const int pt = 32 * pw + lane;
-        // Row of the raw stage holding tile row pt: the tile row itself (cp.async copies), or, for
-        // TMA tiles, its place in the stage's two 64-row boxes (gate/up: gate rows, then up rows).
-        const int arow = TMA_A && gateup ? ((pt & 1) ? 64 : 0) + (pt >> 1) : pt;
-        const int rsw = (arow >> 1) & 3;  // 16-byte chunk q of row r sits at q ^ ((r >> 1) & 3): no bank
-                                          // conflicts (the TMA tiles' 64-byte swizzle is the same pattern)
-        Cursor lc{static_cast<int>(blockIdx.x), 0, 0};
-        int l_use = 0, l_dec = -1;
-        bool l_two = false;  // the fetched item's slot holds 2-bit codes
-        Item l_it{};
-        const uint8_t* l_wslot = nullptr;  // compact storage: the fetched item's slot's first row
-        auto fetch = [&]() {  // this warp's rows of use l_use into raw slot l_use % kRaw (one commit group)
-            if (lc.item < total) {
-                if (lc.item != l_dec) {
-                    l_it = item_at(lc.j, lc.item);
-                    l_dec = lc.item;
-                    l_two = a.slot_bits && a.slot_bits[l_it.slot] == 2;
-                    // compact storage: the slot at its offset (low four bits cleared so every 16-byte
-                    // copy stays aligned)
-                    if (COMPACT) l_wslot = a.w + (__ldg(a.w_off + l_it.slot) & ~int64_t(15));
-                }
-                // the slot's rows: uniform (K / 2 bytes apart), or compact (K / 4 apart in a 2-bit slot)
-                const uint8_t* wslot = COMPACT ? l_wslot : a.w + static_cast<int64_t>(l_it.slot) * rows_per_slot * (K / 2);
-                const int64_t rstr = COMPACT && l_two ? K / 4 : K / 2;
-                uint8_t* dst = raw + (l_use % kRaw) * kRawStage;
-                if (!l_two) {
-#pragma unroll
-                    for (int q = 0; q < kPieces; ++q) {  // kPieces lanes per row, contiguous 16-byte pieces
-                        const int idx = 32 * q + lane;
-                        const int row = 32 * pw + idx / kPieces, piece = kh * kPieces + idx % kPieces;
-                        cp_async16(dst + row * 64 + 16 * (piece ^ ((row >> 1) & 3)),
-                                   wslot + weight_row(l_it.mt, row) * rstr + 64 * lc.ks + 16 * piece);
-                    }
-                } else {
-                    // a 2-bit row holds a use's 128 codes in 32 bytes: this warp's K part is the first
-                    // kPieces / 2 of its pieces
-#pragma unroll
-                    for (int q = 0; q < kPieces; ++q) {
-                        const int idx = 32 * q + lane, lp = idx % kPieces;
-                        const int row = 32 * pw + idx / kPieces, piece = kh * kPieces + lp;
-                        if (lp < kPieces / 2)
-                            cp_async16(dst + row * 64 + 16 * (piece ^ ((row >> 1) & 3)),
-                                       wslot + weight_row(l_it.mt, row) * rstr + 32 * lc.ks +
-                                           16 * (kh * (kPieces / 2) + lp));
-                    }
-                }
-                advance(lc);
-            }
-            cp_async_commit();  // one group per use, empty or not, so the group count stays aligned
-            ++l_use;
-        };
+        // Row of the raw stage holding tile row pt: its place in the stage's two 64-row boxes (gate/up:
+        // the tile's gate rows, then its up rows; down: rows 0-63, then 64-127).
+        const int arow = gateup ? ((pt & 1) ? 64 : 0) + (pt >> 1) : pt;
+        const int rsw = (arow >> 1) & 3;  // 64-byte swizzle: 16-byte chunk q of box row r at q ^ ((r >> 1) & 3)
         bool ok = true;
-        if (!TMA_A)
-            for (int d = 0; d < kRaw - 1; ++d) fetch();
         int use = 0;
         for (int item = blockIdx.x, j = 0; item < total && ok; item += gridDim.x, ++j) {
             // Scaled (down) modes: A carries each code times its group's scale over the row's
@@ -616,20 +550,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             for (int ks = 0; ks < ksteps; ++ks, ++use) {
                 const float sg = scaled ? __ldg(srow + ks / spg) : 0.f;  // (loaded ahead of the waits)
-                if (TMA_A) {  // the stage's tiles have landed
-                    if (!__all_sync(0xffffffffu, wait_bar(raw_full + use % kRaw, (use / kRaw) & 1, ctl))) {
-                        ok = false;
-                        break;
-                    }
-                } else {
-                    fetch();                      // use + kRaw - 1 into the slot of use - 1
-                    cp_async_wait<kRaw - 1>();    // this lane's copies for this use have landed
-                    __syncwarp();                 // ... and the other lanes' copies of this warp's rows
+                // the stage's tiles have landed
+                if (!__all_sync(0xffffffffu, wait_bar(raw_full + use % kRaw, (use / kRaw) & 1, ctl))) {
+                    ok = false;
+                    break;
                 }
-                const uint4* rp = reinterpret_cast<const uint4*>(raw + (use % kRaw) * kRawStage + arow * 64);
                 uint4 rw[kPieces];
+                if (two) {  // a 2-bit tile: 32-byte rows, 32-byte swizzle (chunk q at q ^ ((r >> 2) & 1))
+                    const uint4* rp = reinterpret_cast<const uint4*>(raw + (use % kRaw) * kRawStage + arow * 32);
 #pragma unroll
-                for (int q = 0; q < kPieces; ++q) rw[q] = rp[(kh * kPieces + q) ^ rsw];
+                    for (int q = 0; q < kPieces / 2; ++q) rw[q] = rp[(kh * (kPieces / 2) + q) ^ ((arow >> 2) & 1)];
+                } else {
+                    const uint4* rp = reinterpret_cast<const uint4*>(raw + (use % kRaw) * kRawStage + arow * 64);
+#pragma unroll
+                    for (int q = 0; q < kPieces; ++q) rw[q] = rp[(kh * kPieces + q) ^ rsw];
+                }
                 const int s = use % kAStages;
                 // The A stage is free once the MMAs of use - kAStages have completed (warp-uniform
                 // outcome: the tensor-memory stores below are warp-aligned).
@@ -668,10 +603,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tmem_st32(ta + 32 * h2, av);
                 }
                 tmem_st_wait();
-                // TMA_A: the raw stage goes back to the loader only now that the unpack above has
-                // consumed the loaded words (an arrival right after the loads let the next tile's TMA
-                // write overtake loads still in flight: the async proxy is not ordered behind them)
-                if (TMA_A) mbar_arrive(raw_empty + use % kRaw);
+                // The raw stage goes back to the loader only now that the unpack above has consumed the
+                // loaded words (an arrival right after the loads let the next tile's TMA write overtake
+                // loads still in flight: the async proxy is not ordered behind them).
+                mbar_arrive(raw_empty + use % kRaw);
                 // Thread 0 holds its arrival back until the use's B tiles have landed, so the MMA
                 // thread waits on one barrier per use.
                 if (!__all_sync(0xffffffffu, pt != 0 || kh != 0 || wait_bar(b_full + use % kBStages, (use / kBStages) & 1, ctl))) {
@@ -682,7 +617,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_arrive(a_full + s);
             }
         }
-        cp_async_wait<0>();  // no copy is left in flight when the CTA leaves
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issue (lane 0)
         // Use u: wait for its B stage, a drained accumulator (at a group's
@@ -730,20 +664,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
     } else if (warp == kAWarp) {
-        // ------------------------------------------------------------ A tiles (lane 0, TMA_A)
+        // ------------------------------------------------------------ A tiles (lane 0)
         // The packed rows of use u go into raw stage u % kRaw once the producers
         // have read use u - kRaw from it: two 2-D TMA tiles of 64 rows x 64 bytes
         // (128 codes), 64-byte swizzle (gate/up: the 64 gate rows, then the 64 up
-        // rows of the weight tile; down: rows 0-63 and 64-127).  A thread of its
-        // own: a thread's copies to one barrier measured as waiting for its
-        // copies to the barrier before.
-        if (TMA_A && lane == 0) {
+        // rows of the weight tile; down: rows 0-63 and 64-127); a 2-bit slot's
+        // tiles are 64 rows x 32 bytes, 32-byte swizzle.  A thread of its own: a
+        // thread's copies to one barrier measured as waiting for its copies to
+        // the barrier before.
+        if (lane == 0) {
             int use = 0;
             bool ok = true;
             for (int item = blockIdx.x, j = 0; item < total && ok; item += gridDim.x, ++j) {
                 const Item it = item_at(j, item);
-                const int y0 = static_cast<int>(it.slot * rows_per_slot + (gateup ? 64 : 128) * it.mt);
-                const int y1 = gateup ? static_cast<int>(it.slot * rows_per_slot + a.I + 64 * it.mt) : y0 + 64;
+                // a 2-bit slot: 32 bytes of a row per use, through its own map
+                const bool two = a.slot_bits && a.slot_bits[it.slot] == 2;
+                const CUtensorMap* map = two ? &amap2 : &amap;
+                const int rb = two ? 32 : 64;
+                // the slot's first row in the map's rows: uniform, or compact (its offset over its row
+                // length; the offsets are multiples of it)
+                const int ybase = COMPACT ? static_cast<int>((__ldg(a.w_off + it.slot) & ~int64_t(15)) / (two ? K / 4 : K / 2))
+                                          : static_cast<int>(it.slot * rows_per_slot);
+                const int y0 = ybase + (gateup ? 64 : 128) * it.mt;
+                const int y1 = gateup ? static_cast<int>(ybase + a.I + 64 * it.mt) : y0 + 64;
                 for (int ks = 0; ks < ksteps; ++ks, ++use) {
                     const int r = use % kRaw;
                     if (use >= kRaw && !wait_bar(raw_empty + r, ((use / kRaw) & 1) ^ 1, ctl)) {
@@ -751,9 +694,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     uint8_t* dst = raw + r * kRawStage;
-                    mbar_expect_tx(raw_full + r, kRawStage);
-                    tma_tile2d(dst, &amap, 64 * ks, y0, raw_full + r);
-                    tma_tile2d(dst + 64 * 64, &amap, 64 * ks, y1, raw_full + r);
+                    mbar_expect_tx(raw_full + r, 128 * rb);
+                    tma_tile2d(dst, map, rb * ks, y0, raw_full + r);
+                    tma_tile2d(dst + 64 * rb, map, rb * ks, y1, raw_full + r);
                 }
             }
             // every tile issued above lands before the CTA leaves
@@ -1083,17 +1026,23 @@ cudaError_t make_bmap(const TcArgs& a, CUtensorMap* bmap) {
 
 // Packed weight rows of every slot as one 2-D uint8 tensor (K/2 bytes per row): 64-byte x 64-row
 // boxes, 64-byte swizzle (16-byte chunk q of box row r at q ^ ((r >> 1) & 3)).
-cudaError_t make_amap(const TcArgs& a, CUtensorMap* amap) {
+// two: the map of the 2-bit slots (32 code bytes of a row per 128 codes: 32-byte x 64-row boxes,
+// 32-byte swizzle), whose rows are K/2 bytes apart in the uniform layout and K/4 in the compact one.
+// Compact storage has no single row count: the map spans as many rows as a map may, and the slots'
+// offsets (inside the caller's buffer) keep every box in it.
+cudaError_t make_amap(const TcArgs& a, bool two, CUtensorMap* amap) {
     Encode encode = nullptr;
     if (cudaError_t e = get_encode(&encode); e != cudaSuccess) return e;
     const cuuint32_t elem[2] = {1, 1};
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K / 2),
-                                static_cast<cuuint64_t>(a.n_slots) * static_cast<cuuint64_t>(a.rows_per_slot)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K / 2)};
-    const cuuint32_t box[2] = {64, 64};
+    const cuuint64_t pitch = static_cast<cuuint64_t>(a.w_off && two ? a.K / 4 : a.K / 2);
+    const cuuint64_t rows = a.w_off ? std::min<cuuint64_t>((cuuint64_t(1) << 31) - 1, ((cuuint64_t(1) << 40) - 1) / pitch)
+                                    : static_cast<cuuint64_t>(a.n_slots) * static_cast<cuuint64_t>(a.rows_per_slot);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(two ? a.K / 4 : a.K / 2), rows};
+    const cuuint64_t strides[1] = {pitch};
+    const cuuint32_t box[2] = {two ? 32u : 64u, 64};
     const CUresult r = encode(amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.w), dims, strides, box, elem,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, two ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -1124,9 +1073,9 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* 
     }
 }
 
-template <TcMode MODE, bool COMPACT = false, bool TMA_A = false>
+template <TcMode MODE, bool COMPACT = false>
 cudaError_t launch_mode_tc(const TcArgs& a, int n_mt, cudaStream_t st) {
-    auto kern = tc_gemm_kernel<MODE, COMPACT, TMA_A>;
+    auto kern = tc_gemm_kernel<MODE, COMPACT>;
     static std::mutex mu;
     static std::map<int, bool> attr_set;
     int dev = 0;
@@ -1141,10 +1090,11 @@ cudaError_t launch_mode_tc(const TcArgs& a, int n_mt, cudaStream_t st) {
     }
     alignas(64) CUtensorMap bmap{};
     if (cudaError_t e = make_bmap(a, &bmap); e != cudaSuccess) return e;
-    alignas(64) CUtensorMap amap{};
-    if (TMA_A)
-        if (cudaError_t e = make_amap(a, &amap); e != cudaSuccess) return e;
-    kern<<<num_sms(), kTcThreads, kSmemTc, st>>>(a, n_mt, bmap, amap);
+    alignas(64) CUtensorMap amap{}, amap2{};
+    if (cudaError_t e = make_amap(a, false, &amap); e != cudaSuccess) return e;
+    if (a.slot_bits)
+        if (cudaError_t e = make_amap(a, true, &amap2); e != cudaSuccess) return e;
+    kern<<<num_sms(), kTcThreads, kSmemTc, st>>>(a, n_mt, bmap, amap, amap2);
     return cudaGetLastError();
 }
 
@@ -1165,21 +1115,18 @@ cudaError_t launch_tc_gemm(TcMode mode, const TcArgs& a, cudaStream_t st) {
     const int n_mt = static_cast<int>(gateup ? a.I / 64 : a.H / 128);
     if (n_mt < 1 || n_mt > 256) return cudaErrorInvalidValue;  // weight tile index kept in 8 bits
     switch (mode) {
-        // int4 banks: A tiles by TMA; mixed banks: the producers' copies (compact storage: its own variant)
+        // (compact storage: a variant of its own)
         case TcMode::kGateUp:
             return a.w_off ? launch_mode_tc<TcMode::kGateUp, true>(a, n_mt, st)
-                 : a.slot_bits ? launch_mode_tc<TcMode::kGateUp>(a, n_mt, st)
-                               : launch_mode_tc<TcMode::kGateUp, false, true>(a, n_mt, st);
+                           : launch_mode_tc<TcMode::kGateUp>(a, n_mt, st);
         case TcMode::kDown:
             return a.w_off ? launch_mode_tc<TcMode::kDown, true>(a, n_mt, st)
-                 : a.slot_bits ? launch_mode_tc<TcMode::kDown>(a, n_mt, st)
-                               : launch_mode_tc<TcMode::kDown, false, true>(a, n_mt, st);
+                           : launch_mode_tc<TcMode::kDown>(a, n_mt, st);
         case TcMode::kDownY:
             return a.w_off ? launch_mode_tc<TcMode::kDownY, true>(a, n_mt, st)
-                 : a.slot_bits ? launch_mode_tc<TcMode::kDownY>(a, n_mt, st)
-                               : launch_mode_tc<TcMode::kDownY, false, true>(a, n_mt, st);
-        case TcMode::kGateUpPartials: return launch_mode_tc<TcMode::kGateUpPartials, false, true>(a, n_mt, st);
-        default: return launch_mode_tc<TcMode::kDownPartials, false, true>(a, n_mt, st);
+                           : launch_mode_tc<TcMode::kDownY>(a, n_mt, st);
+        case TcMode::kGateUpPartials: return launch_mode_tc<TcMode::kGateUpPartials>(a, n_mt, st);
+        default: return launch_mode_tc<TcMode::kDownPartials>(a, n_mt, st);
     }
 }
 

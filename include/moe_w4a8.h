@@ -404,10 +404,13 @@ int moe_w4a8_mixed_bank_layout(const uint8_t* slot_bits, const moe_dims_t* d, in
  * at w13_packed + w13_off[e] (2I rows of H codes) and w2_packed + w2_off[e]
  * (H rows of I codes), DEVICE int64 arrays of E+S entries (for example the
  * layout above), each row K/4 bytes (2-bit slot) or K/2 bytes (4-bit slot)
- * after the one before.  Offsets must be multiples of 16 (the kernels clear
- * their low four bits, so a wrong offset reads wrong bytes, never a
- * misaligned address) and, like the bank pointers themselves, lie inside
- * the caller's buffers: they are not checked.  Scales, slot_bits, engines,
+ * after the one before.  Each offset must be a multiple of its slot's row
+ * length (K/2 bytes, or K/4 for a 2-bit slot), as the layout above gives:
+ * the tcgen05 engine addresses slot e's rows from w_off[e] / row length,
+ * and the kernels clear the offsets' low four bits, so a wrong offset reads
+ * wrong bytes, never a misaligned address.  Like the bank pointers
+ * themselves, the offsets must lie inside the caller's buffers: they are
+ * not checked.  Scales, slot_bits, engines,
  * size limits and errors as for moe_w4a8_forward_w2w4 (null offsets:
  * MOE_ERR_INVALID_ARG); the output equals moe_w4a8_forward_w2w4's on the
  * same codes bit for bit.
