@@ -132,4 +132,21 @@ __device__ __forceinline__ int requant_code(float h, float s) {
     return static_cast<int>(q);
 }
 
+// The same code from s and its reciprocal rs = 1 / s (correctly rounded): h * rs
+// is within 2^-23 relative of h / s (|h / s| <= 127), so it rounds to the same
+// integer unless it lies within 1e-4 of a half-integer; only then is the exact
+// division computed.  The rare exact path is kept out of line (the run-once
+// code of a launch is fetched cold, so it is kept small).
+static __device__ __noinline__ float rint_div_exact(float h, float s) { return rintf(__fdiv_rn(h, s)); }
+
+__device__ __forceinline__ int requant_code_fast(float h, float s, float rs) {
+    if (!(s > 0.0f)) return 0;
+    const float f = h * rs;
+    const float d = fabsf(f - floorf(f) - 0.5f);
+    float q = rintf(f);
+    if (d < 1e-4f) q = rint_div_exact(h, s);
+    q = fminf(fmaxf(q, -127.0f), 127.0f);
+    return static_cast<int>(q);
+}
+
 }  // namespace moe

@@ -944,49 +944,80 @@ __global__ void prep_x16_kernel(const int8_t* __restrict__ x, int64_t T, int64_t
 
 // h fp32 -> requantised codes as fp16 in the engine's K order, one warp per
 // pair row: the row maximum of |h| (-> amax bits and s_h = max / 127), then
-// the codes (fp32 decision, IEEE division).  With hq_in (no h) the int8
-// codes are converted as given.
+// the codes (RNE(h / s) decided in fp32: by the reciprocal, and by the IEEE
+// division within 1e-4 of a half-step).  With hq_in (no h) the int8 codes are
+// converted as given.
+// NV > 0: I = 256 NV, each lane keeps its 8 NV values of the row in registers (one read of h);
+// NV = 0: any I, the row read twice.
+template <int NV>
 __global__ void prep_h16_kernel(const float* __restrict__ h, uint32_t* __restrict__ amax,
                                 const int8_t* __restrict__ hq_in, int64_t P, int64_t I, __half* __restrict__ out,
                                 float* __restrict__ s_h) {
     const int lane = threadIdx.x & 31;
     const int64_t nw = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    auto store8 = [&](int64_t row, int64_t k, const int (&code)[8]) {
+        __half2 o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = __halves2half2(__int2half_rn(code[e]), __int2half_rn(code[e + 4]));
+        *reinterpret_cast<uint4*>(out + row * I + k) = *reinterpret_cast<const uint4*>(o);
+    };
+    auto finish_max = [&](int64_t row, float m, float& s, float& rs) {
+        m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
+        s = requant_scale(__float_as_uint(m));
+        rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
+        if (lane == 0) {
+            if (amax) amax[row] = __float_as_uint(m);
+            if (s_h) s_h[row] = s;
+        }
+    };
+    auto absmax8 = [](const float4& f0, const float4& f1) {
+        return fmaxf(fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f0.z), fabsf(f0.w))),
+                     fmaxf(fmaxf(fabsf(f1.x), fabsf(f1.y)), fmaxf(fabsf(f1.z), fabsf(f1.w))));
+    };
     for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); row < P; row += nw) {
         const float* hr = h ? h + row * I : nullptr;
-        float s = 0.f;
-        if (hr) {
-            float m = 0.f;
+        if (!hr) {  // the codes as given
+            for (int64_t k = 8 * lane; k < I; k += 256) {
+                const uint2 v = *reinterpret_cast<const uint2*>(hq_in + row * I + k);
+                const int8_t* b = reinterpret_cast<const int8_t*>(&v);
+                int code[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) code[e] = b[e];
+                store8(row, k, code);
+            }
+            continue;
+        }
+        float s, rs, m = 0.f;
+        if (NV > 0) {
+            float4 f[NV > 0 ? NV : 1][2];
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                f[v][0] = __ldcs(reinterpret_cast<const float4*>(hr + 8 * lane + 256 * v));
+                f[v][1] = __ldcs(reinterpret_cast<const float4*>(hr + 8 * lane + 256 * v + 4));
+                m = fmaxf(m, absmax8(f[v][0], f[v][1]));
+            }
+            finish_max(row, m, s, rs);
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const float g[8] = {f[v][0].x, f[v][0].y, f[v][0].z, f[v][0].w, f[v][1].x, f[v][1].y, f[v][1].z, f[v][1].w};
+                int code[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) code[e] = requant_code_fast(g[e], s, rs);
+                store8(row, 8 * lane + 256 * v, code);
+            }
+        } else {
+            for (int64_t k = 8 * lane; k < I; k += 256)
+                m = fmaxf(m, absmax8(*reinterpret_cast<const float4*>(hr + k), *reinterpret_cast<const float4*>(hr + k + 4)));
+            finish_max(row, m, s, rs);
             for (int64_t k = 8 * lane; k < I; k += 256) {
                 const float4 f0 = *reinterpret_cast<const float4*>(hr + k);
                 const float4 f1 = *reinterpret_cast<const float4*>(hr + k + 4);
-                m = fmaxf(m, fmaxf(fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f0.z), fabsf(f0.w))),
-                                   fmaxf(fmaxf(fabsf(f1.x), fabsf(f1.y)), fmaxf(fabsf(f1.z), fabsf(f1.w)))));
-            }
-            m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
-            s = requant_scale(__float_as_uint(m));
-            if (lane == 0) {
-                if (amax) amax[row] = __float_as_uint(m);
-                if (s_h) s_h[row] = s;
-            }
-        }
-        for (int64_t k = 8 * lane; k < I; k += 256) {
-            int code[8];
-            if (hr) {
-                const float4 f0 = *reinterpret_cast<const float4*>(hr + k);
-                const float4 f1 = *reinterpret_cast<const float4*>(hr + k + 4);
-                const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+                const float g[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+                int code[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) code[e] = requant_code(f[e], s);
-            } else {
-                const uint2 v = *reinterpret_cast<const uint2*>(hq_in + row * I + k);
-                const int8_t* b = reinterpret_cast<const int8_t*>(&v);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) code[e] = b[e];
+                for (int e = 0; e < 8; ++e) code[e] = requant_code_fast(g[e], s, rs);
+                store8(row, k, code);
             }
-            __half2 o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[e] = __halves2half2(__int2half_rn(code[e]), __int2half_rn(code[e + 4]));
-            *reinterpret_cast<uint4*>(out + row * I + k) = *reinterpret_cast<const uint4*>(o);
         }
     }
 }
@@ -1154,8 +1185,14 @@ cudaError_t launch_combine_bf16(const __nv_bfloat16* y, const float* wts, const 
 cudaError_t launch_prep_h16(const float* h, uint32_t* amax, const int8_t* hq_in, int64_t P, int64_t I, __half* h16,
                             float* s_h, cudaStream_t st) {
     const int64_t blocks = std::min<int64_t>((P + 7) / 8, static_cast<int64_t>(num_sms()) * 8);
-    prep_h16_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(h, amax, hq_in, P, I, h16,
-                                                                                          s_h);
+    const unsigned grid = static_cast<unsigned>(std::max<int64_t>(blocks, 1));
+    switch (I) {  // rows of up to 1024 values stay in registers
+        case 256: prep_h16_kernel<1><<<grid, 256, 0, st>>>(h, amax, hq_in, P, I, h16, s_h); break;
+        case 512: prep_h16_kernel<2><<<grid, 256, 0, st>>>(h, amax, hq_in, P, I, h16, s_h); break;
+        case 768: prep_h16_kernel<3><<<grid, 256, 0, st>>>(h, amax, hq_in, P, I, h16, s_h); break;
+        case 1024: prep_h16_kernel<4><<<grid, 256, 0, st>>>(h, amax, hq_in, P, I, h16, s_h); break;
+        default: prep_h16_kernel<0><<<grid, 256, 0, st>>>(h, amax, hq_in, P, I, h16, s_h); break;
+    }
     return cudaGetLastError();
 }
 
