@@ -827,13 +827,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_fence_after();
                     const uint32_t tb = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + b * kTileN + c_base;
 #pragma unroll
-                    for (int i = 0; i < kColsW / 8; ++i) {  // 8 columns at a time (64 running sums + 8 loaded)
-                        if (8 * i < nloc) {
-                            uint32_t v[8];
-                            tmem_ld8(tb + 8 * i, v);
+                    for (int i = 0; i < kColsW / 16; ++i) {  // 16 columns at a time (64 running sums + 16 loaded)
+                        if (16 * i < nloc) {
+                            uint32_t v[16];
+                            tmem_ld8(tb + 16 * i, v);
+                            tmem_ld8(tb + 16 * i + 8, v + 8);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int c = 0; c < 8; ++c) acc[8 * i + c] = fmaf(__uint_as_float(v[c]), sc, acc[8 * i + c]);
+                            for (int c = 0; c < 16; ++c) acc[16 * i + c] = fmaf(__uint_as_float(v[c]), sc, acc[16 * i + c]);
                         }
                     }
                     tc_fence_before();
