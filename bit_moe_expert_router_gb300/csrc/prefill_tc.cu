@@ -55,8 +55,9 @@
 //     requests cost far more than the bytes.)
 // Persistent CTAs (one per SM) walk the (slot, token tile, weight tile)
 // items with the weight tile fastest, so the CTAs working at one time share
-// the token rows in L2.  Every item costs the same MMA time (K / 16 MMAs of
-// any width), so a static round-robin deal balances the grid.
+// the token rows in L2.  An item's A stages and accumulator drains, which
+// set its pace, do not depend on its width (a narrow tile only shortens its
+// MMAs), so a static round-robin deal balances the grid.
 //
 // Epilogue.  Gate/up: h = SiLU(x_scale G_gate) * (x_scale G_up) by pair row.
 // Down: Y = s_h * sum_q s2 P2 by pair row, stored in bf16 for the combine
@@ -72,10 +73,9 @@
 // of A, rows 32 (w % 4) .. +31; 2-9 for the down projection, two K halves
 // per row) and then the epilogue (warp w: TMEM lanes 32 (w % 4) .. +31 =
 // tile rows, a column range per group of four warps), 18 the A tiles (one
-// thread).  The MMA
-// thread does nothing but wait, issue and commit, and it has the lowest
-// warp id: with busy warps beside it on its scheduler each of its
-// instructions otherwise waited tens of cycles, and its loop has to stay
+// thread).  The MMA thread does nothing but wait, issue and commit, and it
+// has the lowest warp id: with busy warps beside it on its scheduler each of
+// its instructions otherwise waited tens of cycles, and its loop has to stay
 // inside the MMA time of a use.  Every wait is bounded (the waiting thread
 // sleeps in the barrier test); a timeout sets the status word and every role
 // leaves cleanly.
