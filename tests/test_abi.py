@@ -231,6 +231,11 @@ def test_compact_mixed_bank_layout_matches_the_generators_compaction(lib):
     assert np.array_equal(g13.numpy(), o13) and np.array_equal(g2.numpy(), o2)
     assert (n13, n2) == (w13c.size, w2c.size)
     assert np.all(g13.numpy() % 16 == 0) and np.all(g2.numpy() % 16 == 0)
+    # each offset a multiple of its slot's row length (the tcgen05 engine's tiles address a slot's rows
+    # from offset / row length)
+    rl13 = np.where(bank.slot_bits == 2, w.H // 4, w.H // 2)
+    rl2 = np.where(bank.slot_bits == 2, w.I // 4, w.I // 2)
+    assert np.all(g13.numpy() % rl13 == 0) and np.all(g2.numpy() % rl2 == 0)
     # a 2-bit slot takes half the bytes of a 4-bit one in both banks
     n4 = int((bank.slot_bits == 4).sum())
     assert n13 == (2 * n4 + (w.E + w.S - n4)) * 2 * w.I * w.H // 4
