@@ -339,6 +339,29 @@ def test_binding_checks_tensors_before_calling_the_library(lib):
                                       good["w2"], good["s2"], d, torch.zeros(4, 255), ws)
 
 
+def test_binding_checks_the_compact_bank_entry(lib):
+    """The compact mixed-bank entry refuses wrong arguments in the binding itself (no CUDA call: on a
+    machine without a GPU the first argument's checks are the ones reached), and the layout helper
+    wants the slot widths as a host tensor of E+S entries."""
+    import torch
+    from bit_moe_expert_router_gb300 import binding
+    d = binding.dims_of(4, 256, 128, 8, 1, 2, 64)
+    slots = d.E + d.n_shared
+    args = [torch.zeros(4, 256, dtype=torch.int8), torch.zeros(4), torch.zeros(4, 8),
+            torch.zeros(4096, dtype=torch.uint8), torch.zeros(slots, dtype=torch.int64), torch.zeros(slots, 256, 4),
+            torch.zeros(4096, dtype=torch.uint8), torch.zeros(slots, dtype=torch.int64), torch.zeros(slots, 256, 2),
+            torch.full((slots,), 4, dtype=torch.uint8)]
+    ws = torch.zeros(1024, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="x_q must be a CUDA tensor"):
+        binding.moe_w4a8_forward_w2w4_compact(*args, d, torch.zeros(4, 256), ws)
+    with pytest.raises(TypeError, match="x_q: dtype"):
+        binding.moe_w4a8_forward_w2w4_compact(torch.zeros(4, 256), *args[1:], d, torch.zeros(4, 256), ws)
+    with pytest.raises(ValueError, match="slot_bits must be a contiguous CPU tensor"):
+        binding.moe_w4a8_mixed_bank_layout(torch.full((slots - 1,), 4, dtype=torch.uint8), d)
+    with pytest.raises(TypeError, match="slot_bits: dtype"):
+        binding.moe_w4a8_mixed_bank_layout(torch.full((slots,), 4, dtype=torch.int32), d)
+
+
 def test_binding_checks_the_workspace_and_the_device(lib):
     """Every call needs a CUDA uint8 workspace and all device tensors on one device (checked before any call)."""
     import torch
